@@ -1,0 +1,313 @@
+"""Masked attention forward for GB300 (sm_103a): Python binding of libmattn.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libmattn.so`` behind the C ABI of ``include/mattn.h``.  PyTorch
+provides device memory and streams.  There is no fallback: if the library
+is missing or the device is not sm_103, the calls raise.
+
+    import block_sparse_attention_masked_gb300 as mattn
+    mask = mattn.prepare(spec, H=16, N=16384, device="cuda")
+    o, lse = mattn.attention(q, k, v, mask)
+
+``spec`` is a mask description with the attributes kind ("full", "chunk",
+"sliding", "causal_window", "block"), head_param (per head C / w / W / Bs),
+perm (per head None or an int array, perm[p] = token at position p),
+perm_grid (per head None or (rows, cols) for the column-major walk of a
+raster grid), block (bool [H, Nb, Nb]) and sink (float [H] or None).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmattn.so")
+
+OK = 0
+ERR_INVALID_ARG = -1
+ERR_UNSUPPORTED = -2
+ERR_CUDA = -3
+ERR_TIMEOUT = -4
+ERR_NO_DEVICE = -5
+ERR_CAPACITY = -6
+
+KIND = {"full": 0, "chunk": 1, "sliding": 2, "causal_window": 3, "block": 4}
+BF16, F32 = 0, 1
+ORDER_RASTER = -1
+ORDER_COLUMN_MAJOR = -2
+TILE = 128
+TILE_FULL, TILE_PARTIAL = 1, 2
+
+
+class MattnError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{msg} ({code})")
+        self.code = code
+
+
+class MaskDesc(ctypes.Structure):
+    _fields_ = [
+        ("kind", ctypes.c_int32),
+        ("param", ctypes.c_int32),
+        ("head_param", ctypes.POINTER(ctypes.c_int32)),
+        ("head_order", ctypes.POINTER(ctypes.c_int32)),
+        ("grid_rows", ctypes.c_int32),
+        ("grid_cols", ctypes.c_int32),
+        ("perm", ctypes.c_void_p),
+        ("n_perm", ctypes.c_int32),
+        ("block_bits", ctypes.c_void_p),
+        ("block_heads", ctypes.c_int32),
+        ("sink", ctypes.c_void_p),
+        ("softmax_scale", ctypes.c_float),
+        ("flags", ctypes.c_uint32),
+    ]
+
+
+EXPORTS = (
+    "mattn_fwd", "mattn_fwd_host", "mattn_count_pairs", "mattn_plan_tiles", "mattn_plan_tiles_device",
+    "mattn_device_status", "mattn_set_wait_timeout_ns", "mattn_status_string", "mattn_last_error",
+    "mattn_version",
+)
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmattn.so (built by ``build.py`` / ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"libmattn.so is not built ({LIB_PATH}); run "
+                           "python -m block_sparse_attention_masked_gb300.build")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, u64p = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_uint64)
+    dp = ctypes.POINTER(MaskDesc)
+    L.mattn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, dp, vp]
+    L.mattn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, dp, vp]
+    L.mattn_count_pairs.argtypes = [dp, i32, i32, i32, u64p]
+    L.mattn_plan_tiles.argtypes = [dp, i32, i32, vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]
+    L.mattn_plan_tiles_device.argtypes = [dp, i32, i32, vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t), vp]
+    L.mattn_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    L.mattn_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+    L.mattn_status_string.restype = ctypes.c_char_p
+    L.mattn_status_string.argtypes = [i32]
+    L.mattn_last_error.restype = ctypes.c_char_p
+    L.mattn_last_error.argtypes = []
+    L.mattn_version.argtypes = []
+    for name in ("mattn_fwd", "mattn_fwd_host", "mattn_count_pairs", "mattn_plan_tiles",
+                 "mattn_plan_tiles_device", "mattn_device_status", "mattn_set_wait_timeout_ns",
+                 "mattn_version"):
+        getattr(L, name).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def _check(rc: int) -> None:
+    if rc != OK:
+        L = lib()
+        raise MattnError(rc, f"{L.mattn_status_string(rc).decode()}: {L.mattn_last_error().decode()}")
+
+
+def pack_block_bits(block: np.ndarray) -> np.ndarray:
+    """bool [Hb, Nb, Nb] -> uint64 [Hb, Nb, ceil(Nb/64)], bit n of row m = B[m][n]."""
+    block = np.asarray(block, dtype=bool)
+    if block.ndim == 2:
+        block = block[None]
+    hb, nb, nb2 = block.shape
+    if nb != nb2:
+        raise ValueError("block matrix must be square")
+    wpr = (nb + 63) // 64
+    padded = np.zeros((hb, nb, wpr * 64), dtype=bool)
+    padded[:, :, :nb] = block
+    by = np.packbits(padded.reshape(hb, nb, wpr, 64), axis=-1, bitorder="little")  # [hb, nb, wpr, 8]
+    return by.view("<u8").reshape(hb, nb, wpr).copy()
+
+
+class PreparedMask:
+    """A mask descriptor plus the buffers it points at (kept alive here)."""
+
+    def __init__(self, spec, H: int, N: int, device="cuda", scale: Optional[float] = None,
+                 host_side: bool = False):
+        import torch
+
+        self.H, self.N = H, N
+        self.kind = spec.kind
+        self._keep = []
+        d = MaskDesc()
+        d.kind = KIND[spec.kind]
+        params = [int(x) for x in spec.head_param]
+        if len(params) != H:
+            raise ValueError("head_param must have H entries")
+        d.param = params[0] if spec.kind != "full" else 0
+        self._params = (ctypes.c_int32 * H)(*params)
+        d.head_param = self._params
+        orders = [ORDER_RASTER] * H
+        grid = None
+        explicit = []
+        perms = getattr(spec, "perm", None)
+        grids = getattr(spec, "perm_grid", None)
+        for h in range(H):
+            g = grids[h] if grids is not None else None
+            pm = perms[h] if perms is not None else None
+            if g is not None:
+                if grid is not None and tuple(g) != grid:
+                    raise ValueError("all column-major heads must share one grid")
+                grid = tuple(int(x) for x in g)
+                orders[h] = ORDER_COLUMN_MAJOR
+            elif pm is not None:
+                orders[h] = len(explicit)
+                explicit.append(np.asarray(pm, dtype=np.int32))
+        self._orders = (ctypes.c_int32 * H)(*orders)
+        d.head_order = self._orders
+        if grid is not None:
+            d.grid_rows, d.grid_cols = grid
+        if explicit:
+            arr = np.stack(explicit).astype(np.int32)
+            t = torch.from_numpy(arr)
+            t = t if host_side else t.to(device)
+            self._keep.append(t)
+            d.perm = t.data_ptr()
+            d.n_perm = len(explicit)
+        if spec.kind == "block":
+            words = pack_block_bits(spec.block)
+            self.block_words_host = words
+            t = torch.from_numpy(words.view(np.int64))
+            t = t if host_side else t.to(device)
+            self._keep.append(t)
+            d.block_bits = t.data_ptr()
+            d.block_heads = words.shape[0]
+        sink = getattr(spec, "sink", None)
+        if sink is not None:
+            t = torch.tensor(np.asarray(sink, dtype=np.float32))
+            t = t if host_side else t.to(device)
+            self._keep.append(t)
+            d.sink = t.data_ptr()
+        d.softmax_scale = 0.0 if scale is None else float(scale)
+        d.flags = 0
+        self.desc = d
+
+    def host_desc(self):
+        """A copy of the descriptor whose block bits point at host memory."""
+        d = MaskDesc.from_buffer_copy(self.desc)
+        if self.kind == "block":
+            d.block_bits = self.block_words_host.ctypes.data
+        d._owner = self  # the arrays the copied pointers refer to live in self
+        return d
+
+
+def prepare(spec, H: int, N: int, device="cuda", scale: Optional[float] = None) -> PreparedMask:
+    return PreparedMask(spec, H, N, device=device, scale=scale)
+
+
+def _dtype_code(t) -> int:
+    import torch
+
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"unsupported dtype {t.dtype} (bf16 or fp32)")
+
+
+def attention(q, k, v, mask: PreparedMask, out=None, lse=None, want_lse: bool = True, stream=None):
+    """O, LSE of the masked attention forward on CUDA tensors [B, H, N, d]."""
+    import torch
+
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors (use attention_host for host buffers)")
+    for t in (q, k, v):
+        if not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous [B, H, N, d]")
+    B, H, N, d = q.shape
+    if k.shape != q.shape or v.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must have the same shape and dtype")
+    if out is None:
+        out = torch.empty_like(q)
+    if want_lse and lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    rc = lib().mattn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                         lse.data_ptr() if lse is not None else None, B, H, N, d, _dtype_code(q),
+                         ctypes.byref(mask.desc), stream)
+    _check(rc)
+    return out, lse
+
+
+def attention_host(q, k, v, spec_or_mask, out=None, lse=None, stream=None):
+    """The same on host (CPU, ideally pinned) tensors: copies in, computes, copies out."""
+    import torch
+
+    B, H, N, d = q.shape
+    mask = spec_or_mask if isinstance(spec_or_mask, PreparedMask) else PreparedMask(
+        spec_or_mask, H, N, host_side=True)
+    desc = mask.host_desc()
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32)
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    rc = lib().mattn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                              B, H, N, d, _dtype_code(q), ctypes.byref(desc), stream)
+    _check(rc)
+    return out, lse
+
+
+def count_pairs(spec_or_mask, B: int, H: int, N: int) -> int:
+    mask = spec_or_mask if isinstance(spec_or_mask, PreparedMask) else PreparedMask(
+        spec_or_mask, H, N, host_side=True)
+    desc = mask.host_desc()
+    out = ctypes.c_uint64(0)
+    _check(lib().mattn_count_pairs(ctypes.byref(desc), B, H, N, ctypes.byref(out)))
+    return int(out.value)
+
+
+def plan_tiles(spec_or_mask, H: int, N: int) -> np.ndarray:
+    """int32 [n, 4] (h, qt, kt, class) from the host planner."""
+    mask = spec_or_mask if isinstance(spec_or_mask, PreparedMask) else PreparedMask(
+        spec_or_mask, H, N, host_side=True)
+    desc = mask.host_desc()
+    n = ctypes.c_size_t(0)
+    rc = lib().mattn_plan_tiles(ctypes.byref(desc), H, N, None, 0, ctypes.byref(n))
+    if rc not in (OK, ERR_CAPACITY):
+        _check(rc)
+    buf = np.zeros((max(1, n.value), 4), dtype=np.int32)
+    _check(lib().mattn_plan_tiles(ctypes.byref(desc), H, N, buf.ctypes.data, n.value, ctypes.byref(n)))
+    return buf[:n.value]
+
+
+def plan_tiles_device(mask: PreparedMask, H: int, N: int, stream=None) -> np.ndarray:
+    """int32 [n, 4] from the device tile walker the attention kernel uses."""
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    n = ctypes.c_size_t(0)
+    rc = lib().mattn_plan_tiles_device(ctypes.byref(mask.desc), H, N, None, 0, ctypes.byref(n), stream)
+    if rc not in (OK, ERR_CAPACITY):
+        _check(rc)
+    buf = np.zeros((max(1, n.value), 4), dtype=np.int32)
+    _check(lib().mattn_plan_tiles_device(ctypes.byref(mask.desc), H, N, buf.ctypes.data, n.value,
+                                         ctypes.byref(n), stream))
+    return buf[:n.value]
+
+
+def device_status(stream=None):
+    """(status, detail word); synchronises the stream and clears the device error word."""
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    word = ctypes.c_uint32(0)
+    rc = lib().mattn_device_status(stream, ctypes.byref(word))
+    return rc, int(word.value)
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    _check(lib().mattn_set_wait_timeout_ns(int(ns)))

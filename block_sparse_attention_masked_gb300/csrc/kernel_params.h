@@ -1,0 +1,69 @@
+// Launch parameters shared by the host API and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+namespace mattn {
+
+// Per-head table (device int32 [H][4]).
+enum HeadField : int { kHeadParam = 0, kHeadLoad = 1, kHeadStore = 2, kHeadPermRow = 3 };
+enum LoadMode : int { kLoadRaster = 0, kLoadColumnMajor = 1 };
+enum StoreMode : int { kStoreIdentity = 0, kStoreColumnMajor = 1, kStoreExplicit = 2 };
+
+// Device error-word bits (which wait gave up).
+enum ErrBits : uint32_t {
+  kErrProducer = 1u << 0,
+  kErrMma = 1u << 1,
+  kErrSoftmax = 1u << 2,
+  kErrEpilogue = 1u << 3,
+  kErrSelfTest = 1u << 4,
+};
+
+struct FwdParams {
+  // [0]: 64-column chunks (128-byte swizzle); [1]: the 16- or 32-column rest.
+  CUtensorMap tq[2], tk[2], tv[2];  // [B*H][N][d] views
+  CUtensorMap cq[2], ck[2], cv[2];  // column-major views [B*H][rows][cols][d]
+  void* o;                          // [B][H][N][d], bf16 or fp32
+  float* lse;                       // [B][H][N] or null
+  const int2* items;                // (b*H + h, query-tile pair)
+  const int32_t* head_info;         // [H][4], HeadField
+  const int32_t* perm;              // explicit orders [n_perm][N]
+  const uint64_t* block_bits;       // [block_heads][Nb][wpr]
+  const float* sink;                // [H] or null
+  uint32_t* err;                    // device error word
+  unsigned long long timeout_ns;
+  int n_items;
+  int B, H, N;
+  int kind;
+  int block_heads, block_wpr, block_c, block_nb;
+  int grid_rows, grid_cols;
+  float scale_log2;                 // softmax scale * log2(e)
+  int self_test_timeout;            // 1: wait on a barrier nothing arrives on (tests)
+};
+
+struct PlanDumpParams {
+  const int32_t* head_info;
+  const uint64_t* block_bits;
+  int H, N, kind, block_heads, block_wpr, block_c, block_nb;
+  int32_t* out;     // [H][nt][nt][4]
+  int32_t* counts;  // [H][nt]
+};
+
+struct GatherParams {
+  const void* src[3];
+  void* dst[3];
+  const int32_t* head_info;
+  const int32_t* perm;
+  int B, H, N, d;
+  int src_f32;
+  int grid_rows, grid_cols;
+};
+
+// Launchers (attention_fwd.cu).
+cudaError_t launch_attention(const FwdParams& p, int d, bool out_f32, cudaStream_t stream);
+size_t attention_smem_bytes(int d);
+cudaError_t launch_plan_dump(const PlanDumpParams& p, cudaStream_t stream);
+cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream);
+
+}  // namespace mattn

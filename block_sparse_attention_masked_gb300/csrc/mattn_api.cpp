@@ -1,0 +1,662 @@
+// Host side of libmattn: argument validation, the tile planner and work
+// list, per-device state, TMA descriptors and kernel launches behind the C
+// ABI declared in include/mattn.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <memory>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "kernel_params.h"
+#include "mattn.h"
+#include "plan_rules.h"
+
+namespace mattn {
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(MATTN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define MATTN_CUDA(call, what)                   \
+  do {                                           \
+    cudaError_t e_ = (call);                     \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+std::atomic<unsigned long long> g_timeout_ns{0};
+
+unsigned long long wait_timeout_ns() {
+  unsigned long long t = g_timeout_ns.load();
+  if (t) return t;
+  const char* env = getenv("MATTN_WAIT_TIMEOUT_NS");
+  unsigned long long v = env ? strtoull(env, nullptr, 10) : 0ull;
+  if (!v) v = 2000000000ull;
+  g_timeout_ns.store(v);
+  return v;
+}
+
+// ------------------------------------------------------------ mask normalisation
+struct HeadPlan {
+  int param;
+  int load;   // LoadMode
+  int store;  // StoreMode
+  int perm_row;
+};
+
+struct Normalized {
+  int kind;
+  int B, H, N, d, dtype;
+  std::vector<HeadPlan> heads;
+  bool need_copy;     // reorder / convert into a bf16 copy in position order
+  bool any_colmajor_tma;
+  int block_c, block_nb, block_wpr, block_heads;
+  float scale;
+};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int normalize(const mattn_mask_desc* desc, int B, int H, int N, int d, int dtype, bool need_data, Normalized* out) {
+  if (!desc) return fail(MATTN_ERR_INVALID_ARG, "mask descriptor is NULL");
+  if (desc->flags != 0) return fail(MATTN_ERR_INVALID_ARG, "flags must be 0");
+  if (B < 1 || H < 1 || N < 1) return fail(MATTN_ERR_INVALID_ARG, "B, H, N must be >= 1 (got %d, %d, %d)", B, H, N);
+  if (N > (1 << 30)) return fail(MATTN_ERR_UNSUPPORTED, "N = %d exceeds 2^30", N);
+  if ((int64_t)B * H > (1 << 30)) return fail(MATTN_ERR_UNSUPPORTED, "B*H too large");
+  if (need_data) {
+    if (d != 32 && d != 64 && d != 80 && d != 96 && d != 128)
+      return fail(MATTN_ERR_UNSUPPORTED, "head dim %d not supported (32, 64, 80, 96, 128)", d);
+    if (dtype != MATTN_BF16 && dtype != MATTN_F32) return fail(MATTN_ERR_UNSUPPORTED, "dtype %d not supported", dtype);
+  }
+  if (desc->kind < MATTN_FULL || desc->kind > MATTN_BLOCK_SPARSE)
+    return fail(MATTN_ERR_INVALID_ARG, "unknown mask kind %d", desc->kind);
+  if (!(desc->softmax_scale >= 0.f) || std::isinf(desc->softmax_scale))
+    return fail(MATTN_ERR_INVALID_ARG, "softmax_scale must be finite and >= 0");
+  Normalized n;
+  n.kind = desc->kind;
+  n.B = B; n.H = H; n.N = N; n.d = d; n.dtype = dtype;
+  n.scale = desc->softmax_scale > 0.f ? desc->softmax_scale : (d > 0 ? 1.0f / std::sqrt((float)d) : 1.0f);
+  n.heads.resize(H);
+  n.need_copy = need_data && dtype == MATTN_F32;
+  n.any_colmajor_tma = false;
+  n.block_c = n.block_nb = n.block_wpr = 0;
+  n.block_heads = 1;
+  for (int h = 0; h < H; ++h) {
+    int prm = desc->head_param ? desc->head_param[h] : desc->param;
+    if (n.kind != MATTN_FULL && prm < 1)
+      return fail(MATTN_ERR_INVALID_ARG, "mask parameter of head %d must be >= 1 (got %d)", h, prm);
+    if (n.kind == MATTN_FULL) prm = 0;
+    n.heads[h].param = prm;
+    int order = desc->head_order ? desc->head_order[h] : MATTN_ORDER_RASTER;
+    n.heads[h].perm_row = -1;
+    if (order == MATTN_ORDER_RASTER) {
+      n.heads[h].load = kLoadRaster;
+      n.heads[h].store = kStoreIdentity;
+    } else if (order == MATTN_ORDER_COLUMN_MAJOR) {
+      if (desc->grid_rows < 1 || desc->grid_cols < 1 || (int64_t)desc->grid_rows * desc->grid_cols != N)
+        return fail(MATTN_ERR_INVALID_ARG, "column-major order needs grid_rows * grid_cols == N (%d x %d vs %d)",
+                    desc->grid_rows, desc->grid_cols, N);
+      n.heads[h].store = kStoreColumnMajor;
+      if (desc->grid_rows % kTile == 0) {
+        n.heads[h].load = kLoadColumnMajor;
+      } else {
+        n.heads[h].load = kLoadRaster;
+        n.need_copy = true;
+      }
+    } else if (order >= 0) {
+      if (!desc->perm || order >= desc->n_perm)
+        return fail(MATTN_ERR_INVALID_ARG, "head %d selects explicit order %d but n_perm = %d", h, order, desc->n_perm);
+      n.heads[h].load = kLoadRaster;
+      n.heads[h].store = kStoreExplicit;
+      n.heads[h].perm_row = order;
+      n.need_copy = true;
+    } else {
+      return fail(MATTN_ERR_INVALID_ARG, "head %d has invalid order code %d", h, order);
+    }
+  }
+  if (n.need_copy) {
+    for (auto& hp : n.heads) hp.load = kLoadRaster;  // the copy is already in position order
+  } else {
+    for (auto& hp : n.heads) n.any_colmajor_tma |= hp.load == kLoadColumnMajor;
+  }
+  if (n.kind == MATTN_BLOCK_SPARSE) {
+    const int bs = n.heads[0].param;
+    for (int h = 1; h < H; ++h)
+      if (n.heads[h].param != bs) return fail(MATTN_ERR_UNSUPPORTED, "block size must be the same for every head");
+    if (bs % kTile != 0) return fail(MATTN_ERR_UNSUPPORTED, "block size %d is not a multiple of %d", bs, kTile);
+    if (!desc->block_bits) return fail(MATTN_ERR_INVALID_ARG, "block-sparse mask without block_bits");
+    if (desc->block_heads != 1 && desc->block_heads != H)
+      return fail(MATTN_ERR_INVALID_ARG, "block_heads must be 1 or H (got %d)", desc->block_heads);
+    n.block_c = bs / kTile;
+    n.block_nb = (N + bs - 1) / bs;
+    n.block_wpr = (n.block_nb + 63) / 64;
+    n.block_heads = desc->block_heads;
+  }
+  *out = std::move(n);
+  return MATTN_OK;
+}
+
+// ------------------------------------------------------------ planning (host)
+template <typename Fn>
+void walk_tiles_host(const Normalized& n, const uint64_t* host_bits, int h, int qt, Fn&& fn) {
+  if (n.kind == kBlockSparse) {
+    const uint64_t* bits = host_bits + (int64_t)((n.block_heads == 1) ? 0 : h) * n.block_nb * n.block_wpr;
+    for (int kt = block_next_kt(bits, n.block_wpr, n.block_c, qt, 0, qt); kt != 0x7fffffff;
+         kt = block_next_kt(bits, n.block_wpr, n.block_c, qt, kt + 1, qt))
+      fn(kt, block_tile_class(qt, kt, n.N));
+  } else {
+    KRange r = interval_krange(n.kind, n.heads[h].param, n.N, qt);
+    for (int kt = r.lo; kt <= r.hi; ++kt) fn(kt, interval_tile_class(r, kt));
+  }
+}
+
+int interval_tiles(const Normalized& n, int h, int qt) {
+  if (qt * (int64_t)kTile >= n.N) return 0;
+  KRange r = interval_krange(n.kind, n.heads[h].param, n.N, qt);
+  return r.hi >= r.lo ? r.hi - r.lo + 1 : 0;
+}
+
+// Work list: one item per (b*H + h, query-tile pair), heaviest first.
+std::vector<int2> build_items(const Normalized& n) {
+  const int nt = (n.N + kTile - 1) / kTile;
+  const int npairs = (nt + 1) / 2;
+  std::vector<int2> items;
+  items.reserve((size_t)n.B * n.H * npairs);
+  for (int bh = 0; bh < n.B * n.H; ++bh)
+    for (int pr = 0; pr < npairs; ++pr) items.push_back(make_int2(bh, pr));
+  if (n.kind == kBlockSparse) {
+    // cost grows with the query tile under causality: later pairs first
+    std::stable_sort(items.begin(), items.end(), [](const int2& a, const int2& b) { return a.y > b.y; });
+  } else {
+    std::vector<int> cost((size_t)n.H * npairs);
+    for (int h = 0; h < n.H; ++h)
+      for (int pr = 0; pr < npairs; ++pr)
+        cost[(size_t)h * npairs + pr] = interval_tiles(n, h, 2 * pr) + interval_tiles(n, h, 2 * pr + 1);
+    const int H = n.H;
+    std::stable_sort(items.begin(), items.end(), [&](const int2& a, const int2& b) {
+      return cost[(size_t)(a.x % H) * npairs + a.y] > cost[(size_t)(b.x % H) * npairs + b.y];
+    });
+  }
+  return items;
+}
+
+// ------------------------------------------------------------ per-device state
+struct Plan {
+  std::vector<int2> items_host;
+  std::vector<int32_t> head_info_host;
+  int2* items = nullptr;
+  int32_t* head_info = nullptr;
+};
+
+struct DeviceBuf {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+  int reserve(size_t need, const char* what) {
+    if (need <= bytes) return MATTN_OK;
+    if (ptr) cudaFree(ptr);
+    ptr = nullptr;
+    bytes = 0;
+    cudaError_t e = cudaMalloc(&ptr, need);
+    if (e != cudaSuccess) {
+      ptr = nullptr;
+      return cuda_fail(e, what);
+    }
+    bytes = need;
+    return MATTN_OK;
+  }
+};
+
+struct DeviceState {
+  uint32_t* err = nullptr;
+  DeviceBuf copy;      // reordered / converted q, k, v
+  DeviceBuf host_io;   // mattn_fwd_host staging
+  DeviceBuf dump;      // plan dump
+  std::map<std::string, std::unique_ptr<Plan>> plans;
+};
+
+std::mutex g_mutex;
+std::map<int, std::unique_ptr<DeviceState>> g_devices;
+
+int device_state(DeviceState** out) {
+  int dev = -1;
+  MATTN_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  auto it = g_devices.find(dev);
+  if (it == g_devices.end()) {
+    int major = 0, minor = 0;
+    MATTN_CUDA(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev), "compute capability");
+    MATTN_CUDA(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev), "compute capability");
+    if (major != 10 || minor != 3)
+      return fail(MATTN_ERR_NO_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a", dev, major, minor);
+    auto st = std::make_unique<DeviceState>();
+    MATTN_CUDA(cudaMalloc(&st->err, sizeof(uint32_t)), "cudaMalloc(error word)");
+    MATTN_CUDA(cudaMemset(st->err, 0, sizeof(uint32_t)), "cudaMemset(error word)");
+    it = g_devices.emplace(dev, std::move(st)).first;
+  }
+  *out = it->second.get();
+  return MATTN_OK;
+}
+
+std::string plan_key(const Normalized& n) {
+  std::string k;
+  char buf[96];
+  snprintf(buf, sizeof(buf), "%d|%d|%d|%d|%d|", n.kind, n.B, n.H, n.N, n.need_copy ? 1 : 0);
+  k += buf;
+  for (const auto& hp : n.heads) {
+    snprintf(buf, sizeof(buf), "%d,%d,%d,%d;", hp.param, hp.load, hp.store, hp.perm_row);
+    k += buf;
+  }
+  return k;
+}
+
+int get_plan(DeviceState* st, const Normalized& n, cudaStream_t stream, Plan** out) {
+  std::string key = plan_key(n);
+  auto it = st->plans.find(key);
+  if (it != st->plans.end()) {
+    *out = it->second.get();
+    return MATTN_OK;
+  }
+  auto pl = std::make_unique<Plan>();
+  pl->items_host = build_items(n);
+  pl->head_info_host.resize((size_t)n.H * 4);
+  for (int h = 0; h < n.H; ++h) {
+    pl->head_info_host[h * 4 + kHeadParam] = n.heads[h].param;
+    pl->head_info_host[h * 4 + kHeadLoad] = n.heads[h].load;
+    pl->head_info_host[h * 4 + kHeadStore] = n.heads[h].store;
+    pl->head_info_host[h * 4 + kHeadPermRow] = n.heads[h].perm_row;
+  }
+  MATTN_CUDA(cudaMalloc(&pl->items, std::max<size_t>(1, pl->items_host.size()) * sizeof(int2)), "cudaMalloc(items)");
+  MATTN_CUDA(cudaMalloc(&pl->head_info, pl->head_info_host.size() * sizeof(int32_t)), "cudaMalloc(head table)");
+  MATTN_CUDA(cudaMemcpyAsync(pl->items, pl->items_host.data(), pl->items_host.size() * sizeof(int2),
+                             cudaMemcpyHostToDevice, stream),
+             "upload items");
+  MATTN_CUDA(cudaMemcpyAsync(pl->head_info, pl->head_info_host.data(), pl->head_info_host.size() * sizeof(int32_t),
+                             cudaMemcpyHostToDevice, stream),
+             "upload head table");
+  MATTN_CUDA(cudaStreamSynchronize(stream), "plan upload");
+  *out = pl.get();
+  st->plans.emplace(key, std::move(pl));
+  return MATTN_OK;
+}
+
+// ------------------------------------------------------------ TMA descriptors
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int get_encoder() {
+  if (g_encode) return MATTN_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+    return fail(MATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return MATTN_OK;
+}
+
+int encode(CUtensorMap* tm, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+           const cuuint32_t* box, CUtensorMapSwizzle sw) {
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return MATTN_OK;
+}
+
+// Raster views [B*H][N][d] and, when asked, column-major views
+// [B*H][rows][cols][d] of one bf16 tensor: map [0] covers 64-column chunks
+// (128-byte swizzle), map [1] the 16- or 32-column rest.
+int make_maps(const Normalized& n, const void* base, CUtensorMap raster[2], CUtensorMap colmaj[2], int rows, int cols) {
+  const int d = n.d;
+  const int chunks = d / 64, rem = d % 64;
+  const cuuint64_t bh = (cuuint64_t)n.B * n.H;
+  const CUtensorMapSwizzle rem_sw = rem == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B;
+  memset(raster, 0, 2 * sizeof(CUtensorMap));
+  memset(colmaj, 0, 2 * sizeof(CUtensorMap));
+  const char* rem_base = static_cast<const char*>(base) + (size_t)chunks * 64 * 2;
+  {
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)n.N * d * 2};
+    if (chunks) {
+      cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n.N, bh};
+      cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1};
+      int rc = encode(&raster[0], base, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+      if (rc) return rc;
+    }
+    if (rem) {
+      cuuint64_t dims[3] = {(cuuint64_t)rem, (cuuint64_t)n.N, bh};
+      cuuint32_t box[3] = {(cuuint32_t)rem, (cuuint32_t)kTile, 1};
+      int rc = encode(&raster[1], rem_base, 3, dims, strides, box, rem_sw);
+      if (rc) return rc;
+    }
+  }
+  if (rows > 0) {
+    cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)cols * d * 2, (cuuint64_t)n.N * d * 2};
+    if (chunks) {
+      cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)cols, (cuuint64_t)rows, bh};
+      cuuint32_t box[4] = {64, 1, (cuuint32_t)kTile, 1};
+      int rc = encode(&colmaj[0], base, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+      if (rc) return rc;
+    }
+    if (rem) {
+      cuuint64_t dims[4] = {(cuuint64_t)rem, (cuuint64_t)cols, (cuuint64_t)rows, bh};
+      cuuint32_t box[4] = {(cuuint32_t)rem, 1, (cuuint32_t)kTile, 1};
+      int rc = encode(&colmaj[1], rem_base, 4, dims, strides, box, rem_sw);
+      if (rc) return rc;
+    }
+  }
+  return MATTN_OK;
+}
+
+int check_device_ptrs(const void* q, const void* k, const void* v, const void* o, const float* lse) {
+  if (!q || !k || !v || !o) return fail(MATTN_ERR_INVALID_ARG, "q, k, v and o must be non-NULL");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+    return fail(MATTN_ERR_UNSUPPORTED, "q, k, v and o must be 16-byte aligned");
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return fail(MATTN_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+  return MATTN_OK;
+}
+
+int fwd_locked(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d, int dtype,
+               const mattn_mask_desc* desc, cudaStream_t stream, int self_test) {
+  Normalized n;
+  int rc = normalize(desc, B, H, N, d, dtype, true, &n);
+  if (rc) return rc;
+  rc = check_device_ptrs(q, k, v, o, lse);
+  if (rc) return rc;
+  DeviceState* st = nullptr;
+  rc = device_state(&st);
+  if (rc) return rc;
+  rc = get_encoder();
+  if (rc) return rc;
+  Plan* plan = nullptr;
+  rc = get_plan(st, n, stream, &plan);
+  if (rc) return rc;
+
+  const size_t elems = (size_t)B * H * N * d;
+  const void* src[3] = {q, k, v};
+  const void* use[3] = {q, k, v};
+  if (n.need_copy) {
+    rc = st->copy.reserve(3 * elems * 2, "cudaMalloc(reorder workspace)");
+    if (rc) return rc;
+    GatherParams gp;
+    memset(&gp, 0, sizeof(gp));
+    for (int t = 0; t < 3; ++t) {
+      gp.src[t] = src[t];
+      gp.dst[t] = static_cast<char*>(st->copy.ptr) + (size_t)t * elems * 2;
+      use[t] = gp.dst[t];
+    }
+    gp.head_info = plan->head_info;
+    gp.perm = desc->perm;
+    gp.B = B; gp.H = H; gp.N = N; gp.d = d;
+    gp.src_f32 = dtype == MATTN_F32;
+    gp.grid_rows = desc->grid_rows;
+    gp.grid_cols = desc->grid_cols;
+    MATTN_CUDA(launch_gather(gp, stream), "gather launch");
+  }
+
+  FwdParams p;
+  memset(&p, 0, sizeof(p));
+  const int rows = n.any_colmajor_tma ? desc->grid_rows : 0;
+  const int cols = n.any_colmajor_tma ? desc->grid_cols : 0;
+  if ((rc = make_maps(n, use[0], p.tq, p.cq, rows, cols))) return rc;
+  if ((rc = make_maps(n, use[1], p.tk, p.ck, rows, cols))) return rc;
+  if ((rc = make_maps(n, use[2], p.tv, p.cv, rows, cols))) return rc;
+  p.o = o;
+  p.lse = lse;
+  p.items = plan->items;
+  p.n_items = (int)plan->items_host.size();
+  p.head_info = plan->head_info;
+  p.perm = desc->perm;
+  p.block_bits = n.kind == kBlockSparse ? desc->block_bits : nullptr;
+  p.sink = desc->sink;
+  p.err = st->err;
+  p.timeout_ns = wait_timeout_ns();
+  p.B = B; p.H = H; p.N = N;
+  p.kind = n.kind;
+  p.block_heads = n.block_heads;
+  p.block_wpr = n.block_wpr;
+  p.block_c = n.block_c;
+  p.block_nb = n.block_nb;
+  p.grid_rows = desc->grid_rows;
+  p.grid_cols = desc->grid_cols;
+  p.scale_log2 = n.scale * 1.4426950408889634f;
+  p.self_test_timeout = self_test;
+  MATTN_CUDA(launch_attention(p, d, dtype == MATTN_F32, stream), "attention launch");
+  return MATTN_OK;
+}
+
+}  // namespace
+}  // namespace mattn
+
+using namespace mattn;
+
+extern "C" {
+
+int mattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d, int dtype,
+              const mattn_mask_desc* desc, void* stream) {
+  std::lock_guard<std::mutex> lk(g_mutex);
+  return fwd_locked(q, k, v, o, lse, B, H, N, d, dtype, desc, static_cast<cudaStream_t>(stream), 0);
+}
+
+// Test hook (not in the public header): the same launch, with the MMA warp
+// first waiting on a barrier that nothing ever arrives on, so that the
+// bounded-wait / error-word path can be exercised without a hang.
+int mattn_internal_fwd_wait_selftest(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                                     int N, int d, int dtype, const mattn_mask_desc* desc, void* stream) {
+  std::lock_guard<std::mutex> lk(g_mutex);
+  return fwd_locked(q, k, v, o, lse, B, H, N, d, dtype, desc, static_cast<cudaStream_t>(stream), 1);
+}
+
+int mattn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                   int dtype, const mattn_mask_desc* desc, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  std::lock_guard<std::mutex> lk(g_mutex);
+  Normalized n;
+  int rc = normalize(desc, B, H, N, d, dtype, true, &n);
+  if (rc) return rc;
+  if (!q || !k || !v || !o) return fail(MATTN_ERR_INVALID_ARG, "q, k, v and o must be non-NULL");
+  DeviceState* st = nullptr;
+  if ((rc = device_state(&st))) return rc;
+  const size_t esz = dtype == MATTN_F32 ? 4 : 2;
+  const size_t tensor = (size_t)B * H * N * d * esz;
+  const size_t lse_bytes = (size_t)B * H * N * 4;
+  const size_t sink_bytes = desc->sink ? (size_t)H * 4 : 0;
+  const size_t bits_bytes =
+      n.kind == kBlockSparse ? (size_t)n.block_heads * n.block_nb * n.block_wpr * sizeof(uint64_t) : 0;
+  const size_t perm_bytes = (desc->perm && desc->n_perm > 0) ? (size_t)desc->n_perm * N * sizeof(int32_t) : 0;
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t total = 4 * up(tensor) + up(lse_bytes) + up(sink_bytes) + up(bits_bytes) + up(perm_bytes);
+  if ((rc = st->host_io.reserve(total, "cudaMalloc(host staging)"))) return rc;
+  char* base = static_cast<char*>(st->host_io.ptr);
+  char* dq = base;
+  char* dk = dq + up(tensor);
+  char* dv = dk + up(tensor);
+  char* dout = dv + up(tensor);
+  float* dlse = reinterpret_cast<float*>(dout + up(tensor));
+  char* dsink = reinterpret_cast<char*>(dlse) + up(lse_bytes);
+  char* dbits = dsink + up(sink_bytes);
+  char* dperm = dbits + up(bits_bytes);
+  MATTN_CUDA(cudaMemcpyAsync(dq, q, tensor, cudaMemcpyHostToDevice, stream), "copy q");
+  MATTN_CUDA(cudaMemcpyAsync(dk, k, tensor, cudaMemcpyHostToDevice, stream), "copy k");
+  MATTN_CUDA(cudaMemcpyAsync(dv, v, tensor, cudaMemcpyHostToDevice, stream), "copy v");
+  mattn_mask_desc dd = *desc;
+  if (desc->sink) {
+    MATTN_CUDA(cudaMemcpyAsync(dsink, desc->sink, sink_bytes, cudaMemcpyHostToDevice, stream), "copy sink");
+    dd.sink = reinterpret_cast<const float*>(dsink);
+  }
+  if (bits_bytes) {
+    MATTN_CUDA(cudaMemcpyAsync(dbits, desc->block_bits, bits_bytes, cudaMemcpyHostToDevice, stream), "copy bits");
+    dd.block_bits = reinterpret_cast<const uint64_t*>(dbits);
+  }
+  if (perm_bytes) {
+    MATTN_CUDA(cudaMemcpyAsync(dperm, desc->perm, perm_bytes, cudaMemcpyHostToDevice, stream), "copy perm");
+    dd.perm = reinterpret_cast<const int32_t*>(dperm);
+  }
+  rc = fwd_locked(dq, dk, dv, dout, lse ? dlse : nullptr, B, H, N, d, dtype, &dd, stream, 0);
+  if (rc) return rc;
+  MATTN_CUDA(cudaMemcpyAsync(o, dout, tensor, cudaMemcpyDeviceToHost, stream), "copy o");
+  if (lse) MATTN_CUDA(cudaMemcpyAsync(lse, dlse, lse_bytes, cudaMemcpyDeviceToHost, stream), "copy lse");
+  MATTN_CUDA(cudaStreamSynchronize(stream), "stream sync");
+  return MATTN_OK;
+}
+
+int mattn_count_pairs(const mattn_mask_desc* desc, int B, int H, int N, uint64_t* pairs_out) {
+  if (!pairs_out) return fail(MATTN_ERR_INVALID_ARG, "pairs_out is NULL");
+  Normalized n;
+  int rc = normalize(desc, B, H, N, 0, MATTN_BF16, false, &n);
+  if (rc) return rc;
+  uint64_t total = 0;
+  for (int h = 0; h < H; ++h) {
+    if (n.kind == kBlockSparse) {
+      const uint64_t* bits =
+          desc->block_bits + (int64_t)((n.block_heads == 1) ? 0 : h) * n.block_nb * n.block_wpr;
+      const int64_t bs = n.heads[h].param;
+      for (int m = 0; m < n.block_nb; ++m) {
+        const int64_t r0 = m * bs, r1 = std::min<int64_t>(N, r0 + bs);  // rows [r0, r1)
+        for (int nb = 0; nb <= m; ++nb) {
+          if (!block_bit(bits, n.block_wpr, m, nb)) continue;
+          if (nb < m) {
+            total += (uint64_t)(r1 - r0) * (uint64_t)bs;
+          } else {
+            // diagonal block: row p sees keys r0 .. p
+            const int64_t len = r1 - r0;
+            total += (uint64_t)(len * (len + 1) / 2);
+          }
+        }
+      }
+    } else {
+      for (int64_t p = 0; p < N; ++p) {
+        int64_t lo, hi;
+        row_interval(n.kind, n.heads[h].param, N, p, &lo, &hi);
+        lo = std::max<int64_t>(0, lo);
+        hi = std::min<int64_t>(N - 1, hi);
+        if (hi >= lo) total += (uint64_t)(hi - lo + 1);
+      }
+    }
+  }
+  *pairs_out = total * (uint64_t)B;
+  return MATTN_OK;
+}
+
+int mattn_plan_tiles(const mattn_mask_desc* desc, int H, int N, int32_t* out, size_t cap, size_t* n_out) {
+  if (!n_out) return fail(MATTN_ERR_INVALID_ARG, "n_out is NULL");
+  if (cap && !out) return fail(MATTN_ERR_INVALID_ARG, "out is NULL with cap > 0");
+  Normalized n;
+  int rc = normalize(desc, 1, H, N, 0, MATTN_BF16, false, &n);
+  if (rc) return rc;
+  const int nt = (N + kTile - 1) / kTile;
+  size_t cnt = 0;
+  for (int h = 0; h < H; ++h)
+    for (int qt = 0; qt < nt; ++qt)
+      walk_tiles_host(n, desc->block_bits, h, qt, [&](int kt, int cls) {
+        if (cnt < cap) {
+          out[4 * cnt + 0] = h;
+          out[4 * cnt + 1] = qt;
+          out[4 * cnt + 2] = kt;
+          out[4 * cnt + 3] = cls;
+        }
+        ++cnt;
+      });
+  *n_out = cnt;
+  if (cnt > cap) return fail(MATTN_ERR_CAPACITY, "plan has %zu tiles, buffer holds %zu", cnt, cap);
+  return MATTN_OK;
+}
+
+int mattn_plan_tiles_device(const mattn_mask_desc* desc, int H, int N, int32_t* out, size_t cap, size_t* n_out,
+                            void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (!n_out) return fail(MATTN_ERR_INVALID_ARG, "n_out is NULL");
+  if (cap && !out) return fail(MATTN_ERR_INVALID_ARG, "out is NULL with cap > 0");
+  std::lock_guard<std::mutex> lk(g_mutex);
+  Normalized n;
+  int rc = normalize(desc, 1, H, N, 0, MATTN_BF16, false, &n);
+  if (rc) return rc;
+  DeviceState* st = nullptr;
+  if ((rc = device_state(&st))) return rc;
+  Plan* plan = nullptr;
+  if ((rc = get_plan(st, n, stream, &plan))) return rc;
+  const int nt = (N + kTile - 1) / kTile;
+  const size_t slots = (size_t)H * nt * nt * 4;
+  if (slots > ((size_t)1 << 31)) return fail(MATTN_ERR_UNSUPPORTED, "plan dump too large (H * nt^2 = %zu)", slots / 4);
+  if ((rc = st->dump.reserve((slots + (size_t)H * nt) * sizeof(int32_t), "cudaMalloc(plan dump)"))) return rc;
+  PlanDumpParams pp;
+  pp.head_info = plan->head_info;
+  pp.block_bits = n.kind == kBlockSparse ? desc->block_bits : nullptr;
+  pp.H = H; pp.N = N; pp.kind = n.kind;
+  pp.block_heads = n.block_heads; pp.block_wpr = n.block_wpr; pp.block_c = n.block_c; pp.block_nb = n.block_nb;
+  pp.out = static_cast<int32_t*>(st->dump.ptr);
+  pp.counts = pp.out + slots;
+  MATTN_CUDA(launch_plan_dump(pp, stream), "plan dump launch");
+  std::vector<int32_t> host(slots + (size_t)H * nt);
+  MATTN_CUDA(cudaMemcpyAsync(host.data(), st->dump.ptr, host.size() * sizeof(int32_t), cudaMemcpyDeviceToHost, stream),
+             "plan dump copy");
+  MATTN_CUDA(cudaStreamSynchronize(stream), "plan dump sync");
+  size_t cnt = 0;
+  for (int h = 0; h < H; ++h)
+    for (int qt = 0; qt < nt; ++qt) {
+      const int c = host[slots + (size_t)h * nt + qt];
+      const int32_t* src = host.data() + ((size_t)h * nt + qt) * nt * 4;
+      for (int i = 0; i < c; ++i, ++cnt)
+        if (cnt < cap) memcpy(out + 4 * cnt, src + 4 * i, 4 * sizeof(int32_t));
+    }
+  *n_out = cnt;
+  if (cnt > cap) return fail(MATTN_ERR_CAPACITY, "plan has %zu tiles, buffer holds %zu", cnt, cap);
+  return MATTN_OK;
+}
+
+int mattn_device_status(void* stream, uint32_t* detail_out) {
+  std::lock_guard<std::mutex> lk(g_mutex);
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc) return rc;
+  MATTN_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "stream sync");
+  uint32_t word = 0;
+  MATTN_CUDA(cudaMemcpy(&word, st->err, sizeof(word), cudaMemcpyDeviceToHost), "read error word");
+  MATTN_CUDA(cudaMemset(st->err, 0, sizeof(word)), "clear error word");
+  if (detail_out) *detail_out = word;
+  if (word) return fail(MATTN_ERR_TIMEOUT, "a device wait gave up (error word 0x%x)", word);
+  return MATTN_OK;
+}
+
+int mattn_set_wait_timeout_ns(uint64_t ns) {
+  g_timeout_ns.store(ns);
+  if (!ns) wait_timeout_ns();
+  return MATTN_OK;
+}
+
+const char* mattn_status_string(int status) {
+  switch (status) {
+    case MATTN_OK: return "MATTN_OK";
+    case MATTN_ERR_INVALID_ARG: return "MATTN_ERR_INVALID_ARG";
+    case MATTN_ERR_UNSUPPORTED: return "MATTN_ERR_UNSUPPORTED";
+    case MATTN_ERR_CUDA: return "MATTN_ERR_CUDA";
+    case MATTN_ERR_TIMEOUT: return "MATTN_ERR_TIMEOUT";
+    case MATTN_ERR_NO_DEVICE: return "MATTN_ERR_NO_DEVICE";
+    case MATTN_ERR_CAPACITY: return "MATTN_ERR_CAPACITY";
+    default: return "MATTN_ERR_UNKNOWN";
+  }
+}
+
+const char* mattn_last_error(void) { return g_last_error; }
+
+int mattn_version(void) { return 100; }
+
+}  // extern "C"

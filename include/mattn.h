@@ -1,0 +1,193 @@
+/*
+ * mattn.h -- C ABI of libmattn, the masked attention forward for GB300 (sm_103a).
+ *
+ * The operation (one call computes it for every batch entry b and head h):
+ *
+ *   O[b,h,i,:] = sum_{j in N_h(i)} a_ij V[b,h,j,:]
+ *   a_ij       = exp(s_ij) / ( sum_{j' in N_h(i)} exp(s_ij') + exp(sink_h) )
+ *   s_ij       = scale * <Q[b,h,i,:], K[b,h,j,:]>,   scale = 1/sqrt(d) by default
+ *   LSE[b,h,i] = log( sum_{j in N_h(i)} exp(s_ij) + exp(sink_h) )   (natural log)
+ *
+ * Sources: the score and its 1/sqrt(d) scaling -- "Vision transformers and
+ * hybrid architectures", section 2 (self-attention from first principles);
+ * the per-head sink logit that enters only the denominator -- "Semantic Head
+ * Specialization Guides Hybrid ViT Attention for Multimodal LLMs" (SHS
+ * slides), the sink slide, Eq. 1; the neighbour set N(i) the softmax runs
+ * over -- SHS slides, local-attention recap slide; the block-selection
+ * matrix expanded to tokens, M_B[i,j] = B[floor(i/Bs), floor(j/Bs)] and
+ * j <= i -- "RRAttention" section 2.1, Eq. 1-2; head-wise causal windows --
+ * "Asymmetric Attention Heads", section "What was done" and Table 2.
+ *
+ * N_h(i) is defined on SEQUENCE POSITIONS.  Each head may read its tokens in
+ * a different order (the 1D serialisation of a 2D patch grid, SHS slides
+ * "Factor 2"): position p of head h holds caller token t = order_h(p).  The
+ * mask is evaluated on positions; O and LSE are returned in caller token
+ * order, so one call is a drop-in attention layer.
+ *
+ * Memory layout: q, k, v and o are dense row-major [B][H][N][d] tensors of
+ * one element type (bf16, or fp32 for q/k/v/o with MATTN_F32), base address
+ * 16-byte aligned; lse is fp32 [B][H][N].  Supported head dims: 32, 64, 80,
+ * 96, 128.  fp32 inputs are rounded to bf16 on the device before the
+ * tensor-core products (accumulation is fp32 throughout); O is written in
+ * the input element type.
+ *
+ * Ownership: the caller owns every buffer and the stream.  The library keeps
+ * per-device internal state (work lists, converted or reordered copies of
+ * inputs, an error word) that it allocates on first use and reuses; it never
+ * synchronises the caller's stream on the normal path (mattn_fwd returns
+ * after the launches are queued).
+ *
+ * Errors: every entry point returns MATTN_OK (0) or a negative mattn_status.
+ * Arguments are validated on the host before anything is launched; on error
+ * nothing is launched and mattn_last_error() describes the cause.  A device
+ * wait that exceeds its time limit (a broken pipeline; it should never
+ * happen) makes the kernel record MATTN_ERR_TIMEOUT in the device error word
+ * and return early instead of hanging; mattn_device_status() reports it.
+ * No entry point aborts or throws.
+ */
+#ifndef MATTN_H_
+#define MATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MATTN_OK = 0,
+  MATTN_ERR_INVALID_ARG = -1,  /* null pointer, bad size, bad mask parameter */
+  MATTN_ERR_UNSUPPORTED = -2,  /* valid request outside what is implemented  */
+  MATTN_ERR_CUDA = -3,         /* a CUDA runtime / driver call failed         */
+  MATTN_ERR_TIMEOUT = -4,      /* a device wait ran past its limit            */
+  MATTN_ERR_NO_DEVICE = -5,    /* no sm_103 device is current                 */
+  MATTN_ERR_CAPACITY = -6      /* more than a fixed-size buffer can hold      */
+} mattn_status;
+
+/* Mask kinds; all heads of one call share the kind (per-head parameters). */
+typedef enum {
+  MATTN_FULL = 0,          /* every key                                            */
+  MATTN_CHUNK = 1,         /* same chunk: floor(p/C) == floor(q/C)                  */
+  MATTN_SLIDING = 2,       /* bidirectional band: |p - q| <= w (w keys per side)    */
+  MATTN_CAUSAL_WINDOW = 3, /* causal window of W keys: 0 <= p - q < W               */
+  MATTN_BLOCK_SPARSE = 4   /* B[floor(p/Bs)][floor(q/Bs)] and q <= p                */
+} mattn_kind;
+
+typedef enum { MATTN_BF16 = 0, MATTN_F32 = 1 } mattn_dtype;
+
+/* Per-head token order codes for mattn_mask_desc.head_order. */
+#define MATTN_ORDER_RASTER (-1)       /* identity: position p holds token p             */
+#define MATTN_ORDER_COLUMN_MAJOR (-2) /* grid_rows x grid_cols raster grid walked       */
+                                      /* column by column: position p = c*rows + r      */
+                                      /* holds token r*cols + c                         */
+/* A value k >= 0 selects explicit order k: perm[k*N + p] = token at position p. */
+
+#define MATTN_TILE 128 /* query / key tile edge of the tile plan */
+
+typedef struct {
+  int32_t kind;              /* mattn_kind                                                */
+  int32_t param;             /* C, w, W or Bs for every head (ignored for MATTN_FULL);     */
+                             /* must be >= 1; MATTN_BLOCK_SPARSE needs Bs % 128 == 0      */
+  const int32_t* head_param; /* optional HOST [H]: per-head override of param             */
+  const int32_t* head_order; /* optional HOST [H]: MATTN_ORDER_* or explicit order index  */
+                             /* (NULL = every head raster)                                */
+  int32_t grid_rows;         /* grid of MATTN_ORDER_COLUMN_MAJOR: rows * cols == N         */
+  int32_t grid_cols;
+  const int32_t* perm;       /* explicit orders, DEVICE int32 [n_perm][N]; each row must   */
+  int32_t n_perm;            /* be a permutation of 0..N-1 (not checked on the device)     */
+  const uint64_t* block_bits;/* MATTN_BLOCK_SPARSE: DEVICE (mattn_fwd) or HOST (planning    */
+                             /* and counting calls) bitmaps [block_heads][Nb][words],      */
+                             /* Nb = ceil(N/Bs), words = ceil(Nb/64); bit n of row m is    */
+                             /* word[n/64] >> (n%64) & 1 = B[m][n]; bits above the         */
+                             /* diagonal are ignored (causality, RRAttention Eq. 5)        */
+  int32_t block_heads;       /* 1 (one matrix for all heads) or H                          */
+  const float* sink;         /* optional DEVICE fp32 [H] sink logits (NULL = no sink);     */
+                             /* HOST for mattn_fwd_host                                    */
+  float softmax_scale;       /* 0 => 1/sqrt(d)                                             */
+  uint32_t flags;            /* reserved, must be 0                                        */
+} mattn_mask_desc;
+
+/*
+ * mattn_fwd -- masked attention forward on the current CUDA device.
+ *   q, k, v  DEVICE [B][H][N][d] inputs (dtype: MATTN_BF16 or MATTN_F32).
+ *   o        DEVICE [B][H][N][d] output, same dtype as the inputs.
+ *   lse      DEVICE fp32 [B][H][N] log-sum-exp output, or NULL.
+ *   stream   a cudaStream_t (NULL = legacy default stream).
+ * Rows with no visible key and no sink get O = 0 and LSE = -inf.  Work is
+ * done only on the 128 x 128 (query, key) tiles that hold at least one
+ * visible pair (mattn_plan_tiles lists them); masking is applied only on
+ * the PARTIAL ones.  Asynchronous: returns once the work is queued.
+ */
+int mattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+              int B, int H, int N, int d, int dtype,
+              const mattn_mask_desc* desc, void* stream);
+
+/*
+ * mattn_fwd_host -- the same operation on HOST buffers: copies q, k, v (and
+ * the sink and block bitmaps, which are then HOST pointers too) to device
+ * memory owned by the library, runs mattn_fwd on `stream`, copies o and lse
+ * back and synchronises the stream.  Pinned host memory gives full copy
+ * bandwidth; pageable memory works.  lse may be NULL.
+ */
+int mattn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
+                   int B, int H, int N, int d, int dtype,
+                   const mattn_mask_desc* desc, void* stream);
+
+/*
+ * mattn_count_pairs -- exact number of visible (query, key) pairs summed over
+ * B and H (the unit of the effective-FLOP count, 4*d FLOPs per pair).  Host
+ * only; block_bits are read as HOST memory.
+ */
+int mattn_count_pairs(const mattn_mask_desc* desc, int B, int H, int N, uint64_t* pairs_out);
+
+/*
+ * mattn_plan_tiles -- the tile plan in position space: for every head h the
+ * (query tile, key tile) pairs with at least one visible pair, as int32
+ * quadruples (h, qt, kt, cls) sorted by (h, qt, kt); cls = 1 FULL (all
+ * 128 x 128 pairs exist and are visible, no masking), 2 PARTIAL (masked
+ * elementwise).  Host only, block_bits are HOST memory.  Writes at most
+ * `cap` quadruples to `out` (HOST int32 [cap*4], may be NULL when cap == 0)
+ * and the total count to *n_out; returns MATTN_ERR_CAPACITY when cap is too
+ * small (after setting *n_out).
+ */
+int mattn_plan_tiles(const mattn_mask_desc* desc, int H, int N, int32_t* out, size_t cap,
+                     size_t* n_out);
+
+/*
+ * mattn_plan_tiles_device -- the same quadruples, produced by the DEVICE tile
+ * walker that mattn_fwd runs (block_bits DEVICE memory), copied back to the
+ * HOST buffer `out`.  Synchronises `stream`.
+ */
+int mattn_plan_tiles_device(const mattn_mask_desc* desc, int H, int N, int32_t* out, size_t cap,
+                            size_t* n_out, void* stream);
+
+/*
+ * mattn_device_status -- synchronises `stream`, then reads and clears the
+ * current device's error word: MATTN_OK, or MATTN_ERR_TIMEOUT when a kernel
+ * gave up on a wait since the last call.  *detail_out (may be NULL) receives
+ * the raw word (which wait gave up).
+ */
+int mattn_device_status(void* stream, uint32_t* detail_out);
+
+/*
+ * mattn_set_wait_timeout_ns -- limit for every device-side wait (default
+ * 2e9 ns, i.e. 2 s; also read from the environment variable
+ * MATTN_WAIT_TIMEOUT_NS at first use).  0 restores the default.
+ */
+int mattn_set_wait_timeout_ns(uint64_t ns);
+
+/* Human-readable name of a status code (static string). */
+const char* mattn_status_string(int status);
+
+/* Message of the last error raised on the calling thread (static per thread). */
+const char* mattn_last_error(void);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int mattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MATTN_H_ */

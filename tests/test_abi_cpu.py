@@ -1,0 +1,173 @@
+"""CPU checks of the C ABI: the library loads, exports every declared symbol,
+validates arguments, and its host planner / pair counter agree bit-exactly
+with the oracle's dense enumeration.  No compute call touches a GPU here."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from conftest import ROOT
+from oracle import dense
+from workloads import MaskSpec, WORKLOADS, bernoulli_causal_blocks, column_major_order, make_mask
+
+mattn = pytest.importorskip("block_sparse_attention_masked_gb300")
+
+
+@pytest.fixture(scope="session")
+def L():
+    if not os.path.exists(mattn.LIB_PATH):
+        from block_sparse_attention_masked_gb300 import build
+
+        build.build()
+    return mattn.lib()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "mattn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mattn_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = _declared_functions()
+    assert "mattn_fwd" in names and "mattn_count_pairs" in names
+    for name in names:
+        assert hasattr(L, name), name
+    assert set(mattn.EXPORTS) == set(names)
+
+
+def test_status_strings_and_version(L):
+    assert L.mattn_status_string(0) == b"MATTN_OK"
+    assert L.mattn_status_string(-4) == b"MATTN_ERR_TIMEOUT"
+    assert L.mattn_version() >= 100
+
+
+def test_struct_layout_matches_header():
+    # x86-64 / aarch64 LP64: 4+4 + 8 + 8 + 4+4 + 8 + 4(+4) + 8 + 4(+4) + 8 + 4 + 4
+    assert ctypes.sizeof(mattn.MaskDesc) == 80
+    assert mattn.MaskDesc.block_bits.offset == 48
+    assert mattn.MaskDesc.sink.offset == 64
+
+
+def _desc(kind, param, **kw):
+    d = mattn.MaskDesc()
+    d.kind = kind
+    d.param = param
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d
+
+
+def test_invalid_arguments_rejected_on_host(L):
+    out = ctypes.c_uint64(0)
+    assert L.mattn_count_pairs(None, 1, 1, 16, ctypes.byref(out)) == mattn.ERR_INVALID_ARG
+    assert L.mattn_count_pairs(ctypes.byref(_desc(9, 1)), 1, 1, 16, ctypes.byref(out)) == mattn.ERR_INVALID_ARG
+    assert L.mattn_count_pairs(ctypes.byref(_desc(2, 0)), 1, 1, 16, ctypes.byref(out)) == mattn.ERR_INVALID_ARG
+    assert L.mattn_count_pairs(ctypes.byref(_desc(2, 3)), 1, 0, 16, ctypes.byref(out)) == mattn.ERR_INVALID_ARG
+    assert L.mattn_count_pairs(ctypes.byref(_desc(4, 64)), 1, 1, 256, ctypes.byref(out)) == mattn.ERR_UNSUPPORTED
+    assert L.mattn_count_pairs(ctypes.byref(_desc(4, 128)), 1, 1, 256, ctypes.byref(out)) == mattn.ERR_INVALID_ARG
+    bad_scale = _desc(0, 0, softmax_scale=-1.0)
+    assert L.mattn_count_pairs(ctypes.byref(bad_scale), 1, 1, 16, ctypes.byref(out)) == mattn.ERR_INVALID_ARG
+    flags = _desc(0, 0, flags=1)
+    assert L.mattn_count_pairs(ctypes.byref(flags), 1, 1, 16, ctypes.byref(out)) == mattn.ERR_INVALID_ARG
+    order = (ctypes.c_int32 * 1)(mattn.ORDER_COLUMN_MAJOR)
+    cm = _desc(2, 3, head_order=order, grid_rows=3, grid_cols=5)
+    assert L.mattn_count_pairs(ctypes.byref(cm), 1, 1, 16, ctypes.byref(out)) == mattn.ERR_INVALID_ARG
+    assert b"grid_rows" in L.mattn_last_error()
+    # mattn_fwd validates before touching a device
+    d = _desc(2, 3)
+    x = ctypes.c_void_p(16)
+    assert L.mattn_fwd(x, x, x, x, None, 1, 1, 16, 72, 0, ctypes.byref(d), None) == mattn.ERR_UNSUPPORTED
+    assert L.mattn_fwd(None, x, x, x, None, 1, 1, 16, 64, 0, ctypes.byref(d), None) == mattn.ERR_INVALID_ARG
+    assert L.mattn_fwd(ctypes.c_void_p(8), x, x, x, None, 1, 1, 16, 64, 0, ctypes.byref(d), None) == \
+        mattn.ERR_UNSUPPORTED
+    assert L.mattn_fwd(x, x, x, x, None, 1, 1, 16, 64, 7, ctypes.byref(d), None) == mattn.ERR_UNSUPPORTED
+
+
+def test_capacity_error_reports_count(L):
+    spec = MaskSpec("full", [0])
+    m = mattn.PreparedMask(spec, 1, 512, host_side=True)
+    d = m.host_desc()
+    n = ctypes.c_size_t(0)
+    buf = np.zeros((3, 4), dtype=np.int32)
+    rc = L.mattn_plan_tiles(ctypes.byref(d), 1, 512, buf.ctypes.data, 3, ctypes.byref(n))
+    assert rc == mattn.ERR_CAPACITY and n.value == 16
+
+
+def test_pack_block_bits_roundtrip():
+    blk = bernoulli_causal_blocks(3, 70, 5)
+    words = mattn.pack_block_bits(blk)
+    assert words.shape == (3, 70, 2) and words.dtype == np.uint64
+    for h in range(3):
+        for m in range(70):
+            for nb in range(70):
+                bit = (int(words[h, m, nb // 64]) >> (nb % 64)) & 1
+                assert bit == int(blk[h, m, nb])
+
+
+def _spec_cases(n):
+    rng = np.random.default_rng(7)
+    yield "full", MaskSpec("full", [0, 0])
+    yield "chunk", MaskSpec("chunk", [64, 200])
+    yield "sliding", MaskSpec("sliding", [32, 300])
+    yield "causal", MaskSpec("causal_window", [128, 77])
+    for bs in (128, 256):
+        nb = -(-n // bs)
+        yield f"block{bs}", MaskSpec("block", [bs, bs], block=bernoulli_causal_blocks(2, nb, bs))
+    # upper-triangle bits present in the input must be ignored
+    nb = -(-n // 128)
+    blk = rng.random((2, nb, nb)) < 0.5
+    yield "block_upper", MaskSpec("block", [128, 128], block=blk)
+
+
+@pytest.mark.parametrize("n", [1000, 1024, 129])
+def test_host_plan_matches_oracle_tiles(L, n):
+    for name, spec in _spec_cases(n):
+        tiles = mattn.plan_tiles(spec, 2, n)
+        for h in range(2):
+            got = [tuple(int(x) for x in t[1:]) for t in tiles if t[0] == h]
+            assert got == dense.tile_list(spec, h, n, 128), (name, h)
+
+
+def test_host_plan_matches_oracle_at_workload_sizes(L):
+    for wl_name, mask in (("vit4096", "chunk256"), ("vit4096", "sliding128"), ("vit16384", "sliding256_rowcol"),
+                          ("vit16384", "chunk512"), ("causal4096", "causal_window_sink")):
+        wl = WORKLOADS[wl_name]
+        spec = make_mask(wl, mask)
+        tiles = mattn.plan_tiles(spec, wl.H, wl.N)
+        for h in (0, wl.H - 1):
+            got = [tuple(int(x) for x in t[1:]) for t in tiles if t[0] == h]
+            assert got == dense.tile_list(spec, h, wl.N, 128), (wl_name, mask, h)
+
+
+@pytest.mark.parametrize("n", [257, 1000, 4096])
+def test_pair_count_matches_oracle(L, n):
+    for name, spec in _spec_cases(n):
+        assert mattn.count_pairs(spec, 3, 2, n) == 3 * dense.pair_count(spec, n, n_heads=2), name
+
+
+def test_pair_count_workloads(L):
+    """Exact unmasked pairs of the workloads (the unit of the metric)."""
+    wl = WORKLOADS["vit16384"]
+    assert mattn.count_pairs(make_mask(wl, "full"), 1, 16, 16384) == 16 * 16384 ** 2
+    assert mattn.count_pairs(make_mask(wl, "sliding256_rowcol"), 1, 16, 16384) == 16 * 8339200
+    assert mattn.count_pairs(make_mask(wl, "chunk512"), 1, 16, 16384) == 16 * 8388608
+    wl4 = WORKLOADS["causal4096"]
+    spec = make_mask(wl4, "causal_window_sink")
+    per = {512: 1966336, 1024: 3670528, 2048: 6292480, 4096: 8390656}
+    assert mattn.count_pairs(spec, 1, 16, 4096) == sum(per[w] for w in spec.head_param)
+    assert sorted(spec.head_param) == sorted([512, 1024, 2048, 4096] * 4)
+
+
+def test_column_major_grid_description_matches_explicit_order(L):
+    n = 256
+    perm = column_major_order(16, 16)
+    grid = MaskSpec("sliding", [20], perm=[perm], perm_grid=[(16, 16)])
+    explicit = MaskSpec("sliding", [20], perm=[perm])
+    a = mattn.PreparedMask(grid, 1, n, host_side=True).host_desc()
+    b = mattn.PreparedMask(explicit, 1, n, host_side=True).host_desc()
+    assert a.head_order[0] == mattn.ORDER_COLUMN_MAJOR and (a.grid_rows, a.grid_cols) == (16, 16)
+    assert b.head_order[0] == 0 and b.n_perm == 1
