@@ -1,0 +1,449 @@
+"""Benchmark of the masked attention forward on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--quick]
+
+One step = one masked attention forward over the headline workload (the
+128K-token block-sparse causal prefill: B1 H32 N131072 d128 bf16, block 128,
+diagonal + first column kept, other causal blocks Bernoulli(0.5)), i.e. the
+whole hot path: device tile walk, TMA loads, Q K^T, boundary masking, online
+softmax, P V, epilogue.  Metric: effective TFLOP/s = 4 * d * (exact unmasked
+query-key pairs) / time.  The other workloads (tiny fp32 ViT, 896^2 and
+1792^2 ViT layers, head-wise causal windows with sinks) are timed kernel by
+kernel and reported under "workloads".
+
+With --gpus N > 1 (launched by torchrun) every rank runs an independent
+replica of the step on its own GPU (the path has no exchange step); the time
+is the max over ranks and value = all ranks' units / that time ("weak").
+--impl reference times the fp64 CPU oracle (the reference arm here) on a
+bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "effective attention TFLOP/s (unmasked FLOPs) and % of GB300 BF16 peak"
+HEADLINE = ("bsparse128k", "block128")
+KERNEL_SOURCES = ["block_sparse_attention_masked_gb300/csrc/attention_fwd.cu",
+                  "block_sparse_attention_masked_gb300/csrc/ptx.cuh",
+                  "block_sparse_attention_masked_gb300/csrc/plan_rules.h"]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"bf16_tflops": d["bf16_tflops"], "bf16_tflops_sustained": d.get("bf16_tflops_sustained"),
+                "hbm_gbs": d["hbm_gbs"], "source": "measured"}
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def profile_traffic(workload: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it matches the
+    current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"attention_fwd_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith("- "):
+                k, v = line.strip()[2:].split(":", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    try:
+        return int(float(vals["traffic_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------ distributed
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, value: float, device=None) -> float:
+    if dist is None:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"mattn_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sms, maxes, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sms.append(float(parts[1]))
+                    maxes.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.remove(self.path)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes), "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+# ------------------------------------------------------------------ GPU arm
+def effective_flops(pairs: int, d: int) -> float:
+    return 4.0 * d * pairs
+
+
+def time_kernel(fn, iters: int, warmup: int, flush=None):
+    """Median CUDA-event time (ms) of fn() over iters runs, L2 flushed before each."""
+    import torch
+
+    for _ in range(warmup):
+        if flush is not None:
+            flush()
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(iters):
+        if flush is not None:
+            flush()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        fn()
+        e.record()
+        e.synchronize()
+        times.append(s.elapsed_time(e))
+    return statistics.median(times), times
+
+
+def run_gpu(args):
+    import torch
+
+    import block_sparse_attention_masked_gb300 as mattn
+    from workloads import WORKLOADS, make_mask, make_workload_inputs
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = init_dist(world, "nccl")
+    mattn.lib()
+    peaks = measured_peaks()
+    dev = f"cuda:{local}"
+
+    # ---------------- headline step
+    wl_name, mask_name = HEADLINE
+    wl = WORKLOADS[wl_name]
+    q, k, v = make_workload_inputs(wl, seed=0, device=dev)
+    spec = make_mask(wl, mask_name, seed=0)
+    mask = mattn.prepare(spec, wl.H, wl.N, device=dev)
+    pairs = mattn.count_pairs(spec, wl.B, wl.H, wl.N)
+    flops = effective_flops(pairs, wl.d)
+    o = torch.empty_like(q)
+    lse = torch.empty((wl.B, wl.H, wl.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        mattn.attention(q, k, v, mask, out=o, lse=lse)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    rc, word = mattn.device_status()
+    if rc != 0:
+        raise RuntimeError(f"device error word {word:#x} after warm-up")
+    with ClockSampler(local) as clk:
+        barrier(dist)
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        t0 = time.perf_counter()
+        for s, e in ev:
+            s.record(stream)
+            step()
+            e.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        barrier(dist)
+    step_ms = [s.elapsed_time(e) for s, e in ev]
+    total_ms = sum(step_ms)
+    total_ms = max_over_ranks(dist, total_ms, device=dev)
+    ms_per_step = total_ms / args.steps
+    rc, word = mattn.device_status()
+    if rc != 0:
+        raise RuntimeError(f"device error word {word:#x} after timed steps")
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    per_launch_ms = statistics.mean(step_ms)
+    achieved = flops / (per_launch_ms * 1e-3) / 1e12
+    traffic = profile_traffic(wl_name)
+
+    # ---------------- end to end through the host-buffer entry point
+    e2e = None
+    if not args.quick:
+        qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+        oh = torch.empty_like(qh).pin_memory()
+        lh = torch.empty((wl.B, wl.H, wl.N), dtype=torch.float32).pin_memory()
+        hmask = mattn.PreparedMask(spec, wl.H, wl.N, host_side=True)
+        for _ in range(max(1, min(args.warmup, 2))):
+            mattn.attention_host(qh, kh, vh, hmask, out=oh, lse=lh)
+        e2e_steps = max(1, min(args.steps, 5))
+        barrier(dist)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            mattn.attention_host(qh, kh, vh, hmask, out=oh, lse=lh)
+        e2e_s = max_over_ranks(dist, time.perf_counter() - t0, device=dev)
+        barrier(dist)
+        tensor_bytes = q.numel() * q.element_size()
+        bits_bytes = int(hmask.block_words_host.nbytes) if spec.kind == "block" else 0
+        e2e = {"value": round(world * flops * e2e_steps / e2e_s / 1e12, 2), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": 3 * tensor_bytes + bits_bytes,
+               "d2h_bytes_per_step": tensor_bytes + lse.numel() * 4,
+               "ms_per_step": round(1e3 * e2e_s / e2e_steps, 3), "entry_point": "mattn_fwd_host"}
+        del qh, kh, vh, oh, lh
+
+    del q, k, v, o, lse
+    torch.cuda.empty_cache()
+
+    # ---------------- every workload, kernel by kernel
+    workloads = {}
+    if not args.quick:
+        flush_buf = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+        def flush():
+            flush_buf.zero_()
+
+        for name, wlx in WORKLOADS.items():
+            qx, kx, vx = make_workload_inputs(wlx, seed=0, device=dev)
+            in_bytes = 3 * qx.numel() * qx.element_size()
+            for m in wlx.masks:
+                sp = make_mask(wlx, m, seed=0)
+                mk = mattn.prepare(sp, wlx.H, wlx.N, device=dev)
+                ox = torch.empty_like(qx)
+                lx = torch.empty((wlx.B, wlx.H, wlx.N), dtype=torch.float32, device=dev)
+                pr = mattn.count_pairs(sp, wlx.B, wlx.H, wlx.N)
+                fl = effective_flops(pr, wlx.d)
+                iters = 5 if name == "bsparse128k" else 20
+                med, _ = time_kernel(lambda: mattn.attention(qx, kx, vx, mk, out=ox, lse=lx), iters, 3,
+                                     flush=None if in_bytes > 2 * 129e6 else flush)
+                out_bytes = ox.numel() * ox.element_size() + lx.numel() * 4
+                tf = fl / (med * 1e-3) / 1e12
+                workloads[f"{name}/{m}"] = {
+                    "ms": round(med, 4), "tflops": round(tf, 1), "pct_peak": round(100 * tf / peaks["bf16_tflops"], 1),
+                    "pairs": pr, "hbm_gbs_min_traffic": round((in_bytes + out_bytes) / (med * 1e-3) / 1e9, 1),
+                    "l2": "inputs > L2" if in_bytes > 2 * 129e6 else "flushed (512 MiB write) before each run"}
+            del qx, kx, vx
+            torch.cuda.empty_cache()
+        rc, word = mattn.device_status()
+        if rc != 0:
+            raise RuntimeError(f"device error word {word:#x} after the workload sweep")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.quick:
+        cpu = cpu_baseline(seconds=args.cpu_seconds)
+
+    if rank == 0:
+        clocks = clk.summary()
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl_name, "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d, "mask": mask_name,
+                       "mask_detail": wl.description, "pairs": pairs, "l2": "inputs larger than L2 (3 GiB)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "pct_of_peak": round(100 * value / world / peaks["bf16_tflops"], 1),
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                         "traffic": traffic, "peak_source": peaks["source"] + " burst bf16 (cuBLAS)",
+                         "kernel": "attention_fwd_kernel<128,false>"},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "wall_s_timed": round(wall, 3),
+            "workloads": workloads,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ oracle (CPU) arm
+def oracle_sample(seconds_target: float = 15.0):
+    """Time the oracle on sampled rows of head 0 of the headline workload.
+
+    Inputs are drawn with the workload recipe on the CPU (same shapes and
+    distribution); returns (effective TFLOP/s, seconds, rows, description)."""
+    import torch
+
+    from oracle import dense
+    from workloads import WORKLOADS, make_mask
+
+    wl_name, mask_name = HEADLINE
+    wl = WORKLOADS[wl_name]
+    g = torch.Generator().manual_seed(0)
+    shape = (1, 1, wl.N, wl.d)
+    q, k, v = (torch.randn(shape, generator=g).to(torch.bfloat16).float().numpy() for _ in range(3))
+    spec = make_mask(wl, mask_name, seed=0, heads=1)
+    rng = np.random.default_rng(0)
+    rows_all = rng.permutation(wl.N)
+    done_rows, t_total, pairs = 0, 0.0, 0
+    chunk = 32
+    while t_total < seconds_target and done_rows + chunk <= wl.N:
+        rows = np.sort(rows_all[done_rows:done_rows + chunk])
+        t0 = time.perf_counter()
+        dense.attention(q, k, v, spec, rows=rows)
+        t_total += time.perf_counter() - t0
+        blk = np.asarray(spec.block)[0]
+        bs = spec.head_param[0]
+        for r in rows:  # allowed keys of row r (counted outside the timed region)
+            m = r // bs
+            kept = np.nonzero(blk[m, :m])[0]
+            pairs += len(kept) * bs + (r - m * bs + 1) * int(blk[m, m])
+        done_rows += chunk
+    tf = effective_flops(pairs, wl.d) / t_total / 1e12
+    desc = (f"{wl_name}/{mask_name}: {done_rows} random query rows of head 0, all {wl.N} keys scored in fp64 "
+            f"(numpy), {t_total:.1f} s")
+    return tf, t_total, done_rows, desc
+
+
+def cpu_cores() -> int:
+    try:
+        import threadpoolctl
+
+        info = threadpoolctl.threadpool_info()
+        n = max((i.get("num_threads", 0) for i in info), default=0)
+        if n:
+            return int(n)
+    except Exception:
+        pass
+    return len(os.sched_getaffinity(0))
+
+
+def cpu_baseline(seconds: float = 15.0):
+    tf, secs, rows, desc = oracle_sample(seconds)
+    return {"value": round(tf, 6), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle", "sample": desc}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    per_step = max(1.0, args.cpu_seconds / max(1, args.steps))
+    for _ in range(args.warmup):
+        oracle_sample(0.5)
+    vals, secs = [], 0.0
+    rows_total = 0
+    for _ in range(args.steps):
+        tf, s, rows, desc = oracle_sample(per_step)
+        vals.append(tf)
+        secs += s
+        rows_total += rows
+    value = statistics.mean(vals)
+    from workloads import WORKLOADS
+
+    wl = WORKLOADS[HEADLINE[0]]
+    line = {
+        "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": HEADLINE[0], "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d, "mask": HEADLINE[1]},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"{rows_total} sampled query rows of head 0 over {args.steps} steps"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--quick", action="store_true", help="headline step only (no e2e, sweep or oracle)")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -3,9 +3,10 @@
 Tolerances (spec contract for bf16 inputs with fp32 accumulation):
 max |O_gpu - O_oracle| <= 2e-2 and ||O_gpu - O_oracle||_2 / ||O_oracle||_2
 <= 5e-3 over all compared elements; |LSE_gpu - LSE_oracle| <= 1e-3 (the
-pages state no LSE tolerance; a bf16 input error of 2^-9 on a score of size
-~5 moves the LSE by ~1e-2 * softmax weight, far below this bound for the
-workloads' score ranges, and fp32 accumulation adds < 1e-5).
+pages state no LSE tolerance; with bf16 inputs both sides see the same
+values and only fp32 accumulation and the exp2/log2 approximations differ,
+~1e-6).  fp32 inputs are rounded to bf16 on the device, which moves each
+score by a bounded amount; their LSE tolerance adds that per-row bound.
 The tile plans the device walks must equal the oracle's enumeration exactly.
 """
 
@@ -76,10 +77,22 @@ def check(q, k, v, spec, rows=None, heads=None, tag=""):
     rel = np.linalg.norm(got_o - ref_o) / max(np.linalg.norm(ref_o), 1e-30)
     fin = np.isfinite(ref_lse)
     assert np.array_equal(fin, np.isfinite(got_lse)), f"{tag}: LSE -inf pattern differs"
+    lse_tol = np.full(ref_lse.shape, LSE_ABS)
+    if q.dtype == torch.float32:
+        # fp32 inputs are rounded to bf16 (relative error <= 2^-9 per element)
+        # before the products: to first order every score moves by at most
+        # scale * 2^-8 * sum_c |q_ic||k_jc|, and the LSE (a softmax-weighted
+        # mean of the scores) by at most the largest such move over j.
+        scale = 1.0 / np.sqrt(d)
+        qa, ka = np.abs(sel(q)[0]), np.abs(sel(k)[0])
+        bound = np.stack([(qa[i][rows_arr] @ ka[i].T).max(axis=1) for i in range(len(heads))])
+        lse_tol = np.maximum(lse_tol, scale * 2.0 ** -8 * bound + 1e-4)
+    diff = np.where(fin, got_lse, 0.0) - np.where(fin, ref_lse, 0.0)
+    lse_bad = fin & (np.abs(diff) > lse_tol)
     lse_err = np.abs(got_lse[fin] - ref_lse[fin]).max() if fin.any() else 0.0
     assert err.max() <= MAX_ABS, f"{tag}: max abs {err.max():.3e}"
     assert rel <= REL_L2, f"{tag}: rel L2 {rel:.3e}"
-    assert lse_err <= LSE_ABS, f"{tag}: lse err {lse_err:.3e}"
+    assert not lse_bad.any(), f"{tag}: lse err {lse_err:.3e} above tolerance"
     return o, lse
 
 
