@@ -206,8 +206,12 @@ def run_gpu(args):
     dev = f"cuda:{local}"
 
     # ---------------- headline step
-    wl_name, mask_name = HEADLINE
+    wl_name, mask_name = args.workload or HEADLINE[0], args.mask or HEADLINE[1]
     wl = WORKLOADS[wl_name]
+    if args.n or args.heads:  # same recipe at a smaller size (profiling cases)
+        import dataclasses
+
+        wl = dataclasses.replace(wl, N=args.n or wl.N, H=args.heads or wl.H)
     q, k, v = make_workload_inputs(wl, seed=0, device=dev)
     spec = make_mask(wl, mask_name, seed=0)
     mask = mattn.prepare(spec, wl.H, wl.N, device=dev)
@@ -436,6 +440,10 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--quick", action="store_true", help="headline step only (no e2e, sweep or oracle)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--workload", default=None, help="headline workload name (default bsparse128k)")
+    ap.add_argument("--mask", default=None, help="mask of that workload")
+    ap.add_argument("--n", type=int, default=0, help="shrink N (profiling cases)")
+    ap.add_argument("--heads", type=int, default=0, help="shrink H (profiling cases)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

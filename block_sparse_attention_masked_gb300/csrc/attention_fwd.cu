@@ -14,7 +14,8 @@
 //
 // Roles (384 threads):
 //   warp 0        TMA producer: Q_0, Q_1 once, then K/V tiles into rings
-//   warp 1        tensor-memory allocator and single-thread MMA issuer
+//   warp 1        tensor-memory allocator; MMA issuer of sub-tile 0
+//   warp 2        MMA issuer of sub-tile 1
 //   warps 4..7    softmax + epilogue of sub-tile 0 (one query row per thread)
 //   warps 8..11   softmax + epilogue of sub-tile 1
 // Tensor memory (512 columns x 128 lanes, fp32):
@@ -57,6 +58,15 @@ struct Geo {
   static constexpr uint32_t kRemSwizzle = (kRem == 16) ? ptx::kSw32 : ptx::kSw64;
   static constexpr int kRemRowBytes = kRem * 2;           // 32 or 64
   static_assert(kTileBytes % 1024 == 0, "tiles must keep 1 KiB alignment");
+  // V is the MN-major B operand of one N = D MMA per 16 keys (an MMA costs
+  // the same ~64 cycles for any N <= 128), so it needs one swizzle across
+  // all D columns: atoms of kVW columns (64 -> 128-byte swizzle, 32 -> 64,
+  // 16 -> 32), one TMA box per atom column.
+  static constexpr int kVW = (D % 64 == 0) ? 64 : ((D % 32 == 0) ? 32 : 16);
+  static constexpr int kVChunks = D / kVW;
+  static constexpr int kVChunkBytes = kTile * kVW * 2;
+  static constexpr uint32_t kVSwizzle = kVW == 64 ? ptx::kSw128 : (kVW == 32 ? ptx::kSw64 : ptx::kSw32);
+  static_assert(kVChunks * kVChunkBytes == kTileBytes, "V tile size");
 };
 
 struct Barriers {
@@ -67,71 +77,89 @@ struct Barriers {
   uint64_t p_full[2];
   uint64_t o_final[2];
   uint64_t never;       // self-test: nothing ever arrives here
-  uint64_t drain;       // MMA drain on abort
+  uint64_t drain[2];    // MMA drain on abort, one per issuer
   uint32_t tmem_base;
   int abort_flag;
+};
+
+// Block-selection rows of up to this many 64-bit words (N <= 2^21 at
+// Bs = 128) are staged in shared memory; longer rows are read in place.
+constexpr int kMaxRowWords = 256;
+
+// Key-tile walk of one 128-row query sub-tile.
+struct SubPlan {
+  int qt;
+  bool rows;                 // the sub-tile has query rows (< N)
+  bool has_tiles;            // and at least one key tile
+  KRange r;                  // interval kinds
+  int ktmax;                 // block kind: last admissible key tile
+  const uint64_t* row;       // block kind: the sub-tile's bitmap row
 };
 
 // Work description of one CTA, computed identically by every thread.
 struct ItemPlan {
   int bh, h, b;
-  int qt[2];
-  bool rows[2];         // sub-tile has query rows (< N)
-  bool has_tiles[2];    // and at least one key tile
-  KRange r[2];          // interval kinds
-  int ktmax[2];         // block kind: last admissible key tile
-  const uint64_t* bits; // block kind: this head's bitmap
+  SubPlan sp0, sp1;
 };
 
-__device__ __forceinline__ int sub_next(const FwdParams& p, const ItemPlan& ip, int s, int from) {
-  if (!ip.rows[s]) return kNoTile;
-  if (p.kind == kBlockSparse) {
-    return block_next_kt(ip.bits, p.block_wpr, p.block_c, ip.qt[s], from, ip.ktmax[s]);
-  }
-  int kt = from > ip.r[s].lo ? from : ip.r[s].lo;
-  return kt <= ip.r[s].hi ? kt : kNoTile;
+__device__ __forceinline__ int sub_next(const FwdParams& p, const SubPlan& sp, int from) {
+  if (!sp.rows) return kNoTile;
+  if (p.kind == kBlockSparse) return block_row_next_kt(sp.row, p.block_c, from, sp.ktmax);
+  int kt = from > sp.r.lo ? from : sp.r.lo;
+  return kt <= sp.r.hi ? kt : kNoTile;
 }
 
-__device__ __forceinline__ bool sub_uses(const FwdParams& p, const ItemPlan& ip, int s, int kt) {
-  if (!ip.rows[s]) return false;
-  if (p.kind == kBlockSparse) {
-    return kt <= ip.ktmax[s] && block_bit(ip.bits, p.block_wpr, ip.qt[s] / p.block_c, kt / p.block_c);
-  }
-  return kt >= ip.r[s].lo && kt <= ip.r[s].hi;
+__device__ __forceinline__ bool sub_uses(const FwdParams& p, const SubPlan& sp, int kt) {
+  if (!sp.rows) return false;
+  if (p.kind == kBlockSparse) return kt <= sp.ktmax && block_row_bit(sp.row, kt / p.block_c);
+  return kt >= sp.r.lo && kt <= sp.r.hi;
 }
 
-__device__ __forceinline__ bool sub_partial(const FwdParams& p, const ItemPlan& ip, int s, int kt) {
-  if (p.kind == kBlockSparse) return block_tile_class(ip.qt[s], kt, p.N) == kTilePartial;
-  return interval_tile_class(ip.r[s], kt) == kTilePartial;
+__device__ __forceinline__ bool sub_partial(const FwdParams& p, const SubPlan& sp, int kt) {
+  if (p.kind == kBlockSparse) return block_tile_class(sp.qt, kt, p.N) == kTilePartial;
+  return interval_tile_class(sp.r, kt) == kTilePartial;
 }
 
 __device__ __forceinline__ int union_next(const FwdParams& p, const ItemPlan& ip, int from) {
-  int a = sub_next(p, ip, 0, from);
-  int c = sub_next(p, ip, 1, from);
+  int a = sub_next(p, ip.sp0, from);
+  int c = sub_next(p, ip.sp1, from);
   return a < c ? a : c;
 }
 
-__device__ __forceinline__ ItemPlan make_plan(const FwdParams& p, int item) {
+// Global bitmap row of sub-tile s of work item `it` (block kind).
+__device__ __forceinline__ const uint64_t* global_row(const FwdParams& p, int2 it, int s) {
+  const int h = it.x % p.H;
+  const int hb = (p.block_heads == 1) ? 0 : h;
+  const int qt = 2 * it.y + s;
+  return p.block_bits + ((int64_t)hb * p.block_nb + qt / p.block_c) * p.block_wpr;
+}
+
+__device__ __forceinline__ SubPlan make_subplan(const FwdParams& p, int2 it, int s, int param,
+                                                const uint64_t* staged_rows) {
+  SubPlan sp;
+  const int nt = (p.N + kTile - 1) / kTile;
+  sp.qt = 2 * it.y + s;
+  sp.rows = sp.qt < nt;
+  sp.ktmax = sp.qt < nt ? sp.qt : nt - 1;
+  sp.row = nullptr;
+  if (p.kind != kBlockSparse) {
+    sp.r = interval_krange(p.kind, param, p.N, sp.qt);
+  } else {
+    sp.r.lo = 0; sp.r.hi = -1; sp.r.flo = 0; sp.r.fhi = -1;
+    if (sp.rows) sp.row = staged_rows ? staged_rows + s * kMaxRowWords : global_row(p, it, s);
+  }
+  sp.has_tiles = sub_next(p, sp, 0) != kNoTile;
+  return sp;
+}
+
+__device__ __forceinline__ ItemPlan make_plan(const FwdParams& p, int2 it, const uint64_t* staged_rows) {
   ItemPlan ip;
-  int2 it = p.items[item];
   ip.bh = it.x;
   ip.h = it.x % p.H;
   ip.b = it.x / p.H;
-  const int nt = (p.N + kTile - 1) / kTile;
   const int param = p.head_info[ip.h * 4 + kHeadParam];
-  ip.bits = nullptr;
-  if (p.kind == kBlockSparse) {
-    int hb = (p.block_heads == 1) ? 0 : ip.h;
-    ip.bits = p.block_bits + (int64_t)hb * p.block_nb * p.block_wpr;
-  }
-  for (int s = 0; s < 2; ++s) {
-    ip.qt[s] = 2 * it.y + s;
-    ip.rows[s] = ip.qt[s] < nt;
-    ip.ktmax[s] = ip.qt[s] < nt ? ip.qt[s] : nt - 1;
-    if (p.kind != kBlockSparse) ip.r[s] = interval_krange(p.kind, param, p.N, ip.qt[s]);
-    else { ip.r[s].lo = 0; ip.r[s].hi = -1; ip.r[s].flo = 0; ip.r[s].fhi = -1; }
-  }
-  for (int s = 0; s < 2; ++s) ip.has_tiles[s] = sub_next(p, ip, s, 0) != kNoTile;
+  ip.sp0 = make_subplan(p, it, 0, param, staged_rows);
+  ip.sp1 = make_subplan(p, it, 1, param, staged_rows);
   return ip;
 }
 
@@ -161,55 +189,73 @@ __device__ __forceinline__ void load_tile(const FwdParams& p, const CUtensorMap*
   }
 }
 
-// S = Q K^T for one sub-tile: D/16 MMAs of M128 N128 K16, both operands K-major.
+// TMA load of one 128-row V tile in its uniform-swizzle layout (map [0] of
+// the V views has a kVW-column box).
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint32_t q_smem, uint32_t k_smem) {
+__device__ __forceinline__ void load_v_tile(const FwdParams& p, bool column_major, uint8_t* dst, uint64_t* bar,
+                                            int p0, int bh) {
+  using G = Geo<D>;
+  if (!column_major) {
+#pragma unroll
+    for (int c = 0; c < G::kVChunks; ++c)
+      ptx::tma_load_3d(dst + c * G::kVChunkBytes, &p.tv[0], bar, c * G::kVW, p0, bh);
+  } else {
+    const int col = p0 / p.grid_rows;
+    const int r0 = p0 - col * p.grid_rows;
+#pragma unroll
+    for (int c = 0; c < G::kVChunks; ++c)
+      ptx::tma_load_4d(dst + c * G::kVChunkBytes, &p.cv[0], bar, c * G::kVW, col, r0, bh);
+  }
+}
+
+// S = Q K^T for one sub-tile: D/16 MMAs of M128 N128 K16, both operands K-major.
+// Operand addresses are passed pre-shifted (shared address >> 4, the
+// descriptor's start-address field): the issuing thread then spends one add
+// per operand per MMA, the high descriptor words being compile-time constants.
+__device__ __forceinline__ uint64_t desc_of(uint32_t lo, uint32_t hi) { return ((uint64_t)hi << 32) | lo; }
+
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint32_t q_addr4, uint32_t k_addr4) {
   using G = Geo<D>;
   constexpr uint32_t idesc = ptx::idesc_bf16(128, 128, 0);
+  constexpr uint32_t lbo = 1u << 16;  // unused for swizzled K-major operands
+  constexpr uint32_t hi128 = ptx::smem_desc_hi(1024, ptx::kSw128);
+  constexpr uint32_t hiR = ptx::smem_desc_hi(8 * G::kRemRowBytes, G::kRemSwizzle);
   int step = 0;
 #pragma unroll
   for (int c = 0; c < G::kChunks; ++c) {
 #pragma unroll
     for (int k = 0; k < 4; ++k, ++step) {
-      uint32_t off = c * G::kChunkBytes + k * 32;
-      uint64_t a = ptx::smem_desc(q_smem + off, 16, 1024, ptx::kSw128);
-      uint64_t b = ptx::smem_desc(k_smem + off, 16, 1024, ptx::kSw128);
-      ptx::mma_ss(s_tmem, a, b, idesc, step > 0);
+      const uint32_t off4 = ((c * G::kChunkBytes + k * 32) >> 4) + lbo;
+      ptx::mma_ss(s_tmem, desc_of(q_addr4 + off4, hi128), desc_of(k_addr4 + off4, hi128), idesc, step > 0);
     }
   }
   if (G::kRem) {
 #pragma unroll
     for (int k = 0; k < G::kRem / 16; ++k, ++step) {
-      uint32_t off = G::kChunks * G::kChunkBytes + k * 32;
-      uint64_t a = ptx::smem_desc(q_smem + off, 16, 8 * G::kRemRowBytes, G::kRemSwizzle);
-      uint64_t b = ptx::smem_desc(k_smem + off, 16, 8 * G::kRemRowBytes, G::kRemSwizzle);
-      ptx::mma_ss(s_tmem, a, b, idesc, step > 0);
+      const uint32_t off4 = ((G::kChunks * G::kChunkBytes + k * 32) >> 4) + lbo;
+      ptx::mma_ss(s_tmem, desc_of(q_addr4 + off4, hiR), desc_of(k_addr4 + off4, hiR), idesc, step > 0);
     }
   }
 }
 
 // O += P V for one sub-tile: P (128 x 128 keys, bf16 pairs in TMEM) is the
-// A operand; V (keys x d, d contiguous) is an MN-major B operand.  One MMA
-// per 16 keys and per column chunk.
+// A operand; V (keys x d, d contiguous) is an MN-major B operand whose
+// kVW-column atoms lie kVChunkBytes apart (leading byte offset) and whose
+// 8-key groups lie 8 rows apart (stride byte offset).  One N = D MMA per
+// 16 keys.
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_smem, bool accumulate) {
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_addr4, bool accumulate) {
   using G = Geo<D>;
-  constexpr uint32_t idesc64 = ptx::idesc_bf16(128, 64, 1);
-  constexpr uint32_t idescR = ptx::idesc_bf16(128, G::kRem ? G::kRem : 16, 1);
+  constexpr uint32_t idesc = ptx::idesc_bf16(128, D, 1);
+  constexpr uint32_t row_bytes = G::kVW * 2;
+  constexpr uint32_t lbo = (uint32_t)(G::kVChunkBytes >> 4) << 16;
+  constexpr uint32_t hi = ptx::smem_desc_hi(8 * row_bytes, G::kVSwizzle);
 #pragma unroll
   for (int k = 0; k < kTile / 16; ++k) {
     const uint32_t acc = (accumulate || k > 0) ? 1u : 0u;
     const uint32_t a = p_tmem + k * 8;  // 16 bf16 keys = 8 columns
-#pragma unroll
-    for (int c = 0; c < G::kChunks; ++c) {
-      uint64_t bdesc = ptx::smem_desc(v_smem + c * G::kChunkBytes + k * 16 * 128, G::kChunkBytes, 1024, ptx::kSw128);
-      ptx::mma_ts(o_tmem + c * 64, a, bdesc, idesc64, acc);
-    }
-    if (G::kRem) {
-      uint64_t bdesc = ptx::smem_desc(v_smem + G::kChunks * G::kChunkBytes + k * 16 * G::kRemRowBytes,
-                                      G::kRemBytes, 8 * G::kRemRowBytes, G::kRemSwizzle);
-      ptx::mma_ts(o_tmem + G::kChunks * 64, a, bdesc, idescR, acc);
-    }
+    ptx::mma_ts(o_tmem, a, desc_of(v_addr4 + ((k * 16 * row_bytes) >> 4) + lbo, hi), idesc, acc);
   }
 }
 
@@ -234,10 +280,22 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
   uint8_t* sk = sq + 2 * G::kTileBytes;
   uint8_t* sv = sk + KS * G::kTileBytes;
   Barriers* bar = reinterpret_cast<Barriers*>(sv + VS * G::kTileBytes);
+  uint64_t* staged_rows = reinterpret_cast<uint64_t*>(bar + 1);  // [2][kMaxRowWords]
   volatile int* abort_flag = &bar->abort_flag;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int2 item = p.items[blockIdx.x];
+  const bool stage_rows = p.kind == kBlockSparse && p.block_wpr <= kMaxRowWords;
+  if (stage_rows && (warp == 2 || warp == 3)) {
+    // the two bitmap rows this CTA walks, copied once to shared memory
+    const int s = warp - 2;
+    const int nt = (p.N + kTile - 1) / kTile;
+    if (2 * item.y + s < nt) {
+      const uint64_t* src = global_row(p, item, s);
+      for (int w = lane; w < p.block_wpr; w += 32) staged_rows[s * kMaxRowWords + w] = src[w];
+    }
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
@@ -248,12 +306,13 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
     }
     for (int i = 0; i < 3; ++i) {
       ptx::mbar_init(&bar->k_full[i], 1);
-      ptx::mbar_init(&bar->k_empty[i], 1);
+      ptx::mbar_init(&bar->k_empty[i], 2);  // one commit from each MMA issuer
       ptx::mbar_init(&bar->v_full[i], 1);
-      ptx::mbar_init(&bar->v_empty[i], 1);
+      ptx::mbar_init(&bar->v_empty[i], 2);
     }
     ptx::mbar_init(&bar->never, 1);
-    ptx::mbar_init(&bar->drain, 1);
+    ptx::mbar_init(&bar->drain[0], 1);
+    ptx::mbar_init(&bar->drain[1], 1);
     bar->abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -266,19 +325,26 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
   ptx::tc_fence_after();
   const uint32_t tmem = bar->tmem_base;
 
-  const ItemPlan ip = make_plan(p, blockIdx.x);
+  const ItemPlan ip = make_plan(p, item, stage_rows ? staged_rows : nullptr);
   const int load_mode = p.head_info[ip.h * 4 + kHeadLoad];
   const bool colmaj = load_mode == kLoadColumnMajor;
 
+  // Registers: 384 threads launched at 168 each; the producer / MMA
+  // warpgroup gives up to 72 so that each softmax warpgroup can hold a full
+  // 128-column score row (216 per thread, 72 + 2 * 216 = 3 * 168).  Each
+  // role branch starts with its own budget change.
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    ptx::setmaxnreg_dec<72>();
     if (lane == 0) {
       const CUtensorMap* mq = colmaj ? p.cq : p.tq;
       ptx::prefetch_tmap(&mq[0]);
+#pragma unroll
       for (int s = 0; s < 2; ++s) {
-        if (!ip.has_tiles[s]) continue;
+        const SubPlan& sp = s ? ip.sp1 : ip.sp0;
+        if (!sp.has_tiles) continue;
         ptx::mbar_arrive_expect_tx(&bar->q_full[s], G::kTileBytes);
-        load_tile<D>(p, p.tq, p.cq, colmaj, sq + s * G::kTileBytes, &bar->q_full[s], ip.qt[s] * kTile, ip.bh);
+        load_tile<D>(p, p.tq, p.cq, colmaj, sq + s * G::kTileBytes, &bar->q_full[s], sp.qt * kTile, ip.bh);
       }
       int j = 0;
       for (int kt = union_next(p, ip, 0); kt != kNoTile; kt = union_next(p, ip, kt + 1), ++j) {
@@ -294,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
           break;
         }
         ptx::mbar_arrive_expect_tx(&bar->v_full[vs], G::kTileBytes);
-        load_tile<D>(p, p.tv, p.cv, colmaj, sv + vs * G::kTileBytes, &bar->v_full[vs], kt * kTile, ip.bh);
+        load_v_tile<D>(p, colmaj, sv + vs * G::kTileBytes, &bar->v_full[vs], kt * kTile, ip.bh);
       }
       if (*abort_flag) {
         // let copies already in flight land before the CTA's shared memory goes away
@@ -302,71 +368,73 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
         while (ptx::globaltimer_ns() - t0 < 2000000ull) { }
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp 1 issues the MMAs of query sub-tile 0, warp 2 those of sub-tile 1,
+    // so that neither waits behind the other's softmax: the tensor core
+    // interleaves two independent instruction streams.  Both walk the same
+    // key-tile list in order; every K / V ring slot is released by one
+    // commit from each issuer per entry (the empty barriers count 2).  An
+    // issuer that skips an entry still waits for the slot to be filled before
+    // releasing it, which keeps the two issuers' arrivals in phase order.
+    ptx::setmaxnreg_dec<72>();
+    const int s = warp - 1;
+    const SubPlan sp = s ? ip.sp1 : ip.sp0;
     if (lane == 0) {
       bool ok = true;
-      if (p.self_test_timeout) {
+      if (p.self_test_timeout && s == 0) {
         // nothing ever arrives on this barrier: exercises the bounded-wait path
         if (!ptx::mbar_wait(&bar->never, 0, p.timeout_ns, abort_flag)) {
           raise_error(p, bar, kErrSelfTest);
           ok = false;
         }
       }
-      for (int s = 0; s < 2 && ok; ++s) {
-        if (!ip.has_tiles[s]) continue;
-        if (!ptx::mbar_wait(&bar->q_full[s], 0, p.timeout_ns, abort_flag)) {
-          raise_error(p, bar, kErrMma);
-          ok = false;
-        }
+      if (ok && sp.has_tiles && !ptx::mbar_wait(&bar->q_full[s], 0, p.timeout_ns, abort_flag)) {
+        raise_error(p, bar, kErrMma);
+        ok = false;
       }
       ptx::tc_fence_after();
-      const uint32_t q_smem = ptx::smem_addr(sq);
-      const uint32_t k_smem = ptx::smem_addr(sk);
-      const uint32_t v_smem = ptx::smem_addr(sv);
-      bool pend[2] = {false, false};
-      bool first[2] = {true, true};
-      uint32_t pcount[2] = {0, 0};
+      constexpr uint32_t tile4 = G::kTileBytes >> 4;  // descriptor start-address units
+      const uint32_t q4 = (ptx::smem_addr(sq) >> 4) + s * tile4;
+      const uint32_t k4 = ptx::smem_addr(sk) >> 4;
+      const uint32_t v4 = ptx::smem_addr(sv) >> 4;
+      const uint32_t s_tm = tmem + s * 128;
+      const uint32_t o_tm = tmem + 256 + s * 128;
+      bool pend = false, first = true, issued_any = false;
+      uint32_t pcount = 0;
       int j = 0;
-      bool issued_any = false;
       if (ok) {
         for (int kt = union_next(p, ip, 0); kt != kNoTile; kt = union_next(p, ip, kt + 1), ++j) {
           const int ks = j % KS;
           if (j >= 1) {
+            // finish the previous entry: its P V (when this sub-tile used it), then release V
             const int e = j - 1;
             if (!ptx::mbar_wait(&bar->v_full[e % VS], (e / VS) & 1, p.timeout_ns, abort_flag)) {
               raise_error(p, bar, kErrMma); ok = false; break;
             }
-          }
-          bool k_ready = false;
-          for (int s = 0; s < 2 && ok; ++s) {
-            if (pend[s]) {
-              if (!ptx::mbar_wait(&bar->p_full[s], pcount[s] & 1, p.timeout_ns, abort_flag)) {
+            if (pend) {
+              if (!ptx::mbar_wait(&bar->p_full[s], pcount & 1, p.timeout_ns, abort_flag)) {
                 raise_error(p, bar, kErrMma); ok = false; break;
               }
-              ++pcount[s];
+              ++pcount;
               ptx::tc_fence_after();
-              issue_pv<D>(tmem + 256 + s * 128, tmem + s * 128, v_smem + ((j - 1) % VS) * G::kTileBytes, !first[s]);
-              first[s] = false;
-              pend[s] = false;
+              issue_pv<D>(o_tm, s_tm, v4 + (e % VS) * tile4, !first);
+              first = false;
+              pend = false;
             }
-            if (sub_uses(p, ip, s, kt)) {
-              if (!k_ready) {
-                if (!ptx::mbar_wait(&bar->k_full[ks], (j / KS) & 1, p.timeout_ns, abort_flag)) {
-                  raise_error(p, bar, kErrMma); ok = false; break;
-                }
-                ptx::tc_fence_after();
-                k_ready = true;
-              }
-              issue_qk<D>(tmem + s * 128, q_smem + s * G::kTileBytes, k_smem + ks * G::kTileBytes);
-              ptx::mma_commit(&bar->s_full[s]);
-              pend[s] = true;
-              issued_any = true;
-            }
+            ptx::mma_commit(&bar->v_empty[e % VS]);
           }
-          if (!ok) break;
+          if (!ptx::mbar_wait(&bar->k_full[ks], (j / KS) & 1, p.timeout_ns, abort_flag)) {
+            raise_error(p, bar, kErrMma); ok = false; break;
+          }
+          ptx::tc_fence_after();
+          if (sub_uses(p, sp, kt)) {
+            issue_qk<D>(s_tm, q4, k4 + ks * tile4);
+            ptx::mma_commit(&bar->s_full[s]);
+            pend = true;
+            issued_any = true;
+          }
           ptx::mma_commit(&bar->k_empty[ks]);
-          if (j >= 1) ptx::mma_commit(&bar->v_empty[(j - 1) % VS]);
         }
       }
       if (ok && j >= 1) {
@@ -374,38 +442,41 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
         if (!ptx::mbar_wait(&bar->v_full[e % VS], (e / VS) & 1, p.timeout_ns, abort_flag)) {
           raise_error(p, bar, kErrMma); ok = false;
         }
-        for (int s = 0; s < 2 && ok; ++s) {
-          if (!pend[s]) continue;
-          if (!ptx::mbar_wait(&bar->p_full[s], pcount[s] & 1, p.timeout_ns, abort_flag)) {
-            raise_error(p, bar, kErrMma); ok = false; break;
+        if (ok && pend) {
+          if (!ptx::mbar_wait(&bar->p_full[s], pcount & 1, p.timeout_ns, abort_flag)) {
+            raise_error(p, bar, kErrMma); ok = false;
+          } else {
+            ++pcount;
+            ptx::tc_fence_after();
+            issue_pv<D>(o_tm, s_tm, v4 + (e % VS) * tile4, !first);
+            first = false;
+            pend = false;
           }
-          ++pcount[s];
-          ptx::tc_fence_after();
-          issue_pv<D>(tmem + 256 + s * 128, tmem + s * 128, v_smem + (e % VS) * G::kTileBytes, !first[s]);
-          first[s] = false;
-          pend[s] = false;
         }
         if (ok) {
           ptx::mma_commit(&bar->v_empty[e % VS]);
-          for (int s = 0; s < 2; ++s)
-            if (ip.has_tiles[s]) ptx::mma_commit(&bar->o_final[s]);
+          if (sp.has_tiles) ptx::mma_commit(&bar->o_final[s]);
         }
       }
       if (!ok && issued_any) {
         // wait (bounded) for the MMAs already issued before tensor memory is freed
-        ptx::mma_commit(&bar->drain);
-        ptx::mbar_wait_time_only(&bar->drain, 0, p.timeout_ns);
+        ptx::mma_commit(&bar->drain[s]);
+        ptx::mbar_wait_time_only(&bar->drain[s], 0, p.timeout_ns);
       }
     }
-  } else if (warp >= 4) {
+  } else if (warp < 4) {
+    ptx::setmaxnreg_dec<72>();  // idle warp of the first warpgroup
+  } else {
     // ------------------------------------------------------------ softmax + epilogue
+    ptx::setmaxnreg_inc<216>();
     const int s = (warp - 4) >> 2;
     const int quarter = warp & 3;  // tensor-memory lane quarter this warp may access
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t s_tmem = tmem + lane_off + s * 128;
     const uint32_t o_tmem = tmem + lane_off + 256 + s * 128;
-    const int64_t pos = (int64_t)ip.qt[s] * kTile + row;
+    const SubPlan sp = s ? ip.sp1 : ip.sp0;
+    const int64_t pos = (int64_t)sp.qt * kTile + row;
     const int h = ip.h;
     const int param = p.head_info[h * 4 + kHeadParam];
     int64_t lo, hi;
@@ -417,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
     float l = 0.f;        // running sum of exp2(x - m)
     int count = 0;
     bool ok = true;
-    for (int kt = sub_next(p, ip, s, 0); kt != kNoTile; kt = sub_next(p, ip, s, kt + 1), ++count) {
+    for (int kt = sub_next(p, sp, 0); kt != kNoTile; kt = sub_next(p, sp, kt + 1), ++count) {
       bool got = ptx::mbar_wait(&bar->s_full[s], count & 1, p.timeout_ns, abort_flag);
       if (!__all_sync(0xffffffffu, got)) {
         if (lane == 0) raise_error(p, bar, kErrSoftmax);
@@ -431,17 +502,27 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
       ptx::tmem_ld32(s_tmem + 64, *reinterpret_cast<float(*)[32]>(&x[64]));
       ptx::tmem_ld32(s_tmem + 96, *reinterpret_cast<float(*)[32]>(&x[96]));
       ptx::tmem_wait_ld();
-      if (sub_partial(p, ip, s, kt)) {
+      if (sub_partial(p, sp, kt)) {
+        // visible key columns of this row inside the tile: [c_lo, c_hi]
         const int64_t k0 = (int64_t)kt * kTile;
+        const int c_lo = (int)(lo - k0 < -1 ? -1 : (lo - k0 > 128 ? 128 : lo - k0));
+        const int c_hi = (int)(hi - k0 < -1 ? -1 : (hi - k0 > 128 ? 128 : hi - k0));
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          const int64_t q = k0 + c;
-          if (q < lo || q > hi) x[c] = -INFINITY;
-        }
+        for (int c = 0; c < 128; ++c)
+          if (c < c_lo || c > c_hi) x[c] = -INFINITY;
       }
-      float mx = x[0];
+      // row max over 8 independent chains (short dependency paths)
+      float mx;
+      {
+        float a[8];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, x[c]);
+        for (int i = 0; i < 8; ++i) a[i] = x[i];
+#pragma unroll
+        for (int c = 8; c < 128; c += 8)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) a[i] = fmaxf(a[i], x[c + i]);
+        mx = fmaxf(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])), fmaxf(fmaxf(a[4], a[5]), fmaxf(a[6], a[7])));
+      }
       mx *= sl2;
       const float m_new = fmaxf(m, mx);
       const bool need_rescale = (m != -INFINITY) && (m_new - m > kRescaleThreshold);
@@ -466,27 +547,36 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
         }
       }
       const float mref = (m == -INFINITY) ? 0.f : m;
-      float sum = 0.f;
+      // P = exp2(s * scale * log2e - m): packed two-lane FMAs for the
+      // arguments, four independent packed accumulators for the row sum
+      const float2 sl2v = make_float2(sl2, sl2);
+      const float2 negm = make_float2(-mref, -mref);
+      float2 acc[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
 #pragma unroll
       for (int c0 = 0; c0 < 128; c0 += 32) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ptx::ex2(fmaf(x[c0 + 2 * i], sl2, -mref));
-          const float p1 = ptx::ex2(fmaf(x[c0 + 2 * i + 1], sl2, -mref));
-          sum += p0 + p1;
-          pk[i] = ptx::pack_bf16x2(p0, p1);
+          const float2 t = ptx::ffma2(make_float2(x[c0 + 2 * i], x[c0 + 2 * i + 1]), sl2v, negm);
+          const float2 pp = make_float2(ptx::ex2(t.x), ptx::ex2(t.y));
+          acc[i & 3] = ptx::fadd2(acc[i & 3], pp);
+          pk[i] = ptx::pack_bf16x2(pp.x, pp.y);
         }
         ptx::tmem_st16(s_tmem + c0 / 2, pk);
       }
-      l += sum;
+      const float2 acc01 = ptx::fadd2(acc[0], acc[1]);
+      const float2 acc23 = ptx::fadd2(acc[2], acc[3]);
+      const float2 accs = ptx::fadd2(acc01, acc23);
+      l += accs.x + accs.y;
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(&bar->p_full[s]);
     }
 
     // ---------------------------------------------------------- epilogue
-    if (ok && ip.rows[s]) {
+    if (ok && sp.rows) {
       bool have_o = false;
       if (count > 0) {
         bool got = ptx::mbar_wait(&bar->o_final[s], 0, p.timeout_ns, abort_flag);
@@ -634,7 +724,8 @@ cudaError_t launch_one(const FwdParams& p, cudaStream_t stream) {
 template <int D>
 size_t smem_for() {
   using G = Geo<D>;
-  size_t bytes = (size_t)(2 + 2 * G::kStages) * G::kTileBytes + sizeof(Barriers) + 1024;
+  size_t bytes = (size_t)(2 + 2 * G::kStages) * G::kTileBytes + sizeof(Barriers) +
+                 2 * kMaxRowWords * sizeof(uint64_t) + 1024;
   // at least ~120 KiB so that one CTA owns an SM (and all of its tensor memory)
   return bytes < 120 * 1024 ? 120 * 1024 : bytes;
 }

@@ -366,6 +366,35 @@ int make_maps(const Normalized& n, const void* base, CUtensorMap raster[2], CUte
   return MATTN_OK;
 }
 
+// Views of V in one uniform swizzle (map [0] only): boxes of vw columns,
+// vw = 64 when d % 64 == 0, else 32 when d % 32 == 0, else 16; the kernel's
+// P V product reads all d columns as one MN-major operand.
+int make_v_maps(const Normalized& n, const void* base, CUtensorMap raster[2], CUtensorMap colmaj[2], int rows,
+                int cols) {
+  const int d = n.d;
+  const int vw = d % 64 == 0 ? 64 : (d % 32 == 0 ? 32 : 16);
+  const CUtensorMapSwizzle sw =
+      vw == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : (vw == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+  const cuuint64_t bh = (cuuint64_t)n.B * n.H;
+  memset(raster, 0, 2 * sizeof(CUtensorMap));
+  memset(colmaj, 0, 2 * sizeof(CUtensorMap));
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n.N, bh};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)n.N * d * 2};
+    cuuint32_t box[3] = {(cuuint32_t)vw, (cuuint32_t)kTile, 1};
+    int rc = encode(&raster[0], base, 3, dims, strides, box, sw);
+    if (rc) return rc;
+  }
+  if (rows > 0) {
+    cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)cols, (cuuint64_t)rows, bh};
+    cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)cols * d * 2, (cuuint64_t)n.N * d * 2};
+    cuuint32_t box[4] = {(cuuint32_t)vw, 1, (cuuint32_t)kTile, 1};
+    int rc = encode(&colmaj[0], base, 4, dims, strides, box, sw);
+    if (rc) return rc;
+  }
+  return MATTN_OK;
+}
+
 int check_device_ptrs(const void* q, const void* k, const void* v, const void* o, const float* lse) {
   if (!q || !k || !v || !o) return fail(MATTN_ERR_INVALID_ARG, "q, k, v and o must be non-NULL");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
@@ -418,7 +447,7 @@ int fwd_locked(const void* q, const void* k, const void* v, void* o, float* lse,
   const int cols = n.any_colmajor_tma ? desc->grid_cols : 0;
   if ((rc = make_maps(n, use[0], p.tq, p.cq, rows, cols))) return rc;
   if ((rc = make_maps(n, use[1], p.tk, p.ck, rows, cols))) return rc;
-  if ((rc = make_maps(n, use[2], p.tv, p.cv, rows, cols))) return rc;
+  if ((rc = make_v_maps(n, use[2], p.tv, p.cv, rows, cols))) return rc;
   p.o = o;
   p.lse = lse;
   p.items = plan->items;

@@ -113,13 +113,13 @@ MATTN_HD bool block_bit(const uint64_t* bits, int wpr, int m, int nblk) {
   return (bits[(int64_t)m * wpr + (nblk >> 6)] >> (nblk & 63)) & 1ull;
 }
 
-// Smallest kept key tile kt >= from with kt <= ktmax for query tile qt of a
+MATTN_HD bool block_row_bit(const uint64_t* row, int nblk) { return (row[nblk >> 6] >> (nblk & 63)) & 1ull; }
+
+// Smallest kept key tile kt >= from with kt <= ktmax in one bitmap row of a
 // block-sparse head (Bs = 128*c); returns INT32_MAX when there is none.
-MATTN_HD int block_next_kt(const uint64_t* bits, int wpr, int c, int qt, int from, int ktmax) {
+MATTN_HD int block_row_next_kt(const uint64_t* row, int c, int from, int ktmax) {
   if (from < 0) from = 0;
   if (from > ktmax) return 0x7fffffff;
-  int m = qt / c;
-  const uint64_t* row = bits + (int64_t)m * wpr;
   int nb0 = from / c;
   if ((row[nb0 >> 6] >> (nb0 & 63)) & 1ull) return from;
   int nb = nb0 + 1;
@@ -139,6 +139,11 @@ MATTN_HD int block_next_kt(const uint64_t* bits, int wpr, int c, int qt, int fro
   if (nb > nbmax) return 0x7fffffff;
   int kt = nb * c;
   return kt <= ktmax ? kt : 0x7fffffff;
+}
+
+// The same for query tile qt of a head whose bitmap starts at `bits`.
+MATTN_HD int block_next_kt(const uint64_t* bits, int wpr, int c, int qt, int from, int ktmax) {
+  return block_row_next_kt(bits + (int64_t)(qt / c) * wpr, c, from, ktmax);
 }
 
 MATTN_HD int block_tile_class(int qt, int kt, int64_t n) {
