@@ -259,6 +259,42 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
   }
 }
 
+// Of every 16 column pairs of a FULL tile, this many take their exponential
+// from the FMA-pipe polynomial instead of MUFU ex2.  Measured on GB300 the
+// MUFU is not the limiter of this softmax (it retires a warp's ex2 in ~4
+// cycles) and every emulated share tried (3..9 of 16) was slower, so the
+// default is 0; the polynomial stays available and tested.
+#ifndef MATTN_EXP_EMU_PAIRS
+#define MATTN_EXP_EMU_PAIRS 0
+#endif
+constexpr int kExpEmuPairs = MATTN_EXP_EMU_PAIRS;
+
+// P = exp2(x * sl2 - mref) for the 128 scores of this thread's row, packed
+// to bf16 pairs and stored to tensor memory at p_tmem (64 columns); returns
+// the fp32 row sum as two partial lanes.  The last EMU pairs of every
+// 16-pair chunk use the polynomial exp2.
+template <int EMU>
+__device__ __forceinline__ float2 exp_to_tmem(const float (&x)[128], float sl2, float mref, uint32_t p_tmem) {
+  const float2 sl2v = make_float2(sl2, sl2);
+  const float2 negm = make_float2(-mref, -mref);
+  float2 acc[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int c0 = 0; c0 < 128; c0 += 32) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float2 t = ptx::ffma2(make_float2(x[c0 + 2 * i], x[c0 + 2 * i + 1]), sl2v, negm);
+      const float2 pp = (i >= 16 - EMU) ? ptx::exp2_poly2(t) : make_float2(ptx::ex2(t.x), ptx::ex2(t.y));
+      acc[i & 3] = ptx::fadd2(acc[i & 3], pp);
+      pk[i] = ptx::pack_bf16x2(pp.x, pp.y);
+    }
+    ptx::tmem_st16(p_tmem + c0 / 2, pk);
+  }
+  return ptx::fadd2(ptx::fadd2(acc[0], acc[1]), ptx::fadd2(acc[2], acc[3]));
+}
+
 __device__ __forceinline__ int64_t token_of(const FwdParams& p, int store_mode, int perm_row, int64_t pos) {
   if (store_mode == kStoreColumnMajor) {
     int64_t c = pos / p.grid_rows;
@@ -502,7 +538,8 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
       ptx::tmem_ld32(s_tmem + 64, *reinterpret_cast<float(*)[32]>(&x[64]));
       ptx::tmem_ld32(s_tmem + 96, *reinterpret_cast<float(*)[32]>(&x[96]));
       ptx::tmem_wait_ld();
-      if (sub_partial(p, sp, kt)) {
+      const bool partial = sub_partial(p, sp, kt);
+      if (partial) {
         // visible key columns of this row inside the tile: [c_lo, c_hi]
         const int64_t k0 = (int64_t)kt * kTile;
         const int c_lo = (int)(lo - k0 < -1 ? -1 : (lo - k0 > 128 ? 128 : lo - k0));
@@ -511,7 +548,8 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
         for (int c = 0; c < 128; ++c)
           if (c < c_lo || c > c_hi) x[c] = -INFINITY;
       }
-      // row max over 8 independent chains (short dependency paths)
+      // row max over 8 independent chains (short dependency paths; measured
+      // faster here than three-input maxima)
       float mx;
       {
         float a[8];
@@ -547,28 +585,11 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
         }
       }
       const float mref = (m == -INFINITY) ? 0.f : m;
-      // P = exp2(s * scale * log2e - m): packed two-lane FMAs for the
-      // arguments, four independent packed accumulators for the row sum
-      const float2 sl2v = make_float2(sl2, sl2);
-      const float2 negm = make_float2(-mref, -mref);
-      float2 acc[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 t = ptx::ffma2(make_float2(x[c0 + 2 * i], x[c0 + 2 * i + 1]), sl2v, negm);
-          const float2 pp = make_float2(ptx::ex2(t.x), ptx::ex2(t.y));
-          acc[i & 3] = ptx::fadd2(acc[i & 3], pp);
-          pk[i] = ptx::pack_bf16x2(pp.x, pp.y);
-        }
-        ptx::tmem_st16(s_tmem + c0 / 2, pk);
-      }
-      const float2 acc01 = ptx::fadd2(acc[0], acc[1]);
-      const float2 acc23 = ptx::fadd2(acc[2], acc[3]);
-      const float2 accs = ptx::fadd2(acc01, acc23);
+      // P = exp2(s * scale * log2e - m) into tensor memory; on FULL tiles a
+      // share of the exponentials runs on the FMA pipe (every argument is
+      // finite there), on PARTIAL tiles all use MUFU ex2 (exp2(-inf) = 0)
+      const float2 accs = partial ? exp_to_tmem<0>(x, sl2, mref, s_tmem)
+                                  : exp_to_tmem<kExpEmuPairs>(x, sl2, mref, s_tmem);
       l += accs.x + accs.y;
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
@@ -711,6 +732,17 @@ __global__ void gather_kernel(const GatherParams p) {
   *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dst[t]) + row * p.d + c8) = out;
 }
 
+// Test hook: the softmax's polynomial exp2 next to CUDA's exp2f.
+__global__ void exp2_check_kernel(const float* x, float* y_poly, float* y_ref, int n) {
+  const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
+  if (i + 1 >= n) return;
+  const float2 r = ptx::exp2_poly2(make_float2(x[i], x[i + 1]));
+  y_poly[i] = r.x;
+  y_poly[i + 1] = r.y;
+  y_ref[i] = exp2f(x[i]);
+  y_ref[i + 1] = exp2f(x[i + 1]);
+}
+
 template <int D, bool F32>
 cudaError_t launch_one(const FwdParams& p, cudaStream_t stream) {
   const size_t smem = attention_smem_bytes(D);
@@ -765,6 +797,12 @@ cudaError_t launch_plan_dump(const PlanDumpParams& p, cudaStream_t stream) {
   const int total = p.H * nt;
   if (total == 0) return cudaSuccess;
   plan_dump_kernel<<<(total + 127) / 128, 128, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_exp2_check(const float* x, float* y_poly, float* y_ref, int n, cudaStream_t stream) {
+  if (n < 2) return cudaSuccess;
+  exp2_check_kernel<<<(n / 2 + 255) / 256, 256, 0, stream>>>(x, y_poly, y_ref, n & ~1);
   return cudaGetLastError();
 }
 

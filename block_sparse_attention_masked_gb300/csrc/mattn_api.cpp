@@ -494,6 +494,14 @@ int mattn_internal_fwd_wait_selftest(const void* q, const void* k, const void* v
   return fwd_locked(q, k, v, o, lse, B, H, N, d, dtype, desc, static_cast<cudaStream_t>(stream), 1);
 }
 
+// Test hook (not in the public header): evaluates the softmax's polynomial
+// exp2 and CUDA's exp2f on n device floats, for an accuracy test.
+int mattn_internal_exp2_check(const float* x, float* y_poly, float* y_ref, int n, void* stream) {
+  if (!x || !y_poly || !y_ref || n < 0) return fail(MATTN_ERR_INVALID_ARG, "bad arguments");
+  MATTN_CUDA(launch_exp2_check(x, y_poly, y_ref, n, static_cast<cudaStream_t>(stream)), "exp2 check launch");
+  return MATTN_OK;
+}
+
 int mattn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
                    int dtype, const mattn_mask_desc* desc, void* stream_) {
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
