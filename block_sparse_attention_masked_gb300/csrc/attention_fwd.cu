@@ -41,10 +41,17 @@ constexpr int kThreads = 384;
 constexpr int kNoTile = 0x7fffffff;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-// A new row maximum replaces the running one only when it exceeds it by more
-// than 2^8 (log2 domain); below that the stale maximum is kept, which is
-// exact because O and l share it, and P stays <= 256 (fine in bf16 / fp32).
-constexpr float kRescaleThreshold = 8.0f;
+// The running row maximum m only guards against overflow: numerator and
+// denominator share it, so any m gives the same result.  A tile is
+// exponentiated against the stale m as long as its row sum of P stays below
+// 2^40 (no overflow in fp32 or bf16, nor in O's fp32 accumulation); a tile
+// above it is redone against the tile's true maximum.
+constexpr float kMaxTileSum = 1099511627776.0f;  // 2^40
+// Registers per thread after setmaxnreg: producer / MMA-issuer warpgroup and the
+// two softmax warpgroups (their sum times 128 equals the launch budget).
+constexpr uint32_t kRegsControl = 72;
+constexpr uint32_t kRegsSoftmax = 216;
+static_assert(kRegsControl + 2 * kRegsSoftmax == 3 * 168, "register split must match the launch budget");
 
 template <int D>
 struct Geo {
@@ -80,6 +87,7 @@ struct Barriers {
   uint64_t drain[2];    // MMA drain on abort, one per issuer
   uint32_t tmem_base;
   int abort_flag;
+  int mma_lock;         // held by one MMA issuer while it pushes one group
 };
 
 // Block-selection rows of up to this many 64-bit words (N <= 2^21 at
@@ -163,6 +171,24 @@ __device__ __forceinline__ ItemPlan make_plan(const FwdParams& p, int2 it, const
   return ip;
 }
 
+// Issuers' lock (a shared-memory word): held only while one issuer pushes one
+// MMA group, which waits on nothing but the tensor queue, so it is always
+// released; the bounded spin gives up on abort or timeout like any wait.
+__device__ __forceinline__ bool mma_lock_acquire(Barriers* bar, uint64_t timeout_ns, volatile int* abort_flag) {
+  if (atomicCAS(&bar->mma_lock, 0, 1) == 0) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t it = 1; it < 0x80000000u; ++it) {
+    if (atomicCAS(&bar->mma_lock, 0, 1) == 0) return true;
+    if ((it & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (ptx::globaltimer_ns() - t0 > timeout_ns) return false;
+    }
+  }
+  return false;
+}
+
+__device__ __forceinline__ void mma_lock_release(Barriers* bar) { atomicExch(&bar->mma_lock, 0); }
+
 __device__ __forceinline__ void raise_error(const FwdParams& p, Barriers* bar, uint32_t bit) {
   *reinterpret_cast<volatile int*>(&bar->abort_flag) = 1;
   atomicOr(p.err, bit);
@@ -227,14 +253,14 @@ __device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint32_t q_addr4, uint
 #pragma unroll
     for (int k = 0; k < 4; ++k, ++step) {
       const uint32_t off4 = ((c * G::kChunkBytes + k * 32) >> 4) + lbo;
-      ptx::mma_ss(s_tmem, desc_of(q_addr4 + off4, hi128), desc_of(k_addr4 + off4, hi128), idesc, step > 0);
+      ptx::mma_ss_elect(s_tmem, desc_of(q_addr4 + off4, hi128), desc_of(k_addr4 + off4, hi128), idesc, step > 0);
     }
   }
   if (G::kRem) {
 #pragma unroll
     for (int k = 0; k < G::kRem / 16; ++k, ++step) {
       const uint32_t off4 = ((G::kChunks * G::kChunkBytes + k * 32) >> 4) + lbo;
-      ptx::mma_ss(s_tmem, desc_of(q_addr4 + off4, hiR), desc_of(k_addr4 + off4, hiR), idesc, step > 0);
+      ptx::mma_ss_elect(s_tmem, desc_of(q_addr4 + off4, hiR), desc_of(k_addr4 + off4, hiR), idesc, step > 0);
     }
   }
 }
@@ -255,44 +281,80 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
   for (int k = 0; k < kTile / 16; ++k) {
     const uint32_t acc = (accumulate || k > 0) ? 1u : 0u;
     const uint32_t a = p_tmem + k * 8;  // 16 bf16 keys = 8 columns
-    ptx::mma_ts(o_tmem, a, desc_of(v_addr4 + ((k * 16 * row_bytes) >> 4) + lbo, hi), idesc, acc);
+    ptx::mma_ts_elect(o_tmem, a, desc_of(v_addr4 + ((k * 16 * row_bytes) >> 4) + lbo, hi), idesc, acc);
   }
 }
 
-// Of every 16 column pairs of a FULL tile, this many take their exponential
-// from the FMA-pipe polynomial instead of MUFU ex2.  Measured on GB300 the
-// MUFU is not the limiter of this softmax (it retires a warp's ex2 in ~4
-// cycles) and every emulated share tried (3..9 of 16) was slower, so the
-// default is 0; the polynomial stays available and tested.
-#ifndef MATTN_EXP_EMU_PAIRS
-#define MATTN_EXP_EMU_PAIRS 0
-#endif
-constexpr int kExpEmuPairs = MATTN_EXP_EMU_PAIRS;
+// Row sums of one tile's P: `exact` adds the fp32 values (for the LSE and
+// the sink's share), `stored` adds the values as stored in bf16 (for the
+// normalisation of O, so that numerator and denominator use the very same
+// weights).
+struct TileSums {
+  float exact, stored;
+};
 
-// P = exp2(x * sl2 - mref) for the 128 scores of this thread's row, packed
-// to bf16 pairs and stored to tensor memory at p_tmem (64 columns); returns
-// the fp32 row sum as two partial lanes.  The last EMU pairs of every
-// 16-pair chunk use the polynomial exp2.
-template <int EMU>
-__device__ __forceinline__ float2 exp_to_tmem(const float (&x)[128], float sl2, float mref, uint32_t p_tmem) {
+// P = exp2(x * sl2 - mref) for the 128 scores of this thread's row, stored
+// to tensor memory at p_tmem as bf16 pairs (64 columns).  bf16 is taken by
+// truncating the fp32 value (a byte permute on the integer pipe; the
+// round-to-nearest conversion instruction shares the pipe of the ex2's and
+// measured ~35% slower here); normalising O by the sum of the truncated
+// values keeps the weights exactly consistent.  All exponentials use MUFU
+// ex2 (moving a share to the FMA-pipe polynomial ptx::exp2_poly2 measured
+// slower at every share tried).
+__device__ __forceinline__ TileSums exp_to_tmem(const float (&x)[128], float sl2, float mref, uint32_t p_tmem) {
   const float2 sl2v = make_float2(sl2, sl2);
   const float2 negm = make_float2(-mref, -mref);
-  float2 acc[4];
+  float2 acc[2], acct[2];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
+  for (int i = 0; i < 2; ++i) {
+    acc[i] = make_float2(0.f, 0.f);
+    acct[i] = make_float2(0.f, 0.f);
+  }
 #pragma unroll
   for (int c0 = 0; c0 < 128; c0 += 32) {
     uint32_t pk[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const float2 t = ptx::ffma2(make_float2(x[c0 + 2 * i], x[c0 + 2 * i + 1]), sl2v, negm);
-      const float2 pp = (i >= 16 - EMU) ? ptx::exp2_poly2(t) : make_float2(ptx::ex2(t.x), ptx::ex2(t.y));
-      acc[i & 3] = ptx::fadd2(acc[i & 3], pp);
-      pk[i] = ptx::pack_bf16x2(pp.x, pp.y);
+      const float2 pp = make_float2(ptx::ex2(t.x), ptx::ex2(t.y));
+      const uint32_t w = __byte_perm(__float_as_uint(pp.x), __float_as_uint(pp.y), 0x7632);  // hi16(y):hi16(x)
+      pk[i] = w;
+      acc[i & 1] = ptx::fadd2(acc[i & 1], pp);
+      acct[i & 1] = ptx::fadd2(acct[i & 1], make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)));
     }
     ptx::tmem_st16(p_tmem + c0 / 2, pk);
   }
-  return ptx::fadd2(ptx::fadd2(acc[0], acc[1]), ptx::fadd2(acc[2], acc[3]));
+  const float2 a = ptx::fadd2(acc[0], acc[1]);
+  const float2 b = ptx::fadd2(acct[0], acct[1]);
+  return TileSums{a.x + a.y, b.x + b.y};
+}
+
+// Maximum of the 128 raw scores of this thread's row (8 independent chains;
+// measured faster here than three-input maxima).
+__device__ __forceinline__ float row_max(const float (&x)[128]) {
+  float a[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a[i] = x[i];
+#pragma unroll
+  for (int c = 8; c < 128; c += 8)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = fmaxf(a[i], x[c + i]);
+  return fmaxf(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])), fmaxf(fmaxf(a[4], a[5]), fmaxf(a[6], a[7])));
+}
+
+// O row *= alpha in tensor memory (warp-collective; alpha is per lane).
+template <int D>
+__device__ __forceinline__ void rescale_o(uint32_t o_tmem, float alpha) {
+#pragma unroll
+  for (int c0 = 0; c0 < D; c0 += 16) {
+    float ov[16];
+    ptx::tmem_ld16(o_tmem + c0, ov);
+    ptx::tmem_wait_ld();
+    uint32_t ou[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) ou[i] = __float_as_uint(ov[i] * alpha);
+    ptx::tmem_st16(o_tmem + c0, ou);
+  }
 }
 
 __device__ __forceinline__ int64_t token_of(const FwdParams& p, int store_mode, int perm_row, int64_t pos) {
@@ -350,6 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
     ptx::mbar_init(&bar->drain[0], 1);
     ptx::mbar_init(&bar->drain[1], 1);
     bar->abort_flag = 0;
+    bar->mma_lock = 0;
     ptx::fence_barrier_init();
   }
   if (warp == 1) {
@@ -366,12 +429,12 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
   const bool colmaj = load_mode == kLoadColumnMajor;
 
   // Registers: 384 threads launched at 168 each; the producer / MMA
-  // warpgroup gives up to 72 so that each softmax warpgroup can hold a full
-  // 128-column score row (216 per thread, 72 + 2 * 216 = 3 * 168).  Each
+  // warpgroup gives up to kRegsControl so that each softmax warpgroup can hold
+  // a full 128-column score row (kRegsControl + 2 * kRegsSoftmax = 3 * 168).  Each
   // role branch starts with its own budget change.
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    ptx::setmaxnreg_dec<72>();
+    ptx::setmaxnreg_dec<kRegsControl>();
     if (lane == 0) {
       const CUtensorMap* mq = colmaj ? p.cq : p.tq;
       ptx::prefetch_tmap(&mq[0]);
@@ -407,104 +470,123 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
   } else if (warp == 1 || warp == 2) {
     // ------------------------------------------------------------ MMA issuers
     // Warp 1 issues the MMAs of query sub-tile 0, warp 2 those of sub-tile 1,
-    // so that neither waits behind the other's softmax: the tensor core
-    // interleaves two independent instruction streams.  Both walk the same
+    // so that neither waits behind the other's softmax.  Both walk the same
     // key-tile list in order; every K / V ring slot is released by one
     // commit from each issuer per entry (the empty barriers count 2).  An
     // issuer that skips an entry still waits for the slot to be filled before
     // releasing it, which keeps the two issuers' arrivals in phase order.
-    ptx::setmaxnreg_dec<72>();
+    // The whole warp runs the loop (warp-uniform control flow and operand
+    // arithmetic, which the compiler keeps in uniform registers); one elected
+    // lane issues each tcgen05 instruction.
+    ptx::setmaxnreg_dec<kRegsControl>();
     const int s = warp - 1;
     const SubPlan sp = s ? ip.sp1 : ip.sp0;
-    if (lane == 0) {
-      bool ok = true;
-      if (p.self_test_timeout && s == 0) {
-        // nothing ever arrives on this barrier: exercises the bounded-wait path
-        if (!ptx::mbar_wait(&bar->never, 0, p.timeout_ns, abort_flag)) {
-          raise_error(p, bar, kErrSelfTest);
-          ok = false;
-        }
-      }
-      if (ok && sp.has_tiles && !ptx::mbar_wait(&bar->q_full[s], 0, p.timeout_ns, abort_flag)) {
-        raise_error(p, bar, kErrMma);
+    auto wait_all = [&](uint64_t* b, uint32_t parity) {
+      return __all_sync(0xffffffffu, ptx::mbar_wait(b, parity, p.timeout_ns, abort_flag));
+    };
+    auto fail = [&]() {
+      if (lane == 0) raise_error(p, bar, kErrMma);
+    };
+    bool ok = true;
+    if (p.self_test_timeout && s == 0) {
+      // nothing ever arrives on this barrier: exercises the bounded-wait path
+      if (!wait_all(&bar->never, 0)) {
+        if (lane == 0) raise_error(p, bar, kErrSelfTest);
         ok = false;
       }
-      ptx::tc_fence_after();
-      constexpr uint32_t tile4 = G::kTileBytes >> 4;  // descriptor start-address units
-      const uint32_t q4 = (ptx::smem_addr(sq) >> 4) + s * tile4;
-      const uint32_t k4 = ptx::smem_addr(sk) >> 4;
-      const uint32_t v4 = ptx::smem_addr(sv) >> 4;
-      const uint32_t s_tm = tmem + s * 128;
-      const uint32_t o_tm = tmem + 256 + s * 128;
-      bool pend = false, first = true, issued_any = false;
-      uint32_t pcount = 0;
-      int j = 0;
-      if (ok) {
-        for (int kt = union_next(p, ip, 0); kt != kNoTile; kt = union_next(p, ip, kt + 1), ++j) {
-          const int ks = j % KS;
-          if (j >= 1) {
-            // finish the previous entry: its P V (when this sub-tile used it), then release V
-            const int e = j - 1;
-            if (!ptx::mbar_wait(&bar->v_full[e % VS], (e / VS) & 1, p.timeout_ns, abort_flag)) {
-              raise_error(p, bar, kErrMma); ok = false; break;
-            }
-            if (pend) {
-              if (!ptx::mbar_wait(&bar->p_full[s], pcount & 1, p.timeout_ns, abort_flag)) {
-                raise_error(p, bar, kErrMma); ok = false; break;
-              }
-              ++pcount;
-              ptx::tc_fence_after();
-              issue_pv<D>(o_tm, s_tm, v4 + (e % VS) * tile4, !first);
-              first = false;
-              pend = false;
-            }
-            ptx::mma_commit(&bar->v_empty[e % VS]);
-          }
-          if (!ptx::mbar_wait(&bar->k_full[ks], (j / KS) & 1, p.timeout_ns, abort_flag)) {
-            raise_error(p, bar, kErrMma); ok = false; break;
-          }
-          ptx::tc_fence_after();
-          if (sub_uses(p, sp, kt)) {
-            issue_qk<D>(s_tm, q4, k4 + ks * tile4);
-            ptx::mma_commit(&bar->s_full[s]);
-            pend = true;
-            issued_any = true;
-          }
-          ptx::mma_commit(&bar->k_empty[ks]);
-        }
-      }
-      if (ok && j >= 1) {
+    }
+    if (ok && sp.has_tiles && !wait_all(&bar->q_full[s], 0)) {
+      fail();
+      ok = false;
+    }
+    ptx::tc_fence_after();
+    constexpr uint32_t tile4 = G::kTileBytes >> 4;  // descriptor start-address units
+    const uint32_t q4 = (ptx::smem_addr(sq) >> 4) + s * tile4;
+    const uint32_t k4 = ptx::smem_addr(sk) >> 4;
+    const uint32_t v4 = ptx::smem_addr(sv) >> 4;
+    const uint32_t s_tm = tmem + s * 128;
+    const uint32_t o_tm = tmem + 256 + s * 128;
+    bool pend = false, first = true, issued_any = false;
+    uint32_t pcount = 0;
+    int j = 0;
+    if (ok) {
+      for (int kt = union_next(p, ip, 0); kt != kNoTile; kt = union_next(p, ip, kt + 1), ++j) {
+        const int ks = j % KS;
         const int e = j - 1;
-        if (!ptx::mbar_wait(&bar->v_full[e % VS], (e / VS) & 1, p.timeout_ns, abort_flag)) {
-          raise_error(p, bar, kErrMma); ok = false;
+        // every input of this step first: V of the previous entry, this
+        // sub-tile's P of the previous entry, K of this entry (K arrives
+        // through the async proxy the MMA reads, so no tcgen05 fence)
+        if (j >= 1 && !wait_all(&bar->v_full[e % VS], (e / VS) & 1)) {
+          fail(); ok = false; break;
         }
-        if (ok && pend) {
-          if (!ptx::mbar_wait(&bar->p_full[s], pcount & 1, p.timeout_ns, abort_flag)) {
-            raise_error(p, bar, kErrMma); ok = false;
-          } else {
-            ++pcount;
-            ptx::tc_fence_after();
-            issue_pv<D>(o_tm, s_tm, v4 + (e % VS) * tile4, !first);
-            first = false;
-            pend = false;
+        if (pend) {
+          if (!wait_all(&bar->p_full[s], pcount & 1)) {
+            fail(); ok = false; break;
           }
+          ++pcount;
+          ptx::tc_fence_after();
         }
-        if (ok) {
-          ptx::mma_commit(&bar->v_empty[e % VS]);
-          if (sp.has_tiles) ptx::mma_commit(&bar->o_final[s]);
+        if (!wait_all(&bar->k_full[ks], (j / KS) & 1)) {
+          fail(); ok = false; break;
         }
-      }
-      if (!ok && issued_any) {
-        // wait (bounded) for the MMAs already issued before tensor memory is freed
-        ptx::mma_commit(&bar->drain[s]);
-        ptx::mbar_wait_time_only(&bar->drain[s], 0, p.timeout_ns);
+        const bool use = sub_uses(p, sp, kt);
+        // then the group P V(e) + S(j), issued under the issuers' lock so the
+        // two sub-tiles' groups run back to back instead of interleaving
+        // (interleaved groups finish together and the two softmaxes then run
+        // in lockstep while the tensor core idles)
+        bool locked = true;
+        if (lane == 0) locked = mma_lock_acquire(bar, p.timeout_ns, abort_flag);
+        if (!__shfl_sync(0xffffffffu, locked, 0)) {
+          fail(); ok = false; break;
+        }
+        if (pend) {
+          issue_pv<D>(o_tm, s_tm, v4 + (e % VS) * tile4, !first);
+          first = false;
+          pend = false;
+        }
+        if (j >= 1) ptx::mma_commit_elect(&bar->v_empty[e % VS]);
+        if (use) {
+          issue_qk<D>(s_tm, q4, k4 + ks * tile4);
+          ptx::mma_commit_elect(&bar->s_full[s]);
+          pend = true;
+          issued_any = true;
+        }
+        ptx::mma_commit_elect(&bar->k_empty[ks]);
+        __syncwarp();
+        if (lane == 0) mma_lock_release(bar);
       }
     }
+    if (ok && j >= 1) {
+      const int e = j - 1;
+      if (!wait_all(&bar->v_full[e % VS], (e / VS) & 1)) {
+        fail(); ok = false;
+      }
+      if (ok && pend) {
+        if (!wait_all(&bar->p_full[s], pcount & 1)) {
+          fail(); ok = false;
+        } else {
+          ++pcount;
+          ptx::tc_fence_after();
+          issue_pv<D>(o_tm, s_tm, v4 + (e % VS) * tile4, !first);
+          first = false;
+          pend = false;
+        }
+      }
+      if (ok) {
+        ptx::mma_commit_elect(&bar->v_empty[e % VS]);
+        if (sp.has_tiles) ptx::mma_commit_elect(&bar->o_final[s]);
+      }
+    }
+    if (!ok && issued_any) {
+      // wait (bounded) for the MMAs already issued before tensor memory is freed
+      ptx::mma_commit_elect(&bar->drain[s]);
+      ptx::mbar_wait_time_only(&bar->drain[s], 0, p.timeout_ns);
+    }
   } else if (warp < 4) {
-    ptx::setmaxnreg_dec<72>();  // idle warp of the first warpgroup
+    ptx::setmaxnreg_dec<kRegsControl>();  // idle warp of the first warpgroup
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    ptx::setmaxnreg_inc<216>();
+    ptx::setmaxnreg_inc<kRegsSoftmax>();
     const int s = (warp - 4) >> 2;
     const int quarter = warp & 3;  // tensor-memory lane quarter this warp may access
     const int row = quarter * 32 + lane;
@@ -520,8 +602,9 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
     if (hi > p.N - 1) hi = p.N - 1;
     const float sl2 = p.scale_log2;
 
-    float m = -INFINITY;  // running max of scaled scores, log2 domain
-    float l = 0.f;        // running sum of exp2(x - m)
+    float m = -INFINITY;  // running (stale) max of scaled scores, log2 domain
+    float l = 0.f;        // running sum of exp2(x - m) in fp32 (LSE, sink share)
+    float lt = 0.f;       // the same over the bf16 values P V accumulated (O's normaliser)
     int count = 0;
     bool ok = true;
     for (int kt = sub_next(p, sp, 0); kt != kNoTile; kt = sub_next(p, sp, kt + 1), ++count) {
@@ -548,49 +631,38 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
         for (int c = 0; c < 128; ++c)
           if (c < c_lo || c > c_hi) x[c] = -INFINITY;
       }
-      // row max over 8 independent chains (short dependency paths; measured
-      // faster here than three-input maxima)
-      float mx;
-      {
-        float a[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) a[i] = x[i];
-#pragma unroll
-        for (int c = 8; c < 128; c += 8)
-#pragma unroll
-          for (int i = 0; i < 8; ++i) a[i] = fmaxf(a[i], x[c + i]);
-        mx = fmaxf(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])), fmaxf(fmaxf(a[4], a[5]), fmaxf(a[6], a[7])));
+      // P = exp2(s * scale * log2e - m) into tensor memory.  tcgen05.ld / st
+      // are warp-collective, so every branch below is taken by whole warps
+      // (each lane applying its own factors).
+      TileSums ts;
+      bool slow = __any_sync(0xffffffffu, m == -INFINITY);
+      if (!slow) {
+        // Running maximum known: exponentiate against it directly.  It only
+        // guards against overflow (the final normalisation uses the same m
+        // for numerator and denominator), so it is kept while every P stays
+        // below 2^40; a tile that breaks this (rare) is redone below.
+        ts = exp_to_tmem(x, sl2, m, s_tmem);
+        slow = __any_sync(0xffffffffu, !(ts.exact <= kMaxTileSum));
+        if (slow) ptx::tmem_wait_st();  // let these stores land before they are overwritten
       }
-      mx *= sl2;
-      const float m_new = fmaxf(m, mx);
-      const bool need_rescale = (m != -INFINITY) && (m_new - m > kRescaleThreshold);
-      if (m == -INFINITY) m = m_new;  // nothing accumulated yet (all earlier P were zero)
-      // tcgen05.ld / st are warp-collective: the whole warp rescales when any
-      // of its rows must, each lane with its own factor (1 when not needed)
-      if (__any_sync(0xffffffffu, need_rescale)) {
-        const float alpha = need_rescale ? ptx::ex2(m - m_new) : 1.f;
-#pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 16) {
-          float ov[16];
-          ptx::tmem_ld16(o_tmem + c0, ov);
-          ptx::tmem_wait_ld();
-          uint32_t ou[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) ou[i] = __float_as_uint(ov[i] * alpha);
-          ptx::tmem_st16(o_tmem + c0, ou);
+      if (slow) {
+        // tile maximum first (also the first tile of a row)
+        const float m_new = fmaxf(m, row_max(x) * sl2);
+        const bool need_rescale = (m != -INFINITY) && (m_new > m);
+        if (m == -INFINITY) m = m_new;  // nothing accumulated yet (all earlier P were zero)
+        if (__any_sync(0xffffffffu, need_rescale)) {
+          const float alpha = need_rescale ? ptx::ex2(m - m_new) : 1.f;
+          rescale_o<D>(o_tmem, alpha);
+          if (need_rescale) {
+            l *= alpha;
+            lt *= alpha;
+            m = m_new;
+          }
         }
-        if (need_rescale) {
-          l *= alpha;
-          m = m_new;
-        }
+        ts = exp_to_tmem(x, sl2, (m == -INFINITY) ? 0.f : m, s_tmem);
       }
-      const float mref = (m == -INFINITY) ? 0.f : m;
-      // P = exp2(s * scale * log2e - m) into tensor memory; on FULL tiles a
-      // share of the exponentials runs on the FMA pipe (every argument is
-      // finite there), on PARTIAL tiles all use MUFU ex2 (exp2(-inf) = 0)
-      const float2 accs = partial ? exp_to_tmem<0>(x, sl2, mref, s_tmem)
-                                  : exp_to_tmem<kExpEmuPairs>(x, sl2, mref, s_tmem);
-      l += accs.x + accs.y;
+      l += ts.exact;
+      lt += ts.stored;
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(&bar->p_full[s]);
@@ -615,10 +687,12 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
         float o_scale = 0.f;
         float lse_v = -INFINITY;
         if (M != -INFINITY) {
+          // O = (sum of bf16 P V / sum of bf16 P) * (share of the mass left by
+          // the sink, from the fp32 sums); LSE from the fp32 normaliser
           const float em = (m == -INFINITY) ? 0.f : ptx::ex2(m - M);
           const float lf = l * em + ((b2 == -INFINITY) ? 0.f : ptx::ex2(b2 - M));
           if (lf > 0.f) {
-            o_scale = em / lf;
+            if (lt > 0.f) o_scale = (em / lf) * (l / lt);
             lse_v = (M + ptx::lg2(lf)) * kLn2;
           }
         }
