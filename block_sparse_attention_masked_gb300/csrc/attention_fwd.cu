@@ -285,31 +285,18 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
   }
 }
 
-// Row sums of one tile's P: `exact` adds the fp32 values (for the LSE and
-// the sink's share), `stored` adds the values as stored in bf16 (for the
-// normalisation of O, so that numerator and denominator use the very same
-// weights).
-struct TileSums {
-  float exact, stored;
-};
-
 // P = exp2(x * sl2 - mref) for the 128 scores of this thread's row, stored
-// to tensor memory at p_tmem as bf16 pairs (64 columns).  bf16 is taken by
-// truncating the fp32 value (a byte permute on the integer pipe; the
-// round-to-nearest conversion instruction shares the pipe of the ex2's and
-// measured ~35% slower here); normalising O by the sum of the truncated
-// values keeps the weights exactly consistent.  All exponentials use MUFU
-// ex2 (moving a share to the FMA-pipe polynomial ptx::exp2_poly2 measured
-// slower at every share tried).
-__device__ __forceinline__ TileSums exp_to_tmem(const float (&x)[128], float sl2, float mref, uint32_t p_tmem) {
+// to tensor memory at p_tmem as bf16 pairs (64 columns, round to nearest);
+// returns the row sum of the fp32 values.  All exponentials use MUFU ex2:
+// moving a share to the FMA-pipe polynomial ptx::exp2_poly2 measured slower
+// at every share tried, as did a truncating pack with a second sum over the
+// truncated values (one more add and two integer ops per pair).
+__device__ __forceinline__ float exp_to_tmem(const float (&x)[128], float sl2, float mref, uint32_t p_tmem) {
   const float2 sl2v = make_float2(sl2, sl2);
   const float2 negm = make_float2(-mref, -mref);
-  float2 acc[2], acct[2];
+  float2 acc[2];
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    acc[i] = make_float2(0.f, 0.f);
-    acct[i] = make_float2(0.f, 0.f);
-  }
+  for (int i = 0; i < 2; ++i) acc[i] = make_float2(0.f, 0.f);
 #pragma unroll
   for (int c0 = 0; c0 < 128; c0 += 32) {
     uint32_t pk[16];
@@ -317,16 +304,13 @@ __device__ __forceinline__ TileSums exp_to_tmem(const float (&x)[128], float sl2
     for (int i = 0; i < 16; ++i) {
       const float2 t = ptx::ffma2(make_float2(x[c0 + 2 * i], x[c0 + 2 * i + 1]), sl2v, negm);
       const float2 pp = make_float2(ptx::ex2(t.x), ptx::ex2(t.y));
-      const uint32_t w = __byte_perm(__float_as_uint(pp.x), __float_as_uint(pp.y), 0x7632);  // hi16(y):hi16(x)
-      pk[i] = w;
+      pk[i] = ptx::pack_bf16x2(pp.x, pp.y);
       acc[i & 1] = ptx::fadd2(acc[i & 1], pp);
-      acct[i & 1] = ptx::fadd2(acct[i & 1], make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)));
     }
     ptx::tmem_st16(p_tmem + c0 / 2, pk);
   }
   const float2 a = ptx::fadd2(acc[0], acc[1]);
-  const float2 b = ptx::fadd2(acct[0], acct[1]);
-  return TileSums{a.x + a.y, b.x + b.y};
+  return a.x + a.y;
 }
 
 // Maximum of the 128 raw scores of this thread's row (8 independent chains;
@@ -603,8 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
     const float sl2 = p.scale_log2;
 
     float m = -INFINITY;  // running (stale) max of scaled scores, log2 domain
-    float l = 0.f;        // running sum of exp2(x - m) in fp32 (LSE, sink share)
-    float lt = 0.f;       // the same over the bf16 values P V accumulated (O's normaliser)
+    float l = 0.f;        // running sum of exp2(x - m) in fp32
     int count = 0;
     bool ok = true;
     for (int kt = sub_next(p, sp, 0); kt != kNoTile; kt = sub_next(p, sp, kt + 1), ++count) {
@@ -634,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
       // P = exp2(s * scale * log2e - m) into tensor memory.  tcgen05.ld / st
       // are warp-collective, so every branch below is taken by whole warps
       // (each lane applying its own factors).
-      TileSums ts;
+      float ts;
       bool slow = __any_sync(0xffffffffu, m == -INFINITY);
       if (!slow) {
         // Running maximum known: exponentiate against it directly.  It only
@@ -642,7 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
         // for numerator and denominator), so it is kept while every P stays
         // below 2^40; a tile that breaks this (rare) is redone below.
         ts = exp_to_tmem(x, sl2, m, s_tmem);
-        slow = __any_sync(0xffffffffu, !(ts.exact <= kMaxTileSum));
+        slow = __any_sync(0xffffffffu, !(ts <= kMaxTileSum));
         if (slow) ptx::tmem_wait_st();  // let these stores land before they are overwritten
       }
       if (slow) {
@@ -655,14 +638,12 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
           rescale_o<D>(o_tmem, alpha);
           if (need_rescale) {
             l *= alpha;
-            lt *= alpha;
             m = m_new;
           }
         }
         ts = exp_to_tmem(x, sl2, (m == -INFINITY) ? 0.f : m, s_tmem);
       }
-      l += ts.exact;
-      lt += ts.stored;
+      l += ts;
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(&bar->p_full[s]);
@@ -687,12 +668,12 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
         float o_scale = 0.f;
         float lse_v = -INFINITY;
         if (M != -INFINITY) {
-          // O = (sum of bf16 P V / sum of bf16 P) * (share of the mass left by
-          // the sink, from the fp32 sums); LSE from the fp32 normaliser
+          // O = sum of P V / (l + exp(sink)) with both terms taken against
+          // the common maximum M; the LSE from the same normaliser
           const float em = (m == -INFINITY) ? 0.f : ptx::ex2(m - M);
           const float lf = l * em + ((b2 == -INFINITY) ? 0.f : ptx::ex2(b2 - M));
           if (lf > 0.f) {
-            if (lt > 0.f) o_scale = (em / lf) * (l / lt);
+            o_scale = em / lf;
             lse_v = (M + ptx::lg2(lf)) * kLn2;
           }
         }
