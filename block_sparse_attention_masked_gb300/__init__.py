@@ -41,6 +41,8 @@ ORDER_RASTER = -1
 ORDER_COLUMN_MAJOR = -2
 TILE = 128
 TILE_FULL, TILE_PARTIAL = 1, 2
+FLAG_SCHEDULE_PAIRED, FLAG_SCHEDULE_SPLIT = 1, 2
+SCHEDULE = {None: 0, "auto": 0, "paired": FLAG_SCHEDULE_PAIRED, "split": FLAG_SCHEDULE_SPLIT}
 
 
 class MattnError(RuntimeError):
@@ -132,7 +134,7 @@ class PreparedMask:
     """A mask descriptor plus the buffers it points at (kept alive here)."""
 
     def __init__(self, spec, H: int, N: int, device="cuda", scale: Optional[float] = None,
-                 host_side: bool = False):
+                 host_side: bool = False, schedule: Optional[str] = None):
         import torch
 
         self.H, self.N = H, N
@@ -188,7 +190,9 @@ class PreparedMask:
             self._keep.append(t)
             d.sink = t.data_ptr()
         d.softmax_scale = 0.0 if scale is None else float(scale)
-        d.flags = 0
+        if schedule not in SCHEDULE:
+            raise ValueError(f"schedule must be one of {sorted(k for k in SCHEDULE if k)} or None")
+        d.flags = SCHEDULE[schedule]
         self.desc = d
 
     def host_desc(self):
@@ -200,8 +204,11 @@ class PreparedMask:
         return d
 
 
-def prepare(spec, H: int, N: int, device="cuda", scale: Optional[float] = None) -> PreparedMask:
-    return PreparedMask(spec, H, N, device=device, scale=scale)
+def prepare(spec, H: int, N: int, device="cuda", scale: Optional[float] = None,
+            schedule: Optional[str] = None) -> PreparedMask:
+    """schedule: None / "auto" (library's choice), "paired" or "split" (the
+    MATTN_FLAG_SCHEDULE_* flags); the result is the same up to rounding."""
+    return PreparedMask(spec, H, N, device=device, scale=scale, schedule=schedule)
 
 
 def _dtype_code(t) -> int:

@@ -1,9 +1,15 @@
 // Masked attention forward for sm_103a: TMA-staged tiles, tcgen05 MMAs with
 // tensor-memory accumulators, warp-specialised online softmax.
 //
-// What one CTA computes: query rows [256*pair, 256*pair + 256) of one
-// (batch, head), as two 128-row query sub-tiles s = 0, 1 that share the
-// staged K/V tiles.  For every key tile kt the mask touches (plan_rules.h),
+// What one CTA computes, in one of two schedules:
+//   paired: query rows [256*pair, 256*pair + 256) of one (batch, head), as
+//     two 128-row query sub-tiles s = 0, 1 that share the staged K/V tiles
+//     (for masks whose neighbouring query tiles see mostly the same keys);
+//   split: query rows [128*qt, 128*qt + 128), its key tiles dealt out
+//     alternately to two sub-tile pipelines s = 0, 1 that keep separate
+//     running (m, l, O) and are merged at the end (for masks whose
+//     neighbouring query tiles share few key tiles, e.g. 128-blocks).
+// For every key tile kt a sub-tile takes (plan_rules.h),
 //     S_s  = Q_s K_kt^T                        (tcgen05.mma, smem x smem -> TMEM)
 //     P_s  = exp2(S_s * scale*log2e - m_s)     (softmax warps, online max m_s)
 //     O_s += P_s V_kt                          (tcgen05.mma, P from TMEM, V from smem)
@@ -13,9 +19,10 @@
 // transformers lesson -- tile, fuse the softmax, never materialise N x N).
 //
 // Roles (384 threads):
-//   warp 0        TMA producer: Q_0, Q_1 once, then K/V tiles into rings
+//   warp 0        TMA producer: Q once, then K tiles into their ring
 //   warp 1        tensor-memory allocator; MMA issuer of sub-tile 0
 //   warp 2        MMA issuer of sub-tile 1
+//   warp 3        TMA producer of the V ring
 //   warps 4..7    softmax + epilogue of sub-tile 0 (one query row per thread)
 //   warps 8..11   softmax + epilogue of sub-tile 1
 // Tensor memory (512 columns x 128 lanes, fp32):
@@ -87,7 +94,8 @@ struct Barriers {
   uint64_t drain[2];    // MMA drain on abort, one per issuer
   uint32_t tmem_base;
   int abort_flag;
-  int mma_lock;         // held by one MMA issuer while it pushes one group
+  uint32_t mma_turn;    // ticket of the MMA group that may be issued next
+  float xch[2][3][kTile];  // split schedule: per sub-tile (m, l, tile count) of each row
 };
 
 // Block-selection rows of up to this many 64-bit words (N <= 2^21 at
@@ -128,17 +136,23 @@ __device__ __forceinline__ bool sub_partial(const FwdParams& p, const SubPlan& s
   return interval_tile_class(sp.r, kt) == kTilePartial;
 }
 
+// Next key tile of the CTA's list: the union of both sub-tiles' tiles when
+// paired, the one query tile's tiles when split.
 __device__ __forceinline__ int union_next(const FwdParams& p, const ItemPlan& ip, int from) {
   int a = sub_next(p, ip.sp0, from);
+  if (p.split) return a;
   int c = sub_next(p, ip.sp1, from);
   return a < c ? a : c;
 }
+
+// Query tile of sub-tile s of work item `it`.
+__device__ __forceinline__ int item_qt(const FwdParams& p, int2 it, int s) { return p.split ? it.y : 2 * it.y + s; }
 
 // Global bitmap row of sub-tile s of work item `it` (block kind).
 __device__ __forceinline__ const uint64_t* global_row(const FwdParams& p, int2 it, int s) {
   const int h = it.x % p.H;
   const int hb = (p.block_heads == 1) ? 0 : h;
-  const int qt = 2 * it.y + s;
+  const int qt = item_qt(p, it, s);
   return p.block_bits + ((int64_t)hb * p.block_nb + qt / p.block_c) * p.block_wpr;
 }
 
@@ -146,7 +160,7 @@ __device__ __forceinline__ SubPlan make_subplan(const FwdParams& p, int2 it, int
                                                 const uint64_t* staged_rows) {
   SubPlan sp;
   const int nt = (p.N + kTile - 1) / kTile;
-  sp.qt = 2 * it.y + s;
+  sp.qt = item_qt(p, it, s);
   sp.rows = sp.qt < nt;
   sp.ktmax = sp.qt < nt ? sp.qt : nt - 1;
   sp.row = nullptr;
@@ -154,7 +168,7 @@ __device__ __forceinline__ SubPlan make_subplan(const FwdParams& p, int2 it, int
     sp.r = interval_krange(p.kind, param, p.N, sp.qt);
   } else {
     sp.r.lo = 0; sp.r.hi = -1; sp.r.flo = 0; sp.r.fhi = -1;
-    if (sp.rows) sp.row = staged_rows ? staged_rows + s * kMaxRowWords : global_row(p, it, s);
+    if (sp.rows) sp.row = staged_rows ? staged_rows + (p.split ? 0 : s) * kMaxRowWords : global_row(p, it, s);
   }
   sp.has_tiles = sub_next(p, sp, 0) != kNoTile;
   return sp;
@@ -171,14 +185,19 @@ __device__ __forceinline__ ItemPlan make_plan(const FwdParams& p, int2 it, const
   return ip;
 }
 
-// Issuers' lock (a shared-memory word): held only while one issuer pushes one
-// MMA group, which waits on nothing but the tensor queue, so it is always
-// released; the bounded spin gives up on abort or timeout like any wait.
-__device__ __forceinline__ bool mma_lock_acquire(Barriers* bar, uint64_t timeout_ns, volatile int* abort_flag) {
-  if (atomicCAS(&bar->mma_lock, 0, 1) == 0) return true;
+// Issue order of the MMA groups (a shared-memory word): the group with
+// ticket t is pushed once mma_turn == t, and its issuer then passes the turn
+// on.  Paired: entry j's group of sub-tile s has ticket 2j + s; split: entry
+// j's group has ticket j.  A plain load / store pair: far cheaper on the
+// critical path than an atomic lock.  The bounded spin gives up on abort or
+// timeout like any wait.
+__device__ __forceinline__ bool mma_turn_wait(Barriers* bar, uint32_t ticket, uint64_t timeout_ns,
+                                              volatile int* abort_flag) {
+  const uint32_t a = ptx::smem_addr(&bar->mma_turn);
+  if (ptx::ld_shared_acquire(a) == ticket) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   for (uint32_t it = 1; it < 0x80000000u; ++it) {
-    if (atomicCAS(&bar->mma_lock, 0, 1) == 0) return true;
+    if (ptx::ld_shared_acquire(a) == ticket) return true;
     if ((it & 63u) == 0) {
       if (*abort_flag) return false;
       if (ptx::globaltimer_ns() - t0 > timeout_ns) return false;
@@ -187,7 +206,9 @@ __device__ __forceinline__ bool mma_lock_acquire(Barriers* bar, uint64_t timeout
   return false;
 }
 
-__device__ __forceinline__ void mma_lock_release(Barriers* bar) { atomicExch(&bar->mma_lock, 0); }
+__device__ __forceinline__ void mma_turn_pass(Barriers* bar, uint32_t ticket) {
+  ptx::st_release_shared(ptx::smem_addr(&bar->mma_turn), ticket + 1u);
+}
 
 __device__ __forceinline__ void raise_error(const FwdParams& p, Barriers* bar, uint32_t bit) {
   *reinterpret_cast<volatile int*>(&bar->abort_flag) = 1;
@@ -341,6 +362,13 @@ __device__ __forceinline__ void rescale_o(uint32_t o_tmem, float alpha) {
   }
 }
 
+// Split schedule: O columns [0, kOHalf) are written by sub-tile 0's threads,
+// [kOHalf, D) by sub-tile 1's (whole 16-column loads).
+template <int D>
+__host__ __device__ constexpr int kOHalf() {
+  return 16 * ((D + 31) / 32);
+}
+
 __device__ __forceinline__ int64_t token_of(const FwdParams& p, int store_mode, int perm_row, int64_t pos) {
   if (store_mode == kStoreColumnMajor) {
     int64_t c = pos / p.grid_rows;
@@ -369,11 +397,11 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
   const int lane = threadIdx.x & 31;
   const int2 item = p.items[blockIdx.x];
   const bool stage_rows = p.kind == kBlockSparse && p.block_wpr <= kMaxRowWords;
-  if (stage_rows && (warp == 2 || warp == 3)) {
-    // the two bitmap rows this CTA walks, copied once to shared memory
+  if (stage_rows && (warp == 2 || (warp == 3 && !p.split))) {
+    // the bitmap rows this CTA walks, copied once to shared memory
     const int s = warp - 2;
     const int nt = (p.N + kTile - 1) / kTile;
-    if (2 * item.y + s < nt) {
+    if (item_qt(p, item, s) < nt) {
       const uint64_t* src = global_row(p, item, s);
       for (int w = lane; w < p.block_wpr; w += 32) staged_rows[s * kMaxRowWords + w] = src[w];
     }
@@ -388,15 +416,17 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
     }
     for (int i = 0; i < 3; ++i) {
       ptx::mbar_init(&bar->k_full[i], 1);
-      ptx::mbar_init(&bar->k_empty[i], 2);  // one commit from each MMA issuer
+      // released by a commit from each MMA issuer (paired) or from the one
+      // issuer the entry is dealt to (split)
+      ptx::mbar_init(&bar->k_empty[i], p.split ? 1 : 2);
       ptx::mbar_init(&bar->v_full[i], 1);
-      ptx::mbar_init(&bar->v_empty[i], 2);
+      ptx::mbar_init(&bar->v_empty[i], p.split ? 1 : 2);
     }
     ptx::mbar_init(&bar->never, 1);
     ptx::mbar_init(&bar->drain[0], 1);
     ptx::mbar_init(&bar->drain[1], 1);
     bar->abort_flag = 0;
-    bar->mma_lock = 0;
+    bar->mma_turn = 0;
     ptx::fence_barrier_init();
   }
   if (warp == 1) {
@@ -416,34 +446,43 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
   // warpgroup gives up to kRegsControl so that each softmax warpgroup can hold
   // a full 128-column score row (kRegsControl + 2 * kRegsSoftmax = 3 * 168).  Each
   // role branch starts with its own budget change.
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp == 0 || warp == 3) {
+    // ------------------------------------------------------------ producers
+    // Warp 0 loads Q and the K ring, warp 3 the V ring, each walking the
+    // CTA's key-tile list in order: a K load never queues behind a V slot
+    // that is still being read (V is released only after P V, K already
+    // after S).
     ptx::setmaxnreg_dec<kRegsControl>();
     if (lane == 0) {
-      const CUtensorMap* mq = colmaj ? p.cq : p.tq;
-      ptx::prefetch_tmap(&mq[0]);
+      const bool is_k = warp == 0;
+      if (is_k) {
+        const CUtensorMap* mq = colmaj ? p.cq : p.tq;
+        ptx::prefetch_tmap(&mq[0]);
 #pragma unroll
-      for (int s = 0; s < 2; ++s) {
-        const SubPlan& sp = s ? ip.sp1 : ip.sp0;
-        if (!sp.has_tiles) continue;
-        ptx::mbar_arrive_expect_tx(&bar->q_full[s], G::kTileBytes);
-        load_tile<D>(p, p.tq, p.cq, colmaj, sq + s * G::kTileBytes, &bar->q_full[s], sp.qt * kTile, ip.bh);
+        for (int s = 0; s < 2; ++s) {
+          const SubPlan& sp = s ? ip.sp1 : ip.sp0;
+          if (!sp.has_tiles || (p.split && s == 1)) continue;  // split: one Q tile for both pipelines
+          ptx::mbar_arrive_expect_tx(&bar->q_full[s], G::kTileBytes);
+          load_tile<D>(p, p.tq, p.cq, colmaj, sq + s * G::kTileBytes, &bar->q_full[s], sp.qt * kTile, ip.bh);
+        }
       }
+      uint64_t* empty = is_k ? bar->k_empty : bar->v_empty;
+      uint64_t* full = is_k ? bar->k_full : bar->v_full;
+      uint8_t* ring = is_k ? sk : sv;
+      constexpr int S = KS;
+      static_assert(KS == VS, "one ring depth for K and V");
       int j = 0;
       for (int kt = union_next(p, ip, 0); kt != kNoTile; kt = union_next(p, ip, kt + 1), ++j) {
-        const int ks = j % KS, vs = j % VS;
-        if (!ptx::mbar_wait(&bar->k_empty[ks], ((j / KS) & 1) ^ 1, p.timeout_ns, abort_flag)) {
+        const int slot = j % S;
+        if (!ptx::mbar_wait(&empty[slot], ((j / S) & 1) ^ 1, p.timeout_ns, abort_flag)) {
           raise_error(p, bar, kErrProducer);
           break;
         }
-        ptx::mbar_arrive_expect_tx(&bar->k_full[ks], G::kTileBytes);
-        load_tile<D>(p, p.tk, p.ck, colmaj, sk + ks * G::kTileBytes, &bar->k_full[ks], kt * kTile, ip.bh);
-        if (!ptx::mbar_wait(&bar->v_empty[vs], ((j / VS) & 1) ^ 1, p.timeout_ns, abort_flag)) {
-          raise_error(p, bar, kErrProducer);
-          break;
-        }
-        ptx::mbar_arrive_expect_tx(&bar->v_full[vs], G::kTileBytes);
-        load_v_tile<D>(p, colmaj, sv + vs * G::kTileBytes, &bar->v_full[vs], kt * kTile, ip.bh);
+        ptx::mbar_arrive_expect_tx(&full[slot], G::kTileBytes);
+        if (is_k)
+          load_tile<D>(p, p.tk, p.ck, colmaj, ring + slot * G::kTileBytes, &full[slot], kt * kTile, ip.bh);
+        else
+          load_v_tile<D>(p, colmaj, ring + slot * G::kTileBytes, &full[slot], kt * kTile, ip.bh);
       }
       if (*abort_flag) {
         // let copies already in flight land before the CTA's shared memory goes away
@@ -453,15 +492,17 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
     }
   } else if (warp == 1 || warp == 2) {
     // ------------------------------------------------------------ MMA issuers
-    // Warp 1 issues the MMAs of query sub-tile 0, warp 2 those of sub-tile 1,
-    // so that neither waits behind the other's softmax.  Both walk the same
-    // key-tile list in order; every K / V ring slot is released by one
-    // commit from each issuer per entry (the empty barriers count 2).  An
-    // issuer that skips an entry still waits for the slot to be filled before
+    // Warp 1 issues the MMAs of sub-tile 0, warp 2 those of sub-tile 1, so
+    // that neither waits behind the other's softmax.  Both walk the CTA's
+    // key-tile list in order.  Paired: every K / V ring slot is released by
+    // one commit from each issuer (the empty barriers count 2); an issuer
+    // that skips an entry still waits for the slot to be filled before
     // releasing it, which keeps the two issuers' arrivals in phase order.
-    // The whole warp runs the loop (warp-uniform control flow and operand
-    // arithmetic, which the compiler keeps in uniform registers); one elected
-    // lane issues each tcgen05 instruction.
+    // Split: entry j belongs to issuer j % 2 alone, which releases it; the
+    // other issuer never touches it.  The whole warp runs the loop
+    // (warp-uniform control flow and operand arithmetic, which the compiler
+    // keeps in uniform registers); one elected lane issues each tcgen05
+    // instruction.
     ptx::setmaxnreg_dec<kRegsControl>();
     const int s = warp - 1;
     const SubPlan sp = s ? ip.sp1 : ip.sp0;
@@ -479,28 +520,38 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
         ok = false;
       }
     }
-    if (ok && sp.has_tiles && !wait_all(&bar->q_full[s], 0)) {
+    const int qs = p.split ? 0 : s;  // Q tile this sub-tile multiplies
+    if (ok && sp.has_tiles && !wait_all(&bar->q_full[qs], 0)) {
       fail();
       ok = false;
     }
     ptx::tc_fence_after();
     constexpr uint32_t tile4 = G::kTileBytes >> 4;  // descriptor start-address units
-    const uint32_t q4 = (ptx::smem_addr(sq) >> 4) + s * tile4;
+    const uint32_t q4 = (ptx::smem_addr(sq) >> 4) + qs * tile4;
     const uint32_t k4 = ptx::smem_addr(sk) >> 4;
     const uint32_t v4 = ptx::smem_addr(sv) >> 4;
     const uint32_t s_tm = tmem + s * 128;
     const uint32_t o_tm = tmem + 256 + s * 128;
     bool pend = false, first = true, issued_any = false;
+    int pe = 0;  // entry whose P V is pending
     uint32_t pcount = 0;
     int j = 0;
     if (ok) {
       for (int kt = union_next(p, ip, 0); kt != kNoTile; kt = union_next(p, ip, kt + 1), ++j) {
+        const bool use = p.split ? ((j & 1) == s) : sub_uses(p, sp, kt);
+        if (p.split && !use) continue;  // the other issuer's entry
         const int ks = j % KS;
-        const int e = j - 1;
-        // every input of this step first: V of the previous entry, this
-        // sub-tile's P of the previous entry, K of this entry (K arrives
-        // through the async proxy the MMA reads, so no tcgen05 fence)
-        if (j >= 1 && !wait_all(&bar->v_full[e % VS], (e / VS) & 1)) {
+        // the V slot read and released at this step: the previous entry
+        // (paired), the pending product's entry (split)
+        const bool rel_v = p.split ? pend : (j >= 1);
+        const int ve = p.split ? pe : j - 1;
+        // every input of this step first: V and K (both arrive through the
+        // async proxy the MMA reads, so no tcgen05 fence), then -- last, as
+        // it is the one that arrives last -- this sub-tile's pending P
+        if (rel_v && !wait_all(&bar->v_full[ve % VS], (ve / VS) & 1)) {
+          fail(); ok = false; break;
+        }
+        if (!wait_all(&bar->k_full[ks], (j / KS) & 1)) {
           fail(); ok = false; break;
         }
         if (pend) {
@@ -510,39 +561,37 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
           ++pcount;
           ptx::tc_fence_after();
         }
-        if (!wait_all(&bar->k_full[ks], (j / KS) & 1)) {
-          fail(); ok = false; break;
-        }
-        const bool use = sub_uses(p, sp, kt);
-        // then the group P V(e) + S(j), issued under the issuers' lock so the
-        // two sub-tiles' groups run back to back instead of interleaving
+        // then the group P V(pe) + S(j), in ticket order so that the two
+        // sub-tiles' groups run back to back instead of interleaving
         // (interleaved groups finish together and the two softmaxes then run
         // in lockstep while the tensor core idles)
-        bool locked = true;
-        if (lane == 0) locked = mma_lock_acquire(bar, p.timeout_ns, abort_flag);
-        if (!__shfl_sync(0xffffffffu, locked, 0)) {
+        const uint32_t ticket = p.split ? (uint32_t)j : (uint32_t)(2 * j + s);
+        if (!__all_sync(0xffffffffu, mma_turn_wait(bar, ticket, p.timeout_ns, abort_flag))) {
           fail(); ok = false; break;
         }
         if (pend) {
-          issue_pv<D>(o_tm, s_tm, v4 + (e % VS) * tile4, !first);
+          issue_pv<D>(o_tm, s_tm, v4 + (ve % VS) * tile4, !first);
           first = false;
           pend = false;
         }
-        if (j >= 1) ptx::mma_commit_elect(&bar->v_empty[e % VS]);
+        if (use) issue_qk<D>(s_tm, q4, k4 + ks * tile4);
+        __syncwarp();
+        if (lane == 0) mma_turn_pass(bar, ticket);
+        // commits after the turn has passed: each tracks this thread's own
+        // MMAs only, so the other issuer need not wait for them
         if (use) {
-          issue_qk<D>(s_tm, q4, k4 + ks * tile4);
           ptx::mma_commit_elect(&bar->s_full[s]);
           pend = true;
+          pe = j;
           issued_any = true;
         }
+        if (rel_v) ptx::mma_commit_elect(&bar->v_empty[ve % VS]);
         ptx::mma_commit_elect(&bar->k_empty[ks]);
-        __syncwarp();
-        if (lane == 0) mma_lock_release(bar);
       }
     }
-    if (ok && j >= 1) {
-      const int e = j - 1;
-      if (!wait_all(&bar->v_full[e % VS], (e / VS) & 1)) {
+    if (ok && (p.split ? pend : j >= 1)) {
+      const int ve = p.split ? pe : j - 1;
+      if (!wait_all(&bar->v_full[ve % VS], (ve / VS) & 1)) {
         fail(); ok = false;
       }
       if (ok && pend) {
@@ -551,23 +600,19 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
         } else {
           ++pcount;
           ptx::tc_fence_after();
-          issue_pv<D>(o_tm, s_tm, v4 + (e % VS) * tile4, !first);
+          issue_pv<D>(o_tm, s_tm, v4 + (ve % VS) * tile4, !first);
           first = false;
           pend = false;
         }
       }
-      if (ok) {
-        ptx::mma_commit_elect(&bar->v_empty[e % VS]);
-        if (sp.has_tiles) ptx::mma_commit_elect(&bar->o_final[s]);
-      }
+      if (ok) ptx::mma_commit_elect(&bar->v_empty[ve % VS]);
     }
+    if (ok && issued_any) ptx::mma_commit_elect(&bar->o_final[s]);
     if (!ok && issued_any) {
       // wait (bounded) for the MMAs already issued before tensor memory is freed
       ptx::mma_commit_elect(&bar->drain[s]);
       ptx::mbar_wait_time_only(&bar->drain[s], 0, p.timeout_ns);
     }
-  } else if (warp < 4) {
-    ptx::setmaxnreg_dec<kRegsControl>();  // idle warp of the first warpgroup
   } else {
     // ------------------------------------------------------------ softmax + epilogue
     ptx::setmaxnreg_inc<kRegsSoftmax>();
@@ -588,9 +633,11 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
 
     float m = -INFINITY;  // running (stale) max of scaled scores, log2 domain
     float l = 0.f;        // running sum of exp2(x - m) in fp32
-    int count = 0;
+    int count = 0;  // key tiles this sub-tile has processed
     bool ok = true;
-    for (int kt = sub_next(p, sp, 0); kt != kNoTile; kt = sub_next(p, sp, kt + 1), ++count) {
+    int jj = 0;     // entry of the CTA's list
+    for (int kt = sub_next(p, sp, 0); kt != kNoTile; kt = sub_next(p, sp, kt + 1), ++jj) {
+      if (p.split && (jj & 1) != s) continue;  // dealt to the other pipeline
       bool got = ptx::mbar_wait(&bar->s_full[s], count & 1, p.timeout_ns, abort_flag);
       if (!__all_sync(0xffffffffu, got)) {
         if (lane == 0) raise_error(p, bar, kErrSoftmax);
@@ -647,33 +694,60 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(&bar->p_full[s]);
+      ++count;
     }
 
     // ---------------------------------------------------------- epilogue
+    // Paired: each sub-tile writes its own rows.  Split: both sub-tiles hold
+    // partial (m, l, O) of the same rows; they exchange (m, l, count) and
+    // each writes half of the O columns, O = (O_0 e_0 + O_1 e_1) / (l_0 e_0 +
+    // l_1 e_1 + exp(sink)) with e_s = exp2(m_s - M) against the common
+    // maximum M (the merge of two online-softmax states).
+    float m_o = -INFINITY, l_o = 0.f;
+    int count_o = 0;
+    if (p.split) {
+      bar->xch[s][0][row] = m;
+      bar->xch[s][1][row] = l;
+      bar->xch[s][2][row] = (float)count;
+      asm volatile("bar.sync 1, 256;" ::: "memory");  // the eight softmax warps
+      m_o = bar->xch[s ^ 1][0][row];
+      l_o = bar->xch[s ^ 1][1][row];
+      count_o = (int)bar->xch[s ^ 1][2][row];
+    }
     if (ok && sp.rows) {
-      bool have_o = false;
-      if (count > 0) {
-        bool got = ptx::mbar_wait(&bar->o_final[s], 0, p.timeout_ns, abort_flag);
+      // O accumulators this thread reads: its own; when split, also the other's
+      bool have_o = false, have_oo = false;
+      auto wait_final = [&](int t) {
+        bool got = ptx::mbar_wait(&bar->o_final[t], 0, p.timeout_ns, abort_flag);
         if (!__all_sync(0xffffffffu, got)) {
           if (lane == 0) raise_error(p, bar, kErrEpilogue);
-          ok = false;
-        } else {
-          ptx::tc_fence_after();
-          have_o = true;
+          return false;
         }
+        ptx::tc_fence_after();
+        return true;
+      };
+      if (count > 0) {
+        have_o = wait_final(s);
+        ok = have_o;
+      }
+      if (ok && p.split && count_o > 0) {
+        have_oo = wait_final(s ^ 1);
+        ok = have_oo;
       }
       if (ok) {
         const float b2 = p.sink ? p.sink[h] * kLog2e : -INFINITY;
-        const float M = fmaxf(m, b2);
-        float o_scale = 0.f;
+        const float M = fmaxf(fmaxf(m, m_o), b2);
+        float o_scale = 0.f, oo_scale = 0.f;
         float lse_v = -INFINITY;
         if (M != -INFINITY) {
-          // O = sum of P V / (l + exp(sink)) with both terms taken against
+          // O = sum of P V / (l + exp(sink)) with every term taken against
           // the common maximum M; the LSE from the same normaliser
           const float em = (m == -INFINITY) ? 0.f : ptx::ex2(m - M);
-          const float lf = l * em + ((b2 == -INFINITY) ? 0.f : ptx::ex2(b2 - M));
+          const float eo = (m_o == -INFINITY) ? 0.f : ptx::ex2(m_o - M);
+          const float lf = l * em + l_o * eo + ((b2 == -INFINITY) ? 0.f : ptx::ex2(b2 - M));
           if (lf > 0.f) {
             o_scale = em / lf;
+            oo_scale = eo / lf;
             lse_v = (M + ptx::lg2(lf)) * kLn2;
           }
         }
@@ -682,34 +756,46 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
         const int perm_row = p.head_info[h * 4 + kHeadPermRow];
         const int64_t tok = valid ? token_of(p, store_mode, perm_row, pos) : 0;
         const int64_t orow = ((int64_t)ip.bh * p.N + tok) * D;
+        // columns written: all (paired); this sub-tile's half (split)
+        const int c_begin = (p.split && s == 1) ? kOHalf<D>() : 0;
+        const int c_end = (p.split && s == 0) ? kOHalf<D>() : D;
+        const uint32_t oo_tmem = tmem + lane_off + 256 + (s ^ 1) * 128;
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 16) {
+          if (c0 < c_begin || c0 >= c_end) continue;  // warp-uniform
           float ov[16];
           if (have_o) {
             ptx::tmem_ld16(o_tmem + c0, ov);
             ptx::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ov[i] *= o_scale;
           } else {
 #pragma unroll
             for (int i = 0; i < 16; ++i) ov[i] = 0.f;
+          }
+          if (have_oo) {
+            float ow[16];
+            ptx::tmem_ld16(oo_tmem + c0, ow);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ov[i] = fmaf(ow[i], oo_scale, ov[i]);
           }
           if (valid) {
             if (OUT_F32) {
               float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.o) + orow + c0);
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
-                dst[i] = make_float4(ov[4 * i] * o_scale, ov[4 * i + 1] * o_scale, ov[4 * i + 2] * o_scale,
-                                     ov[4 * i + 3] * o_scale);
+              for (int i = 0; i < 4; ++i) dst[i] = make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
             } else {
               uint32_t pk[8];
 #pragma unroll
-              for (int i = 0; i < 8; ++i) pk[i] = ptx::pack_bf16x2(ov[2 * i] * o_scale, ov[2 * i + 1] * o_scale);
+              for (int i = 0; i < 8; ++i) pk[i] = ptx::pack_bf16x2(ov[2 * i], ov[2 * i + 1]);
               uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + orow + c0);
               dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
               dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
             }
           }
         }
-        if (valid && p.lse) p.lse[(int64_t)ip.bh * p.N + tok] = lse_v;
+        if (valid && p.lse && (!p.split || s == 0)) p.lse[(int64_t)ip.bh * p.N + tok] = lse_v;
       }
     }
   }

@@ -26,7 +26,7 @@ struct FwdParams {
   CUtensorMap cq[2], ck[2], cv[2];  // column-major views [B*H][rows][cols][d]
   void* o;                          // [B][H][N][d], bf16 or fp32
   float* lse;                       // [B][H][N] or null
-  const int2* items;                // (b*H + h, query-tile pair)
+  const int2* items;                // (b*H + h, query-tile pair), or (b*H + h, query tile) when split
   const int32_t* head_info;         // [H][4], HeadField
   const int32_t* perm;              // explicit orders [n_perm][N]
   const uint64_t* block_bits;       // [block_heads][Nb][wpr]
@@ -40,6 +40,9 @@ struct FwdParams {
   int grid_rows, grid_cols;
   float scale_log2;                 // softmax scale * log2(e)
   int self_test_timeout;            // 1: wait on a barrier nothing arrives on (tests)
+  int split;                        // 0: a CTA takes two query tiles that share each key tile;
+                                    // 1: a CTA takes one query tile, its key tiles dealt
+                                    //    alternately to two sub-tile pipelines
 };
 
 struct PlanDumpParams {

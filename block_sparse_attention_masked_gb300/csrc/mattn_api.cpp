@@ -73,13 +73,16 @@ struct Normalized {
   bool any_colmajor_tma;
   int block_c, block_nb, block_wpr, block_heads;
   float scale;
+  bool split;         // schedule: one query tile per CTA, key tiles dealt to two pipelines
 };
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int normalize(const mattn_mask_desc* desc, int B, int H, int N, int d, int dtype, bool need_data, Normalized* out) {
   if (!desc) return fail(MATTN_ERR_INVALID_ARG, "mask descriptor is NULL");
-  if (desc->flags != 0) return fail(MATTN_ERR_INVALID_ARG, "flags must be 0");
+  if (desc->flags != 0 && desc->flags != MATTN_FLAG_SCHEDULE_PAIRED && desc->flags != MATTN_FLAG_SCHEDULE_SPLIT)
+    return fail(MATTN_ERR_INVALID_ARG, "flags must be 0, MATTN_FLAG_SCHEDULE_PAIRED or MATTN_FLAG_SCHEDULE_SPLIT (got %u)",
+                desc->flags);
   if (B < 1 || H < 1 || N < 1) return fail(MATTN_ERR_INVALID_ARG, "B, H, N must be >= 1 (got %d, %d, %d)", B, H, N);
   if (N > (1 << 30)) return fail(MATTN_ERR_UNSUPPORTED, "N = %d exceeds 2^30", N);
   if ((int64_t)B * H > (1 << 30)) return fail(MATTN_ERR_UNSUPPORTED, "B*H too large");
@@ -152,6 +155,11 @@ int normalize(const mattn_mask_desc* desc, int B, int H, int N, int d, int dtype
     n.block_wpr = (n.block_nb + 63) / 64;
     n.block_heads = desc->block_heads;
   }
+  // Schedule: SPLIT when neighbouring query tiles share few key tiles (block
+  // rows of one tile: independent rows of the block matrix), else PAIRED.
+  n.split = n.kind == kBlockSparse && n.block_c == 1;
+  if (desc->flags == MATTN_FLAG_SCHEDULE_PAIRED) n.split = false;
+  if (desc->flags == MATTN_FLAG_SCHEDULE_SPLIT) n.split = true;
   *out = std::move(n);
   return MATTN_OK;
 }
@@ -176,22 +184,24 @@ int interval_tiles(const Normalized& n, int h, int qt) {
   return r.hi >= r.lo ? r.hi - r.lo + 1 : 0;
 }
 
-// Work list: one item per (b*H + h, query-tile pair), heaviest first.
+// Work list, heaviest first: one item per (b*H + h, query-tile pair), or per
+// (b*H + h, query tile) under the split schedule.
 std::vector<int2> build_items(const Normalized& n) {
   const int nt = (n.N + kTile - 1) / kTile;
-  const int npairs = (nt + 1) / 2;
+  const int npairs = n.split ? nt : (nt + 1) / 2;  // work units per (b, h)
   std::vector<int2> items;
   items.reserve((size_t)n.B * n.H * npairs);
   for (int bh = 0; bh < n.B * n.H; ++bh)
     for (int pr = 0; pr < npairs; ++pr) items.push_back(make_int2(bh, pr));
   if (n.kind == kBlockSparse) {
-    // cost grows with the query tile under causality: later pairs first
+    // cost grows with the query tile under causality: later tiles first
     std::stable_sort(items.begin(), items.end(), [](const int2& a, const int2& b) { return a.y > b.y; });
   } else {
     std::vector<int> cost((size_t)n.H * npairs);
     for (int h = 0; h < n.H; ++h)
       for (int pr = 0; pr < npairs; ++pr)
-        cost[(size_t)h * npairs + pr] = interval_tiles(n, h, 2 * pr) + interval_tiles(n, h, 2 * pr + 1);
+        cost[(size_t)h * npairs + pr] = n.split ? interval_tiles(n, h, pr)
+                                                : interval_tiles(n, h, 2 * pr) + interval_tiles(n, h, 2 * pr + 1);
     const int H = n.H;
     std::stable_sort(items.begin(), items.end(), [&](const int2& a, const int2& b) {
       return cost[(size_t)(a.x % H) * npairs + a.y] > cost[(size_t)(b.x % H) * npairs + b.y];
@@ -259,7 +269,7 @@ int device_state(DeviceState** out) {
 std::string plan_key(const Normalized& n) {
   std::string k;
   char buf[96];
-  snprintf(buf, sizeof(buf), "%d|%d|%d|%d|%d|", n.kind, n.B, n.H, n.N, n.need_copy ? 1 : 0);
+  snprintf(buf, sizeof(buf), "%d|%d|%d|%d|%d|%d|", n.kind, n.B, n.H, n.N, n.need_copy ? 1 : 0, n.split ? 1 : 0);
   k += buf;
   for (const auto& hp : n.heads) {
     snprintf(buf, sizeof(buf), "%d,%d,%d,%d;", hp.param, hp.load, hp.store, hp.perm_row);
@@ -468,6 +478,7 @@ int fwd_locked(const void* q, const void* k, const void* v, void* o, float* lse,
   p.grid_cols = desc->grid_cols;
   p.scale_log2 = n.scale * 1.4426950408889634f;
   p.self_test_timeout = self_test;
+  p.split = n.split ? 1 : 0;
   MATTN_CUDA(launch_attention(p, d, dtype == MATTN_F32, stream), "attention launch");
   return MATTN_OK;
 }

@@ -68,6 +68,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   return false;
 }
 
+// Bounded wait like mbar_wait, sleeping sleep_ns between polls: for a waiter
+// off the critical path that shares its SM sub-partition with latency-bound
+// warps, whose issue slots a tight polling loop would take.
+__device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity, uint64_t timeout_ns,
+                                                  volatile int* abort_flag, uint32_t sleep_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1; it < 0x80000000u; ++it) {
+    __nanosleep(sleep_ns);
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 7u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > timeout_ns) return false;
+    }
+  }
+  return false;
+}
+
 // Bounded wait that ignores the abort flag (used while unwinding, to let
 // operations already issued finish before their resources are released).
 __device__ __forceinline__ bool mbar_wait_time_only(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
@@ -77,6 +95,17 @@ __device__ __forceinline__ bool mbar_wait_time_only(uint64_t* bar, uint32_t pari
     if ((it & 63u) == 63u && globaltimer_ns() - t0 > timeout_ns) return false;
   }
   return false;
+}
+
+// ---------------------------------------------------------------- shared-memory words
+// Loads / stores of a shared-memory word by its shared-window address.
+__device__ __forceinline__ uint32_t ld_shared_acquire(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_shared(uint32_t addr, uint32_t v) {
+  asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 // ---------------------------------------------------------------- TMA

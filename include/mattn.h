@@ -85,6 +85,16 @@ typedef enum { MATTN_BF16 = 0, MATTN_F32 = 1 } mattn_dtype;
 
 #define MATTN_TILE 128 /* query / key tile edge of the tile plan */
 
+/* Schedule flags for mattn_mask_desc.flags (results are the same either way,
+ * up to floating-point rounding order).  A CTA either takes two neighbouring
+ * 128-row query tiles that share each loaded key tile (PAIRED), or one query
+ * tile whose key tiles are dealt alternately to two pipelines merged at the
+ * end (SPLIT).  With neither flag set the library picks: SPLIT for
+ * MATTN_BLOCK_SPARSE with Bs == 128 (neighbouring query tiles then fall in
+ * different block rows and share few key tiles), PAIRED otherwise. */
+#define MATTN_FLAG_SCHEDULE_PAIRED 1u
+#define MATTN_FLAG_SCHEDULE_SPLIT 2u
+
 typedef struct {
   int32_t kind;              /* mattn_kind                                                */
   int32_t param;             /* C, w, W or Bs for every head (ignored for MATTN_FULL);     */
@@ -105,7 +115,7 @@ typedef struct {
   const float* sink;         /* optional DEVICE fp32 [H] sink logits (NULL = no sink);     */
                              /* HOST for mattn_fwd_host                                    */
   float softmax_scale;       /* 0 => 1/sqrt(d)                                             */
-  uint32_t flags;            /* reserved, must be 0                                        */
+  uint32_t flags;            /* 0, MATTN_FLAG_SCHEDULE_PAIRED or MATTN_FLAG_SCHEDULE_SPLIT   */
 } mattn_mask_desc;
 
 /*

@@ -71,8 +71,11 @@ def test_invalid_arguments_rejected_on_host(L):
     assert L.mattn_count_pairs(ctypes.byref(_desc(4, 128)), 1, 1, 256, ctypes.byref(out)) == mattn.ERR_INVALID_ARG
     bad_scale = _desc(0, 0, softmax_scale=-1.0)
     assert L.mattn_count_pairs(ctypes.byref(bad_scale), 1, 1, 16, ctypes.byref(out)) == mattn.ERR_INVALID_ARG
-    flags = _desc(0, 0, flags=1)
-    assert L.mattn_count_pairs(ctypes.byref(flags), 1, 1, 16, ctypes.byref(out)) == mattn.ERR_INVALID_ARG
+    for ok_flags in (mattn.FLAG_SCHEDULE_PAIRED, mattn.FLAG_SCHEDULE_SPLIT):
+        assert L.mattn_count_pairs(ctypes.byref(_desc(0, 0, flags=ok_flags)), 1, 1, 16, ctypes.byref(out)) == mattn.OK
+    for bad_flags in (3, 4, 0x80000000):
+        flags = _desc(0, 0, flags=bad_flags)
+        assert L.mattn_count_pairs(ctypes.byref(flags), 1, 1, 16, ctypes.byref(out)) == mattn.ERR_INVALID_ARG
     order = (ctypes.c_int32 * 1)(mattn.ORDER_COLUMN_MAJOR)
     cm = _desc(2, 3, head_order=order, grid_rows=3, grid_cols=5)
     assert L.mattn_count_pairs(ctypes.byref(cm), 1, 1, 16, ctypes.byref(out)) == mattn.ERR_INVALID_ARG

@@ -57,9 +57,9 @@ def _subset(spec, hs):
                     perm_grid=pick(spec.perm_grid), block=blk, sink=sink)
 
 
-def check(q, k, v, spec, rows=None, heads=None, tag=""):
+def check(q, k, v, spec, rows=None, heads=None, tag="", schedule=None):
     B, H, N, d = q.shape
-    mask = mattn.prepare(spec, H, N)
+    mask = mattn.prepare(spec, H, N, schedule=schedule)
     o, lse = mattn.attention(q, k, v, mask)
     torch.cuda.synchronize()
     rc, word = mattn.device_status()
@@ -116,6 +116,27 @@ def test_kinds_small(d, n):
         check(q, k, v, spec, tag=f"{spec.kind} d{d} n{n}")
 
 
+@pytest.mark.parametrize("schedule", ["paired", "split"])
+@pytest.mark.parametrize("d,n", [(64, 1000), (80, 640), (128, 1300)])
+def test_kinds_both_schedules(schedule, d, n):
+    """Both CTA schedules on every kind: two query tiles sharing each key
+    tile, or one query tile with its key tiles dealt to two pipelines that
+    are merged at the end (odd tile counts leave one pipeline a tile short,
+    one-tile rows leave it empty)."""
+    q, k, v = _qkv(2, 2, n, d, seed=d * n + len(schedule))
+    nb = -(-n // 128)
+    specs = [
+        MaskSpec("full", [0, 0], sink=np.array([1.0, -0.5])),
+        MaskSpec("chunk", [128, 300]),
+        MaskSpec("sliding", [20, 333]),
+        MaskSpec("causal_window", [128, 700], sink=np.array([0.5, -1.0])),
+        MaskSpec("block", [128, 128], block=bernoulli_causal_blocks(2, nb, n + 7)),
+        MaskSpec("block", [256, 256], block=bernoulli_causal_blocks(2, -(-n // 256), n + 8)),
+    ]
+    for spec in specs:
+        check(q, k, v, spec, tag=f"{schedule} {spec.kind} {spec.head_param} d{d} n{n}", schedule=schedule)
+
+
 def test_batch_and_sink_everywhere():
     q, k, v = _qkv(2, 3, 640, 64, seed=3)
     spec = MaskSpec("sliding", [50, 130, 700], sink=np.array([0.0, 2.0, -3.0]))
@@ -163,8 +184,10 @@ def test_empty_rows_and_sink_only_rows():
     o, lse = check(q, k, v, spec, tag="empty rows with sink")
     assert torch.all(o[:, :, :256] == 0)
     spec2 = MaskSpec("block", [128, 128], block=blk)
-    o2, lse2 = check(q, k, v, spec2, tag="empty rows")
-    assert torch.all(torch.isneginf(lse2[:, :, :256]))
+    for schedule in ("paired", "split"):
+        o2, lse2 = check(q, k, v, spec2, tag=f"empty rows {schedule}", schedule=schedule)
+        assert torch.all(torch.isneginf(lse2[:, :, :256]))
+        assert torch.all(o2[:, :, :256] == 0)
 
 
 def test_deterministic():
@@ -247,9 +270,11 @@ def test_workload_causal4096():
     check(q, k, v, spec, rows=rows, heads=heads, tag="causal4096")
 
 
-def test_workload_bsparse128k():
+@pytest.mark.parametrize("schedule", [None, "paired"])
+def test_workload_bsparse128k(schedule):
     wl = WORKLOADS["bsparse128k"]
     q, k, v = make_workload_inputs(wl, seed=0, device="cuda")
     spec = make_mask(wl, "block128")
     rows = _sample_rows(wl.N, [128 * i for i in range(1, 1024, 97)], 192, 4)
-    check(q, k, v, spec, rows=rows, heads=[(0, 0), (0, 13), (0, 31)], tag="bsparse128k")
+    check(q, k, v, spec, rows=rows, heads=[(0, 0), (0, 13), (0, 31)], tag=f"bsparse128k {schedule}",
+          schedule=schedule)
