@@ -70,7 +70,7 @@ class MaskDesc(ctypes.Structure):
 
 
 EXPORTS = (
-    "mattn_fwd", "mattn_fwd_host", "mattn_count_pairs", "mattn_plan_tiles", "mattn_plan_tiles_device",
+    "mattn_fwd", "mattn_fwd_host", "mattn_fwd_noalloc", "mattn_count_pairs", "mattn_plan_tiles", "mattn_plan_tiles_device",
     "mattn_device_status", "mattn_set_wait_timeout_ns", "mattn_status_string", "mattn_last_error",
     "mattn_version",
 )
@@ -91,6 +91,8 @@ def lib() -> ctypes.CDLL:
     dp = ctypes.POINTER(MaskDesc)
     L.mattn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, dp, vp]
     L.mattn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, dp, vp]
+    L.mattn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, dp, vp,
+                                    ctypes.POINTER(ctypes.c_uint32)]
     L.mattn_count_pairs.argtypes = [dp, i32, i32, i32, u64p]
     L.mattn_plan_tiles.argtypes = [dp, i32, i32, vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]
     L.mattn_plan_tiles_device.argtypes = [dp, i32, i32, vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t), vp]
@@ -101,7 +103,7 @@ def lib() -> ctypes.CDLL:
     L.mattn_last_error.restype = ctypes.c_char_p
     L.mattn_last_error.argtypes = []
     L.mattn_version.argtypes = []
-    for name in ("mattn_fwd", "mattn_fwd_host", "mattn_count_pairs", "mattn_plan_tiles",
+    for name in ("mattn_fwd", "mattn_fwd_host", "mattn_fwd_noalloc", "mattn_count_pairs", "mattn_plan_tiles",
                  "mattn_plan_tiles_device", "mattn_device_status", "mattn_set_wait_timeout_ns",
                  "mattn_version"):
         getattr(L, name).restype = ctypes.c_int
@@ -242,6 +244,33 @@ def attention(q, k, v, mask: PreparedMask, out=None, lse=None, want_lse: bool = 
     rc = lib().mattn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                          lse.data_ptr() if lse is not None else None, B, H, N, d, _dtype_code(q),
                          ctypes.byref(mask.desc), stream)
+    _check(rc)
+    return out, lse
+
+
+def attention_noalloc(q, k, v, mask: PreparedMask, out, lse=None, stream=None, check_wait: bool = True):
+    """The same forward through ``mattn_fwd_noalloc``, which allocates no
+    device memory: the caller passes ``out`` (and ``lse``) preallocated; the
+    kernel's work list lives in a fixed static array of the library (bf16
+    inputs read in place only; see the header for the limits).  With
+    ``check_wait`` the call synchronises the stream and raises if a device
+    wait gave up.  Returns (out, lse)."""
+    import torch
+
+    if not (q.is_cuda and k.is_cuda and v.is_cuda and out.is_cuda):
+        raise ValueError("q, k, v and out must be CUDA tensors")
+    for t in (q, k, v, out):
+        if not t.is_contiguous():
+            raise ValueError("q, k, v and out must be contiguous [B, H, N, d]")
+    B, H, N, d = q.shape
+    if k.shape != q.shape or v.shape != q.shape or out.shape != q.shape:
+        raise ValueError("q, k, v and out must have the same shape")
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    word = ctypes.c_uint32(0)
+    rc = lib().mattn_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                 lse.data_ptr() if lse is not None else None, B, H, N, d, _dtype_code(q),
+                                 ctypes.byref(mask.desc), stream, ctypes.byref(word) if check_wait else None)
     _check(rc)
     return out, lse
 

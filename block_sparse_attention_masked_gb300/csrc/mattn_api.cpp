@@ -19,6 +19,7 @@
 #include <vector>
 
 #include "kernel_params.h"
+#include "launch_prep.h"
 #include "mattn.h"
 #include "plan_rules.h"
 
@@ -484,6 +485,80 @@ int fwd_locked(const void* q, const void* k, const void* v, void* o, float* lse,
 }
 
 }  // namespace
+
+int report_error(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int prepare_in_place_launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                            int d, int dtype, const mattn_mask_desc* desc, int max_heads, size_t max_items,
+                            InPlaceLaunch* out) {
+  Normalized n;
+  int rc = normalize(desc, B, H, N, d, dtype, true, &n);
+  if (rc) return rc;
+  rc = check_device_ptrs(q, k, v, o, lse);
+  if (rc) return rc;
+  if (n.need_copy)
+    return fail(MATTN_ERR_UNSUPPORTED,
+                "inputs need the reorder / convert pre-pass (fp32 inputs, explicit orders, or a column-major grid "
+                "whose row count is not a multiple of %d); only bf16 inputs read in place are supported here",
+                kTile);
+  if (H > max_heads) return fail(MATTN_ERR_CAPACITY, "H = %d heads exceeds the limit of %d", H, max_heads);
+  std::vector<int2> items = build_items(n);
+  if (items.size() > max_items)
+    return fail(MATTN_ERR_CAPACITY, "the launch has %zu work items, more than the limit of %zu", items.size(),
+                max_items);
+  int dev = -1, major = 0, minor = 0;
+  MATTN_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  MATTN_CUDA(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev), "compute capability");
+  MATTN_CUDA(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev), "compute capability");
+  if (major != 10 || minor != 3)
+    return fail(MATTN_ERR_NO_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a", dev, major, minor);
+  if ((rc = get_encoder())) return rc;
+
+  FwdParams& p = out->p;
+  memset(&p, 0, sizeof(p));
+  const int rows = n.any_colmajor_tma ? desc->grid_rows : 0;
+  const int cols = n.any_colmajor_tma ? desc->grid_cols : 0;
+  if ((rc = make_maps(n, q, p.tq, p.cq, rows, cols))) return rc;
+  if ((rc = make_maps(n, k, p.tk, p.ck, rows, cols))) return rc;
+  if ((rc = make_v_maps(n, v, p.tv, p.cv, rows, cols))) return rc;
+  p.o = o;
+  p.lse = lse;
+  p.items = nullptr;
+  p.n_items = (int)items.size();
+  p.head_info = nullptr;
+  p.perm = nullptr;
+  p.block_bits = n.kind == kBlockSparse ? desc->block_bits : nullptr;
+  p.sink = desc->sink;
+  p.err = nullptr;
+  p.timeout_ns = wait_timeout_ns();
+  p.B = B; p.H = H; p.N = N;
+  p.kind = n.kind;
+  p.block_heads = n.block_heads;
+  p.block_wpr = n.block_wpr;
+  p.block_c = n.block_c;
+  p.block_nb = n.block_nb;
+  p.grid_rows = desc->grid_rows;
+  p.grid_cols = desc->grid_cols;
+  p.scale_log2 = n.scale * 1.4426950408889634f;
+  p.self_test_timeout = 0;
+  p.split = n.split ? 1 : 0;
+  out->items = std::move(items);
+  out->head_info.assign((size_t)H * 4, 0);
+  for (int h = 0; h < H; ++h) {
+    out->head_info[h * 4 + kHeadParam] = n.heads[h].param;
+    out->head_info[h * 4 + kHeadLoad] = n.heads[h].load;
+    out->head_info[h * 4 + kHeadStore] = n.heads[h].store;
+    out->head_info[h * 4 + kHeadPermRow] = n.heads[h].perm_row;
+  }
+  return MATTN_OK;
+}
+
 }  // namespace mattn
 
 using namespace mattn;

@@ -145,6 +145,59 @@ int mattn_fwd_host(const void* q, const void* k, const void* v, void* o, float* 
                    const mattn_mask_desc* desc, void* stream);
 
 /*
+ * mattn_fwd_noalloc -- mattn_fwd for callers that must not allocate device
+ * memory.  The pages have no counterpart: this entry point serves the
+ * library's callers, not the method.
+ *
+ * Who needs it: mattn_fwd allocates on first use (the work list, the
+ * per-head table and the error word of each new mask, with cudaMalloc).
+ * Some callers cannot allow that: a framework whose pooling allocator has
+ * reserved the device memory up front, so that an allocation outside the
+ * pool can fail or go unaccounted; a serving loop that forbids allocation
+ * after start-up, because cudaMalloc and cudaFree may synchronise the
+ * device and take unbounded time; a plug-in host that hands the operator
+ * its buffers and gives it no allocator.  This entry point runs the same
+ * attention kernel with that bookkeeping in a fixed static device array
+ * inside the library instead, and calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *
+ *   q, k, v, o, lse, B, H, N, d, dtype, desc, stream: as for mattn_fwd.
+ *   wait_error_out  optional HOST pointer.  NULL: the call is asynchronous
+ *                   like mattn_fwd (a device wait that gives up is then not
+ *                   reported).  Non-NULL: the call synchronises `stream`,
+ *                   stores the kernel's error word there (0 = none) and
+ *                   returns MATTN_ERR_TIMEOUT if it is non-zero.
+ *
+ * Limits (the static array is sized for them, MATTN_NOALLOC_SCRATCH_BYTES
+ * in all, held on every device that loads the library until the process
+ * exits):
+ *   - H <= MATTN_NOALLOC_MAX_HEADS;
+ *   - at most MATTN_NOALLOC_MAX_ITEMS work items, where a launch has
+ *     B*H*ceil(ceil(N/128)/2) items under the paired schedule and
+ *     B*H*ceil(N/128) under the split one (the 128K-token, 32-head
+ *     block-sparse prefill has 32768);
+ *   - bf16 inputs read in place: every head raster, or column-major over a
+ *     grid whose row count is a multiple of 128.  fp32 inputs and explicit
+ *     orders need a reorder buffer and give MATTN_ERR_UNSUPPORTED.
+ * Beyond a limit the call returns MATTN_ERR_CAPACITY (or UNSUPPORTED) with
+ * a message in mattn_last_error() and launches nothing.
+ *
+ * Sharing: every call on a device uses the same static array and leaves
+ * its work list there; each call rewrites what it reads and clears the
+ * error word first, on `stream`.  Calls whose work overlaps on the GPU
+ * (different streams, or several host threads) therefore race on the
+ * array: order them, e.g. on one stream.  The first call on a device looks
+ * up the array's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture begins.
+ */
+#define MATTN_NOALLOC_MAX_HEADS 4096
+#define MATTN_NOALLOC_MAX_ITEMS 65536
+#define MATTN_NOALLOC_SCRATCH_BYTES (256 + 16 * MATTN_NOALLOC_MAX_HEADS + 8 * MATTN_NOALLOC_MAX_ITEMS)
+int mattn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                      int B, int H, int N, int d, int dtype,
+                      const mattn_mask_desc* desc, void* stream, uint32_t* wait_error_out);
+
+/*
  * mattn_count_pairs -- exact number of visible (query, key) pairs summed over
  * B and H (the unit of the effective-FLOP count, 4*d FLOPs per pair).  Host
  * only; block_bits are read as HOST memory.
