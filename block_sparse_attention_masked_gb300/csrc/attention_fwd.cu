@@ -216,14 +216,17 @@ __device__ __forceinline__ void raise_error(const FwdParams& p, Barriers* bar, u
 }
 
 // TMA load of one 128-row tile (all d columns) starting at sequence position p0.
+// `policy` is the L2 eviction priority of the tile's lines.
 template <int D>
 __device__ __forceinline__ void load_tile(const FwdParams& p, const CUtensorMap* raster, const CUtensorMap* colmaj,
-                                          bool column_major, uint8_t* dst, uint64_t* bar, int p0, int bh) {
+                                          bool column_major, uint8_t* dst, uint64_t* bar, int p0, int bh,
+                                          uint64_t policy) {
   using G = Geo<D>;
   if (!column_major) {
 #pragma unroll
-    for (int c = 0; c < G::kChunks; ++c) ptx::tma_load_3d(dst + c * G::kChunkBytes, &raster[0], bar, c * 64, p0, bh);
-    if (G::kRem) ptx::tma_load_3d(dst + G::kChunks * G::kChunkBytes, &raster[1], bar, 0, p0, bh);
+    for (int c = 0; c < G::kChunks; ++c)
+      ptx::tma_load_3d_hint(dst + c * G::kChunkBytes, &raster[0], bar, c * 64, p0, bh, policy);
+    if (G::kRem) ptx::tma_load_3d_hint(dst + G::kChunks * G::kChunkBytes, &raster[1], bar, 0, p0, bh, policy);
   } else {
     // position p = c * rows + r holds token r * cols + c; a 128-position tile is
     // one grid column c, rows r0 .. r0 + 127 (rows % 128 == 0 is required).
@@ -231,8 +234,9 @@ __device__ __forceinline__ void load_tile(const FwdParams& p, const CUtensorMap*
     const int r0 = p0 - col * p.grid_rows;
 #pragma unroll
     for (int c = 0; c < G::kChunks; ++c)
-      ptx::tma_load_4d(dst + c * G::kChunkBytes, &colmaj[0], bar, c * 64, col, r0, bh);
-    if (G::kRem) ptx::tma_load_4d(dst + G::kChunks * G::kChunkBytes, &colmaj[1], bar, 0, col, r0, bh);
+      ptx::tma_load_4d_hint(dst + c * G::kChunkBytes, &colmaj[0], bar, c * 64, col, r0, bh, policy);
+    if (G::kRem)
+      ptx::tma_load_4d_hint(dst + G::kChunks * G::kChunkBytes, &colmaj[1], bar, 0, col, r0, bh, policy);
   }
 }
 
@@ -240,18 +244,18 @@ __device__ __forceinline__ void load_tile(const FwdParams& p, const CUtensorMap*
 // the V views has a kVW-column box).
 template <int D>
 __device__ __forceinline__ void load_v_tile(const FwdParams& p, bool column_major, uint8_t* dst, uint64_t* bar,
-                                            int p0, int bh) {
+                                            int p0, int bh, uint64_t policy) {
   using G = Geo<D>;
   if (!column_major) {
 #pragma unroll
     for (int c = 0; c < G::kVChunks; ++c)
-      ptx::tma_load_3d(dst + c * G::kVChunkBytes, &p.tv[0], bar, c * G::kVW, p0, bh);
+      ptx::tma_load_3d_hint(dst + c * G::kVChunkBytes, &p.tv[0], bar, c * G::kVW, p0, bh, policy);
   } else {
     const int col = p0 / p.grid_rows;
     const int r0 = p0 - col * p.grid_rows;
 #pragma unroll
     for (int c = 0; c < G::kVChunks; ++c)
-      ptx::tma_load_4d(dst + c * G::kVChunkBytes, &p.cv[0], bar, c * G::kVW, col, r0, bh);
+      ptx::tma_load_4d_hint(dst + c * G::kVChunkBytes, &p.cv[0], bar, c * G::kVW, col, r0, bh, policy);
   }
 }
 
@@ -455,6 +459,9 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
     ptx::setmaxnreg_dec<kRegsControl>();
     if (lane == 0) {
       const bool is_k = warp == 0;
+      // K and V tiles are re-read by the other query tiles of the head (keep
+      // them in L2); a Q tile is read by this CTA alone
+      const uint64_t keep = ptx::l2_policy_evict_last();
       if (is_k) {
         const CUtensorMap* mq = colmaj ? p.cq : p.tq;
         ptx::prefetch_tmap(&mq[0]);
@@ -463,7 +470,8 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
           const SubPlan& sp = s ? ip.sp1 : ip.sp0;
           if (!sp.has_tiles || (p.split && s == 1)) continue;  // split: one Q tile for both pipelines
           ptx::mbar_arrive_expect_tx(&bar->q_full[s], G::kTileBytes);
-          load_tile<D>(p, p.tq, p.cq, colmaj, sq + s * G::kTileBytes, &bar->q_full[s], sp.qt * kTile, ip.bh);
+          load_tile<D>(p, p.tq, p.cq, colmaj, sq + s * G::kTileBytes, &bar->q_full[s], sp.qt * kTile, ip.bh,
+                       ptx::l2_policy_evict_first());
         }
       }
       uint64_t* empty = is_k ? bar->k_empty : bar->v_empty;
@@ -480,9 +488,9 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
         }
         ptx::mbar_arrive_expect_tx(&full[slot], G::kTileBytes);
         if (is_k)
-          load_tile<D>(p, p.tk, p.ck, colmaj, ring + slot * G::kTileBytes, &full[slot], kt * kTile, ip.bh);
+          load_tile<D>(p, p.tk, p.ck, colmaj, ring + slot * G::kTileBytes, &full[slot], kt * kTile, ip.bh, keep);
         else
-          load_v_tile<D>(p, colmaj, ring + slot * G::kTileBytes, &full[slot], kt * kTile, ip.bh);
+          load_v_tile<D>(p, colmaj, ring + slot * G::kTileBytes, &full[slot], kt * kTile, ip.bh, keep);
       }
       if (*abort_flag) {
         // let copies already in flight land before the CTA's shared memory goes away

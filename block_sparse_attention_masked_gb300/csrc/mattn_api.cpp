@@ -185,19 +185,23 @@ int interval_tiles(const Normalized& n, int h, int qt) {
   return r.hi >= r.lo ? r.hi - r.lo + 1 : 0;
 }
 
-// Work list, heaviest first: one item per (b*H + h, query-tile pair), or per
-// (b*H + h, query tile) under the split schedule.
+// Work list: one item per (b*H + h, query-tile pair), or per (b*H + h,
+// query tile) under the split schedule.
 std::vector<int2> build_items(const Normalized& n) {
   const int nt = (n.N + kTile - 1) / kTile;
   const int npairs = n.split ? nt : (nt + 1) / 2;  // work units per (b, h)
   std::vector<int2> items;
   items.reserve((size_t)n.B * n.H * npairs);
-  for (int bh = 0; bh < n.B * n.H; ++bh)
-    for (int pr = 0; pr < npairs; ++pr) items.push_back(make_int2(bh, pr));
   if (n.kind == kBlockSparse) {
-    // cost grows with the query tile under causality: later tiles first
-    std::stable_sort(items.begin(), items.end(), [](const int2& a, const int2& b) { return a.y > b.y; });
+    // Head by head, and inside a head the later query tiles (more key tiles
+    // under causality) first.  The CTAs in flight then share one head's K
+    // and V, which fit in L2, instead of streaming every head's at once; the
+    // lightest tiles of the last head end the launch.
+    for (int bh = 0; bh < n.B * n.H; ++bh)
+      for (int pr = npairs - 1; pr >= 0; --pr) items.push_back(make_int2(bh, pr));
   } else {
+    for (int bh = 0; bh < n.B * n.H; ++bh)
+      for (int pr = 0; pr < npairs; ++pr) items.push_back(make_int2(bh, pr));
     std::vector<int> cost((size_t)n.H * npairs);
     for (int h = 0; h < n.H; ++h)
       for (int pr = 0; pr < npairs; ++pr)
