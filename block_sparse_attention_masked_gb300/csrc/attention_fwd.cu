@@ -272,20 +272,22 @@ __device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint32_t q_addr4, uint
   constexpr uint32_t lbo = 1u << 16;  // unused for swizzled K-major operands
   constexpr uint32_t hi128 = ptx::smem_desc_hi(1024, ptx::kSw128);
   constexpr uint32_t hiR = ptx::smem_desc_hi(8 * G::kRemRowBytes, G::kRemSwizzle);
-  int step = 0;
-#pragma unroll
-  for (int c = 0; c < G::kChunks; ++c) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k, ++step) {
-      const uint32_t off4 = ((c * G::kChunkBytes + k * 32) >> 4) + lbo;
-      ptx::mma_ss_elect(s_tmem, desc_of(q_addr4 + off4, hi128), desc_of(k_addr4 + off4, hi128), idesc, step > 0);
-    }
+  // Runtime loops (one thread issues): the tensor pipe takes an MMA every
+  // ~64 cycles, so unrolling buys nothing and only lengthens the code the
+  // issuing warp has to fetch.
+  uint32_t acc = 0;
+#pragma unroll 1
+  for (int step = 0; step < G::kChunks * 4; ++step) {
+    const uint32_t off4 = (uint32_t)(((step >> 2) * G::kChunkBytes + (step & 3) * 32) >> 4) + lbo;
+    ptx::mma_ss(s_tmem, desc_of(q_addr4 + off4, hi128), desc_of(k_addr4 + off4, hi128), idesc, acc);
+    acc = 1;
   }
   if (G::kRem) {
-#pragma unroll
-    for (int k = 0; k < G::kRem / 16; ++k, ++step) {
-      const uint32_t off4 = ((G::kChunks * G::kChunkBytes + k * 32) >> 4) + lbo;
-      ptx::mma_ss_elect(s_tmem, desc_of(q_addr4 + off4, hiR), desc_of(k_addr4 + off4, hiR), idesc, step > 0);
+#pragma unroll 1
+    for (int k = 0; k < G::kRem / 16; ++k) {
+      const uint32_t off4 = (uint32_t)((G::kChunks * G::kChunkBytes + k * 32) >> 4) + lbo;
+      ptx::mma_ss(s_tmem, desc_of(q_addr4 + off4, hiR), desc_of(k_addr4 + off4, hiR), idesc, acc);
+      acc = 1;
     }
   }
 }
@@ -294,7 +296,7 @@ __device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint32_t q_addr4, uint
 // A operand; V (keys x d, d contiguous) is an MN-major B operand whose
 // kVW-column atoms lie kVChunkBytes apart (leading byte offset) and whose
 // 8-key groups lie 8 rows apart (stride byte offset).  One N = D MMA per
-// 16 keys.
+// 16 keys, issued by one thread.
 template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_addr4, bool accumulate) {
   using G = Geo<D>;
@@ -302,11 +304,12 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
   constexpr uint32_t row_bytes = G::kVW * 2;
   constexpr uint32_t lbo = (uint32_t)(G::kVChunkBytes >> 4) << 16;
   constexpr uint32_t hi = ptx::smem_desc_hi(8 * row_bytes, G::kVSwizzle);
-#pragma unroll
+  uint32_t acc = accumulate ? 1u : 0u;
+#pragma unroll 1
   for (int k = 0; k < kTile / 16; ++k) {
-    const uint32_t acc = (accumulate || k > 0) ? 1u : 0u;
-    const uint32_t a = p_tmem + k * 8;  // 16 bf16 keys = 8 columns
-    ptx::mma_ts_elect(o_tmem, a, desc_of(v_addr4 + ((k * 16 * row_bytes) >> 4) + lbo, hi), idesc, acc);
+    // 16 bf16 keys = 8 tensor-memory columns of P; 16 rows of V
+    ptx::mma_ts(o_tmem, p_tmem + k * 8, desc_of(v_addr4 + ((k * 16 * row_bytes) >> 4) + lbo, hi), idesc, acc);
+    acc = 1;
   }
 }
 
@@ -577,13 +580,15 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
         if (!__all_sync(0xffffffffu, mma_turn_wait(bar, ticket, p.timeout_ns, abort_flag))) {
           fail(); ok = false; break;
         }
+        if (ptx::elect_one()) {
+          if (pend) issue_pv<D>(o_tm, s_tm, v4 + (ve % VS) * tile4, !first);
+          if (use) issue_qk<D>(s_tm, q4, k4 + ks * tile4);
+        }
+        __syncwarp();
         if (pend) {
-          issue_pv<D>(o_tm, s_tm, v4 + (ve % VS) * tile4, !first);
           first = false;
           pend = false;
         }
-        if (use) issue_qk<D>(s_tm, q4, k4 + ks * tile4);
-        __syncwarp();
         if (lane == 0) mma_turn_pass(bar, ticket);
         // commits after the turn has passed: each tracks this thread's own
         // MMAs only, so the other issuer need not wait for them
@@ -608,7 +613,8 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
         } else {
           ++pcount;
           ptx::tc_fence_after();
-          issue_pv<D>(o_tm, s_tm, v4 + (ve % VS) * tile4, !first);
+          if (ptx::elect_one()) issue_pv<D>(o_tm, s_tm, v4 + (ve % VS) * tile4, !first);
+          __syncwarp();
           first = false;
           pend = false;
         }
