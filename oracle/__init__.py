@@ -14,8 +14,13 @@ Modules
            the tile enumeration and the exact unmasked-pair count.
 ``brute``  a pure-Python loop version for N <= 16, written independently from
            the same definitions; it is one of the pins of ``dense``.
+``rr_select``  RRAttention's dynamic block selection (round-robin query
+           sampling, stride importance, block aggregation, top-tau with the
+           last query block kept), in fp64 numpy.
+``rr_brute``   the same selection as pure-Python loops for tiny heads, one
+           of the pins of ``rr_select``.
 
-Every function of ``dense`` is pinned by a ``-m "not gpu"`` test against
+Every function of ``dense`` and ``rr_select`` is pinned by a ``-m "not gpu"`` test against
 something other than itself (closed forms, the worked example of the SHS
 slides, structural special cases, brute force); none is "parity unpinned".
 """
