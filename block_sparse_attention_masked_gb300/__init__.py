@@ -42,6 +42,7 @@ ORDER_COLUMN_MAJOR = -2
 TILE = 128
 TILE_FULL, TILE_PARTIAL = 1, 2
 FLAG_SCHEDULE_PAIRED, FLAG_SCHEDULE_SPLIT = 1, 2
+RR_SINK_RECENT = 1
 SCHEDULE = {None: 0, "auto": 0, "paired": FLAG_SCHEDULE_PAIRED, "split": FLAG_SCHEDULE_SPLIT}
 
 
@@ -70,7 +71,7 @@ class MaskDesc(ctypes.Structure):
 
 
 EXPORTS = (
-    "mattn_fwd", "mattn_fwd_host", "mattn_fwd_noalloc", "mattn_count_pairs", "mattn_plan_tiles", "mattn_plan_tiles_device",
+    "mattn_fwd", "mattn_fwd_host", "mattn_fwd_noalloc", "mattn_rr_select", "mattn_count_pairs", "mattn_plan_tiles", "mattn_plan_tiles_device",
     "mattn_device_status", "mattn_set_wait_timeout_ns", "mattn_status_string", "mattn_last_error",
     "mattn_version",
 )
@@ -93,6 +94,8 @@ def lib() -> ctypes.CDLL:
     L.mattn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, dp, vp]
     L.mattn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, dp, vp,
                                     ctypes.POINTER(ctypes.c_uint32)]
+    L.mattn_rr_select.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i32, ctypes.c_float, ctypes.c_uint32,
+                                  vp, vp, vp]
     L.mattn_count_pairs.argtypes = [dp, i32, i32, i32, u64p]
     L.mattn_plan_tiles.argtypes = [dp, i32, i32, vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]
     L.mattn_plan_tiles_device.argtypes = [dp, i32, i32, vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t), vp]
@@ -103,7 +106,7 @@ def lib() -> ctypes.CDLL:
     L.mattn_last_error.restype = ctypes.c_char_p
     L.mattn_last_error.argtypes = []
     L.mattn_version.argtypes = []
-    for name in ("mattn_fwd", "mattn_fwd_host", "mattn_fwd_noalloc", "mattn_count_pairs", "mattn_plan_tiles",
+    for name in ("mattn_fwd", "mattn_fwd_host", "mattn_fwd_noalloc", "mattn_rr_select", "mattn_count_pairs", "mattn_plan_tiles",
                  "mattn_plan_tiles_device", "mattn_device_status", "mattn_set_wait_timeout_ns",
                  "mattn_version"):
         getattr(L, name).restype = ctypes.c_int
@@ -273,6 +276,68 @@ def attention_noalloc(q, k, v, mask: PreparedMask, out, lse=None, stream=None, c
                                  ctypes.byref(mask.desc), stream, ctypes.byref(word) if check_wait else None)
     _check(rc)
     return out, lse
+
+
+def unpack_block_bits(words: np.ndarray, nb: int) -> np.ndarray:
+    """uint64 [..., Nb, ceil(Nb/64)] -> bool [..., Nb, Nb] (inverse of pack_block_bits)."""
+    words = np.ascontiguousarray(np.asarray(words).view("<u8"))
+    by = words.view(np.uint8).reshape(words.shape[:-1] + (words.shape[-1] * 8,))
+    bits = np.unpackbits(by, axis=-1, bitorder="little")
+    return bits[..., :nb].astype(bool)
+
+
+def rr_select(q, k, stride: int = 8, block: int = 128, tau: float = 0.95, sink_recent: bool = False,
+              want_scores: bool = False, stream=None):
+    """RRAttention's dynamic block selection on CUDA bf16 tensors [B, H, N, d].
+
+    Returns (bits, scores): bits int64 [B*H, Nb, ceil(Nb/64)] on the device,
+    the block_bits layout of the attention mask (one [H, Nb, ..] slab per
+    batch entry); scores fp32 [B*H, Nb, Nb] or None."""
+    import torch
+
+    if not (q.is_cuda and k.is_cuda):
+        raise ValueError("q and k must be CUDA tensors")
+    for t in (q, k):
+        if not t.is_contiguous():
+            raise ValueError("q and k must be contiguous [B, H, N, d]")
+    B, H, N, d = q.shape
+    if k.shape != q.shape or k.dtype != q.dtype:
+        raise ValueError("q and k must have the same shape and dtype")
+    if stride <= 0 or block % stride or N % stride:
+        raise ValueError("the stride must divide N and the block size")
+    nb = -(-(N // stride) // (block // stride))
+    wpr = (nb + 63) // 64
+    bits = torch.empty((B * H, nb, wpr), dtype=torch.int64, device=q.device)
+    scores = torch.empty((B * H, nb, nb), dtype=torch.float32, device=q.device) if want_scores else None
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    rc = lib().mattn_rr_select(q.data_ptr(), k.data_ptr(), B, H, N, d, _dtype_code(q), stride, block, float(tau),
+                               RR_SINK_RECENT if sink_recent else 0, bits.data_ptr(),
+                               scores.data_ptr() if scores is not None else None, stream)
+    _check(rc)
+    return bits, scores
+
+
+class DeviceBlockMask:
+    """A block-sparse mask descriptor over block bits already on the device
+    (e.g. from rr_select): ``bits`` int64 [H, Nb, ceil(Nb/64)] for one batch
+    entry, block size ``block``; optional per-head ``sink`` (fp32 [H] on the device)."""
+
+    def __init__(self, bits, H: int, N: int, block: int, sink=None, schedule: Optional[str] = None):
+        d = MaskDesc()
+        d.kind = KIND["block"]
+        d.param = int(block)
+        self._params = (ctypes.c_int32 * H)(*([int(block)] * H))
+        d.head_param = self._params
+        d.block_bits = bits.data_ptr()
+        d.block_heads = int(bits.shape[0])
+        if sink is not None:
+            d.sink = sink.data_ptr()
+        d.softmax_scale = 0.0
+        d.flags = SCHEDULE[schedule]
+        self._keep = (bits, sink)
+        self.desc = d
+        self.H, self.N, self.kind = H, N, "block"
 
 
 def attention_host(q, k, v, spec_or_mask, out=None, lse=None, stream=None):

@@ -2,6 +2,8 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace mattn {
@@ -62,6 +64,37 @@ struct GatherParams {
   int src_f32;
   int grid_rows, grid_cols;
 };
+
+// RRAttention block selection (rr_select.cu).
+struct RrParams {
+  CUtensorMap tq[2];      // sampled queries: view [B*H][L/S][S][d], 64-column boxes (map [0])
+  CUtensorMap tk[2];      // stride key sums [B*H][L/S][d], 64-column boxes (map [0])
+  float* block_scores;    // out: [B*H][nb][nb]
+  uint32_t* err;          // device error word
+  unsigned long long timeout_ns;
+  int BH, H, n_s, S, g, nb;  // n_s = L/S strides, g = strides per block, nb blocks
+  float scale_log2;       // log2(e) / (S sqrt(d))
+};
+
+struct RrSumParams {
+  const __nv_bfloat16* k;  // [B*H][N][d]
+  __nv_bfloat16* ksum;     // [B*H][N/S][d]
+  int BH, N, n_s, d, S;
+};
+
+struct RrTopParams {
+  const float* scores;  // [B*H][nb][nb]
+  uint64_t* bits;       // out: [B*H][nb][wpr]
+  int BH, nb, wpr, p2;  // p2: power of two >= max(nb, 256), the sort length
+  float tau;
+  int sink_recent;
+};
+
+cudaError_t launch_rr_stride_sum(const RrSumParams& p, cudaStream_t stream);
+cudaError_t launch_rr_scores(const RrParams& p, int d, cudaStream_t stream);
+cudaError_t launch_rr_topk(const RrTopParams& p, cudaStream_t stream);
+size_t rr_scores_smem_bytes(int d);
+size_t rr_topk_smem_bytes(int p2, int wpr);
 
 // Launchers (attention_fwd.cu).
 cudaError_t launch_attention(const FwdParams& p, int d, bool out_f32, cudaStream_t stream);

@@ -246,6 +246,8 @@ struct DeviceState {
   DeviceBuf copy;      // reordered / converted q, k, v
   DeviceBuf host_io;   // mattn_fwd_host staging
   DeviceBuf dump;      // plan dump
+  DeviceBuf rr_ksum;   // block selection: stride key sums
+  DeviceBuf rr_scores; // block selection: block scores when the caller passes none
   std::map<std::string, std::unique_ptr<Plan>> plans;
 };
 
@@ -642,6 +644,82 @@ int mattn_fwd_host(const void* q, const void* k, const void* v, void* o, float* 
   MATTN_CUDA(cudaMemcpyAsync(o, dout, tensor, cudaMemcpyDeviceToHost, stream), "copy o");
   if (lse) MATTN_CUDA(cudaMemcpyAsync(lse, dlse, lse_bytes, cudaMemcpyDeviceToHost, stream), "copy lse");
   MATTN_CUDA(cudaStreamSynchronize(stream), "stream sync");
+  return MATTN_OK;
+}
+
+int mattn_rr_select(const void* q, const void* k, int B, int H, int N, int d, int dtype, int stride, int block,
+                    float tau, uint32_t flags, uint64_t* block_bits, float* block_scores, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  std::lock_guard<std::mutex> lk(g_mutex);
+  if (!q || !k || !block_bits) return fail(MATTN_ERR_INVALID_ARG, "q, k and block_bits must be non-NULL");
+  if (B < 1 || H < 1 || N < 1) return fail(MATTN_ERR_INVALID_ARG, "B, H, N must be >= 1 (got %d, %d, %d)", B, H, N);
+  if ((int64_t)B * H > (1 << 20)) return fail(MATTN_ERR_UNSUPPORTED, "B*H too large");
+  if (dtype != MATTN_BF16) return fail(MATTN_ERR_UNSUPPORTED, "block selection takes bf16 inputs only");
+  if (d != 64 && d != 128) return fail(MATTN_ERR_UNSUPPORTED, "block selection supports head dim 64 or 128 (got %d)", d);
+  if (!aligned16(q) || !aligned16(k)) return fail(MATTN_ERR_UNSUPPORTED, "q and k must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(block_bits) & 7u) || (reinterpret_cast<uintptr_t>(block_scores) & 3u))
+    return fail(MATTN_ERR_INVALID_ARG, "block_bits must be 8-byte and block_scores 4-byte aligned");
+  if (stride < 1 || N % stride != 0)
+    return fail(MATTN_ERR_INVALID_ARG, "the stride must be >= 1 and divide N (stride %d, N %d)", stride, N);
+  if (block < stride || block % stride != 0)
+    return fail(MATTN_ERR_INVALID_ARG, "the block size must be a multiple of the stride (block %d, stride %d)", block,
+                stride);
+  const int g = block / stride;
+  if (g != 4 && g != 8 && g != 16 && g != 32)
+    return fail(MATTN_ERR_UNSUPPORTED, "block / stride must be 4, 8, 16 or 32 (got %d)", g);
+  if (!(tau > 0.f && tau <= 1.f)) return fail(MATTN_ERR_INVALID_ARG, "tau must lie in (0, 1] (got %g)", (double)tau);
+  if (flags & ~MATTN_RR_SINK_RECENT) return fail(MATTN_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+  const int n_s = N / stride;
+  const int nb = (n_s + g - 1) / g;
+  if (nb > 8192) return fail(MATTN_ERR_UNSUPPORTED, "more than 8192 blocks per row (%d)", nb);
+  const int wpr = (nb + 63) / 64;
+  int p2 = 256;
+  while (p2 < nb) p2 <<= 1;
+  const int BH = B * H;
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc) return rc;
+  if ((rc = get_encoder())) return rc;
+  if ((rc = st->rr_ksum.reserve((size_t)BH * n_s * d * 2, "cudaMalloc(stride key sums)"))) return rc;
+  if (!block_scores) {
+    if ((rc = st->rr_scores.reserve((size_t)BH * nb * nb * sizeof(float), "cudaMalloc(block scores)"))) return rc;
+    block_scores = static_cast<float*>(st->rr_scores.ptr);
+  }
+  RrSumParams sp;
+  sp.k = static_cast<const __nv_bfloat16*>(k);
+  sp.ksum = static_cast<__nv_bfloat16*>(st->rr_ksum.ptr);
+  sp.BH = BH; sp.N = N; sp.n_s = n_s; sp.d = d; sp.S = stride;
+  MATTN_CUDA(launch_rr_stride_sum(sp, stream), "stride sum launch");
+
+  RrParams rp;
+  memset(&rp, 0, sizeof(rp));
+  {
+    // sampled queries: element (c, o, i, bh) = Q[bh][i*stride + o][c] (Eq. 6-7)
+    cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)stride, (cuuint64_t)n_s, (cuuint64_t)BH};
+    cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)stride * d * 2, (cuuint64_t)N * d * 2};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)kTile, 1};
+    if ((rc = encode(&rp.tq[0], q, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))) return rc;
+  }
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n_s, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)n_s * d * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1};
+    if ((rc = encode(&rp.tk[0], st->rr_ksum.ptr, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))) return rc;
+  }
+  rp.block_scores = block_scores;
+  rp.err = st->err;
+  rp.timeout_ns = wait_timeout_ns();
+  rp.BH = BH; rp.H = H; rp.n_s = n_s; rp.S = stride; rp.g = g; rp.nb = nb;
+  rp.scale_log2 = (float)(1.4426950408889634 / (stride * std::sqrt((double)d)));
+  MATTN_CUDA(launch_rr_scores(rp, d, stream), "block score launch");
+
+  RrTopParams tp;
+  tp.scores = block_scores;
+  tp.bits = block_bits;
+  tp.BH = BH; tp.nb = nb; tp.wpr = wpr; tp.p2 = p2;
+  tp.tau = tau;
+  tp.sink_recent = (flags & MATTN_RR_SINK_RECENT) ? 1 : 0;
+  MATTN_CUDA(launch_rr_topk(tp, stream), "top-tau launch");
   return MATTN_OK;
 }
 

@@ -198,6 +198,46 @@ int mattn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, floa
                       const mattn_mask_desc* desc, void* stream, uint32_t* wait_error_out);
 
 /*
+ * mattn_rr_select -- RRAttention's dynamic block selection: the block-selection
+ * bitmap B of every (batch entry, head), from Q and K ("RRAttention",
+ * section 3, Eq. 6-12, with the causality of section 2.1, Eq. 5):
+ *   - head h samples one query per stride of `stride` tokens, at offset
+ *     stride - 1 - (h mod stride) inside the stride (Eq. 6-7);
+ *   - the importance of key stride j for sampled query i is
+ *     I_ij = q_i . (sum of the stride's keys) / (stride sqrt(d)) (Eq. 8),
+ *     normalised by a softmax over every key stride (Eq. 9);
+ *   - block score S_mn = sum of those probabilities over the strides of
+ *     query block m and key block n, blocks of `block` tokens (Eq. 10);
+ *   - per query block, the key blocks in decreasing score order are kept
+ *     until their share of the row's total reaches tau (Eq. 11; equal
+ *     scores: smaller block index first), the last query block keeps every
+ *     block (Eq. 12), and blocks above the diagonal are dropped (Eq. 5).
+ *   With MATTN_RR_SINK_RECENT the first key block and the diagonal block of
+ *   every query block are kept too (the page's "sink and recent" option).
+ *
+ *   q, k         DEVICE bf16 [B][H][N][d], d = 64 or 128, 16-byte aligned.
+ *   stride       tokens per stride; must divide N.
+ *   block        block size, a multiple of stride with block/stride in
+ *                {4, 8, 16, 32} (the page's configuration: stride 8,
+ *                block 128).
+ *   tau          threshold in (0, 1] (the page uses 0.9 and 0.95).
+ *   block_bits   DEVICE output [B*H][Nb][ceil(Nb/64)] uint64, Nb =
+ *                ceil(N / block), bit n of row m = B[m][n]: the layout of
+ *                mattn_mask_desc.block_bits, one [H][Nb][..] slab per batch
+ *                entry.
+ *   block_scores optional DEVICE output fp32 [B*H][Nb][Nb], the scores S
+ *                (NULL: kept in library memory).
+ * Nb must not exceed 8192.  Asynchronous on `stream`; library workspace
+ * (the stride key sums, and the scores when block_scores is NULL) is
+ * allocated on first use and reused.  A device wait that gives up is
+ * reported by mattn_device_status.
+ */
+#define MATTN_RR_SINK_RECENT 1u
+int mattn_rr_select(const void* q, const void* k, int B, int H, int N, int d, int dtype,
+                    int stride, int block, float tau, uint32_t flags,
+                    uint64_t* block_bits, float* block_scores, void* stream);
+
+/*
  * mattn_count_pairs -- exact number of visible (query, key) pairs summed over
  * B and H (the unit of the effective-FLOP count, 4*d FLOPs per pair).  Host
  * only; block_bits are read as HOST memory.
