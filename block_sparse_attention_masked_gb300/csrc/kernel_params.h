@@ -85,7 +85,7 @@ struct RrSumParams {
 struct RrTopParams {
   const float* scores;  // [B*H][nb][nb]
   uint64_t* bits;       // out: [B*H][nb][wpr]
-  int BH, nb, wpr, p2;  // p2: power of two >= max(nb, 256), the sort length
+  int BH, nb, wpr;
   float tau;
   int sink_recent;
 };
@@ -94,7 +94,6 @@ cudaError_t launch_rr_stride_sum(const RrSumParams& p, cudaStream_t stream);
 cudaError_t launch_rr_scores(const RrParams& p, int d, cudaStream_t stream);
 cudaError_t launch_rr_topk(const RrTopParams& p, cudaStream_t stream);
 size_t rr_scores_smem_bytes(int d);
-size_t rr_topk_smem_bytes(int p2, int wpr);
 
 // Launchers (attention_fwd.cu).
 cudaError_t launch_attention(const FwdParams& p, int d, bool out_f32, cudaStream_t stream);

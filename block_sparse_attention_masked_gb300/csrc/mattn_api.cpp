@@ -673,8 +673,6 @@ int mattn_rr_select(const void* q, const void* k, int B, int H, int N, int d, in
   const int nb = (n_s + g - 1) / g;
   if (nb > 8192) return fail(MATTN_ERR_UNSUPPORTED, "more than 8192 blocks per row (%d)", nb);
   const int wpr = (nb + 63) / 64;
-  int p2 = 256;
-  while (p2 < nb) p2 <<= 1;
   const int BH = B * H;
   DeviceState* st = nullptr;
   int rc = device_state(&st);
@@ -716,7 +714,7 @@ int mattn_rr_select(const void* q, const void* k, int B, int H, int N, int d, in
   RrTopParams tp;
   tp.scores = block_scores;
   tp.bits = block_bits;
-  tp.BH = BH; tp.nb = nb; tp.wpr = wpr; tp.p2 = p2;
+  tp.BH = BH; tp.nb = nb; tp.wpr = wpr;
   tp.tau = tau;
   tp.sink_recent = (flags & MATTN_RR_SINK_RECENT) ? 1 : 0;
   MATTN_CUDA(launch_rr_topk(tp, stream), "top-tau launch");

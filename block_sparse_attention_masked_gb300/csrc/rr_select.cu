@@ -5,7 +5,7 @@
 // Three launches:
 //   rr_stride_sum_kernel  Ksum_j = sum of the S keys of stride j (Eq. 8's key
 //                         aggregation), bf16 [B*H][L/S][d].  HBM-bound.
-//   rr_scores_kernel      per (head, 128 sampled query strides): the
+//   rr_scores_kernel      per (head, 2 x 128 sampled query strides): the
 //                         sampled queries (Eq. 6-7, read through a strided
 //                         TMA view, no gather) times Ksum^T on the tensor
 //                         cores (Eq. 8), the row softmax over every key stride
@@ -15,11 +15,13 @@
 //                         the probabilities of each g x g (query, key) stride
 //                         square, g = Bs/S, into one block score, so the
 //                         L/S x L/S importance matrix never reaches memory.
-//   rr_topk_kernel        per (head, query block): sort the block scores in
-//                         decreasing order, keep the shortest prefix whose
-//                         share of the row reaches tau (Eq. 11), add the last
-//                         query block (Eq. 12), drop blocks above the diagonal
-//                         (Eq. 5), write the bitmap row.
+//   rr_topk_kernel        per (head, query block): keep the key blocks that
+//                         the scores sorted in decreasing order need for
+//                         their share of the row to reach tau (Eq. 11; found
+//                         by a bitwise threshold search with exact integer
+//                         sums, no sort), add the last query block (Eq. 12),
+//                         drop blocks above the diagonal (Eq. 5), write the
+//                         bitmap row.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -33,13 +35,15 @@
 namespace mattn {
 namespace {
 
-constexpr int kRrThreads = 256;
-constexpr int kRrStages = 2;  // Ksum ring; two CTAs share an SM
+constexpr int kRrThreads = 256;      // top-k kernel
+constexpr int kRrScoreThreads = 384; // score kernel: 4 control warps + 2 x 4 row warps
+constexpr int kRrStages = 4;         // Ksum ring depth
+constexpr int kRrQTiles = 2;         // sampled-query tiles per CTA, sharing every Ksum tile
 
 struct RrBarriers {
   uint64_t q_full;
   uint64_t k_full[kRrStages], k_empty[kRrStages];
-  uint64_t s_full[2], s_empty[2];
+  uint64_t s_full[kRrQTiles][2], s_empty[kRrQTiles][2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -50,28 +54,79 @@ __device__ __forceinline__ void rr_raise(const RrParams& p, RrBarriers* bar, uin
   atomicOr(p.err, bit);
 }
 
-// Grid (ceil(n_s / 128), B*H); 256 threads: warp 0 loads (TMA), warp 1
-// allocates tensor memory and issues the MMAs, warps 4..7 hold one sampled
-// query stride (a row of S) per thread.  Tensor memory: two 128-column S
-// buffers, so the product of the next key tile runs while this one is
-// exponentiated.
+// Pass 0 over one 128-column tile of a row: running maximum m and sum l of
+// exp2(x * sl2 - m) (Eq. 9's denominator, log2 domain); columns >= ncols
+// are absent.
+template <bool RAGGED>
+__device__ __forceinline__ void rr_pass0(const float (&x)[128], float sl2, int ncols, float& m, float& l) {
+  float cm = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < 128; ++c)
+    if (!RAGGED || c < ncols) cm = fmaxf(cm, x[c]);
+  const float m_new = fmaxf(m, cm * sl2);
+  if (m_new == -INFINITY) return;
+  const float2 sl2v = make_float2(sl2, sl2);
+  const float2 negm = make_float2(-m_new, -m_new);
+  float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+  for (int c = 0; c < 128; c += 2) {
+    const float2 t = ptx::ffma2(make_float2(x[c], x[c + 1]), sl2v, negm);
+    float2 e = make_float2(ptx::ex2(t.x), ptx::ex2(t.y));
+    if (RAGGED) {
+      if (c >= ncols) e.x = 0.f;
+      if (c + 1 >= ncols) e.y = 0.f;
+    }
+    acc[(c >> 1) & 1] = ptx::fadd2(acc[(c >> 1) & 1], e);
+  }
+  const float2 a = ptx::fadd2(acc[0], acc[1]);
+  l = (m == -INFINITY ? 0.f : l * ptx::ex2(m - m_new)) + (a.x + a.y);
+  m = m_new;
+}
+
+// Pass 1 over one tile: P_ij = exp2(x * sl2 - lse2) (Eq. 9) summed over
+// groups of G key strides (Eq. 10, the key side of a block).
+template <int G, bool RAGGED>
+__device__ __forceinline__ void rr_pass1(const float (&x)[128], float sl2, float lse2, int ncols,
+                                         float (&gs)[128 / G]) {
+  const float2 sl2v = make_float2(sl2, sl2);
+  const float2 negl = make_float2(-lse2, -lse2);
+#pragma unroll
+  for (int i = 0; i < 128 / G; ++i) gs[i] = 0.f;
+#pragma unroll
+  for (int c = 0; c < 128; c += 2) {
+    const float2 t = ptx::ffma2(make_float2(x[c], x[c + 1]), sl2v, negl);
+    float2 e = make_float2(ptx::ex2(t.x), ptx::ex2(t.y));
+    if (RAGGED) {
+      if (c >= ncols) e.x = 0.f;
+      if (c + 1 >= ncols) e.y = 0.f;
+    }
+    gs[c / G] += e.x + e.y;
+  }
+}
+
+// Grid (ceil(n_s / 256), B*H); 384 threads: warp 0 loads (TMA), warp 1
+// allocates tensor memory and issues the MMAs, warps 4..7 and 8..11 each
+// hold one 128-row tile of sampled query strides, one row per thread.
+// Tensor memory: per query tile two 128-column S buffers, so the products
+// of the next key tile run while this one is exponentiated.
 template <int D, int G>
-__global__ void __launch_bounds__(kRrThreads, 2) rr_scores_kernel(const __grid_constant__ RrParams p) {
+__global__ void __launch_bounds__(kRrScoreThreads, 1) rr_scores_kernel(const __grid_constant__ RrParams p) {
   using T = Geo<D>;
   static_assert(D % 64 == 0, "sampled-query views use 64-column boxes");
   static_assert(G >= 4 && G <= 32 && (G & (G - 1)) == 0, "strides per block: 4, 8, 16 or 32");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sq = base;
-  uint8_t* sk = sq + T::kTileBytes;
+  uint8_t* sk = sq + kRrQTiles * T::kTileBytes;
   RrBarriers* bar = reinterpret_cast<RrBarriers*>(sk + kRrStages * T::kTileBytes);
   volatile int* abort_flag = &bar->abort_flag;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int qt = blockIdx.x;
   const int bh = blockIdx.y;
   const int h = bh % p.H;
+  const int q0 = blockIdx.x * kRrQTiles * kTile;                 // first sampled stride of the CTA
+  const int nq = (q0 + kTile < p.n_s) ? kRrQTiles : 1;           // query tiles with rows
   const int n_kt = (p.n_s + kTile - 1) / kTile;
   const int steps = 2 * n_kt;  // pass 0 then pass 1 over the key-stride tiles
 
@@ -81,16 +136,17 @@ __global__ void __launch_bounds__(kRrThreads, 2) rr_scores_kernel(const __grid_c
       ptx::mbar_init(&bar->k_full[i], 1);
       ptx::mbar_init(&bar->k_empty[i], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(&bar->s_full[b], 1);
-      ptx::mbar_init(&bar->s_empty[b], 128);
-    }
+    for (int s = 0; s < kRrQTiles; ++s)
+      for (int b = 0; b < 2; ++b) {
+        ptx::mbar_init(&bar->s_full[s][b], 1);
+        ptx::mbar_init(&bar->s_empty[s][b], 128);
+      }
     ptx::mbar_init(&bar->drain, 1);
     bar->abort_flag = 0;
     ptx::fence_barrier_init();
   }
   if (warp == 1) {
-    ptx::tmem_alloc(&bar->tmem_base, 256);
+    ptx::tmem_alloc(&bar->tmem_base, 512);
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
@@ -104,10 +160,12 @@ __global__ void __launch_bounds__(kRrThreads, 2) rr_scores_kernel(const __grid_c
       // Eq. 6: head h samples offset S - 1 - (h mod S) of every stride; the
       // view [B*H][L/S][S][d] turns that into one 128-row box per tile.
       const int off = p.S - 1 - (h % p.S);
-      ptx::mbar_arrive_expect_tx(&bar->q_full, T::kTileBytes);
+      ptx::mbar_arrive_expect_tx(&bar->q_full, nq * T::kTileBytes);
+      for (int s = 0; s < nq; ++s)
 #pragma unroll
-      for (int c = 0; c < T::kChunks; ++c)
-        ptx::tma_load_4d(sq + c * T::kChunkBytes, &p.tq[0], &bar->q_full, c * 64, off, qt * kTile, bh);
+        for (int c = 0; c < T::kChunks; ++c)
+          ptx::tma_load_4d(sq + s * T::kTileBytes + c * T::kChunkBytes, &p.tq[0], &bar->q_full, c * 64, off,
+                           q0 + s * kTile, bh);
       const uint64_t keep = ptx::l2_policy_evict_last();  // every query tile of the head re-reads Ksum
       for (int t = 0; t < steps; ++t) {
         const int slot = t % kRrStages;
@@ -140,14 +198,17 @@ __global__ void __launch_bounds__(kRrThreads, 2) rr_scores_kernel(const __grid_c
     for (int t = 0; ok && t < steps; ++t) {
       const int slot = t % kRrStages;
       const int b = t & 1;
-      ok = wait_all(&bar->k_full[slot], (t / kRrStages) & 1) && wait_all(&bar->s_empty[b], ((t >> 1) & 1) ^ 1);
-      if (!ok) break;
-      ptx::tc_fence_after();
-      if (ptx::elect_one()) issue_qk<D>(tmem + b * 128, q4, k4 + slot * tile4);
-      __syncwarp();
-      ptx::mma_commit_elect(&bar->s_full[b]);
-      ptx::mma_commit_elect(&bar->k_empty[slot]);
-      issued = true;
+      ok = wait_all(&bar->k_full[slot], (t / kRrStages) & 1);
+      for (int s = 0; ok && s < nq; ++s) {
+        ok = wait_all(&bar->s_empty[s][b], ((t >> 1) & 1) ^ 1);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        if (ptx::elect_one()) issue_qk<D>(tmem + (s * 2 + b) * 128, q4 + s * tile4, k4 + slot * tile4);
+        __syncwarp();
+        ptx::mma_commit_elect(&bar->s_full[s][b]);
+        issued = true;
+      }
+      if (ok) ptx::mma_commit_elect(&bar->k_empty[slot]);
     }
     if (!ok) {
       if (lane == 0) rr_raise(p, bar, kErrMma);
@@ -156,76 +217,58 @@ __global__ void __launch_bounds__(kRrThreads, 2) rr_scores_kernel(const __grid_c
         ptx::mbar_wait_time_only(&bar->drain, 0, p.timeout_ns);
       }
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && (warp - 4) / 4 < nq) {
     // ------------------------------------------------------------ softmax and block sums
+    const int s = (warp - 4) >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const int grow = qt * kTile + row;  // sampled query stride of this thread
-    const bool row_ok = grow < p.n_s;
-    const float sl2 = p.scale_log2;     // log2(e) / (S sqrt(d)), Eq. 8's scale
+    const uint32_t s_tmem = tmem + lane_off + s * 256;
+    const int grow = q0 + s * kTile + row;  // sampled query stride of this thread
+    const float sl2 = p.scale_log2;         // log2(e) / (S sqrt(d)), Eq. 8's scale
     float m = -INFINITY, l = 0.f, lse2 = 0.f;
     for (int t = 0; t < steps; ++t) {
       const int b = t & 1;
-      const bool got = ptx::mbar_wait(&bar->s_full[b], (t >> 1) & 1, p.timeout_ns, abort_flag);
+      const bool got = ptx::mbar_wait(&bar->s_full[s][b], (t >> 1) & 1, p.timeout_ns, abort_flag);
       if (!__all_sync(0xffffffffu, got)) {
         if (lane == 0) rr_raise(p, bar, kErrSoftmax);
         break;
       }
       ptx::tc_fence_after();
+      float x[128];
+      ptx::tmem_ld32(s_tmem + b * 128 + 0, *reinterpret_cast<float(*)[32]>(&x[0]));
+      ptx::tmem_ld32(s_tmem + b * 128 + 32, *reinterpret_cast<float(*)[32]>(&x[32]));
+      ptx::tmem_ld32(s_tmem + b * 128 + 64, *reinterpret_cast<float(*)[32]>(&x[64]));
+      ptx::tmem_ld32(s_tmem + b * 128 + 96, *reinterpret_cast<float(*)[32]>(&x[96]));
+      ptx::tmem_wait_ld();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&bar->s_empty[s][b]);  // the row is in registers: buffer b may be overwritten
       const int kt = t % n_kt;
-      const bool second = t >= n_kt;
       const int ncols = min(kTile, p.n_s - kt * kTile);  // key strides present in this tile
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        float x[32];
-        ptx::tmem_ld32(tmem + lane_off + b * 128 + c * 32, x);
-        ptx::tmem_wait_ld();
-        if (c == 3) {
-          ptx::tc_fence_before();
-          ptx::mbar_arrive(&bar->s_empty[b]);  // S buffer b may be overwritten
-        }
-        const int col0 = c * 32;
-        if (!second) {
-          // pass 0 (Eq. 9's denominator): running max and sum, log2 domain
-          float cm = -INFINITY;
+      if (t < n_kt) {
+        if (ncols == kTile) rr_pass0<false>(x, sl2, ncols, m, l);
+        else rr_pass0<true>(x, sl2, ncols, m, l);
+        if (t == n_kt - 1) lse2 = grow < p.n_s ? m + ptx::lg2(l) : INFINITY;  // absent rows add nothing
+      } else {
+        float gs[128 / G];
+        if (ncols == kTile) rr_pass1<G, false>(x, sl2, lse2, ncols, gs);
+        else rr_pass1<G, true>(x, sl2, lse2, ncols, gs);
+        // Eq. 10, the query side: sum over the G rows (lanes) of the block
 #pragma unroll
-          for (int k = 0; k < 32; ++k)
-            if (col0 + k < ncols) cm = fmaxf(cm, x[k]);
-          const float m_new = fmaxf(m, cm * sl2);
-          if (m_new != -INFINITY) {
-            float s = 0.f;
+        for (int off = 1; off < G; off <<= 1)
 #pragma unroll
-            for (int k = 0; k < 32; ++k) s += (col0 + k < ncols) ? ptx::ex2(fmaf(x[k], sl2, -m_new)) : 0.f;
-            l = (m == -INFINITY ? 0.f : l * ptx::ex2(m - m_new)) + s;
-            m = m_new;
-          }
-        } else {
-          // pass 1: P_ij (Eq. 9) summed over g key strides, then over the g
-          // query strides (lanes) of the block (Eq. 10)
-          float gs[32 / G];
+          for (int i = 0; i < 128 / G; ++i) gs[i] += __shfl_xor_sync(0xffffffffu, gs[i], off);
+        if ((lane & (G - 1)) == 0) {
+          const int mb = grow / G;          // query block
+          const int nb0 = kt * (kTile / G);  // first key block of this tile
+          if (mb < p.nb) {
+            float* dst = p.block_scores + ((int64_t)bh * p.nb + mb) * p.nb;
 #pragma unroll
-          for (int i = 0; i < 32 / G; ++i) gs[i] = 0.f;
-#pragma unroll
-          for (int k = 0; k < 32; ++k)
-            gs[k / G] += (row_ok && col0 + k < ncols) ? ptx::ex2(fmaf(x[k], sl2, -lse2)) : 0.f;
-#pragma unroll
-          for (int off = 1; off < G; off <<= 1)
-#pragma unroll
-            for (int i = 0; i < 32 / G; ++i) gs[i] += __shfl_xor_sync(0xffffffffu, gs[i], off);
-          if ((lane & (G - 1)) == 0) {
-            const int mb = grow / G;                    // query block
-            const int nb0 = (kt * kTile + col0) / G;    // first key block of this chunk
-            if (mb < p.nb) {
-              float* dst = p.block_scores + ((int64_t)bh * p.nb + mb) * p.nb;
-#pragma unroll
-              for (int i = 0; i < 32 / G; ++i)
-                if (nb0 + i < p.nb) dst[nb0 + i] = gs[i];
-            }
+            for (int i = 0; i < 128 / G; ++i)
+              if (nb0 + i < p.nb) dst[nb0 + i] = gs[i];
           }
         }
       }
-      if (t == n_kt - 1) lse2 = m + ptx::lg2(l);
     }
   }
 
@@ -233,7 +276,7 @@ __global__ void __launch_bounds__(kRrThreads, 2) rr_scores_kernel(const __grid_c
   __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, 256);
+    ptx::tmem_dealloc(tmem, 512);
   }
 }
 
@@ -270,99 +313,97 @@ __global__ void rr_stride_sum_kernel(const RrSumParams p) {
   *reinterpret_cast<uint4*>(p.ksum + orow * p.d + c8) = out;
 }
 
-// One CTA per (query block m, head bh).  Dynamic shared memory:
-// part[kRrThreads] (double), bits[wpr] (uint64), key[p2] (float), idx[p2] (int).
+// One warp per (head, query block) row of block scores: the top-tau choice
+// of Eq. 11 without sorting.  The decision is taken on the scores quantised
+// to integers, q_n = floor(s_n 2^(30 - e)) with 2^(e-1) <= max_n s_n < 2^e,
+// so every sum below is exact and independent of the order it is formed in:
+//   T  = ceil(tau_q total / 2^20), tau_q = round(tau 2^20), total = sum q_n;
+//   v* = the largest score (as its bit pattern; scores are >= 0, so the
+//        pattern orders like the value) with sum_{s_n >= v*} q_n >= T,
+//        found bit by bit from the top;
+//   kept = every block with s_n > v*, and the first blocks (by index) with
+//          s_n == v* until the kept sum reaches T.
+// That is the shortest prefix of the scores sorted in decreasing order
+// (equal scores by increasing index) whose sum reaches tau times the total.
+// Then the last query block keeps everything (Eq. 12) and blocks above the
+// diagonal go (Eq. 5).  8 warps (rows) per CTA; the row is re-read from L1.
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
 __global__ void __launch_bounds__(kRrThreads) rr_topk_kernel(const RrTopParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  const int p2 = p.p2;
-  double* part = reinterpret_cast<double*>(smem_raw);
-  unsigned long long* bits = reinterpret_cast<unsigned long long*>(part + kRrThreads);
-  float* key = reinterpret_cast<float*>(bits + p.wpr);
-  int* idx = reinterpret_cast<int*>(key + p2);
-  __shared__ int cut;
-  __shared__ double s_total;
-  const int m = blockIdx.x;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int m = blockIdx.x * (kRrThreads / 32) + warp;  // query block of this warp
   const int64_t bh = blockIdx.y;
-  const int tid = threadIdx.x;
+  if (m >= p.nb) return;
   const float* row = p.scores + (bh * p.nb + m) * p.nb;
-  for (int i = tid; i < p2; i += kRrThreads) {
-    key[i] = i < p.nb ? row[i] : -INFINITY;
-    idx[i] = i;
-  }
-  for (int w = tid; w < p.wpr; w += kRrThreads) bits[w] = 0ull;
-  if (tid == 0) cut = p.nb - 1;
-  // bitonic sort: decreasing score, equal scores by increasing block index
-  for (int k = 2; k <= p2; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      __syncthreads();
-      for (int i = tid; i < p2; i += kRrThreads) {
-        const int ixj = i ^ j;
-        if (ixj <= i) continue;
-        const float ka = key[i], kb = key[ixj];
-        const int ia = idx[i], ib = idx[ixj];
-        const bool a_first = (ka > kb) || (ka == kb && ia < ib);
-        const bool ascending_block = (i & k) != 0;  // this half runs the other way
-        if (ascending_block ? a_first : !a_first) {
-          key[i] = kb; key[ixj] = ka;
-          idx[i] = ib; idx[ixj] = ia;
-        }
-      }
+  const int nb = p.nb;
+  // row maximum -> quantisation scale
+  float mx = 0.f;
+  for (int n = lane; n < nb; n += 32) mx = fmaxf(mx, row[n]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  int e = 0;
+  frexpf(mx, &e);  // 2^(e-1) <= mx < 2^e (mx > 0: a row of softmax mass)
+  const int sh = 30 - e;
+  auto quant = [&](float x) -> unsigned long long {
+    return (unsigned long long)__float2uint_rz(scalbnf(fmaxf(x, 0.f), sh));
+  };
+  unsigned long long tot = 0;
+  for (int n = lane; n < nb; n += 32) tot += quant(row[n]);
+  tot = warp_sum_u64(tot);
+  const unsigned long long tau_q = (unsigned long long)llrintf(p.tau * 1048576.0f);
+  const unsigned long long T = (tau_q * tot + ((1ull << 20) - 1)) >> 20;
+  // v*: bit by bit from the top (bit 31 is the sign, always clear)
+  uint32_t vstar = 0;
+  for (int bit = 30; bit >= 0; --bit) {
+    const uint32_t cand = vstar | (1u << bit);
+    unsigned long long a = 0;
+    for (int n = lane; n < nb; n += 32) {
+      const float x = row[n];
+      if (__float_as_uint(fmaxf(x, 0.f)) >= cand) a += quant(x);
     }
+    if (warp_sum_u64(a) >= T) vstar = cand;
   }
-  __syncthreads();
-  // running sums over the sorted scores in fp64 (Eq. 11): each thread owns
-  // a contiguous run of per = p2 / kRrThreads entries
-  const int per = p2 / kRrThreads;
-  const int i0 = tid * per;
-  double mine = 0.0;
-  for (int e = 0; e < per; ++e) {
-    const float v = key[i0 + e];
-    if (v != -INFINITY) mine += (double)v;
+  unsigned long long agt = 0;
+  for (int n = lane; n < nb; n += 32) {
+    const float x = row[n];
+    if (__float_as_uint(fmaxf(x, 0.f)) > vstar) agt += quant(x);
   }
-  part[tid] = mine;
-  __syncthreads();
-  if (tid == 0) {  // exclusive prefix of the per-thread sums, and the row total
-    double run = 0.0;
-    for (int t = 0; t < kRrThreads; ++t) {
-      const double x = part[t];
-      part[t] = run;
-      run += x;
-    }
-    s_total = run;
-  }
-  __syncthreads();
-  const double total = s_total;
-  const double target = (double)p.tau * total;
-  double run = part[tid];
-  for (int e = 0; e < per; ++e) {
-    const float v = key[i0 + e];
-    if (v == -INFINITY) break;
-    run += (double)v;
-    if (run >= target) {
-      atomicMin(&cut, i0 + e);
-      break;
-    }
-  }
-  __syncthreads();
-  for (int i = tid; i <= cut; i += kRrThreads) {
-    const int n = idx[i];
-    atomicOr(&bits[n >> 6], 1ull << (n & 63));
-  }
-  __syncthreads();
+  agt = warp_sum_u64(agt);
+  const unsigned long long qv = quant(__uint_as_float(vstar));
+  // ties at v*: the first c_eq by index (T > agt here, and qv > 0)
+  const unsigned long long c_eq = (T > agt && qv > 0) ? (T - agt + qv - 1) / qv : 0ull;
   uint64_t* out = p.bits + (bh * p.nb + m) * p.wpr;
-  for (int w = tid; w < p.wpr; w += kRrThreads) {
-    uint64_t word = bits[w];
-    if (m == p.nb - 1) word = ~0ull;                       // Eq. 12, the last query block
-    if (p.sink_recent) {
-      if (w == 0) word |= 1ull;                            // first key block
-      if (w == (m >> 6)) word |= 1ull << (m & 63);         // diagonal block
+  unsigned long long ties_before = 0;
+  for (int w = 0; w < p.wpr; ++w) {
+    uint64_t word = 0;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int n = w * 64 + half * 32 + lane;
+      const float x = n < nb ? row[n] : -1.f;
+      const uint32_t kx = __float_as_uint(fmaxf(x, 0.f));
+      const bool tie = n < nb && kx == vstar;
+      const uint32_t tie_mask = __ballot_sync(0xffffffffu, tie);
+      const unsigned long long rank = ties_before + __popc(tie_mask & ((1u << lane) - 1u));
+      const bool keep = n < nb && (kx > vstar || (tie && rank < c_eq));
+      const uint32_t keep_mask = __ballot_sync(0xffffffffu, keep);
+      word |= (uint64_t)keep_mask << (32 * half);
+      ties_before += __popc(tie_mask);
     }
-    // Eq. 5: nothing above the diagonal (n <= m), nothing past the last block
-    const int lo = w * 64;
-    const int hi_keep = min(m, p.nb - 1) - lo;             // highest kept bit in this word
+    if (m == nb - 1) word = ~0ull;                     // Eq. 12, the last query block
+    if (p.sink_recent) {
+      if (w == 0) word |= 1ull;                        // first key block
+      if (w == (m >> 6)) word |= 1ull << (m & 63);     // diagonal block
+    }
+    // Eq. 5: nothing above the diagonal (n <= m)
+    const int hi_keep = m - w * 64;                    // highest kept bit in this word
     if (hi_keep < 0) word = 0ull;
     else if (hi_keep < 63) word &= (2ull << hi_keep) - 1ull;
-    out[w] = word;
+    if (lane == 0) out[w] = word;
   }
 }
 
@@ -372,8 +413,8 @@ cudaError_t launch_scores_one(const RrParams& p, cudaStream_t stream) {
   auto kern = rr_scores_kernel<D, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)((p.n_s + kTile - 1) / kTile), (unsigned)p.BH);
-  kern<<<grid, kRrThreads, smem, stream>>>(p);
+  dim3 grid((unsigned)((p.n_s + kRrQTiles * kTile - 1) / (kRrQTiles * kTile)), (unsigned)p.BH);
+  kern<<<grid, kRrScoreThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -382,12 +423,9 @@ cudaError_t launch_scores_one(const RrParams& p, cudaStream_t stream) {
 size_t rr_scores_smem_bytes(int d) {
   if (d != 64 && d != 128) return 0;
   const size_t tile = (size_t)kTile * d * 2;
-  return (1 + kRrStages) * tile + sizeof(RrBarriers) + 1024;
+  return (kRrQTiles + kRrStages) * tile + sizeof(RrBarriers) + 1024;
 }
 
-size_t rr_topk_smem_bytes(int p2, int wpr) {
-  return (size_t)kRrThreads * sizeof(double) + (size_t)wpr * sizeof(uint64_t) + (size_t)p2 * (sizeof(float) + sizeof(int));
-}
 
 cudaError_t launch_rr_stride_sum(const RrSumParams& p, cudaStream_t stream) {
   const int64_t total = (int64_t)p.BH * p.n_s * (p.d / 8);
@@ -406,11 +444,9 @@ cudaError_t launch_rr_scores(const RrParams& p, int d, cudaStream_t stream) {
 }
 
 cudaError_t launch_rr_topk(const RrTopParams& p, cudaStream_t stream) {
-  const size_t smem = rr_topk_smem_bytes(p.p2, p.wpr);
-  cudaError_t e = cudaFuncSetAttribute(rr_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)p.nb, (unsigned)p.BH);
-  rr_topk_kernel<<<grid, kRrThreads, smem, stream>>>(p);
+  const int rows_per_cta = kRrThreads / 32;
+  dim3 grid((unsigned)((p.nb + rows_per_cta - 1) / rows_per_cta), (unsigned)p.BH);
+  rr_topk_kernel<<<grid, kRrThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
