@@ -309,6 +309,24 @@ def run_gpu(args):
                     "ms": round(med, 4), "tflops": round(tf, 1), "pct_peak": round(100 * tf / peaks["bf16_tflops"], 1),
                     "pairs": pr, "hbm_gbs_min_traffic": round((in_bytes + out_bytes) / (med * 1e-3) / 1e9, 1),
                     "l2": "inputs > L2" if in_bytes > 2 * 129e6 else "flushed (512 MiB write) before each run"}
+            if name == "bsparse128k":
+                # RRAttention's block selection on the same inputs (stride 8,
+                # block 128, tau 0.95): algorithmic work = Eq. 8's product,
+                # 2 d (L/S)^2 FLOPs per head (the kernel forms it twice:
+                # one pass for the row log-sum-exp, one for the block sums)
+                S_rr, bs_rr, tau_rr = 8, 128, 0.95
+                med, _ = time_kernel(lambda: mattn.rr_select(qx, kx, S_rr, bs_rr, tau_rr), 5, 3)
+                ns = wlx.N // S_rr
+                fl = 2.0 * wlx.d * ns * ns * wlx.B * wlx.H
+                bits, _ = mattn.rr_select(qx, kx, S_rr, bs_rr, tau_rr)
+                nbk = wlx.N // bs_rr
+                kept = int(np.unpackbits(bits.cpu().numpy().view(np.uint8)).sum())
+                workloads[f"{name}/rr_select_s8_b128_tau0.95"] = {
+                    "ms": round(med, 4), "tflops_eq8": round(fl / (med * 1e-3) / 1e12, 1),
+                    "kept_causal_block_fraction": round(kept / (wlx.B * wlx.H * nbk * (nbk + 1) / 2), 4),
+                    "share_of_attention_step": round(med / workloads[f"{name}/{wlx.masks[0]}"]["ms"], 4),
+                    "l2": "inputs > L2"}
+                del bits
             del qx, kx, vx
             torch.cuda.empty_cache()
         rc, word = mattn.device_status()
