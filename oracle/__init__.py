@@ -32,6 +32,7 @@ from .dense import (  # noqa: F401
     attention,
     attention_probabilities,
     dense_mask_strip,
+    received_attention,
     tile_list,
     pair_count,
 )

@@ -71,3 +71,33 @@ def attention_head(q, k, v, kind, param=0, perm=None, block=None, sink=None):
         o_rows.append([x / denom for x in row])
         lses.append(top + math.log(denom))
     return o_rows, lses
+
+
+def received_head(q, k, kind, param=0, perm=None, block=None, sink=None):
+    """Column sums of one head's attention matrix: for each key token j, the
+    sum over query tokens i of the weight row i gives j (SHS slides, the
+    received-attention slide).  The weights come from the same neighbour
+    sets and sink as ``attention_head``; lists in, list out."""
+    n = len(q)
+    d = len(q[0])
+    pos_of_token = list(range(n))
+    if perm is not None:
+        for p, t in enumerate(perm):
+            pos_of_token[int(t)] = p
+    received = [0.0] * n
+    for i in range(n):
+        nb = neighbour_set(kind, param, n, pos_of_token[i], pos_of_token, block)
+        scores = []
+        for j in nb:
+            acc = 0.0
+            for c in range(d):
+                acc += float(q[i][c]) * float(k[j][c])
+            scores.append(acc / math.sqrt(d))
+        if not scores and sink is None:
+            continue
+        logits = list(scores) + ([float(sink)] if sink is not None else [])
+        top = max(logits)
+        denom = sum(math.exp(s - top) for s in logits)
+        for s, j in zip(scores, nb):
+            received[j] += math.exp(s - top) / denom
+    return received

@@ -224,6 +224,50 @@ def attention_probabilities(q, k, spec, b: int, h: int,
     return np.where(z[:, None] > 0, e / np.where(z > 0, z, 1.0)[:, None], 0.0)
 
 
+def received_attention(q, k, spec, heads: Optional[Iterable[Tuple[int, int]]] = None,
+                       cols: Optional[Sequence[int]] = None,
+                       scale: Optional[float] = None, row_block: int = 256):
+    """Received attention r_h(j) = sum_i a_ij, the column sums of the
+    attention matrix (SHS slides, the "received attention" slide: every row
+    of the matrix sums to 1, a column sums to the votes token j receives
+    from the queries that may see it).  a_ij is the weight the forward
+    gives key j in row i, so with a sink the rows sum to Z_i/(Z_i + exp(s_aux))
+    and the sink's share is not received by any token.
+
+    Steps per head: the forward's log-sum-exp lse_i of every row (all N
+    rows; ``attention`` above), then r_j = sum over rows i that may see j of
+    exp(s_ij - lse_i).  ``cols``: caller token indices to return (default
+    all).  Returns float64 [len(heads), len(cols)].
+    """
+    q = np.asarray(q)
+    k = np.asarray(k)
+    bsz, nh, n, d = q.shape
+    if heads is None:
+        heads = [(b, h) for b in range(bsz) for h in range(nh)]
+    heads = list(heads)
+    cols = np.arange(n) if cols is None else np.asarray(cols, dtype=np.int64)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = np.zeros((len(heads), len(cols)), dtype=np.float64)
+    zeros_v = np.zeros((bsz, nh, n, 1))
+    for hi, (b, h) in enumerate(heads):
+        _, lse = attention(q, k, zeros_v, spec, heads=[(b, h)], scale=scale, row_block=row_block)
+        lse = lse[0]
+        kh = np.asarray(k[b, h][cols], dtype=np.float64)
+        pos = inverse_permutation(_head_perm(spec, h), n)
+        param = _head_param(spec, h)
+        blk = _head_block(spec, h)
+        for r0 in range(0, n, row_block):
+            r = np.arange(r0, min(n, r0 + row_block))
+            qh = np.asarray(q[b, h][r], dtype=np.float64)
+            s = scale * (qh @ kh.T)
+            keep = allowed(spec.kind, param, pos[r][:, None], pos[cols][None, :], blk)
+            fin = np.isfinite(lse[r])[:, None]
+            a = np.where(keep & fin, np.exp(np.where(keep, s, 0.0) - np.where(fin, lse[r][:, None], 0.0)), 0.0)
+            out[hi] += a.sum(axis=0)
+    return out
+
+
 def dense_mask_strip(spec, h: int, n: int, p0: int, p1: int) -> np.ndarray:
     """Rows p0..p1-1 of the mask M in *position* space, bool [p1-p0, n]."""
     p = np.arange(p0, p1, dtype=np.int64)[:, None]

@@ -355,3 +355,68 @@ def test_tile_counts_closed_forms(n, kind, param):
         assert (nf, npart) == _tile_closed_form_causal(nt, param // 128)
     else:
         assert (nf, npart) == (nt * (param // 128), 0)
+
+
+# -- received attention ------------------------------------------------------
+
+@pytest.mark.parametrize("kind,param", [("full", 0), ("chunk", 8), ("sliding", 5), ("causal_window", 9)])
+def test_received_attention_conserves_row_mass(kind, param):
+    """Every row of the attention matrix sums to 1 (SHS slides), so the
+    column sums add up to N (catches summing rows instead of columns, or a
+    missing normalisation)."""
+    n = 40
+    q, k = _rand((1, 1, n, 6), 1), _rand((1, 1, n, 6), 2)
+    r = dense.received_attention(q, k, _one_head(kind, param))[0]
+    assert r.sum() == pytest.approx(n, rel=1e-12)
+    assert (r >= 0).all()
+
+
+def test_received_attention_chunks_keep_their_mass():
+    """Chunk mask: queries only see their own chunk, so each chunk's columns
+    receive exactly C (catches leakage across chunk borders)."""
+    n, c = 48, 12
+    q, k = _rand((1, 1, n, 5), 3), _rand((1, 1, n, 5), 4)
+    r = dense.received_attention(q, k, _one_head("chunk", c))[0]
+    np.testing.assert_allclose(r.reshape(n // c, c).sum(axis=1), c, rtol=1e-12)
+
+
+def test_received_attention_zero_query_closed_forms():
+    """q = 0 makes every visible score equal, so a_ij = 1/|N(i)| (plus the
+    sink: 1/(|N(i)| + e^b)).  Causal (W >= N): r_j = sum_{i>=j} 1/(i+1) =
+    H_N - H_j; sliding w: r_j = sum over |i-j| <= w of 1/|N(i)| with
+    |N(i)| = min(n-1, i+w) - max(0, i-w) + 1 counted by hand; the sink share
+    is what the columns no longer receive (catches a transposed mask or a
+    sink that adds to the columns)."""
+    n, w, b = 30, 4, 0.7
+    q = np.zeros((1, 1, n, 3))
+    k = _rand((1, 1, n, 3), 5)
+    r = dense.received_attention(q, k, _one_head("causal_window", n + 5))[0]
+    harm = np.concatenate([[0.0], np.cumsum(1.0 / np.arange(1, n + 1))])
+    np.testing.assert_allclose(r, harm[n] - harm[np.arange(n)], rtol=1e-12)
+    size = np.array([min(n - 1, i + w) - max(0, i - w) + 1 for i in range(n)], dtype=float)
+    want = np.array([sum(1.0 / size[i] for i in range(max(0, j - w), min(n - 1, j + w) + 1)) for j in range(n)])
+    np.testing.assert_allclose(dense.received_attention(q, k, _one_head("sliding", w))[0], want, rtol=1e-12)
+    want_sink = np.array([sum(1.0 / (size[i] + math.exp(b)) for i in range(max(0, j - w), min(n - 1, j + w) + 1))
+                          for j in range(n)])
+    np.testing.assert_allclose(dense.received_attention(q, k, _one_head("sliding", w, sink=b))[0], want_sink,
+                               rtol=1e-12)
+
+
+@pytest.mark.parametrize("kind,param", [("full", 0), ("chunk", 4), ("sliding", 3), ("causal_window", 5),
+                                        ("block", 4)])
+def test_received_attention_matches_brute_force(kind, param):
+    """The fp64 column sums against the pure-Python loops, with a token
+    order and a sink (catches an ordering slip between positions and tokens)."""
+    n = 16
+    q, k = _rand((1, 1, n, 4), 6), _rand((1, 1, n, 4), 7)
+    perm = np.random.default_rng(8).permutation(n)
+    block = None
+    if kind == "block":
+        block = np.random.default_rng(9).random((n // param, n // param)) < 0.6
+        np.fill_diagonal(block, True)
+    for pm, sink in ((None, None), (perm, -0.4)):
+        spec = _one_head(kind, param, perm=pm, block=block, sink=sink)
+        r = dense.received_attention(q, k, spec)[0]
+        rb = brute.received_head(q[0, 0].tolist(), k[0, 0].tolist(), kind, param, perm=pm,
+                                 block=None if block is None else block.tolist(), sink=sink)
+        np.testing.assert_allclose(r, rb, rtol=1e-12, atol=1e-15)
