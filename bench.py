@@ -364,6 +364,41 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------------------ other stages (profiling aid)
+def run_stage(args):
+    """Time RRAttention's block selection (stride 8, block 128, tau 0.95) or
+    the received attention on the headline workload's inputs: warm-up, then
+    ``steps`` timed calls; one short JSON line."""
+    import dataclasses
+
+    import torch
+
+    import block_sparse_attention_masked_gb300 as mattn
+    from workloads import WORKLOADS, make_mask, make_workload_inputs
+
+    torch.cuda.set_device(0)
+    wl = WORKLOADS[args.workload or HEADLINE[0]]
+    if args.n or args.heads:
+        wl = dataclasses.replace(wl, N=args.n or wl.N, H=args.heads or wl.H)
+    q, k, v = make_workload_inputs(wl, seed=0, device="cuda")
+    if args.stage == "rr_select":
+        def fn():
+            mattn.rr_select(q, k, 8, 128, 0.95)
+    else:
+        mask = mattn.prepare(make_mask(wl, args.mask or HEADLINE[1], seed=0), wl.H, wl.N)
+        _, lse = mattn.attention(q, k, v, mask)
+        r = torch.empty_like(lse)
+
+        def fn():
+            mattn.received(q, k, lse, mask, out=r)
+    med, times = time_kernel(fn, args.steps, args.warmup)
+    rc, word = mattn.device_status()
+    if rc != 0:
+        raise RuntimeError(f"device error word {word:#x}")
+    print(json.dumps({"stage": args.stage, "workload": wl.name,
+                      "N": wl.N, "H": wl.H, "d": wl.d, "ms_median": round(med, 4), "steps": args.steps}), flush=True)
+
+
 # ------------------------------------------------------------------ oracle (CPU) arm
 def oracle_sample(seconds_target: float = 15.0):
     """Time the oracle on sampled rows of head 0 of the headline workload.
@@ -463,11 +498,16 @@ def main():
     ap.add_argument("--mask", default=None, help="mask of that workload")
     ap.add_argument("--n", type=int, default=0, help="shrink N (profiling cases)")
     ap.add_argument("--heads", type=int, default=0, help="shrink H (profiling cases)")
+    ap.add_argument("--stage", default="attention", choices=["attention", "rr_select", "received"],
+                    help="profiling aid: time one other stage on the headline inputs instead of the step "
+                         "(prints a short line, not the benchmark record)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.stage != "attention":
+        run_stage(args)
     else:
         run_gpu(args)
 

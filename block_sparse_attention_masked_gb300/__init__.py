@@ -71,7 +71,8 @@ class MaskDesc(ctypes.Structure):
 
 
 EXPORTS = (
-    "mattn_fwd", "mattn_fwd_host", "mattn_fwd_noalloc", "mattn_rr_select", "mattn_count_pairs", "mattn_plan_tiles", "mattn_plan_tiles_device",
+    "mattn_fwd", "mattn_fwd_host", "mattn_fwd_noalloc", "mattn_rr_select", "mattn_received",
+    "mattn_count_pairs", "mattn_plan_tiles", "mattn_plan_tiles_device",
     "mattn_device_status", "mattn_set_wait_timeout_ns", "mattn_status_string", "mattn_last_error",
     "mattn_version",
 )
@@ -96,6 +97,7 @@ def lib() -> ctypes.CDLL:
                                     ctypes.POINTER(ctypes.c_uint32)]
     L.mattn_rr_select.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i32, ctypes.c_float, ctypes.c_uint32,
                                   vp, vp, vp]
+    L.mattn_received.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, dp, vp]
     L.mattn_count_pairs.argtypes = [dp, i32, i32, i32, u64p]
     L.mattn_plan_tiles.argtypes = [dp, i32, i32, vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]
     L.mattn_plan_tiles_device.argtypes = [dp, i32, i32, vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t), vp]
@@ -106,7 +108,8 @@ def lib() -> ctypes.CDLL:
     L.mattn_last_error.restype = ctypes.c_char_p
     L.mattn_last_error.argtypes = []
     L.mattn_version.argtypes = []
-    for name in ("mattn_fwd", "mattn_fwd_host", "mattn_fwd_noalloc", "mattn_rr_select", "mattn_count_pairs", "mattn_plan_tiles",
+    for name in ("mattn_fwd", "mattn_fwd_host", "mattn_fwd_noalloc", "mattn_rr_select", "mattn_received",
+                 "mattn_count_pairs", "mattn_plan_tiles",
                  "mattn_plan_tiles_device", "mattn_device_status", "mattn_set_wait_timeout_ns",
                  "mattn_version"):
         getattr(L, name).restype = ctypes.c_int
@@ -338,6 +341,29 @@ class DeviceBlockMask:
         self._keep = (bits, sink)
         self.desc = d
         self.H, self.N, self.kind = H, N, "block"
+
+
+def received(q, k, lse, mask, out=None, stream=None):
+    """Received attention r [B, H, N] (fp32, caller token order): the column
+    sums of the attention matrix of the forward that wrote ``lse`` with the
+    same q, k and mask."""
+    import torch
+
+    if not (q.is_cuda and k.is_cuda and lse.is_cuda):
+        raise ValueError("q, k and lse must be CUDA tensors")
+    for t in (q, k, lse):
+        if not t.is_contiguous():
+            raise ValueError("q, k and lse must be contiguous")
+    B, H, N, d = q.shape
+    if k.shape != q.shape or k.dtype != q.dtype or tuple(lse.shape) != (B, H, N) or lse.dtype != torch.float32:
+        raise ValueError("k must match q; lse must be fp32 [B, H, N]")
+    if out is None:
+        out = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    _check(lib().mattn_received(q.data_ptr(), k.data_ptr(), lse.data_ptr(), out.data_ptr(), B, H, N, d,
+                                _dtype_code(q), ctypes.byref(mask.desc), stream))
+    return out
 
 
 def attention_host(q, k, v, spec_or_mask, out=None, lse=None, stream=None):

@@ -95,6 +95,28 @@ cudaError_t launch_rr_scores(const RrParams& p, int d, cudaStream_t stream);
 cudaError_t launch_rr_topk(const RrTopParams& p, cudaStream_t stream);
 size_t rr_scores_smem_bytes(int d);
 
+// Received attention (received.cu).
+struct RecvParams {
+  CUtensorMap tq[2], tk[2];   // [B*H][N][d] views (map [1]: the 16/32-column rest)
+  CUtensorMap cq[2], ck[2];   // column-major views [B*H][rows][cols][d]
+  float* lse2p;               // workspace [B*H][lse_pitch]: lse in position order, log2 domain
+  float* r;                   // out: [B][H][N] received attention, caller token order
+  const int32_t* head_info;   // [H][4], HeadField
+  const int32_t* perm;        // explicit orders [n_perm][N]
+  const uint64_t* block_bits; // [block_heads][Nb][wpr]
+  uint32_t* err;
+  unsigned long long timeout_ns;
+  int64_t lse_pitch;          // a multiple of 128 >= N
+  int B, H, N;
+  int kind;
+  int block_heads, block_wpr, block_c, block_nb;
+  int grid_rows, grid_cols;
+  float scale_log2;
+};
+
+cudaError_t launch_received(const RecvParams& p, const float* lse, int d, cudaStream_t stream);
+size_t received_smem_bytes(int d);
+
 // Launchers (attention_fwd.cu).
 cudaError_t launch_attention(const FwdParams& p, int d, bool out_f32, cudaStream_t stream);
 size_t attention_smem_bytes(int d);

@@ -248,6 +248,7 @@ struct DeviceState {
   DeviceBuf dump;      // plan dump
   DeviceBuf rr_ksum;   // block selection: stride key sums
   DeviceBuf rr_scores; // block selection: block scores when the caller passes none
+  DeviceBuf recv_lse;  // received attention: the lse in position order
   std::map<std::string, std::unique_ptr<Plan>> plans;
 };
 
@@ -644,6 +645,71 @@ int mattn_fwd_host(const void* q, const void* k, const void* v, void* o, float* 
   MATTN_CUDA(cudaMemcpyAsync(o, dout, tensor, cudaMemcpyDeviceToHost, stream), "copy o");
   if (lse) MATTN_CUDA(cudaMemcpyAsync(lse, dlse, lse_bytes, cudaMemcpyDeviceToHost, stream), "copy lse");
   MATTN_CUDA(cudaStreamSynchronize(stream), "stream sync");
+  return MATTN_OK;
+}
+
+int mattn_received(const void* q, const void* k, const float* lse, float* r, int B, int H, int N, int d, int dtype,
+                   const mattn_mask_desc* desc, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  std::lock_guard<std::mutex> lk(g_mutex);
+  Normalized n;
+  int rc = normalize(desc, B, H, N, d, dtype, true, &n);
+  if (rc) return rc;
+  if (!q || !k || !lse || !r) return fail(MATTN_ERR_INVALID_ARG, "q, k, lse and r must be non-NULL");
+  if (!aligned16(q) || !aligned16(k)) return fail(MATTN_ERR_UNSUPPORTED, "q and k must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(r) & 3u))
+    return fail(MATTN_ERR_INVALID_ARG, "lse and r must be 4-byte aligned");
+  DeviceState* st = nullptr;
+  if ((rc = device_state(&st))) return rc;
+  if ((rc = get_encoder())) return rc;
+  Plan* plan = nullptr;
+  if ((rc = get_plan(st, n, stream, &plan))) return rc;
+  const size_t elems = (size_t)B * H * N * d;
+  const void* use[2] = {q, k};
+  if (n.need_copy) {
+    if ((rc = st->copy.reserve(3 * elems * 2, "cudaMalloc(reorder workspace)"))) return rc;
+    GatherParams gp;
+    memset(&gp, 0, sizeof(gp));
+    const void* src[3] = {q, k, k};
+    for (int t = 0; t < 3; ++t) {
+      gp.src[t] = src[t];
+      gp.dst[t] = static_cast<char*>(st->copy.ptr) + (size_t)t * elems * 2;
+    }
+    use[0] = gp.dst[0];
+    use[1] = gp.dst[1];
+    gp.head_info = plan->head_info;
+    gp.perm = desc->perm;
+    gp.B = B; gp.H = H; gp.N = N; gp.d = d;
+    gp.src_f32 = dtype == MATTN_F32;
+    gp.grid_rows = desc->grid_rows;
+    gp.grid_cols = desc->grid_cols;
+    MATTN_CUDA(launch_gather(gp, stream), "gather launch");
+  }
+  RecvParams p;
+  memset(&p, 0, sizeof(p));
+  const int rows = n.any_colmajor_tma ? desc->grid_rows : 0;
+  const int cols = n.any_colmajor_tma ? desc->grid_cols : 0;
+  if ((rc = make_maps(n, use[0], p.tq, p.cq, rows, cols))) return rc;
+  if ((rc = make_maps(n, use[1], p.tk, p.ck, rows, cols))) return rc;
+  p.lse_pitch = ((int64_t)N + 127) / 128 * 128;
+  if ((rc = st->recv_lse.reserve((size_t)B * H * p.lse_pitch * sizeof(float), "cudaMalloc(received lse)"))) return rc;
+  p.lse2p = static_cast<float*>(st->recv_lse.ptr);
+  p.r = r;
+  p.head_info = plan->head_info;
+  p.perm = desc->perm;
+  p.block_bits = n.kind == kBlockSparse ? desc->block_bits : nullptr;
+  p.err = st->err;
+  p.timeout_ns = wait_timeout_ns();
+  p.B = B; p.H = H; p.N = N;
+  p.kind = n.kind;
+  p.block_heads = n.block_heads;
+  p.block_wpr = n.block_wpr;
+  p.block_c = n.block_c;
+  p.block_nb = n.block_nb;
+  p.grid_rows = desc->grid_rows;
+  p.grid_cols = desc->grid_cols;
+  p.scale_log2 = n.scale * 1.4426950408889634f;
+  MATTN_CUDA(launch_received(p, lse, d, stream), "received attention launch");
   return MATTN_OK;
 }
 

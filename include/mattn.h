@@ -198,6 +198,28 @@ int mattn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, floa
                       const mattn_mask_desc* desc, void* stream, uint32_t* wait_error_out);
 
 /*
+ * mattn_received -- received attention, the column sums of the masked
+ * attention matrix ("Semantic Head Specialization Guides Hybrid ViT
+ * Attention for Multimodal LLMs" (SHS slides), the received-attention slide):
+ *   r[b,h,j] = sum over the queries i that may see j of a_ij,
+ *   a_ij     = exp(s_ij - lse[b,h,i]),
+ * where lse is the log-sum-exp mattn_fwd wrote for the same q, k and mask
+ * (so with a sink the rows sum to less than 1 and the sink's share is
+ * received by no token; for the mass without the sink, pass the lse of a
+ * forward without it).
+ *   q, k      DEVICE [B][H][N][d] as for mattn_fwd (same dtypes and orders).
+ *   lse       DEVICE fp32 [B][H][N], caller token order (mattn_fwd's output).
+ *   r         DEVICE fp32 [B][H][N] output, caller token order.
+ *   desc      the mask of the forward (the sink pointer is not read).
+ * Asynchronous on `stream`; library workspace (the lse in sequence-position
+ * order, reordered inputs when the forward needs them) is allocated on
+ * first use.
+ */
+int mattn_received(const void* q, const void* k, const float* lse, float* r,
+                   int B, int H, int N, int d, int dtype,
+                   const mattn_mask_desc* desc, void* stream);
+
+/*
  * mattn_rr_select -- RRAttention's dynamic block selection: the block-selection
  * bitmap B of every (batch entry, head), from Q and K ("RRAttention",
  * section 3, Eq. 6-12, with the causality of section 2.1, Eq. 5):
