@@ -328,6 +328,21 @@ def run_gpu(args):
                     "share_of_attention_step": round(med / workloads[f"{name}/{wlx.masks[0]}"]["ms"], 4),
                     "l2": "inputs > L2"}
                 del bits
+            if name in ("bsparse128k", "vit16384"):
+                # received attention (column sums of the attention matrix) of
+                # the workload's first mask, from the forward's LSE: one
+                # QK^T product per visible pair, 2 d FLOPs
+                m0 = wlx.masks[0]
+                mk = mattn.prepare(make_mask(wlx, m0, seed=0), wlx.H, wlx.N, device=dev)
+                _, lx = mattn.attention(qx, kx, vx, mk)
+                rx = torch.empty_like(lx)
+                med, _ = time_kernel(lambda: mattn.received(qx, kx, lx, mk, out=rx), 5 if name == "bsparse128k" else 20,
+                                     3, flush=None if name == "bsparse128k" else flush)
+                pr = workloads[f"{name}/{m0}"]["pairs"]
+                workloads[f"{name}/received_{m0}"] = {
+                    "ms": round(med, 4), "tflops_qk": round(2.0 * wlx.d * pr / (med * 1e-3) / 1e12, 1),
+                    "pct_peak": round(100 * 2.0 * wlx.d * pr / (med * 1e-3) / 1e12 / peaks["bf16_tflops"], 1)}
+                del lx, rx
             del qx, kx, vx
             torch.cuda.empty_cache()
         rc, word = mattn.device_status()
