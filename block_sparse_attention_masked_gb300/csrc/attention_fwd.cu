@@ -61,6 +61,22 @@ constexpr uint32_t kRegsControl = 72;
 constexpr uint32_t kRegsSoftmax = 216;
 static_assert(kRegsControl + 2 * kRegsSoftmax == 3 * 168, "register split must match the launch budget");
 
+// The CTA's key-tile list: entry j (0 <= j < n) is key tile kt(j).  Paired,
+// sub-tile s multiplies entry j when uses(j, s); split, entry j belongs to
+// pipeline j % 2.  Interval kinds: the entries are the key tiles lo .. lo +
+// n - 1 (the union of the sub-tiles' ranges, which overlap or touch), each
+// sub-tile using its own range.  Block kind: the entries sit in shared
+// memory as kt | use0 << 30 | use1 << 31, built once per CTA.  Reading an
+// entry is one add or one shared load, which keeps the loops of the
+// copy and MMA warps short.
+struct TileList {
+  int n, lo;
+  int lo0, hi0, lo1, hi1;
+  int use_n0, use_n1;  // block kind: entries sub-tile 0 / 1 uses
+  const uint32_t* e;
+  bool block;
+};
+
 struct Barriers {
   uint64_t q_full[2];
   uint64_t k_full[3], k_empty[3];
@@ -73,21 +89,21 @@ struct Barriers {
   uint32_t tmem_base;
   int abort_flag;
   uint32_t mma_turn;    // ticket of the MMA group that may be issued next
+  int list_n[3];        // block kind: entries of the CTA's key-tile list, and per sub-tile
+  TileList tl;          // the CTA's key-tile list (read by every role from shared memory)
   float xch[2][3][kTile];  // split schedule: per sub-tile (m, l, tile count) of each row
 };
 
-// Block-selection rows of up to this many 64-bit words (N <= 2^21 at
-// Bs = 128) are staged in shared memory; longer rows are read in place.
-constexpr int kMaxRowWords = 256;
+// Capacity of the per-CTA key-tile list of block-sparse masks (a query
+// tile sees at most N/128 key tiles, so N <= 128 * kMaxList).
+constexpr int kMaxList = kBlockListMax;
 
-// Key-tile walk of one 128-row query sub-tile.
+// Key-tile plan of one 128-row query sub-tile.
 struct SubPlan {
   int qt;
   bool rows;                 // the sub-tile has query rows (< N)
-  bool has_tiles;            // and at least one key tile
   KRange r;                  // interval kinds
-  int ktmax;                 // block kind: last admissible key tile
-  const uint64_t* row;       // block kind: the sub-tile's bitmap row
+  int ktmax;                 // block kind: last admissible key tile (causality)
 };
 
 // Work description of one CTA, computed identically by every thread.
@@ -95,33 +111,6 @@ struct ItemPlan {
   int bh, h, b;
   SubPlan sp0, sp1;
 };
-
-__device__ __forceinline__ int sub_next(const FwdParams& p, const SubPlan& sp, int from) {
-  if (!sp.rows) return kNoTile;
-  if (p.kind == kBlockSparse) return block_row_next_kt(sp.row, p.block_c, from, sp.ktmax);
-  int kt = from > sp.r.lo ? from : sp.r.lo;
-  return kt <= sp.r.hi ? kt : kNoTile;
-}
-
-__device__ __forceinline__ bool sub_uses(const FwdParams& p, const SubPlan& sp, int kt) {
-  if (!sp.rows) return false;
-  if (p.kind == kBlockSparse) return kt <= sp.ktmax && block_row_bit(sp.row, kt / p.block_c);
-  return kt >= sp.r.lo && kt <= sp.r.hi;
-}
-
-__device__ __forceinline__ bool sub_partial(const FwdParams& p, const SubPlan& sp, int kt) {
-  if (p.kind == kBlockSparse) return block_tile_class(sp.qt, kt, p.N) == kTilePartial;
-  return interval_tile_class(sp.r, kt) == kTilePartial;
-}
-
-// Next key tile of the CTA's list: the union of both sub-tiles' tiles when
-// paired, the one query tile's tiles when split.
-__device__ __forceinline__ int union_next(const FwdParams& p, const ItemPlan& ip, int from) {
-  int a = sub_next(p, ip.sp0, from);
-  if (p.split) return a;
-  int c = sub_next(p, ip.sp1, from);
-  return a < c ? a : c;
-}
 
 // Query tile of sub-tile s of work item `it`.
 __device__ __forceinline__ int item_qt(const FwdParams& p, int2 it, int s) { return p.split ? it.y : 2 * it.y + s; }
@@ -134,33 +123,146 @@ __device__ __forceinline__ const uint64_t* global_row(const FwdParams& p, int2 i
   return p.block_bits + ((int64_t)hb * p.block_nb + qt / p.block_c) * p.block_wpr;
 }
 
-__device__ __forceinline__ SubPlan make_subplan(const FwdParams& p, int2 it, int s, int param,
-                                                const uint64_t* staged_rows) {
+__device__ __forceinline__ SubPlan make_subplan(const FwdParams& p, int2 it, int s, int param) {
   SubPlan sp;
   const int nt = (p.N + kTile - 1) / kTile;
   sp.qt = item_qt(p, it, s);
   sp.rows = sp.qt < nt;
   sp.ktmax = sp.qt < nt ? sp.qt : nt - 1;
-  sp.row = nullptr;
-  if (p.kind != kBlockSparse) {
+  if (p.kind != kBlockSparse && sp.rows) {
     sp.r = interval_krange(p.kind, param, p.N, sp.qt);
   } else {
-    sp.r.lo = 0; sp.r.hi = -1; sp.r.flo = 0; sp.r.fhi = -1;
-    if (sp.rows) sp.row = staged_rows ? staged_rows + (p.split ? 0 : s) * kMaxRowWords : global_row(p, it, s);
+    sp.r.lo = 1; sp.r.hi = 0; sp.r.flo = 0; sp.r.fhi = -1;  // empty
   }
-  sp.has_tiles = sub_next(p, sp, 0) != kNoTile;
   return sp;
 }
 
-__device__ __forceinline__ ItemPlan make_plan(const FwdParams& p, int2 it, const uint64_t* staged_rows) {
+__device__ __forceinline__ ItemPlan make_plan(const FwdParams& p, int2 it) {
   ItemPlan ip;
   ip.bh = it.x;
   ip.h = it.x % p.H;
   ip.b = it.x / p.H;
   const int param = p.head_info[ip.h * 4 + kHeadParam];
-  ip.sp0 = make_subplan(p, it, 0, param, staged_rows);
-  ip.sp1 = make_subplan(p, it, 1, param, staged_rows);
+  ip.sp0 = make_subplan(p, it, 0, param);
+  ip.sp1 = make_subplan(p, it, 1, param);
   return ip;
+}
+
+__device__ __forceinline__ int list_kt(const TileList& L, int j) {
+  return L.block ? (int)(L.e[j] & 0x3fffffffu) : L.lo + j;
+}
+
+__device__ __forceinline__ bool list_uses(const TileList& L, int j, int s) {
+  if (L.block) return (L.e[j] >> (30 + s)) & 1u;
+  const int kt = L.lo + j;
+  return s ? (kt >= L.lo1 && kt <= L.hi1) : (kt >= L.lo0 && kt <= L.hi0);
+}
+
+// Whether sub-tile s (split: pipeline s, which shares the one query tile)
+// has any key tile: its Q tile is loaded and waited for only then.
+__device__ __forceinline__ bool list_has(const TileList& L, int s, bool split) {
+  if (split) return L.n > 0;
+  if (L.block) return (s ? L.use_n1 : L.use_n0) > 0;
+  return s ? L.lo1 <= L.hi1 : L.lo0 <= L.hi0;
+}
+
+__device__ __forceinline__ TileList make_list(const FwdParams& p, const ItemPlan& ip, const uint32_t* entries,
+                                              const int* block_counts) {
+  TileList L;
+  L.block = p.kind == kBlockSparse;
+  L.e = entries;
+  L.use_n0 = L.block ? block_counts[1] : 0;
+  L.use_n1 = L.block ? block_counts[2] : 0;
+  L.lo0 = ip.sp0.r.lo; L.hi0 = ip.sp0.r.hi;
+  L.lo1 = ip.sp1.r.lo; L.hi1 = ip.sp1.r.hi;
+  if (L.block) {
+    L.n = block_counts[0];
+    L.lo = 0;
+  } else {
+    const bool e0 = L.lo0 <= L.hi0, e1 = L.lo1 <= L.hi1;
+    L.lo = e0 ? (e1 ? min(L.lo0, L.lo1) : L.lo0) : L.lo1;
+    const int hi = e0 ? (e1 ? max(L.hi0, L.hi1) : L.hi0) : L.hi1;
+    L.n = (e0 || e1) ? hi - L.lo + 1 : 0;
+  }
+  return L;
+}
+
+__device__ __forceinline__ bool sub_partial(const FwdParams& p, const SubPlan& sp, int kt) {
+  if (p.kind == kBlockSparse) return block_tile_class(sp.qt, kt, p.N) == kTilePartial;
+  return interval_tile_class(sp.r, kt) == kTilePartial;
+}
+
+// Block kind: one warp writes the CTA's entries to `list` (ascending key
+// tiles; the union of the sub-tiles' kept tiles at or below their
+// diagonals) and counts[0..2] = their number and the entries sub-tile 0 and
+// sub-tile 1 use.
+// Lanes take 64-bit words of the bitmap rows, a warp prefix sum of their
+// tile counts gives each lane its first output slot, and each lane then
+// writes its own words' tiles.
+__device__ __forceinline__ void build_block_list(const FwdParams& p, int2 item, const ItemPlan& ip, uint32_t* list,
+                                                 int* counts, int lane) {
+  const int c = p.block_c;
+  int used0 = 0, used1 = 0;
+  const int km0 = ip.sp0.rows ? ip.sp0.ktmax : -1;
+  const int km1 = ip.sp1.rows ? ip.sp1.ktmax : -1;
+  const int km = km0 > km1 ? km0 : km1;
+  int base = 0;
+  if (km >= 0) {
+    const uint64_t* row0 = km0 >= 0 ? global_row(p, item, 0) : nullptr;
+    const uint64_t* row1 = km1 >= 0 ? global_row(p, item, 1) : nullptr;
+    const int nb0 = km0 >= 0 ? km0 / c : -1, nb1 = km1 >= 0 ? km1 / c : -1;  // last block of each sub-tile
+    const int nbm = km / c;
+    const int nwords = nbm / 64 + 1;
+    auto keep_upto = [](int w, int nbl) -> uint64_t {  // bits n <= nbl of word w
+      const int hi = nbl - w * 64;
+      return hi < 0 ? 0ull : (hi >= 63 ? ~0ull : ((2ull << hi) - 1ull));
+    };
+    for (int w0 = 0; w0 < nwords; w0 += 32) {
+      const int w = w0 + lane;
+      uint64_t u0 = 0, u1 = 0;
+      if (w < nwords) {
+        if (row0) u0 = row0[w] & keep_upto(w, nb0);
+        if (row1) u1 = row1[w] & keep_upto(w, nb1);
+      }
+      const uint64_t U = u0 | u1;
+      // tiles from this word: c per kept block, fewer for the block holding km
+      int cnt = __popcll(U) * c;
+      if (w == nbm / 64 && ((U >> (nbm % 64)) & 1ull)) cnt -= c - (km - nbm * c + 1);
+      int incl = cnt;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      int pos = base + incl - cnt;
+      uint64_t bits = U;
+      while (bits) {
+        const int bpos = __ffsll((long long)bits) - 1;
+        bits &= bits - 1ull;
+        const int n = w * 64 + bpos;
+        for (int i = 0; i < c; ++i) {
+          const int kt = n * c + i;
+          if (kt > km) break;
+          const uint32_t use0 = (((u0 >> bpos) & 1ull) && kt <= km0) ? 1u : 0u;
+          const uint32_t use1 = (((u1 >> bpos) & 1ull) && kt <= km1) ? 1u : 0u;
+          list[pos++] = (uint32_t)kt | (use0 << 30) | (use1 << 31);
+          used0 += (int)use0;
+          used1 += (int)use1;
+        }
+      }
+      base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    used0 += __shfl_xor_sync(0xffffffffu, used0, off);
+    used1 += __shfl_xor_sync(0xffffffffu, used1, off);
+  }
+  if (lane == 0) {
+    counts[0] = base;
+    counts[1] = used0;
+    counts[2] = used1;
+  }
 }
 
 // Issue order of the MMA groups (a shared-memory word): the group with
@@ -342,22 +444,14 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
   uint8_t* sk = sq + 2 * G::kTileBytes;
   uint8_t* sv = sk + KS * G::kTileBytes;
   Barriers* bar = reinterpret_cast<Barriers*>(sv + VS * G::kTileBytes);
-  uint64_t* staged_rows = reinterpret_cast<uint64_t*>(bar + 1);  // [2][kMaxRowWords]
+  uint32_t* list_e = reinterpret_cast<uint32_t*>(bar + 1);  // block kind: [kMaxList] key-tile entries
   volatile int* abort_flag = &bar->abort_flag;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int2 item = p.items[blockIdx.x];
-  const bool stage_rows = p.kind == kBlockSparse && p.block_wpr <= kMaxRowWords;
-  if (stage_rows && (warp == 2 || (warp == 3 && !p.split))) {
-    // the bitmap rows this CTA walks, copied once to shared memory
-    const int s = warp - 2;
-    const int nt = (p.N + kTile - 1) / kTile;
-    if (item_qt(p, item, s) < nt) {
-      const uint64_t* src = global_row(p, item, s);
-      for (int w = lane; w < p.block_wpr; w += 32) staged_rows[s * kMaxRowWords + w] = src[w];
-    }
-  }
+  const ItemPlan ip = make_plan(p, item);
+  if (p.kind == kBlockSparse && warp == 2) build_block_list(p, item, ip, list_e, bar->list_n, lane);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
@@ -390,7 +484,9 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
   ptx::tc_fence_after();
   const uint32_t tmem = bar->tmem_base;
 
-  const ItemPlan ip = make_plan(p, item, stage_rows ? staged_rows : nullptr);
+  if (threadIdx.x == 0) bar->tl = make_list(p, ip, list_e, bar->list_n);
+  __syncthreads();
+  const TileList& L = bar->tl;
   const int load_mode = p.head_info[ip.h * 4 + kHeadLoad];
   const bool colmaj = load_mode == kLoadColumnMajor;
 
@@ -416,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
           const SubPlan& sp = s ? ip.sp1 : ip.sp0;
-          if (!sp.has_tiles || (p.split && s == 1)) continue;  // split: one Q tile for both pipelines
+          if (!list_has(L, s, p.split) || (p.split && s == 1)) continue;  // split: one Q tile for both pipelines
           ptx::mbar_arrive_expect_tx(&bar->q_full[s], G::kTileBytes);
           load_tile<D>(p, p.tq, p.cq, colmaj, sq + s * G::kTileBytes, &bar->q_full[s], sp.qt * kTile, ip.bh,
                        ptx::l2_policy_evict_first());
@@ -427,8 +523,8 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
       uint8_t* ring = is_k ? sk : sv;
       constexpr int S = KS;
       static_assert(KS == VS, "one ring depth for K and V");
-      int j = 0;
-      for (int kt = union_next(p, ip, 0); kt != kNoTile; kt = union_next(p, ip, kt + 1), ++j) {
+      for (int j = 0; j < L.n; ++j) {
+        const int kt = list_kt(L, j);
         const int slot = j % S;
         if (!ptx::mbar_wait(&empty[slot], ((j / S) & 1) ^ 1, p.timeout_ns, abort_flag)) {
           raise_error(p, bar, kErrProducer);
@@ -461,7 +557,6 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
     // instruction.
     ptx::setmaxnreg_dec<kRegsControl>();
     const int s = warp - 1;
-    const SubPlan sp = s ? ip.sp1 : ip.sp0;
     auto wait_all = [&](uint64_t* b, uint32_t parity) {
       return __all_sync(0xffffffffu, ptx::mbar_wait(b, parity, p.timeout_ns, abort_flag));
     };
@@ -477,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
       }
     }
     const int qs = p.split ? 0 : s;  // Q tile this sub-tile multiplies
-    if (ok && sp.has_tiles && !wait_all(&bar->q_full[qs], 0)) {
+    if (ok && list_has(L, s, p.split) && !wait_all(&bar->q_full[qs], 0)) {
       fail();
       ok = false;
     }
@@ -493,9 +588,9 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
     uint32_t pcount = 0;
     int j = 0;
     if (ok) {
-      for (int kt = union_next(p, ip, 0); kt != kNoTile; kt = union_next(p, ip, kt + 1), ++j) {
-        const bool use = p.split ? ((j & 1) == s) : sub_uses(p, sp, kt);
-        if (p.split && !use) continue;  // the other issuer's entry
+      // split: this issuer's entries are j = s, s + 2, ...
+      for (j = p.split ? s : 0; j < L.n; j += p.split ? 2 : 1) {
+        const bool use = p.split || list_uses(L, j, s);
         const int ks = j % KS;
         // the V slot read and released at this step: the previous entry
         // (paired), the pending product's entry (split)
@@ -594,9 +689,10 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
     float l = 0.f;        // running sum of exp2(x - m) in fp32
     int count = 0;  // key tiles this sub-tile has processed
     bool ok = true;
-    int jj = 0;     // entry of the CTA's list
-    for (int kt = sub_next(p, sp, 0); kt != kNoTile; kt = sub_next(p, sp, kt + 1), ++jj) {
-      if (p.split && (jj & 1) != s) continue;  // dealt to the other pipeline
+    // entries of the CTA's list this sub-tile (split: pipeline) multiplies
+    for (int jj = p.split ? s : 0; jj < L.n; jj += p.split ? 2 : 1) {
+      if (!p.split && !list_uses(L, jj, s)) continue;
+      const int kt = list_kt(L, jj);
       bool got = ptx::mbar_wait(&bar->s_full[s], count & 1, p.timeout_ns, abort_flag);
       if (!__all_sync(0xffffffffu, got)) {
         if (lane == 0) raise_error(p, bar, kErrSoftmax);
@@ -857,7 +953,7 @@ template <int D>
 size_t smem_for() {
   using G = Geo<D>;
   size_t bytes = (size_t)(2 + 2 * G::kStages) * G::kTileBytes + sizeof(Barriers) +
-                 2 * kMaxRowWords * sizeof(uint64_t) + 1024;
+                 kMaxList * sizeof(uint32_t) + 1024;
   // at least ~120 KiB so that one CTA owns an SM (and all of its tensor memory)
   return bytes < 120 * 1024 ? 120 * 1024 : bytes;
 }

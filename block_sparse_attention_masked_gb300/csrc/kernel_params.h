@@ -8,6 +8,9 @@
 
 namespace mattn {
 
+// Block-sparse masks: capacity of a CTA's key-tile list, so N <= 128 * this.
+constexpr int kBlockListMax = 4096;
+
 // Per-head table (device int32 [H][4]).
 enum HeadField : int { kHeadParam = 0, kHeadLoad = 1, kHeadStore = 2, kHeadPermRow = 3 };
 enum LoadMode : int { kLoadRaster = 0, kLoadColumnMajor = 1 };

@@ -148,6 +148,8 @@ int normalize(const mattn_mask_desc* desc, int B, int H, int N, int d, int dtype
     for (int h = 1; h < H; ++h)
       if (n.heads[h].param != bs) return fail(MATTN_ERR_UNSUPPORTED, "block size must be the same for every head");
     if (bs % kTile != 0) return fail(MATTN_ERR_UNSUPPORTED, "block size %d is not a multiple of %d", bs, kTile);
+    if ((N + kTile - 1) / kTile > kBlockListMax)
+      return fail(MATTN_ERR_UNSUPPORTED, "block-sparse masks support N <= %d (got %d)", kBlockListMax * kTile, N);
     if (!desc->block_bits) return fail(MATTN_ERR_INVALID_ARG, "block-sparse mask without block_bits");
     if (desc->block_heads != 1 && desc->block_heads != H)
       return fail(MATTN_ERR_INVALID_ARG, "block_heads must be 1 or H (got %d)", desc->block_heads);
