@@ -25,7 +25,18 @@ namespace {
 
 constexpr int kRcThreads = 384;
 constexpr int kRcStages = 3;
-constexpr int kNone = 0x7fffffff;
+
+// The CTA's query-tile list: entry j is query tile qt(j); key tile s of the
+// CTA multiplies it when uses(j, s).  Interval kinds: qt(j) = lo + j, the
+// union of the two key tiles' query ranges (adjacent key tiles have
+// overlapping or touching ranges), each key tile using its own range.
+// Block kind: entries qt | use0 << 30 | use1 << 31 in shared memory, built
+// once per CTA by one warp walking the bitmap column of each key tile.
+struct QList {
+  int n, lo, lo0, hi0, lo1, hi1;
+  const uint32_t* e;
+  int block;
+};
 
 struct RcBarriers {
   uint64_t k_full;
@@ -34,7 +45,16 @@ struct RcBarriers {
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
+  int list_n;
+  QList ql;
 };
+
+__device__ __forceinline__ int ql_qt(const QList& Q, int j) { return Q.block ? (int)(Q.e[j] & 0x3fffffffu) : Q.lo + j; }
+__device__ __forceinline__ bool ql_uses(const QList& Q, int j, int s) {
+  if (Q.block) return (Q.e[j] >> (30 + s)) & 1u;
+  const int qt = Q.lo + j;
+  return s ? (qt >= Q.lo1 && qt <= Q.hi1) : (qt >= Q.lo0 && qt <= Q.hi0);
+}
 
 __device__ __forceinline__ void rc_raise(const RecvParams& p, RcBarriers* bar, uint32_t bit) {
   *reinterpret_cast<volatile int*>(&bar->abort_flag) = 1;
@@ -56,25 +76,48 @@ __device__ __forceinline__ void col_interval(int kind, int64_t param, int64_t n,
   }
 }
 
-// Next query tile >= from that sees key tile kt (kNone when there is none).
-__device__ __forceinline__ int next_qt(const RecvParams& p, const uint64_t* bits, int param, int kt, int from) {
+// Interval kinds: the query tiles [*qlo, *qhi] that see key tile kt (empty: qlo > qhi).
+__device__ __forceinline__ void q_range(const RecvParams& p, int param, int kt, int* qlo, int* qhi) {
   const int nt = (p.N + kTile - 1) / kTile;
-  if (kt >= nt) return kNone;
-  if (p.kind == kBlockSparse) {
-    const int nb = kt / p.block_c;  // key block
-    for (int qt = from > kt ? from : kt; qt < nt; ++qt)
-      if ((bits[(int64_t)(qt / p.block_c) * p.block_wpr + (nb >> 6)] >> (nb & 63)) & 1ull) return qt;
-    return kNone;
+  if (kt >= nt) {
+    *qlo = 1; *qhi = 0;
+    return;
   }
   const int64_t t0 = (int64_t)kt * kTile;
   const int64_t t1 = (t0 + kTile < p.N ? t0 + kTile : p.N) - 1;
   int64_t lo0, hi0, lo1, hi1;
   col_interval(p.kind, param, p.N, t0, &lo0, &hi0);
   col_interval(p.kind, param, p.N, t1, &lo1, &hi1);
-  const int qlo = (int)(lo0 < 0 ? 0 : lo0 / kTile);
-  const int qhi = (int)((hi1 > p.N - 1 ? p.N - 1 : hi1) / kTile);
-  const int qt = from > qlo ? from : qlo;
-  return qt <= qhi ? qt : kNone;
+  *qlo = (int)(lo0 < 0 ? 0 : lo0 / kTile);
+  *qhi = (int)((hi1 > p.N - 1 ? p.N - 1 : hi1) / kTile);
+}
+
+// Block kind: one warp lists, in increasing order, the query tiles qt >=
+// kt0 whose bitmap row keeps key tile kt0 or kt0 + 1 (and qt >= that key
+// tile), 32 rows per step: a ballot per key tile, the union's ballot gives
+// every lane its output slot.
+__device__ __forceinline__ void build_q_list(const RecvParams& p, const uint64_t* bits, int kt0, int nk, uint32_t* list,
+                                             int* n_out, int lane) {
+  const int nt = (p.N + kTile - 1) / kTile;
+  const int c = p.block_c;
+  const int nb0 = kt0 / c, nb1 = (kt0 + 1) / c;
+  int base = 0;
+  for (int q0 = kt0; q0 < nt; q0 += 32) {
+    const int qt = q0 + lane;
+    bool u0 = false, u1 = false;
+    if (qt < nt) {
+      const uint64_t* row = bits + (int64_t)(qt / c) * p.block_wpr;
+      u0 = (row[nb0 >> 6] >> (nb0 & 63)) & 1ull;
+      u1 = nk > 1 && qt >= kt0 + 1 && ((row[nb1 >> 6] >> (nb1 & 63)) & 1ull);
+    }
+    const uint32_t any = __ballot_sync(0xffffffffu, u0 || u1);
+    if (u0 || u1) {
+      const int pos = base + __popc(any & ((1u << lane) - 1u));
+      list[pos] = (uint32_t)qt | ((u0 ? 1u : 0u) << 30) | ((u1 ? 1u : 0u) << 31);
+    }
+    base += __popc(any);
+  }
+  if (lane == 0) *n_out = base;
 }
 
 __device__ __forceinline__ int64_t rc_token_of(const RecvParams& p, int store_mode, int perm_row, int64_t pos) {
@@ -128,15 +171,8 @@ __global__ void __launch_bounds__(kRcThreads, 1) received_kernel(const __grid_co
   const uint64_t* bits =
       p.kind == kBlockSparse ? p.block_bits + (int64_t)((p.block_heads == 1) ? 0 : h) * p.block_nb * p.block_wpr
                              : nullptr;
-  // union walk of the two key tiles' query tiles
-  auto next_entry = [&](int from, int* qt, bool* use0, bool* use1) {
-    const int a = next_qt(p, bits, param, kt0, from);
-    const int b = nk > 1 ? next_qt(p, bits, param, kt0 + 1, from) : kNone;
-    *qt = a < b ? a : b;
-    *use0 = a == *qt;
-    *use1 = b == *qt;
-    return *qt != kNone;
-  };
+  uint32_t* list_e = reinterpret_cast<uint32_t*>(bar + 1);  // block kind: [kBlockListMax] entries
+  if (p.kind == kBlockSparse && warp == 2) build_q_list(p, bits, kt0, nk, list_e, &bar->list_n, lane);
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(&bar->k_full, 1);
@@ -161,6 +197,26 @@ __global__ void __launch_bounds__(kRcThreads, 1) received_kernel(const __grid_co
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = bar->tmem_base;
+  if (threadIdx.x == 0) {
+    QList Q;
+    Q.block = p.kind == kBlockSparse;
+    Q.e = list_e;
+    q_range(p, param, kt0, &Q.lo0, &Q.hi0);
+    if (nk > 1) q_range(p, param, kt0 + 1, &Q.lo1, &Q.hi1);
+    else { Q.lo1 = 1; Q.hi1 = 0; }
+    if (Q.block) {
+      Q.n = bar->list_n;
+      Q.lo = 0;
+    } else {
+      const bool e0 = Q.lo0 <= Q.hi0, e1 = Q.lo1 <= Q.hi1;
+      Q.lo = e0 ? (e1 ? min(Q.lo0, Q.lo1) : Q.lo0) : Q.lo1;
+      const int hi = e0 ? (e1 ? max(Q.hi0, Q.hi1) : Q.hi0) : Q.hi1;
+      Q.n = (e0 || e1) ? hi - Q.lo + 1 : 0;
+    }
+    bar->ql = Q;
+  }
+  __syncthreads();
+  const QList& QL = bar->ql;
 
   if (warp == 0) {
     // ------------------------------------------------------------ loads
@@ -168,10 +224,8 @@ __global__ void __launch_bounds__(kRcThreads, 1) received_kernel(const __grid_co
       ptx::mbar_arrive_expect_tx(&bar->k_full, nk * T::kTileBytes);
       for (int s = 0; s < nk; ++s)
         rc_load<D>(p.tk, p.ck, colmaj, p.grid_rows, sk + s * T::kTileBytes, &bar->k_full, (kt0 + s) * kTile, bh);
-      int qt;
-      bool u0, u1;
-      int j = 0;
-      for (bool more = next_entry(0, &qt, &u0, &u1); more; more = next_entry(qt + 1, &qt, &u0, &u1), ++j) {
+      for (int j = 0; j < QL.n; ++j) {
+        const int qt = ql_qt(QL, j);
         const int slot = j % kRcStages;
         if (!ptx::mbar_wait(&bar->q_empty[slot], ((j / kRcStages) & 1) ^ 1, p.timeout_ns, abort_flag)) {
           rc_raise(p, bar, kErrProducer);
@@ -196,14 +250,11 @@ __global__ void __launch_bounds__(kRcThreads, 1) received_kernel(const __grid_co
     const uint32_t k4 = ptx::smem_addr(sk) >> 4;
     const uint32_t q4 = ptx::smem_addr(sq) >> 4;
     int used[2] = {0, 0};
-    int qt;
-    bool u0, u1;
-    int j = 0;
-    for (bool more = next_entry(0, &qt, &u0, &u1); ok && more; more = next_entry(qt + 1, &qt, &u0, &u1), ++j) {
+    for (int j = 0; ok && j < QL.n; ++j) {
       const int slot = j % kRcStages;
       ok = wait_all(&bar->q_full[slot], (j / kRcStages) & 1);
-      for (int s = 0; ok && s < 2; ++s) {
-        if (!(s ? u1 : u0)) continue;
+      for (int s = 0; ok && s < nk; ++s) {
+        if (!ql_uses(QL, j, s)) continue;
         const int b = used[s] & 1;
         ok = wait_all(&bar->s_empty[s][b], ((used[s] >> 1) & 1) ^ 1);
         if (!ok) break;
@@ -238,10 +289,9 @@ __global__ void __launch_bounds__(kRcThreads, 1) received_kernel(const __grid_co
     const float* lse2 = p.lse2p + (int64_t)bh * p.lse_pitch;  // log2-domain lse in position order
     float racc = 0.f;
     int cnt = 0;
-    int qt;
-    bool u0, u1;
-    for (bool more = next_entry(0, &qt, &u0, &u1); more; more = next_entry(qt + 1, &qt, &u0, &u1)) {
-      if (!(s ? u1 : u0)) continue;
+    for (int j = 0; j < QL.n; ++j) {
+      if (!ql_uses(QL, j, s)) continue;
+      const int qt = ql_qt(QL, j);
       const int b = cnt & 1;
       const bool got = ptx::mbar_wait(&bar->s_full[s][b], (cnt >> 1) & 1, p.timeout_ns, abort_flag);
       if (!__all_sync(0xffffffffu, got)) {
@@ -341,7 +391,7 @@ size_t received_smem_bytes(int d) {
     case 128: tile = Geo<128>::kTileBytes; break;
     default: return 0;
   }
-  return (2 + kRcStages) * tile + sizeof(RcBarriers) + 1024;
+  return (2 + kRcStages) * tile + sizeof(RcBarriers) + kBlockListMax * sizeof(uint32_t) + 1024;
 }
 
 cudaError_t launch_received(const RecvParams& p, const float* lse, int d, cudaStream_t stream) {
