@@ -293,7 +293,7 @@ def run_gpu(args):
 
         for name, wlx in WORKLOADS.items():
             qx, kx, vx = make_workload_inputs(wlx, seed=0, device=dev)
-            in_bytes = 3 * qx.numel() * qx.element_size()
+            in_bytes = (qx.numel() + kx.numel() + vx.numel()) * qx.element_size()
             for m in wlx.masks:
                 sp = make_mask(wlx, m, seed=0)
                 mk = mattn.prepare(sp, wlx.H, wlx.N, device=dev)

@@ -13,7 +13,9 @@ is missing or the device is not sm_103, the calls raise.
 "sliding", "causal_window", "block"), head_param (per head C / w / W / Bs),
 perm (per head None or an int array, perm[p] = token at position p),
 perm_grid (per head None or (rows, cols) for the column-major walk of a
-raster grid), block (bool [H, Nb, Nb]) and sink (float [H] or None).
+raster grid), block (bool [H, Nb, Nb]), sink (float [H] or None) and
+sink_tokens (causal_window: the first sink_tokens positions stay visible).
+k and v may have fewer heads than q (grouped-query attention).
 """
 
 from __future__ import annotations
@@ -67,11 +69,12 @@ class MaskDesc(ctypes.Structure):
         ("sink", ctypes.c_void_p),
         ("softmax_scale", ctypes.c_float),
         ("flags", ctypes.c_uint32),
+        ("sink_tokens", ctypes.c_int32),
     ]
 
 
 EXPORTS = (
-    "mattn_fwd", "mattn_fwd_host", "mattn_fwd_noalloc", "mattn_rr_select", "mattn_received",
+    "mattn_fwd", "mattn_fwd_gqa", "mattn_fwd_host", "mattn_fwd_noalloc", "mattn_rr_select", "mattn_received",
     "mattn_count_pairs", "mattn_plan_tiles", "mattn_plan_tiles_device",
     "mattn_device_status", "mattn_set_wait_timeout_ns", "mattn_status_string", "mattn_last_error",
     "mattn_version",
@@ -92,6 +95,7 @@ def lib() -> ctypes.CDLL:
     vp, i32, u64p = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_uint64)
     dp = ctypes.POINTER(MaskDesc)
     L.mattn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, dp, vp]
+    L.mattn_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, dp, vp]
     L.mattn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, dp, vp]
     L.mattn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, dp, vp,
                                     ctypes.POINTER(ctypes.c_uint32)]
@@ -108,7 +112,7 @@ def lib() -> ctypes.CDLL:
     L.mattn_last_error.restype = ctypes.c_char_p
     L.mattn_last_error.argtypes = []
     L.mattn_version.argtypes = []
-    for name in ("mattn_fwd", "mattn_fwd_host", "mattn_fwd_noalloc", "mattn_rr_select", "mattn_received",
+    for name in ("mattn_fwd", "mattn_fwd_gqa", "mattn_fwd_host", "mattn_fwd_noalloc", "mattn_rr_select", "mattn_received",
                  "mattn_count_pairs", "mattn_plan_tiles",
                  "mattn_plan_tiles_device", "mattn_device_status", "mattn_set_wait_timeout_ns",
                  "mattn_version"):
@@ -201,6 +205,7 @@ class PreparedMask:
         if schedule not in SCHEDULE:
             raise ValueError(f"schedule must be one of {sorted(k for k in SCHEDULE if k)} or None")
         d.flags = SCHEDULE[schedule]
+        d.sink_tokens = int(getattr(spec, "sink_tokens", 0) or 0)
         self.desc = d
 
     def host_desc(self):
@@ -239,17 +244,22 @@ def attention(q, k, v, mask: PreparedMask, out=None, lse=None, want_lse: bool = 
         if not t.is_contiguous():
             raise ValueError("q, k, v must be contiguous [B, H, N, d]")
     B, H, N, d = q.shape
-    if k.shape != q.shape or v.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
-        raise ValueError("q, k, v must have the same shape and dtype")
+    H_kv = k.shape[1]
+    if (k.shape != (B, H_kv, N, d) or v.shape != k.shape or k.dtype != q.dtype or v.dtype != q.dtype
+            or H % H_kv):
+        raise ValueError("q [B, H, N, d] and k, v [B, H_kv, N, d] (H a multiple of H_kv) of one dtype")
     if out is None:
         out = torch.empty_like(q)
     if want_lse and lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     if stream is None:
         stream = torch.cuda.current_stream(q.device).cuda_stream
-    rc = lib().mattn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                         lse.data_ptr() if lse is not None else None, B, H, N, d, _dtype_code(q),
-                         ctypes.byref(mask.desc), stream)
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+            lse.data_ptr() if lse is not None else None)
+    if H_kv == H:
+        rc = lib().mattn_fwd(*args, B, H, N, d, _dtype_code(q), ctypes.byref(mask.desc), stream)
+    else:
+        rc = lib().mattn_fwd_gqa(*args, B, H, H_kv, N, d, _dtype_code(q), ctypes.byref(mask.desc), stream)
     _check(rc)
     return out, lse
 

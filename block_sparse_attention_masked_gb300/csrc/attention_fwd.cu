@@ -71,7 +71,9 @@ static_assert(kRegsControl + 2 * kRegsSoftmax == 3 * 168, "register split must m
 // copy and MMA warps short.
 struct TileList {
   int n, lo;
+  int na;              // interval kinds: leading entries 0 .. na - 1 are sink tiles below lo
   int lo0, hi0, lo1, hi1;
+  int ns0, ns1;        // sink tiles of each sub-tile (causal window with sink tokens)
   int use_n0, use_n1;  // block kind: entries sub-tile 0 / 1 uses
   const uint32_t* e;
   bool block;
@@ -102,13 +104,16 @@ constexpr int kMaxList = kBlockListMax;
 struct SubPlan {
   int qt;
   bool rows;                 // the sub-tile has query rows (< N)
-  KRange r;                  // interval kinds
+  KRange r;                  // interval kinds (causal window with sink tokens: the window part)
+  int ns;                    // sink tiles [0, ns) (causal window with sink tokens)
+  int param;                 // the head's mask parameter
   int ktmax;                 // block kind: last admissible key tile (causality)
 };
 
 // Work description of one CTA, computed identically by every thread.
 struct ItemPlan {
   int bh, h, b;
+  int bh_kv;  // K / V head row of (b, h): b * H_kv + h / kv_group
   SubPlan sp0, sp1;
 };
 
@@ -129,8 +134,11 @@ __device__ __forceinline__ SubPlan make_subplan(const FwdParams& p, int2 it, int
   sp.qt = item_qt(p, it, s);
   sp.rows = sp.qt < nt;
   sp.ktmax = sp.qt < nt ? sp.qt : nt - 1;
+  sp.param = param;
+  sp.ns = 0;
   if (p.kind != kBlockSparse && sp.rows) {
     sp.r = interval_krange(p.kind, param, p.N, sp.qt);
+    sp.ns = sink_tiles(p.sink_tokens, p.N, sp.qt);
   } else {
     sp.r.lo = 1; sp.r.hi = 0; sp.r.flo = 0; sp.r.fhi = -1;  // empty
   }
@@ -142,6 +150,7 @@ __device__ __forceinline__ ItemPlan make_plan(const FwdParams& p, int2 it) {
   ip.bh = it.x;
   ip.h = it.x % p.H;
   ip.b = it.x / p.H;
+  ip.bh_kv = ip.b * p.H_kv + ip.h / p.kv_group;
   const int param = p.head_info[ip.h * 4 + kHeadParam];
   ip.sp0 = make_subplan(p, it, 0, param);
   ip.sp1 = make_subplan(p, it, 1, param);
@@ -149,13 +158,13 @@ __device__ __forceinline__ ItemPlan make_plan(const FwdParams& p, int2 it) {
 }
 
 __device__ __forceinline__ int list_kt(const TileList& L, int j) {
-  return L.block ? (int)(L.e[j] & 0x3fffffffu) : L.lo + j;
+  return L.block ? (int)(L.e[j] & 0x3fffffffu) : (j < L.na ? j : L.lo + j - L.na);
 }
 
 __device__ __forceinline__ bool list_uses(const TileList& L, int j, int s) {
   if (L.block) return (L.e[j] >> (30 + s)) & 1u;
-  const int kt = L.lo + j;
-  return s ? (kt >= L.lo1 && kt <= L.hi1) : (kt >= L.lo0 && kt <= L.hi0);
+  const int kt = list_kt(L, j);
+  return s ? ((kt >= L.lo1 && kt <= L.hi1) || kt < L.ns1) : ((kt >= L.lo0 && kt <= L.hi0) || kt < L.ns0);
 }
 
 // Whether sub-tile s (split: pipeline s, which shares the one query tile)
@@ -175,20 +184,36 @@ __device__ __forceinline__ TileList make_list(const FwdParams& p, const ItemPlan
   L.use_n1 = L.block ? block_counts[2] : 0;
   L.lo0 = ip.sp0.r.lo; L.hi0 = ip.sp0.r.hi;
   L.lo1 = ip.sp1.r.lo; L.hi1 = ip.sp1.r.hi;
+  L.ns0 = ip.sp0.ns; L.ns1 = ip.sp1.ns;
+  L.na = 0;
   if (L.block) {
     L.n = block_counts[0];
     L.lo = 0;
   } else {
     const bool e0 = L.lo0 <= L.hi0, e1 = L.lo1 <= L.hi1;
     L.lo = e0 ? (e1 ? min(L.lo0, L.lo1) : L.lo0) : L.lo1;
-    const int hi = e0 ? (e1 ? max(L.hi0, L.hi1) : L.hi0) : L.hi1;
+    int hi = e0 ? (e1 ? max(L.hi0, L.hi1) : L.hi0) : L.hi1;
     L.n = (e0 || e1) ? hi - L.lo + 1 : 0;
+    // sink tiles: a segment 0 .. ns - 1 before the window's tiles, or one
+    // segment 0 .. hi when they meet
+    const int ns = max(L.ns0, L.ns1);
+    if (ns > 0 && L.n > 0) {
+      if (ns >= L.lo) {
+        hi = max(hi, ns - 1);
+        L.lo = 0;
+        L.n = hi + 1;
+      } else {
+        L.na = ns;
+        L.n += ns;
+      }
+    }
   }
   return L;
 }
 
 __device__ __forceinline__ bool sub_partial(const FwdParams& p, const SubPlan& sp, int kt) {
   if (p.kind == kBlockSparse) return block_tile_class(sp.qt, kt, p.N) == kTilePartial;
+  if (p.sink_tokens > 0) return sink_window_tile_class(sp.param, p.sink_tokens, p.N, sp.qt, kt) == kTilePartial;
   return interval_tile_class(sp.r, kt) == kTilePartial;
 }
 
@@ -532,9 +557,9 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
         }
         ptx::mbar_arrive_expect_tx(&full[slot], G::kTileBytes);
         if (is_k)
-          load_tile<D>(p, p.tk, p.ck, colmaj, ring + slot * G::kTileBytes, &full[slot], kt * kTile, ip.bh, keep);
+          load_tile<D>(p, p.tk, p.ck, colmaj, ring + slot * G::kTileBytes, &full[slot], kt * kTile, ip.bh_kv, keep);
         else
-          load_v_tile<D>(p, colmaj, ring + slot * G::kTileBytes, &full[slot], kt * kTile, ip.bh, keep);
+          load_v_tile<D>(p, colmaj, ring + slot * G::kTileBytes, &full[slot], kt * kTile, ip.bh_kv, keep);
       }
       if (*abort_flag) {
         // let copies already in flight land before the CTA's shared memory goes away
@@ -683,6 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
     int64_t lo, hi;
     row_interval(p.kind, param, p.N, pos, &lo, &hi);
     if (hi > p.N - 1) hi = p.N - 1;
+    const int64_t sink_hi = sink_last(p.sink_tokens, pos);  // sink keys [0, sink_hi]
     const float sl2 = p.scale_log2;
 
     float m = -INFINITY;  // running (stale) max of scaled scores, log2 domain
@@ -712,9 +738,17 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
         const int64_t k0 = (int64_t)kt * kTile;
         const int c_lo = (int)(lo - k0 < -1 ? -1 : (lo - k0 > 128 ? 128 : lo - k0));
         const int c_hi = (int)(hi - k0 < -1 ? -1 : (hi - k0 > 128 ? 128 : hi - k0));
+        // and the sink keys of the tile: columns [0, c_s]
+        const int c_s = (int)(sink_hi - k0 < -1 ? -1 : (sink_hi - k0 > 128 ? 128 : sink_hi - k0));
+        if (c_s < 0) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c < c_lo || c > c_hi) x[c] = -INFINITY;
+          for (int c = 0; c < 128; ++c)
+            if (c < c_lo || c > c_hi) x[c] = -INFINITY;
+        } else {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if ((c < c_lo || c > c_hi) && c > c_s) x[c] = -INFINITY;
+        }
       }
       // P = exp2(s * scale * log2e - m) into tensor memory.  tcgen05.ld / st
       // are warp-collective, so every branch below is taken by whole warps
@@ -883,9 +917,16 @@ __global__ void plan_dump_kernel(const PlanDumpParams p) {
     }
   } else {
     KRange r = interval_krange(p.kind, param, p.N, qt);
+    const int ns = sink_tiles(p.sink_tokens, p.N, qt);
+    for (int kt = 0; kt < ns && kt < r.lo; ++kt) {  // sink tiles below the window
+      out[4 * n + 0] = h; out[4 * n + 1] = qt; out[4 * n + 2] = kt;
+      out[4 * n + 3] = sink_window_tile_class(param, p.sink_tokens, p.N, qt, kt);
+      ++n;
+    }
     for (int kt = r.lo; kt <= r.hi; ++kt) {
       out[4 * n + 0] = h; out[4 * n + 1] = qt; out[4 * n + 2] = kt;
-      out[4 * n + 3] = interval_tile_class(r, kt);
+      out[4 * n + 3] = p.sink_tokens > 0 ? sink_window_tile_class(param, p.sink_tokens, p.N, qt, kt)
+                                         : interval_tile_class(r, kt);
       ++n;
     }
   }
@@ -893,7 +934,9 @@ __global__ void plan_dump_kernel(const PlanDumpParams p) {
 }
 
 // Reorder to sequence positions (and round fp32 to bf16): one thread per 8
-// elements of one destination row, for q, k and v (blockIdx.y).
+// elements of one destination row, for q, k and v (blockIdx.y).  K and V
+// rows of query head h are read from K / V head h / kv_group, so that the
+// copies have one head per query head.
 __global__ void gather_kernel(const GatherParams p) {
   const int t = blockIdx.y;
   const int64_t vec_per_row = p.d / 8;
@@ -913,7 +956,8 @@ __global__ void gather_kernel(const GatherParams p) {
   } else if (store_mode == kStoreExplicit) {
     tok = p.perm[(int64_t)p.head_info[h * 4 + kHeadPermRow] * p.N + pos];
   }
-  const int64_t src_off = (bh * p.N + tok) * p.d + c8;
+  const int64_t src_bh = t == 0 ? bh : (bh / p.H) * (p.H / p.kv_group) + h / p.kv_group;
+  const int64_t src_off = (src_bh * p.N + tok) * p.d + c8;
   uint4 out;
   if (p.src_f32) {
     const float4* s = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.src[t]) + src_off);

@@ -40,7 +40,10 @@ struct FwdParams {
   unsigned long long timeout_ns;
   int n_items;
   int B, H, N;
+  int H_kv, kv_group;               // K / V heads (tk, ck, tv, cv are [B*H_kv] views);
+                                    // query head h reads K / V head h / kv_group
   int kind;
+  int sink_tokens;                  // kCausalWindow: first positions every later query sees
   int block_heads, block_wpr, block_c, block_nb;
   int grid_rows, grid_cols;
   float scale_log2;                 // softmax scale * log2(e)
@@ -54,16 +57,18 @@ struct PlanDumpParams {
   const int32_t* head_info;
   const uint64_t* block_bits;
   int H, N, kind, block_heads, block_wpr, block_c, block_nb;
+  int sink_tokens;
   int32_t* out;     // [H][nt][nt][4]
   int32_t* counts;  // [H][nt]
 };
 
 struct GatherParams {
-  const void* src[3];
-  void* dst[3];
+  const void* src[3];               // q [B][H][N][d]; k, v [B][H / kv_group][N][d]
+  void* dst[3];                     // [B][H][N][d] each (k, v repeated per query head)
   const int32_t* head_info;
   const int32_t* perm;
   int B, H, N, d;
+  int kv_group;
   int src_f32;
   int grid_rows, grid_cols;
 };

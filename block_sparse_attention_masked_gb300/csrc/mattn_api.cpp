@@ -73,6 +73,7 @@ struct Normalized {
   bool need_copy;     // reorder / convert into a bf16 copy in position order
   bool any_colmajor_tma;
   int block_c, block_nb, block_wpr, block_heads;
+  int sink_tokens;    // causal window: leading positions every later query sees
   float scale;
   bool split;         // schedule: one query tile per CTA, key tiles dealt to two pipelines
 };
@@ -105,6 +106,10 @@ int normalize(const mattn_mask_desc* desc, int B, int H, int N, int d, int dtype
   n.any_colmajor_tma = false;
   n.block_c = n.block_nb = n.block_wpr = 0;
   n.block_heads = 1;
+  if (desc->sink_tokens < 0) return fail(MATTN_ERR_INVALID_ARG, "sink_tokens must be >= 0 (got %d)", desc->sink_tokens);
+  if (desc->sink_tokens > 0 && desc->kind != MATTN_CAUSAL_WINDOW)
+    return fail(MATTN_ERR_INVALID_ARG, "sink_tokens applies to MATTN_CAUSAL_WINDOW masks only");
+  n.sink_tokens = desc->sink_tokens;
   for (int h = 0; h < H; ++h) {
     int prm = desc->head_param ? desc->head_param[h] : desc->param;
     if (n.kind != MATTN_FULL && prm < 1)
@@ -175,6 +180,13 @@ void walk_tiles_host(const Normalized& n, const uint64_t* host_bits, int h, int 
     for (int kt = block_next_kt(bits, n.block_wpr, n.block_c, qt, 0, qt); kt != 0x7fffffff;
          kt = block_next_kt(bits, n.block_wpr, n.block_c, qt, kt + 1, qt))
       fn(kt, block_tile_class(qt, kt, n.N));
+  } else if (n.sink_tokens > 0) {
+    // the sink tiles below the window, then the window's tiles
+    const int w = n.heads[h].param;
+    KRange r = interval_krange(n.kind, w, n.N, qt);
+    const int ns = sink_tiles(n.sink_tokens, n.N, qt);
+    for (int kt = 0; kt < ns && kt < r.lo; ++kt) fn(kt, sink_window_tile_class(w, n.sink_tokens, n.N, qt, kt));
+    for (int kt = r.lo; kt <= r.hi; ++kt) fn(kt, sink_window_tile_class(w, n.sink_tokens, n.N, qt, kt));
   } else {
     KRange r = interval_krange(n.kind, n.heads[h].param, n.N, qt);
     for (int kt = r.lo; kt <= r.hi; ++kt) fn(kt, interval_tile_class(r, kt));
@@ -184,7 +196,9 @@ void walk_tiles_host(const Normalized& n, const uint64_t* host_bits, int h, int 
 int interval_tiles(const Normalized& n, int h, int qt) {
   if (qt * (int64_t)kTile >= n.N) return 0;
   KRange r = interval_krange(n.kind, n.heads[h].param, n.N, qt);
-  return r.hi >= r.lo ? r.hi - r.lo + 1 : 0;
+  const int win = r.hi >= r.lo ? r.hi - r.lo + 1 : 0;
+  const int ns = sink_tiles(n.sink_tokens, n.N, qt);
+  return win + (ns < r.lo ? ns : r.lo);  // sink tiles below the window
 }
 
 // Work list: one item per (b*H + h, query-tile pair), or per (b*H + h,
@@ -279,7 +293,8 @@ int device_state(DeviceState** out) {
 std::string plan_key(const Normalized& n) {
   std::string k;
   char buf[96];
-  snprintf(buf, sizeof(buf), "%d|%d|%d|%d|%d|%d|", n.kind, n.B, n.H, n.N, n.need_copy ? 1 : 0, n.split ? 1 : 0);
+  snprintf(buf, sizeof(buf), "%d|%d|%d|%d|%d|%d|%d|", n.kind, n.B, n.H, n.N, n.need_copy ? 1 : 0, n.split ? 1 : 0,
+           n.sink_tokens);
   k += buf;
   for (const auto& hp : n.heads) {
     snprintf(buf, sizeof(buf), "%d,%d,%d,%d;", hp.param, hp.load, hp.store, hp.perm_row);
@@ -342,13 +357,15 @@ int encode(CUtensorMap* tm, const void* base, int rank, const cuuint64_t* dims, 
   return MATTN_OK;
 }
 
-// Raster views [B*H][N][d] and, when asked, column-major views
-// [B*H][rows][cols][d] of one bf16 tensor: map [0] covers 64-column chunks
-// (128-byte swizzle), map [1] the 16- or 32-column rest.
-int make_maps(const Normalized& n, const void* base, CUtensorMap raster[2], CUtensorMap colmaj[2], int rows, int cols) {
+// Raster views [heads][N][d] and, when asked, column-major views
+// [heads][rows][cols][d] of one bf16 tensor (heads = B * its head count):
+// map [0] covers 64-column chunks (128-byte swizzle), map [1] the 16- or
+// 32-column rest.
+int make_maps(const Normalized& n, const void* base, CUtensorMap raster[2], CUtensorMap colmaj[2], int rows, int cols,
+              int64_t heads) {
   const int d = n.d;
   const int chunks = d / 64, rem = d % 64;
-  const cuuint64_t bh = (cuuint64_t)n.B * n.H;
+  const cuuint64_t bh = (cuuint64_t)heads;
   const CUtensorMapSwizzle rem_sw = rem == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B;
   memset(raster, 0, 2 * sizeof(CUtensorMap));
   memset(colmaj, 0, 2 * sizeof(CUtensorMap));
@@ -390,12 +407,12 @@ int make_maps(const Normalized& n, const void* base, CUtensorMap raster[2], CUte
 // vw = 64 when d % 64 == 0, else 32 when d % 32 == 0, else 16; the kernel's
 // P V product reads all d columns as one MN-major operand.
 int make_v_maps(const Normalized& n, const void* base, CUtensorMap raster[2], CUtensorMap colmaj[2], int rows,
-                int cols) {
+                int cols, int64_t heads) {
   const int d = n.d;
   const int vw = d % 64 == 0 ? 64 : (d % 32 == 0 ? 32 : 16);
   const CUtensorMapSwizzle sw =
       vw == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : (vw == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
-  const cuuint64_t bh = (cuuint64_t)n.B * n.H;
+  const cuuint64_t bh = (cuuint64_t)heads;
   memset(raster, 0, 2 * sizeof(CUtensorMap));
   memset(colmaj, 0, 2 * sizeof(CUtensorMap));
   {
@@ -423,8 +440,10 @@ int check_device_ptrs(const void* q, const void* k, const void* v, const void* o
   return MATTN_OK;
 }
 
-int fwd_locked(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d, int dtype,
-               const mattn_mask_desc* desc, cudaStream_t stream, int self_test) {
+int fwd_locked(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N, int d,
+               int dtype, const mattn_mask_desc* desc, cudaStream_t stream, int self_test) {
+  if (H_kv < 1 || H % H_kv != 0)
+    return fail(MATTN_ERR_INVALID_ARG, "the query head count %d must be a multiple of the K/V head count %d", H, H_kv);
   Normalized n;
   int rc = normalize(desc, B, H, N, d, dtype, true, &n);
   if (rc) return rc;
@@ -455,19 +474,24 @@ int fwd_locked(const void* q, const void* k, const void* v, void* o, float* lse,
     gp.head_info = plan->head_info;
     gp.perm = desc->perm;
     gp.B = B; gp.H = H; gp.N = N; gp.d = d;
+    gp.kv_group = H / H_kv;
     gp.src_f32 = dtype == MATTN_F32;
     gp.grid_rows = desc->grid_rows;
     gp.grid_cols = desc->grid_cols;
     MATTN_CUDA(launch_gather(gp, stream), "gather launch");
   }
+  // the copies hold one K / V head per query head
+  const int kv_heads = n.need_copy ? H : H_kv;
 
   FwdParams p;
   memset(&p, 0, sizeof(p));
   const int rows = n.any_colmajor_tma ? desc->grid_rows : 0;
   const int cols = n.any_colmajor_tma ? desc->grid_cols : 0;
-  if ((rc = make_maps(n, use[0], p.tq, p.cq, rows, cols))) return rc;
-  if ((rc = make_maps(n, use[1], p.tk, p.ck, rows, cols))) return rc;
-  if ((rc = make_v_maps(n, use[2], p.tv, p.cv, rows, cols))) return rc;
+  if ((rc = make_maps(n, use[0], p.tq, p.cq, rows, cols, (int64_t)B * H))) return rc;
+  if ((rc = make_maps(n, use[1], p.tk, p.ck, rows, cols, (int64_t)B * kv_heads))) return rc;
+  if ((rc = make_v_maps(n, use[2], p.tv, p.cv, rows, cols, (int64_t)B * kv_heads))) return rc;
+  p.H_kv = kv_heads;
+  p.kv_group = H / kv_heads;
   p.o = o;
   p.lse = lse;
   p.items = plan->items;
@@ -480,6 +504,7 @@ int fwd_locked(const void* q, const void* k, const void* v, void* o, float* lse,
   p.timeout_ns = wait_timeout_ns();
   p.B = B; p.H = H; p.N = N;
   p.kind = n.kind;
+  p.sink_tokens = n.sink_tokens;
   p.block_heads = n.block_heads;
   p.block_wpr = n.block_wpr;
   p.block_c = n.block_c;
@@ -533,9 +558,11 @@ int prepare_in_place_launch(const void* q, const void* k, const void* v, void* o
   memset(&p, 0, sizeof(p));
   const int rows = n.any_colmajor_tma ? desc->grid_rows : 0;
   const int cols = n.any_colmajor_tma ? desc->grid_cols : 0;
-  if ((rc = make_maps(n, q, p.tq, p.cq, rows, cols))) return rc;
-  if ((rc = make_maps(n, k, p.tk, p.ck, rows, cols))) return rc;
-  if ((rc = make_v_maps(n, v, p.tv, p.cv, rows, cols))) return rc;
+  if ((rc = make_maps(n, q, p.tq, p.cq, rows, cols, (int64_t)B * H))) return rc;
+  if ((rc = make_maps(n, k, p.tk, p.ck, rows, cols, (int64_t)B * H))) return rc;
+  if ((rc = make_v_maps(n, v, p.tv, p.cv, rows, cols, (int64_t)B * H))) return rc;
+  p.H_kv = H;
+  p.kv_group = 1;
   p.o = o;
   p.lse = lse;
   p.items = nullptr;
@@ -548,6 +575,7 @@ int prepare_in_place_launch(const void* q, const void* k, const void* v, void* o
   p.timeout_ns = wait_timeout_ns();
   p.B = B; p.H = H; p.N = N;
   p.kind = n.kind;
+  p.sink_tokens = n.sink_tokens;
   p.block_heads = n.block_heads;
   p.block_wpr = n.block_wpr;
   p.block_c = n.block_c;
@@ -577,7 +605,13 @@ extern "C" {
 int mattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d, int dtype,
               const mattn_mask_desc* desc, void* stream) {
   std::lock_guard<std::mutex> lk(g_mutex);
-  return fwd_locked(q, k, v, o, lse, B, H, N, d, dtype, desc, static_cast<cudaStream_t>(stream), 0);
+  return fwd_locked(q, k, v, o, lse, B, H, H, N, d, dtype, desc, static_cast<cudaStream_t>(stream), 0);
+}
+
+int mattn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N,
+                  int d, int dtype, const mattn_mask_desc* desc, void* stream) {
+  std::lock_guard<std::mutex> lk(g_mutex);
+  return fwd_locked(q, k, v, o, lse, B, H, H_kv, N, d, dtype, desc, static_cast<cudaStream_t>(stream), 0);
 }
 
 // Test hook (not in the public header): the same launch, with the MMA warp
@@ -586,7 +620,7 @@ int mattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, 
 int mattn_internal_fwd_wait_selftest(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                                      int N, int d, int dtype, const mattn_mask_desc* desc, void* stream) {
   std::lock_guard<std::mutex> lk(g_mutex);
-  return fwd_locked(q, k, v, o, lse, B, H, N, d, dtype, desc, static_cast<cudaStream_t>(stream), 1);
+  return fwd_locked(q, k, v, o, lse, B, H, H, N, d, dtype, desc, static_cast<cudaStream_t>(stream), 1);
 }
 
 // Test hook (not in the public header): evaluates the softmax's polynomial
@@ -642,7 +676,7 @@ int mattn_fwd_host(const void* q, const void* k, const void* v, void* o, float* 
     MATTN_CUDA(cudaMemcpyAsync(dperm, desc->perm, perm_bytes, cudaMemcpyHostToDevice, stream), "copy perm");
     dd.perm = reinterpret_cast<const int32_t*>(dperm);
   }
-  rc = fwd_locked(dq, dk, dv, dout, lse ? dlse : nullptr, B, H, N, d, dtype, &dd, stream, 0);
+  rc = fwd_locked(dq, dk, dv, dout, lse ? dlse : nullptr, B, H, H, N, d, dtype, &dd, stream, 0);
   if (rc) return rc;
   MATTN_CUDA(cudaMemcpyAsync(o, dout, tensor, cudaMemcpyDeviceToHost, stream), "copy o");
   if (lse) MATTN_CUDA(cudaMemcpyAsync(lse, dlse, lse_bytes, cudaMemcpyDeviceToHost, stream), "copy lse");
@@ -657,6 +691,7 @@ int mattn_received(const void* q, const void* k, const float* lse, float* r, int
   Normalized n;
   int rc = normalize(desc, B, H, N, d, dtype, true, &n);
   if (rc) return rc;
+  if (n.sink_tokens > 0) return fail(MATTN_ERR_UNSUPPORTED, "received attention does not take sink tokens");
   if (!q || !k || !lse || !r) return fail(MATTN_ERR_INVALID_ARG, "q, k, lse and r must be non-NULL");
   if (!aligned16(q) || !aligned16(k)) return fail(MATTN_ERR_UNSUPPORTED, "q and k must be 16-byte aligned");
   if ((reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(r) & 3u))
@@ -682,6 +717,7 @@ int mattn_received(const void* q, const void* k, const float* lse, float* r, int
     gp.head_info = plan->head_info;
     gp.perm = desc->perm;
     gp.B = B; gp.H = H; gp.N = N; gp.d = d;
+    gp.kv_group = 1;
     gp.src_f32 = dtype == MATTN_F32;
     gp.grid_rows = desc->grid_rows;
     gp.grid_cols = desc->grid_cols;
@@ -691,8 +727,8 @@ int mattn_received(const void* q, const void* k, const float* lse, float* r, int
   memset(&p, 0, sizeof(p));
   const int rows = n.any_colmajor_tma ? desc->grid_rows : 0;
   const int cols = n.any_colmajor_tma ? desc->grid_cols : 0;
-  if ((rc = make_maps(n, use[0], p.tq, p.cq, rows, cols))) return rc;
-  if ((rc = make_maps(n, use[1], p.tk, p.ck, rows, cols))) return rc;
+  if ((rc = make_maps(n, use[0], p.tq, p.cq, rows, cols, (int64_t)B * H))) return rc;
+  if ((rc = make_maps(n, use[1], p.tk, p.ck, rows, cols, (int64_t)B * H))) return rc;
   p.lse_pitch = ((int64_t)N + 127) / 128 * 128;
   if ((rc = st->recv_lse.reserve((size_t)B * H * p.lse_pitch * sizeof(float), "cudaMalloc(received lse)"))) return rc;
   p.lse2p = static_cast<float*>(st->recv_lse.ptr);
@@ -820,6 +856,9 @@ int mattn_count_pairs(const mattn_mask_desc* desc, int B, int H, int N, uint64_t
         lo = std::max<int64_t>(0, lo);
         hi = std::min<int64_t>(N - 1, hi);
         if (hi >= lo) total += (uint64_t)(hi - lo + 1);
+        // sink keys below the window: [0, min(S - 1, p, lo - 1)]
+        const int64_t sl = std::min<int64_t>(sink_last(n.sink_tokens, p), lo - 1);
+        if (sl >= 0) total += (uint64_t)(sl + 1);
       }
     }
   }
@@ -872,6 +911,7 @@ int mattn_plan_tiles_device(const mattn_mask_desc* desc, int H, int N, int32_t* 
   pp.head_info = plan->head_info;
   pp.block_bits = n.kind == kBlockSparse ? desc->block_bits : nullptr;
   pp.H = H; pp.N = N; pp.kind = n.kind;
+  pp.sink_tokens = n.sink_tokens;
   pp.block_heads = n.block_heads; pp.block_wpr = n.block_wpr; pp.block_c = n.block_c; pp.block_nb = n.block_nb;
   pp.out = static_cast<int32_t*>(st->dump.ptr);
   pp.counts = pp.out + slots;
@@ -928,6 +968,6 @@ const char* mattn_status_string(int status) {
 
 const char* mattn_last_error(void) { return g_last_error; }
 
-int mattn_version(void) { return 100; }
+int mattn_version(void) { return 101; }
 
 }  // extern "C"

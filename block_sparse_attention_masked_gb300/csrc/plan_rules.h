@@ -108,6 +108,43 @@ MATTN_HD KRange interval_krange(int kind, int64_t param, int64_t n, int qt) {
   return r;
 }
 
+// Causal window with sink tokens: a causal window of W keys plus the first
+// S tokens of the sequence ("Sliding window attention vs. linear attention
+// at equal memory" (Bifocal page), the StreamingLLM sink-token student: a
+// 572-token window plus the first 4 tokens).  Row p sees [p - W + 1, p]
+// and [0, min(S - 1, p)].  The window part is interval_krange's
+// kCausalWindow range; the sink keys add the leading key tiles
+// [0, sink_tiles) to a query tile's list.
+
+// Last sink key visible to row p (-1: none).
+MATTN_HD int64_t sink_last(int64_t s, int64_t p) { return s > 0 ? imin64(s - 1, p) : -1; }
+
+// Leading key tiles holding sink keys that some row of query tile qt sees.
+MATTN_HD int sink_tiles(int64_t s, int64_t n, int qt) {
+  const int64_t p0 = (int64_t)qt * kTile;
+  const int64_t p1 = imin64(n, p0 + kTile) - 1;
+  if (s <= 0 || p0 > p1) return 0;
+  const int64_t last = imin64(imin64(s - 1, p1), n - 1);  // the last row sees the most
+  return (int)(last / kTile) + 1;
+}
+
+// Exact class of a visited key tile kt of query tile qt: FULL when every
+// (p, q) of the two complete tiles is visible.  Every row must see the
+// tile's last key (causality: p0 >= k1), and the last row's window must
+// start at or before the first key of the tile that no sink covers (none
+// when the whole tile is sink keys).
+MATTN_HD int sink_window_tile_class(int64_t w, int64_t s, int64_t n, int qt, int kt) {
+  const int64_t p0 = (int64_t)qt * kTile, k0 = (int64_t)kt * kTile;
+  const int64_t p1 = p0 + kTile - 1, k1 = k0 + kTile - 1;
+  if (p1 > n - 1 || k1 > n - 1) return kTilePartial;  // incomplete tile
+  if (p0 < k1) return kTilePartial;
+  if (k1 >= s) {
+    const int64_t e = k0 >= s ? k0 : s;  // first key of the tile outside the sink
+    if (p1 - w + 1 > e) return kTilePartial;
+  }
+  return kTileFull;
+}
+
 // Block-selection bit B[m][nblk] of one head's bitmap (words per row = wpr).
 MATTN_HD bool block_bit(const uint64_t* bits, int wpr, int m, int nblk) {
   return (bits[(int64_t)m * wpr + (nblk >> 6)] >> (nblk & 63)) & 1ull;

@@ -116,6 +116,14 @@ typedef struct {
                              /* HOST for mattn_fwd_host                                    */
   float softmax_scale;       /* 0 => 1/sqrt(d)                                             */
   uint32_t flags;            /* 0, MATTN_FLAG_SCHEDULE_PAIRED or MATTN_FLAG_SCHEDULE_SPLIT   */
+  int32_t sink_tokens;       /* MATTN_CAUSAL_WINDOW only (else must be 0): S >= 0 sink      */
+                             /* tokens, the first S positions, visible to every query at    */
+                             /* or after them besides its window: query p sees             */
+                             /* [p - W + 1, p] and [0, min(S - 1, p)] ("Sliding window      */
+                             /* attention vs. linear attention at equal memory" (Bifocal    */
+                             /* page): a 572-token window plus the first 4 tokens, the      */
+                             /* StreamingLLM sink tokens).  Not to be confused with `sink`, */
+                             /* the learned per-head logit.  mattn_received rejects S > 0.  */
 } mattn_mask_desc;
 
 /*
@@ -132,6 +140,25 @@ typedef struct {
 int mattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
               int B, int H, int N, int d, int dtype,
               const mattn_mask_desc* desc, void* stream);
+
+/*
+ * mattn_fwd_gqa -- mattn_fwd with grouped-query attention: the H query
+ * heads share H_kv key/value heads, query head h reading K/V head
+ * h / (H / H_kv) (consecutive query heads form a group).  Source: "Sliding
+ * window attention vs. linear attention at equal memory" (Bifocal page),
+ * section "Comparison at equal memory": the Qwen3-4B students keep the
+ * teacher's grouped-query attention, 32 query heads sharing 8 key/value
+ * heads; the speed test's configuration has 16 query heads and 4
+ * key/value heads.  Everything else (masks, orders, sink) is per query
+ * head, as for mattn_fwd.
+ *   q, o     DEVICE [B][H][N][d];  k, v  DEVICE [B][H_kv][N][d];
+ *   lse      DEVICE fp32 [B][H][N] or NULL.
+ *   H_kv >= 1 and H % H_kv == 0, else MATTN_ERR_INVALID_ARG; H_kv == H is
+ *   mattn_fwd.  Other arguments, ownership and errors as for mattn_fwd.
+ */
+int mattn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                  int B, int H, int H_kv, int N, int d, int dtype,
+                  const mattn_mask_desc* desc, void* stream);
 
 /*
  * mattn_fwd_host -- the same operation on HOST buffers: copies q, k, v (and

@@ -14,8 +14,12 @@ from __future__ import annotations
 import math
 
 
-def neighbour_set(kind, param, n, pos_i, pos_of_token, block=None):
-    """List of caller token indices j that query position ``pos_i`` may see."""
+def neighbour_set(kind, param, n, pos_i, pos_of_token, block=None, sink_tokens=0):
+    """List of caller token indices j that query position ``pos_i`` may see.
+
+    ``sink_tokens`` (causal_window only): positions 0 .. sink_tokens - 1 stay
+    visible to every query at or after them (the Bifocal page: a window
+    plus the first 4 tokens of the sequence)."""
     out = []
     for j in range(n):
         pj = pos_of_token[j]
@@ -28,8 +32,9 @@ def neighbour_set(kind, param, n, pos_i, pos_of_token, block=None):
             # param neighbours to the left and param to the right, plus itself
             ok = pos_i - param <= pj <= pos_i + param
         elif kind == "causal_window":
-            # itself and the param - 1 positions before it
-            ok = pos_i - param < pj <= pos_i
+            # itself and the param - 1 positions before it, and the first
+            # sink_tokens positions when they are not after it
+            ok = pos_i - param < pj <= pos_i or (pj < sink_tokens and pj <= pos_i)
         elif kind == "block":
             ok = bool(block[pos_i // param][pj // param]) and pj <= pos_i
         else:
@@ -39,7 +44,7 @@ def neighbour_set(kind, param, n, pos_i, pos_of_token, block=None):
     return out
 
 
-def attention_head(q, k, v, kind, param=0, perm=None, block=None, sink=None):
+def attention_head(q, k, v, kind, param=0, perm=None, block=None, sink=None, sink_tokens=0):
     """One head: q, k, v are lists of lists (n x d).  Returns (o, lse) lists."""
     n = len(q)
     d = len(q[0])
@@ -49,7 +54,7 @@ def attention_head(q, k, v, kind, param=0, perm=None, block=None, sink=None):
             pos_of_token[int(t)] = p
     o_rows, lses = [], []
     for i in range(n):
-        nb = neighbour_set(kind, param, n, pos_of_token[i], pos_of_token, block)
+        nb = neighbour_set(kind, param, n, pos_of_token[i], pos_of_token, block, sink_tokens)
         scores = []
         for j in nb:
             acc = 0.0

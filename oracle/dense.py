@@ -42,7 +42,7 @@ PARTIAL_TILE = 2
 
 
 def allowed(kind: str, param: int, p: np.ndarray, q: np.ndarray,
-            block_h: Optional[np.ndarray] = None) -> np.ndarray:
+            block_h: Optional[np.ndarray] = None, sink_tokens: int = 0) -> np.ndarray:
     """M(p, q): may the query at position p see the key at position q?
 
     ``p`` and ``q`` broadcast against each other (integer arrays).
@@ -59,7 +59,12 @@ def allowed(kind: str, param: int, p: np.ndarray, q: np.ndarray,
     - causal_window, W = param: a causal local window of W tokens (Asymmetric
       Attention Heads, "What was done", candidate windows 512..4096 of
       Table 2).  Reading: 0 <= p - q < W, i.e. W keys including the query
-      itself, so W >= N is plain causal attention.
+      itself, so W >= N is plain causal attention.  With ``sink_tokens`` S
+      > 0 the first S positions stay visible as well (the Bifocal page,
+      "Comparison at equal memory" and "Details": the SWA student with
+      StreamingLLM sink tokens keeps a 572-token window plus the first 4
+      tokens of the sequence): M(p, q) = window or (q < S and q <= p).
+      Reading: the sink tokens obey causality like every other key.
     - block, B = param: the block-selection matrix expanded to tokens,
       M_B[p, q] = B[floor(p/B), floor(q/B)] and q <= p (RRAttention, section
       2.1, Eq. 1-2).  Reading: block indices are 0-based (Eq. 2 uses floor);
@@ -74,7 +79,10 @@ def allowed(kind: str, param: int, p: np.ndarray, q: np.ndarray,
     if kind == "sliding":
         return np.abs(p - q) <= param
     if kind == "causal_window":
-        return (p - q >= 0) & (p - q < param)
+        win = (p - q >= 0) & (p - q < param)
+        if sink_tokens > 0:
+            win = win | ((q < sink_tokens) & (q <= p))
+        return win
     if kind == "block":
         if block_h is None:
             raise ValueError("block mask needs the block-selection matrix")
@@ -114,6 +122,10 @@ def _head_perm(spec, h: int):
     return perms[h]
 
 
+def _sink_tokens(spec) -> int:
+    return int(getattr(spec, "sink_tokens", 0) or 0)
+
+
 def _head_sink(spec, h: int) -> Optional[float]:
     sink = getattr(spec, "sink", None)
     if sink is None:
@@ -126,9 +138,13 @@ def attention(q, k, v, spec, rows: Optional[Sequence[int]] = None,
               scale: Optional[float] = None, row_block: int = 256):
     """Masked attention forward in fp64, the plain definition.
 
-    q, k, v: arrays [B, H, N, d] of any float dtype (upcast exactly to fp64;
-    bf16 and fp32 values are exact in fp64).  ``spec`` describes the mask
-    (kind, head_param[h], perm[h], block, sink).
+    q: array [B, H, N, d]; k, v: arrays [B, H_kv, N, d] with H a multiple
+    of H_kv, of any float dtype (upcast exactly to fp64; bf16 and fp32
+    values are exact in fp64).  H_kv < H is grouped-query attention (the
+    Bifocal page, "Comparison at equal memory": 32 query heads sharing 8
+    key/value heads): query head h reads key/value head h // (H / H_kv),
+    consecutive query heads forming a group.  ``spec`` describes the mask
+    (kind, head_param[h], perm[h], block, sink), per query head.
 
     ``heads``: iterable of (b, h) pairs to compute (default: all).
     ``rows``: caller token indices to compute for every selected head
@@ -154,6 +170,10 @@ def attention(q, k, v, spec, rows: Optional[Sequence[int]] = None,
     k = np.asarray(k)
     v = np.asarray(v)
     bsz, nh, n, d = q.shape
+    nkv = k.shape[1]
+    if nh % nkv or v.shape[1] != nkv:
+        raise ValueError("the query head count must be a multiple of the key/value head count")
+    group = nh // nkv
     if heads is None:
         heads = [(b, h) for b in range(bsz) for h in range(nh)]
     heads = list(heads)
@@ -163,8 +183,8 @@ def attention(q, k, v, spec, rows: Optional[Sequence[int]] = None,
     o_out = np.zeros((len(heads), len(rows), d), dtype=np.float64)
     lse_out = np.full((len(heads), len(rows)), -np.inf, dtype=np.float64)
     for hi, (b, h) in enumerate(heads):
-        kh = np.asarray(k[b, h], dtype=np.float64)
-        vh = np.asarray(v[b, h], dtype=np.float64)
+        kh = np.asarray(k[b, h // group], dtype=np.float64)
+        vh = np.asarray(v[b, h // group], dtype=np.float64)
         pos = inverse_permutation(_head_perm(spec, h), n)
         param = _head_param(spec, h)
         blk = _head_block(spec, h)
@@ -174,7 +194,7 @@ def attention(q, k, v, spec, rows: Optional[Sequence[int]] = None,
             qh = np.asarray(q[b, h][r], dtype=np.float64)
             s = scale * (qh @ kh.T)                          # step 1
             keep = allowed(spec.kind, param, pos[r][:, None],
-                           pos[None, :], blk)                # step 2
+                           pos[None, :], blk, _sink_tokens(spec))  # step 2
             s = np.where(keep, s, -np.inf)
             m = s.max(axis=1)                                # step 3
             if sink is not None:
@@ -210,7 +230,7 @@ def attention_probabilities(q, k, spec, b: int, h: int,
     pos = inverse_permutation(_head_perm(spec, h), n)
     s = scale * (q @ k.T)
     keep = allowed(spec.kind, _head_param(spec, h), pos[:, None], pos[None, :],
-                   _head_block(spec, h))
+                   _head_block(spec, h), _sink_tokens(spec))
     s = np.where(keep, s, -np.inf)
     sink = _head_sink(spec, h)
     m = s.max(axis=1)
@@ -261,7 +281,7 @@ def received_attention(q, k, spec, heads: Optional[Iterable[Tuple[int, int]]] = 
             r = np.arange(r0, min(n, r0 + row_block))
             qh = np.asarray(q[b, h][r], dtype=np.float64)
             s = scale * (qh @ kh.T)
-            keep = allowed(spec.kind, param, pos[r][:, None], pos[cols][None, :], blk)
+            keep = allowed(spec.kind, param, pos[r][:, None], pos[cols][None, :], blk, _sink_tokens(spec))
             fin = np.isfinite(lse[r])[:, None]
             a = np.where(keep & fin, np.exp(np.where(keep, s, 0.0) - np.where(fin, lse[r][:, None], 0.0)), 0.0)
             out[hi] += a.sum(axis=0)
@@ -272,7 +292,7 @@ def dense_mask_strip(spec, h: int, n: int, p0: int, p1: int) -> np.ndarray:
     """Rows p0..p1-1 of the mask M in *position* space, bool [p1-p0, n]."""
     p = np.arange(p0, p1, dtype=np.int64)[:, None]
     qq = np.arange(n, dtype=np.int64)[None, :]
-    return allowed(spec.kind, _head_param(spec, h), p, qq, _head_block(spec, h))
+    return allowed(spec.kind, _head_param(spec, h), p, qq, _head_block(spec, h), _sink_tokens(spec))
 
 
 def tile_list(spec, h: int, n: int, tile: int = 128) -> List[Tuple[int, int, int]]:

@@ -46,10 +46,11 @@ def test_status_strings_and_version(L):
 
 
 def test_struct_layout_matches_header():
-    # x86-64 / aarch64 LP64: 4+4 + 8 + 8 + 4+4 + 8 + 4(+4) + 8 + 4(+4) + 8 + 4 + 4
-    assert ctypes.sizeof(mattn.MaskDesc) == 80
+    # x86-64 / aarch64 LP64: 4+4 + 8 + 8 + 4+4 + 8 + 4(+4) + 8 + 4(+4) + 8 + 4 + 4 + 4(+4)
+    assert ctypes.sizeof(mattn.MaskDesc) == 88
     assert mattn.MaskDesc.block_bits.offset == 48
     assert mattn.MaskDesc.sink.offset == 64
+    assert mattn.MaskDesc.sink_tokens.offset == 80
 
 
 def _desc(kind, param, **kw):
@@ -80,8 +81,20 @@ def test_invalid_arguments_rejected_on_host(L):
     cm = _desc(2, 3, head_order=order, grid_rows=3, grid_cols=5)
     assert L.mattn_count_pairs(ctypes.byref(cm), 1, 1, 16, ctypes.byref(out)) == mattn.ERR_INVALID_ARG
     assert b"grid_rows" in L.mattn_last_error()
+    # sink tokens: causal windows only, never negative
+    assert L.mattn_count_pairs(ctypes.byref(_desc(2, 3, sink_tokens=4)), 1, 1, 16, ctypes.byref(out)) == \
+        mattn.ERR_INVALID_ARG
+    assert L.mattn_count_pairs(ctypes.byref(_desc(3, 3, sink_tokens=-1)), 1, 1, 16, ctypes.byref(out)) == \
+        mattn.ERR_INVALID_ARG
+    assert L.mattn_count_pairs(ctypes.byref(_desc(3, 3, sink_tokens=4)), 1, 1, 16, ctypes.byref(out)) == mattn.OK
     # mattn_fwd validates before touching a device
     d = _desc(2, 3)
+    x16 = ctypes.c_void_p(16)
+    # grouped-query attention: H must be a multiple of H_kv
+    assert L.mattn_fwd_gqa(x16, x16, x16, x16, None, 1, 6, 4, 16, 64, 0, ctypes.byref(d), None) == \
+        mattn.ERR_INVALID_ARG
+    assert L.mattn_fwd_gqa(x16, x16, x16, x16, None, 1, 6, 0, 16, 64, 0, ctypes.byref(d), None) == \
+        mattn.ERR_INVALID_ARG
     x = ctypes.c_void_p(16)
     assert L.mattn_fwd(x, x, x, x, None, 1, 1, 16, 72, 0, ctypes.byref(d), None) == mattn.ERR_UNSUPPORTED
     assert L.mattn_fwd(None, x, x, x, None, 1, 1, 16, 64, 0, ctypes.byref(d), None) == mattn.ERR_INVALID_ARG
@@ -117,6 +130,11 @@ def _spec_cases(n):
     yield "chunk", MaskSpec("chunk", [64, 200])
     yield "sliding", MaskSpec("sliding", [32, 300])
     yield "causal", MaskSpec("causal_window", [128, 77])
+    # causal windows with sink tokens: 4 sinks (one partial tile), sinks over
+    # more than one tile, a window that reaches back into the sinks
+    yield "causal_sink4", MaskSpec("causal_window", [128, 77], sink_tokens=4)
+    yield "causal_sink130", MaskSpec("causal_window", [572, 300], sink_tokens=130)
+    yield "causal_sink128", MaskSpec("causal_window", [40, 200], sink_tokens=128)
     for bs in (128, 256):
         nb = -(-n // bs)
         yield f"block{bs}", MaskSpec("block", [bs, bs], block=bernoulli_causal_blocks(2, nb, bs))

@@ -420,3 +420,90 @@ def test_received_attention_matches_brute_force(kind, param):
         rb = brute.received_head(q[0, 0].tolist(), k[0, 0].tolist(), kind, param, perm=pm,
                                  block=None if block is None else block.tolist(), sink=sink)
         np.testing.assert_allclose(r, rb, rtol=1e-12, atol=1e-15)
+
+
+# -- grouped-query attention --------------------------------------------------------
+
+@pytest.mark.parametrize("kind,param", [("full", 0), ("causal_window", 5), ("sliding", 3)])
+def test_gqa_equals_mha_with_repeated_kv(kind, param):
+    """Grouped-query attention (the Bifocal page: 32 query heads sharing 8
+    key/value heads) is multi-head attention whose key/value heads are
+    repeated for the consecutive query heads of their group.  Catches a
+    wrong head mapping (h % H_kv instead of h // group) or K and V taken
+    from different heads."""
+    B, H, Hkv, n, d = 2, 6, 2, 19, 4
+    q = _rand((B, H, n, d), 1)
+    k = _rand((B, Hkv, n, d), 2)
+    v = _rand((B, Hkv, n, d), 3)
+    spec = MaskSpec(kind, [param] * H, sink=np.linspace(-1.0, 1.0, H))
+    o, lse = dense.attention(q, k, v, spec)
+    kr, vr = np.repeat(k, H // Hkv, axis=1), np.repeat(v, H // Hkv, axis=1)
+    o2, lse2 = dense.attention(q, kr, vr, spec)
+    np.testing.assert_array_equal(o, o2)
+    np.testing.assert_array_equal(lse, lse2)
+    # and head by head against the brute force on the shared key/value head
+    for b in range(B):
+        for h in range(H):
+            bo, blse = brute.attention_head(q[b, h].tolist(), kr[b, h].tolist(), vr[b, h].tolist(), kind, param,
+                                            sink=spec.sink[h])
+            np.testing.assert_allclose(o[b * H + h], np.array(bo), rtol=0, atol=1e-12)
+            np.testing.assert_allclose(lse[b * H + h], np.array(blse), rtol=0, atol=1e-12)
+
+
+# -- causal window with sink tokens (StreamingLLM) ------------------------------------
+
+def test_sink_token_budget_worked_example():
+    """The Bifocal page gives the SWA student with sink tokens a 572-token
+    window plus the first 4 tokens, for the same 576 cached tokens per layer
+    as the 576-token window of the other student: a query far from the
+    start sees exactly 576 keys (catches a window of W + 1 keys, or sink
+    tokens counted when the window already covers them)."""
+    for n, w, s, p, count, first in read_golden("swa_sink_tokens_budget.txt"):
+        n, w, s, p, count, first = map(int, (n, w, s, p, count, first))
+        spec = MaskSpec("causal_window", [w], sink_tokens=s)
+        row = dense.dense_mask_strip(spec, 0, n, p, p + 1)[0]
+        assert int(row.sum()) == count
+        keys = np.nonzero(row)[0]
+        assert keys[0] == 0 and keys[-1] == p
+        assert int(keys[min(s, len(keys) - 1)]) == first  # the first key after the sinks
+        got = brute.neighbour_set("causal_window", w, n, p, list(range(n)), sink_tokens=s)
+        assert got == list(keys)
+
+
+@pytest.mark.parametrize("n,w,s", [(64, 9, 3), (200, 50, 4), (300, 128, 40)])
+def test_sink_token_pair_count_closed_form(n, w, s):
+    """Rows p >= W see W window keys plus min(S, p - W + 1) sink keys below
+    the window; rows p < W see all p + 1 keys: pairs = N W - W (W - 1) / 2 +
+    S (S + 1) / 2 + S (N - W - S) for N - W >= S."""
+    spec = MaskSpec("causal_window", [w], sink_tokens=s)
+    expect = n * w - w * (w - 1) // 2 + s * (s + 1) // 2 + s * (n - w - s)
+    assert dense.pair_count(spec, n) == expect
+
+
+def test_sink_tokens_change_nothing_when_the_window_covers_all():
+    """W >= N already sees every earlier key (plain causal attention)."""
+    n, d = 23, 4
+    q, k, v = (_rand((1, 1, n, d), s) for s in (4, 5, 6))
+    a = dense.attention(q, k, v, MaskSpec("causal_window", [n], sink_tokens=5))
+    b = dense.attention(q, k, v, MaskSpec("causal_window", [n]))
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("n,d", [(12, 4), (16, 3)])
+def test_sink_tokens_match_brute_force(n, d):
+    """Independent enumeration of the window-plus-sinks neighbour sets, with
+    and without a permutation and a sink logit."""
+    q, k, v = (_rand((1, 1, n, d), s + 7 * n) for s in (1, 2, 3))
+    perm = random_order(n, n + 1)
+    for w, s in ((3, 2), (4, 5), (1, 1)):
+        for use_perm in (False, True):
+            for sink in (None, -0.4):
+                spec = _one_head("causal_window", w, perm=perm if use_perm else None, sink=sink)
+                spec.sink_tokens = s
+                o, lse = dense.attention(q, k, v, spec)
+                bo, blse = brute.attention_head(q[0, 0].tolist(), k[0, 0].tolist(), v[0, 0].tolist(),
+                                                "causal_window", w, perm if use_perm else None, None, sink,
+                                                sink_tokens=s)
+                np.testing.assert_allclose(o[0], np.array(bo), rtol=0, atol=1e-12)
+                np.testing.assert_allclose(lse[0], np.array(blse), rtol=0, atol=1e-12)

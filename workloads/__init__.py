@@ -40,6 +40,8 @@ class MaskSpec:
                 passing the array).
     block:      bool [H, Nb, Nb] block-selection matrices (kind "block").
     sink:       float [H] sink logits, or None.
+    sink_tokens: kind "causal_window": the first sink_tokens positions stay
+                visible to every query at or after them (0 = none).
     """
 
     kind: str
@@ -49,6 +51,7 @@ class MaskSpec:
     block: Optional[np.ndarray] = None
     sink: Optional[np.ndarray] = None
     name: str = ""
+    sink_tokens: int = 0
 
 
 def column_major_order(rows: int, cols: int) -> np.ndarray:
@@ -98,6 +101,7 @@ class Workload:
     grid: Optional[tuple]
     masks: Sequence[str]
     description: str
+    kv_heads: Optional[int] = None  # grouped-query attention: K / V heads (None = H)
 
 
 WORKLOADS = {
@@ -124,6 +128,13 @@ WORKLOADS = {
         ("block128",),
         "128K prefill B1 H32 d128 bf16 N(0,1); block 128 (Nb 1024): diagonal and "
         "first column kept, other causal blocks Bernoulli(0.5), per head"),
+    "gqa32k": Workload(
+        "gqa32k", 1, 32, 32768, 128, "bf16", 1.0, None,
+        ("swa572_sinktok4", "swa576_sink"),
+        "LM prefill with grouped-query attention (Qwen3-4B layout: 32 query heads "
+        "sharing 8 K/V heads, d128), B1 N32768 bf16 N(0,1); causal window 572 plus "
+        "the first 4 tokens (StreamingLLM sink tokens), or window 576 with a "
+        "learned sink logit ~ N(0,1) per head", kv_heads=8),
 }
 
 
@@ -160,6 +171,12 @@ def make_mask(wl: Workload, mask: str, seed: int = 0, n: Optional[int] = None,
         windows = rng.permutation(sizes)
         sink = rng.standard_normal(nh)
         return MaskSpec("causal_window", [int(x) for x in windows], sink=sink, name=mask)
+    if mask.startswith("swa") and "_sinktok" in mask:
+        w, s = mask[3:].split("_sinktok")
+        return MaskSpec("causal_window", [int(w)] * nh, sink_tokens=int(s), name=mask)
+    if mask.startswith("swa") and mask.endswith("_sink"):
+        rng = np.random.default_rng(seed)
+        return MaskSpec("causal_window", [int(mask[3:-5])] * nh, sink=rng.standard_normal(nh), name=mask)
     if mask.startswith("block"):
         bs = int(mask[5:])
         nb = (n + bs - 1) // bs
@@ -169,8 +186,9 @@ def make_mask(wl: Workload, mask: str, seed: int = 0, n: Optional[int] = None,
 
 
 def make_qkv(B: int, H: int, N: int, d: int, dtype: str = "bf16", value_scale: float = 1.0,
-             seed: int = 0, device: str = "cpu"):
-    """Seeded q, k, v tensors [B, H, N, d] (torch), drawn in the order q, k, v.
+             seed: int = 0, device: str = "cpu", kv_heads: Optional[int] = None):
+    """Seeded q [B, H, N, d] and k, v [B, kv_heads, N, d] tensors (torch;
+    kv_heads defaults to H), drawn in the order q, k, v.
 
     fp32 draws from N(0,1), multiplied by ``value_scale``, then cast to the
     dtype.  On a CUDA device the CUDA generator is used (different stream of
@@ -182,8 +200,9 @@ def make_qkv(B: int, H: int, N: int, d: int, dtype: str = "bf16", value_scale: f
     g = torch.Generator(device=device).manual_seed(seed)
     tdt = {"bf16": torch.bfloat16, "f32": torch.float32}[dtype]
     out = []
-    for _ in range(3):
-        x = torch.randn((B, H, N, d), generator=g, device=device, dtype=torch.float32)
+    for i in range(3):
+        nh = H if (i == 0 or kv_heads is None) else kv_heads
+        x = torch.randn((B, nh, N, d), generator=g, device=device, dtype=torch.float32)
         if value_scale != 1.0:
             x.mul_(value_scale)
         out.append(x.to(tdt))
@@ -194,4 +213,5 @@ def make_workload_inputs(wl: Workload, seed: int = 0, device: str = "cpu",
                          n: Optional[int] = None, heads: Optional[int] = None):
     n = wl.N if n is None else n
     nh = wl.H if heads is None else heads
-    return make_qkv(wl.B, nh, n, wl.d, wl.dtype, wl.value_scale, seed, device)
+    kv = None if wl.kv_heads is None else max(1, wl.kv_heads * nh // wl.H)
+    return make_qkv(wl.B, nh, n, wl.d, wl.dtype, wl.value_scale, seed, device, kv_heads=kv)
