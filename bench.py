@@ -292,6 +292,9 @@ def run_gpu(args):
             flush_buf.zero_()
 
         for name, wlx in WORKLOADS.items():
+            if name.startswith("decode"):
+                workloads.update(decode_sweep(name, wlx, dev, peaks))
+                continue
             qx, kx, vx = make_workload_inputs(wlx, seed=0, device=dev)
             in_bytes = (qx.numel() + kx.numel() + vx.numel()) * qx.element_size()
             for m in wlx.masks:
@@ -380,6 +383,51 @@ def run_gpu(args):
 
 
 # ------------------------------------------------------------------ other stages (profiling aid)
+def decode_visible_keys(spec, h: int, length: int) -> int:
+    """Keys the decode query (position length - 1) of head h sees."""
+    if spec.kind == "full":
+        return length
+    w = int(spec.head_param[h])
+    win = min(w, length)
+    return win + max(0, min(int(spec.sink_tokens or 0), length - win))
+
+
+def decode_sweep(name, wl, dev, peaks):
+    """Decode steps of a workload: one query per sequence against a full
+    cache of wl.N tokens.  HBM-bound: the K and V rows each step reads."""
+    import torch
+    import block_sparse_attention_masked_gb300 as mattn
+    from workloads import make_decode_inputs, make_mask
+
+    q, k, v = make_decode_inputs(wl, seed=0, device=dev)
+    flush_buf = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    out = {}
+    kv = wl.kv_heads or wl.H
+    for m in wl.masks:
+        sp = make_mask(wl, m, seed=0)
+        mk = mattn.prepare(sp, wl.H, wl.N, device=dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((wl.B, wl.H), dtype=torch.float32, device=dev)
+        # distinct K/V rows read: the union of the group's visible keys (the
+        # heads of a group share one window size here)
+        rows = wl.B * kv * decode_visible_keys(sp, 0, wl.N)
+        big = rows * wl.d * 4 > 2 * 129e6
+        med, _ = time_kernel(lambda: mattn.decode(q, k, v, mk, out=o, lse=lse), 20, 3,
+                             flush=None if big else (lambda: flush_buf.zero_()))
+        pairs = wl.B * sum(decode_visible_keys(sp, h, wl.N) for h in range(wl.H))
+        group = wl.H // kv
+        bytes_rw = 2 * rows * wl.d * 2 + q.numel() * 2 * 2 + lse.numel() * 4
+        gbs = bytes_rw / (med * 1e-3) / 1e9
+        out[f"{name}/{m}"] = {
+            "ms": round(med, 4), "tflops": round(4.0 * wl.d * pairs / (med * 1e-3) / 1e12, 2),
+            "hbm_gbs": round(gbs, 1), "pct_hbm": round(100 * gbs / peaks["hbm_gbs"], 1),
+            "kv_rows_read": rows, "query_heads_per_kv_head": group,
+            "l2": "rows read larger than L2" if big else "flushed (512 MiB write) before each run"}
+    del q, k, v, flush_buf
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_stage(args):
     """Time RRAttention's block selection (stride 8, block 128, tau 0.95) or
     the received attention on the headline workload's inputs: warm-up, then

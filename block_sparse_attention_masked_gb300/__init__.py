@@ -74,7 +74,8 @@ class MaskDesc(ctypes.Structure):
 
 
 EXPORTS = (
-    "mattn_fwd", "mattn_fwd_gqa", "mattn_fwd_host", "mattn_fwd_noalloc", "mattn_rr_select", "mattn_received",
+    "mattn_fwd", "mattn_fwd_gqa", "mattn_fwd_host", "mattn_fwd_noalloc", "mattn_decode", "mattn_rr_select",
+    "mattn_received",
     "mattn_count_pairs", "mattn_plan_tiles", "mattn_plan_tiles_device",
     "mattn_device_status", "mattn_set_wait_timeout_ns", "mattn_status_string", "mattn_last_error",
     "mattn_version",
@@ -96,6 +97,7 @@ def lib() -> ctypes.CDLL:
     dp = ctypes.POINTER(MaskDesc)
     L.mattn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, dp, vp]
     L.mattn_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, dp, vp]
+    L.mattn_decode.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, dp, vp]
     L.mattn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, dp, vp]
     L.mattn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, dp, vp,
                                     ctypes.POINTER(ctypes.c_uint32)]
@@ -112,7 +114,7 @@ def lib() -> ctypes.CDLL:
     L.mattn_last_error.restype = ctypes.c_char_p
     L.mattn_last_error.argtypes = []
     L.mattn_version.argtypes = []
-    for name in ("mattn_fwd", "mattn_fwd_gqa", "mattn_fwd_host", "mattn_fwd_noalloc", "mattn_rr_select", "mattn_received",
+    for name in ("mattn_fwd", "mattn_fwd_gqa", "mattn_fwd_host", "mattn_fwd_noalloc", "mattn_decode", "mattn_rr_select", "mattn_received",
                  "mattn_count_pairs", "mattn_plan_tiles",
                  "mattn_plan_tiles_device", "mattn_device_status", "mattn_set_wait_timeout_ns",
                  "mattn_version"):
@@ -260,6 +262,39 @@ def attention(q, k, v, mask: PreparedMask, out=None, lse=None, want_lse: bool = 
         rc = lib().mattn_fwd(*args, B, H, N, d, _dtype_code(q), ctypes.byref(mask.desc), stream)
     else:
         rc = lib().mattn_fwd_gqa(*args, B, H, H_kv, N, d, _dtype_code(q), ctypes.byref(mask.desc), stream)
+    _check(rc)
+    return out, lse
+
+
+def decode(q, k_cache, v_cache, mask: PreparedMask, seq_lens=None, out=None, lse=None, want_lse: bool = True,
+           stream=None):
+    """One query per sequence against its key/value cache (``mattn_decode``).
+
+    q: CUDA bf16 [B, H, d]; k_cache, v_cache: [B, H_kv, L, d]; seq_lens:
+    CUDA int32 [B] (cached tokens with the new one; None = L).  ``mask``
+    is prepared for H heads (kind "full" or "causal_window"; its N is not
+    used).  Returns (o [B, H, d], lse [B, H] fp32 or None)."""
+    import torch
+
+    for t in (q, k_cache, v_cache):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k_cache and v_cache must be contiguous CUDA tensors")
+    B, H, d = q.shape
+    _, H_kv, L, _ = k_cache.shape
+    if k_cache.shape != (B, H_kv, L, d) or v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache must be [B, H_kv, L, d]")
+    if seq_lens is not None and (seq_lens.dtype != torch.int32 or seq_lens.shape != (B,) or not seq_lens.is_cuda):
+        raise ValueError("seq_lens must be a CUDA int32 tensor [B]")
+    if out is None:
+        out = torch.empty_like(q)
+    if want_lse and lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    rc = lib().mattn_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(),
+                            lse.data_ptr() if lse is not None else None,
+                            seq_lens.data_ptr() if seq_lens is not None else None,
+                            B, H, H_kv, L, d, _dtype_code(q), ctypes.byref(mask.desc), stream)
     _check(rc)
     return out, lse
 

@@ -125,6 +125,34 @@ struct RecvParams {
 cudaError_t launch_received(const RecvParams& p, const float* lse, int d, cudaStream_t stream);
 size_t received_smem_bytes(int d);
 
+// Decode-shaped attention (decode.cu): one query per sequence against its
+// key/value cache, split over the cache into chunks.
+struct DecodeParams {
+  const void* q;              // [B][H][D] bf16
+  const void* k;              // [B][H_kv][L][D] bf16
+  const void* v;              // [B][H_kv][L][D] bf16
+  const int32_t* seq_lens;    // [B] cached tokens per sequence (new token included), or null: L
+  const int32_t* head_info;   // [H][4], HeadField (kHeadParam: the window W)
+  const float* sink;          // [H] or null
+  float* part_o;              // [B*H][n_split][D] chunk states: unnormalised O
+  float* part_ml;             // [B*H][n_split][2] chunk states: max (log2 domain), sum
+  void* o;                    // [B][H][D] bf16 or fp32
+  float* lse;                 // [B][H] or null
+  int B, H, H_kv, L;
+  int n_split, chunk;         // chunks per sequence, keys per chunk
+  int kind;                   // kFull or kCausalWindow
+  int sink_tokens;
+  float scale_log2;
+  int out_f32;
+  uint32_t* err;              // device error word (a ring wait that gave up)
+  unsigned long long timeout_ns;
+};
+
+// Most chunks per sequence a decode launch uses.
+constexpr int kDecodeMaxSplits = 1024;
+
+cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream);
+
 // Launchers (attention_fwd.cu).
 cudaError_t launch_attention(const FwdParams& p, int d, bool out_f32, cudaStream_t stream);
 size_t attention_smem_bytes(int d);

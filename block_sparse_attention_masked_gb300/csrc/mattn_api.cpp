@@ -265,6 +265,8 @@ struct DeviceState {
   DeviceBuf rr_ksum;   // block selection: stride key sums
   DeviceBuf rr_scores; // block selection: block scores when the caller passes none
   DeviceBuf recv_lse;  // received attention: the lse in position order
+  DeviceBuf dec_part;  // decode: per-chunk softmax states
+  std::map<std::string, std::unique_ptr<DeviceBuf>> dec_heads;  // decode: per-head tables by content
   std::map<std::string, std::unique_ptr<Plan>> plans;
 };
 
@@ -681,6 +683,98 @@ int mattn_fwd_host(const void* q, const void* k, const void* v, void* o, float* 
   MATTN_CUDA(cudaMemcpyAsync(o, dout, tensor, cudaMemcpyDeviceToHost, stream), "copy o");
   if (lse) MATTN_CUDA(cudaMemcpyAsync(lse, dlse, lse_bytes, cudaMemcpyDeviceToHost, stream), "copy lse");
   MATTN_CUDA(cudaStreamSynchronize(stream), "stream sync");
+  return MATTN_OK;
+}
+
+int mattn_decode(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* seq_lens, int B,
+                 int H, int H_kv, int L, int d, int dtype, const mattn_mask_desc* desc, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  std::lock_guard<std::mutex> lk(g_mutex);
+  if (!desc) return fail(MATTN_ERR_INVALID_ARG, "mask descriptor is NULL");
+  if (!q || !k || !v || !o) return fail(MATTN_ERR_INVALID_ARG, "q, k, v and o must be non-NULL");
+  if (B < 1 || H < 1 || H_kv < 1 || L < 1) return fail(MATTN_ERR_INVALID_ARG, "B, H, H_kv, L must be >= 1");
+  if (H % H_kv) return fail(MATTN_ERR_INVALID_ARG, "H = %d is not a multiple of H_kv = %d", H, H_kv);
+  if (H / H_kv > 8) return fail(MATTN_ERR_UNSUPPORTED, "decode supports up to 8 query heads per key/value head");
+  if (d != 64 && d != 128 && d != 256) return fail(MATTN_ERR_UNSUPPORTED, "decode head dim %d (64, 128, 256)", d);
+  if (dtype != MATTN_BF16) return fail(MATTN_ERR_UNSUPPORTED, "decode takes bf16 q, k, v");
+  if (desc->kind != MATTN_FULL && desc->kind != MATTN_CAUSAL_WINDOW)
+    return fail(MATTN_ERR_UNSUPPORTED, "decode masks: MATTN_FULL or MATTN_CAUSAL_WINDOW (got kind %d)", desc->kind);
+  if (desc->head_order)
+    for (int h = 0; h < H; ++h)
+      if (desc->head_order[h] != MATTN_ORDER_RASTER)
+        return fail(MATTN_ERR_UNSUPPORTED, "decode reads the cache in sequence order (head_order must be raster)");
+  if (desc->sink_tokens < 0) return fail(MATTN_ERR_INVALID_ARG, "sink_tokens must be >= 0");
+  if (desc->sink_tokens > 0 && desc->kind != MATTN_CAUSAL_WINDOW)
+    return fail(MATTN_ERR_INVALID_ARG, "sink_tokens applies to MATTN_CAUSAL_WINDOW masks only");
+  if (!(desc->softmax_scale >= 0.f) || std::isinf(desc->softmax_scale))
+    return fail(MATTN_ERR_INVALID_ARG, "softmax_scale must be finite and >= 0");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+    return fail(MATTN_ERR_UNSUPPORTED, "q, k, v and o must be 16-byte aligned");
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return fail(MATTN_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+  if (seq_lens && (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return fail(MATTN_ERR_INVALID_ARG, "seq_lens must be 4-byte aligned");
+  std::vector<int32_t> head((size_t)H * 4, 0);
+  for (int h = 0; h < H; ++h) {
+    const int w = desc->head_param ? desc->head_param[h] : desc->param;
+    if (desc->kind == MATTN_CAUSAL_WINDOW && w < 1)
+      return fail(MATTN_ERR_INVALID_ARG, "window of head %d must be >= 1 (got %d)", h, w);
+    head[(size_t)h * 4 + kHeadParam] = desc->kind == MATTN_CAUSAL_WINDOW ? w : 0;
+  }
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc) return rc;
+  int dev = 0, sms = 0;
+  MATTN_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  MATTN_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "SM count");
+  // chunks of the keys a key/value head's query heads may see (every
+  // cached key, or at most the widest window plus the sink tokens): one
+  // CTA per SM over the launch, 64-key multiples, at most kDecodeMaxSplits
+  int64_t nvis = L;
+  if (desc->kind == MATTN_CAUSAL_WINDOW) {
+    int64_t wmax = 1;
+    for (int h = 0; h < H; ++h) wmax = std::max<int64_t>(wmax, head[(size_t)h * 4 + kHeadParam]);
+    nvis = std::min<int64_t>(L, wmax + desc->sink_tokens);
+  }
+  const int64_t groups = (int64_t)B * H_kv;
+  int64_t want = ((int64_t)sms + groups - 1) / groups;
+  if (want < 1) want = 1;
+  int64_t chunk = ((nvis + want - 1) / want + 63) / 64 * 64;
+  const int64_t min_chunk = ((nvis + kDecodeMaxSplits - 1) / kDecodeMaxSplits + 63) / 64 * 64;
+  chunk = std::max<int64_t>(std::max<int64_t>(chunk, 64), min_chunk);
+  const int n_split = (int)((nvis + chunk - 1) / chunk);
+  const size_t part_floats = (size_t)B * H * n_split * ((size_t)d + 2);
+  if ((rc = st->dec_part.reserve(part_floats * sizeof(float), "cudaMalloc(decode chunk states)"))) return rc;
+  // the per-head table, uploaded once per distinct content
+  std::string hkey(reinterpret_cast<const char*>(head.data()), head.size() * sizeof(int32_t));
+  auto hit = st->dec_heads.find(hkey);
+  if (hit == st->dec_heads.end()) {
+    auto buf = std::make_unique<DeviceBuf>();
+    if ((rc = buf->reserve(head.size() * sizeof(int32_t), "cudaMalloc(decode head table)"))) return rc;
+    MATTN_CUDA(cudaMemcpy(buf->ptr, head.data(), head.size() * sizeof(int32_t), cudaMemcpyHostToDevice),
+               "upload decode head table");
+    hit = st->dec_heads.emplace(hkey, std::move(buf)).first;
+  }
+  DecodeParams p;
+  memset(&p, 0, sizeof(p));
+  p.q = q; p.k = k; p.v = v;
+  p.seq_lens = seq_lens;
+  p.head_info = static_cast<const int32_t*>(hit->second->ptr);
+  p.sink = desc->sink;
+  p.part_o = static_cast<float*>(st->dec_part.ptr);
+  p.part_ml = p.part_o + (size_t)B * H * n_split * d;
+  p.o = o;
+  p.lse = lse;
+  p.B = B; p.H = H; p.H_kv = H_kv; p.L = L;
+  p.n_split = n_split;
+  p.chunk = (int)chunk;
+  p.kind = desc->kind == MATTN_CAUSAL_WINDOW ? kCausalWindow : kFull;
+  p.sink_tokens = desc->sink_tokens;
+  const float scale = desc->softmax_scale > 0.f ? desc->softmax_scale : 1.0f / std::sqrt((float)d);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.out_f32 = 0;
+  p.err = st->err;
+  p.timeout_ns = wait_timeout_ns();
+  MATTN_CUDA(launch_decode(p, d, stream), "decode launch");
   return MATTN_OK;
 }
 

@@ -151,6 +151,16 @@ __device__ __forceinline__ void tma_load_4d_hint(void* dst, const CUtensorMap* t
       : "memory");
 }
 
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
+// from global to this CTA's shared memory, completing on mbarrier `bar`.
+__device__ __forceinline__ void bulk_load_g2s(void* sdst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(sdst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
 // L2 policies: keep (K, V tiles that many query tiles re-read) or drop
 // first (Q tiles, read once).
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {

@@ -161,6 +161,39 @@ int mattn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* l
                   const mattn_mask_desc* desc, void* stream);
 
 /*
+ * mattn_decode -- decode-shaped attention: one new query token per
+ * sequence against that sequence's key/value cache.  Source: "Sliding
+ * window attention vs. linear attention at equal memory" (Bifocal page),
+ * "Details", the speed test: each request reads a 1K..128K-token prompt,
+ * then generates tokens one by one, with 16 query heads sharing 4
+ * key/value heads of dimension 256; the SWA students keep the last 572 or
+ * 576 tokens (plus 4 sink tokens, or a learned sink logit).  The query of
+ * sequence b sits at position len_b - 1 and sees, per query head h:
+ *   MATTN_FULL            every cached key 0 .. len_b - 1;
+ *   MATTN_CAUSAL_WINDOW   the last W_h cached keys and the first
+ *                         desc->sink_tokens ones;
+ * with the optional learned sink logit in the denominator, as mattn_fwd.
+ *   q        DEVICE bf16 [B][H][d];   o  DEVICE bf16 [B][H][d];
+ *   k, v     DEVICE bf16 [B][H_kv][L][d], the caches (capacity L tokens);
+ *            query head h reads key/value head h / (H / H_kv);
+ *   lse      DEVICE fp32 [B][H] or NULL;
+ *   seq_lens DEVICE int32 [B]: len_b, cached tokens of sequence b with the
+ *            new one, or NULL for len_b = L.  Values outside 0..L are
+ *            clamped to it; len_b = 0 gives O = 0 and LSE = -inf (or the
+ *            sink logit).
+ *   d in {64, 128, 256}; H % H_kv == 0 and H / H_kv <= 8; mask kinds
+ *   MATTN_FULL or MATTN_CAUSAL_WINDOW, raster order (head_order NULL or all
+ *   MATTN_ORDER_RASTER).  Other requests: MATTN_ERR_UNSUPPORTED or
+ *   MATTN_ERR_INVALID_ARG, checked on the host before any launch.
+ * The library splits each cache into chunks processed in parallel and
+ * merges their softmax states (a per-device workspace of B*H*chunks*(d+2)
+ * floats, allocated on first use and reused).  Asynchronous, like mattn_fwd.
+ */
+int mattn_decode(const void* q, const void* k, const void* v, void* o, float* lse,
+                 const int32_t* seq_lens, int B, int H, int H_kv, int L, int d, int dtype,
+                 const mattn_mask_desc* desc, void* stream);
+
+/*
  * mattn_fwd_host -- the same operation on HOST buffers: copies q, k, v (and
  * the sink and block bitmaps, which are then HOST pointers too) to device
  * memory owned by the library, runs mattn_fwd on `stream`, copies o and lse

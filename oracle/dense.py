@@ -333,3 +333,53 @@ def pair_count(spec, n: int, batch: int = 1, n_heads: Optional[int] = None,
         for p0 in range(0, n, strip_rows):
             total += int(dense_mask_strip(spec, h, n, p0, min(n, p0 + strip_rows)).sum())
     return total * batch
+
+
+def decode(q, k, v, seq_lens, spec, scale: Optional[float] = None):
+    """Decode-shaped attention in fp64: one new query per sequence against
+    its key/value cache (the Bifocal page, "Details": the speed test reads a
+    prompt, then generates one token at a time; 16 query heads share 4
+    key/value heads of dimension 256).
+
+    q: [B, H, d], the query of sequence b's newest token, which sits at
+    position len_b - 1; k, v: [B, H_kv, L, d] caches whose first len_b rows
+    are valid (seq_lens[b] = len_b; None means L).  Query head h reads
+    key/value head h // (H / H_kv).  The keys it may see are those of
+    ``allowed`` for p = len_b - 1 (full: all len_b keys; causal window W:
+    the last W, plus the first ``sink_tokens``), and the softmax with the
+    optional sink logit is the one of ``attention``: m = max(kept scores,
+    sink), Z = sum exp(s - m) + exp(sink - m), o = sum exp(s - m) v / Z,
+    lse = m + ln Z; no kept key and no sink gives o = 0, lse = -inf.
+    Returns (o [B, H, d], lse [B, H]) in float64.
+    """
+    q = np.asarray(q)
+    k = np.asarray(k)
+    v = np.asarray(v)
+    bsz, nh, d = q.shape
+    nkv, L = k.shape[1], k.shape[2]
+    group = nh // nkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    lens = [L] * bsz if seq_lens is None else [int(x) for x in np.asarray(seq_lens)]
+    o_out = np.zeros((bsz, nh, d), dtype=np.float64)
+    lse_out = np.full((bsz, nh), -np.inf, dtype=np.float64)
+    for b in range(bsz):
+        n = max(0, min(L, lens[b]))
+        for h in range(nh):
+            kh = np.asarray(k[b, h // group, :n], dtype=np.float64)
+            vh = np.asarray(v[b, h // group, :n], dtype=np.float64)
+            s = scale * (kh @ np.asarray(q[b, h], dtype=np.float64))
+            keep = allowed(spec.kind, _head_param(spec, h), np.int64(n - 1), np.arange(n, dtype=np.int64),
+                           None, _sink_tokens(spec))
+            s = np.where(keep, s, -np.inf)
+            sink = _head_sink(spec, h)
+            m = s.max() if n else -np.inf
+            if sink is not None:
+                m = max(m, sink)
+            if not np.isfinite(m):
+                continue
+            e = np.exp(s - m)
+            z = e.sum() + (math.exp(sink - m) if sink is not None else 0.0)
+            o_out[b, h] = (e @ vh) / z
+            lse_out[b, h] = m + math.log(z)
+    return o_out, lse_out

@@ -507,3 +507,36 @@ def test_sink_tokens_match_brute_force(n, d):
                                                 sink_tokens=s)
                 np.testing.assert_allclose(o[0], np.array(bo), rtol=0, atol=1e-12)
                 np.testing.assert_allclose(lse[0], np.array(blse), rtol=0, atol=1e-12)
+
+
+# -- decode ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("kind,param,s", [("full", 0, 0), ("causal_window", 7, 0), ("causal_window", 5, 3)])
+def test_decode_is_the_last_row_of_the_forward(kind, param, s):
+    """A decode step is the forward's row len - 1 over the first len cached
+    tokens, with the new query in that row (catches an off-by-one in the
+    query position, a window counted from the cache capacity instead of
+    the sequence length, or the wrong key/value head)."""
+    B, H, Hkv, L, d = 2, 4, 2, 30, 5
+    k = _rand((B, Hkv, L, d), 11)
+    v = _rand((B, Hkv, L, d), 12)
+    qd = _rand((B, H, d), 13)
+    lens = [L, 17]
+    spec = MaskSpec(kind, [param] * H, sink=np.array([0.3, -0.2, 1.0, 0.0]), sink_tokens=s)
+    o, lse = dense.decode(qd, k, v, lens, spec)
+    for b in range(B):
+        n = lens[b]
+        qf = _rand((1, H, n, d), 14)
+        qf[0, :, n - 1] = qd[b]
+        fo, flse = dense.attention(qf, k[b:b + 1, :, :n], v[b:b + 1, :, :n], spec, rows=[n - 1])
+        np.testing.assert_allclose(o[b], fo[:, 0], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lse[b], flse[:, 0], rtol=0, atol=1e-13)
+
+
+def test_decode_empty_sequence():
+    """len = 0: no key; o = 0 and lse = -inf, or the sink logit alone."""
+    k = _rand((1, 1, 8, 3), 1)
+    q = _rand((1, 2, 3), 2)
+    o, lse = dense.decode(q, k, k, [0], MaskSpec("full", [0, 0], sink=np.array([-np.inf, 0.7])))
+    assert np.all(o == 0)
+    assert lse[0, 0] == -np.inf and lse[0, 1] == pytest.approx(0.7)

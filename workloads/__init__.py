@@ -135,6 +135,13 @@ WORKLOADS = {
         "sharing 8 K/V heads, d128), B1 N32768 bf16 N(0,1); causal window 572 plus "
         "the first 4 tokens (StreamingLLM sink tokens), or window 576 with a "
         "learned sink logit ~ N(0,1) per head", kv_heads=8),
+    "decode128k": Workload(
+        "decode128k", 1, 16, 131072, 256, "bf16", 1.0, None,
+        ("full", "swa576_sink", "swa572_sinktok4"),
+        "decode step after a 128K-token prompt (the speed-test layout: 16 query heads "
+        "sharing 4 K/V heads, d256), B1, one new query per sequence against a full "
+        "bf16 N(0,1) cache of 131072 tokens; full, window 576 with a learned sink "
+        "logit, or window 572 plus 4 sink tokens", kv_heads=4),
 }
 
 
@@ -207,6 +214,20 @@ def make_qkv(B: int, H: int, N: int, d: int, dtype: str = "bf16", value_scale: f
             x.mul_(value_scale)
         out.append(x.to(tdt))
     return tuple(out)
+
+
+def make_decode_inputs(wl: Workload, seed: int = 0, device: str = "cpu"):
+    """Seeded decode inputs (torch): q [B, H, d] (the new tokens' queries),
+    then the caches k, v [B, kv_heads, N, d], drawn in that order."""
+    import torch
+
+    g = torch.Generator(device=device).manual_seed(seed)
+    tdt = {"bf16": torch.bfloat16, "f32": torch.float32}[wl.dtype]
+    kv = wl.kv_heads or wl.H
+    q = torch.randn((wl.B, wl.H, wl.d), generator=g, device=device) * wl.value_scale
+    k = torch.randn((wl.B, kv, wl.N, wl.d), generator=g, device=device) * wl.value_scale
+    v = torch.randn((wl.B, kv, wl.N, wl.d), generator=g, device=device) * wl.value_scale
+    return q.to(tdt), k.to(tdt), v.to(tdt)
 
 
 def make_workload_inputs(wl: Workload, seed: int = 0, device: str = "cpu",
