@@ -440,6 +440,24 @@ def run_stage(args):
     from workloads import WORKLOADS, make_mask, make_workload_inputs
 
     torch.cuda.set_device(0)
+    if args.stage == "decode":
+        from workloads import make_decode_inputs
+
+        wl = WORKLOADS[args.workload or "decode128k"]
+        if args.n:
+            wl = dataclasses.replace(wl, N=args.n)
+        q, k, v = make_decode_inputs(wl, seed=0, device="cuda")
+        dmask = mattn.prepare(make_mask(wl, args.mask or wl.masks[0], seed=0), wl.H, wl.N)
+        o = torch.empty_like(q)
+        lse = torch.empty((wl.B, wl.H), dtype=torch.float32, device="cuda")
+        med, _ = time_kernel(lambda: mattn.decode(q, k, v, dmask, out=o, lse=lse), args.steps, args.warmup)
+        rc, word = mattn.device_status()
+        if rc != 0:
+            raise RuntimeError(f"device error word {word:#x}")
+        print(json.dumps({"stage": "decode", "workload": wl.name, "mask": args.mask or wl.masks[0], "L": wl.N,
+                          "H": wl.H, "H_kv": wl.kv_heads, "d": wl.d, "ms_median": round(med, 4),
+                          "steps": args.steps}), flush=True)
+        return
     wl = WORKLOADS[args.workload or HEADLINE[0]]
     if args.n or args.heads:
         wl = dataclasses.replace(wl, N=args.n or wl.N, H=args.heads or wl.H)
@@ -561,7 +579,7 @@ def main():
     ap.add_argument("--mask", default=None, help="mask of that workload")
     ap.add_argument("--n", type=int, default=0, help="shrink N (profiling cases)")
     ap.add_argument("--heads", type=int, default=0, help="shrink H (profiling cases)")
-    ap.add_argument("--stage", default="attention", choices=["attention", "rr_select", "received"],
+    ap.add_argument("--stage", default="attention", choices=["attention", "rr_select", "received", "decode"],
                     help="profiling aid: time one other stage on the headline inputs instead of the step "
                          "(prints a short line, not the benchmark record)")
     args = ap.parse_args()

@@ -15,8 +15,9 @@
 //     of those heads.  Its producer warp streams the chunk's K and V rows
 //     into a ring of shared-memory slots with bulk async copies (keys of a
 //     cache are contiguous rows, so a slot is one or two copies per tensor),
-//     keeping ~100 KB in flight per SM.  Eight consumer warps take the slots
-//     in turn.  In a slot, KPG = 32 / GP keys at a time: lane l holds dims
+//     keeping ~128 KB in flight per SM; a slot holds 32 keys, in groups of
+//     KPG = 32 / GP keys, and each (slot, group) pair of the ring has one
+//     owner among up to twelve consumer warps.  In a group: lane l holds dims
 //     [l*VPL, (l+1)*VPL) of every query (VPL = D / 32) and of each row, forms
 //     the KPG x GP partial dot products, and a reduce-scatter across the
 //     lanes leaves lane j with the score of pair j = (key j / GP, head
@@ -44,8 +45,6 @@
 namespace mattn {
 namespace {
 
-constexpr int kDecConsumers = 8;                 // consumer warps
-constexpr int kDecThreads = 32 * (kDecConsumers + 1);
 constexpr float kLog2eD = 1.4426950408889634f;
 constexpr float kLn2D = 0.6931471805599453f;
 constexpr int kDecRingBytes = 144 * 1024;
@@ -57,13 +56,25 @@ template <int D, int GP>
 struct DecGeo {
   static constexpr int VPL = D / 32;                  // dims per lane
   static constexpr int KPG = 32 / GP;                 // keys per group (one score per lane)
-  static constexpr int U = KPG > 8 ? KPG : 8;         // keys per ring slot
-  static constexpr int GPS = U / KPG;                 // groups per slot
+  static constexpr int U = 32;                        // keys per ring slot (one bulk copy per tensor)
+  static constexpr int GPS = U / KPG;                 // groups per slot (= GP), each taken by one warp
   static constexpr int kRow = D * 2;                  // bytes of a bf16 row
   static constexpr int kSlot = 2 * U * kRow;          // K rows, then V rows
   static constexpr int NS0 = kDecRingBytes / kSlot;
   static constexpr int NS = NS0 > 32 ? 32 : NS0;      // ring slots
-  static constexpr int kCons = NS < kDecConsumers ? NS : kDecConsumers;  // consumer warps used
+  // consumer warps: twelve (three per SM sub-partition), eight when the
+  // queries and accumulators of G = 8 heads at d = 256 need more registers
+  static constexpr int kConsW = (D * GP >= 2048) ? 8 : 12;
+  static constexpr int kThreads = 32 * (kConsW + 1);  // consumers, then the producer warp
+  // consumer warps that take groups: the largest divisor of NS * GPS up to
+  // kConsW, so that every (ring slot, group) pair has one fixed owner warp
+  static constexpr int largest_divisor(int n, int cap) {
+    int best = 1;
+    for (int k = 1; k <= cap; ++k)
+      if (n % k == 0) best = k;
+    return best;
+  }
+  static constexpr int kCons = largest_divisor(NS * GPS, kConsW);
   static_assert(VPL == 2 || VPL == 4 || VPL == 8, "D must be 64, 128 or 256");
   static_assert(NS >= 2, "ring too small");
 };
@@ -96,8 +107,10 @@ struct DecBar {
 };
 
 template <int D, int GP>
-__global__ void __launch_bounds__(kDecThreads, 1) decode_split_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(DecGeo<D, GP>::kThreads, 1) decode_split_kernel(const DecodeParams p) {
   using Geo = DecGeo<D, GP>;
+  constexpr int kDecConsumers = Geo::kConsW;
+  constexpr int kDecThreads = Geo::kThreads;
   constexpr int VPL = Geo::VPL, KPG = Geo::KPG, U = Geo::U, NS = Geo::NS;
   extern __shared__ __align__(128) uint8_t dsm[];
   uint8_t* ring = dsm;                                               // [NS][2][U][D] bf16
@@ -146,7 +159,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_split_kernel(const Deco
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
       ptx::mbar_init(&bar->full[i], 1);
-      ptx::mbar_init(&bar->empty[i], 1);
+      ptx::mbar_init(&bar->empty[i], Geo::GPS);  // one arrival per group of the slot
     }
     bar->abort_flag = 0;
     ptx::fence_barrier_init();
@@ -218,8 +231,17 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_split_kernel(const Deco
     }
     const int wlo = gl < G ? window_lo(p, p.head_info[(kvh * G + gl) * 4 + kHeadParam], qpos) : len;
     float* wpw = wp + warp * 32;
-    for (int s = warp; s < nslots; s += Geo::kCons) {
+    // Group gi of the chunk's slot s sits in ring slot s % NS.  Each (ring
+    // slot, group) pair has one owner warp, (slot * GPS + gi) % kCons, which
+    // takes that pair's groups in order, round after round: a warp waits for
+    // round r of a ring slot only after it consumed round r - 1 itself, so
+    // the parity of its wait always names the right round (copies land out
+    // of order, so a warp that skipped rounds could mistake an older
+    // round's completed phase for the one it waits for).
+    for (int gid = 0; gid < nslots * Geo::GPS; ++gid) {
+      const int s = gid / Geo::GPS, gi = gid % Geo::GPS;
       const int slot = s % NS;
+      if ((slot * Geo::GPS + gi) % Geo::kCons != warp) continue;  // warp-uniform
       const bool got = ptx::mbar_wait(&bar->full[slot], (s / NS) & 1, p.timeout_ns, abort_flag);
       if (!__all_sync(0xffffffffu, got)) {
         if (lane == 0) {
@@ -230,8 +252,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_split_kernel(const Deco
       }
       const uint8_t* sk = ring + slot * Geo::kSlot + lane * VPL * 2;
       const uint8_t* sv = sk + U * Geo::kRow;
-#pragma unroll
-      for (int gi = 0; gi < Geo::GPS; ++gi) {
+      {
         const int i0 = i_begin + s * U + gi * KPG;  // list index of the group's first key
         // partial dot products of the group's KPG keys with the GP queries
         float part[32];
@@ -404,13 +425,13 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeParams p)
 template <int D, int GP>
 cudaError_t launch_split(const DecodeParams& p, cudaStream_t stream) {
   using Geo = DecGeo<D, GP>;
-  static_assert(kDecConsumers * GP * D * 4 <= Geo::NS * Geo::kSlot, "the warps' O must fit in the ring");
-  const size_t smem = (size_t)Geo::NS * Geo::kSlot + sizeof(DecBar) + kDecConsumers * 32 * sizeof(float) +
-                      kDecConsumers * GP * 2 * sizeof(float);
+  static_assert(Geo::kConsW * GP * D * 4 <= Geo::NS * Geo::kSlot, "the warps' O must fit in the ring");
+  const size_t smem = (size_t)Geo::NS * Geo::kSlot + sizeof(DecBar) + Geo::kConsW * 32 * sizeof(float) +
+                      Geo::kConsW * GP * 2 * sizeof(float);
   auto kern = decode_split_kernel<D, GP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(p.n_split, p.B * p.H_kv), kDecThreads, smem, stream>>>(p);
+  kern<<<dim3(p.n_split, p.B * p.H_kv), Geo::kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
