@@ -51,6 +51,8 @@ struct FwdParams {
   int split;                        // 0: a CTA takes two query tiles that share each key tile;
                                     // 1: a CTA takes one query tile, its key tiles dealt
                                     //    alternately to two sub-tile pipelines
+                                    //    (head dim 256: one query tile per CTA, one pipeline)
+  int out_f32;                      // head dim 256 kernel: O in fp32 (else bf16)
 };
 
 struct PlanDumpParams {
@@ -152,6 +154,12 @@ struct DecodeParams {
 constexpr int kDecodeMaxSplits = 1024;
 
 cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream);
+
+// Head dim 256 (attention_d256.cu): one query tile per work item, inputs in
+// raster order; tq is a [B*H][N][256] view with 64 x 128 boxes, tk and tv
+// [B*H_kv][N][256] views with 64 x 64 boxes (128-byte swizzle).
+cudaError_t launch_attention_d256(const FwdParams& p, cudaStream_t stream);
+size_t attention_d256_smem_bytes();
 
 // Launchers (attention_fwd.cu).
 cudaError_t launch_attention(const FwdParams& p, int d, bool out_f32, cudaStream_t stream);

@@ -89,8 +89,8 @@ int normalize(const mattn_mask_desc* desc, int B, int H, int N, int d, int dtype
   if (N > (1 << 30)) return fail(MATTN_ERR_UNSUPPORTED, "N = %d exceeds 2^30", N);
   if ((int64_t)B * H > (1 << 30)) return fail(MATTN_ERR_UNSUPPORTED, "B*H too large");
   if (need_data) {
-    if (d != 32 && d != 64 && d != 80 && d != 96 && d != 128)
-      return fail(MATTN_ERR_UNSUPPORTED, "head dim %d not supported (32, 64, 80, 96, 128)", d);
+    if (d != 32 && d != 64 && d != 80 && d != 96 && d != 128 && d != 256)
+      return fail(MATTN_ERR_UNSUPPORTED, "head dim %d not supported (32, 64, 80, 96, 128, 256)", d);
     if (dtype != MATTN_BF16 && dtype != MATTN_F32) return fail(MATTN_ERR_UNSUPPORTED, "dtype %d not supported", dtype);
   }
   if (desc->kind < MATTN_FULL || desc->kind > MATTN_BLOCK_SPARSE)
@@ -168,6 +168,17 @@ int normalize(const mattn_mask_desc* desc, int B, int H, int N, int d, int dtype
   n.split = n.kind == kBlockSparse && n.block_c == 1;
   if (desc->flags == MATTN_FLAG_SCHEDULE_PAIRED) n.split = false;
   if (desc->flags == MATTN_FLAG_SCHEDULE_SPLIT) n.split = true;
+  if (need_data && d == 256) {
+    // the head dim 256 kernel: one query tile per work item, interval masks,
+    // inputs in raster order (other orders through the reorder copy)
+    if (n.kind == kBlockSparse)
+      return fail(MATTN_ERR_UNSUPPORTED, "head dim 256 supports the interval masks (not block-sparse)");
+    for (const auto& hp : n.heads)
+      if (hp.store != kStoreIdentity) n.need_copy = true;
+    for (auto& hp : n.heads) hp.load = kLoadRaster;
+    n.any_colmajor_tma = false;
+    n.split = true;
+  }
   *out = std::move(n);
   return MATTN_OK;
 }
@@ -364,7 +375,7 @@ int encode(CUtensorMap* tm, const void* base, int rank, const cuuint64_t* dims, 
 // map [0] covers 64-column chunks (128-byte swizzle), map [1] the 16- or
 // 32-column rest.
 int make_maps(const Normalized& n, const void* base, CUtensorMap raster[2], CUtensorMap colmaj[2], int rows, int cols,
-              int64_t heads) {
+              int64_t heads, int box_rows = kTile) {
   const int d = n.d;
   const int chunks = d / 64, rem = d % 64;
   const cuuint64_t bh = (cuuint64_t)heads;
@@ -376,7 +387,7 @@ int make_maps(const Normalized& n, const void* base, CUtensorMap raster[2], CUte
     cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)n.N * d * 2};
     if (chunks) {
       cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n.N, bh};
-      cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1};
+      cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
       int rc = encode(&raster[0], base, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
       if (rc) return rc;
     }
@@ -489,9 +500,17 @@ int fwd_locked(const void* q, const void* k, const void* v, void* o, float* lse,
   memset(&p, 0, sizeof(p));
   const int rows = n.any_colmajor_tma ? desc->grid_rows : 0;
   const int cols = n.any_colmajor_tma ? desc->grid_cols : 0;
-  if ((rc = make_maps(n, use[0], p.tq, p.cq, rows, cols, (int64_t)B * H))) return rc;
-  if ((rc = make_maps(n, use[1], p.tk, p.ck, rows, cols, (int64_t)B * kv_heads))) return rc;
-  if ((rc = make_v_maps(n, use[2], p.tv, p.cv, rows, cols, (int64_t)B * kv_heads))) return rc;
+  if (d == 256) {
+    // 64-column chunks with 128-byte swizzle for Q (128-row boxes) and for K
+    // and V (64-row boxes; V's MN-major atoms have the same layout)
+    if ((rc = make_maps(n, use[0], p.tq, p.cq, 0, 0, (int64_t)B * H, kTile))) return rc;
+    if ((rc = make_maps(n, use[1], p.tk, p.ck, 0, 0, (int64_t)B * kv_heads, 64))) return rc;
+    if ((rc = make_maps(n, use[2], p.tv, p.cv, 0, 0, (int64_t)B * kv_heads, 64))) return rc;
+  } else {
+    if ((rc = make_maps(n, use[0], p.tq, p.cq, rows, cols, (int64_t)B * H))) return rc;
+    if ((rc = make_maps(n, use[1], p.tk, p.ck, rows, cols, (int64_t)B * kv_heads))) return rc;
+    if ((rc = make_v_maps(n, use[2], p.tv, p.cv, rows, cols, (int64_t)B * kv_heads))) return rc;
+  }
   p.H_kv = kv_heads;
   p.kv_group = H / kv_heads;
   p.o = o;
@@ -516,7 +535,11 @@ int fwd_locked(const void* q, const void* k, const void* v, void* o, float* lse,
   p.scale_log2 = n.scale * 1.4426950408889634f;
   p.self_test_timeout = self_test;
   p.split = n.split ? 1 : 0;
-  MATTN_CUDA(launch_attention(p, d, dtype == MATTN_F32, stream), "attention launch");
+  p.out_f32 = dtype == MATTN_F32 ? 1 : 0;
+  if (d == 256)
+    MATTN_CUDA(launch_attention_d256(p, stream), "attention launch (head dim 256)");
+  else
+    MATTN_CUDA(launch_attention(p, d, dtype == MATTN_F32, stream), "attention launch");
   return MATTN_OK;
 }
 
@@ -538,6 +561,7 @@ int prepare_in_place_launch(const void* q, const void* k, const void* v, void* o
   if (rc) return rc;
   rc = check_device_ptrs(q, k, v, o, lse);
   if (rc) return rc;
+  if (d == 256) return fail(MATTN_ERR_UNSUPPORTED, "head dim 256 is not supported by the no-allocation entry point");
   if (n.need_copy)
     return fail(MATTN_ERR_UNSUPPORTED,
                 "inputs need the reorder / convert pre-pass (fp32 inputs, explicit orders, or a column-major grid "
@@ -786,6 +810,7 @@ int mattn_received(const void* q, const void* k, const float* lse, float* r, int
   int rc = normalize(desc, B, H, N, d, dtype, true, &n);
   if (rc) return rc;
   if (n.sink_tokens > 0) return fail(MATTN_ERR_UNSUPPORTED, "received attention does not take sink tokens");
+  if (d == 256) return fail(MATTN_ERR_UNSUPPORTED, "received attention supports head dims up to 128");
   if (!q || !k || !lse || !r) return fail(MATTN_ERR_INVALID_ARG, "q, k, lse and r must be non-NULL");
   if (!aligned16(q) || !aligned16(k)) return fail(MATTN_ERR_UNSUPPORTED, "q and k must be 16-byte aligned");
   if ((reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(r) & 3u))

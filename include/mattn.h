@@ -27,7 +27,9 @@
  * Memory layout: q, k, v and o are dense row-major [B][H][N][d] tensors of
  * one element type (bf16, or fp32 for q/k/v/o with MATTN_F32), base address
  * 16-byte aligned; lse is fp32 [B][H][N].  Supported head dims: 32, 64, 80,
- * 96, 128.  fp32 inputs are rounded to bf16 on the device before the
+ * 96, 128, and 256 for every kind but MATTN_BLOCK_SPARSE (the head dim of
+ * the Bifocal page's speed-test layout; other token orders go through the
+ * reorder copy at d = 256).  fp32 inputs are rounded to bf16 on the device before the
  * tensor-core products (accumulation is fp32 throughout); O is written in
  * the input element type.
  *

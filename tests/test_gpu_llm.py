@@ -167,3 +167,66 @@ def test_gqa32k_full_size_sampled(mask):
     rows = sorted({0, 1, 3, 4, 5, 127, 128, 571, 572, 575, 576, 577, 4095, 4096, wl.N - 129, wl.N - 128,
                    wl.N - 1} | set(int(x) for x in rng.integers(0, wl.N, 40)))
     check_gqa(q, k, v, spec, rows=rows, groups=[0, wl.kv_heads - 1], tag=f"gqa32k {mask}")
+
+
+# ---------------------------------------------------------------- head dim 256
+
+@pytest.mark.parametrize("H,Hkv,n", [(4, 1, 1000), (16, 4, 700), (2, 2, 300)])
+def test_d256_kinds(H, Hkv, n):
+    """Head dim 256 (the speed-test layout) on every interval mask, with a
+    sink logit and sink tokens, several tiles and a ragged last tile."""
+    q, k, v = make_qkv(1, H, n, 256, "bf16", 1.0, seed=7 * n + H, device="cuda", kv_heads=Hkv)
+    sink = np.linspace(-1.0, 1.0, H)
+    specs = [
+        MaskSpec("full", [0] * H),
+        MaskSpec("causal_window", [n] * H),
+        MaskSpec("chunk", [256] * H),
+        MaskSpec("sliding", [100] * H, sink=sink),
+        MaskSpec("causal_window", [300] * H, sink=sink),
+        MaskSpec("causal_window", [200] * H, sink_tokens=4),
+        MaskSpec("causal_window", [64] * H, sink_tokens=130),
+    ]
+    for spec in specs:
+        check_gqa(q, k, v, spec, tag=f"d256 {spec.kind} {spec.head_param[0]} H{H}/{Hkv} n{n} st{spec.sink_tokens}")
+
+
+def test_d256_fp32_and_orders():
+    """fp32 inputs and column-major / explicit orders go through the reorder
+    copy; outputs come back in caller order."""
+    n, H = 512, 2
+    q, k, v = make_qkv(1, H, n, 256, "f32", 1.0, seed=9, device="cuda")
+    check_gqa(q, k, v, MaskSpec("causal_window", [200, 333], sink=np.array([0.3, -0.3])), tag="d256 fp32")
+    from workloads import column_major_order, random_order
+
+    qb, kb, vb = make_qkv(1, H, n, 256, "bf16", 0.5, seed=10, device="cuda")
+    spec = MaskSpec("sliding", [40, 40], perm=[column_major_order(128, 4), random_order(n, 3)],
+                    perm_grid=[(128, 4), None])
+    mask = mattn.prepare(spec, H, n)
+    o, lse = mattn.attention(qb, kb, vb, mask)
+    torch.cuda.synchronize()
+    ref_o, ref_lse = dense.attention(_host(qb), _host(kb), _host(vb), spec)
+    got = np.stack([_host(o[0, h]) for h in range(H)]).astype(np.float64)
+    assert np.abs(got - ref_o).max() <= MAX_ABS
+    assert np.linalg.norm(got - ref_o) / np.linalg.norm(ref_o) <= REL_L2
+    assert np.abs(np.stack([_host(lse[0, h]) for h in range(H)]) - ref_lse).max() <= LSE_ABS
+
+
+def test_d256_rejects_block_sparse():
+    n = 256
+    q, k, v = make_qkv(1, 1, n, 256, "bf16", 1.0, seed=1, device="cuda")
+    spec = MaskSpec("block", [128], block=bernoulli_causal_blocks(1, 2, 1))
+    with pytest.raises(mattn.MattnError):
+        mattn.attention(q, k, v, mattn.prepare(spec, 1, n))
+
+
+@pytest.mark.parametrize("mask", ["causal", "swa576_sink"])
+def test_prefill_d256_full_size_sampled(mask):
+    """The 16K-token d256 prefill the bench times (16 query heads, 4 K/V
+    heads), sampled rows of the first and last groups."""
+    wl = WORKLOADS["prefill_d256"]
+    q, k, v = make_workload_inputs(wl, seed=0, device="cuda")
+    spec = make_mask(wl, mask)
+    rng = np.random.default_rng(5)
+    rows = sorted({0, 1, 63, 64, 127, 128, 575, 576, 577, wl.N - 65, wl.N - 64, wl.N - 1}
+                  | set(int(x) for x in rng.integers(0, wl.N, 24)))
+    check_gqa(q, k, v, spec, rows=rows, groups=[0, wl.kv_heads - 1], tag=f"prefill_d256 {mask}")

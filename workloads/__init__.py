@@ -135,6 +135,12 @@ WORKLOADS = {
         "sharing 8 K/V heads, d128), B1 N32768 bf16 N(0,1); causal window 572 plus "
         "the first 4 tokens (StreamingLLM sink tokens), or window 576 with a "
         "learned sink logit ~ N(0,1) per head", kv_heads=8),
+    "prefill_d256": Workload(
+        "prefill_d256", 1, 16, 16384, 256, "bf16", 1.0, None,
+        ("causal", "swa576_sink"),
+        "LM prefill of a 16K-token prompt in the speed-test layout (16 query heads "
+        "sharing 4 K/V heads of dimension 256), B1 bf16 N(0,1); causal, or causal "
+        "window 576 with a learned sink logit ~ N(0,1) per head", kv_heads=4),
     "decode128k": Workload(
         "decode128k", 1, 16, 131072, 256, "bf16", 1.0, None,
         ("full", "swa576_sink", "swa572_sinktok4"),
@@ -178,6 +184,8 @@ def make_mask(wl: Workload, mask: str, seed: int = 0, n: Optional[int] = None,
         windows = rng.permutation(sizes)
         sink = rng.standard_normal(nh)
         return MaskSpec("causal_window", [int(x) for x in windows], sink=sink, name=mask)
+    if mask == "causal":
+        return MaskSpec("causal_window", [n] * nh, name=mask)
     if mask.startswith("swa") and "_sinktok" in mask:
         w, s = mask[3:].split("_sinktok")
         return MaskSpec("causal_window", [int(w)] * nh, sink_tokens=int(s), name=mask)
