@@ -43,9 +43,10 @@ ORDER_RASTER = -1
 ORDER_COLUMN_MAJOR = -2
 TILE = 128
 TILE_FULL, TILE_PARTIAL = 1, 2
-FLAG_SCHEDULE_PAIRED, FLAG_SCHEDULE_SPLIT = 1, 2
+FLAG_SCHEDULE_PAIRED, FLAG_SCHEDULE_SPLIT, FLAG_SCHEDULE_SINGLE = 1, 2, 4
 RR_SINK_RECENT = 1
-SCHEDULE = {None: 0, "auto": 0, "paired": FLAG_SCHEDULE_PAIRED, "split": FLAG_SCHEDULE_SPLIT}
+SCHEDULE = {None: 0, "auto": 0, "paired": FLAG_SCHEDULE_PAIRED, "split": FLAG_SCHEDULE_SPLIT,
+            "single": FLAG_SCHEDULE_SINGLE}
 
 
 class MattnError(RuntimeError):

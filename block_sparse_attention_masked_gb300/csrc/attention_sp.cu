@@ -1,22 +1,23 @@
-// Masked attention forward for head dim 256 on sm_103a (the speed-test
-// layout of the Bifocal page, "Details": query and key/value heads of
-// dimension 256).
-//
-// At d = 256 an O accumulator takes 256 of the 512 tensor-memory columns,
-// so a CTA holds one 128-row query tile (the d <= 128 kernel holds two):
-//   S_j  = Q K_j^T        M128 N64 K256   (16 MMAs of K16, smem x smem -> TMEM)
+// Single-pipeline masked attention forward for sm_103a: one 128-row query
+// tile per CTA, S double-buffered in tensor memory.  It serves head dim 256
+// (the speed-test layout of the Bifocal page, "Details": query and
+// key/value heads of dimension 256), where an O accumulator takes 256 of the
+// 512 tensor-memory columns so that the two-sub-tile kernel does not fit,
+// and, on request, head dim 128.  With KT keys per key tile:
+//   S_j  = Q K_j^T        M128 N=KT K=D   (D/16 MMAs of K16, smem x smem -> TMEM)
 //   P_j  = exp2(S_j * scale*log2e - m)    (softmax warps, one row per thread)
-//   O   += P_j V_j        M128 N256 K64   (4 MMAs of K16, P from TMEM)
-// over 64-key tiles j.  S is double-buffered, so the product of tile j + 1
-// runs while the softmax works on tile j:
+//   O   += P_j V_j        M128 N=D  K=KT  (KT/16 MMAs of K16, P from TMEM)
+// (D, KT) = (256, 64) or (128, 128).  S is double-buffered, so the product
+// of tile j + 1 runs while the softmax works on tile j:
 //   issue order  S_0, S_1, [P_0] PV_0, S_2, [P_1] PV_1, S_3, ...
-// Tensor memory: S_0 [0, 64), S_1 [64, 128) (P as bf16 pairs in the first 32
-// columns of its S), O [256, 512).  Shared memory: Q 64 KB, K and V rings of
-// two 32 KB tiles each.
+// Tensor memory: S_0 [0, KT), S_1 [KT, 2 KT) (P as bf16 pairs in the first
+// KT/2 columns of its S), O [256, 256 + D).  Shared memory: Q (D/4 KB), K
+// and V rings of two KT x D tiles each, and for block-sparse masks the
+// CTA's key-tile list.
 //
-// The key tiles are the 128-key tiles of the interval rules (plan_rules.h:
-// full, chunk, sliding, causal window with sink tokens), each taken as two
-// 64-key halves; the mask is applied on the halves of PARTIAL tiles.
+// The key tiles are the 128-key tiles of the plan (plan_rules.h: interval
+// masks incl. sink tokens, or the block-selection matrix), each taken as
+// 128 / KT pieces; the mask is applied on the pieces of PARTIAL tiles.
 // Inputs are read in raster order (the host reorders other orders into a
 // position-order copy first).
 //
@@ -36,14 +37,21 @@
 namespace mattn {
 namespace {
 
-constexpr int kD = 256;
-constexpr int kKT = 64;                           // keys per key tile
 constexpr int kThreadsD256 = 256;
 constexpr int kStagesD256 = 2;
-constexpr int kQBytes = kTile * kD * 2;           // 64 KB: 4 chunks of 128 rows x 64 columns
-constexpr int kQChunk = kTile * 64 * 2;           // 16 KB
-constexpr int kKVBytes = kKT * kD * 2;            // 32 KB: 4 chunks of 64 rows x 64 columns
-constexpr int kKVChunk = kKT * 64 * 2;            // 8 KB
+
+// Shared-memory geometry: Q and K / V tiles as 64-column chunks of 128-byte
+// rows (128-byte swizzle), as TMA writes them.
+template <int D, int KT>
+struct SpGeo {
+  static_assert(D % 64 == 0 && D <= 256 && (KT == 64 || KT == 128), "single-pipeline geometry");
+  static constexpr int kQChunk = kTile * 64 * 2;  // 16 KB
+  static constexpr int kQBytes = (D / 64) * kQChunk;
+  static constexpr int kKVChunk = KT * 64 * 2;
+  static constexpr int kKVBytes = (D / 64) * kKVChunk;
+  static constexpr int kSub = kTile / KT;         // key tiles per 128-key plan tile
+};
+
 constexpr float kLog2eX = 1.4426950408889634f;
 constexpr float kLn2X = 0.6931471805599453f;
 constexpr float kMaxTileSumX = 1099511627776.0f;  // 2^40, as in the d <= 128 kernel
@@ -59,32 +67,89 @@ struct BarD256 {
   uint64_t never;    // self-test: nothing ever arrives here
   uint32_t tmem_base;
   int abort_flag;
+  int list_n;        // block kind: entries of the CTA's key-tile list
 };
 
 __device__ __forceinline__ uint64_t dsc(uint32_t lo, uint32_t hi) { return ((uint64_t)hi << 32) | lo; }
 
-// The CTA's 128-key tiles: the sink tiles below the window, then the window.
+// The CTA's 128-key tiles: interval masks, the sink tiles below the window
+// then the window; block masks, a list in shared memory.
 struct ListD256 {
   int n, na, lo;
   KRange r;
   int param;
+  const uint32_t* e;  // block kind: the entries
 };
 
-__device__ __forceinline__ int list_kt_d256(const ListD256& L, int j) { return j < L.na ? j : L.lo + (j - L.na); }
+__device__ __forceinline__ int list_kt_d256(const ListD256& L, int j) {
+  return L.e ? (int)L.e[j] : (j < L.na ? j : L.lo + (j - L.na));
+}
+
+// Block kind: one warp writes the key tiles of query tile qt (ascending; kept
+// blocks at or below the diagonal, tiles up to qt) to `list`, their number
+// to *count.  Lanes take 64-bit words of the bitmap row; a warp prefix sum
+// of their tile counts gives each lane its first output slot.
+__device__ __forceinline__ void build_list_sp(const FwdParams& p, int h, int qt, uint32_t* list, int* count,
+                                              int lane) {
+  const int c = p.block_c;
+  const int hb = (p.block_heads == 1) ? 0 : h;
+  const uint64_t* row = p.block_bits + ((int64_t)hb * p.block_nb + qt / c) * p.block_wpr;
+  const int nbl = qt / c;  // last admissible block
+  const int nwords = nbl / 64 + 1;
+  int base = 0;
+  for (int w0 = 0; w0 < nwords; w0 += 32) {
+    const int w = w0 + lane;
+    uint64_t u = 0;
+    if (w < nwords) {
+      const int top = nbl - w * 64;
+      u = row[w] & (top >= 63 ? ~0ull : ((2ull << top) - 1ull));
+    }
+    int cnt = __popcll(u) * c;
+    if (w == nbl / 64 && ((u >> (nbl % 64)) & 1ull)) cnt -= c - (qt - nbl * c + 1);
+    int incl = cnt;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    int pos = base + incl - cnt;
+    uint64_t bits = u;
+    while (bits) {
+      const int bpos = __ffsll((long long)bits) - 1;
+      bits &= bits - 1ull;
+      const int n = w * 64 + bpos;
+      for (int i = 0; i < c; ++i) {
+        const int kt = n * c + i;
+        if (kt > qt) break;
+        list[pos++] = (uint32_t)kt;
+      }
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) *count = base;
+}
 
 __device__ __forceinline__ void fail_d256(const FwdParams& p, BarD256* bar, uint32_t bit) {
   *reinterpret_cast<volatile int*>(&bar->abort_flag) = 1;
   atomicOr(p.err, bit);
 }
 
-__global__ void __launch_bounds__(kThreadsD256, 1) attention_d256_kernel(const __grid_constant__ FwdParams p) {
+template <int D, int KT>
+__global__ void __launch_bounds__(kThreadsD256, 1) attention_sp_kernel(const __grid_constant__ FwdParams p) {
+  using SG = SpGeo<D, KT>;
+  constexpr int kD = D, kKT = KT;
+  constexpr int kQBytes = SG::kQBytes, kQChunk = SG::kQChunk;
+  constexpr int kKVBytes = SG::kKVBytes, kKVChunk = SG::kKVChunk;
+  constexpr int kSub = SG::kSub;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sq = base;
   uint8_t* sk = sq + kQBytes;
   uint8_t* sv = sk + kStagesD256 * kKVBytes;
   BarD256* bar = reinterpret_cast<BarD256*>(sv + kStagesD256 * kKVBytes);
+  uint32_t* list_e = reinterpret_cast<uint32_t*>(bar + 1);  // block kind: [kBlockListMax] key tiles
   volatile int* abort_flag = &bar->abort_flag;
+  const bool block = p.kind == kBlockSparse;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int2 item = p.items[blockIdx.x];  // (b * H + h, query tile)
@@ -92,14 +157,17 @@ __global__ void __launch_bounds__(kThreadsD256, 1) attention_d256_kernel(const _
   const int h = bh % p.H, b = bh / p.H;
   const int bh_kv = b * p.H_kv + h / p.kv_group;
   const int param = p.head_info[h * 4 + kHeadParam];
+  if (block && warp == 2) build_list_sp(p, h, qt, list_e, &bar->list_n, lane);
   // key-tile list (128-key tiles) of this query tile
   ListD256 L;
   L.param = param;
-  L.r = interval_krange(p.kind, param, p.N, qt);
+  L.e = nullptr;
+  L.r.lo = 1; L.r.hi = 0; L.r.flo = 0; L.r.fhi = -1;
+  if (!block) L.r = interval_krange(p.kind, param, p.N, qt);
   L.lo = L.r.lo;
   L.n = L.r.hi >= L.r.lo ? L.r.hi - L.r.lo + 1 : 0;
   L.na = 0;
-  const int ns = sink_tiles(p.sink_tokens, p.N, qt);
+  const int ns = block ? 0 : sink_tiles(p.sink_tokens, p.N, qt);
   if (ns > 0 && L.n > 0) {
     if (ns >= L.lo) {
       const int hi = L.r.hi > ns - 1 ? L.r.hi : ns - 1;
@@ -109,14 +177,6 @@ __global__ void __launch_bounds__(kThreadsD256, 1) attention_d256_kernel(const _
       L.na = ns;
       L.n += ns;
     }
-  }
-  // 64-key halves: tile j of the list gives halves 2j, 2j + 1 (the second
-  // only when it holds keys < N)
-  auto half_key0 = [&](int t) { return list_kt_d256(L, t >> 1) * kTile + (t & 1) * kKT; };
-  int n_half = 0;
-  if (L.n > 0) {
-    const int last_kt = list_kt_d256(L, L.n - 1);
-    n_half = 2 * L.n - ((last_kt * kTile + kKT >= p.N) ? 1 : 0);
   }
 
   if (threadIdx.x == 0) {
@@ -146,6 +206,18 @@ __global__ void __launch_bounds__(kThreadsD256, 1) attention_d256_kernel(const _
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = bar->tmem_base;
+  if (block) {
+    L.e = list_e;
+    L.n = bar->list_n;
+  }
+  // key tiles of KT keys: plan tile j gives pieces kSub j .. kSub j + kSub - 1
+  // (the last ones only when they hold keys < N)
+  auto half_key0 = [&](int t) { return list_kt_d256(L, t / kSub) * kTile + (t % kSub) * kKT; };
+  int n_half = 0;
+  if (L.n > 0) {
+    const int last_kt = list_kt_d256(L, L.n - 1);
+    n_half = kSub * L.n - ((kSub == 2 && last_kt * kTile + kKT >= p.N) ? 1 : 0);
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -154,7 +226,7 @@ __global__ void __launch_bounds__(kThreadsD256, 1) attention_d256_kernel(const _
       const uint64_t once = ptx::l2_policy_evict_first();
       ptx::mbar_arrive_expect_tx(&bar->q_full, kQBytes);
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < kD / 64; ++c)
         ptx::tma_load_3d_hint(sq + c * kQChunk, &p.tq[0], &bar->q_full, c * 64, qt * kTile, bh, once);
       // K and V halves in list order, interleaved so that neither ring
       // waits behind the other
@@ -168,7 +240,7 @@ __global__ void __launch_bounds__(kThreadsD256, 1) attention_d256_kernel(const _
         }
         ptx::mbar_arrive_expect_tx(&bar->k_full[slot], kKVBytes);
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < kD / 64; ++c)
           ptx::tma_load_3d_hint(sk + slot * kKVBytes + c * kKVChunk, &p.tk[0], &bar->k_full[slot], c * 64, k0,
                                 bh_kv, keep);
         if (!ptx::mbar_wait(&bar->v_empty[slot], par, p.timeout_ns, abort_flag)) {
@@ -177,7 +249,7 @@ __global__ void __launch_bounds__(kThreadsD256, 1) attention_d256_kernel(const _
         }
         ptx::mbar_arrive_expect_tx(&bar->v_full[slot], kKVBytes);
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < kD / 64; ++c)
           ptx::tma_load_3d_hint(sv + slot * kKVBytes + c * kKVChunk, &p.tv[0], &bar->v_full[slot], c * 64, k0,
                                 bh_kv, keep);
       }
@@ -216,7 +288,7 @@ __global__ void __launch_bounds__(kThreadsD256, 1) attention_d256_kernel(const _
       if (ptx::elect_one()) {
         uint32_t acc = 0;
 #pragma unroll 1
-        for (int step = 0; step < 16; ++step) {
+        for (int step = 0; step < kD / 16; ++step) {
           const uint32_t qo = (uint32_t)(((step >> 2) * kQChunk + (step & 3) * 32) >> 4) + lbo_k;
           const uint32_t ko = (uint32_t)((slot * kKVBytes + (step >> 2) * kKVChunk + (step & 3) * 32) >> 4) + lbo_k;
           ptx::mma_ss(s_tm, dsc(q4 + qo, hi128), dsc(k4 + ko, hi128), idesc_qk, acc);
@@ -295,21 +367,28 @@ __global__ void __launch_bounds__(kThreadsD256, 1) attention_d256_kernel(const _
         break;
       }
       ptx::tc_fence_after();
-      float x[64];
-      ptx::tmem_ld32(s_tmem + 0, *reinterpret_cast<float(*)[32]>(&x[0]));
-      ptx::tmem_ld32(s_tmem + 32, *reinterpret_cast<float(*)[32]>(&x[32]));
-      ptx::tmem_wait_ld();
-      const int kt = list_kt_d256(L, t >> 1);
-      const int64_t k0 = (int64_t)half_key0(t);
-      const bool partial = p.sink_tokens > 0 ? sink_window_tile_class(param, p.sink_tokens, p.N, qt, kt) == kTilePartial
-                                             : interval_tile_class(L.r, kt) == kTilePartial;
-      if (partial || k0 + kKT > p.N) {
-        const int c_lo = (int)(lo - k0 < -1 ? -1 : (lo - k0 > 64 ? 64 : lo - k0));
-        const int c_hi = (int)(hi - k0 < -1 ? -1 : (hi - k0 > 64 ? 64 : hi - k0));
-        const int c_s = (int)(sink_hi - k0 < -1 ? -1 : (sink_hi - k0 > 64 ? 64 : sink_hi - k0));
+      float x[kKT];
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if ((c < c_lo || c > c_hi) && c > c_s) x[c] = -INFINITY;
+      for (int c0 = 0; c0 < kKT; c0 += 32) ptx::tmem_ld32(s_tmem + c0, *reinterpret_cast<float(*)[32]>(&x[c0]));
+      ptx::tmem_wait_ld();
+      const int kt = list_kt_d256(L, t / kSub);
+      const int64_t k0 = (int64_t)half_key0(t);
+      const bool partial = block ? block_tile_class(qt, kt, p.N) == kTilePartial
+                           : p.sink_tokens > 0 ? sink_window_tile_class(param, p.sink_tokens, p.N, qt, kt) == kTilePartial
+                                               : interval_tile_class(L.r, kt) == kTilePartial;
+      if (partial || k0 + kKT > p.N) {
+        const int c_lo = (int)(lo - k0 < -1 ? -1 : (lo - k0 > kKT ? kKT : lo - k0));
+        const int c_hi = (int)(hi - k0 < -1 ? -1 : (hi - k0 > kKT ? kKT : hi - k0));
+        const int c_s = (int)(sink_hi - k0 < -1 ? -1 : (sink_hi - k0 > kKT ? kKT : sink_hi - k0));
+        if (c_s < 0) {
+#pragma unroll
+          for (int c = 0; c < kKT; ++c)
+            if (c < c_lo || c > c_hi) x[c] = -INFINITY;
+        } else {
+#pragma unroll
+          for (int c = 0; c < kKT; ++c)
+            if ((c < c_lo || c > c_hi) && c > c_s) x[c] = -INFINITY;
+        }
       }
       // exponentiate against the running (stale) maximum; a tile whose row
       // sum would pass 2^40 is redone against its own maximum, rescaling O
@@ -317,17 +396,21 @@ __global__ void __launch_bounds__(kThreadsD256, 1) attention_d256_kernel(const _
       auto exp_pass = [&](float mref, float& sum) {
         const float2 sl2v = make_float2(sl2, sl2);
         const float2 negm = make_float2(-mref, -mref);
-        float2 acc = make_float2(0.f, 0.f);
-        uint32_t pk[32];
+        float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float2 tt = ptx::ffma2(make_float2(x[2 * i], x[2 * i + 1]), sl2v, negm);
-          const float2 pp = make_float2(ptx::ex2(tt.x), ptx::ex2(tt.y));
-          pk[i] = ptx::pack_bf16x2(pp.x, pp.y);
-          acc = ptx::fadd2(acc, pp);
+        for (int c0 = 0; c0 < kKT; c0 += 64) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float2 tt = ptx::ffma2(make_float2(x[c0 + 2 * i], x[c0 + 2 * i + 1]), sl2v, negm);
+            const float2 pp = make_float2(ptx::ex2(tt.x), ptx::ex2(tt.y));
+            pk[i] = ptx::pack_bf16x2(pp.x, pp.y);
+            acc[i & 1] = ptx::fadd2(acc[i & 1], pp);
+          }
+          ptx::tmem_st32(s_tmem + c0 / 2, pk);
         }
-        ptx::tmem_st32(s_tmem, pk);
-        sum = acc.x + acc.y;
+        const float2 a = ptx::fadd2(acc[0], acc[1]);
+        sum = a.x + a.y;
       };
       float ts = 0.f;
       bool slow = __any_sync(0xffffffffu, m == -INFINITY);
@@ -339,7 +422,7 @@ __global__ void __launch_bounds__(kThreadsD256, 1) attention_d256_kernel(const _
       if (slow) {
         float mx = x[0];
 #pragma unroll
-        for (int c = 1; c < 64; ++c) mx = fmaxf(mx, x[c]);
+        for (int c = 1; c < kKT; ++c) mx = fmaxf(mx, x[c]);
         const float m_new = fmaxf(m, mx * sl2);
         const bool need_rescale = (m != -INFINITY) && (m_new > m);
         if (m == -INFINITY) m = m_new;
@@ -448,19 +531,33 @@ __global__ void __launch_bounds__(kThreadsD256, 1) attention_d256_kernel(const _
   }
 }
 
-}  // namespace
-
-size_t attention_d256_smem_bytes() {
-  return 1024 + (size_t)kQBytes + 2 * kStagesD256 * (size_t)kKVBytes + sizeof(BarD256);
+template <int D, int KT>
+size_t sp_smem_bytes() {
+  return 1024 + (size_t)SpGeo<D, KT>::kQBytes + 2 * kStagesD256 * (size_t)SpGeo<D, KT>::kKVBytes + sizeof(BarD256) +
+         kBlockListMax * sizeof(uint32_t);
 }
 
-cudaError_t launch_attention_d256(const FwdParams& p, cudaStream_t stream) {
-  if (p.n_items <= 0) return cudaSuccess;
-  const size_t smem = attention_d256_smem_bytes();
-  cudaError_t e = cudaFuncSetAttribute(attention_d256_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+template <int D, int KT>
+cudaError_t launch_sp(const FwdParams& p, cudaStream_t stream) {
+  const size_t smem = sp_smem_bytes<D, KT>();
+  auto kern = attention_sp_kernel<D, KT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  attention_d256_kernel<<<p.n_items, kThreadsD256, smem, stream>>>(p);
+  kern<<<p.n_items, kThreadsD256, smem, stream>>>(p);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+int attention_sp_key_tile(int d) { return d == 256 ? 64 : 128; }
+
+cudaError_t launch_attention_sp(const FwdParams& p, int d, cudaStream_t stream) {
+  if (p.n_items <= 0) return cudaSuccess;
+  switch (d) {
+    case 128: return launch_sp<128, 128>(p, stream);
+    case 256: return launch_sp<256, 64>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace mattn

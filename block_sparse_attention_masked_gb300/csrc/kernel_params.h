@@ -155,11 +155,12 @@ constexpr int kDecodeMaxSplits = 1024;
 
 cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream);
 
-// Head dim 256 (attention_d256.cu): one query tile per work item, inputs in
-// raster order; tq is a [B*H][N][256] view with 64 x 128 boxes, tk and tv
-// [B*H_kv][N][256] views with 64 x 64 boxes (128-byte swizzle).
-cudaError_t launch_attention_d256(const FwdParams& p, cudaStream_t stream);
-size_t attention_d256_smem_bytes();
+// Single-pipeline kernel (attention_sp.cu), head dim 256, or 128 on request:
+// one query tile per work item, inputs in raster order; tq is a
+// [B*H][N][d] view with 64 x 128 boxes, tk and tv [B*H_kv][N][d] views with
+// 64 x attention_sp_key_tile(d) boxes (128-byte swizzle).
+cudaError_t launch_attention_sp(const FwdParams& p, int d, cudaStream_t stream);
+int attention_sp_key_tile(int d);
 
 // Launchers (attention_fwd.cu).
 cudaError_t launch_attention(const FwdParams& p, int d, bool out_f32, cudaStream_t stream);

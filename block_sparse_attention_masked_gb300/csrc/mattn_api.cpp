@@ -76,14 +76,16 @@ struct Normalized {
   int sink_tokens;    // causal window: leading positions every later query sees
   float scale;
   bool split;         // schedule: one query tile per CTA, key tiles dealt to two pipelines
+  bool single;        // the single-pipeline kernel (head dim 256, or 128 on request)
 };
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int normalize(const mattn_mask_desc* desc, int B, int H, int N, int d, int dtype, bool need_data, Normalized* out) {
   if (!desc) return fail(MATTN_ERR_INVALID_ARG, "mask descriptor is NULL");
-  if (desc->flags != 0 && desc->flags != MATTN_FLAG_SCHEDULE_PAIRED && desc->flags != MATTN_FLAG_SCHEDULE_SPLIT)
-    return fail(MATTN_ERR_INVALID_ARG, "flags must be 0, MATTN_FLAG_SCHEDULE_PAIRED or MATTN_FLAG_SCHEDULE_SPLIT (got %u)",
+  if (desc->flags != 0 && desc->flags != MATTN_FLAG_SCHEDULE_PAIRED && desc->flags != MATTN_FLAG_SCHEDULE_SPLIT &&
+      desc->flags != MATTN_FLAG_SCHEDULE_SINGLE)
+    return fail(MATTN_ERR_INVALID_ARG, "flags must be 0 or one MATTN_FLAG_SCHEDULE_* flag (got %u)",
                 desc->flags);
   if (B < 1 || H < 1 || N < 1) return fail(MATTN_ERR_INVALID_ARG, "B, H, N must be >= 1 (got %d, %d, %d)", B, H, N);
   if (N > (1 << 30)) return fail(MATTN_ERR_UNSUPPORTED, "N = %d exceeds 2^30", N);
@@ -168,11 +170,13 @@ int normalize(const mattn_mask_desc* desc, int B, int H, int N, int d, int dtype
   n.split = n.kind == kBlockSparse && n.block_c == 1;
   if (desc->flags == MATTN_FLAG_SCHEDULE_PAIRED) n.split = false;
   if (desc->flags == MATTN_FLAG_SCHEDULE_SPLIT) n.split = true;
-  if (need_data && d == 256) {
-    // the head dim 256 kernel: one query tile per work item, interval masks,
-    // inputs in raster order (other orders through the reorder copy)
-    if (n.kind == kBlockSparse)
-      return fail(MATTN_ERR_UNSUPPORTED, "head dim 256 supports the interval masks (not block-sparse)");
+  n.single = false;
+  if (need_data && desc->flags == MATTN_FLAG_SCHEDULE_SINGLE && d != 128 && d != 256)
+    return fail(MATTN_ERR_UNSUPPORTED, "the single-pipeline schedule takes head dim 128 or 256 (got %d)", d);
+  if (need_data && (d == 256 || desc->flags == MATTN_FLAG_SCHEDULE_SINGLE)) {
+    // the single-pipeline kernel: one query tile per work item, inputs in
+    // raster order (other orders through the reorder copy)
+    n.single = true;
     for (const auto& hp : n.heads)
       if (hp.store != kStoreIdentity) n.need_copy = true;
     for (auto& hp : n.heads) hp.load = kLoadRaster;
@@ -306,8 +310,8 @@ int device_state(DeviceState** out) {
 std::string plan_key(const Normalized& n) {
   std::string k;
   char buf[96];
-  snprintf(buf, sizeof(buf), "%d|%d|%d|%d|%d|%d|%d|", n.kind, n.B, n.H, n.N, n.need_copy ? 1 : 0, n.split ? 1 : 0,
-           n.sink_tokens);
+  snprintf(buf, sizeof(buf), "%d|%d|%d|%d|%d|%d|%d|%d|", n.kind, n.B, n.H, n.N, n.need_copy ? 1 : 0, n.split ? 1 : 0,
+           n.sink_tokens, n.single ? 1 : 0);
   k += buf;
   for (const auto& hp : n.heads) {
     snprintf(buf, sizeof(buf), "%d,%d,%d,%d;", hp.param, hp.load, hp.store, hp.perm_row);
@@ -500,12 +504,13 @@ int fwd_locked(const void* q, const void* k, const void* v, void* o, float* lse,
   memset(&p, 0, sizeof(p));
   const int rows = n.any_colmajor_tma ? desc->grid_rows : 0;
   const int cols = n.any_colmajor_tma ? desc->grid_cols : 0;
-  if (d == 256) {
+  if (n.single) {
     // 64-column chunks with 128-byte swizzle for Q (128-row boxes) and for K
-    // and V (64-row boxes; V's MN-major atoms have the same layout)
+    // and V (key-tile boxes; V's MN-major atoms have the same layout)
+    const int kt = attention_sp_key_tile(d);
     if ((rc = make_maps(n, use[0], p.tq, p.cq, 0, 0, (int64_t)B * H, kTile))) return rc;
-    if ((rc = make_maps(n, use[1], p.tk, p.ck, 0, 0, (int64_t)B * kv_heads, 64))) return rc;
-    if ((rc = make_maps(n, use[2], p.tv, p.cv, 0, 0, (int64_t)B * kv_heads, 64))) return rc;
+    if ((rc = make_maps(n, use[1], p.tk, p.ck, 0, 0, (int64_t)B * kv_heads, kt))) return rc;
+    if ((rc = make_maps(n, use[2], p.tv, p.cv, 0, 0, (int64_t)B * kv_heads, kt))) return rc;
   } else {
     if ((rc = make_maps(n, use[0], p.tq, p.cq, rows, cols, (int64_t)B * H))) return rc;
     if ((rc = make_maps(n, use[1], p.tk, p.ck, rows, cols, (int64_t)B * kv_heads))) return rc;
@@ -536,8 +541,8 @@ int fwd_locked(const void* q, const void* k, const void* v, void* o, float* lse,
   p.self_test_timeout = self_test;
   p.split = n.split ? 1 : 0;
   p.out_f32 = dtype == MATTN_F32 ? 1 : 0;
-  if (d == 256)
-    MATTN_CUDA(launch_attention_d256(p, stream), "attention launch (head dim 256)");
+  if (n.single)
+    MATTN_CUDA(launch_attention_sp(p, d, stream), "attention launch (single pipeline)");
   else
     MATTN_CUDA(launch_attention(p, d, dtype == MATTN_F32, stream), "attention launch");
   return MATTN_OK;
@@ -561,7 +566,8 @@ int prepare_in_place_launch(const void* q, const void* k, const void* v, void* o
   if (rc) return rc;
   rc = check_device_ptrs(q, k, v, o, lse);
   if (rc) return rc;
-  if (d == 256) return fail(MATTN_ERR_UNSUPPORTED, "head dim 256 is not supported by the no-allocation entry point");
+  if (n.single)
+    return fail(MATTN_ERR_UNSUPPORTED, "the no-allocation entry point runs the two-sub-tile kernel (head dim <= 128)");
   if (n.need_copy)
     return fail(MATTN_ERR_UNSUPPORTED,
                 "inputs need the reorder / convert pre-pass (fp32 inputs, explicit orders, or a column-major grid "

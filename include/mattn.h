@@ -27,9 +27,8 @@
  * Memory layout: q, k, v and o are dense row-major [B][H][N][d] tensors of
  * one element type (bf16, or fp32 for q/k/v/o with MATTN_F32), base address
  * 16-byte aligned; lse is fp32 [B][H][N].  Supported head dims: 32, 64, 80,
- * 96, 128, and 256 for every kind but MATTN_BLOCK_SPARSE (the head dim of
- * the Bifocal page's speed-test layout; other token orders go through the
- * reorder copy at d = 256).  fp32 inputs are rounded to bf16 on the device before the
+ * 96, 128 and 256 (the head dim of the Bifocal page's speed-test layout;
+ * other token orders go through the reorder copy at d = 256).  fp32 inputs are rounded to bf16 on the device before the
  * tensor-core products (accumulation is fp32 throughout); O is written in
  * the input element type.
  *
@@ -96,6 +95,11 @@ typedef enum { MATTN_BF16 = 0, MATTN_F32 = 1 } mattn_dtype;
  * different block rows and share few key tiles), PAIRED otherwise. */
 #define MATTN_FLAG_SCHEDULE_PAIRED 1u
 #define MATTN_FLAG_SCHEDULE_SPLIT 2u
+/* Head dim 128 only (head dim 256 always runs this way): one 128-row query
+ * tile per CTA in a single pipeline whose S is double-buffered in tensor
+ * memory, so that the next key tile's Q K^T runs during the softmax of
+ * this one.  Other token orders go through the reorder copy. */
+#define MATTN_FLAG_SCHEDULE_SINGLE 4u
 
 typedef struct {
   int32_t kind;              /* mattn_kind                                                */
@@ -117,7 +121,7 @@ typedef struct {
   const float* sink;         /* optional DEVICE fp32 [H] sink logits (NULL = no sink);     */
                              /* HOST for mattn_fwd_host                                    */
   float softmax_scale;       /* 0 => 1/sqrt(d)                                             */
-  uint32_t flags;            /* 0, MATTN_FLAG_SCHEDULE_PAIRED or MATTN_FLAG_SCHEDULE_SPLIT   */
+  uint32_t flags;            /* 0 or one MATTN_FLAG_SCHEDULE_* flag                          */
   int32_t sink_tokens;       /* MATTN_CAUSAL_WINDOW only (else must be 0): S >= 0 sink      */
                              /* tokens, the first S positions, visible to every query at    */
                              /* or after them besides its window: query p sees             */

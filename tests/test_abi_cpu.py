@@ -72,9 +72,9 @@ def test_invalid_arguments_rejected_on_host(L):
     assert L.mattn_count_pairs(ctypes.byref(_desc(4, 128)), 1, 1, 256, ctypes.byref(out)) == mattn.ERR_INVALID_ARG
     bad_scale = _desc(0, 0, softmax_scale=-1.0)
     assert L.mattn_count_pairs(ctypes.byref(bad_scale), 1, 1, 16, ctypes.byref(out)) == mattn.ERR_INVALID_ARG
-    for ok_flags in (mattn.FLAG_SCHEDULE_PAIRED, mattn.FLAG_SCHEDULE_SPLIT):
+    for ok_flags in (mattn.FLAG_SCHEDULE_PAIRED, mattn.FLAG_SCHEDULE_SPLIT, mattn.FLAG_SCHEDULE_SINGLE):
         assert L.mattn_count_pairs(ctypes.byref(_desc(0, 0, flags=ok_flags)), 1, 1, 16, ctypes.byref(out)) == mattn.OK
-    for bad_flags in (3, 4, 0x80000000):
+    for bad_flags in (3, 5, 8, 0x80000000):
         flags = _desc(0, 0, flags=bad_flags)
         assert L.mattn_count_pairs(ctypes.byref(flags), 1, 1, 16, ctypes.byref(out)) == mattn.ERR_INVALID_ARG
     order = (ctypes.c_int32 * 1)(mattn.ORDER_COLUMN_MAJOR)
@@ -101,6 +101,9 @@ def test_invalid_arguments_rejected_on_host(L):
     assert L.mattn_fwd(ctypes.c_void_p(8), x, x, x, None, 1, 1, 16, 64, 0, ctypes.byref(d), None) == \
         mattn.ERR_UNSUPPORTED
     assert L.mattn_fwd(x, x, x, x, None, 1, 1, 16, 64, 7, ctypes.byref(d), None) == mattn.ERR_UNSUPPORTED
+    # the single-pipeline schedule takes head dim 128 or 256
+    single = _desc(2, 3, flags=mattn.FLAG_SCHEDULE_SINGLE)
+    assert L.mattn_fwd(x, x, x, x, None, 1, 1, 16, 64, 0, ctypes.byref(single), None) == mattn.ERR_UNSUPPORTED
 
 
 def test_capacity_error_reports_count(L):

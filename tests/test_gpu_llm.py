@@ -211,12 +211,51 @@ def test_d256_fp32_and_orders():
     assert np.abs(np.stack([_host(lse[0, h]) for h in range(H)]) - ref_lse).max() <= LSE_ABS
 
 
-def test_d256_rejects_block_sparse():
-    n = 256
-    q, k, v = make_qkv(1, 1, n, 256, "bf16", 1.0, seed=1, device="cuda")
-    spec = MaskSpec("block", [128], block=bernoulli_causal_blocks(1, 2, 1))
-    with pytest.raises(mattn.MattnError):
-        mattn.attention(q, k, v, mattn.prepare(spec, 1, n))
+@pytest.mark.parametrize("bs,n", [(128, 1000), (256, 1300)])
+def test_d256_block_sparse(bs, n):
+    """Block-sparse masks at head dim 256 (the CTA's key-tile list from the
+    bitmap, causal diagonal tiles masked), with GQA and a sink logit."""
+    H, Hkv = 4, 2
+    q, k, v = make_qkv(1, H, n, 256, "bf16", 1.0, seed=bs + n, device="cuda", kv_heads=Hkv)
+    spec = MaskSpec("block", [bs] * H, block=bernoulli_causal_blocks(H, -(-n // bs), n + bs),
+                    sink=np.linspace(-0.5, 0.5, H))
+    check_gqa(q, k, v, spec, tag=f"d256 block{bs} n{n}")
+
+
+@pytest.mark.parametrize("n", [1000, 4096])
+def test_single_schedule_d128(n):
+    """Head dim 128 in the single-pipeline schedule (one query tile per CTA,
+    S double-buffered): block-sparse, causal window with sink tokens, full."""
+    H, Hkv = 4, 2
+    q, k, v = make_qkv(1, H, n, 128, "bf16", 1.0, seed=n + 3, device="cuda", kv_heads=Hkv)
+    nb = -(-n // 128)
+    specs = [MaskSpec("block", [128] * H, block=bernoulli_causal_blocks(H, nb, n)),
+             MaskSpec("causal_window", [300] * H, sink_tokens=4, sink=np.linspace(-1, 1, H)),
+             MaskSpec("full", [0] * H)]
+    for spec in specs:
+        B, Hq, N, d = q.shape
+        mask = mattn.prepare(spec, Hq, N, schedule="single")
+        o, lse = mattn.attention(q, k, v, mask)
+        torch.cuda.synchronize()
+        ref = mattn.attention(q, k, v, mattn.prepare(spec, Hq, N))
+        torch.cuda.synchronize()
+        # the same result as the two-sub-tile kernel up to rounding order
+        assert (o.float() - ref[0].float()).abs().max().item() <= 2e-2
+        assert (lse - ref[1]).abs().max().item() <= 1e-3
+        if n <= 1000:
+            sub = [0, Hkv - 1]
+            for g in sub:
+                hs = list(range(g * 2, g * 2 + 2))
+                qs = _host(q[:, hs[0]:hs[-1] + 1])
+                ks, vs = _host(k[:, g:g + 1]), _host(v[:, g:g + 1])
+                ss = MaskSpec(spec.kind, [spec.head_param[h] for h in hs],
+                              sink=None if spec.sink is None else np.asarray(spec.sink)[hs],
+                              block=None if spec.block is None else np.asarray(spec.block)[hs],
+                              sink_tokens=spec.sink_tokens)
+                ref_o, _ = dense.attention(qs, ks, vs, ss)
+                got = np.stack([_host(o[0, h]) for h in hs]).astype(np.float64)
+                assert np.abs(got - ref_o[:]).max() <= MAX_ABS
+                assert np.linalg.norm(got - ref_o) / np.linalg.norm(ref_o) <= REL_L2
 
 
 @pytest.mark.parametrize("mask", ["causal", "swa576_sink"])
