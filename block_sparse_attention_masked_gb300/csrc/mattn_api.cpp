@@ -283,6 +283,8 @@ struct DeviceState {
   DeviceBuf dec_part;  // decode: per-chunk softmax states
   std::map<std::string, std::unique_ptr<DeviceBuf>> dec_heads;  // decode: per-head tables by content
   std::map<std::string, std::unique_ptr<Plan>> plans;
+  cudaStream_t io_stream = nullptr;      // mattn_fwd_host: copies in and out
+  std::vector<cudaEvent_t> io_events;    // mattn_fwd_host: chunk hand-offs
 };
 
 std::mutex g_mutex;
@@ -673,8 +675,10 @@ int mattn_fwd_host(const void* q, const void* k, const void* v, void* o, float* 
   if (!q || !k || !v || !o) return fail(MATTN_ERR_INVALID_ARG, "q, k, v and o must be non-NULL");
   DeviceState* st = nullptr;
   if ((rc = device_state(&st))) return rc;
+  if (!st->io_stream) MATTN_CUDA(cudaStreamCreateWithFlags(&st->io_stream, cudaStreamNonBlocking), "copy stream");
   const size_t esz = dtype == MATTN_F32 ? 4 : 2;
-  const size_t tensor = (size_t)B * H * N * d * esz;
+  const size_t head_elems = (size_t)N * d;  // one head of one batch entry
+  const size_t tensor = (size_t)B * H * head_elems * esz;
   const size_t lse_bytes = (size_t)B * H * N * 4;
   const size_t sink_bytes = desc->sink ? (size_t)H * 4 : 0;
   const size_t bits_bytes =
@@ -692,26 +696,89 @@ int mattn_fwd_host(const void* q, const void* k, const void* v, void* o, float* 
   char* dsink = reinterpret_cast<char*>(dlse) + up(lse_bytes);
   char* dbits = dsink + up(sink_bytes);
   char* dperm = dbits + up(bits_bytes);
-  MATTN_CUDA(cudaMemcpyAsync(dq, q, tensor, cudaMemcpyHostToDevice, stream), "copy q");
-  MATTN_CUDA(cudaMemcpyAsync(dk, k, tensor, cudaMemcpyHostToDevice, stream), "copy k");
-  MATTN_CUDA(cudaMemcpyAsync(dv, v, tensor, cudaMemcpyHostToDevice, stream), "copy v");
+  cudaStream_t io = st->io_stream;
+  // the mask's device copies first, on the copy stream
   mattn_mask_desc dd = *desc;
   if (desc->sink) {
-    MATTN_CUDA(cudaMemcpyAsync(dsink, desc->sink, sink_bytes, cudaMemcpyHostToDevice, stream), "copy sink");
+    MATTN_CUDA(cudaMemcpyAsync(dsink, desc->sink, sink_bytes, cudaMemcpyHostToDevice, io), "copy sink");
     dd.sink = reinterpret_cast<const float*>(dsink);
   }
   if (bits_bytes) {
-    MATTN_CUDA(cudaMemcpyAsync(dbits, desc->block_bits, bits_bytes, cudaMemcpyHostToDevice, stream), "copy bits");
+    MATTN_CUDA(cudaMemcpyAsync(dbits, desc->block_bits, bits_bytes, cudaMemcpyHostToDevice, io), "copy bits");
     dd.block_bits = reinterpret_cast<const uint64_t*>(dbits);
   }
   if (perm_bytes) {
-    MATTN_CUDA(cudaMemcpyAsync(dperm, desc->perm, perm_bytes, cudaMemcpyHostToDevice, stream), "copy perm");
+    MATTN_CUDA(cudaMemcpyAsync(dperm, desc->perm, perm_bytes, cudaMemcpyHostToDevice, io), "copy perm");
     dd.perm = reinterpret_cast<const int32_t*>(dperm);
   }
-  rc = fwd_locked(dq, dk, dv, dout, lse ? dlse : nullptr, B, H, H, N, d, dtype, &dd, stream, 0);
-  if (rc) return rc;
-  MATTN_CUDA(cudaMemcpyAsync(o, dout, tensor, cudaMemcpyDeviceToHost, stream), "copy o");
-  if (lse) MATTN_CUDA(cudaMemcpyAsync(lse, dlse, lse_bytes, cudaMemcpyDeviceToHost, stream), "copy lse");
+  // Pipeline over chunks of heads (about six per call, whole heads of one
+  // batch entry each): the compute stream starts on a chunk as soon as its
+  // inputs are in, while the copy stream brings the next ones.
+  const int per_b = std::max(1, std::min(H, (6 + B - 1) / B));
+  const int hc = (H + per_b - 1) / per_b;
+  struct Chunk { int b, h0, h1; };
+  std::vector<Chunk> chunks;
+  for (int b = 0; b < B; ++b)
+    for (int h0 = 0; h0 < H; h0 += hc) chunks.push_back({b, h0, std::min(H, h0 + hc)});
+  while (st->io_events.size() < 2 * chunks.size()) {
+    cudaEvent_t e;
+    MATTN_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming), "cudaEventCreate");
+    st->io_events.push_back(e);
+  }
+  // the compute stream's earlier work comes first
+  cudaEvent_t* ev = st->io_events.data();
+  MATTN_CUDA(cudaEventRecord(ev[0], stream), "event record");
+  MATTN_CUDA(cudaStreamWaitEvent(io, ev[0], 0), "stream wait");
+  // the copy stream takes every chunk's inputs first (each a set of
+  // contiguous copies), so that they stream in at full bandwidth while the
+  // compute stream starts on the first chunks; the outputs follow it back,
+  // chunk by chunk, each after its own compute
+  auto chunk_off = [&](const Chunk& ch) { return ((size_t)ch.b * H + ch.h0) * head_elems * esz; };
+  auto chunk_bytes = [&](const Chunk& ch) { return (size_t)(ch.h1 - ch.h0) * head_elems * esz; };
+  for (size_t c = 0; c < chunks.size(); ++c) {
+    const size_t off = chunk_off(chunks[c]), bytes = chunk_bytes(chunks[c]);
+    MATTN_CUDA(cudaMemcpyAsync(dq + off, static_cast<const char*>(q) + off, bytes, cudaMemcpyHostToDevice, io),
+               "copy q");
+    MATTN_CUDA(cudaMemcpyAsync(dk + off, static_cast<const char*>(k) + off, bytes, cudaMemcpyHostToDevice, io),
+               "copy k");
+    MATTN_CUDA(cudaMemcpyAsync(dv + off, static_cast<const char*>(v) + off, bytes, cudaMemcpyHostToDevice, io),
+               "copy v");
+    MATTN_CUDA(cudaEventRecord(ev[2 * c], io), "event record");
+  }
+  for (size_t c = 0; c < chunks.size(); ++c) {
+    const Chunk& ch = chunks[c];
+    const size_t off = chunk_off(ch);
+    MATTN_CUDA(cudaStreamWaitEvent(stream, ev[2 * c], 0), "stream wait");
+    // the chunk's heads as a call of their own
+    mattn_mask_desc cd = dd;
+    if (desc->head_param) cd.head_param = desc->head_param + ch.h0;
+    if (desc->head_order) cd.head_order = desc->head_order + ch.h0;
+    if (dd.sink) cd.sink = dd.sink + ch.h0;
+    if (bits_bytes && n.block_heads == H) {
+      cd.block_bits = dd.block_bits + (size_t)ch.h0 * n.block_nb * n.block_wpr;
+      cd.block_heads = ch.h1 - ch.h0;
+    }
+    const size_t lse_off = ((size_t)ch.b * H + ch.h0) * N;
+    rc = fwd_locked(dq + off, dk + off, dv + off, dout + off, lse ? dlse + lse_off : nullptr, 1, ch.h1 - ch.h0,
+                    ch.h1 - ch.h0, N, d, dtype, &cd, stream, 0);
+    if (rc) {
+      cudaStreamSynchronize(io);
+      return rc;
+    }
+    MATTN_CUDA(cudaEventRecord(ev[2 * c + 1], stream), "event record");
+  }
+  for (size_t c = 0; c < chunks.size(); ++c) {
+    const Chunk& ch = chunks[c];
+    const size_t off = chunk_off(ch), bytes = chunk_bytes(ch);
+    const size_t lse_off = ((size_t)ch.b * H + ch.h0) * N;
+    MATTN_CUDA(cudaStreamWaitEvent(io, ev[2 * c + 1], 0), "stream wait");
+    MATTN_CUDA(cudaMemcpyAsync(static_cast<char*>(o) + off, dout + off, bytes, cudaMemcpyDeviceToHost, io), "copy o");
+    if (lse)
+      MATTN_CUDA(cudaMemcpyAsync(lse + lse_off, dlse + lse_off, (size_t)(ch.h1 - ch.h0) * N * 4,
+                                 cudaMemcpyDeviceToHost, io),
+                 "copy lse");
+  }
+  MATTN_CUDA(cudaStreamSynchronize(io), "copy stream sync");
   MATTN_CUDA(cudaStreamSynchronize(stream), "stream sync");
   return MATTN_OK;
 }

@@ -202,9 +202,12 @@ int mattn_decode(const void* q, const void* k, const void* v, void* o, float* ls
 /*
  * mattn_fwd_host -- the same operation on HOST buffers: copies q, k, v (and
  * the sink and block bitmaps, which are then HOST pointers too) to device
- * memory owned by the library, runs mattn_fwd on `stream`, copies o and lse
- * back and synchronises the stream.  Pinned host memory gives full copy
- * bandwidth; pageable memory works.  lse may be NULL.
+ * memory owned by the library, runs the forward on `stream`, copies o and
+ * lse back and synchronises.  The work is cut into chunks of whole heads
+ * (about six per call): a second stream owned by the library copies chunk
+ * c in and chunk c - 1's output back while `stream` computes, so the
+ * copies overlap the kernels.  Pinned host memory gives full copy
+ * bandwidth and the overlap; pageable memory works.  lse may be NULL.
  */
 int mattn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
                    int B, int H, int N, int d, int dtype,

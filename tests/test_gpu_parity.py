@@ -278,3 +278,26 @@ def test_workload_bsparse128k(schedule):
     rows = _sample_rows(wl.N, [128 * i for i in range(1, 1024, 97)], 192, 4)
     check(q, k, v, spec, rows=rows, heads=[(0, 0), (0, 13), (0, 31)], tag=f"bsparse128k {schedule}",
           schedule=schedule)
+
+
+def test_host_pipeline_over_head_chunks():
+    """mattn_fwd_host cuts the call into chunks of heads on two streams: per
+    head parameters, per head block bitmaps, sinks and explicit orders must
+    follow their heads into the chunks (B = 2, H = 7: chunks of uneven
+    size), and the result equals the device entry point's."""
+    B, H, N, d = 2, 7, 640, 64
+    q, k, v = make_qkv(B, H, N, d, "bf16", 1.0, 21, device="cpu")
+    nb = -(-N // 128)
+    perm = random_order(N, 4)
+    specs = [
+        MaskSpec("block", [128] * H, block=bernoulli_causal_blocks(H, nb, 5), sink=np.linspace(-1, 1, H)),
+        MaskSpec("causal_window", [64, 128, 200, 300, 640, 17, 1], sink=np.linspace(1, -1, H)),
+        MaskSpec("sliding", [20] * H, perm=[None, None, None, perm, None, perm, None]),
+    ]
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    for spec in specs:
+        o, lse = mattn.attention_host(q.pin_memory(), k.pin_memory(), v.pin_memory(), spec)
+        od, lsed = mattn.attention(qd, kd, vd, mattn.prepare(spec, H, N))
+        torch.cuda.synchronize()
+        assert torch.equal(o, od.cpu()), spec.kind
+        assert torch.equal(lse, lsed.cpu()), spec.kind
