@@ -41,6 +41,10 @@ KIND = {"full": 0, "chunk": 1, "sliding": 2, "causal_window": 3, "block": 4}
 BF16, F32 = 0, 1
 ORDER_RASTER = -1
 ORDER_COLUMN_MAJOR = -2
+ORDER_BLOCK2X2_ROW = -3
+ORDER_BLOCK2X2_COL = -4
+_GRID_ORDERS = {"column_major": ORDER_COLUMN_MAJOR, "block2x2_row": ORDER_BLOCK2X2_ROW,
+                "block2x2_col": ORDER_BLOCK2X2_COL}
 TILE = 128
 TILE_FULL, TILE_PARTIAL = 1, 2
 FLAG_SCHEDULE_PAIRED, FLAG_SCHEDULE_SPLIT, FLAG_SCHEDULE_SINGLE = 1, 2, 4
@@ -172,10 +176,11 @@ class PreparedMask:
             g = grids[h] if grids is not None else None
             pm = perms[h] if perms is not None else None
             if g is not None:
-                if grid is not None and tuple(g) != grid:
-                    raise ValueError("all column-major heads must share one grid")
-                grid = tuple(int(x) for x in g)
-                orders[h] = ORDER_COLUMN_MAJOR
+                gg = (int(g[0]), int(g[1]))
+                if grid is not None and gg != grid:
+                    raise ValueError("all grid-ordered heads must share one grid")
+                grid = gg
+                orders[h] = _GRID_ORDERS[g[2] if len(g) > 2 else "column_major"]
             elif pm is not None:
                 orders[h] = len(explicit)
                 explicit.append(np.asarray(pm, dtype=np.int32))

@@ -320,18 +320,40 @@ __device__ __forceinline__ void raise_error(const FwdParams& p, Barriers* bar, u
   atomicOr(p.err, bit);
 }
 
-// TMA load of one 128-row tile (all d columns) starting at sequence position p0.
-// `policy` is the L2 eviction priority of the tile's lines.
+// 2x2-block row-major order: the 5D view's coordinates (C, R + bh * rows/2)
+// of the tile at position p0 (32 blocks of one block row: cols % 64 == 0).
+__device__ __forceinline__ void block2x2_coords(const FwdParams& p, int p0, int bh, int* c3, int* c4) {
+  const int blk = p0 >> 2;
+  const int half_cols = p.grid_cols >> 1;
+  const int R = blk / half_cols;
+  *c3 = blk - R * half_cols;
+  *c4 = R + bh * (p.grid_rows >> 1);
+}
+
+// TMA load of one 128-row tile (all d columns) starting at sequence position
+// p0, through the raster view, the column-major view or the 2x2-block view
+// (`mode`, a LoadMode).  `policy` is the L2 eviction priority of the tile's
+// lines.
 template <int D>
 __device__ __forceinline__ void load_tile(const FwdParams& p, const CUtensorMap* raster, const CUtensorMap* colmaj,
-                                          bool column_major, uint8_t* dst, uint64_t* bar, int p0, int bh,
-                                          uint64_t policy) {
+                                          const CUtensorMap* blocks, int mode, uint8_t* dst, uint64_t* bar, int p0,
+                                          int bh, uint64_t policy) {
   using G = Geo<D>;
-  if (!column_major) {
+  if (mode == kLoadRaster) {
 #pragma unroll
     for (int c = 0; c < G::kChunks; ++c)
       ptx::tma_load_3d_hint(dst + c * G::kChunkBytes, &raster[0], bar, c * 64, p0, bh, policy);
     if (G::kRem) ptx::tma_load_3d_hint(dst + G::kChunks * G::kChunkBytes, &raster[1], bar, 0, p0, bh, policy);
+  } else if (mode == kLoadBlock2x2Row) {
+    // the box (d chunk, dc 2, dr 2, 32 blocks) lands in position order:
+    // row C * 4 + dr * 2 + dc of the tile
+    int c3, c4;
+    block2x2_coords(p, p0, bh, &c3, &c4);
+#pragma unroll
+    for (int c = 0; c < G::kChunks; ++c)
+      ptx::tma_load_5d_hint(dst + c * G::kChunkBytes, &blocks[0], bar, c * 64, 0, 0, c3, c4, policy);
+    if (G::kRem)
+      ptx::tma_load_5d_hint(dst + G::kChunks * G::kChunkBytes, &blocks[1], bar, 0, 0, 0, c3, c4, policy);
   } else {
     // position p = c * rows + r holds token r * cols + c; a 128-position tile is
     // one grid column c, rows r0 .. r0 + 127 (rows % 128 == 0 is required).
@@ -348,13 +370,19 @@ __device__ __forceinline__ void load_tile(const FwdParams& p, const CUtensorMap*
 // TMA load of one 128-row V tile in its uniform-swizzle layout (map [0] of
 // the V views has a kVW-column box).
 template <int D>
-__device__ __forceinline__ void load_v_tile(const FwdParams& p, bool column_major, uint8_t* dst, uint64_t* bar,
-                                            int p0, int bh, uint64_t policy) {
+__device__ __forceinline__ void load_v_tile(const FwdParams& p, int mode, uint8_t* dst, uint64_t* bar, int p0,
+                                            int bh, uint64_t policy) {
   using G = Geo<D>;
-  if (!column_major) {
+  if (mode == kLoadRaster) {
 #pragma unroll
     for (int c = 0; c < G::kVChunks; ++c)
       ptx::tma_load_3d_hint(dst + c * G::kVChunkBytes, &p.tv[0], bar, c * G::kVW, p0, bh, policy);
+  } else if (mode == kLoadBlock2x2Row) {
+    int c3, c4;
+    block2x2_coords(p, p0, bh, &c3, &c4);
+#pragma unroll
+    for (int c = 0; c < G::kVChunks; ++c)
+      ptx::tma_load_5d_hint(dst + c * G::kVChunkBytes, &p.bv[0], bar, c * G::kVW, 0, 0, c3, c4, policy);
   } else {
     const int col = p0 / p.grid_rows;
     const int r0 = p0 - col * p.grid_rows;
@@ -449,13 +477,8 @@ __host__ __device__ constexpr int kOHalf() {
 }
 
 __device__ __forceinline__ int64_t token_of(const FwdParams& p, int store_mode, int perm_row, int64_t pos) {
-  if (store_mode == kStoreColumnMajor) {
-    int64_t c = pos / p.grid_rows;
-    int64_t r = pos - c * p.grid_rows;
-    return r * p.grid_cols + c;
-  }
-  if (store_mode == kStoreExplicit) return p.perm[(int64_t)perm_row * p.N + pos];
-  return pos;
+  return token_at(store_mode, p.grid_rows, p.grid_cols,
+                  store_mode == kStoreExplicit ? p.perm + (int64_t)perm_row * p.N : nullptr, pos);
 }
 
 template <int D, bool OUT_F32>
@@ -513,7 +536,6 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
   __syncthreads();
   const TileList& L = bar->tl;
   const int load_mode = p.head_info[ip.h * 4 + kHeadLoad];
-  const bool colmaj = load_mode == kLoadColumnMajor;
 
   // Registers: 384 threads launched at 168 each; the producer / MMA
   // warpgroup gives up to kRegsControl so that each softmax warpgroup can hold
@@ -532,14 +554,14 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
       // them in L2); a Q tile is read by this CTA alone
       const uint64_t keep = ptx::l2_policy_evict_last();
       if (is_k) {
-        const CUtensorMap* mq = colmaj ? p.cq : p.tq;
+        const CUtensorMap* mq = load_mode == kLoadColumnMajor ? p.cq : (load_mode == kLoadBlock2x2Row ? p.bq : p.tq);
         ptx::prefetch_tmap(&mq[0]);
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
           const SubPlan& sp = s ? ip.sp1 : ip.sp0;
           if (!list_has(L, s, p.split) || (p.split && s == 1)) continue;  // split: one Q tile for both pipelines
           ptx::mbar_arrive_expect_tx(&bar->q_full[s], G::kTileBytes);
-          load_tile<D>(p, p.tq, p.cq, colmaj, sq + s * G::kTileBytes, &bar->q_full[s], sp.qt * kTile, ip.bh,
+          load_tile<D>(p, p.tq, p.cq, p.bq, load_mode, sq + s * G::kTileBytes, &bar->q_full[s], sp.qt * kTile, ip.bh,
                        ptx::l2_policy_evict_first());
         }
       }
@@ -557,9 +579,10 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
         }
         ptx::mbar_arrive_expect_tx(&full[slot], G::kTileBytes);
         if (is_k)
-          load_tile<D>(p, p.tk, p.ck, colmaj, ring + slot * G::kTileBytes, &full[slot], kt * kTile, ip.bh_kv, keep);
+          load_tile<D>(p, p.tk, p.ck, p.bk, load_mode, ring + slot * G::kTileBytes, &full[slot], kt * kTile, ip.bh_kv,
+                       keep);
         else
-          load_v_tile<D>(p, colmaj, ring + slot * G::kTileBytes, &full[slot], kt * kTile, ip.bh_kv, keep);
+          load_v_tile<D>(p, load_mode, ring + slot * G::kTileBytes, &full[slot], kt * kTile, ip.bh_kv, keep);
       }
       if (*abort_flag) {
         // let copies already in flight land before the CTA's shared memory goes away
@@ -949,13 +972,11 @@ __global__ void gather_kernel(const GatherParams p) {
   const int64_t bh = row / p.N;
   const int h = (int)(bh % p.H);
   const int store_mode = p.head_info[h * 4 + kHeadStore];
-  int64_t tok = pos;
-  if (store_mode == kStoreColumnMajor) {
-    int64_t c = pos / p.grid_rows;
-    tok = (pos - c * p.grid_rows) * p.grid_cols + c;
-  } else if (store_mode == kStoreExplicit) {
-    tok = p.perm[(int64_t)p.head_info[h * 4 + kHeadPermRow] * p.N + pos];
-  }
+  const int64_t tok = token_at(store_mode, p.grid_rows, p.grid_cols,
+                               store_mode == kStoreExplicit
+                                   ? p.perm + (int64_t)p.head_info[h * 4 + kHeadPermRow] * p.N
+                                   : nullptr,
+                               pos);
   const int64_t src_bh = t == 0 ? bh : (bh / p.H) * (p.H / p.kv_group) + h / p.kv_group;
   const int64_t src_off = (src_bh * p.N + tok) * p.d + c8;
   uint4 out;

@@ -483,14 +483,13 @@ __global__ void __launch_bounds__(kThreadsD256, 1) attention_sp_kernel(const __g
       }
       // caller token of this position (the inputs were reordered to
       // positions; the output goes back to token order)
-      int64_t tok = pos;
       const int store_mode = p.head_info[h * 4 + kHeadStore];
-      if (valid && store_mode == kStoreColumnMajor) {
-        const int64_t c = pos / p.grid_rows;
-        tok = (pos - c * p.grid_rows) * p.grid_cols + c;
-      } else if (valid && store_mode == kStoreExplicit) {
-        tok = p.perm[(int64_t)p.head_info[h * 4 + kHeadPermRow] * p.N + pos];
-      }
+      const int64_t tok = !valid ? pos
+                                 : token_at(store_mode, p.grid_rows, p.grid_cols,
+                                            store_mode == kStoreExplicit
+                                                ? p.perm + (int64_t)p.head_info[h * 4 + kHeadPermRow] * p.N
+                                                : nullptr,
+                                            pos);
       const int64_t orow = ((int64_t)bh * p.N + tok) * kD;
 #pragma unroll 1
       for (int c0 = 0; c0 < kD; c0 += 32) {

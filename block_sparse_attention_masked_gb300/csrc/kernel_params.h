@@ -13,8 +13,45 @@ constexpr int kBlockListMax = 4096;
 
 // Per-head table (device int32 [H][4]).
 enum HeadField : int { kHeadParam = 0, kHeadLoad = 1, kHeadStore = 2, kHeadPermRow = 3 };
-enum LoadMode : int { kLoadRaster = 0, kLoadColumnMajor = 1 };
-enum StoreMode : int { kStoreIdentity = 0, kStoreColumnMajor = 1, kStoreExplicit = 2 };
+enum LoadMode : int { kLoadRaster = 0, kLoadColumnMajor = 1, kLoadBlock2x2Row = 2 };
+enum StoreMode : int {
+  kStoreIdentity = 0,
+  kStoreColumnMajor = 1,
+  kStoreExplicit = 2,
+  kStoreBlock2x2Row = 3,
+  kStoreBlock2x2Col = 4,
+};
+
+// Caller token at sequence position pos of a head in store mode `mode` on a
+// rows x cols raster grid (perm_row: the head's explicit order, or null).
+//   column-major      p = c * rows + r                        -> r * cols + c
+//   2x2 blocks, rows  blocks left to right, then top to bottom, each block's
+//                     four patches in raster order            -> (2R + dr) * cols + 2C + dc
+//   2x2 blocks, cols  blocks top to bottom, then left to right
+// (SHS slides, "Factor 2": orders (c) and (d) over the 2x2 patch blocks that
+// Qwen2.5-VL merges; the walk inside a block is not given and is read as
+// raster).
+__host__ __device__ __forceinline__ int64_t token_at(int mode, int64_t rows, int64_t cols, const int32_t* perm_row,
+                                                     int64_t pos) {
+  if (mode == kStoreColumnMajor) {
+    const int64_t c = pos / rows;
+    return (pos - c * rows) * cols + c;
+  }
+  if (mode == kStoreBlock2x2Row || mode == kStoreBlock2x2Col) {
+    const int64_t blk = pos >> 2, dr = (pos >> 1) & 1, dc = pos & 1;
+    int64_t R, C;
+    if (mode == kStoreBlock2x2Row) {
+      R = blk / (cols / 2);
+      C = blk - R * (cols / 2);
+    } else {
+      C = blk / (rows / 2);
+      R = blk - C * (rows / 2);
+    }
+    return (2 * R + dr) * cols + 2 * C + dc;
+  }
+  if (mode == kStoreExplicit) return perm_row[pos];
+  return pos;
+}
 
 // Device error-word bits (which wait gave up).
 enum ErrBits : uint32_t {
@@ -29,6 +66,7 @@ struct FwdParams {
   // [0]: 64-column chunks (128-byte swizzle); [1]: the 16- or 32-column rest.
   CUtensorMap tq[2], tk[2], tv[2];  // [B*H][N][d] views
   CUtensorMap cq[2], ck[2], cv[2];  // column-major views [B*H][rows][cols][d]
+  CUtensorMap bq[2], bk[2], bv[2];  // 2x2-block row-major views [B*H*rows/2][cols/2][2][2][d]
   void* o;                          // [B][H][N][d], bf16 or fp32
   float* lse;                       // [B][H][N] or null
   const int2* items;                // (b*H + h, query-tile pair), or (b*H + h, query tile) when split

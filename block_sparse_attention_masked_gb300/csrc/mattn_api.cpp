@@ -72,6 +72,7 @@ struct Normalized {
   std::vector<HeadPlan> heads;
   bool need_copy;     // reorder / convert into a bf16 copy in position order
   bool any_colmajor_tma;
+  bool any_block_tma;  // some head reads the 2x2-block row-major order through 5D TMA views
   int block_c, block_nb, block_wpr, block_heads;
   int sink_tokens;    // causal window: leading positions every later query sees
   float scale;
@@ -81,7 +82,11 @@ struct Normalized {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int normalize(const mattn_mask_desc* desc, int B, int H, int N, int d, int dtype, bool need_data, Normalized* out) {
+// allow_block_tma: the caller's kernel reads the 2x2-block row-major order
+// through its 5D TMA views (the attention forward); otherwise such heads go
+// through the reorder copy.
+int normalize(const mattn_mask_desc* desc, int B, int H, int N, int d, int dtype, bool need_data, Normalized* out,
+              bool allow_block_tma = true) {
   if (!desc) return fail(MATTN_ERR_INVALID_ARG, "mask descriptor is NULL");
   if (desc->flags != 0 && desc->flags != MATTN_FLAG_SCHEDULE_PAIRED && desc->flags != MATTN_FLAG_SCHEDULE_SPLIT &&
       desc->flags != MATTN_FLAG_SCHEDULE_SINGLE)
@@ -134,6 +139,21 @@ int normalize(const mattn_mask_desc* desc, int B, int H, int N, int d, int dtype
         n.heads[h].load = kLoadRaster;
         n.need_copy = true;
       }
+    } else if (order == MATTN_ORDER_BLOCK2X2_ROW || order == MATTN_ORDER_BLOCK2X2_COL) {
+      if (desc->grid_rows < 2 || desc->grid_cols < 2 || (int64_t)desc->grid_rows * desc->grid_cols != N ||
+          (desc->grid_rows & 1) || (desc->grid_cols & 1))
+        return fail(MATTN_ERR_INVALID_ARG,
+                    "2x2-block orders need an even grid with grid_rows * grid_cols == N (%d x %d vs %d)",
+                    desc->grid_rows, desc->grid_cols, N);
+      const bool row = order == MATTN_ORDER_BLOCK2X2_ROW;
+      n.heads[h].store = row ? kStoreBlock2x2Row : kStoreBlock2x2Col;
+      // a 128-position tile is 32 blocks of one block row when cols % 64 == 0
+      if (row && allow_block_tma && desc->grid_cols % 64 == 0) {
+        n.heads[h].load = kLoadBlock2x2Row;
+      } else {
+        n.heads[h].load = kLoadRaster;
+        n.need_copy = true;
+      }
     } else if (order >= 0) {
       if (!desc->perm || order >= desc->n_perm)
         return fail(MATTN_ERR_INVALID_ARG, "head %d selects explicit order %d but n_perm = %d", h, order, desc->n_perm);
@@ -145,10 +165,14 @@ int normalize(const mattn_mask_desc* desc, int B, int H, int N, int d, int dtype
       return fail(MATTN_ERR_INVALID_ARG, "head %d has invalid order code %d", h, order);
     }
   }
+  n.any_block_tma = false;
   if (n.need_copy) {
     for (auto& hp : n.heads) hp.load = kLoadRaster;  // the copy is already in position order
   } else {
-    for (auto& hp : n.heads) n.any_colmajor_tma |= hp.load == kLoadColumnMajor;
+    for (auto& hp : n.heads) {
+      n.any_colmajor_tma |= hp.load == kLoadColumnMajor;
+      n.any_block_tma |= hp.load == kLoadBlock2x2Row;
+    }
   }
   if (n.kind == MATTN_BLOCK_SPARSE) {
     const int bs = n.heads[0].param;
@@ -181,6 +205,7 @@ int normalize(const mattn_mask_desc* desc, int B, int H, int N, int d, int dtype
       if (hp.store != kStoreIdentity) n.need_copy = true;
     for (auto& hp : n.heads) hp.load = kLoadRaster;
     n.any_colmajor_tma = false;
+    n.any_block_tma = false;
     n.split = true;
   }
   *out = std::move(n);
@@ -451,6 +476,46 @@ int make_v_maps(const Normalized& n, const void* base, CUtensorMap raster[2], CU
   return MATTN_OK;
 }
 
+// 2x2-block row-major views [heads * rows/2][cols/2][2][2][d] of one bf16
+// tensor, in the box order (d chunk, dc, dr, block column, block row) so that
+// a box of 32 blocks lands in sequence-position order.  K-major tiles (Q, K):
+// map [0] covers 64-column chunks (128-byte swizzle), map [1] the 16- or
+// 32-column rest; V (v_layout): map [0] with the uniform kVW-column boxes.
+int make_block_maps(const Normalized& n, const void* base, CUtensorMap maps[2], int rows, int cols, int64_t heads,
+                    bool v_layout) {
+  const int d = n.d;
+  memset(maps, 0, 2 * sizeof(CUtensorMap));
+  const cuuint64_t es = 2;
+  cuuint64_t strides[4] = {(cuuint64_t)d * es, (cuuint64_t)cols * d * es, 2 * (cuuint64_t)d * es,
+                           2 * (cuuint64_t)cols * d * es};
+  auto one = [&](CUtensorMap* m, const void* b, int width, CUtensorMapSwizzle sw) {
+    cuuint64_t dims[5] = {(cuuint64_t)width, 2, 2, (cuuint64_t)cols / 2, (cuuint64_t)(rows / 2) * heads};
+    cuuint32_t box[5] = {(cuuint32_t)(v_layout ? width : (width >= 64 ? 64 : width)), 2, 2, 32, 1};
+    return encode(m, b, 5, dims, strides, box, sw);
+  };
+  if (v_layout) {
+    const int vw = d % 64 == 0 ? 64 : (d % 32 == 0 ? 32 : 16);
+    const CUtensorMapSwizzle sw =
+        vw == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : (vw == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+    cuuint64_t dims[5] = {(cuuint64_t)d, 2, 2, (cuuint64_t)cols / 2, (cuuint64_t)(rows / 2) * heads};
+    cuuint32_t box[5] = {(cuuint32_t)vw, 2, 2, 32, 1};
+    return encode(&maps[0], base, 5, dims, strides, box, sw);
+  }
+  const int chunks = d / 64, rem = d % 64;
+  if (chunks) {
+    cuuint64_t dims[5] = {(cuuint64_t)d, 2, 2, (cuuint64_t)cols / 2, (cuuint64_t)(rows / 2) * heads};
+    cuuint32_t box[5] = {64, 2, 2, 32, 1};
+    int rc = encode(&maps[0], base, 5, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc) return rc;
+  }
+  if (rem) {
+    const char* rem_base = static_cast<const char*>(base) + (size_t)chunks * 64 * 2;
+    int rc = one(&maps[1], rem_base, rem, rem == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B);
+    if (rc) return rc;
+  }
+  return MATTN_OK;
+}
+
 int check_device_ptrs(const void* q, const void* k, const void* v, const void* o, const float* lse) {
   if (!q || !k || !v || !o) return fail(MATTN_ERR_INVALID_ARG, "q, k, v and o must be non-NULL");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
@@ -517,6 +582,12 @@ int fwd_locked(const void* q, const void* k, const void* v, void* o, float* lse,
     if ((rc = make_maps(n, use[0], p.tq, p.cq, rows, cols, (int64_t)B * H))) return rc;
     if ((rc = make_maps(n, use[1], p.tk, p.ck, rows, cols, (int64_t)B * kv_heads))) return rc;
     if ((rc = make_v_maps(n, use[2], p.tv, p.cv, rows, cols, (int64_t)B * kv_heads))) return rc;
+    if (n.any_block_tma) {
+      const int gr = desc->grid_rows, gc = desc->grid_cols;
+      if ((rc = make_block_maps(n, use[0], p.bq, gr, gc, (int64_t)B * H, false))) return rc;
+      if ((rc = make_block_maps(n, use[1], p.bk, gr, gc, (int64_t)B * kv_heads, false))) return rc;
+      if ((rc = make_block_maps(n, use[2], p.bv, gr, gc, (int64_t)B * kv_heads, true))) return rc;
+    }
   }
   p.H_kv = kv_heads;
   p.kv_group = H / kv_heads;
@@ -595,6 +666,11 @@ int prepare_in_place_launch(const void* q, const void* k, const void* v, void* o
   if ((rc = make_maps(n, q, p.tq, p.cq, rows, cols, (int64_t)B * H))) return rc;
   if ((rc = make_maps(n, k, p.tk, p.ck, rows, cols, (int64_t)B * H))) return rc;
   if ((rc = make_v_maps(n, v, p.tv, p.cv, rows, cols, (int64_t)B * H))) return rc;
+  if (n.any_block_tma) {
+    if ((rc = make_block_maps(n, q, p.bq, desc->grid_rows, desc->grid_cols, (int64_t)B * H, false))) return rc;
+    if ((rc = make_block_maps(n, k, p.bk, desc->grid_rows, desc->grid_cols, (int64_t)B * H, false))) return rc;
+    if ((rc = make_block_maps(n, v, p.bv, desc->grid_rows, desc->grid_cols, (int64_t)B * H, true))) return rc;
+  }
   p.H_kv = H;
   p.kv_group = 1;
   p.o = o;
@@ -880,7 +956,7 @@ int mattn_received(const void* q, const void* k, const float* lse, float* r, int
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   std::lock_guard<std::mutex> lk(g_mutex);
   Normalized n;
-  int rc = normalize(desc, B, H, N, d, dtype, true, &n);
+  int rc = normalize(desc, B, H, N, d, dtype, true, &n, false);
   if (rc) return rc;
   if (n.sink_tokens > 0) return fail(MATTN_ERR_UNSUPPORTED, "received attention does not take sink tokens");
   if (d == 256) return fail(MATTN_ERR_UNSUPPORTED, "received attention supports head dims up to 128");

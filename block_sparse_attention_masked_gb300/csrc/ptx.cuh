@@ -161,6 +161,16 @@ __device__ __forceinline__ void bulk_load_g2s(void* sdst, const void* gsrc, uint
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_5d_hint(void* dst, const CUtensorMap* tm, uint64_t* bar, int c0, int c1,
+                                                 int c2, int c3, int c4, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+      "l"(policy)
+      : "memory");
+}
+
 // L2 policies: keep (K, V tiles that many query tiles re-read) or drop
 // first (Q tiles, read once).
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {

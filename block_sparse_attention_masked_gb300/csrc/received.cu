@@ -121,12 +121,8 @@ __device__ __forceinline__ void build_q_list(const RecvParams& p, const uint64_t
 }
 
 __device__ __forceinline__ int64_t rc_token_of(const RecvParams& p, int store_mode, int perm_row, int64_t pos) {
-  if (store_mode == kStoreColumnMajor) {
-    const int64_t c = pos / p.grid_rows;
-    return (pos - c * p.grid_rows) * p.grid_cols + c;
-  }
-  if (store_mode == kStoreExplicit) return p.perm[(int64_t)perm_row * p.N + pos];
-  return pos;
+  return token_at(store_mode, p.grid_rows, p.grid_cols,
+                  store_mode == kStoreExplicit ? p.perm + (int64_t)perm_row * p.N : nullptr, pos);
 }
 
 // TMA load of one 128-row tile at sequence position p0 (raster view, or the

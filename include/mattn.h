@@ -82,6 +82,14 @@ typedef enum { MATTN_BF16 = 0, MATTN_F32 = 1 } mattn_dtype;
 #define MATTN_ORDER_COLUMN_MAJOR (-2) /* grid_rows x grid_cols raster grid walked       */
                                       /* column by column: position p = c*rows + r      */
                                       /* holds token r*cols + c                         */
+#define MATTN_ORDER_BLOCK2X2_ROW (-3) /* 2x2 patch blocks of the grid, blocks left to right  */
+                                      /* then top to bottom, each block's patches in raster */
+                                      /* order: position 4*(R*cols/2 + C) + 2*dr + dc holds */
+                                      /* token (2R+dr)*cols + 2C+dc (SHS slides, Factor 2,  */
+                                      /* order (c); read through TMA when cols % 64 == 0)   */
+#define MATTN_ORDER_BLOCK2X2_COL (-4) /* the same blocks top to bottom then left to right:  */
+                                      /* position 4*(C*rows/2 + R) + 2*dr + dc (order (d))  */
+                                      /* Both need even grid_rows and grid_cols.            */
 /* A value k >= 0 selects explicit order k: perm[k*N + p] = token at position p. */
 
 #define MATTN_TILE 128 /* query / key tile edge of the tile plan */

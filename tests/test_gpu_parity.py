@@ -301,3 +301,49 @@ def test_host_pipeline_over_head_chunks():
         torch.cuda.synchronize()
         assert torch.equal(o, od.cpu()), spec.kind
         assert torch.equal(lse, lsed.cpu()), spec.kind
+
+
+@pytest.mark.parametrize("d", [64, 80, 128])
+@pytest.mark.parametrize("rows,cols", [(16, 64), (32, 8)])
+def test_block2x2_orders(d, rows, cols):
+    """SWA-1D over the 2x2 patch blocks (SHS slides, Factor 2, orders (c) and
+    (d)) next to raster heads: order (c) is read through 5D TMA views when
+    cols % 64 == 0 (else, like order (d), through the reorder copy); outputs
+    come back in token order."""
+    from workloads import block2x2_order
+
+    n = rows * cols
+    H = 4
+    q, k, v = _qkv(1, H, n, d, seed=rows * 7 + d)
+    row, col = block2x2_order(rows, cols), block2x2_order(rows, cols, by_columns=True)
+    perm = [row, col, None, row]
+    grid = [(rows, cols, "block2x2_row"), (rows, cols, "block2x2_col"), None, (rows, cols, "block2x2_row")]
+    for spec in (MaskSpec("sliding", [40] * H, perm=perm, perm_grid=grid),
+                 MaskSpec("chunk", [128] * H, perm=perm, perm_grid=grid),
+                 MaskSpec("causal_window", [200, 64, 300, 1000], perm=perm, perm_grid=grid,
+                          sink=np.array([0.5, -0.5, 0.0, 1.0]))):
+        check(q, k, v, spec, tag=f"block2x2 {spec.kind} {rows}x{cols} d{d}")
+
+
+def test_block2x2_orders_other_paths():
+    """Order (c) on the paths that read positions through the copy: fp32
+    inputs, the single-pipeline schedule, received attention."""
+    from workloads import block2x2_order
+
+    rows, cols, H = 16, 64, 2
+    n = rows * cols
+    row = block2x2_order(rows, cols)
+    spec = MaskSpec("sliding", [30, 30], perm=[row, None], perm_grid=[(rows, cols, "block2x2_row"), None])
+    q, k, v = _qkv(1, H, n, 64, seed=3, dtype="f32")
+    check(q, k, v, spec, tag="block2x2 fp32")
+    qb, kb, vb = _qkv(1, H, n, 128, seed=4)
+    o1, l1 = mattn.attention(qb, kb, vb, mattn.prepare(spec, H, n))
+    o2, l2 = mattn.attention(qb, kb, vb, mattn.prepare(spec, H, n, schedule="single"))
+    torch.cuda.synchronize()
+    assert (o1.float() - o2.float()).abs().max().item() <= 2e-2
+    assert (l1 - l2).abs().max().item() <= 1e-3
+    r = mattn.received(qb, kb, l1, mattn.prepare(spec, H, n))
+    torch.cuda.synchronize()
+    ref = dense.received_attention(_host(qb), _host(kb), spec)
+    got = _host(r)[0].astype(np.float64)
+    assert (np.abs(got - ref) <= 2e-3 * ref + 1e-5).all()

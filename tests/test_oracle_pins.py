@@ -540,3 +540,23 @@ def test_decode_empty_sequence():
     o, lse = dense.decode(q, k, k, [0], MaskSpec("full", [0, 0], sink=np.array([-np.inf, 0.7])))
     assert np.all(o == 0)
     assert lse[0, 0] == -np.inf and lse[0, 1] == pytest.approx(0.7)
+
+
+def test_block2x2_orders_hand_written():
+    """The 2x2-block orders (c) and (d) of a 4x4 grid written out by hand
+    (pins the generator the tests feed both sides with, and the oracle's
+    inverse permutation of it)."""
+    from workloads import block2x2_order
+
+    row, col = ([int(x) for x in r] for r in read_golden("block2x2_orders_4x4.txt"))
+    assert list(block2x2_order(4, 4)) == row
+    assert list(block2x2_order(4, 4, by_columns=True)) == col
+    pos = dense.inverse_permutation(np.array(row), 16)
+    assert pos[4] == 2 and pos[2] == 4 and pos[15] == 15
+    # a sliding window over order (c) keeps the 2x2 block neighbours together
+    spec = _one_head("sliding", 1, perm=np.array(row))
+    q = np.zeros((1, 1, 16, 2))
+    v = np.arange(32, dtype=np.float64).reshape(1, 1, 16, 2)
+    o, _ = dense.attention(q, q, v, spec)
+    # token 5 sits at position 3, its window holds positions 2..4 = tokens 4, 5, 2
+    np.testing.assert_allclose(o[0, 5], v[0, 0, [4, 5, 2]].mean(axis=0))

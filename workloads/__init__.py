@@ -34,10 +34,11 @@ class MaskSpec:
                 block size B (block); ignored for "full".
     perm:       per head, None (identity) or an int array with
                 perm[p] = caller token index at sequence position p.
-    perm_grid:  per head, None or (rows, cols) when perm is the column-major
-                order of a rows x cols raster grid (a plain description of the
-                same perm, so that a caller can name the order instead of
-                passing the array).
+    perm_grid:  per head, None, (rows, cols) when perm is the column-major
+                order of a rows x cols raster grid, or (rows, cols, kind) with
+                kind "column_major", "block2x2_row" or "block2x2_col" (a plain
+                description of the same perm, so that a caller can name the
+                order instead of passing the array).
     block:      bool [H, Nb, Nb] block-selection matrices (kind "block").
     sink:       float [H] sink logits, or None.
     sink_tokens: kind "causal_window": the first sink_tokens positions stay
@@ -62,6 +63,24 @@ def column_major_order(rows: int, cols: int) -> np.ndarray:
     """
     c, r = np.divmod(np.arange(rows * cols, dtype=np.int64), rows)
     return (r * cols + c).astype(np.int64)
+
+
+def block2x2_order(rows: int, cols: int, by_columns: bool = False) -> np.ndarray:
+    """perm[p] for the walk over the 2x2 patch blocks of a rows x cols
+    raster-numbered grid (SHS slides, Factor 2: Qwen2.5-VL merges 2x2 patches
+    into one block; order (c) takes the blocks left to right then top to
+    bottom, order (d) top to bottom then left to right).  Inside a block the
+    four patches go in raster order (the figure is not in the text; read).
+    Position p = 4 * block + 2 * dr + dc."""
+    if rows % 2 or cols % 2:
+        raise ValueError("2x2-block orders need an even grid")
+    p = np.arange(rows * cols, dtype=np.int64)
+    blk, dr, dc = p // 4, (p // 2) % 2, p % 2
+    if by_columns:
+        C, R = np.divmod(blk, rows // 2)
+    else:
+        R, C = np.divmod(blk, cols // 2)
+    return ((2 * R + dr) * cols + 2 * C + dc).astype(np.int64)
 
 
 def random_order(n: int, seed: int) -> np.ndarray:
@@ -115,7 +134,7 @@ WORKLOADS = {
         "896^2 ViT layer: 64x64 grid raster order, B1 H16 N4096 d80, bf16 0.5*N(0,1)"),
     "vit16384": Workload(
         "vit16384", 1, 16, 16384, 80, "bf16", 0.5, (128, 128),
-        ("sliding256_rowcol", "full", "chunk512"),
+        ("sliding256_rowcol", "full", "chunk512", "sliding256_blocks"),
         "1792^2 ViT layer: 128x128 grid, B1 H16 N16384 d80, bf16 0.5*N(0,1); "
         "sliding window 256 on raster order for heads 0-7 and column-major order for heads 8-15"),
     "causal4096": Workload(
@@ -164,6 +183,19 @@ def make_mask(wl: Workload, mask: str, seed: int = 0, n: Optional[int] = None,
         return MaskSpec("full", [0] * nh, name=mask)
     if mask.startswith("chunk"):
         return MaskSpec("chunk", [int(mask[5:])] * nh, name=mask)
+    if mask.startswith("sliding") and mask.endswith("_blocks"):
+        # SWA-1D over the 2x2 patch blocks: row order (c) on the first half of
+        # the heads, column order (d) on the second (SHS slides, Factor 2)
+        w = int(mask[len("sliding"):-len("_blocks")])
+        side = int(round(n ** 0.5))
+        if side * side != n:
+            raise ValueError("2x2-block orders need a square grid here")
+        perm, grid = [None] * nh, [None] * nh
+        for h in range(nh):
+            by_cols = h >= nh // 2
+            perm[h] = block2x2_order(side, side, by_cols)
+            grid[h] = (side, side, "block2x2_col" if by_cols else "block2x2_row")
+        return MaskSpec("sliding", [w] * nh, perm=perm, perm_grid=grid, name=mask)
     if mask.startswith("sliding") and mask.endswith("_rowcol"):
         w = int(mask[len("sliding"):-len("_rowcol")])
         side = int(round(n ** 0.5))
