@@ -320,35 +320,47 @@ __device__ __forceinline__ void raise_error(const FwdParams& p, Barriers* bar, u
   atomicOr(p.err, bit);
 }
 
-// 2x2-block row-major order: the 5D view's coordinates (C, R + bh * rows/2)
-// of the tile at position p0 (32 blocks of one block row: cols % 64 == 0).
-__device__ __forceinline__ void block2x2_coords(const FwdParams& p, int p0, int bh, int* c3, int* c4) {
+// 2x2-block orders: the 5D view's coordinates (c3, c4) of the tile at
+// position p0 (32 consecutive blocks).  Row-major view (d, dc, dr, C,
+// R + bh * rows/2): 32 blocks of one block row (cols % 64 == 0).
+// Column-major view (d, dc, dr, R + bh * rows/2, C): 32 blocks of one block
+// column (rows % 64 == 0).
+__device__ __forceinline__ void block2x2_coords(const FwdParams& p, int mode, int p0, int bh, int* c3, int* c4) {
   const int blk = p0 >> 2;
-  const int half_cols = p.grid_cols >> 1;
-  const int R = blk / half_cols;
-  *c3 = blk - R * half_cols;
-  *c4 = R + bh * (p.grid_rows >> 1);
+  const int half_rows = p.grid_rows >> 1;
+  if (mode == kLoadBlock2x2Row) {
+    const int half_cols = p.grid_cols >> 1;
+    const int R = blk / half_cols;
+    *c3 = blk - R * half_cols;
+    *c4 = R + bh * half_rows;
+  } else {
+    const int C = blk / half_rows;
+    *c3 = blk - C * half_rows + bh * half_rows;
+    *c4 = C;
+  }
 }
 
-// TMA load of one 128-row tile (all d columns) starting at sequence position
-// p0, through the raster view, the column-major view or the 2x2-block view
-// (`mode`, a LoadMode).  `policy` is the L2 eviction priority of the tile's
-// lines.
+// TMA load of one 128-row Q (is_k false) or K tile (all d columns) starting
+// at sequence position p0, through the raster view, the column-major view or
+// a 2x2-block view (`mode`, a LoadMode).  `policy` is the L2 eviction
+// priority of the tile's lines.
 template <int D>
-__device__ __forceinline__ void load_tile(const FwdParams& p, const CUtensorMap* raster, const CUtensorMap* colmaj,
-                                          const CUtensorMap* blocks, int mode, uint8_t* dst, uint64_t* bar, int p0,
+__device__ __forceinline__ void load_tile(const FwdParams& p, bool is_k, int mode, uint8_t* dst, uint64_t* bar, int p0,
                                           int bh, uint64_t policy) {
   using G = Geo<D>;
   if (mode == kLoadRaster) {
+    const CUtensorMap* raster = is_k ? p.tk : p.tq;
 #pragma unroll
     for (int c = 0; c < G::kChunks; ++c)
       ptx::tma_load_3d_hint(dst + c * G::kChunkBytes, &raster[0], bar, c * 64, p0, bh, policy);
     if (G::kRem) ptx::tma_load_3d_hint(dst + G::kChunks * G::kChunkBytes, &raster[1], bar, 0, p0, bh, policy);
-  } else if (mode == kLoadBlock2x2Row) {
+  } else if (mode == kLoadBlock2x2Row || mode == kLoadBlock2x2Col) {
     // the box (d chunk, dc 2, dr 2, 32 blocks) lands in position order:
-    // row C * 4 + dr * 2 + dc of the tile
+    // row 4 * block + 2 * dr + dc of the tile
+    const CUtensorMap* blocks =
+        mode == kLoadBlock2x2Row ? (is_k ? p.bk : p.bq) : (is_k ? p.bck : p.bcq);
     int c3, c4;
-    block2x2_coords(p, p0, bh, &c3, &c4);
+    block2x2_coords(p, mode, p0, bh, &c3, &c4);
 #pragma unroll
     for (int c = 0; c < G::kChunks; ++c)
       ptx::tma_load_5d_hint(dst + c * G::kChunkBytes, &blocks[0], bar, c * 64, 0, 0, c3, c4, policy);
@@ -357,6 +369,7 @@ __device__ __forceinline__ void load_tile(const FwdParams& p, const CUtensorMap*
   } else {
     // position p = c * rows + r holds token r * cols + c; a 128-position tile is
     // one grid column c, rows r0 .. r0 + 127 (rows % 128 == 0 is required).
+    const CUtensorMap* colmaj = is_k ? p.ck : p.cq;
     const int col = p0 / p.grid_rows;
     const int r0 = p0 - col * p.grid_rows;
 #pragma unroll
@@ -377,12 +390,13 @@ __device__ __forceinline__ void load_v_tile(const FwdParams& p, int mode, uint8_
 #pragma unroll
     for (int c = 0; c < G::kVChunks; ++c)
       ptx::tma_load_3d_hint(dst + c * G::kVChunkBytes, &p.tv[0], bar, c * G::kVW, p0, bh, policy);
-  } else if (mode == kLoadBlock2x2Row) {
+  } else if (mode == kLoadBlock2x2Row || mode == kLoadBlock2x2Col) {
+    const CUtensorMap* blocks = mode == kLoadBlock2x2Row ? p.bv : p.bcv;
     int c3, c4;
-    block2x2_coords(p, p0, bh, &c3, &c4);
+    block2x2_coords(p, mode, p0, bh, &c3, &c4);
 #pragma unroll
     for (int c = 0; c < G::kVChunks; ++c)
-      ptx::tma_load_5d_hint(dst + c * G::kVChunkBytes, &p.bv[0], bar, c * G::kVW, 0, 0, c3, c4, policy);
+      ptx::tma_load_5d_hint(dst + c * G::kVChunkBytes, &blocks[0], bar, c * G::kVW, 0, 0, c3, c4, policy);
   } else {
     const int col = p0 / p.grid_rows;
     const int r0 = p0 - col * p.grid_rows;
@@ -554,14 +568,17 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
       // them in L2); a Q tile is read by this CTA alone
       const uint64_t keep = ptx::l2_policy_evict_last();
       if (is_k) {
-        const CUtensorMap* mq = load_mode == kLoadColumnMajor ? p.cq : (load_mode == kLoadBlock2x2Row ? p.bq : p.tq);
+        const CUtensorMap* mq = load_mode == kLoadColumnMajor   ? p.cq
+                                : load_mode == kLoadBlock2x2Row ? p.bq
+                                : load_mode == kLoadBlock2x2Col ? p.bcq
+                                                                : p.tq;
         ptx::prefetch_tmap(&mq[0]);
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
           const SubPlan& sp = s ? ip.sp1 : ip.sp0;
           if (!list_has(L, s, p.split) || (p.split && s == 1)) continue;  // split: one Q tile for both pipelines
           ptx::mbar_arrive_expect_tx(&bar->q_full[s], G::kTileBytes);
-          load_tile<D>(p, p.tq, p.cq, p.bq, load_mode, sq + s * G::kTileBytes, &bar->q_full[s], sp.qt * kTile, ip.bh,
+          load_tile<D>(p, false, load_mode, sq + s * G::kTileBytes, &bar->q_full[s], sp.qt * kTile, ip.bh,
                        ptx::l2_policy_evict_first());
         }
       }
@@ -579,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
         }
         ptx::mbar_arrive_expect_tx(&full[slot], G::kTileBytes);
         if (is_k)
-          load_tile<D>(p, p.tk, p.ck, p.bk, load_mode, ring + slot * G::kTileBytes, &full[slot], kt * kTile, ip.bh_kv,
+          load_tile<D>(p, true, load_mode, ring + slot * G::kTileBytes, &full[slot], kt * kTile, ip.bh_kv,
                        keep);
         else
           load_v_tile<D>(p, load_mode, ring + slot * G::kTileBytes, &full[slot], kt * kTile, ip.bh_kv, keep);

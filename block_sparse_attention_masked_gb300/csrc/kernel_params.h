@@ -13,7 +13,7 @@ constexpr int kBlockListMax = 4096;
 
 // Per-head table (device int32 [H][4]).
 enum HeadField : int { kHeadParam = 0, kHeadLoad = 1, kHeadStore = 2, kHeadPermRow = 3 };
-enum LoadMode : int { kLoadRaster = 0, kLoadColumnMajor = 1, kLoadBlock2x2Row = 2 };
+enum LoadMode : int { kLoadRaster = 0, kLoadColumnMajor = 1, kLoadBlock2x2Row = 2, kLoadBlock2x2Col = 3 };
 enum StoreMode : int {
   kStoreIdentity = 0,
   kStoreColumnMajor = 1,
@@ -67,6 +67,7 @@ struct FwdParams {
   CUtensorMap tq[2], tk[2], tv[2];  // [B*H][N][d] views
   CUtensorMap cq[2], ck[2], cv[2];  // column-major views [B*H][rows][cols][d]
   CUtensorMap bq[2], bk[2], bv[2];  // 2x2-block row-major views [B*H*rows/2][cols/2][2][2][d]
+  CUtensorMap bcq[2], bck[2], bcv[2];  // 2x2-block column-major views [cols/2][B*H*rows/2][2][2][d]
   void* o;                          // [B][H][N][d], bf16 or fp32
   float* lse;                       // [B][H][N] or null
   const int2* items;                // (b*H + h, query-tile pair), or (b*H + h, query tile) when split

@@ -72,7 +72,8 @@ struct Normalized {
   std::vector<HeadPlan> heads;
   bool need_copy;     // reorder / convert into a bf16 copy in position order
   bool any_colmajor_tma;
-  bool any_block_tma;  // some head reads the 2x2-block row-major order through 5D TMA views
+  bool any_block_tma;      // some head reads the 2x2-block row-major order through 5D TMA views
+  bool any_block_col_tma;  // some head reads the 2x2-block column-major order through 5D TMA views
   int block_c, block_nb, block_wpr, block_heads;
   int sink_tokens;    // causal window: leading positions every later query sees
   float scale;
@@ -148,8 +149,9 @@ int normalize(const mattn_mask_desc* desc, int B, int H, int N, int d, int dtype
       const bool row = order == MATTN_ORDER_BLOCK2X2_ROW;
       n.heads[h].store = row ? kStoreBlock2x2Row : kStoreBlock2x2Col;
       // a 128-position tile is 32 blocks of one block row when cols % 64 == 0
-      if (row && allow_block_tma && desc->grid_cols % 64 == 0) {
-        n.heads[h].load = kLoadBlock2x2Row;
+      // (row order), of one block column when rows % 64 == 0 (column order)
+      if (allow_block_tma && (row ? desc->grid_cols : desc->grid_rows) % 64 == 0) {
+        n.heads[h].load = row ? kLoadBlock2x2Row : kLoadBlock2x2Col;
       } else {
         n.heads[h].load = kLoadRaster;
         n.need_copy = true;
@@ -166,12 +168,14 @@ int normalize(const mattn_mask_desc* desc, int B, int H, int N, int d, int dtype
     }
   }
   n.any_block_tma = false;
+  n.any_block_col_tma = false;
   if (n.need_copy) {
     for (auto& hp : n.heads) hp.load = kLoadRaster;  // the copy is already in position order
   } else {
     for (auto& hp : n.heads) {
       n.any_colmajor_tma |= hp.load == kLoadColumnMajor;
       n.any_block_tma |= hp.load == kLoadBlock2x2Row;
+      n.any_block_col_tma |= hp.load == kLoadBlock2x2Col;
     }
   }
   if (n.kind == MATTN_BLOCK_SPARSE) {
@@ -206,6 +210,7 @@ int normalize(const mattn_mask_desc* desc, int B, int H, int N, int d, int dtype
     for (auto& hp : n.heads) hp.load = kLoadRaster;
     n.any_colmajor_tma = false;
     n.any_block_tma = false;
+    n.any_block_col_tma = false;
     n.split = true;
   }
   *out = std::move(n);
@@ -476,42 +481,54 @@ int make_v_maps(const Normalized& n, const void* base, CUtensorMap raster[2], CU
   return MATTN_OK;
 }
 
-// 2x2-block row-major views [heads * rows/2][cols/2][2][2][d] of one bf16
-// tensor, in the box order (d chunk, dc, dr, block column, block row) so that
-// a box of 32 blocks lands in sequence-position order.  K-major tiles (Q, K):
-// map [0] covers 64-column chunks (128-byte swizzle), map [1] the 16- or
-// 32-column rest; V (v_layout): map [0] with the uniform kVW-column boxes.
+// 5D views of one bf16 [heads][rows][cols][d] raster tensor in the 2x2-block
+// orders, so that a box (d chunk, dc 2, dr 2, 32 blocks, 1) lands in
+// sequence-position order.  Row-major blocks (by_cols false): dims (d, dc,
+// dr, C, R + head * rows/2); column-major blocks: (d, dc, dr, R + head *
+// rows/2, C).  K-major tiles (Q, K): map [0] covers 64-column chunks
+// (128-byte swizzle), map [1] the 16- or 32-column rest; V (v_layout): map
+// [0] with the uniform kVW-column boxes.
 int make_block_maps(const Normalized& n, const void* base, CUtensorMap maps[2], int rows, int cols, int64_t heads,
-                    bool v_layout) {
+                    bool v_layout, bool by_cols) {
   const int d = n.d;
   memset(maps, 0, 2 * sizeof(CUtensorMap));
   const cuuint64_t es = 2;
-  cuuint64_t strides[4] = {(cuuint64_t)d * es, (cuuint64_t)cols * d * es, 2 * (cuuint64_t)d * es,
-                           2 * (cuuint64_t)cols * d * es};
-  auto one = [&](CUtensorMap* m, const void* b, int width, CUtensorMapSwizzle sw) {
-    cuuint64_t dims[5] = {(cuuint64_t)width, 2, 2, (cuuint64_t)cols / 2, (cuuint64_t)(rows / 2) * heads};
-    cuuint32_t box[5] = {(cuuint32_t)(v_layout ? width : (width >= 64 ? 64 : width)), 2, 2, 32, 1};
+  const cuuint64_t s_c = 2 * (cuuint64_t)d * es, s_r = 2 * (cuuint64_t)cols * d * es;
+  const cuuint64_t n_c = (cuuint64_t)cols / 2, n_r = (cuuint64_t)(rows / 2) * heads;
+  cuuint64_t strides[4] = {(cuuint64_t)d * es, (cuuint64_t)cols * d * es, by_cols ? s_r : s_c, by_cols ? s_c : s_r};
+  auto one = [&](CUtensorMap* m, const void* b, int width, int box_w, CUtensorMapSwizzle sw) {
+    cuuint64_t dims[5] = {(cuuint64_t)width, 2, 2, by_cols ? n_r : n_c, by_cols ? n_c : n_r};
+    cuuint32_t box[5] = {(cuuint32_t)box_w, 2, 2, 32, 1};
     return encode(m, b, 5, dims, strides, box, sw);
   };
   if (v_layout) {
     const int vw = d % 64 == 0 ? 64 : (d % 32 == 0 ? 32 : 16);
     const CUtensorMapSwizzle sw =
         vw == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : (vw == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
-    cuuint64_t dims[5] = {(cuuint64_t)d, 2, 2, (cuuint64_t)cols / 2, (cuuint64_t)(rows / 2) * heads};
-    cuuint32_t box[5] = {(cuuint32_t)vw, 2, 2, 32, 1};
-    return encode(&maps[0], base, 5, dims, strides, box, sw);
+    return one(&maps[0], base, d, vw, sw);
   }
   const int chunks = d / 64, rem = d % 64;
   if (chunks) {
-    cuuint64_t dims[5] = {(cuuint64_t)d, 2, 2, (cuuint64_t)cols / 2, (cuuint64_t)(rows / 2) * heads};
-    cuuint32_t box[5] = {64, 2, 2, 32, 1};
-    int rc = encode(&maps[0], base, 5, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    int rc = one(&maps[0], base, d, 64, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc) return rc;
   }
   if (rem) {
     const char* rem_base = static_cast<const char*>(base) + (size_t)chunks * 64 * 2;
-    int rc = one(&maps[1], rem_base, rem, rem == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B);
+    int rc = one(&maps[1], rem_base, rem, rem, rem == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B);
     if (rc) return rc;
+  }
+  return MATTN_OK;
+}
+
+// The 2x2-block views that the heads' load modes need.
+int make_all_block_maps(const Normalized& n, const void* q, const void* k, const void* v, FwdParams* p, int rows,
+                        int cols, int64_t heads_q, int64_t heads_kv) {
+  int rc;
+  for (int by_cols = 0; by_cols < 2; ++by_cols) {
+    if (!(by_cols ? n.any_block_col_tma : n.any_block_tma)) continue;
+    if ((rc = make_block_maps(n, q, by_cols ? p->bcq : p->bq, rows, cols, heads_q, false, by_cols))) return rc;
+    if ((rc = make_block_maps(n, k, by_cols ? p->bck : p->bk, rows, cols, heads_kv, false, by_cols))) return rc;
+    if ((rc = make_block_maps(n, v, by_cols ? p->bcv : p->bv, rows, cols, heads_kv, true, by_cols))) return rc;
   }
   return MATTN_OK;
 }
@@ -582,12 +599,9 @@ int fwd_locked(const void* q, const void* k, const void* v, void* o, float* lse,
     if ((rc = make_maps(n, use[0], p.tq, p.cq, rows, cols, (int64_t)B * H))) return rc;
     if ((rc = make_maps(n, use[1], p.tk, p.ck, rows, cols, (int64_t)B * kv_heads))) return rc;
     if ((rc = make_v_maps(n, use[2], p.tv, p.cv, rows, cols, (int64_t)B * kv_heads))) return rc;
-    if (n.any_block_tma) {
-      const int gr = desc->grid_rows, gc = desc->grid_cols;
-      if ((rc = make_block_maps(n, use[0], p.bq, gr, gc, (int64_t)B * H, false))) return rc;
-      if ((rc = make_block_maps(n, use[1], p.bk, gr, gc, (int64_t)B * kv_heads, false))) return rc;
-      if ((rc = make_block_maps(n, use[2], p.bv, gr, gc, (int64_t)B * kv_heads, true))) return rc;
-    }
+    if ((rc = make_all_block_maps(n, use[0], use[1], use[2], &p, desc->grid_rows, desc->grid_cols, (int64_t)B * H,
+                                  (int64_t)B * kv_heads)))
+      return rc;
   }
   p.H_kv = kv_heads;
   p.kv_group = H / kv_heads;
@@ -666,11 +680,8 @@ int prepare_in_place_launch(const void* q, const void* k, const void* v, void* o
   if ((rc = make_maps(n, q, p.tq, p.cq, rows, cols, (int64_t)B * H))) return rc;
   if ((rc = make_maps(n, k, p.tk, p.ck, rows, cols, (int64_t)B * H))) return rc;
   if ((rc = make_v_maps(n, v, p.tv, p.cv, rows, cols, (int64_t)B * H))) return rc;
-  if (n.any_block_tma) {
-    if ((rc = make_block_maps(n, q, p.bq, desc->grid_rows, desc->grid_cols, (int64_t)B * H, false))) return rc;
-    if ((rc = make_block_maps(n, k, p.bk, desc->grid_rows, desc->grid_cols, (int64_t)B * H, false))) return rc;
-    if ((rc = make_block_maps(n, v, p.bv, desc->grid_rows, desc->grid_cols, (int64_t)B * H, true))) return rc;
-  }
+  if ((rc = make_all_block_maps(n, q, k, v, &p, desc->grid_rows, desc->grid_cols, (int64_t)B * H, (int64_t)B * H)))
+    return rc;
   p.H_kv = H;
   p.kv_group = 1;
   p.o = o;

@@ -88,8 +88,11 @@ typedef enum { MATTN_BF16 = 0, MATTN_F32 = 1 } mattn_dtype;
                                       /* token (2R+dr)*cols + 2C+dc (SHS slides, Factor 2,  */
                                       /* order (c); read through TMA when cols % 64 == 0)   */
 #define MATTN_ORDER_BLOCK2X2_COL (-4) /* the same blocks top to bottom then left to right:  */
-                                      /* position 4*(C*rows/2 + R) + 2*dr + dc (order (d))  */
-                                      /* Both need even grid_rows and grid_cols.            */
+                                      /* position 4*(C*rows/2 + R) + 2*dr + dc (order (d);  */
+                                      /* read through TMA when rows % 64 == 0).  Both need  */
+                                      /* even grid_rows and grid_cols; a call in which some */
+                                      /* head's order is not read through TMA reorders all  */
+                                      /* heads through a position-order copy first.         */
 /* A value k >= 0 selects explicit order k: perm[k*N + p] = token at position p. */
 
 #define MATTN_TILE 128 /* query / key tile edge of the tile plan */

@@ -106,6 +106,33 @@ def test_invalid_arguments_rejected_on_host(L):
     assert L.mattn_fwd(x, x, x, x, None, 1, 1, 16, 64, 0, ctypes.byref(single), None) == mattn.ERR_UNSUPPORTED
 
 
+@pytest.mark.parametrize("rows,cols,orders,copy", [
+    (64, 64, "rc-r", False),   # both 2x2-block orders through 5D TMA views
+    (16, 64, "r-r-", False),   # order (c): cols % 64 == 0
+    (128, 16, "c-cc", False),  # order (d): rows % 64 == 0
+    (16, 64, "rc-r", True),    # order (d) with rows % 64 != 0: all heads through the copy
+    (128, 16, "rc--", True),   # order (c) with cols % 64 != 0
+    (64, 64, "rcc-", False),
+])
+def test_block2x2_orders_pick_tma_views(L, rows, cols, orders, copy):
+    """Which 2x2-block orders are read in place through TMA views and which
+    send the call through the reorder copy, told apart on the host: the
+    no-allocation entry point refuses a call that needs the copy before it
+    checks its head capacity, so with H above that capacity the first case
+    returns UNSUPPORTED (the copy) and the second CAPACITY.  Neither touches
+    a device."""
+    H = 4097  # MATTN_NOALLOC_MAX_HEADS + 1
+    code = {"r": mattn.ORDER_BLOCK2X2_ROW, "c": mattn.ORDER_BLOCK2X2_COL, "-": mattn.ORDER_RASTER}
+    arr = (ctypes.c_int32 * H)(*[code[orders[h % len(orders)]] for h in range(H)])
+    d = _desc(2, 40, head_order=arr, grid_rows=rows, grid_cols=cols)
+    x = ctypes.c_void_p(16)
+    rc = L.mattn_fwd_noalloc(x, x, x, x, None, 1, H, rows * cols, 64, 0, ctypes.byref(d), None, None)
+    if copy:
+        assert rc == mattn.ERR_UNSUPPORTED and b"reorder" in L.mattn_last_error()
+    else:
+        assert rc == mattn.ERR_CAPACITY, L.mattn_last_error()
+
+
 def test_capacity_error_reports_count(L):
     spec = MaskSpec("full", [0])
     m = mattn.PreparedMask(spec, 1, 512, host_side=True)

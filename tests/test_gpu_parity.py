@@ -304,25 +304,32 @@ def test_host_pipeline_over_head_chunks():
 
 
 @pytest.mark.parametrize("d", [64, 80, 128])
-@pytest.mark.parametrize("rows,cols", [(16, 64), (32, 8)])
-def test_block2x2_orders(d, rows, cols):
+@pytest.mark.parametrize("rows,cols,orders", [
+    (64, 64, "rc-r"),   # both orders through 5D TMA views
+    (16, 64, "r-r-"),   # order (c) through TMA, raster heads beside it
+    (128, 16, "c-cc"),  # order (d) through TMA
+    (16, 64, "rc-r"),   # order (d) cannot: every head through the reorder copy
+    (32, 8, "rc-r"),    # neither order through TMA
+])
+def test_block2x2_orders(d, rows, cols, orders):
     """SWA-1D over the 2x2 patch blocks (SHS slides, Factor 2, orders (c) and
     (d)) next to raster heads: order (c) is read through 5D TMA views when
-    cols % 64 == 0 (else, like order (d), through the reorder copy); outputs
-    come back in token order."""
+    cols % 64 == 0, order (d) when rows % 64 == 0; otherwise every head of
+    the call goes through the reorder copy.  Outputs come back in token
+    order."""
     from workloads import block2x2_order
 
     n = rows * cols
-    H = 4
-    q, k, v = _qkv(1, H, n, d, seed=rows * 7 + d)
+    H = len(orders)
+    q, k, v = _qkv(1, H, n, d, seed=rows * 7 + cols + d)
     row, col = block2x2_order(rows, cols), block2x2_order(rows, cols, by_columns=True)
-    perm = [row, col, None, row]
-    grid = [(rows, cols, "block2x2_row"), (rows, cols, "block2x2_col"), None, (rows, cols, "block2x2_row")]
+    perm = [{"r": row, "c": col, "-": None}[o] for o in orders]
+    grid = [{"r": (rows, cols, "block2x2_row"), "c": (rows, cols, "block2x2_col"), "-": None}[o] for o in orders]
     for spec in (MaskSpec("sliding", [40] * H, perm=perm, perm_grid=grid),
                  MaskSpec("chunk", [128] * H, perm=perm, perm_grid=grid),
                  MaskSpec("causal_window", [200, 64, 300, 1000], perm=perm, perm_grid=grid,
                           sink=np.array([0.5, -0.5, 0.0, 1.0]))):
-        check(q, k, v, spec, tag=f"block2x2 {spec.kind} {rows}x{cols} d{d}")
+        check(q, k, v, spec, tag=f"block2x2 {spec.kind} {rows}x{cols} {orders} d{d}")
 
 
 def test_block2x2_orders_other_paths():
