@@ -168,11 +168,12 @@ __global__ void __launch_bounds__(DecGeo<D, GP>::kThreads, 1) decode_split_kerne
 
   float m = -INFINITY;  // consumers: running max of head gl (same on every lane of gl)
   float l = 0.f;        // consumers: this lane's share of head gl's running sum
-  float o[GP][VPL];
+  // O of every head, this lane's dims as pairs (packed f32x2 arithmetic)
+  float2 o[GP][VPL / 2];
 #pragma unroll
   for (int g = 0; g < GP; ++g)
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) o[g][i] = 0.f;
+    for (int i = 0; i < VPL / 2; ++i) o[g][i] = make_float2(0.f, 0.f);
   const int gl = lane % GP, kl = lane / GP;
 
   if (warp == kDecConsumers) {
@@ -212,7 +213,8 @@ __global__ void __launch_bounds__(DecGeo<D, GP>::kThreads, 1) decode_split_kerne
   } else if (warp < Geo::kCons) {
     // ------------------------------------------------------------ consumers
     // queries of the group, scaled into the log2 domain, this lane's dims
-    float q[GP][VPL];
+    // as pairs
+    float2 q[GP][VPL / 2];
 #pragma unroll
     for (int g = 0; g < GP; ++g) {
       if (g < G) {
@@ -221,12 +223,11 @@ __global__ void __launch_bounds__(DecGeo<D, GP>::kThreads, 1) decode_split_kerne
 #pragma unroll
         for (int i = 0; i < VPL / 2; ++i) {
           const uint32_t w = __ldg(src + i);
-          q[g][2 * i] = bf_lo(w) * p.scale_log2;
-          q[g][2 * i + 1] = bf_hi(w) * p.scale_log2;
+          q[g][i] = make_float2(bf_lo(w) * p.scale_log2, bf_hi(w) * p.scale_log2);
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < VPL; ++i) q[g][i] = 0.f;
+        for (int i = 0; i < VPL / 2; ++i) q[g][i] = make_float2(0.f, 0.f);
       }
     }
     const int wlo = gl < G ? window_lo(p, p.head_info[(kvh * G + gl) * 4 + kHeadParam], qpos) : len;
@@ -260,15 +261,15 @@ __global__ void __launch_bounds__(DecGeo<D, GP>::kThreads, 1) decode_split_kerne
         for (int kk = 0; kk < KPG; ++kk) {
           uint32_t kw[VPL / 2];
           load_row_s<VPL>(sk + (gi * KPG + kk) * Geo::kRow, kw);
+          float2 kf[VPL / 2];
+#pragma unroll
+          for (int w = 0; w < VPL / 2; ++w) kf[w] = make_float2(bf_lo(kw[w]), bf_hi(kw[w]));
 #pragma unroll
           for (int g = 0; g < GP; ++g) {
-            float acc = 0.f;
+            float2 acc = ptx::fmul2(q[g][0], kf[0]);
 #pragma unroll
-            for (int w = 0; w < VPL / 2; ++w) {
-              acc = fmaf(q[g][2 * w], bf_lo(kw[w]), acc);
-              acc = fmaf(q[g][2 * w + 1], bf_hi(kw[w]), acc);
-            }
-            part[kk * GP + g] = acc;
+            for (int w = 1; w < VPL / 2; ++w) acc = ptx::ffma2(q[g][w], kf[w], acc);
+            part[kk * GP + g] = acc.x + acc.y;
           }
         }
         // reduce-scatter over the lanes: lane j ends with the sum of pair j
@@ -303,25 +304,24 @@ __global__ void __launch_bounds__(DecGeo<D, GP>::kThreads, 1) decode_split_kerne
 #pragma unroll
         for (int g = 0; g < GP; ++g) {
           const float a = __shfl_sync(0xffffffffu, alpha, g);
+          const float2 a2 = make_float2(a, a);
 #pragma unroll
-          for (int i = 0; i < VPL; ++i) o[g][i] *= a;
+          for (int i = 0; i < VPL / 2; ++i) o[g][i] = ptx::fmul2(o[g][i], a2);
         }
 #pragma unroll
         for (int kk = 0; kk < KPG; ++kk) {
           if (i0 + kk >= i_end) break;  // warp-uniform: rows past the chunk hold stale data
           uint32_t vw[VPL / 2];
           load_row_s<VPL>(sv + (gi * KPG + kk) * Geo::kRow, vw);
-          float vf[VPL];
+          float2 vf[VPL / 2];
 #pragma unroll
-          for (int w = 0; w < VPL / 2; ++w) {
-            vf[2 * w] = bf_lo(vw[w]);
-            vf[2 * w + 1] = bf_hi(vw[w]);
-          }
+          for (int w = 0; w < VPL / 2; ++w) vf[w] = make_float2(bf_lo(vw[w]), bf_hi(vw[w]));
 #pragma unroll
           for (int g = 0; g < GP; ++g) {
             const float pg = wpw[kk * GP + g];
+            const float2 pg2 = make_float2(pg, pg);
 #pragma unroll
-            for (int t = 0; t < VPL; ++t) o[g][t] = fmaf(pg, vf[t], o[g][t]);
+            for (int t = 0; t < VPL / 2; ++t) o[g][t] = ptx::ffma2(pg2, vf[t], o[g][t]);
           }
         }
         __syncwarp();
@@ -342,7 +342,10 @@ __global__ void __launch_bounds__(DecGeo<D, GP>::kThreads, 1) decode_split_kerne
 #pragma unroll
     for (int g = 0; g < GP; ++g)
 #pragma unroll
-      for (int i = 0; i < VPL; ++i) wo[((warp * GP) + g) * D + lane * VPL + i] = o[g][i];
+      for (int i = 0; i < VPL / 2; ++i) {
+        wo[((warp * GP) + g) * D + lane * VPL + 2 * i] = o[g][i].x;
+        wo[((warp * GP) + g) * D + lane * VPL + 2 * i + 1] = o[g][i].y;
+      }
   }
   __syncthreads();
   if (*abort_flag) return;
