@@ -911,8 +911,12 @@ int mattn_decode(const void* q, const void* k, const void* v, void* o, float* ls
   MATTN_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
   MATTN_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "SM count");
   // chunks of the keys a key/value head's query heads may see (every
-  // cached key, or at most the widest window plus the sink tokens): one
-  // CTA per SM over the launch, 64-key multiples, at most kDecodeMaxSplits
+  // cached key, or at most the widest window plus the sink tokens), in
+  // 64-key multiples, at most kDecodeMaxSplits per group.  A CTA holds its
+  // SM (its ring fills the shared memory), so the launch runs in waves of
+  // `sms` CTAs: the number of chunks per group is the one of up to four
+  // waves that fills them best, each extra wave charged 2% for its CTAs'
+  // start-up (the first copies' latency before the stream flows).
   int64_t nvis = L;
   if (desc->kind == MATTN_CAUSAL_WINDOW) {
     int64_t wmax = 1;
@@ -920,8 +924,18 @@ int mattn_decode(const void* q, const void* k, const void* v, void* o, float* ls
     nvis = std::min<int64_t>(L, wmax + desc->sink_tokens);
   }
   const int64_t groups = (int64_t)B * H_kv;
-  int64_t want = ((int64_t)sms + groups - 1) / groups;
-  if (want < 1) want = 1;
+  int64_t want = 1;
+  double best = -1.0;
+  for (int64_t waves = 1; waves <= 4; ++waves) {
+    const int64_t ns = std::max<int64_t>(1, waves * sms / groups);
+    const int64_t ctas = groups * ns;
+    const int64_t used = (ctas + sms - 1) / sms;
+    const double fill = (double)ctas / (double)(used * sms) - 0.02 * (double)(used - 1);
+    if (fill > best + 1e-9) {
+      best = fill;
+      want = ns;
+    }
+  }
   int64_t chunk = ((nvis + want - 1) / want + 63) / 64 * 64;
   const int64_t min_chunk = ((nvis + kDecodeMaxSplits - 1) / kDecodeMaxSplits + 63) / 64 * 64;
   chunk = std::max<int64_t>(std::max<int64_t>(chunk, 64), min_chunk);
