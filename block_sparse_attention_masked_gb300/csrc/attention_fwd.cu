@@ -91,6 +91,8 @@ struct Barriers {
   uint32_t tmem_base;
   int abort_flag;
   uint32_t mma_turn;    // ticket of the MMA group that may be issued next
+  int head_store, head_perm_row;  // the head's store mode and explicit-order row, for the epilogue
+  float sink_log2;                // the head's sink logit in the log2 domain (-inf: none)
   int list_n[3];        // block kind: entries of the CTA's key-tile list, and per sub-tile
   TileList tl;          // the CTA's key-tile list (read by every role from shared memory)
   float xch[2][3][kTile];  // split schedule: per sub-tile (m, l, tile count) of each row
@@ -145,13 +147,12 @@ __device__ __forceinline__ SubPlan make_subplan(const FwdParams& p, int2 it, int
   return sp;
 }
 
-__device__ __forceinline__ ItemPlan make_plan(const FwdParams& p, int2 it) {
+__device__ __forceinline__ ItemPlan make_plan(const FwdParams& p, int2 it, int param) {
   ItemPlan ip;
   ip.bh = it.x;
   ip.h = it.x % p.H;
   ip.b = it.x / p.H;
   ip.bh_kv = ip.b * p.H_kv + ip.h / p.kv_group;
-  const int param = p.head_info[ip.h * 4 + kHeadParam];
   ip.sp0 = make_subplan(p, it, 0, param);
   ip.sp1 = make_subplan(p, it, 1, param);
   return ip;
@@ -495,6 +496,27 @@ __device__ __forceinline__ int64_t token_of(const FwdParams& p, int store_mode, 
                   store_mode == kStoreExplicit ? p.perm + (int64_t)perm_row * p.N : nullptr, pos);
 }
 
+// The CTA's Q tiles: one per sub-tile that has key tiles (split: the one
+// query tile both pipelines share).  Issued by the K producer thread.
+template <int D>
+__device__ __forceinline__ void issue_q_loads(const FwdParams& p, const ItemPlan& ip, const TileList& L, int load_mode,
+                                              uint8_t* sq, Barriers* bar) {
+  using G = Geo<D>;
+  const CUtensorMap* mq = load_mode == kLoadColumnMajor   ? p.cq
+                          : load_mode == kLoadBlock2x2Row ? p.bq
+                          : load_mode == kLoadBlock2x2Col ? p.bcq
+                                                          : p.tq;
+  ptx::prefetch_tmap(&mq[0]);
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    const SubPlan& sp = s ? ip.sp1 : ip.sp0;
+    if (!list_has(L, s, p.split) || (p.split && s == 1)) continue;  // split: one Q tile for both pipelines
+    ptx::mbar_arrive_expect_tx(&bar->q_full[s], G::kTileBytes);
+    load_tile<D>(p, false, load_mode, sq + s * G::kTileBytes, &bar->q_full[s], sp.qt * kTile, ip.bh,
+                 ptx::l2_policy_evict_first());
+  }
+}
+
 template <int D, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid_constant__ FwdParams p) {
   using G = Geo<D>;
@@ -512,8 +534,18 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int2 item = p.items[blockIdx.x];
-  const ItemPlan ip = make_plan(p, item);
+  // the head's row of the per-head table (param, load, store, perm_row) in
+  // one load
+  const int4 head_row = __ldg(reinterpret_cast<const int4*>(p.head_info) + item.x % p.H);
+  const ItemPlan ip = make_plan(p, item, head_row.x);
+  const int load_mode = head_row.y;
   if (p.kind == kBlockSparse && warp == 2) build_block_list(p, item, ip, list_e, bar->list_n, lane);
+  // Q tiles and the first ring's K tiles requested before the set-up below
+  // (interval kinds, whose key-tile list needs no shared state), so that
+  // their DRAM latency overlaps it; the K producer continues from k_early
+  int k_early = 0;
+  bool q_early = false;
+  if (threadIdx.x == 96) bar->sink_log2 = p.sink ? __ldg(p.sink + item.x % p.H) * kLog2e : -INFINITY;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
@@ -535,7 +567,22 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
     ptx::mbar_init(&bar->drain[1], 1);
     bar->abort_flag = 0;
     bar->mma_turn = 0;
+    bar->head_store = head_row.z;
+    bar->head_perm_row = head_row.w;
     ptx::fence_barrier_init();
+    if (p.kind != kBlockSparse) {
+      ptx::fence_proxy_async_shared();
+      const TileList L0 = make_list(p, ip, nullptr, nullptr);
+      issue_q_loads<D>(p, ip, L0, load_mode, sq, bar);
+      q_early = true;
+      k_early = L0.n < KS ? L0.n : KS;
+      const uint64_t keep = ptx::l2_policy_evict_last();
+      for (int j = 0; j < k_early; ++j) {  // fresh ring slots: nothing to wait for
+        ptx::mbar_arrive_expect_tx(&bar->k_full[j], G::kTileBytes);
+        load_tile<D>(p, true, load_mode, sk + j * G::kTileBytes, &bar->k_full[j], list_kt(L0, j) * kTile,
+                     ip.bh_kv, keep);
+      }
+    }
   }
   if (warp == 1) {
     ptx::tmem_alloc(&bar->tmem_base, 512);
@@ -549,7 +596,6 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
   if (threadIdx.x == 0) bar->tl = make_list(p, ip, list_e, bar->list_n);
   __syncthreads();
   const TileList& L = bar->tl;
-  const int load_mode = p.head_info[ip.h * 4 + kHeadLoad];
 
   // Registers: 384 threads launched at 168 each; the producer / MMA
   // warpgroup gives up to kRegsControl so that each softmax warpgroup can hold
@@ -567,27 +613,13 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
       // K and V tiles are re-read by the other query tiles of the head (keep
       // them in L2); a Q tile is read by this CTA alone
       const uint64_t keep = ptx::l2_policy_evict_last();
-      if (is_k) {
-        const CUtensorMap* mq = load_mode == kLoadColumnMajor   ? p.cq
-                                : load_mode == kLoadBlock2x2Row ? p.bq
-                                : load_mode == kLoadBlock2x2Col ? p.bcq
-                                                                : p.tq;
-        ptx::prefetch_tmap(&mq[0]);
-#pragma unroll
-        for (int s = 0; s < 2; ++s) {
-          const SubPlan& sp = s ? ip.sp1 : ip.sp0;
-          if (!list_has(L, s, p.split) || (p.split && s == 1)) continue;  // split: one Q tile for both pipelines
-          ptx::mbar_arrive_expect_tx(&bar->q_full[s], G::kTileBytes);
-          load_tile<D>(p, false, load_mode, sq + s * G::kTileBytes, &bar->q_full[s], sp.qt * kTile, ip.bh,
-                       ptx::l2_policy_evict_first());
-        }
-      }
+      if (is_k && !q_early) issue_q_loads<D>(p, ip, L, load_mode, sq, bar);
       uint64_t* empty = is_k ? bar->k_empty : bar->v_empty;
       uint64_t* full = is_k ? bar->k_full : bar->v_full;
       uint8_t* ring = is_k ? sk : sv;
       constexpr int S = KS;
       static_assert(KS == VS, "one ring depth for K and V");
-      for (int j = 0; j < L.n; ++j) {
+      for (int j = is_k ? k_early : 0; j < L.n; ++j) {
         const int kt = list_kt(L, j);
         const int slot = j % S;
         if (!ptx::mbar_wait(&empty[slot], ((j / S) & 1) ^ 1, p.timeout_ns, abort_flag)) {
@@ -744,7 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
     const SubPlan sp = s ? ip.sp1 : ip.sp0;
     const int64_t pos = (int64_t)sp.qt * kTile + row;
     const int h = ip.h;
-    const int param = p.head_info[h * 4 + kHeadParam];
+    const int param = head_row.x;
     int64_t lo, hi;
     row_interval(p.kind, param, p.N, pos, &lo, &hi);
     if (hi > p.N - 1) hi = p.N - 1;
@@ -864,7 +896,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
         ok = have_oo;
       }
       if (ok) {
-        const float b2 = p.sink ? p.sink[h] * kLog2e : -INFINITY;
+        const float b2 = bar->sink_log2;
         const float M = fmaxf(fmaxf(m, m_o), b2);
         float o_scale = 0.f, oo_scale = 0.f;
         float lse_v = -INFINITY;
@@ -881,8 +913,8 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
           }
         }
         const bool valid = pos < p.N;
-        const int store_mode = p.head_info[h * 4 + kHeadStore];
-        const int perm_row = p.head_info[h * 4 + kHeadPermRow];
+        const int store_mode = bar->head_store;
+        const int perm_row = bar->head_perm_row;
         const int64_t tok = valid ? token_of(p, store_mode, perm_row, pos) : 0;
         const int64_t orow = ((int64_t)ip.bh * p.N + tok) * D;
         // columns written: all (paired); this sub-tile's half (split)
