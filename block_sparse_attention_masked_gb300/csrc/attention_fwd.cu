@@ -775,7 +775,6 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
     const uint32_t o_tmem = tmem + lane_off + 256 + s * 128;
     const SubPlan sp = s ? ip.sp1 : ip.sp0;
     const int64_t pos = (int64_t)sp.qt * kTile + row;
-    const int h = ip.h;
     const int param = head_row.x;
     int64_t lo, hi;
     row_interval(p.kind, param, p.N, pos, &lo, &hi);
