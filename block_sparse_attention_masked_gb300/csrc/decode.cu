@@ -15,7 +15,7 @@
 //     of those heads.  Its producer warp streams the chunk's K and V rows
 //     into a ring of shared-memory slots with bulk async copies (keys of a
 //     cache are contiguous rows, so a slot is one or two copies per tensor),
-//     keeping ~128 KB in flight per SM; a slot holds 32 keys, in groups of
+//     keeping up to 192 KB in flight per SM; a slot holds 32 keys, in groups of
 //     KPG = 32 / GP keys, and each (slot, group) pair of the ring has one
 //     owner among up to twelve consumer warps.  In a group: lane l holds dims
 //     [l*VPL, (l+1)*VPL) of every query (VPL = D / 32) and of each row, forms
@@ -47,7 +47,7 @@ namespace {
 
 constexpr float kLog2eD = 1.4426950408889634f;
 constexpr float kLn2D = 0.6931471805599453f;
-constexpr int kDecRingBytes = 144 * 1024;
+constexpr int kDecRingBytes = 192 * 1024;  // at d = 256: six 32-key slots, groups for twelve warps
 
 __device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
