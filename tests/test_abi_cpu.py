@@ -70,6 +70,11 @@ def test_invalid_arguments_rejected_on_host(L):
     assert L.mattn_count_pairs(ctypes.byref(_desc(2, 3)), 1, 0, 16, ctypes.byref(out)) == mattn.ERR_INVALID_ARG
     assert L.mattn_count_pairs(ctypes.byref(_desc(4, 64)), 1, 1, 256, ctypes.byref(out)) == mattn.ERR_UNSUPPORTED
     assert L.mattn_count_pairs(ctypes.byref(_desc(4, 128)), 1, 1, 256, ctypes.byref(out)) == mattn.ERR_INVALID_ARG
+    # block-sparse N is capped by the per-CTA key-tile list (4096 tiles of 128)
+    bits = np.zeros(4097 * 65, dtype=np.uint64)
+    big = _desc(4, 128, block_bits=bits.ctypes.data, block_heads=1)
+    assert L.mattn_count_pairs(ctypes.byref(big), 1, 1, 128 * 4096 + 1, ctypes.byref(out)) == mattn.ERR_UNSUPPORTED
+    assert b"524288" in L.mattn_last_error()
     bad_scale = _desc(0, 0, softmax_scale=-1.0)
     assert L.mattn_count_pairs(ctypes.byref(bad_scale), 1, 1, 16, ctypes.byref(out)) == mattn.ERR_INVALID_ARG
     for ok_flags in (mattn.FLAG_SCHEDULE_PAIRED, mattn.FLAG_SCHEDULE_SPLIT, mattn.FLAG_SCHEDULE_SINGLE):

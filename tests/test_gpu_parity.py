@@ -332,6 +332,20 @@ def test_block2x2_orders(d, rows, cols, orders):
         check(q, k, v, spec, tag=f"block2x2 {spec.kind} {rows}x{cols} {orders} d{d}")
 
 
+def test_block_sparse_at_the_list_capacity():
+    """The largest block-sparse N, 128 * 4096 = 524288 tokens: with every
+    causal block kept, the last query tile's key-tile list holds 4096
+    entries, the per-CTA capacity.  Sampled rows (the first and last, tile
+    edges, random) against the oracle."""
+    n, d = 128 * 4096, 64
+    q, k, v = _qkv(1, 1, n, d, seed=77)
+    nb = n // 128
+    spec = MaskSpec("block", [128], block=np.tril(np.ones((nb, nb), dtype=bool))[None])
+    rng = np.random.default_rng(5)
+    rows = np.unique(np.concatenate([[0, 127, 128, n - 129, n - 128, n - 1], rng.integers(0, n, 40)]))
+    check(q, k, v, spec, rows=rows, tag="block list capacity")
+
+
 def test_block2x2_orders_other_paths():
     """Order (c) on the paths that read positions through the copy: fp32
     inputs, the single-pipeline schedule, received attention."""
