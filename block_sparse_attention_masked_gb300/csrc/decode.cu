@@ -120,6 +120,8 @@ __global__ void __launch_bounds__(DecGeo<D, GP>::kThreads, 1) decode_split_kerne
   float* wo = reinterpret_cast<float*>(ring);                        // [kDecConsumers][GP][D], after the loop
   volatile int* abort_flag = &bar->abort_flag;
 
+  // the combine grid may be scheduled now; it waits for this grid to finish
+  asm volatile("griddepcontrol.launch_dependents;");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = blockIdx.x;
   const int bkv = blockIdx.y;
@@ -381,6 +383,9 @@ template <int D>
 __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeParams p) {
   __shared__ float es[kDecodeMaxSplits];
   __shared__ float red[D / 32];
+  // launched as a programmatic dependent of the split grid: its chunk
+  // states are complete and visible past this point
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t bh = blockIdx.x;
   const int h = (int)(bh % p.H);
   const int c = threadIdx.x, warp = c >> 5, lane = c & 31;
@@ -449,8 +454,21 @@ cudaError_t launch_d(const DecodeParams& p, int gp, cudaStream_t stream) {
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
-  decode_combine_kernel<D><<<p.B * p.H, D, 0, stream>>>(p);
-  return cudaGetLastError();
+  // Programmatic dependent launch: the combine grid is scheduled while the
+  // split grid still runs (each split CTA allows it at its start) and waits
+  // in griddepcontrol.wait until the split grid has completed and its
+  // writes are visible, so the second launch's latency is hidden.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.B * p.H);
+  cfg.blockDim = dim3(D);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, p);
 }
 
 }  // namespace
