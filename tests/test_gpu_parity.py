@@ -1,6 +1,6 @@
 """GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
 
-Tolerances (spec contract for bf16 inputs with fp32 accumulation):
+Tolerances (for bf16 inputs with fp32 accumulation):
 max |O_gpu - O_oracle| <= 2e-2 and ||O_gpu - O_oracle||_2 / ||O_oracle||_2
 <= 5e-3 over all compared elements; |LSE_gpu - LSE_oracle| <= 1e-3 (the
 pages state no LSE tolerance; with bf16 inputs both sides see the same
