@@ -303,6 +303,29 @@ def test_host_pipeline_over_head_chunks():
         assert torch.equal(lse, lsed.cpu()), spec.kind
 
 
+def test_host_pipeline_with_grid_orders():
+    """mattn_fwd_host over head chunks with per-head grid orders (raster,
+    both 2x2-block orders, the column-major grid transpose): chunks whose
+    heads all read through tensor maps run in place, the others through the
+    reorder copy; every chunk's result equals the device entry point's."""
+    from workloads import block2x2_order
+
+    B, H, side, d = 1, 7, 64, 64
+    N = side * side
+    q, k, v = make_qkv(B, H, N, d, "bf16", 1.0, 23, device="cpu")
+    row, col = block2x2_order(side, side), block2x2_order(side, side, by_columns=True)
+    code = {"-": (None, None), "r": (row, (side, side, "block2x2_row")), "c": (col, (side, side, "block2x2_col")),
+            "t": (column_major_order(side, side), (side, side))}
+    orders = "-rc-trc"
+    spec = MaskSpec("sliding", [40, 90, 150, 64, 33, 200, 1],
+                    perm=[code[o][0] for o in orders], perm_grid=[code[o][1] for o in orders])
+    o, lse = mattn.attention_host(q.pin_memory(), k.pin_memory(), v.pin_memory(), spec)
+    od, lsed = mattn.attention(q.cuda(), k.cuda(), v.cuda(), mattn.prepare(spec, H, N))
+    torch.cuda.synchronize()
+    assert torch.equal(o, od.cpu())
+    assert torch.equal(lse, lsed.cpu())
+
+
 @pytest.mark.parametrize("d", [64, 80, 128])
 @pytest.mark.parametrize("rows,cols,orders", [
     (64, 64, "rc-r"),   # both orders through 5D TMA views

@@ -77,13 +77,23 @@ def test_noalloc_matches_mattn_fwd_on_consecutive_calls(L):
     grid = [None, None, (128, 16), (128, 16), None, None]
     spec_b = MaskSpec("sliding", [100, 37, 100, 256, 5, 1000], perm_grid=grid,
                       sink=np.linspace(-1.0, 1.0, hb))
-    cases = {"A": (qa, ka, va, mattn.prepare(spec_a, ha, na)), "B": (qb, kb, vb, mattn.prepare(spec_b, hb, nb_))}
+    # call C: the two 2x2-block orders over a 64 x 64 grid, both read in
+    # place through 5D tensor maps
+    from workloads import block2x2_order
+
+    nc, hc, dc = 64 * 64, 2, 64
+    qc, kc, vc = make_qkv(1, hc, nc, dc, "bf16", 1.0, seed=13, device="cuda")
+    spec_c = MaskSpec("sliding", [90, 300],
+                      perm=[block2x2_order(64, 64), block2x2_order(64, 64, by_columns=True)],
+                      perm_grid=[(64, 64, "block2x2_row"), (64, 64, "block2x2_col")])
+    cases = {"A": (qa, ka, va, mattn.prepare(spec_a, ha, na)), "B": (qb, kb, vb, mattn.prepare(spec_b, hb, nb_)),
+             "C": (qc, kc, vc, mattn.prepare(spec_c, hc, nc))}
     refs = {}
     for name, (q, k, v, mask) in cases.items():
         refs[name] = mattn.attention(q, k, v, mask)
     torch.cuda.synchronize()
     assert mattn.device_status()[0] == 0
-    for i, name in enumerate(["A", "B", "A", "B"]):
+    for i, name in enumerate(["A", "B", "C", "A", "B", "C"]):
         q, k, v, mask = cases[name]
         o = torch.full_like(q, float("nan"))
         lse = torch.full(q.shape[:3], float("nan"), dtype=torch.float32, device=q.device)
