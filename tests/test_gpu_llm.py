@@ -63,7 +63,9 @@ def check_gqa(q, k, v, spec, rows=None, groups=None, tag=""):
         sub = MaskSpec(spec.kind, [spec.head_param[h] for h in hs],
                        sink=None if spec.sink is None else np.asarray(spec.sink)[hs],
                        block=None if spec.block is None else np.asarray(spec.block)[hs],
-                       sink_tokens=spec.sink_tokens)
+                       sink_tokens=spec.sink_tokens,
+                       perm=None if spec.perm is None else [spec.perm[h] for h in hs],
+                       perm_grid=None if spec.perm_grid is None else [spec.perm_grid[h] for h in hs])
         qs = _host(q[:, g * G:(g + 1) * G])
         ks, vs = _host(k[:, g:g + 1]), _host(v[:, g:g + 1])
         ref_o, ref_lse = dense.attention(qs, ks, vs, sub, rows=rows_arr)
@@ -140,6 +142,23 @@ def test_gqa_fp32_inputs_and_column_major():
     assert np.abs(got - ref_o).max() <= MAX_ABS
     assert np.linalg.norm(got - ref_o) / np.linalg.norm(ref_o) <= REL_L2
     assert np.abs(np.stack([_host(lse[0, h]) for h in range(H)]) - ref_lse).max() <= LSE_ABS
+
+
+def test_gqa_with_2x2_block_orders():
+    """Query heads sharing key/value heads, each query head with its own
+    grid order (both 2x2-block orders and raster over a 64 x 64 grid, read
+    in place through 5D tensor maps): a work item reads its K/V head's rows
+    in its query head's order."""
+    from workloads import block2x2_order
+
+    side, H, Hkv = 64, 4, 2
+    n = side * side
+    q, k, v = make_qkv(1, H, n, 128, "bf16", 1.0, seed=9, device="cuda", kv_heads=Hkv)
+    row, col = block2x2_order(side, side), block2x2_order(side, side, by_columns=True)
+    spec = MaskSpec("sliding", [70, 70, 200, 33], perm=[row, col, None, row],
+                    perm_grid=[(side, side, "block2x2_row"), (side, side, "block2x2_col"), None,
+                               (side, side, "block2x2_row")])
+    check_gqa(q, k, v, spec, tag="gqa 2x2-block orders")
 
 
 def test_device_tile_walk_with_sink_tokens():
