@@ -572,6 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
     ptx::fence_barrier_init();
     if (p.kind != kBlockSparse) {
       ptx::fence_proxy_async_shared();
+      if (p.after_prepass) asm volatile("griddepcontrol.wait;" ::: "memory");
       const TileList L0 = make_list(p, ip, nullptr, nullptr);
       issue_q_loads<D>(p, ip, L0, load_mode, sq, bar);
       q_early = true;
@@ -610,6 +611,8 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
     ptx::setmaxnreg_dec<kRegsControl>();
     if (lane == 0) {
       const bool is_k = warp == 0;
+      // the pre-pass's copies, which the loads below read, are complete
+      if (p.after_prepass) asm volatile("griddepcontrol.wait;" ::: "memory");
       // K and V tiles are re-read by the other query tiles of the head (keep
       // them in L2); a Q tile is read by this CTA alone
       const uint64_t keep = ptx::l2_policy_evict_last();
@@ -1009,6 +1012,8 @@ __global__ void plan_dump_kernel(const PlanDumpParams p) {
 // rows of query head h are read from K / V head h / kv_group, so that the
 // copies have one head per query head.
 __global__ void gather_kernel(const GatherParams p) {
+  // the attention grid that reads these copies may be scheduled now
+  asm volatile("griddepcontrol.launch_dependents;");
   const int t = blockIdx.y;
   const int64_t vec_per_row = p.d / 8;
   const int64_t total = (int64_t)p.B * p.H * p.N * vec_per_row;
@@ -1058,8 +1063,24 @@ cudaError_t launch_one(const FwdParams& p, cudaStream_t stream) {
   auto kern = attention_fwd_kernel<D, F32>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<p.n_items, kThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  if (!p.after_prepass) {
+    kern<<<p.n_items, kThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+  }
+  // After the reorder pre-pass: a programmatic dependent launch, so that the
+  // CTAs are resident and set up when the copies are done (the threads that
+  // issue loads wait in griddepcontrol.wait for them).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.n_items);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 template <int D>

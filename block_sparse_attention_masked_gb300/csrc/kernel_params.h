@@ -92,6 +92,8 @@ struct FwdParams {
                                     //    alternately to two sub-tile pipelines
                                     //    (head dim 256: one query tile per CTA, one pipeline)
   int out_f32;                      // head dim 256 kernel: O in fp32 (else bf16)
+  int after_prepass;                // 1: launched as a programmatic dependent of the reorder
+                                    // pre-pass, whose copies its loads read
 };
 
 struct PlanDumpParams {

@@ -608,6 +608,7 @@ int fwd_locked(const void* q, const void* k, const void* v, void* o, float* lse,
   p.o = o;
   p.lse = lse;
   p.items = plan->items;
+  p.after_prepass = (n.need_copy && !n.single) ? 1 : 0;
   p.n_items = (int)plan->items_host.size();
   p.head_info = plan->head_info;
   p.perm = desc->perm;
