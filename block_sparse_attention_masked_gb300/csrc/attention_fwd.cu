@@ -431,8 +431,8 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
 // P = exp2(x * sl2 - mref) for the 128 scores of this thread's row, stored
 // to tensor memory at p_tmem as bf16 pairs (64 columns, round to nearest);
 // returns the row sum of the fp32 values.  All exponentials use MUFU ex2:
-// moving a share to the FMA-pipe polynomial ptx::exp2_poly2 measured slower
-// at every share tried, as did a truncating pack with a second sum over the
+// moving a share of them to an FMA-pipe polynomial measured slower at every
+// share tried, as did a truncating pack with a second sum over the
 // truncated values (one more add and two integer ops per pair).
 __device__ __forceinline__ float exp_to_tmem(const float (&x)[128], float sl2, float mref, uint32_t p_tmem) {
   const float2 sl2v = make_float2(sl2, sl2);
@@ -548,6 +548,10 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
   if (threadIdx.x == 96) bar->sink_log2 = p.sink ? __ldg(p.sink + item.x % p.H) * kLog2e : -INFINITY;
 
   if (threadIdx.x == 0) {
+    // After the reorder pre-pass: the CTA's bounded waits below must not run
+    // while the pre-pass is still copying, so every thread is held at the
+    // first CTA barrier until its copies are complete.
+    if (p.after_prepass) asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(&bar->q_full[s], 1);
       ptx::mbar_init(&bar->s_full[s], 1);
@@ -572,7 +576,6 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
     ptx::fence_barrier_init();
     if (p.kind != kBlockSparse) {
       ptx::fence_proxy_async_shared();
-      if (p.after_prepass) asm volatile("griddepcontrol.wait;" ::: "memory");
       const TileList L0 = make_list(p, ip, nullptr, nullptr);
       issue_q_loads<D>(p, ip, L0, load_mode, sq, bar);
       q_early = true;
@@ -611,8 +614,6 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
     ptx::setmaxnreg_dec<kRegsControl>();
     if (lane == 0) {
       const bool is_k = warp == 0;
-      // the pre-pass's copies, which the loads below read, are complete
-      if (p.after_prepass) asm volatile("griddepcontrol.wait;" ::: "memory");
       // K and V tiles are re-read by the other query tiles of the head (keep
       // them in L2); a Q tile is read by this CTA alone
       const uint64_t keep = ptx::l2_policy_evict_last();
@@ -1046,17 +1047,6 @@ __global__ void gather_kernel(const GatherParams p) {
   *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dst[t]) + row * p.d + c8) = out;
 }
 
-// Test hook: the softmax's polynomial exp2 next to CUDA's exp2f.
-__global__ void exp2_check_kernel(const float* x, float* y_poly, float* y_ref, int n) {
-  const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
-  if (i + 1 >= n) return;
-  const float2 r = ptx::exp2_poly2(make_float2(x[i], x[i + 1]));
-  y_poly[i] = r.x;
-  y_poly[i + 1] = r.y;
-  y_ref[i] = exp2f(x[i]);
-  y_ref[i + 1] = exp2f(x[i + 1]);
-}
-
 template <int D, bool F32>
 cudaError_t launch_one(const FwdParams& p, cudaStream_t stream) {
   const size_t smem = attention_smem_bytes(D);
@@ -1068,8 +1058,8 @@ cudaError_t launch_one(const FwdParams& p, cudaStream_t stream) {
     return cudaGetLastError();
   }
   // After the reorder pre-pass: a programmatic dependent launch, so that the
-  // CTAs are resident and set up when the copies are done (the threads that
-  // issue loads wait in griddepcontrol.wait for them).
+  // CTAs are resident when the copies are done (thread 0 waits in
+  // griddepcontrol.wait for them before the CTA's first barrier).
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.n_items);
   cfg.blockDim = dim3(kThreads);
@@ -1127,12 +1117,6 @@ cudaError_t launch_plan_dump(const PlanDumpParams& p, cudaStream_t stream) {
   const int total = p.H * nt;
   if (total == 0) return cudaSuccess;
   plan_dump_kernel<<<(total + 127) / 128, 128, 0, stream>>>(p);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_exp2_check(const float* x, float* y_poly, float* y_ref, int n, cudaStream_t stream) {
-  if (n < 2) return cudaSuccess;
-  exp2_check_kernel<<<(n / 2 + 255) / 256, 256, 0, stream>>>(x, y_poly, y_ref, n & ~1);
   return cudaGetLastError();
 }
 

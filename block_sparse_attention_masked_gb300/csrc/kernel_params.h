@@ -208,6 +208,5 @@ cudaError_t launch_attention(const FwdParams& p, int d, bool out_f32, cudaStream
 size_t attention_smem_bytes(int d);
 cudaError_t launch_plan_dump(const PlanDumpParams& p, cudaStream_t stream);
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream);
-cudaError_t launch_exp2_check(const float* x, float* y_poly, float* y_ref, int n, cudaStream_t stream);
 
 }  // namespace mattn

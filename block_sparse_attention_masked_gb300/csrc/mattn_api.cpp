@@ -383,16 +383,21 @@ int get_plan(DeviceState* st, const Normalized& n, cudaStream_t stream, Plan** o
 }
 
 // ------------------------------------------------------------ TMA descriptors
+// The driver's tensor-map encoder, looked up once per process.  Entry points
+// that hold different locks (mattn_fwd under g_mutex, mattn_fwd_noalloc under
+// its own) reach it, so the lookup runs under std::call_once.
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
 
 int get_encoder() {
-  if (g_encode) return MATTN_OK;
-  void* fn = nullptr;
-  cudaDriverEntryPointQueryResult q;
-  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
-    return fail(MATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e == cudaSuccess && q == cudaDriverEntryPointSuccess && fn)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return fail(MATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   return MATTN_OK;
 }
 
@@ -743,14 +748,6 @@ int mattn_internal_fwd_wait_selftest(const void* q, const void* k, const void* v
                                      int N, int d, int dtype, const mattn_mask_desc* desc, void* stream) {
   std::lock_guard<std::mutex> lk(g_mutex);
   return fwd_locked(q, k, v, o, lse, B, H, H, N, d, dtype, desc, static_cast<cudaStream_t>(stream), 1);
-}
-
-// Test hook (not in the public header): evaluates the softmax's polynomial
-// exp2 and CUDA's exp2f on n device floats, for an accuracy test.
-int mattn_internal_exp2_check(const float* x, float* y_poly, float* y_ref, int n, void* stream) {
-  if (!x || !y_poly || !y_ref || n < 0) return fail(MATTN_ERR_INVALID_ARG, "bad arguments");
-  MATTN_CUDA(launch_exp2_check(x, y_poly, y_ref, n, static_cast<cudaStream_t>(stream)), "exp2 check launch");
-  return MATTN_OK;
 }
 
 int mattn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,

@@ -32,7 +32,7 @@ std::mutex g_noalloc_mutex;
 unsigned char* g_scratch_addr[kMaxDevices] = {};
 
 // Device address of the array on the current device, looked up once per
-// device (the first call on each device; it must not run under capture).
+// device (the first call on each device).
 int scratch_on_current_device(unsigned char** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
@@ -64,6 +64,15 @@ int fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse
   int rc = prepare_in_place_launch(q, k, v, o, lse, B, H, N, d, dtype, desc, MATTN_NOALLOC_MAX_HEADS,
                                    (size_t)MATTN_NOALLOC_MAX_ITEMS, &L);
   if (rc) return rc;
+  // The work list and head table are uploaded from host vectors that live
+  // only for this call; a graph would keep pointers to freed host memory, so
+  // a stream under capture is refused before anything is recorded.
+  cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+  MATTN_NOALLOC_CUDA(cudaStreamIsCapturing(stream, &capture), "cudaStreamIsCapturing");
+  if (capture != cudaStreamCaptureStatusNone)
+    return report_error(MATTN_ERR_UNSUPPORTED,
+                        "mattn_fwd_noalloc cannot run on a stream under graph capture (it uploads its work list "
+                        "from host memory that lives only for the call)");
   unsigned char* scratch = nullptr;
   if ((rc = scratch_on_current_device(&scratch))) return rc;
   uint32_t* err = reinterpret_cast<uint32_t*>(scratch + kErrOffset);

@@ -415,31 +415,6 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
   return d;
 }
 
-// 2^x for two values on the FMA and integer pipes instead of the MUFU, for
-// finite x <= 127 (x below -125 is treated as -125, i.e. a value < 2^-125).
-// Range reduction x = n + f with n = round(x): adding 1.5 * 2^23 leaves n in
-// the low mantissa bits of t; f = x - n lies in [-1/2, 1/2].  2^f comes from
-// a degree-3 polynomial fitted here to minimise the relative error on that
-// interval (iteratively reweighted least squares; max relative error 7.5e-5
-// in fp32, far below the 2^-9 rounding of the bf16 P it feeds).  2^n is
-// applied by adding n to the exponent field: (bits(t) << 23) equals n << 23
-// modulo 2^32 because the magic constant's low 9 bits are zero.
-__device__ __forceinline__ float2 exp2_poly2(float2 x) {
-  constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
-  constexpr float c0 = 0.9999281167984009f, c1 = 0.6932609677314758f;
-  constexpr float c2 = 0.24261054396629333f, c3 = 0.05517132207751274f;
-  x.x = fmaxf(x.x, -125.0f);
-  x.y = fmaxf(x.y, -125.0f);
-  const float2 t = fadd2(x, make_float2(kMagic, kMagic));
-  const float2 n = fadd2(t, make_float2(-kMagic, -kMagic));
-  const float2 f = ffma2(n, make_float2(-1.0f, -1.0f), x);
-  float2 p = ffma2(make_float2(c3, c3), f, make_float2(c2, c2));
-  p = ffma2(p, f, make_float2(c1, c1));
-  p = ffma2(p, f, make_float2(c0, c0));
-  return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(t.x) << 23)),
-                     __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23)));
-}
-
 // Register budget of the calling warpgroup (all four warps must execute it).
 template <uint32_t N>
 __device__ __forceinline__ void setmaxnreg_inc() {

@@ -268,7 +268,12 @@ int mattn_fwd_host(const void* q, const void* k, const void* v, void* o, float* 
  * (different streams, or several host threads) therefore race on the
  * array: order them, e.g. on one stream.  The first call on a device looks
  * up the array's device address (cudaGetSymbolAddress) with that device
- * current; make that first call before any stream capture begins.
+ * current.
+ *
+ * Graph capture: the work list and the per-head table are uploaded with
+ * cudaMemcpyAsync from host memory that lives only for the call, which a
+ * captured graph could not replay.  On a stream under capture the call
+ * therefore returns MATTN_ERR_UNSUPPORTED and records nothing.
  */
 #define MATTN_NOALLOC_MAX_HEADS 4096
 #define MATTN_NOALLOC_MAX_ITEMS 65536

@@ -105,30 +105,6 @@ def top_tau(row: np.ndarray, tau: float) -> np.ndarray:
     return keep
 
 
-def top_tau_fixed(row: np.ndarray, tau: float) -> np.ndarray:
-    """Eq. 11 decided on fp32 scores quantised to integers, the form in which
-    a GPU takes the decision so that no sum depends on its order:
-    q_n = floor(s_n 2^(30 - e)) with 2^(e-1) <= max s < 2^e,
-    tau_q = round(tau 2^20) (tau in fp32), T = ceil(tau_q sum(q) / 2^20);
-    keep the shortest prefix of the scores sorted in decreasing order (equal
-    scores: smaller index first) whose q-sum reaches T.  It differs from
-    top_tau only when the running sum passes the threshold within about
-    2^-29 of the row total."""
-    x = np.maximum(np.asarray(row, dtype=np.float32), np.float32(0)).astype(np.float64)
-    e = math.frexp(float(x.max()))[1]
-    q = np.floor(np.ldexp(x, 30 - e)).astype(np.int64)
-    tau_q = int(np.rint(np.float32(tau) * np.float32(1 << 20)))
-    total = int(q.sum())
-    T = (tau_q * total + (1 << 20) - 1) >> 20
-    order = np.lexsort((np.arange(x.size), -x))
-    csum = np.cumsum(q[order])
-    k = int(np.searchsorted(csum, T, side="left"))
-    k = min(k, x.size - 1)
-    keep = np.zeros(x.size, dtype=bool)
-    keep[order[:k + 1]] = True
-    return keep
-
-
 def select_head(q: np.ndarray, k: np.ndarray, S: int, Bs: int, tau: float, h: int,
                 sink_recent: bool = False) -> Tuple[np.ndarray, np.ndarray]:
     """Block-selection matrix B [Nb, Nb] (bool) and block scores S [Nb, Nb]

@@ -29,32 +29,6 @@ def _built():
     mattn.lib()
 
 
-def test_polynomial_exp2_against_cuda_exp2f():
-    L = mattn.lib()
-    L.mattn_internal_exp2_check.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int, ctypes.c_void_p]
-    g = torch.Generator().manual_seed(0)
-    x = torch.cat([torch.linspace(-125.0, 8.0, 1 << 20),
-                   torch.rand(1 << 18, generator=g) * 133.0 - 125.0,
-                   torch.tensor([0.0, -0.5, 0.5, -1.0, 1.0, 7.999, -124.999])]).float()
-    n = x.numel() & ~1
-    x = x[:n].cuda()
-    yp = torch.empty_like(x)
-    yr = torch.empty_like(x)
-    assert L.mattn_internal_exp2_check(x.data_ptr(), yp.data_ptr(), yr.data_ptr(), n,
-                                       torch.cuda.current_stream().cuda_stream) == 0
-    torch.cuda.synchronize()
-    rel = ((yp.double() - yr.double()).abs() / yr.double()).max().item()
-    # the fitted polynomial's bound is 7.5e-5; exp2f itself is within 2 ulp
-    assert rel < 1e-4, rel
-    # arguments below -125 are clamped: the result is 2^-125, not larger
-    xl = torch.tensor([-200.0, -1e30, -126.0, -125.5], device="cuda")
-    yl, yrl = torch.empty_like(xl), torch.empty_like(xl)
-    assert L.mattn_internal_exp2_check(xl.data_ptr(), yl.data_ptr(), yrl.data_ptr(), 4,
-                                       torch.cuda.current_stream().cuda_stream) == 0
-    torch.cuda.synchronize()
-    assert torch.all(yl > 0) and torch.all(yl <= 2.0 ** -124)
-
-
 def test_bounded_wait_reports_timeout_and_context_survives():
     L = mattn.lib()
     f = L.mattn_internal_fwd_wait_selftest

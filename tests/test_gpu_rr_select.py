@@ -11,14 +11,19 @@ What is compared, and how closely:
   |S_gpu - S| <= S * (exp(2 delta_m) - 1) with delta_m the largest delta_i of
   query block m, plus 1e-5 per stride pair for fp32 accumulation and the
   exp2 approximation.
-- The selection (Eq. 11-12, Eq. 5) is an integer result decided by floating
-  point, so both sides take the decision from the same values in the same
-  form: the kernel decides on its scores quantised to integers (exact sums,
-  no order dependence), and the oracle's integer form of Eq. 11
-  (``top_tau_fixed``) applied to the GPU's own scores must give the GPU's
-  bits exactly, on every row.  On inputs with a planted pattern, whose
-  decisions have a wide margin, the GPU's bits must equal the oracle's bits
-  from its own fp64 scores.
+- The selection (Eq. 11) is an integer result decided by floating point.
+  The GPU's bits are compared with the fp64 Eq. 11 rule (``top_tau``)
+  applied to the GPU's own scores.  They must be equal on every row except
+  one whose sorted running sum passes tau times the row total within
+  2^-18 of the total: there the kernel's own precision decides (it sums
+  scores quantised to 2^-30 of the row maximum over at most 1024 blocks,
+  < 2^-19 of the total in all, and rounds tau to a multiple of 2^-20), so
+  either side of the crossing is correct.  On such a row the GPU's set
+  must still be valid: apart from the crossing block, the blocks in which
+  the two sets differ add up to less than that 2^-18 of the total, and no
+  dropped block scores above a kept one (beyond 2^-28 of the row maximum).  On inputs with a planted pattern, whose decisions have a wide
+  margin, the GPU's bits must equal the oracle's bits from its own fp64
+  scores exactly.
 - Eq. 12 and Eq. 5 (last query block full, nothing above the diagonal) are
   checked exactly everywhere, also at the 128K-token, 32-head size on every
   row, with scores compared on sampled rows there.
@@ -56,6 +61,43 @@ def _np(t):
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
+# A crossing of tau * total closer than this share of the total is decided
+# by the kernel's precision (see the module docstring).
+NEAR_CROSSING = 2.0 ** -18
+SCORE_SLACK = 2.0 ** -28
+
+
+def _check_decision(row_scores, gpu_row, tau, m, sink_recent, tag):
+    """Eq. 11 on one query block m: GPU bits vs the fp64 rule on the GPU's
+    own (fp32) scores, with the near-crossing allowance."""
+    x = np.maximum(np.asarray(row_scores, dtype=np.float64), 0.0)
+    nb = x.size
+    causal = np.arange(nb) <= m
+    want = orr.top_tau(x, tau) & causal
+    if sink_recent:
+        want[0] = True
+        want[m] = True
+    if (want == gpu_row).all():
+        return
+    order = np.lexsort((np.arange(nb), -x))
+    csum = np.cumsum(x[order])
+    total = x.sum()
+    gap = np.abs(csum - tau * total).min()
+    assert gap <= NEAR_CROSSING * total, f"{tag}: selection differs away from a near-crossing (gap {gap / total:.3e})"
+    pinned = np.zeros(nb, dtype=bool)
+    if sink_recent:
+        pinned[0] = pinned[m] = True
+    free = causal & ~pinned
+    kept, dropped = x[free & gpu_row], x[free & ~gpu_row]
+    # both sets are prefixes of the same descending order whose sums sit on
+    # either side of the ambiguous crossing: apart from the crossing block
+    # itself, the blocks in one set only add up to less than the ambiguity
+    diff = x[free & (gpu_row != want)]
+    assert diff.sum() - diff.max() <= NEAR_CROSSING * total, f"{tag}: the sets differ beyond the crossing block"
+    if kept.size and dropped.size:
+        assert dropped.max() <= kept.min() + SCORE_SLACK * x.max(), f"{tag}: a dropped block outscores a kept one"
+
+
 def _check_scores(q, k, S, Bs, tau, sink_recent, scores_gpu, bits_gpu, exact_bits):
     B, H, L, d = q.shape
     nb = -(-(L // S) // (Bs // S))
@@ -78,13 +120,9 @@ def _check_scores(q, k, S, Bs, tau, sink_recent, scores_gpu, bits_gpu, exact_bit
             # Eq. 12 and Eq. 5
             assert bits[b, h, nb - 1].all()
             assert not np.triu(bits[b, h], 1).any()
-            # the decision from the GPU's own scores, in the kernel's integer form
+            # Eq. 11 on the GPU's own scores (fp64 rule, near-crossing allowance)
             for m in range(nb - 1):
-                want = orr.top_tau_fixed(sc[b, h, m], tau) & (np.arange(nb) <= m)
-                if sink_recent:
-                    want[0] = True
-                    want[m] = True
-                assert (want == bits[b, h, m]).all(), f"b{b} h{h} m{m}: selection differs"
+                _check_decision(sc[b, h, m], bits[b, h, m], tau, m, sink_recent, f"b{b} h{h} m{m}")
             if exact_bits:
                 assert (bits[b, h] == B_or).all(), f"b{b} h{h}: bits differ from the oracle's"
     return bits
@@ -160,7 +198,7 @@ def test_full_size_128k_sampled_rows():
     """The 128K-token, 32-head prefill recipe (d 128, stride 8, block 128,
     tau 0.95): the whole bitmap obeys Eq. 12 and Eq. 5; on sampled (head,
     query block) rows the scores match the fp64 oracle's row within the
-    derived tolerance and the decision matches the GPU's own scores."""
+    derived tolerance and the decision follows Eq. 11 on the GPU's own scores."""
     B, H, L, d, S, Bs, tau = 1, 32, 131072, 128, 8, 128, 0.95
     q, k, _ = make_qkv(B, H, L, d, "bf16", 1.0, seed=0, device="cuda")
     bits, scores = mattn.rr_select(q, k, S, Bs, tau, want_scores=True)
@@ -185,5 +223,4 @@ def test_full_size_128k_sampled_rows():
             tol = S_row * (np.exp(2 * delta) - 1) + 1e-5 * g * g
             got = scores[int(h), m].cpu().numpy().astype(np.float64)
             assert (np.abs(got - S_row) <= tol).all(), (int(h), m)
-            want = orr.top_tau_fixed(got, tau) & (np.arange(nb) <= m)
-            assert (want == allbits[int(h), m]).all(), (int(h), m)
+            _check_decision(got, allbits[int(h), m], tau, m, False, f"h{int(h)} m{m}")
