@@ -47,10 +47,10 @@ _GRID_ORDERS = {"column_major": ORDER_COLUMN_MAJOR, "block2x2_row": ORDER_BLOCK2
                 "block2x2_col": ORDER_BLOCK2X2_COL}
 TILE = 128
 TILE_FULL, TILE_PARTIAL = 1, 2
-FLAG_SCHEDULE_PAIRED, FLAG_SCHEDULE_SPLIT, FLAG_SCHEDULE_SINGLE = 1, 2, 4
+FLAG_SCHEDULE_PAIRED, FLAG_SCHEDULE_SPLIT, FLAG_SCHEDULE_SINGLE, FLAG_SCHEDULE_PERSISTENT = 1, 2, 4, 8
 RR_SINK_RECENT = 1
 SCHEDULE = {None: 0, "auto": 0, "paired": FLAG_SCHEDULE_PAIRED, "split": FLAG_SCHEDULE_SPLIT,
-            "single": FLAG_SCHEDULE_SINGLE}
+            "single": FLAG_SCHEDULE_SINGLE, "persistent": FLAG_SCHEDULE_PERSISTENT}
 
 
 class MattnError(RuntimeError):

@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libmattn.so")
 BUILD_DIR = os.path.join(PKG, "_build")
 
-SOURCES = ["attention_fwd.cu", "attention_sp.cu", "rr_select.cu", "received.cu", "decode.cu", "mattn_api.cpp",
+SOURCES = ["attention_fwd.cu", "attention_persist.cu", "attention_sp.cu", "rr_select.cu", "received.cu", "decode.cu", "mattn_api.cpp",
            "mattn_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

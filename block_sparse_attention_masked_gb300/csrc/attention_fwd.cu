@@ -36,6 +36,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "attention_tiles.cuh"
 #include "kernel_params.h"
 #include "plan_rules.h"
 #include "ptx.cuh"
@@ -46,38 +47,11 @@ namespace mattn {
 namespace {
 
 constexpr int kThreads = 384;
-constexpr int kNoTile = 0x7fffffff;
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
-// The running row maximum m only guards against overflow: numerator and
-// denominator share it, so any m gives the same result.  A tile is
-// exponentiated against the stale m as long as its row sum of P stays below
-// 2^40 (no overflow in fp32 or bf16, nor in O's fp32 accumulation); a tile
-// above it is redone against the tile's true maximum.
-constexpr float kMaxTileSum = 1099511627776.0f;  // 2^40
 // Registers per thread after setmaxnreg: producer / MMA-issuer warpgroup and the
 // two softmax warpgroups (their sum times 128 equals the launch budget).
 constexpr uint32_t kRegsControl = 72;
 constexpr uint32_t kRegsSoftmax = 216;
 static_assert(kRegsControl + 2 * kRegsSoftmax == 3 * 168, "register split must match the launch budget");
-
-// The CTA's key-tile list: entry j (0 <= j < n) is key tile kt(j).  Paired,
-// sub-tile s multiplies entry j when uses(j, s); split, entry j belongs to
-// pipeline j % 2.  Interval kinds: the entries are the key tiles lo .. lo +
-// n - 1 (the union of the sub-tiles' ranges, which overlap or touch), each
-// sub-tile using its own range.  Block kind: the entries sit in shared
-// memory as kt | use0 << 30 | use1 << 31, built once per CTA.  Reading an
-// entry is one add or one shared load, which keeps the loops of the
-// copy and MMA warps short.
-struct TileList {
-  int n, lo;
-  int na;              // interval kinds: leading entries 0 .. na - 1 are sink tiles below lo
-  int lo0, hi0, lo1, hi1;
-  int ns0, ns1;        // sink tiles of each sub-tile (causal window with sink tokens)
-  int use_n0, use_n1;  // block kind: entries sub-tile 0 / 1 uses
-  const uint32_t* e;
-  bool block;
-};
 
 struct Barriers {
   uint64_t q_full[2];
@@ -97,126 +71,6 @@ struct Barriers {
   TileList tl;          // the CTA's key-tile list (read by every role from shared memory)
   float xch[2][3][kTile];  // split schedule: per sub-tile (m, l, tile count) of each row
 };
-
-// Capacity of the per-CTA key-tile list of block-sparse masks (a query
-// tile sees at most N/128 key tiles, so N <= 128 * kMaxList).
-constexpr int kMaxList = kBlockListMax;
-
-// Key-tile plan of one 128-row query sub-tile.
-struct SubPlan {
-  int qt;
-  bool rows;                 // the sub-tile has query rows (< N)
-  KRange r;                  // interval kinds (causal window with sink tokens: the window part)
-  int ns;                    // sink tiles [0, ns) (causal window with sink tokens)
-  int param;                 // the head's mask parameter
-  int ktmax;                 // block kind: last admissible key tile (causality)
-};
-
-// Work description of one CTA, computed identically by every thread.
-struct ItemPlan {
-  int bh, h, b;
-  int bh_kv;  // K / V head row of (b, h): b * H_kv + h / kv_group
-  SubPlan sp0, sp1;
-};
-
-// Query tile of sub-tile s of work item `it`.
-__device__ __forceinline__ int item_qt(const FwdParams& p, int2 it, int s) { return p.split ? it.y : 2 * it.y + s; }
-
-// Global bitmap row of sub-tile s of work item `it` (block kind).
-__device__ __forceinline__ const uint64_t* global_row(const FwdParams& p, int2 it, int s) {
-  const int h = it.x % p.H;
-  const int hb = (p.block_heads == 1) ? 0 : h;
-  const int qt = item_qt(p, it, s);
-  return p.block_bits + ((int64_t)hb * p.block_nb + qt / p.block_c) * p.block_wpr;
-}
-
-__device__ __forceinline__ SubPlan make_subplan(const FwdParams& p, int2 it, int s, int param) {
-  SubPlan sp;
-  const int nt = (p.N + kTile - 1) / kTile;
-  sp.qt = item_qt(p, it, s);
-  sp.rows = sp.qt < nt;
-  sp.ktmax = sp.qt < nt ? sp.qt : nt - 1;
-  sp.param = param;
-  sp.ns = 0;
-  if (p.kind != kBlockSparse && sp.rows) {
-    sp.r = interval_krange(p.kind, param, p.N, sp.qt);
-    sp.ns = sink_tiles(p.sink_tokens, p.N, sp.qt);
-  } else {
-    sp.r.lo = 1; sp.r.hi = 0; sp.r.flo = 0; sp.r.fhi = -1;  // empty
-  }
-  return sp;
-}
-
-__device__ __forceinline__ ItemPlan make_plan(const FwdParams& p, int2 it, int param) {
-  ItemPlan ip;
-  ip.bh = it.x;
-  ip.h = it.x % p.H;
-  ip.b = it.x / p.H;
-  ip.bh_kv = ip.b * p.H_kv + ip.h / p.kv_group;
-  ip.sp0 = make_subplan(p, it, 0, param);
-  ip.sp1 = make_subplan(p, it, 1, param);
-  return ip;
-}
-
-__device__ __forceinline__ int list_kt(const TileList& L, int j) {
-  return L.block ? (int)(L.e[j] & 0x3fffffffu) : (j < L.na ? j : L.lo + j - L.na);
-}
-
-__device__ __forceinline__ bool list_uses(const TileList& L, int j, int s) {
-  if (L.block) return (L.e[j] >> (30 + s)) & 1u;
-  const int kt = list_kt(L, j);
-  return s ? ((kt >= L.lo1 && kt <= L.hi1) || kt < L.ns1) : ((kt >= L.lo0 && kt <= L.hi0) || kt < L.ns0);
-}
-
-// Whether sub-tile s (split: pipeline s, which shares the one query tile)
-// has any key tile: its Q tile is loaded and waited for only then.
-__device__ __forceinline__ bool list_has(const TileList& L, int s, bool split) {
-  if (split) return L.n > 0;
-  if (L.block) return (s ? L.use_n1 : L.use_n0) > 0;
-  return s ? L.lo1 <= L.hi1 : L.lo0 <= L.hi0;
-}
-
-__device__ __forceinline__ TileList make_list(const FwdParams& p, const ItemPlan& ip, const uint32_t* entries,
-                                              const int* block_counts) {
-  TileList L;
-  L.block = p.kind == kBlockSparse;
-  L.e = entries;
-  L.use_n0 = L.block ? block_counts[1] : 0;
-  L.use_n1 = L.block ? block_counts[2] : 0;
-  L.lo0 = ip.sp0.r.lo; L.hi0 = ip.sp0.r.hi;
-  L.lo1 = ip.sp1.r.lo; L.hi1 = ip.sp1.r.hi;
-  L.ns0 = ip.sp0.ns; L.ns1 = ip.sp1.ns;
-  L.na = 0;
-  if (L.block) {
-    L.n = block_counts[0];
-    L.lo = 0;
-  } else {
-    const bool e0 = L.lo0 <= L.hi0, e1 = L.lo1 <= L.hi1;
-    L.lo = e0 ? (e1 ? min(L.lo0, L.lo1) : L.lo0) : L.lo1;
-    int hi = e0 ? (e1 ? max(L.hi0, L.hi1) : L.hi0) : L.hi1;
-    L.n = (e0 || e1) ? hi - L.lo + 1 : 0;
-    // sink tiles: a segment 0 .. ns - 1 before the window's tiles, or one
-    // segment 0 .. hi when they meet
-    const int ns = max(L.ns0, L.ns1);
-    if (ns > 0 && L.n > 0) {
-      if (ns >= L.lo) {
-        hi = max(hi, ns - 1);
-        L.lo = 0;
-        L.n = hi + 1;
-      } else {
-        L.na = ns;
-        L.n += ns;
-      }
-    }
-  }
-  return L;
-}
-
-__device__ __forceinline__ bool sub_partial(const FwdParams& p, const SubPlan& sp, int kt) {
-  if (p.kind == kBlockSparse) return block_tile_class(sp.qt, kt, p.N) == kTilePartial;
-  if (p.sink_tokens > 0) return sink_window_tile_class(sp.param, p.sink_tokens, p.N, sp.qt, kt) == kTilePartial;
-  return interval_tile_class(sp.r, kt) == kTilePartial;
-}
 
 // Block kind: one warp writes the CTA's entries to `list` (ascending key
 // tiles; the union of the sub-tiles' kept tiles at or below their
@@ -291,209 +145,11 @@ __device__ __forceinline__ void build_block_list(const FwdParams& p, int2 item, 
   }
 }
 
-// Issue order of the MMA groups (a shared-memory word): the group with
-// ticket t is pushed once mma_turn == t, and its issuer then passes the turn
-// on.  Paired: entry j's group of sub-tile s has ticket 2j + s; split: entry
-// j's group has ticket j.  A plain load / store pair: far cheaper on the
-// critical path than an atomic lock.  The bounded spin gives up on abort or
-// timeout like any wait.
-__device__ __forceinline__ bool mma_turn_wait(Barriers* bar, uint32_t ticket, uint64_t timeout_ns,
-                                              volatile int* abort_flag) {
-  const uint32_t a = ptx::smem_addr(&bar->mma_turn);
-  if (ptx::ld_shared_acquire(a) == ticket) return true;
-  const uint64_t t0 = ptx::globaltimer_ns();
-  for (uint32_t it = 1; it < 0x80000000u; ++it) {
-    if (ptx::ld_shared_acquire(a) == ticket) return true;
-    if ((it & 63u) == 0) {
-      if (*abort_flag) return false;
-      if (ptx::globaltimer_ns() - t0 > timeout_ns) return false;
-    }
-  }
-  return false;
-}
-
-__device__ __forceinline__ void mma_turn_pass(Barriers* bar, uint32_t ticket) {
-  ptx::st_release_shared(ptx::smem_addr(&bar->mma_turn), ticket + 1u);
-}
-
-__device__ __forceinline__ void raise_error(const FwdParams& p, Barriers* bar, uint32_t bit) {
-  *reinterpret_cast<volatile int*>(&bar->abort_flag) = 1;
-  atomicOr(p.err, bit);
-}
-
-// 2x2-block orders: the 5D view's coordinates (c3, c4) of the tile at
-// position p0 (32 consecutive blocks).  Row-major view (d, dc, dr, C,
-// R + bh * rows/2): 32 blocks of one block row (cols % 64 == 0).
-// Column-major view (d, dc, dr, R + bh * rows/2, C): 32 blocks of one block
-// column (rows % 64 == 0).
-__device__ __forceinline__ void block2x2_coords(const FwdParams& p, int mode, int p0, int bh, int* c3, int* c4) {
-  const int blk = p0 >> 2;
-  const int half_rows = p.grid_rows >> 1;
-  if (mode == kLoadBlock2x2Row) {
-    const int half_cols = p.grid_cols >> 1;
-    const int R = blk / half_cols;
-    *c3 = blk - R * half_cols;
-    *c4 = R + bh * half_rows;
-  } else {
-    const int C = blk / half_rows;
-    *c3 = blk - C * half_rows + bh * half_rows;
-    *c4 = C;
-  }
-}
-
-// TMA load of one 128-row Q (is_k false) or K tile (all d columns) starting
-// at sequence position p0, through the raster view, the column-major view or
-// a 2x2-block view (`mode`, a LoadMode).  `policy` is the L2 eviction
-// priority of the tile's lines.
-template <int D>
-__device__ __forceinline__ void load_tile(const FwdParams& p, bool is_k, int mode, uint8_t* dst, uint64_t* bar, int p0,
-                                          int bh, uint64_t policy) {
-  using G = Geo<D>;
-  if (mode == kLoadRaster) {
-    const CUtensorMap* raster = is_k ? p.tk : p.tq;
-#pragma unroll
-    for (int c = 0; c < G::kChunks; ++c)
-      ptx::tma_load_3d_hint(dst + c * G::kChunkBytes, &raster[0], bar, c * 64, p0, bh, policy);
-    if (G::kRem) ptx::tma_load_3d_hint(dst + G::kChunks * G::kChunkBytes, &raster[1], bar, 0, p0, bh, policy);
-  } else if (mode == kLoadBlock2x2Row || mode == kLoadBlock2x2Col) {
-    // the box (d chunk, dc 2, dr 2, 32 blocks) lands in position order:
-    // row 4 * block + 2 * dr + dc of the tile
-    const CUtensorMap* blocks =
-        mode == kLoadBlock2x2Row ? (is_k ? p.bk : p.bq) : (is_k ? p.bck : p.bcq);
-    int c3, c4;
-    block2x2_coords(p, mode, p0, bh, &c3, &c4);
-#pragma unroll
-    for (int c = 0; c < G::kChunks; ++c)
-      ptx::tma_load_5d_hint(dst + c * G::kChunkBytes, &blocks[0], bar, c * 64, 0, 0, c3, c4, policy);
-    if (G::kRem)
-      ptx::tma_load_5d_hint(dst + G::kChunks * G::kChunkBytes, &blocks[1], bar, 0, 0, 0, c3, c4, policy);
-  } else {
-    // position p = c * rows + r holds token r * cols + c; a 128-position tile is
-    // one grid column c, rows r0 .. r0 + 127 (rows % 128 == 0 is required).
-    const CUtensorMap* colmaj = is_k ? p.ck : p.cq;
-    const int col = p0 / p.grid_rows;
-    const int r0 = p0 - col * p.grid_rows;
-#pragma unroll
-    for (int c = 0; c < G::kChunks; ++c)
-      ptx::tma_load_4d_hint(dst + c * G::kChunkBytes, &colmaj[0], bar, c * 64, col, r0, bh, policy);
-    if (G::kRem)
-      ptx::tma_load_4d_hint(dst + G::kChunks * G::kChunkBytes, &colmaj[1], bar, 0, col, r0, bh, policy);
-  }
-}
-
-// TMA load of one 128-row V tile in its uniform-swizzle layout (map [0] of
-// the V views has a kVW-column box).
-template <int D>
-__device__ __forceinline__ void load_v_tile(const FwdParams& p, int mode, uint8_t* dst, uint64_t* bar, int p0,
-                                            int bh, uint64_t policy) {
-  using G = Geo<D>;
-  if (mode == kLoadRaster) {
-#pragma unroll
-    for (int c = 0; c < G::kVChunks; ++c)
-      ptx::tma_load_3d_hint(dst + c * G::kVChunkBytes, &p.tv[0], bar, c * G::kVW, p0, bh, policy);
-  } else if (mode == kLoadBlock2x2Row || mode == kLoadBlock2x2Col) {
-    const CUtensorMap* blocks = mode == kLoadBlock2x2Row ? p.bv : p.bcv;
-    int c3, c4;
-    block2x2_coords(p, mode, p0, bh, &c3, &c4);
-#pragma unroll
-    for (int c = 0; c < G::kVChunks; ++c)
-      ptx::tma_load_5d_hint(dst + c * G::kVChunkBytes, &blocks[0], bar, c * G::kVW, 0, 0, c3, c4, policy);
-  } else {
-    const int col = p0 / p.grid_rows;
-    const int r0 = p0 - col * p.grid_rows;
-#pragma unroll
-    for (int c = 0; c < G::kVChunks; ++c)
-      ptx::tma_load_4d_hint(dst + c * G::kVChunkBytes, &p.cv[0], bar, c * G::kVW, col, r0, bh, policy);
-  }
-}
-
-// O += P V for one sub-tile: P (128 x 128 keys, bf16 pairs in TMEM) is the
-// A operand; V (keys x d, d contiguous) is an MN-major B operand whose
-// kVW-column atoms lie kVChunkBytes apart (leading byte offset) and whose
-// 8-key groups lie 8 rows apart (stride byte offset).  One N = D MMA per
-// 16 keys, issued by one thread.
-template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_addr4, bool accumulate) {
-  using G = Geo<D>;
-  constexpr uint32_t idesc = ptx::idesc_bf16(128, D, 1);
-  constexpr uint32_t row_bytes = G::kVW * 2;
-  constexpr uint32_t lbo = (uint32_t)(G::kVChunkBytes >> 4) << 16;
-  constexpr uint32_t hi = ptx::smem_desc_hi(8 * row_bytes, G::kVSwizzle);
-  uint32_t acc = accumulate ? 1u : 0u;
-#pragma unroll 1
-  for (int k = 0; k < kTile / 16; ++k) {
-    // 16 bf16 keys = 8 tensor-memory columns of P; 16 rows of V
-    ptx::mma_ts(o_tmem, p_tmem + k * 8, desc_of(v_addr4 + ((k * 16 * row_bytes) >> 4) + lbo, hi), idesc, acc);
-    acc = 1;
-  }
-}
-
-// P = exp2(x * sl2 - mref) for the 128 scores of this thread's row, stored
-// to tensor memory at p_tmem as bf16 pairs (64 columns, round to nearest);
-// returns the row sum of the fp32 values.  All exponentials use MUFU ex2:
-// moving a share of them to an FMA-pipe polynomial measured slower at every
-// share tried, as did a truncating pack with a second sum over the
-// truncated values (one more add and two integer ops per pair).
-__device__ __forceinline__ float exp_to_tmem(const float (&x)[128], float sl2, float mref, uint32_t p_tmem) {
-  const float2 sl2v = make_float2(sl2, sl2);
-  const float2 negm = make_float2(-mref, -mref);
-  float2 acc[2];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) acc[i] = make_float2(0.f, 0.f);
-#pragma unroll
-  for (int c0 = 0; c0 < 128; c0 += 32) {
-    uint32_t pk[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float2 t = ptx::ffma2(make_float2(x[c0 + 2 * i], x[c0 + 2 * i + 1]), sl2v, negm);
-      const float2 pp = make_float2(ptx::ex2(t.x), ptx::ex2(t.y));
-      pk[i] = ptx::pack_bf16x2(pp.x, pp.y);
-      acc[i & 1] = ptx::fadd2(acc[i & 1], pp);
-    }
-    ptx::tmem_st16(p_tmem + c0 / 2, pk);
-  }
-  const float2 a = ptx::fadd2(acc[0], acc[1]);
-  return a.x + a.y;
-}
-
-// Maximum of the 128 raw scores of this thread's row (8 independent chains;
-// measured faster here than three-input maxima).
-__device__ __forceinline__ float row_max(const float (&x)[128]) {
-  float a[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) a[i] = x[i];
-#pragma unroll
-  for (int c = 8; c < 128; c += 8)
-#pragma unroll
-    for (int i = 0; i < 8; ++i) a[i] = fmaxf(a[i], x[c + i]);
-  return fmaxf(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])), fmaxf(fmaxf(a[4], a[5]), fmaxf(a[6], a[7])));
-}
-
-// O row *= alpha in tensor memory (warp-collective; alpha is per lane).
-template <int D>
-__device__ __forceinline__ void rescale_o(uint32_t o_tmem, float alpha) {
-#pragma unroll
-  for (int c0 = 0; c0 < D; c0 += 16) {
-    float ov[16];
-    ptx::tmem_ld16(o_tmem + c0, ov);
-    ptx::tmem_wait_ld();
-    uint32_t ou[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) ou[i] = __float_as_uint(ov[i] * alpha);
-    ptx::tmem_st16(o_tmem + c0, ou);
-  }
-}
-
 // Split schedule: O columns [0, kOHalf) are written by sub-tile 0's threads,
 // [kOHalf, D) by sub-tile 1's (whole 16-column loads).
 template <int D>
 __host__ __device__ constexpr int kOHalf() {
   return 16 * ((D + 31) / 32);
-}
-
-__device__ __forceinline__ int64_t token_of(const FwdParams& p, int store_mode, int perm_row, int64_t pos) {
-  return token_at(store_mode, p.grid_rows, p.grid_cols,
-                  store_mode == kStoreExplicit ? p.perm + (int64_t)perm_row * p.N : nullptr, pos);
 }
 
 // The CTA's Q tiles: one per sub-tile that has key tiles (split: the one
@@ -899,22 +555,10 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
         ok = have_oo;
       }
       if (ok) {
-        const float b2 = bar->sink_log2;
-        const float M = fmaxf(fmaxf(m, m_o), b2);
-        float o_scale = 0.f, oo_scale = 0.f;
-        float lse_v = -INFINITY;
-        if (M != -INFINITY) {
-          // O = sum of P V / (l + exp(sink)) with every term taken against
-          // the common maximum M; the LSE from the same normaliser
-          const float em = (m == -INFINITY) ? 0.f : ptx::ex2(m - M);
-          const float eo = (m_o == -INFINITY) ? 0.f : ptx::ex2(m_o - M);
-          const float lf = l * em + l_o * eo + ((b2 == -INFINITY) ? 0.f : ptx::ex2(b2 - M));
-          if (lf > 0.f) {
-            o_scale = em / lf;
-            oo_scale = eo / lf;
-            lse_v = (M + ptx::lg2(lf)) * kLn2;
-          }
-        }
+        // O = sum of P V / (l + exp(sink)) with every term taken against
+        // the common maximum; the LSE from the same normaliser
+        float o_scale, oo_scale, lse_v;
+        finalize_row(m, l, m_o, l_o, bar->sink_log2, &o_scale, &oo_scale, &lse_v);
         const bool valid = pos < p.N;
         const int store_mode = bar->head_store;
         const int perm_row = bar->head_perm_row;

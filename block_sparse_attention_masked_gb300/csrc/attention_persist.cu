@@ -1,0 +1,635 @@
+// Persistent masked attention forward for the interval masks (full, chunk,
+// sliding window, causal window with or without sink tokens) on sm_103a.
+//
+// The computation of a work item is that of attention_fwd.cu's paired
+// schedule: query rows [256*pair, 256*pair + 256) of one (batch, head) as
+// two 128-row sub-tiles s = 0, 1 sharing the staged K/V tiles, for every
+// key tile kt of the item's list
+//     S_s  = Q_s K_kt^T                        (tcgen05.mma, smem x smem -> TMEM)
+//     P_s  = exp2(S_s * scale*log2e - m_s)     (softmax warps, online max m_s)
+//     O_s += P_s V_kt                          (tcgen05.mma, P from TMEM, V from smem)
+// and O_s / (l_s + exp(sink)) with the log-sum-exp at the end (SHS slides
+// Eq. 1 for the sink; the FlashAttention idea of the Vision transformers
+// lesson).  What differs is the schedule: the grid has one CTA per SM and
+// CTA c takes work items c, c + G, c + 2G, ... (G = grid size; the host's
+// list is heaviest first).  Its key-tile lists are walked as one stream, so
+// the K/V rings, the MMA issue order and the softmax never drain between
+// items: the next item's Q tiles are loaded while the current one runs (Q
+// slots rotate) and its first Q K^T goes to the tensor core in the same
+// group as the current item's last P V.  The softmax warps of a sub-tile
+// write the item's output while that product runs: they wait for the last
+// P V, read O_s, normalise and store it, then take the next item's first
+// S, which is ready by then.  Masks whose items are short (a window of a
+// few key tiles) spend most of a one-item-per-CTA launch in set-up and
+// epilogue; here those overlap the neighbouring items' work.
+//
+// Roles (384 threads):
+//   warp 0        TMA producer: Q tiles into their slots and K tiles into their ring
+//   warp 1        tensor-memory allocator; MMA issuer of sub-tile 0
+//   warp 2        MMA issuer of sub-tile 1
+//   warp 3        TMA producer of the V ring
+//   warps 4..7    softmax and epilogue of sub-tile 0 (one query row per thread)
+//   warps 8..11   softmax and epilogue of sub-tile 1
+// Tensor memory (512 columns x 128 lanes, fp32): S_0 [0,128), S_1
+// [128,256) (P_s as bf16 pairs in the first 64 columns of S_s), O_0
+// [256,384), O_1 [384,512).  O_s of an item is read once its last P V is
+// done (o_full); the next item's first P V, which overwrites it, is issued
+// only after that item's first P, which the same threads write after
+// reading O_s.
+// Every wait is bounded in time and gives up by raising a CTA-wide abort
+// flag and a device error bit.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "attention_tiles.cuh"
+#include "kernel_params.h"
+#include "plan_rules.h"
+#include "ptx.cuh"
+#include "tile_mma.cuh"
+
+namespace mattn {
+
+namespace {
+
+constexpr int kPThreads = 384;
+// Registers per thread after setmaxnreg: producer / MMA-issuer warpgroup and
+// the two softmax warpgroups (their sum times 128 equals the launch budget).
+constexpr uint32_t kPRegsControl = 72;
+constexpr uint32_t kPRegsSoftmax = 216;
+static_assert(kPRegsControl + 2 * kPRegsSoftmax == 3 * 168, "register split must match the launch budget");
+
+// Q slots: Q tile t = 2 i + s (i = the CTA's i-th item) goes to slot
+// t % kQSlots, free again once the S products of Q tile t - kQSlots are done.
+template <int D>
+struct PGeo {
+  static constexpr int kQSlots = (D <= 96) ? 4 : 3;
+};
+
+struct PBarriers {
+  uint64_t q_full[4], q_empty[4];
+  uint64_t k_full[3], k_empty[3];
+  uint64_t v_full[3], v_empty[3];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_full[2];      // the item's last P V of sub-tile s is done
+  uint64_t drain[2];       // MMA drain on abort, one per issuer
+  uint32_t tmem_base;
+  int abort_flag;
+  uint32_t mma_turn;       // ticket of the MMA group that may be issued next
+};
+
+// One work item as every role reads it: the item and its head's table row.
+struct ItemRef {
+  int2 item;
+  int4 head;  // param, load mode, store mode, explicit-order row
+};
+
+__device__ __forceinline__ ItemRef load_item(const FwdParams& p, int it) {
+  ItemRef r;
+  r.item = __ldg(p.items + it);
+  r.head = __ldg(reinterpret_cast<const int4*>(p.head_info) + r.item.x % p.H);
+  return r;
+}
+
+// The CTA's items it = blockIdx.x + i * gridDim.x.  With kPrefetch the next
+// item's table entries are loaded into registers while the current one is
+// worked on (the MMA issuers, for which an item boundary is on the critical
+// path); the softmax warps, short of registers, only pull the next item's
+// entry into L1 (prefetch_next), and the producers run ahead of everyone.
+template <bool kPrefetch>
+struct ItemCursor {
+  int it, i;
+  ItemRef cur, nxt;
+  __device__ __forceinline__ void start(const FwdParams& p) {
+    it = blockIdx.x;
+    i = 0;
+    if (it < p.n_items) cur = load_item(p, it);
+    if (kPrefetch && it + (int)gridDim.x < p.n_items) nxt = load_item(p, it + gridDim.x);
+  }
+  __device__ __forceinline__ bool valid(const FwdParams& p) const { return it < p.n_items; }
+  __device__ __forceinline__ void prefetch_next(const FwdParams& p) const {
+    if (it + (int)gridDim.x < p.n_items) ptx::prefetch_l1(p.items + it + gridDim.x);
+  }
+  __device__ __forceinline__ void advance(const FwdParams& p) {
+    it += gridDim.x;
+    ++i;
+    if (kPrefetch) {
+      cur = nxt;
+      if (it + (int)gridDim.x < p.n_items) nxt = load_item(p, it + gridDim.x);
+    } else if (it < p.n_items) {
+      cur = load_item(p, it);
+    }
+  }
+};
+
+// Entry indices of the first and last entries sub-tile s uses (interval
+// kinds: one contiguous range of key tiles plus, with sink tokens, a
+// leading segment of sink tiles).
+__device__ __forceinline__ void use_bounds(const TileList& L, int s, int* first, int* last) {
+  *first = -1;
+  *last = -1;
+  for (int j = 0; j < L.n; ++j) {
+    if (list_uses(L, j, s)) {
+      if (*first < 0) *first = j;
+      *last = j;
+    }
+  }
+}
+
+template <int D, bool OUT_F32>
+__global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const __grid_constant__ FwdParams p) {
+  using G = Geo<D>;
+  constexpr int KS = G::kStages;
+  constexpr int VS = G::kStages;
+  constexpr int NQ = PGeo<D>::kQSlots;
+  static_assert(KS == VS, "one ring depth for K and V");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sq = base;
+  uint8_t* sk = sq + NQ * G::kTileBytes;
+  uint8_t* sv = sk + KS * G::kTileBytes;
+  PBarriers* bar = reinterpret_cast<PBarriers*>(sv + VS * G::kTileBytes);
+  volatile int* abort_flag = &bar->abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    // after the reorder pre-pass: no wait of this CTA may start while its
+    // copies are still being written
+    if (p.after_prepass) asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (int i = 0; i < NQ; ++i) {
+      ptx::mbar_init(&bar->q_full[i], 1);
+      ptx::mbar_init(&bar->q_empty[i], 1);
+    }
+    for (int i = 0; i < KS; ++i) {
+      ptx::mbar_init(&bar->k_full[i], 1);
+      ptx::mbar_init(&bar->k_empty[i], 2);  // one commit from each issuer
+      ptx::mbar_init(&bar->v_full[i], 1);
+      ptx::mbar_init(&bar->v_empty[i], 2);
+    }
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(&bar->s_full[s], 1);
+      ptx::mbar_init(&bar->p_full[s], kTile);
+      ptx::mbar_init(&bar->o_full[s], 1);
+      ptx::mbar_init(&bar->drain[s], 1);
+    }
+    bar->abort_flag = 0;
+    bar->mma_turn = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&bar->tmem_base, 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = bar->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ Q and K producer
+    // Two streams served in turn by one thread: the Q tiles (slot t % NQ,
+    // free once the S products of Q tile t - NQ are done) and the K tiles of
+    // the concatenated key-tile lists (ring slot e % KS).  Neither blocks the
+    // other: each is advanced whenever its next slot is free.
+    ptx::setmaxnreg_dec<kPRegsControl>();
+    if (lane == 0) {
+      const uint64_t keep = ptx::l2_policy_evict_last();
+      const uint64_t once = ptx::l2_policy_evict_first();
+      ItemCursor<false> qc, kc;
+      qc.start(p);
+      kc.start(p);
+      ItemPlan qp, kp;
+      TileList ql, kl;
+      if (qc.valid(p)) {
+        qp = make_plan(p, qc.cur.item, qc.cur.head.x);
+        ql = make_list(p, qp, nullptr, nullptr);
+      }
+      if (kc.valid(p)) {
+        kp = make_plan(p, kc.cur.item, kc.cur.head.x);
+        kl = make_list(p, kp, nullptr, nullptr);
+      }
+      int qs = 0;      // sub-tile of the next Q tile
+      int t = 0;       // next Q tile
+      int kj = 0;      // next entry of the current K item
+      int e = 0;       // next entry of the K stream
+      while (kc.valid(p) && kl.n == 0) {  // (no item has an empty list; kept for safety)
+        kc.advance(p);
+        if (kc.valid(p)) {
+          kp = make_plan(p, kc.cur.item, kc.cur.head.x);
+          kl = make_list(p, kp, nullptr, nullptr);
+        }
+      }
+      uint64_t t_idle = 0;  // start of the current stretch without progress
+      uint32_t idle = 0;
+      bool failed = false;
+      while (qc.valid(p) || kc.valid(p)) {
+        bool moved = false;
+        if (qc.valid(p)) {
+          const int slot = t % NQ;
+          if (ptx::mbar_try_wait(&bar->q_empty[slot], ((t / NQ) & 1) ^ 1)) {
+            if (list_has(ql, qs, false)) {
+              const SubPlan& sp = qs ? qp.sp1 : qp.sp0;
+              ptx::mbar_arrive_expect_tx(&bar->q_full[slot], G::kTileBytes);
+              load_tile<D>(p, false, qc.cur.head.y, sq + slot * G::kTileBytes, &bar->q_full[slot], sp.qt * kTile,
+                           qp.bh, once);
+            } else {
+              ptx::mbar_arrive(&bar->q_full[slot]);  // no rows: an empty fill keeps the slot's phases in step
+            }
+            ++t;
+            if (++qs == 2) {
+              qs = 0;
+              qc.advance(p);
+              if (qc.valid(p)) {
+                qp = make_plan(p, qc.cur.item, qc.cur.head.x);
+                ql = make_list(p, qp, nullptr, nullptr);
+              }
+            }
+            moved = true;
+          }
+        }
+        if (kc.valid(p)) {
+          const int slot = e % KS;
+          if (ptx::mbar_try_wait(&bar->k_empty[slot], ((e / KS) & 1) ^ 1)) {
+            ptx::mbar_arrive_expect_tx(&bar->k_full[slot], G::kTileBytes);
+            load_tile<D>(p, true, kc.cur.head.y, sk + slot * G::kTileBytes, &bar->k_full[slot],
+                         list_kt(kl, kj) * kTile, kp.bh_kv, keep);
+            ++e;
+            if (++kj == kl.n) {
+              kj = 0;
+              do {
+                kc.advance(p);
+                if (kc.valid(p)) {
+                  kp = make_plan(p, kc.cur.item, kc.cur.head.x);
+                  kl = make_list(p, kp, nullptr, nullptr);
+                }
+              } while (kc.valid(p) && kl.n == 0);
+            }
+            moved = true;
+          }
+        }
+        if (moved) {
+          idle = 0;
+        } else if ((++idle & 63u) == 0) {
+          // bounded like every wait: give up after timeout_ns without progress
+          if (*abort_flag) break;
+          const uint64_t now = ptx::globaltimer_ns();
+          if (idle == 64) {
+            t_idle = now;
+          } else if (now - t_idle > p.timeout_ns) {
+            failed = true;
+            break;
+          }
+        }
+      }
+      if (failed) raise_error(p, bar, kErrProducer);
+      if (*abort_flag) {
+        uint64_t w0 = ptx::globaltimer_ns();
+        while (ptx::globaltimer_ns() - w0 < 2000000ull) { }
+      }
+    }
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ V producer
+    ptx::setmaxnreg_dec<kPRegsControl>();
+    if (lane == 0) {
+      const uint64_t keep = ptx::l2_policy_evict_last();
+      ItemCursor<false> c;
+      c.start(p);
+      int e = 0;
+      bool ok = true;
+      for (; ok && c.valid(p); c.advance(p)) {
+        const ItemPlan ip = make_plan(p, c.cur.item, c.cur.head.x);
+        const TileList L = make_list(p, ip, nullptr, nullptr);
+        for (int j = 0; j < L.n; ++j, ++e) {
+          const int slot = e % VS;
+          if (!ptx::mbar_wait(&bar->v_empty[slot], ((e / VS) & 1) ^ 1, p.timeout_ns, abort_flag)) {
+            raise_error(p, bar, kErrProducer);
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(&bar->v_full[slot], G::kTileBytes);
+          load_v_tile<D>(p, c.cur.head.y, sv + slot * G::kTileBytes, &bar->v_full[slot], list_kt(L, j) * kTile,
+                         ip.bh_kv, keep);
+        }
+      }
+      if (*abort_flag) {
+        uint64_t w0 = ptx::globaltimer_ns();
+        while (ptx::globaltimer_ns() - w0 < 2000000ull) { }
+      }
+    }
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Issuer s walks every entry e of the CTA's stream (both issuers release
+    // every K / V slot, the empty barriers counting 2) and, in ticket order
+    // 2e + s, issues the group P V(e-1) + S(e): the pending product of the
+    // previous entry (when s used it) and this entry's S (when s uses it).
+    // At an item boundary the group is the last P V of one item and the
+    // first S of the next.  The next item's first P V (accumulate = 0) needs
+    // that item's first P, which the softmax warps write only after reading
+    // O_s: waiting for P is waiting for O_s to be free.
+    ptx::setmaxnreg_dec<kPRegsControl>();
+    const int s = warp - 1;
+    auto wait_all = [&](uint64_t* b, uint32_t parity) {
+      return __all_sync(0xffffffffu, ptx::mbar_wait(b, parity, p.timeout_ns, abort_flag));
+    };
+    constexpr uint32_t tile4 = G::kTileBytes >> 4;  // descriptor start-address units
+    const uint32_t q4 = ptx::smem_addr(sq) >> 4;
+    const uint32_t k4 = ptx::smem_addr(sk) >> 4;
+    const uint32_t v4 = ptx::smem_addr(sv) >> 4;
+    const uint32_t s_tm = tmem + s * 128;
+    const uint32_t o_tm = tmem + 256 + s * 128;
+    bool ok = true, issued_any = false;
+    bool pend = false, pend_first = false, pend_last = false;
+    uint32_t pcount = 0;  // P tiles consumed
+    int e = 0;
+    ItemCursor<true> c;
+    c.start(p);
+    for (; ok && c.valid(p); c.advance(p)) {
+      const ItemPlan ip = make_plan(p, c.cur.item, c.cur.head.x);
+      const TileList L = make_list(p, ip, nullptr, nullptr);
+      int first_use, last_use;
+      use_bounds(L, s, &first_use, &last_use);
+      const int t = 2 * c.i + s;
+      const int qslot = t % NQ;
+      const uint32_t qpar = (t / NQ) & 1;
+      if (first_use < 0) {
+        // no rows in this sub-tile: take the slot's empty fill and hand it back
+        if (!wait_all(&bar->q_full[qslot], qpar)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) ptx::mbar_arrive(&bar->q_empty[qslot]);
+      }
+      for (int j = 0; j < L.n; ++j, ++e) {
+        const bool use = list_uses(L, j, s);
+        const int ks = e % KS;
+        const bool rel_v = e >= 1;
+        const int ve = e - 1;
+        if (rel_v && !wait_all(&bar->v_full[ve % VS], (ve / VS) & 1)) { ok = false; break; }
+        if (!wait_all(&bar->k_full[ks], (e / KS) & 1)) { ok = false; break; }
+        if (pend) {
+          if (!wait_all(&bar->p_full[s], pcount & 1)) { ok = false; break; }
+          ++pcount;
+          ptx::tc_fence_after();
+        }
+        if (use && j == first_use && !wait_all(&bar->q_full[qslot], qpar)) { ok = false; break; }
+        const uint32_t ticket = (uint32_t)(2 * e + s);
+        if (!__all_sync(0xffffffffu, mma_turn_wait(bar, ticket, p.timeout_ns, abort_flag))) { ok = false; break; }
+        if (ptx::elect_one()) {
+          if (pend) issue_pv<D>(o_tm, s_tm, v4 + (ve % VS) * tile4, !pend_first);
+          if (use) issue_qk<D>(s_tm, q4 + qslot * tile4, k4 + ks * tile4);
+        }
+        __syncwarp();
+        if (lane == 0) mma_turn_pass(bar, ticket);
+        if (use) {
+          ptx::mma_commit_elect(&bar->s_full[s]);
+          issued_any = true;
+        }
+        if (rel_v) ptx::mma_commit_elect(&bar->v_empty[ve % VS]);
+        ptx::mma_commit_elect(&bar->k_empty[ks]);
+        if (pend && pend_last) ptx::mma_commit_elect(&bar->o_full[s]);
+        if (use && j == last_use) ptx::mma_commit_elect(&bar->q_empty[qslot]);
+        pend = use;
+        pend_first = use && j == first_use;
+        pend_last = use && j == last_use;
+      }
+    }
+    if (ok && e >= 1) {
+      // the last entry: its V slot and this sub-tile's pending P V
+      const int ve = e - 1;
+      if (!wait_all(&bar->v_full[ve % VS], (ve / VS) & 1)) ok = false;
+      if (ok && pend) {
+        if (!wait_all(&bar->p_full[s], pcount & 1)) {
+          ok = false;
+        } else {
+          ++pcount;
+          ptx::tc_fence_after();
+          if (ptx::elect_one()) issue_pv<D>(o_tm, s_tm, v4 + (ve % VS) * tile4, !pend_first);
+          __syncwarp();
+          ptx::mma_commit_elect(&bar->o_full[s]);
+        }
+      }
+      if (ok) ptx::mma_commit_elect(&bar->v_empty[ve % VS]);
+    }
+    if (!ok) {
+      if (lane == 0) raise_error(p, bar, kErrMma);
+      if (issued_any) {
+        // wait (bounded) for the MMAs already issued before tensor memory is freed
+        ptx::mma_commit_elect(&bar->drain[s]);
+        ptx::mbar_wait_time_only(&bar->drain[s], 0, p.timeout_ns);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    ptx::setmaxnreg_inc<kPRegsSoftmax>();
+    const int s = (warp - 4) >> 2;
+    const int quarter = warp & 3;  // tensor-memory lane quarter this warp may access
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t s_tmem = tmem + lane_off + s * 128;
+    const uint32_t o_tmem = tmem + lane_off + 256 + s * 128;
+    const float sl2 = p.scale_log2;
+    uint32_t count = 0;  // S tiles of this sub-tile so far (all items)
+    int o_items = 0;     // items whose O_s has been read
+    bool ok = true;
+    ItemCursor<false> c;
+    c.start(p);
+    for (; ok && c.valid(p); c.advance(p)) {
+      c.prefetch_next(p);
+      const ItemPlan ip = make_plan(p, c.cur.item, c.cur.head.x);
+      const TileList L = make_list(p, ip, nullptr, nullptr);
+      const SubPlan sp = s ? ip.sp1 : ip.sp0;
+      const int64_t pos = (int64_t)sp.qt * kTile + row;
+      int64_t lo, hi;
+      row_interval(p.kind, c.cur.head.x, p.N, pos, &lo, &hi);
+      if (hi > p.N - 1) hi = p.N - 1;
+      const int64_t sink_hi = sink_last(p.sink_tokens, pos);  // sink keys [0, sink_hi]
+      float m = -INFINITY;  // running (stale) max of scaled scores, log2 domain
+      float l = 0.f;        // running sum of exp2(x - m)
+      for (int jj = 0; jj < L.n; ++jj) {
+        if (!list_uses(L, jj, s)) continue;
+        const int kt = list_kt(L, jj);
+        bool got = ptx::mbar_wait(&bar->s_full[s], count & 1, p.timeout_ns, abort_flag);
+        if (!__all_sync(0xffffffffu, got)) {
+          if (lane == 0) raise_error(p, bar, kErrSoftmax);
+          ok = false;
+          break;
+        }
+        ++count;
+        ptx::tc_fence_after();
+        float x[128];
+        ptx::tmem_ld32(s_tmem + 0, *reinterpret_cast<float(*)[32]>(&x[0]));
+        ptx::tmem_ld32(s_tmem + 32, *reinterpret_cast<float(*)[32]>(&x[32]));
+        ptx::tmem_ld32(s_tmem + 64, *reinterpret_cast<float(*)[32]>(&x[64]));
+        ptx::tmem_ld32(s_tmem + 96, *reinterpret_cast<float(*)[32]>(&x[96]));
+        ptx::tmem_wait_ld();
+        if (sub_partial(p, sp, kt)) {
+          // visible key columns of this row inside the tile: [c_lo, c_hi],
+          // and the sink keys of the tile: columns [0, c_s]
+          const int64_t k0 = (int64_t)kt * kTile;
+          const int c_lo = (int)(lo - k0 < -1 ? -1 : (lo - k0 > 128 ? 128 : lo - k0));
+          const int c_hi = (int)(hi - k0 < -1 ? -1 : (hi - k0 > 128 ? 128 : hi - k0));
+          const int c_s = (int)(sink_hi - k0 < -1 ? -1 : (sink_hi - k0 > 128 ? 128 : sink_hi - k0));
+          if (c_s < 0) {
+#pragma unroll
+            for (int cc = 0; cc < 128; ++cc)
+              if (cc < c_lo || cc > c_hi) x[cc] = -INFINITY;
+          } else {
+#pragma unroll
+            for (int cc = 0; cc < 128; ++cc)
+              if ((cc < c_lo || cc > c_hi) && cc > c_s) x[cc] = -INFINITY;
+          }
+        }
+        // P = exp2(s * scale * log2e - m) into tensor memory (the stale-max
+        // rule of attention_fwd.cu: m only guards against overflow)
+        float ts;
+        bool slow = __any_sync(0xffffffffu, m == -INFINITY);
+        if (!slow) {
+          ts = exp_to_tmem(x, sl2, m, s_tmem);
+          slow = __any_sync(0xffffffffu, !(ts <= kMaxTileSum));
+          if (slow) ptx::tmem_wait_st();
+        }
+        if (slow) {
+          const float m_new = fmaxf(m, row_max(x) * sl2);
+          const bool need_rescale = (m != -INFINITY) && (m_new > m);
+          if (m == -INFINITY) m = m_new;
+          if (__any_sync(0xffffffffu, need_rescale)) {
+            // O_s holds this item's products so far (its P V for the
+            // previous tile is done: S of this tile was committed after it)
+            const float alpha = need_rescale ? ptx::ex2(m - m_new) : 1.f;
+            rescale_o<D>(o_tmem, alpha);
+            if (need_rescale) {
+              l *= alpha;
+              m = m_new;
+            }
+          }
+          ts = exp_to_tmem(x, sl2, (m == -INFINITY) ? 0.f : m, s_tmem);
+        }
+        l += ts;
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&bar->p_full[s]);
+      }
+      if (!ok) break;
+
+      // ---------------------------------------------------------- epilogue
+      // While the tensor core runs this item's last P V and the next item's
+      // first S: wait for the P V, read O_s, write O / (l + exp(sink)) and
+      // the LSE in caller token order.
+      const bool has_o = list_has(L, s, false);
+      if (has_o) {
+        bool got = ptx::mbar_wait(&bar->o_full[s], o_items & 1, p.timeout_ns, abort_flag);
+        if (!__all_sync(0xffffffffu, got)) {
+          if (lane == 0) raise_error(p, bar, kErrEpilogue);
+          ok = false;
+          break;
+        }
+        ++o_items;
+        ptx::tc_fence_after();
+      }
+      const int h = c.cur.item.x % p.H;
+      const float b2 = p.sink ? __ldg(p.sink + h) * kLog2e : -INFINITY;
+      float o_scale, unused, lse_v;
+      finalize_row(m, l, -INFINITY, 0.f, b2, &o_scale, &unused, &lse_v);
+      const bool valid = pos < p.N;
+      const int64_t tok = valid ? token_of(p, c.cur.head.z, c.cur.head.w, pos) : 0;
+      const int64_t orow = ((int64_t)ip.bh * p.N + tok) * D;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 16) {
+        float ov[16];
+        if (has_o) {
+          ptx::tmem_ld16(o_tmem + c0, ov);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) ov[i] *= o_scale;
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) ov[i] = 0.f;
+        }
+        if (valid) {
+          if (OUT_F32) {
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.o) + orow + c0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
+          } else {
+            uint32_t pk[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) pk[i] = ptx::pack_bf16x2(ov[2 * i], ov[2 * i + 1]);
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + orow + c0);
+            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          }
+        }
+      }
+      if (valid && p.lse) p.lse[(int64_t)ip.bh * p.N + tok] = lse_v;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+size_t persist_smem_for() {
+  using G = Geo<D>;
+  return (size_t)(PGeo<D>::kQSlots + 2 * G::kStages) * G::kTileBytes + sizeof(PBarriers) + 1024;
+}
+
+template <int D, bool F32>
+cudaError_t launch_persist_one(const FwdParams& p, int grid, cudaStream_t stream) {
+  const size_t smem = persist_smem_for<D>();
+  auto kern = attention_persist_kernel<D, F32>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kPThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.after_prepass ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+}  // namespace
+
+size_t attention_persist_smem_bytes(int d) {
+  switch (d) {
+    case 32: return persist_smem_for<32>();
+    case 64: return persist_smem_for<64>();
+    case 80: return persist_smem_for<80>();
+    case 96: return persist_smem_for<96>();
+    case 128: return persist_smem_for<128>();
+    default: return 0;
+  }
+}
+
+cudaError_t launch_attention_persist(const FwdParams& p, int d, bool out_f32, int grid, cudaStream_t stream) {
+  if (p.n_items <= 0) return cudaSuccess;
+  if (grid > p.n_items) grid = p.n_items;
+#define MATTN_CASE(DD)                                                                          \
+  case DD:                                                                                      \
+    return out_f32 ? launch_persist_one<DD, true>(p, grid, stream) : launch_persist_one<DD, false>(p, grid, stream);
+  switch (d) {
+    MATTN_CASE(32)
+    MATTN_CASE(64)
+    MATTN_CASE(80)
+    MATTN_CASE(96)
+    MATTN_CASE(128)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef MATTN_CASE
+}
+
+}  // namespace mattn

@@ -203,6 +203,12 @@ cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream);
 cudaError_t launch_attention_sp(const FwdParams& p, int d, cudaStream_t stream);
 int attention_sp_key_tile(int d);
 
+// Persistent kernel for the interval masks (attention_persist.cu): `grid`
+// CTAs (one per SM), CTA c taking work items c, c + grid, ...; the work
+// items and parameters are those of launch_attention's paired schedule.
+cudaError_t launch_attention_persist(const FwdParams& p, int d, bool out_f32, int grid, cudaStream_t stream);
+size_t attention_persist_smem_bytes(int d);
+
 // Launchers (attention_fwd.cu).
 cudaError_t launch_attention(const FwdParams& p, int d, bool out_f32, cudaStream_t stream);
 size_t attention_smem_bytes(int d);

@@ -47,6 +47,9 @@ int cuda_fail(cudaError_t e, const char* what) {
   } while (0)
 
 std::atomic<unsigned long long> g_timeout_ns{0};
+// Test hook: an upper bound on the persistent kernel's grid (0 = one CTA per
+// SM), so that small problems still give each CTA many work items.
+std::atomic<int> g_persist_grid_cap{0};
 
 unsigned long long wait_timeout_ns() {
   unsigned long long t = g_timeout_ns.load();
@@ -79,6 +82,7 @@ struct Normalized {
   float scale;
   bool split;         // schedule: one query tile per CTA, key tiles dealt to two pipelines
   bool single;        // the single-pipeline kernel (head dim 256, or 128 on request)
+  bool persistent;    // the persistent kernel (interval masks, paired work items)
 };
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -90,7 +94,7 @@ int normalize(const mattn_mask_desc* desc, int B, int H, int N, int d, int dtype
               bool allow_block_tma = true) {
   if (!desc) return fail(MATTN_ERR_INVALID_ARG, "mask descriptor is NULL");
   if (desc->flags != 0 && desc->flags != MATTN_FLAG_SCHEDULE_PAIRED && desc->flags != MATTN_FLAG_SCHEDULE_SPLIT &&
-      desc->flags != MATTN_FLAG_SCHEDULE_SINGLE)
+      desc->flags != MATTN_FLAG_SCHEDULE_SINGLE && desc->flags != MATTN_FLAG_SCHEDULE_PERSISTENT)
     return fail(MATTN_ERR_INVALID_ARG, "flags must be 0 or one MATTN_FLAG_SCHEDULE_* flag (got %u)",
                 desc->flags);
   if (B < 1 || H < 1 || N < 1) return fail(MATTN_ERR_INVALID_ARG, "B, H, N must be >= 1 (got %d, %d, %d)", B, H, N);
@@ -213,6 +217,17 @@ int normalize(const mattn_mask_desc* desc, int B, int H, int N, int d, int dtype
     n.any_block_col_tma = false;
     n.split = true;
   }
+  // The persistent kernel: interval masks at head dim <= 128 (paired work
+  // items).  Chosen on request for now.
+  n.persistent = false;
+  if (desc->flags == MATTN_FLAG_SCHEDULE_PERSISTENT) {
+    if (n.kind == kBlockSparse)
+      return fail(MATTN_ERR_UNSUPPORTED, "the persistent schedule takes the interval masks (not block-sparse)");
+    if (need_data && d > 128)
+      return fail(MATTN_ERR_UNSUPPORTED, "the persistent schedule takes head dim <= 128 (got %d)", d);
+    n.persistent = need_data;
+    n.split = false;
+  }
   *out = std::move(n);
   return MATTN_OK;
 }
@@ -304,6 +319,7 @@ struct DeviceBuf {
 
 struct DeviceState {
   uint32_t* err = nullptr;
+  int sm_count = 0;
   DeviceBuf copy;      // reordered / converted q, k, v
   DeviceBuf host_io;   // mattn_fwd_host staging
   DeviceBuf dump;      // plan dump
@@ -331,6 +347,7 @@ int device_state(DeviceState** out) {
     if (major != 10 || minor != 3)
       return fail(MATTN_ERR_NO_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a", dev, major, minor);
     auto st = std::make_unique<DeviceState>();
+    MATTN_CUDA(cudaDeviceGetAttribute(&st->sm_count, cudaDevAttrMultiProcessorCount, dev), "SM count");
     MATTN_CUDA(cudaMalloc(&st->err, sizeof(uint32_t)), "cudaMalloc(error word)");
     MATTN_CUDA(cudaMemset(st->err, 0, sizeof(uint32_t)), "cudaMemset(error word)");
     it = g_devices.emplace(dev, std::move(st)).first;
@@ -636,7 +653,11 @@ int fwd_locked(const void* q, const void* k, const void* v, void* o, float* lse,
   p.out_f32 = dtype == MATTN_F32 ? 1 : 0;
   if (n.single)
     MATTN_CUDA(launch_attention_sp(p, d, stream), "attention launch (single pipeline)");
-  else
+  else if (n.persistent) {
+    const int cap = g_persist_grid_cap.load();
+    const int grid = (cap > 0 && cap < st->sm_count) ? cap : st->sm_count;
+    MATTN_CUDA(launch_attention_persist(p, d, dtype == MATTN_F32, grid, stream), "attention launch (persistent)");
+  } else
     MATTN_CUDA(launch_attention(p, d, dtype == MATTN_F32, stream), "attention launch");
   return MATTN_OK;
 }
@@ -748,6 +769,14 @@ int mattn_internal_fwd_wait_selftest(const void* q, const void* k, const void* v
                                      int N, int d, int dtype, const mattn_mask_desc* desc, void* stream) {
   std::lock_guard<std::mutex> lk(g_mutex);
   return fwd_locked(q, k, v, o, lse, B, H, H, N, d, dtype, desc, static_cast<cudaStream_t>(stream), 1);
+}
+
+// Test hook (not in the public header): caps the persistent kernel's grid
+// at `ctas` CTAs (0 restores one per SM).
+int mattn_internal_set_persist_grid(int ctas) {
+  if (ctas < 0) return fail(MATTN_ERR_INVALID_ARG, "ctas must be >= 0");
+  g_persist_grid_cap.store(ctas);
+  return MATTN_OK;
 }
 
 int mattn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,

@@ -111,6 +111,12 @@ typedef enum { MATTN_BF16 = 0, MATTN_F32 = 1 } mattn_dtype;
  * memory, so that the next key tile's Q K^T runs during the softmax of
  * this one.  Other token orders go through the reorder copy. */
 #define MATTN_FLAG_SCHEDULE_SINGLE 4u
+/* Interval masks (not MATTN_BLOCK_SPARSE), head dim <= 128: the PAIRED work
+ * items run on a persistent grid of one CTA per SM, each CTA walking its
+ * items back to back: the next item's Q tiles load and its first Q K^T runs
+ * while the current item's output is written, instead of every CTA paying
+ * its own set-up and epilogue. */
+#define MATTN_FLAG_SCHEDULE_PERSISTENT 8u
 
 typedef struct {
   int32_t kind;              /* mattn_kind                                                */

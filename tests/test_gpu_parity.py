@@ -54,7 +54,8 @@ def _subset(spec, hs):
         blk = b[hs] if b.ndim == 3 and b.shape[0] > 1 else b
     sink = None if spec.sink is None else np.asarray(spec.sink)[hs]
     return MaskSpec(spec.kind, pick(spec.head_param), perm=pick(spec.perm),
-                    perm_grid=pick(spec.perm_grid), block=blk, sink=sink)
+                    perm_grid=pick(spec.perm_grid), block=blk, sink=sink,
+                    sink_tokens=getattr(spec, "sink_tokens", 0))
 
 
 def check(q, k, v, spec, rows=None, heads=None, tag="", schedule=None):

@@ -1,0 +1,184 @@
+"""GPU parity of the persistent schedule (MATTN_FLAG_SCHEDULE_PERSISTENT):
+one CTA per SM walking paired work items back to back, for the interval
+masks.
+
+Each case is checked twice:
+- against the fp64 oracle with the tolerances of the other parity tests
+  (max abs 2e-2, rel L2 5e-3 on O; LSE 1e-3, plus the bf16-rounding bound
+  for fp32 inputs);
+- against the one-item-per-CTA paired kernel, bit for bit: a work item's
+  arithmetic (products, softmax, accumulation order, epilogue) is the same
+  in both kernels, only the schedule differs.
+
+Small problems have fewer work items than SMs, so most cases also run with
+the grid capped at a few CTAs (a test hook), which gives every CTA many
+items: Q slots wrap several times, the K/V rings run across item
+boundaries, and O accumulators are reused item after item.
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from workloads import (MaskSpec, WORKLOADS, block2x2_order, column_major_order,  # noqa: E402
+                       make_mask, make_qkv, make_workload_inputs, random_order)
+
+pytestmark = pytest.mark.gpu
+
+mattn = pytest.importorskip("block_sparse_attention_masked_gb300")
+
+from test_gpu_parity import check  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import os
+
+    if not os.path.exists(mattn.LIB_PATH):
+        from block_sparse_attention_masked_gb300 import build
+
+        build.build()
+    mattn.lib()
+
+
+@pytest.fixture
+def grid_cap():
+    """Sets the persistent grid cap for one test and restores one CTA per SM."""
+    L = mattn.lib()
+    L.mattn_internal_set_persist_grid.argtypes = [ctypes.c_int]
+
+    def set_cap(n):
+        assert L.mattn_internal_set_persist_grid(n) == 0
+
+    yield set_cap
+    L.mattn_internal_set_persist_grid(0)
+
+
+def _same_as_paired(q, k, v, spec, tag):
+    B, H, N, d = q.shape
+    o_p, l_p = mattn.attention(q, k, v, mattn.prepare(spec, H, N, schedule="persistent"))
+    o_r, l_r = mattn.attention(q, k, v, mattn.prepare(spec, H, N, schedule="paired"))
+    torch.cuda.synchronize()
+    rc, word = mattn.device_status()
+    assert rc == 0, f"{tag}: device error word {word:#x}"
+    assert torch.equal(o_p, o_r), f"{tag}: O differs from the paired kernel"
+    assert torch.equal(l_p, l_r), f"{tag}: LSE differs from the paired kernel"
+
+
+def _specs(H, n):
+    rng = np.random.default_rng(n + H)
+    return [
+        MaskSpec("full", [0] * H),
+        MaskSpec("chunk", [int(x) for x in rng.choice([64, 100, 128, 256, 512], H)]),
+        MaskSpec("sliding", [int(x) for x in rng.choice([1, 37, 128, 200, 256], H)], sink=rng.standard_normal(H)),
+        MaskSpec("causal_window", [int(x) for x in rng.choice([1, 64, 300, 512, 1024], H)], sink=rng.standard_normal(H)),
+        MaskSpec("causal_window", [int(x) for x in rng.choice([60, 128, 572], H)], sink_tokens=4),
+    ]
+
+
+@pytest.mark.parametrize("cap", [0, 3])
+@pytest.mark.parametrize("d", [32, 64, 80, 96, 128])
+@pytest.mark.parametrize("n", [256, 1000, 2200])
+def test_interval_kinds(d, n, cap, grid_cap):
+    """Every interval kind with per-head parameters, ragged N (a partial last
+    query tile, and at 1000 / 2200 an odd tile count whose last pair has one
+    empty sub-tile), with and without a capped grid."""
+    grid_cap(cap)
+    H = 3
+    q, k, v = make_qkv(2, H, n, d, "bf16", 1.0, seed=d * 7 + n, device="cuda")
+    for spec in _specs(H, n):
+        tag = f"{spec.kind} d{d} n{n} cap{cap}"
+        check(q, k, v, spec, tag=tag, schedule="persistent")
+        _same_as_paired(q, k, v, spec, tag)
+
+
+@pytest.mark.parametrize("cap", [0, 2])
+def test_token_orders(cap, grid_cap):
+    """Column-major heads (strided TMA views), the two 2x2-block orders (5D
+    views), an explicit order and fp32 inputs (both through the reorder
+    pre-pass, the kernel then launched as its programmatic dependent)."""
+    grid_cap(cap)
+    rows, cols = 64, 64
+    n, d = rows * cols, 80
+    q, k, v = make_qkv(1, 4, n, d, "bf16", 0.5, seed=5, device="cuda")
+    cm = column_major_order(rows, cols)
+    spec = MaskSpec("sliding", [128, 128, 90, 300],
+                    perm=[None, cm, block2x2_order(rows, cols), block2x2_order(rows, cols, by_columns=True)],
+                    perm_grid=[None, (rows, cols), (rows, cols, "block2x2_row"), (rows, cols, "block2x2_col")])
+    check(q, k, v, spec, tag="grid orders", schedule="persistent")
+    _same_as_paired(q, k, v, spec, "grid orders")
+    rng = np.random.default_rng(9)
+    spec2 = MaskSpec("chunk", [256, 100, 256, 64], perm=[random_order(n, 3), None, cm, None],
+                     sink=rng.standard_normal(4))
+    check(q, k, v, spec2, tag="explicit order", schedule="persistent")
+    _same_as_paired(q, k, v, spec2, "explicit order")
+    qf, kf, vf = make_qkv(1, 2, 1000, 64, "f32", 1.0, seed=6, device="cuda")
+    spec3 = MaskSpec("sliding", [32, 100])
+    check(qf, kf, vf, spec3, tag="fp32", schedule="persistent")
+    _same_as_paired(qf, kf, vf, spec3, "fp32")
+
+
+@pytest.mark.parametrize("cap", [0, 5])
+def test_grouped_query_heads(cap, grid_cap):
+    """Grouped-query attention: 8 query heads sharing 2 K/V heads."""
+    grid_cap(cap)
+    from oracle import dense
+
+    B, H, Hkv, n, d = 1, 8, 2, 3000, 128
+    g = torch.Generator(device="cuda").manual_seed(11)
+    q = torch.randn((B, H, n, d), generator=g, device="cuda").to(torch.bfloat16)
+    k = torch.randn((B, Hkv, n, d), generator=g, device="cuda").to(torch.bfloat16)
+    v = torch.randn((B, Hkv, n, d), generator=g, device="cuda").to(torch.bfloat16)
+    spec = MaskSpec("causal_window", [576] * H, sink=np.linspace(-1, 1, H))
+    o, lse = mattn.attention(q, k, v, mattn.prepare(spec, H, n, schedule="persistent"))
+    o_r, l_r = mattn.attention(q, k, v, mattn.prepare(spec, H, n, schedule="paired"))
+    torch.cuda.synchronize()
+    assert mattn.device_status()[0] == 0
+    assert torch.equal(o, o_r) and torch.equal(lse, l_r)
+    rows = np.unique(np.r_[0, 127, 128, 575, 576, n - 1, np.random.default_rng(0).choice(n, 40, replace=False)])
+    f = lambda t: t.float().cpu().numpy()  # noqa: E731
+    ref_o, ref_l = dense.attention(f(q), f(k), f(v), spec, rows=rows)
+    got = f(o)[0][:, rows]
+    assert np.abs(got - ref_o).max() <= 2e-2
+    assert np.linalg.norm(got - ref_o) / np.linalg.norm(ref_o) <= 5e-3
+    assert np.abs(f(lse)[0][:, rows] - ref_l).max() <= 1e-3
+
+
+@pytest.mark.parametrize("mask", ["sliding256_rowcol", "chunk512", "sliding256_blocks"])
+def test_vit16384_full_size(mask):
+    """The 16,384-token ViT layer (B1 H16 d80) at full size, in the launch
+    configuration the benchmark times: sampled heads (raster, column-major
+    and 2x2-block heads) against the oracle on sampled rows, all heads equal
+    to the paired kernel bit for bit."""
+    wl = WORKLOADS["vit16384"]
+    q, k, v = make_workload_inputs(wl, seed=0, device="cuda")
+    spec = make_mask(wl, mask, seed=0)
+    rng = np.random.default_rng(1)
+    rows = np.unique(np.r_[0, 255, 256, 8191, wl.N - 1, rng.choice(wl.N, 48, replace=False)])
+    check(q, k, v, spec, rows=rows, heads=[(0, 0), (0, 5), (0, 8), (0, 15)], tag=mask, schedule="persistent")
+    _same_as_paired(q, k, v, spec, mask)
+
+
+def test_causal_windows_with_sink_full_size():
+    """The head-wise causal-window LM layer (B1 H16 L4096 d128, windows
+    512..4096, sink logits) at full size."""
+    wl = WORKLOADS["causal4096"]
+    q, k, v = make_workload_inputs(wl, seed=0, device="cuda")
+    spec = make_mask(wl, "causal_window_sink", seed=0)
+    rows = np.unique(np.r_[0, 511, 512, 2047, 2048, 4095, np.random.default_rng(2).choice(4096, 64, replace=False)])
+    check(q, k, v, spec, rows=rows, tag="causal4096", schedule="persistent")
+    _same_as_paired(q, k, v, spec, "causal4096")
+
+
+def test_rejects_block_sparse():
+    from workloads import bernoulli_causal_blocks
+
+    spec = MaskSpec("block", [128, 128], block=bernoulli_causal_blocks(2, 4, 0))
+    q, k, v = make_qkv(1, 2, 512, 64, "bf16", 1.0, seed=0, device="cuda")
+    with pytest.raises(RuntimeError, match="persistent"):
+        mattn.attention(q, k, v, mattn.prepare(spec, 2, 512, schedule="persistent"))
