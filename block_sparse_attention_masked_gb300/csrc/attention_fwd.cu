@@ -471,15 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
         const int c_hi = (int)(hi - k0 < -1 ? -1 : (hi - k0 > 128 ? 128 : hi - k0));
         // and the sink keys of the tile: columns [0, c_s]
         const int c_s = (int)(sink_hi - k0 < -1 ? -1 : (sink_hi - k0 > 128 ? 128 : sink_hi - k0));
-        if (c_s < 0) {
-#pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c < c_lo || c > c_hi) x[c] = -INFINITY;
-        } else {
-#pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if ((c < c_lo || c > c_hi) && c > c_s) x[c] = -INFINITY;
-        }
+        mask_row(x, c_lo, c_hi, c_s);
       }
       // P = exp2(s * scale * log2e - m) into tensor memory.  tcgen05.ld / st
       // are warp-collective, so every branch below is taken by whole warps

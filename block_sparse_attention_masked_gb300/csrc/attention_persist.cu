@@ -80,61 +80,82 @@ struct PBarriers {
   uint32_t mma_turn;       // ticket of the MMA group that may be issued next
 };
 
-// One work item as every role reads it: the item and its head's table row.
-struct ItemRef {
-  int2 item;
-  int4 head;  // param, load mode, store mode, explicit-order row
+// A work item as every role reads it: the plan the host worked out for it
+// (the layout of kPersistItemInt4 in kernel_params.h), no division needed.
+struct PItem {
+  ItemPlan ip;
+  TileList L;
+  int load, store, perm_row;
+  int first0, last0, first1, last1;  // first and last entries each sub-tile uses (-1: none)
+  __device__ __forceinline__ int first(int s) const { return s ? first1 : first0; }
+  __device__ __forceinline__ int last(int s) const { return s ? last1 : last0; }
 };
 
-__device__ __forceinline__ ItemRef load_item(const FwdParams& p, int it) {
-  ItemRef r;
-  r.item = __ldg(p.items + it);
-  r.head = __ldg(reinterpret_cast<const int4*>(p.head_info) + r.item.x % p.H);
+__device__ __forceinline__ const int4* pitem_ptr(const FwdParams& p, int it) {
+  return p.pitems + (size_t)it * kPersistItemInt4;
+}
+
+// Pulls work item `it`'s descriptor into this SM's L1 ahead of its use.
+__device__ __forceinline__ void prefetch_pitem(const FwdParams& p, int it) {
+  if (it < p.n_items) {
+    ptx::prefetch_l1(pitem_ptr(p, it));
+    ptx::prefetch_l1(pitem_ptr(p, it) + kPersistItemInt4 - 1);
+  }
+}
+
+__device__ __forceinline__ PItem load_pitem(const FwdParams& p, int it) {
+  const int4* d = pitem_ptr(p, it);
+  const int4 a = __ldg(d + 0), b = __ldg(d + 1), c = __ldg(d + 2);
+  const int4 f = __ldg(d + 3), g = __ldg(d + 4), u = __ldg(d + 5);
+  PItem r;
+  r.ip.bh = a.x;
+  r.ip.h = a.y;
+  r.ip.b = a.z;
+  r.ip.bh_kv = a.z * p.H_kv + a.y / p.kv_group;
+  r.ip.sp0.qt = a.w;
+  r.ip.sp1.qt = a.w + 1;
+  r.ip.sp0.rows = (int64_t)a.w * kTile < p.N;
+  r.ip.sp1.rows = (int64_t)(a.w + 1) * kTile < p.N;
+  r.ip.sp0.r.lo = c.x; r.ip.sp0.r.hi = c.y; r.ip.sp0.r.flo = f.x; r.ip.sp0.r.fhi = f.y;
+  r.ip.sp1.r.lo = c.z; r.ip.sp1.r.hi = c.w; r.ip.sp1.r.flo = f.z; r.ip.sp1.r.fhi = f.w;
+  r.ip.sp0.ns = g.x;
+  r.ip.sp1.ns = g.y;
+  r.ip.sp0.param = r.ip.sp1.param = b.w;
+  r.ip.sp0.ktmax = r.ip.sp1.ktmax = 0;  // block kind only
+  r.L.n = b.x;
+  r.L.lo = b.y;
+  r.L.na = b.z;
+  r.L.lo0 = c.x; r.L.hi0 = c.y; r.L.lo1 = c.z; r.L.hi1 = c.w;
+  r.L.ns0 = g.x; r.L.ns1 = g.y;
+  r.L.use_n0 = r.L.use_n1 = 0;
+  r.L.e = nullptr;
+  r.L.block = false;
+  r.load = g.z & 0xff;
+  r.store = g.z >> 8;
+  r.perm_row = g.w;
+  r.first0 = u.x; r.last0 = u.y;
+  r.first1 = u.z; r.last1 = u.w;
   return r;
 }
 
-// The CTA's items it = blockIdx.x + i * gridDim.x.  With kPrefetch the next
-// item's table entries are loaded into registers while the current one is
-// worked on (the MMA issuers, for which an item boundary is on the critical
-// path); the softmax warps, short of registers, only pull the next item's
-// entry into L1 (prefetch_next), and the producers run ahead of everyone.
-template <bool kPrefetch>
-struct ItemCursor {
-  int it, i;
-  ItemRef cur, nxt;
-  __device__ __forceinline__ void start(const FwdParams& p) {
-    it = blockIdx.x;
-    i = 0;
-    if (it < p.n_items) cur = load_item(p, it);
-    if (kPrefetch && it + (int)gridDim.x < p.n_items) nxt = load_item(p, it + gridDim.x);
-  }
-  __device__ __forceinline__ bool valid(const FwdParams& p) const { return it < p.n_items; }
-  __device__ __forceinline__ void prefetch_next(const FwdParams& p) const {
-    if (it + (int)gridDim.x < p.n_items) ptx::prefetch_l1(p.items + it + gridDim.x);
-  }
-  __device__ __forceinline__ void advance(const FwdParams& p) {
-    it += gridDim.x;
-    ++i;
-    if (kPrefetch) {
-      cur = nxt;
-      if (it + (int)gridDim.x < p.n_items) nxt = load_item(p, it + gridDim.x);
-    } else if (it < p.n_items) {
-      cur = load_item(p, it);
-    }
-  }
-};
-
-// Entry indices of the first and last entries sub-tile s uses (interval
-// kinds: one contiguous range of key tiles plus, with sink tokens, a
-// leading segment of sink tiles).
-__device__ __forceinline__ void use_bounds(const TileList& L, int s, int* first, int* last) {
-  *first = -1;
-  *last = -1;
-  for (int j = 0; j < L.n; ++j) {
-    if (list_uses(L, j, s)) {
-      if (*first < 0) *first = j;
-      *last = j;
-    }
+// Visible key interval [lo, hi] of query position pos in 32-bit arithmetic
+// (N <= 2^30): the rule of plan_rules.h's row_interval with the parameter
+// clamped to N, which leaves the interval clipped to [0, N - 1] unchanged.
+__device__ __forceinline__ void row_interval32(int kind, int param, int n, int pos, int* lo, int* hi) {
+  const int w = param < n ? param : n;
+  if (kind == kChunk) {
+    const int c0 = (pos / w) * w;
+    *lo = c0;
+    *hi = c0 + w - 1;
+  } else if (kind == kSliding) {
+    *lo = pos - w;
+    *hi = pos + w;
+  } else if (kind == kCausalWindow) {
+    *lo = pos - w + 1;
+    *hi = pos;
+  } else {
+    *lo = 0;
+    *hi = n - 1;
   }
 }
 
@@ -194,79 +215,65 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
     // Two streams served in turn by one thread: the Q tiles (slot t % NQ,
     // free once the S products of Q tile t - NQ are done) and the K tiles of
     // the concatenated key-tile lists (ring slot e % KS).  Neither blocks the
-    // other: each is advanced whenever its next slot is free.
+    // other: each is advanced whenever its next slot is free, polled with the
+    // non-blocking test_wait (a try_wait would suspend the thread on a slot
+    // that stays busy while the other stream's slot frees up).
     ptx::setmaxnreg_dec<kPRegsControl>();
     if (lane == 0) {
       const uint64_t keep = ptx::l2_policy_evict_last();
       const uint64_t once = ptx::l2_policy_evict_first();
-      ItemCursor<false> qc, kc;
-      qc.start(p);
-      kc.start(p);
-      ItemPlan qp, kp;
-      TileList ql, kl;
-      if (qc.valid(p)) {
-        qp = make_plan(p, qc.cur.item, qc.cur.head.x);
-        ql = make_list(p, qp, nullptr, nullptr);
-      }
-      if (kc.valid(p)) {
-        kp = make_plan(p, kc.cur.item, kc.cur.head.x);
-        kl = make_list(p, kp, nullptr, nullptr);
-      }
+      int qit = blockIdx.x, kit = blockIdx.x;  // items of the Q and K streams
+      PItem qi, ki;
+      if (qit < p.n_items) qi = load_pitem(p, qit);
+      if (kit < p.n_items) ki = load_pitem(p, kit);
+      prefetch_pitem(p, qit + gridDim.x);
       int qs = 0;      // sub-tile of the next Q tile
       int t = 0;       // next Q tile
       int kj = 0;      // next entry of the current K item
       int e = 0;       // next entry of the K stream
-      while (kc.valid(p) && kl.n == 0) {  // (no item has an empty list; kept for safety)
-        kc.advance(p);
-        if (kc.valid(p)) {
-          kp = make_plan(p, kc.cur.item, kc.cur.head.x);
-          kl = make_list(p, kp, nullptr, nullptr);
-        }
+      while (kit < p.n_items && ki.L.n == 0) {  // (no item has an empty list; kept for safety)
+        kit += gridDim.x;
+        if (kit < p.n_items) ki = load_pitem(p, kit);
       }
       uint64_t t_idle = 0;  // start of the current stretch without progress
       uint32_t idle = 0;
       bool failed = false;
-      while (qc.valid(p) || kc.valid(p)) {
+      while (qit < p.n_items || kit < p.n_items) {
         bool moved = false;
-        if (qc.valid(p)) {
+        if (kit < p.n_items) {
+          const int slot = e % KS;
+          if (ptx::mbar_test_wait(&bar->k_empty[slot], ((e / KS) & 1) ^ 1)) {
+            ptx::mbar_arrive_expect_tx(&bar->k_full[slot], G::kTileBytes);
+            load_tile<D>(p, true, ki.load, sk + slot * G::kTileBytes, &bar->k_full[slot], list_kt(ki.L, kj) * kTile,
+                         ki.ip.bh_kv, keep);
+            ++e;
+            if (++kj == ki.L.n) {
+              kj = 0;
+              do {
+                kit += gridDim.x;
+                if (kit < p.n_items) ki = load_pitem(p, kit);
+              } while (kit < p.n_items && ki.L.n == 0);
+            }
+            moved = true;
+          }
+        }
+        if (qit < p.n_items) {
           const int slot = t % NQ;
-          if (ptx::mbar_try_wait(&bar->q_empty[slot], ((t / NQ) & 1) ^ 1)) {
-            if (list_has(ql, qs, false)) {
-              const SubPlan& sp = qs ? qp.sp1 : qp.sp0;
+          if (ptx::mbar_test_wait(&bar->q_empty[slot], ((t / NQ) & 1) ^ 1)) {
+            if (qi.first(qs) >= 0) {
+              const SubPlan& sp = qs ? qi.ip.sp1 : qi.ip.sp0;
               ptx::mbar_arrive_expect_tx(&bar->q_full[slot], G::kTileBytes);
-              load_tile<D>(p, false, qc.cur.head.y, sq + slot * G::kTileBytes, &bar->q_full[slot], sp.qt * kTile,
-                           qp.bh, once);
+              load_tile<D>(p, false, qi.load, sq + slot * G::kTileBytes, &bar->q_full[slot], sp.qt * kTile,
+                           qi.ip.bh, once);
             } else {
               ptx::mbar_arrive(&bar->q_full[slot]);  // no rows: an empty fill keeps the slot's phases in step
             }
             ++t;
             if (++qs == 2) {
               qs = 0;
-              qc.advance(p);
-              if (qc.valid(p)) {
-                qp = make_plan(p, qc.cur.item, qc.cur.head.x);
-                ql = make_list(p, qp, nullptr, nullptr);
-              }
-            }
-            moved = true;
-          }
-        }
-        if (kc.valid(p)) {
-          const int slot = e % KS;
-          if (ptx::mbar_try_wait(&bar->k_empty[slot], ((e / KS) & 1) ^ 1)) {
-            ptx::mbar_arrive_expect_tx(&bar->k_full[slot], G::kTileBytes);
-            load_tile<D>(p, true, kc.cur.head.y, sk + slot * G::kTileBytes, &bar->k_full[slot],
-                         list_kt(kl, kj) * kTile, kp.bh_kv, keep);
-            ++e;
-            if (++kj == kl.n) {
-              kj = 0;
-              do {
-                kc.advance(p);
-                if (kc.valid(p)) {
-                  kp = make_plan(p, kc.cur.item, kc.cur.head.x);
-                  kl = make_list(p, kp, nullptr, nullptr);
-                }
-              } while (kc.valid(p) && kl.n == 0);
+              qit += gridDim.x;
+              if (qit < p.n_items) qi = load_pitem(p, qit);
+              prefetch_pitem(p, qit + gridDim.x);
             }
             moved = true;
           }
@@ -296,14 +303,12 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
     ptx::setmaxnreg_dec<kPRegsControl>();
     if (lane == 0) {
       const uint64_t keep = ptx::l2_policy_evict_last();
-      ItemCursor<false> c;
-      c.start(p);
       int e = 0;
       bool ok = true;
-      for (; ok && c.valid(p); c.advance(p)) {
-        const ItemPlan ip = make_plan(p, c.cur.item, c.cur.head.x);
-        const TileList L = make_list(p, ip, nullptr, nullptr);
-        for (int j = 0; j < L.n; ++j, ++e) {
+      for (int it = blockIdx.x; ok && it < p.n_items; it += gridDim.x) {
+        const PItem pi = load_pitem(p, it);
+        prefetch_pitem(p, it + gridDim.x);
+        for (int j = 0; j < pi.L.n; ++j, ++e) {
           const int slot = e % VS;
           if (!ptx::mbar_wait(&bar->v_empty[slot], ((e / VS) & 1) ^ 1, p.timeout_ns, abort_flag)) {
             raise_error(p, bar, kErrProducer);
@@ -311,8 +316,8 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
             break;
           }
           ptx::mbar_arrive_expect_tx(&bar->v_full[slot], G::kTileBytes);
-          load_v_tile<D>(p, c.cur.head.y, sv + slot * G::kTileBytes, &bar->v_full[slot], list_kt(L, j) * kTile,
-                         ip.bh_kv, keep);
+          load_v_tile<D>(p, pi.load, sv + slot * G::kTileBytes, &bar->v_full[slot], list_kt(pi.L, j) * kTile,
+                         pi.ip.bh_kv, keep);
         }
       }
       if (*abort_flag) {
@@ -345,14 +350,13 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
     bool pend = false, pend_first = false, pend_last = false;
     uint32_t pcount = 0;  // P tiles consumed
     int e = 0;
-    ItemCursor<true> c;
-    c.start(p);
-    for (; ok && c.valid(p); c.advance(p)) {
-      const ItemPlan ip = make_plan(p, c.cur.item, c.cur.head.x);
-      const TileList L = make_list(p, ip, nullptr, nullptr);
-      int first_use, last_use;
-      use_bounds(L, s, &first_use, &last_use);
-      const int t = 2 * c.i + s;
+    int i = 0;  // the CTA's item count so far
+    for (int it = blockIdx.x; ok && it < p.n_items; it += gridDim.x, ++i) {
+      const PItem pi = load_pitem(p, it);
+      prefetch_pitem(p, it + gridDim.x);
+      const TileList& L = pi.L;
+      const int first_use = pi.first(s), last_use = pi.last(s);
+      const int t = 2 * i + s;
       const int qslot = t % NQ;
       const uint32_t qpar = (t / NQ) & 1;
       if (first_use < 0) {
@@ -435,18 +439,16 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
     uint32_t count = 0;  // S tiles of this sub-tile so far (all items)
     int o_items = 0;     // items whose O_s has been read
     bool ok = true;
-    ItemCursor<false> c;
-    c.start(p);
-    for (; ok && c.valid(p); c.advance(p)) {
-      c.prefetch_next(p);
-      const ItemPlan ip = make_plan(p, c.cur.item, c.cur.head.x);
-      const TileList L = make_list(p, ip, nullptr, nullptr);
-      const SubPlan sp = s ? ip.sp1 : ip.sp0;
-      const int64_t pos = (int64_t)sp.qt * kTile + row;
-      int64_t lo, hi;
-      row_interval(p.kind, c.cur.head.x, p.N, pos, &lo, &hi);
+    for (int it = blockIdx.x; ok && it < p.n_items; it += gridDim.x) {
+      const PItem pi = load_pitem(p, it);
+      prefetch_pitem(p, it + gridDim.x);
+      const TileList& L = pi.L;
+      const SubPlan& sp = s ? pi.ip.sp1 : pi.ip.sp0;
+      const int pos = sp.qt * kTile + row;
+      int lo, hi;
+      row_interval32(p.kind, sp.param, p.N, pos, &lo, &hi);
       if (hi > p.N - 1) hi = p.N - 1;
-      const int64_t sink_hi = sink_last(p.sink_tokens, pos);  // sink keys [0, sink_hi]
+      const int sink_hi = (int)sink_last(p.sink_tokens, pos);  // sink keys [0, sink_hi]
       float m = -INFINITY;  // running (stale) max of scaled scores, log2 domain
       float l = 0.f;        // running sum of exp2(x - m)
       for (int jj = 0; jj < L.n; ++jj) {
@@ -469,19 +471,11 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
         if (sub_partial(p, sp, kt)) {
           // visible key columns of this row inside the tile: [c_lo, c_hi],
           // and the sink keys of the tile: columns [0, c_s]
-          const int64_t k0 = (int64_t)kt * kTile;
-          const int c_lo = (int)(lo - k0 < -1 ? -1 : (lo - k0 > 128 ? 128 : lo - k0));
-          const int c_hi = (int)(hi - k0 < -1 ? -1 : (hi - k0 > 128 ? 128 : hi - k0));
-          const int c_s = (int)(sink_hi - k0 < -1 ? -1 : (sink_hi - k0 > 128 ? 128 : sink_hi - k0));
-          if (c_s < 0) {
-#pragma unroll
-            for (int cc = 0; cc < 128; ++cc)
-              if (cc < c_lo || cc > c_hi) x[cc] = -INFINITY;
-          } else {
-#pragma unroll
-            for (int cc = 0; cc < 128; ++cc)
-              if ((cc < c_lo || cc > c_hi) && cc > c_s) x[cc] = -INFINITY;
-          }
+          const int k0 = kt * kTile;
+          const int c_lo = min(max(lo - k0, -1), 128);
+          const int c_hi = min(max(hi - k0, -1), 128);
+          const int c_s = min(max(sink_hi - k0, -1), 128);
+          mask_row(x, c_lo, c_hi, c_s);
         }
         // P = exp2(s * scale * log2e - m) into tensor memory (the stale-max
         // rule of attention_fwd.cu: m only guards against overflow)
@@ -530,13 +524,12 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
         ++o_items;
         ptx::tc_fence_after();
       }
-      const int h = c.cur.item.x % p.H;
-      const float b2 = p.sink ? __ldg(p.sink + h) * kLog2e : -INFINITY;
+      const float b2 = p.sink ? __ldg(p.sink + pi.ip.h) * kLog2e : -INFINITY;
       float o_scale, unused, lse_v;
       finalize_row(m, l, -INFINITY, 0.f, b2, &o_scale, &unused, &lse_v);
       const bool valid = pos < p.N;
-      const int64_t tok = valid ? token_of(p, c.cur.head.z, c.cur.head.w, pos) : 0;
-      const int64_t orow = ((int64_t)ip.bh * p.N + tok) * D;
+      const int64_t tok = valid ? token_of(p, pi.store, pi.perm_row, pos) : 0;
+      const int64_t orow = ((int64_t)pi.ip.bh * p.N + tok) * D;
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 16) {
         float ov[16];
@@ -564,7 +557,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
           }
         }
       }
-      if (valid && p.lse) p.lse[(int64_t)ip.bh * p.N + tok] = lse_v;
+      if (valid && p.lse) p.lse[(int64_t)pi.ip.bh * p.N + tok] = lse_v;
     }
   }
 

@@ -143,23 +143,7 @@ __device__ __forceinline__ TileList make_list(const FwdParams& p, const ItemPlan
     L.n = block_counts[0];
     L.lo = 0;
   } else {
-    const bool e0 = L.lo0 <= L.hi0, e1 = L.lo1 <= L.hi1;
-    L.lo = e0 ? (e1 ? min(L.lo0, L.lo1) : L.lo0) : L.lo1;
-    int hi = e0 ? (e1 ? max(L.hi0, L.hi1) : L.hi0) : L.hi1;
-    L.n = (e0 || e1) ? hi - L.lo + 1 : 0;
-    // sink tiles: a segment 0 .. ns - 1 before the window's tiles, or one
-    // segment 0 .. hi when they meet
-    const int ns = max(L.ns0, L.ns1);
-    if (ns > 0 && L.n > 0) {
-      if (ns >= L.lo) {
-        hi = max(hi, ns - 1);
-        L.lo = 0;
-        L.n = hi + 1;
-      } else {
-        L.na = ns;
-        L.n += ns;
-      }
-    }
+    pair_list_span(L.lo0, L.hi0, L.lo1, L.hi1, L.ns0, L.ns1, &L.lo, &L.n, &L.na);
   }
   return L;
 }
@@ -336,6 +320,35 @@ __device__ __forceinline__ float exp_to_tmem(const float (&x)[128], float sl2, f
   }
   const float2 a = ptx::fadd2(acc[0], acc[1]);
   return a.x + a.y;
+}
+
+// Bits of the 32 columns [32g, 32g + 31] inside [lo, hi] (column indices of
+// a 128-column tile; lo > hi: none).
+__device__ __forceinline__ uint32_t range_bits(int g, int lo, int hi) {
+  const int a = lo - 32 * g, b = hi - 32 * g;
+  if (b < 0 || a > 31 || a > b) return 0u;
+  const int a0 = a < 0 ? 0 : a, b0 = b > 31 ? 31 : b;
+  return (0xffffffffu >> (31 - b0)) & (0xffffffffu << a0);
+}
+
+// Boundary mask of one row of a PARTIAL tile: x[c] = -inf for the key
+// columns c of the 128-key tile outside this row's visible interval
+// [c_lo, c_hi] and outside its sink columns [0, c_s] (c_s < 0: none).
+// Each 32-column group gets a visibility bit mask; a column's bit, sign-
+// extended to a full word, selects between x and -inf bitwise, so no
+// column needs a predicate or a branch (per-column branches, or skipping
+// whole groups with warp votes, cost far more here: registers spill).
+__device__ __forceinline__ void mask_row(float (&x)[128], int c_lo, int c_hi, int c_s) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const uint32_t vis = range_bits(g, c_lo, c_hi) | range_bits(g, 0, c_s);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const uint32_t keep = (uint32_t)((int32_t)(vis << (31 - j)) >> 31);  // all ones when column visible
+      const uint32_t xb = __float_as_uint(x[32 * g + j]);
+      x[32 * g + j] = __uint_as_float((xb & keep) | (0xff800000u & ~keep));
+    }
+  }
 }
 
 // Maximum of the 128 raw scores of this thread's row (8 independent chains;

@@ -62,6 +62,16 @@ enum ErrBits : uint32_t {
   kErrSelfTest = 1u << 4,
 };
 
+// A work item of the persistent kernel with its key-tile plan worked out on
+// the host (plan_rules.h), six int4 per item:
+//   [0] b*H + h, h, b, first query tile qt0 (the item's sub-tiles are qt0, qt0 + 1)
+//   [1] list entries n, window start lo, sink entries na, the head's mask parameter
+//   [2] window key tiles lo0, hi0, lo1, hi1 of the two sub-tiles (empty: lo > hi)
+//   [3] FULL key tiles flo0, fhi0, flo1, fhi1 inside them
+//   [4] sink tiles ns0, ns1, load mode | store mode << 8, explicit-order row
+//   [5] first and last entries used by sub-tile 0 and by sub-tile 1 (-1: none)
+constexpr int kPersistItemInt4 = 6;
+
 struct FwdParams {
   // [0]: 64-column chunks (128-byte swizzle); [1]: the 16- or 32-column rest.
   CUtensorMap tq[2], tk[2], tv[2];  // [B*H][N][d] views
@@ -71,6 +81,7 @@ struct FwdParams {
   void* o;                          // [B][H][N][d], bf16 or fp32
   float* lse;                       // [B][H][N] or null
   const int2* items;                // (b*H + h, query-tile pair), or (b*H + h, query tile) when split
+  const int4* pitems;               // persistent kernel: kPersistItemInt4 int4 per work item
   const int32_t* head_info;         // [H][4], HeadField
   const int32_t* perm;              // explicit orders [n_perm][N]
   const uint64_t* block_bits;       // [block_heads][Nb][wpr]

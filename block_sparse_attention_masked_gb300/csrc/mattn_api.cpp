@@ -291,12 +291,58 @@ std::vector<int2> build_items(const Normalized& n) {
   return items;
 }
 
+// Descriptors of the persistent kernel's work items (paired items of an
+// interval mask): each item's key-tile plan from plan_rules.h, in the
+// layout kPersistItemInt4 documents, so that no role of the kernel divides.
+std::vector<int4> build_persist_items(const Normalized& n, const std::vector<int2>& items) {
+  const int nt = (n.N + kTile - 1) / kTile;
+  std::vector<int4> out(items.size() * kPersistItemInt4);
+  for (size_t i = 0; i < items.size(); ++i) {
+    const int bh = items[i].x, h = bh % n.H, b = bh / n.H, qt0 = 2 * items[i].y;
+    const HeadPlan& hp = n.heads[h];
+    KRange r[2];
+    int ns[2];
+    for (int s = 0; s < 2; ++s) {
+      const int qt = qt0 + s;
+      if (qt < nt) {
+        r[s] = interval_krange(n.kind, hp.param, n.N, qt);
+        ns[s] = sink_tiles(n.sink_tokens, n.N, qt);
+      } else {
+        r[s].lo = 1; r[s].hi = 0; r[s].flo = 0; r[s].fhi = -1;  // no rows
+        ns[s] = 0;
+      }
+    }
+    int lo, cnt, na;
+    pair_list_span(r[0].lo, r[0].hi, r[1].lo, r[1].hi, ns[0], ns[1], &lo, &cnt, &na);
+    int first[2] = {-1, -1}, last[2] = {-1, -1};
+    for (int j = 0; j < cnt; ++j) {
+      const int kt = j < na ? j : lo + j - na;
+      for (int s = 0; s < 2; ++s) {
+        if ((kt >= r[s].lo && kt <= r[s].hi) || kt < ns[s]) {
+          if (first[s] < 0) first[s] = j;
+          last[s] = j;
+        }
+      }
+    }
+    int4* d = &out[i * kPersistItemInt4];
+    d[0] = make_int4(bh, h, b, qt0);
+    d[1] = make_int4(cnt, lo, na, hp.param);
+    d[2] = make_int4(r[0].lo, r[0].hi, r[1].lo, r[1].hi);
+    d[3] = make_int4(r[0].flo, r[0].fhi, r[1].flo, r[1].fhi);
+    d[4] = make_int4(ns[0], ns[1], hp.load | (hp.store << 8), hp.perm_row);
+    d[5] = make_int4(first[0], last[0], first[1], last[1]);
+  }
+  return out;
+}
+
 // ------------------------------------------------------------ per-device state
 struct Plan {
   std::vector<int2> items_host;
   std::vector<int32_t> head_info_host;
+  std::vector<int4> pitems_host;  // persistent kernel: the items' descriptors
   int2* items = nullptr;
   int32_t* head_info = nullptr;
+  int4* pitems = nullptr;
 };
 
 struct DeviceBuf {
@@ -359,8 +405,8 @@ int device_state(DeviceState** out) {
 std::string plan_key(const Normalized& n) {
   std::string k;
   char buf[96];
-  snprintf(buf, sizeof(buf), "%d|%d|%d|%d|%d|%d|%d|%d|", n.kind, n.B, n.H, n.N, n.need_copy ? 1 : 0, n.split ? 1 : 0,
-           n.sink_tokens, n.single ? 1 : 0);
+  snprintf(buf, sizeof(buf), "%d|%d|%d|%d|%d|%d|%d|%d|%d|", n.kind, n.B, n.H, n.N, n.need_copy ? 1 : 0, n.split ? 1 : 0,
+           n.sink_tokens, n.single ? 1 : 0, n.persistent ? 1 : 0);
   k += buf;
   for (const auto& hp : n.heads) {
     snprintf(buf, sizeof(buf), "%d,%d,%d,%d;", hp.param, hp.load, hp.store, hp.perm_row);
@@ -384,6 +430,14 @@ int get_plan(DeviceState* st, const Normalized& n, cudaStream_t stream, Plan** o
     pl->head_info_host[h * 4 + kHeadLoad] = n.heads[h].load;
     pl->head_info_host[h * 4 + kHeadStore] = n.heads[h].store;
     pl->head_info_host[h * 4 + kHeadPermRow] = n.heads[h].perm_row;
+  }
+  if (n.persistent) {
+    pl->pitems_host = build_persist_items(n, pl->items_host);
+    MATTN_CUDA(cudaMalloc(&pl->pitems, std::max<size_t>(1, pl->pitems_host.size()) * sizeof(int4)),
+               "cudaMalloc(item descriptors)");
+    MATTN_CUDA(cudaMemcpyAsync(pl->pitems, pl->pitems_host.data(), pl->pitems_host.size() * sizeof(int4),
+                               cudaMemcpyHostToDevice, stream),
+               "upload item descriptors");
   }
   MATTN_CUDA(cudaMalloc(&pl->items, std::max<size_t>(1, pl->items_host.size()) * sizeof(int2)), "cudaMalloc(items)");
   MATTN_CUDA(cudaMalloc(&pl->head_info, pl->head_info_host.size() * sizeof(int32_t)), "cudaMalloc(head table)");
@@ -630,6 +684,7 @@ int fwd_locked(const void* q, const void* k, const void* v, void* o, float* lse,
   p.o = o;
   p.lse = lse;
   p.items = plan->items;
+  p.pitems = plan->pitems;
   p.after_prepass = (n.need_copy && !n.single) ? 1 : 0;
   p.n_items = (int)plan->items_host.size();
   p.head_info = plan->head_info;

@@ -145,6 +145,31 @@ MATTN_HD int sink_window_tile_class(int64_t w, int64_t s, int64_t n, int qt, int
   return kTileFull;
 }
 
+// Key-tile list of a CTA whose two query sub-tiles take the window ranges
+// [lo0, hi0] and [lo1, hi1] (empty when lo > hi; the ranges of neighbouring
+// query tiles overlap or touch) plus the sink tiles [0, ns0) and [0, ns1):
+// entry j < na is sink tile j, entry j >= na is key tile lo + j - na, n
+// entries in all.  The sink tiles form a segment before the window's tiles,
+// or one segment with them when they meet.
+MATTN_HD void pair_list_span(int lo0, int hi0, int lo1, int hi1, int ns0, int ns1, int* lo, int* n, int* na) {
+  const bool e0 = lo0 <= hi0, e1 = lo1 <= hi1;
+  *lo = e0 ? (e1 ? (lo0 < lo1 ? lo0 : lo1) : lo0) : lo1;
+  int hi = e0 ? (e1 ? (hi0 > hi1 ? hi0 : hi1) : hi0) : hi1;
+  *n = (e0 || e1) ? hi - *lo + 1 : 0;
+  *na = 0;
+  const int ns = ns0 > ns1 ? ns0 : ns1;
+  if (ns > 0 && *n > 0) {
+    if (ns >= *lo) {
+      hi = hi > ns - 1 ? hi : ns - 1;
+      *lo = 0;
+      *n = hi + 1;
+    } else {
+      *na = ns;
+      *n += ns;
+    }
+  }
+}
+
 // Block-selection bit B[m][nblk] of one head's bitmap (words per row = wpr).
 MATTN_HD bool block_bit(const uint64_t* bits, int wpr, int m, int nblk) {
   return (bits[(int64_t)m * wpr + (nblk >> 6)] >> (nblk & 63)) & 1ull;

@@ -77,11 +77,17 @@ def test_invalid_arguments_rejected_on_host(L):
     assert b"524288" in L.mattn_last_error()
     bad_scale = _desc(0, 0, softmax_scale=-1.0)
     assert L.mattn_count_pairs(ctypes.byref(bad_scale), 1, 1, 16, ctypes.byref(out)) == mattn.ERR_INVALID_ARG
-    for ok_flags in (mattn.FLAG_SCHEDULE_PAIRED, mattn.FLAG_SCHEDULE_SPLIT, mattn.FLAG_SCHEDULE_SINGLE):
+    for ok_flags in (mattn.FLAG_SCHEDULE_PAIRED, mattn.FLAG_SCHEDULE_SPLIT, mattn.FLAG_SCHEDULE_SINGLE,
+                     mattn.FLAG_SCHEDULE_PERSISTENT):
         assert L.mattn_count_pairs(ctypes.byref(_desc(0, 0, flags=ok_flags)), 1, 1, 16, ctypes.byref(out)) == mattn.OK
-    for bad_flags in (3, 5, 8, 0x80000000):
+    # one schedule flag at most; the persistent schedule takes the interval masks only
+    for bad_flags in (3, 5, 9, 12, 16, 0x80000000):
         flags = _desc(0, 0, flags=bad_flags)
         assert L.mattn_count_pairs(ctypes.byref(flags), 1, 1, 16, ctypes.byref(out)) == mattn.ERR_INVALID_ARG
+    blk_bits = np.ones(1, dtype=np.uint64)
+    persist_blk = _desc(4, 128, block_bits=blk_bits.ctypes.data, block_heads=1, flags=mattn.FLAG_SCHEDULE_PERSISTENT)
+    assert L.mattn_count_pairs(ctypes.byref(persist_blk), 1, 1, 128, ctypes.byref(out)) == mattn.ERR_UNSUPPORTED
+    assert b"persistent" in L.mattn_last_error()
     order = (ctypes.c_int32 * 1)(mattn.ORDER_COLUMN_MAJOR)
     cm = _desc(2, 3, head_order=order, grid_rows=3, grid_cols=5)
     assert L.mattn_count_pairs(ctypes.byref(cm), 1, 1, 16, ctypes.byref(out)) == mattn.ERR_INVALID_ARG
