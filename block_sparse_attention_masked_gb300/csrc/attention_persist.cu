@@ -62,13 +62,18 @@ static_assert(kPRegsControl + 2 * kPRegsSoftmax == 3 * 168, "register split must
 
 // Q slots: Q tile t = 2 i + s (i = the CTA's i-th item) goes to slot
 // t % kQSlots, free again once the S products of Q tile t - kQSlots are done.
-template <int D>
+// Output staging: one tile per sub-tile, written by the softmax warps and
+// stored with TMA (bf16 output at head dim <= 96; at 128 the shared memory
+// is full and rows are stored directly).
+template <int D, bool OUT_F32>
 struct PGeo {
-  static constexpr int kQSlots = (D <= 96) ? 4 : 3;
+  static constexpr int kQSlots = 3;
+  static constexpr bool kStage = (D <= 96) && !OUT_F32;
+  static constexpr int kStageTiles = kStage ? 2 : 0;
 };
 
 struct PBarriers {
-  uint64_t q_full[4], q_empty[4];
+  uint64_t q_full[3], q_empty[3];
   uint64_t k_full[3], k_empty[3];
   uint64_t v_full[3], v_empty[3];
   uint64_t s_full[2];
@@ -164,14 +169,16 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
   using G = Geo<D>;
   constexpr int KS = G::kStages;
   constexpr int VS = G::kStages;
-  constexpr int NQ = PGeo<D>::kQSlots;
+  using PG = PGeo<D, OUT_F32>;
+  constexpr int NQ = PG::kQSlots;
   static_assert(KS == VS, "one ring depth for K and V");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sq = base;
   uint8_t* sk = sq + NQ * G::kTileBytes;
   uint8_t* sv = sk + KS * G::kTileBytes;
-  PBarriers* bar = reinterpret_cast<PBarriers*>(sv + VS * G::kTileBytes);
+  uint8_t* sstage = sv + VS * G::kTileBytes;  // PG::kStageTiles output tiles
+  PBarriers* bar = reinterpret_cast<PBarriers*>(sstage + PG::kStageTiles * G::kTileBytes);
   volatile int* abort_flag = &bar->abort_flag;
 
   const int warp = threadIdx.x >> 5;
@@ -530,30 +537,58 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
       const bool valid = pos < p.N;
       const int64_t tok = valid ? token_of(p, pi.store, pi.perm_row, pos) : 0;
       const int64_t orow = ((int64_t)pi.ip.bh * p.N + tok) * D;
-#pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 16) {
-        float ov[16];
+      if (PG::kStage && p.o_tma) {
+        // Through shared memory: each thread writes its row into this
+        // sub-tile's staging tile, one thread stores the tile with TMA.
+        uint8_t* stage = sstage + s * G::kTileBytes;
+        const bool leader = quarter == 0 && lane == 0;
         if (has_o) {
-          ptx::tmem_ld16(o_tmem + c0, ov);
-          ptx::tmem_wait_ld();
+          if (leader) ptx::bulk_wait_read_all();  // the previous store has read the tile
+          ptx::named_bar_sync(1 + s, 128);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) ov[i] *= o_scale;
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) ov[i] = 0.f;
-        }
-        if (valid) {
-          if (OUT_F32) {
-            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.o) + orow + c0);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
-          } else {
+          for (int c0 = 0; c0 < D; c0 += 16) {
+            float ov[16];
+            ptx::tmem_ld16(o_tmem + c0, ov);
+            ptx::tmem_wait_ld();
             uint32_t pk[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) pk[i] = ptx::pack_bf16x2(ov[2 * i], ov[2 * i + 1]);
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + orow + c0);
-            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            for (int i = 0; i < 8; ++i) pk[i] = ptx::pack_bf16x2(ov[2 * i] * o_scale, ov[2 * i + 1] * o_scale);
+            tile_put16<D>(stage, row, c0 / 8, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+            tile_put16<D>(stage, row, c0 / 8 + 1, make_uint4(pk[4], pk[5], pk[6], pk[7]));
+          }
+          ptx::fence_proxy_async_shared();  // the tile's generic writes, before the async-proxy read
+          ptx::named_bar_sync(1 + s, 128);
+          if (leader) {
+            store_tile<D>(p, pi.load, stage, sp.qt * kTile, pi.ip.bh);
+            ptx::bulk_commit_group();
+          }
+        }
+      } else {
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 16) {
+          float ov[16];
+          if (has_o) {
+            ptx::tmem_ld16(o_tmem + c0, ov);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ov[i] *= o_scale;
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ov[i] = 0.f;
+          }
+          if (valid) {
+            if (OUT_F32) {
+              float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.o) + orow + c0);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) dst[i] = make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
+            } else {
+              uint32_t pk[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) pk[i] = ptx::pack_bf16x2(ov[2 * i], ov[2 * i + 1]);
+              uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + orow + c0);
+              dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            }
           }
         }
       }
@@ -561,6 +596,9 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
     }
   }
 
+  // the output tiles' TMA stores (issued by one thread per sub-tile) have
+  // completed before the CTA and its shared memory go away
+  if (PGeo<D, OUT_F32>::kStage && p.o_tma && warp >= 4 && (warp & 3) == 0 && lane == 0) ptx::bulk_wait_all();
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -569,15 +607,16 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
   }
 }
 
-template <int D>
+template <int D, bool F32>
 size_t persist_smem_for() {
   using G = Geo<D>;
-  return (size_t)(PGeo<D>::kQSlots + 2 * G::kStages) * G::kTileBytes + sizeof(PBarriers) + 1024;
+  using PG = PGeo<D, F32>;
+  return (size_t)(PG::kQSlots + 2 * G::kStages + PG::kStageTiles) * G::kTileBytes + sizeof(PBarriers) + 1024;
 }
 
 template <int D, bool F32>
 cudaError_t launch_persist_one(const FwdParams& p, int grid, cudaStream_t stream) {
-  const size_t smem = persist_smem_for<D>();
+  const size_t smem = persist_smem_for<D, F32>();
   auto kern = attention_persist_kernel<D, F32>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -598,11 +637,11 @@ cudaError_t launch_persist_one(const FwdParams& p, int grid, cudaStream_t stream
 
 size_t attention_persist_smem_bytes(int d) {
   switch (d) {
-    case 32: return persist_smem_for<32>();
-    case 64: return persist_smem_for<64>();
-    case 80: return persist_smem_for<80>();
-    case 96: return persist_smem_for<96>();
-    case 128: return persist_smem_for<128>();
+    case 32: return persist_smem_for<32, false>();
+    case 64: return persist_smem_for<64, false>();
+    case 80: return persist_smem_for<80, false>();
+    case 96: return persist_smem_for<96, false>();
+    case 128: return persist_smem_for<128, false>();
     default: return 0;
   }
 }

@@ -273,6 +273,53 @@ __device__ __forceinline__ void load_v_tile(const FwdParams& p, int mode, uint8_
   }
 }
 
+// TMA store of one 128-row O tile from shared memory (laid out as
+// load_tile writes a Q tile) to the output rows at sequence positions
+// [p0, p0 + 128) of row block bh, through the O view of the head's order
+// (`mode`, a LoadMode; requires p.o_tma).  Rows past N are clipped.
+template <int D>
+__device__ __forceinline__ void store_tile(const FwdParams& p, int mode, const uint8_t* src, int p0, int bh) {
+  using G = Geo<D>;
+  if (mode == kLoadRaster) {
+#pragma unroll
+    for (int c = 0; c < G::kChunks; ++c) ptx::tma_store_3d(&p.o_raster[0], src + c * G::kChunkBytes, c * 64, p0, bh);
+    if (G::kRem) ptx::tma_store_3d(&p.o_raster[1], src + G::kChunks * G::kChunkBytes, 0, p0, bh);
+  } else if (mode == kLoadBlock2x2Row || mode == kLoadBlock2x2Col) {
+    const CUtensorMap* blocks = mode == kLoadBlock2x2Row ? p.o_blk : p.o_blkc;
+    int c3, c4;
+    block2x2_coords(p, mode, p0, bh, &c3, &c4);
+#pragma unroll
+    for (int c = 0; c < G::kChunks; ++c) ptx::tma_store_5d(&blocks[0], src + c * G::kChunkBytes, c * 64, 0, 0, c3, c4);
+    if (G::kRem) ptx::tma_store_5d(&blocks[1], src + G::kChunks * G::kChunkBytes, 0, 0, 0, c3, c4);
+  } else {
+    const int col = p0 / p.grid_rows;
+    const int r0 = p0 - col * p.grid_rows;
+#pragma unroll
+    for (int c = 0; c < G::kChunks; ++c)
+      ptx::tma_store_4d(&p.o_colmaj[0], src + c * G::kChunkBytes, c * 64, col, r0, bh);
+    if (G::kRem) ptx::tma_store_4d(&p.o_colmaj[1], src + G::kChunks * G::kChunkBytes, 0, col, r0, bh);
+  }
+}
+
+// Writes 8 bf16 values (one 16-byte unit u of the d columns) of row `row`
+// into a tile laid out as load_tile writes it: 64-column chunks of 128-byte
+// rows in the 128-byte swizzle (unit index XOR row % 8), then the 16- or
+// 32-column rest in the 32- or 64-byte swizzle.
+template <int D>
+__device__ __forceinline__ void tile_put16(uint8_t* tile, int row, int u, uint4 v) {
+  using G = Geo<D>;
+  const int c = u >> 3;  // 64-column chunk
+  uint8_t* dst;
+  if (c < G::kChunks) {
+    dst = tile + c * G::kChunkBytes + row * 128 + (((u & 7) ^ (row & 7)) << 4);
+  } else {
+    const int ur = u - 8 * G::kChunks;  // unit inside the rest
+    const int sw = G::kRem == 16 ? ((row >> 2) & 1) : ((row >> 1) & 3);
+    dst = tile + G::kChunks * G::kChunkBytes + row * G::kRemRowBytes + ((ur ^ sw) << 4);
+  }
+  *reinterpret_cast<uint4*>(dst) = v;
+}
+
 // O += P V for one sub-tile: P (128 x 128 keys, bf16 pairs in TMEM) is the
 // A operand; V (keys x d, d contiguous) is an MN-major B operand whose
 // kVW-column atoms lie kVChunkBytes apart (leading byte offset) and whose

@@ -78,6 +78,9 @@ struct FwdParams {
   CUtensorMap cq[2], ck[2], cv[2];  // column-major views [B*H][rows][cols][d]
   CUtensorMap bq[2], bk[2], bv[2];  // 2x2-block row-major views [B*H*rows/2][cols/2][2][2][d]
   CUtensorMap bcq[2], bck[2], bcv[2];  // 2x2-block column-major views [cols/2][B*H*rows/2][2][2][d]
+  // Views of O matching tq, cq, bq, bcq (bf16 output written with TMA stores
+  // when o_tma is set: the persistent kernel at head dim <= 96)
+  CUtensorMap o_raster[2], o_colmaj[2], o_blk[2], o_blkc[2];
   void* o;                          // [B][H][N][d], bf16 or fp32
   float* lse;                       // [B][H][N] or null
   const int2* items;                // (b*H + h, query-tile pair), or (b*H + h, query tile) when split
@@ -103,6 +106,8 @@ struct FwdParams {
                                     //    alternately to two sub-tile pipelines
                                     //    (head dim 256: one query tile per CTA, one pipeline)
   int out_f32;                      // head dim 256 kernel: O in fp32 (else bf16)
+  int o_tma;                        // 1: the O views above are set (bf16 output, every head
+                                    // stored in its load order: raster, column-major or 2x2 blocks)
   int after_prepass;                // 1: launched as a programmatic dependent of the reorder
                                     // pre-pass, whose copies its loads read
 };

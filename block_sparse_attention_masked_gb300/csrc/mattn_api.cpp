@@ -679,6 +679,18 @@ int fwd_locked(const void* q, const void* k, const void* v, void* o, float* lse,
                                   (int64_t)B * kv_heads)))
       return rc;
   }
+  if (n.persistent && dtype == MATTN_BF16 && !n.need_copy && d <= 96) {
+    // the persistent kernel stores bf16 output tiles with TMA through views of
+    // O in each head's order (the same views as Q's)
+    if ((rc = make_maps(n, o, p.o_raster, p.o_colmaj, rows, cols, (int64_t)B * H))) return rc;
+    for (int by_cols = 0; by_cols < 2; ++by_cols) {
+      if (!(by_cols ? n.any_block_col_tma : n.any_block_tma)) continue;
+      if ((rc = make_block_maps(n, o, by_cols ? p.o_blkc : p.o_blk, desc->grid_rows, desc->grid_cols, (int64_t)B * H,
+                                false, by_cols)))
+        return rc;
+    }
+    p.o_tma = 1;
+  }
   p.H_kv = kv_heads;
   p.kv_group = H / kv_heads;
   p.o = o;
