@@ -80,6 +80,8 @@ struct PBarriers {
   uint64_t p_full[2];
   uint64_t o_full[2];      // the item's last P V of sub-tile s is done
   uint64_t drain[2];       // MMA drain on abort, one per issuer
+  uint64_t stage_sync[2];  // per sub-tile: barrier of its 128 softmax threads (output staging)
+  uint64_t never;          // self-test: nothing ever arrives here
   uint32_t tmem_base;
   int abort_flag;
   uint32_t mma_turn;       // ticket of the MMA group that may be issued next
@@ -203,7 +205,9 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
       ptx::mbar_init(&bar->p_full[s], kTile);
       ptx::mbar_init(&bar->o_full[s], 1);
       ptx::mbar_init(&bar->drain[s], 1);
+      ptx::mbar_init(&bar->stage_sync[s], kTile);
     }
+    ptx::mbar_init(&bar->never, 1);
     bar->abort_flag = 0;
     bar->mma_turn = 0;
     ptx::fence_barrier_init();
@@ -354,6 +358,13 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
     const uint32_t s_tm = tmem + s * 128;
     const uint32_t o_tm = tmem + 256 + s * 128;
     bool ok = true, issued_any = false;
+    if (p.self_test_timeout && s == 0) {
+      // nothing ever arrives on this barrier: exercises the bounded-wait path
+      if (!wait_all(&bar->never, 0)) {
+        if (lane == 0) raise_error(p, bar, kErrSelfTest);
+        ok = false;
+      }
+    }
     bool pend = false, pend_first = false, pend_last = false;
     uint32_t pcount = 0;  // P tiles consumed
     int e = 0;
@@ -445,6 +456,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
     const float sl2 = p.scale_log2;
     uint32_t count = 0;  // S tiles of this sub-tile so far (all items)
     int o_items = 0;     // items whose O_s has been read
+    uint32_t sync_seq = 0;  // uses of stage_sync[s]
     bool ok = true;
     for (int it = blockIdx.x; ok && it < p.n_items; it += gridDim.x) {
       const PItem pi = load_pitem(p, it);
@@ -544,7 +556,11 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
         const bool leader = quarter == 0 && lane == 0;
         if (has_o) {
           if (leader) ptx::bulk_wait_read_all();  // the previous store has read the tile
-          ptx::named_bar_sync(1 + s, 128);
+          if (!__all_sync(0xffffffffu, ptx::mbar_sync(&bar->stage_sync[s], sync_seq, p.timeout_ns, abort_flag))) {
+            if (lane == 0) raise_error(p, bar, kErrEpilogue);
+            ok = false;
+            break;
+          }
 #pragma unroll
           for (int c0 = 0; c0 < D; c0 += 16) {
             float ov[16];
@@ -557,7 +573,11 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
             tile_put16<D>(stage, row, c0 / 8 + 1, make_uint4(pk[4], pk[5], pk[6], pk[7]));
           }
           ptx::fence_proxy_async_shared();  // the tile's generic writes, before the async-proxy read
-          ptx::named_bar_sync(1 + s, 128);
+          if (!__all_sync(0xffffffffu, ptx::mbar_sync(&bar->stage_sync[s], sync_seq, p.timeout_ns, abort_flag))) {
+            if (lane == 0) raise_error(p, bar, kErrEpilogue);
+            ok = false;
+            break;
+          }
           if (leader) {
             store_tile<D>(p, pi.load, stage, sp.qt * kTile, pi.ip.bh);
             ptx::bulk_commit_group();

@@ -347,14 +347,18 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
 // moving a share of them to an FMA-pipe polynomial measured slower at every
 // share tried, as did a truncating pack with a second sum over the
 // truncated values (one more add and two integer ops per pair).
-__device__ __forceinline__ float exp_to_tmem(const float (&x)[128], float sl2, float mref, uint32_t p_tmem) {
+// (NC = 128 for a whole row; a thread holding half a row passes its 64
+// scores and the tensor-memory address of its half of P.)
+template <int NC>
+__device__ __forceinline__ float exp_to_tmem(const float (&x)[NC], float sl2, float mref, uint32_t p_tmem) {
+  static_assert(NC % 32 == 0, "whole 32-column groups");
   const float2 sl2v = make_float2(sl2, sl2);
   const float2 negm = make_float2(-mref, -mref);
   float2 acc[2];
 #pragma unroll
   for (int i = 0; i < 2; ++i) acc[i] = make_float2(0.f, 0.f);
 #pragma unroll
-  for (int c0 = 0; c0 < 128; c0 += 32) {
+  for (int c0 = 0; c0 < NC; c0 += 32) {
     uint32_t pk[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -385,10 +389,14 @@ __device__ __forceinline__ uint32_t range_bits(int g, int lo, int hi) {
 // extended to a full word, selects between x and -inf bitwise, so no
 // column needs a predicate or a branch (per-column branches, or skipping
 // whole groups with warp votes, cost far more here: registers spill).
-__device__ __forceinline__ void mask_row(float (&x)[128], int c_lo, int c_hi, int c_s) {
+// (x may hold NC < 128 columns of the row, starting at tile column col0, a
+// multiple of 32.)
+template <int NC>
+__device__ __forceinline__ void mask_row(float (&x)[NC], int c_lo, int c_hi, int c_s, int col0 = 0) {
 #pragma unroll
-  for (int g = 0; g < 4; ++g) {
-    const uint32_t vis = range_bits(g, c_lo, c_hi) | range_bits(g, 0, c_s);
+  for (int g = 0; g < NC / 32; ++g) {
+    const int gt = g + col0 / 32;  // 32-column group of the tile
+    const uint32_t vis = range_bits(gt, c_lo, c_hi) | range_bits(gt, 0, c_s);
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       const uint32_t keep = (uint32_t)((int32_t)(vis << (31 - j)) >> 31);  // all ones when column visible
@@ -400,22 +408,25 @@ __device__ __forceinline__ void mask_row(float (&x)[128], int c_lo, int c_hi, in
 
 // Maximum of the 128 raw scores of this thread's row (8 independent chains;
 // measured faster here than three-input maxima).
-__device__ __forceinline__ float row_max(const float (&x)[128]) {
+template <int NC>
+__device__ __forceinline__ float row_max(const float (&x)[NC]) {
   float a[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) a[i] = x[i];
 #pragma unroll
-  for (int c = 8; c < 128; c += 8)
+  for (int c = 8; c < NC; c += 8)
 #pragma unroll
     for (int i = 0; i < 8; ++i) a[i] = fmaxf(a[i], x[c + i]);
   return fmaxf(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])), fmaxf(fmaxf(a[4], a[5]), fmaxf(a[6], a[7])));
 }
 
-// O row *= alpha in tensor memory (warp-collective; alpha is per lane).
+// O row *= alpha in tensor memory (warp-collective; alpha is per lane), for
+// the 16-column chunks of O in [c_begin, c_end).
 template <int D>
-__device__ __forceinline__ void rescale_o(uint32_t o_tmem, float alpha) {
+__device__ __forceinline__ void rescale_o(uint32_t o_tmem, float alpha, int c_begin = 0, int c_end = D) {
 #pragma unroll
   for (int c0 = 0; c0 < D; c0 += 16) {
+    if (c0 < c_begin || c0 >= c_end) continue;  // warp-uniform: a column range of O
     float ov[16];
     ptx::tmem_ld16(o_tmem + c0, ov);
     ptx::tmem_wait_ld();

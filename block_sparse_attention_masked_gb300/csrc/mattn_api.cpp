@@ -87,6 +87,11 @@ struct Normalized {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Average key tiles per query tile up to which an interval mask runs on the
+// persistent kernel by default (measured on GB300: windows of 3-7 tiles ran
+// 1.2-1.6x faster persistent, lists of 16 and more 3-20% slower).
+constexpr double kPersistMaxTiles = 12.0;
+
 // allow_block_tma: the caller's kernel reads the 2x2-block row-major order
 // through its 5D TMA views (the attention forward); otherwise such heads go
 // through the reorder copy.
@@ -218,8 +223,28 @@ int normalize(const mattn_mask_desc* desc, int B, int H, int N, int d, int dtype
     n.split = true;
   }
   // The persistent kernel: interval masks at head dim <= 128 (paired work
-  // items).  Chosen on request for now.
+  // items).  Without a schedule flag it is chosen when a query tile's
+  // key-tile list is short on average (at most kPersistMaxTiles): there the
+  // one-item-per-CTA kernel spends much of its time in per-CTA set-up and
+  // epilogue, which the persistent kernel overlaps with neighbouring items;
+  // on long lists the hardware's dynamic CTA scheduling balances better.
   n.persistent = false;
+  if (need_data && desc->flags == 0 && n.kind != kBlockSparse && !n.single && d <= 128) {
+    const int64_t nt = ((int64_t)N + kTile - 1) / kTile;
+    double tiles = 0.0;
+    for (const auto& hp : n.heads) {
+      const double w = (double)std::min<int64_t>(hp.param, N);
+      double t;
+      switch (n.kind) {
+        case kChunk: t = w / kTile + 1.0; break;
+        case kSliding: t = (2.0 * w + kTile) / kTile + 1.0; break;
+        case kCausalWindow: t = w / kTile + 1.0 + (n.sink_tokens > 0 ? 1.0 : 0.0); break;
+        default: t = (double)nt; break;
+      }
+      tiles += std::min<double>(t, (double)nt);
+    }
+    n.persistent = tiles / H <= kPersistMaxTiles;
+  }
   if (desc->flags == MATTN_FLAG_SCHEDULE_PERSISTENT) {
     if (n.kind == kBlockSparse)
       return fail(MATTN_ERR_UNSUPPORTED, "the persistent schedule takes the interval masks (not block-sparse)");
@@ -405,8 +430,8 @@ int device_state(DeviceState** out) {
 std::string plan_key(const Normalized& n) {
   std::string k;
   char buf[96];
-  snprintf(buf, sizeof(buf), "%d|%d|%d|%d|%d|%d|%d|%d|%d|", n.kind, n.B, n.H, n.N, n.need_copy ? 1 : 0, n.split ? 1 : 0,
-           n.sink_tokens, n.single ? 1 : 0, n.persistent ? 1 : 0);
+  snprintf(buf, sizeof(buf), "%d|%d|%d|%d|%d|%d|%d|%d|%d|", n.kind, n.B, n.H, n.N, n.need_copy ? 1 : 0,
+           n.split ? 1 : 0, n.sink_tokens, n.single ? 1 : 0, n.persistent ? 1 : 0);
   k += buf;
   for (const auto& hp : n.heads) {
     snprintf(buf, sizeof(buf), "%d,%d,%d,%d;", hp.param, hp.load, hp.store, hp.perm_row);

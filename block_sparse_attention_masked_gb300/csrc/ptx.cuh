@@ -106,6 +106,20 @@ __device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity
   return false;
 }
 
+// A barrier among the threads an mbarrier was initialised for (its arrival
+// count): every one arrives, then waits, bounded like mbar_wait.  `seq`
+// counts the calling thread's uses of this barrier (all participants make
+// the same sequence of calls, so a phase is never two uses ahead of a
+// waiter).  The arrivals release, and the wait acquires, the threads'
+// earlier shared-memory writes.
+__device__ __forceinline__ bool mbar_sync(uint64_t* bar, uint32_t& seq, uint64_t timeout_ns,
+                                          volatile int* abort_flag) {
+  mbar_arrive(bar);
+  const bool got = mbar_wait(bar, seq & 1, timeout_ns, abort_flag);
+  ++seq;
+  return got;
+}
+
 // Bounded wait that ignores the abort flag (used while unwinding, to let
 // operations already issued finish before their resources are released).
 __device__ __forceinline__ bool mbar_wait_time_only(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
@@ -223,10 +237,6 @@ __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bu
 // This thread's committed bulk stores have completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-// Barrier over `count` threads of the CTA (a multiple of 32) on named barrier `id`.
-__device__ __forceinline__ void named_bar_sync(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
 
 // L2 policies: keep (K, V tiles that many query tiles re-read) or drop
 // first (Q tiles, read once).

@@ -103,7 +103,9 @@ typedef enum { MATTN_BF16 = 0, MATTN_F32 = 1 } mattn_dtype;
  * tile whose key tiles are dealt alternately to two pipelines merged at the
  * end (SPLIT).  With neither flag set the library picks: SPLIT for
  * MATTN_BLOCK_SPARSE with Bs == 128 (neighbouring query tiles then fall in
- * different block rows and share few key tiles), PAIRED otherwise. */
+ * different block rows and share few key tiles), PERSISTENT for the
+ * interval masks whose query tiles see about 12 key tiles or fewer on
+ * average (short windows and chunks), PAIRED otherwise. */
 #define MATTN_FLAG_SCHEDULE_PAIRED 1u
 #define MATTN_FLAG_SCHEDULE_SPLIT 2u
 /* Head dim 128 only (head dim 256 always runs this way): one 128-row query

@@ -1,6 +1,5 @@
-"""GPU parity of the persistent schedule (MATTN_FLAG_SCHEDULE_PERSISTENT):
-one CTA per SM walking paired work items back to back, for the interval
-masks.
+"""GPU parity of the persistent schedule (MATTN_FLAG_SCHEDULE_PERSISTENT) for
+the interval masks: one CTA per SM walking paired work items back to back.
 
 Each case is checked twice:
 - against the fp64 oracle with the tolerances of the other parity tests
@@ -59,15 +58,30 @@ def grid_cap():
     L.mattn_internal_set_persist_grid(0)
 
 
-def _same_as_paired(q, k, v, spec, tag):
+SCHEDULES = ["persistent"]
+
+
+def _same_as_paired(q, k, v, spec, tag, schedule="persistent"):
+    """The persistent kernel does a paired item's arithmetic exactly: equal
+    bits.  The streamed kernel splits each row's softmax between two thread
+    groups, so its row sums are added in another order: O within one bf16
+    (or 2^-20 fp32) rounding step of the paired result, LSE within 1e-5."""
     B, H, N, d = q.shape
-    o_p, l_p = mattn.attention(q, k, v, mattn.prepare(spec, H, N, schedule="persistent"))
+    o_p, l_p = mattn.attention(q, k, v, mattn.prepare(spec, H, N, schedule=schedule))
     o_r, l_r = mattn.attention(q, k, v, mattn.prepare(spec, H, N, schedule="paired"))
     torch.cuda.synchronize()
     rc, word = mattn.device_status()
     assert rc == 0, f"{tag}: device error word {word:#x}"
-    assert torch.equal(o_p, o_r), f"{tag}: O differs from the paired kernel"
-    assert torch.equal(l_p, l_r), f"{tag}: LSE differs from the paired kernel"
+    if schedule == "persistent":
+        assert torch.equal(o_p, o_r), f"{tag}: O differs from the paired kernel"
+        assert torch.equal(l_p, l_r), f"{tag}: LSE differs from the paired kernel"
+        return
+    step = 2.0 ** -7 if o_p.dtype == torch.bfloat16 else 2.0 ** -20
+    a, r = o_p.float(), o_r.float()
+    assert ((a - r).abs() <= step * r.abs() + 1e-6).all(), f"{tag}: O differs from the paired kernel"
+    fin = torch.isfinite(l_r)
+    assert torch.equal(fin, torch.isfinite(l_p)), f"{tag}: LSE -inf pattern differs"
+    assert (l_p[fin] - l_r[fin]).abs().max().item() <= 1e-5, f"{tag}: LSE differs from the paired kernel"
 
 
 def _specs(H, n):
@@ -81,10 +95,11 @@ def _specs(H, n):
     ]
 
 
+@pytest.mark.parametrize("sched", SCHEDULES)
 @pytest.mark.parametrize("cap", [0, 3])
 @pytest.mark.parametrize("d", [32, 64, 80, 96, 128])
 @pytest.mark.parametrize("n", [256, 1000, 2200])
-def test_interval_kinds(d, n, cap, grid_cap):
+def test_interval_kinds(d, n, cap, sched, grid_cap):
     """Every interval kind with per-head parameters, ragged N (a partial last
     query tile, and at 1000 / 2200 an odd tile count whose last pair has one
     empty sub-tile), with and without a capped grid."""
@@ -92,13 +107,14 @@ def test_interval_kinds(d, n, cap, grid_cap):
     H = 3
     q, k, v = make_qkv(2, H, n, d, "bf16", 1.0, seed=d * 7 + n, device="cuda")
     for spec in _specs(H, n):
-        tag = f"{spec.kind} d{d} n{n} cap{cap}"
-        check(q, k, v, spec, tag=tag, schedule="persistent")
-        _same_as_paired(q, k, v, spec, tag)
+        tag = f"{spec.kind} d{d} n{n} cap{cap} {sched}"
+        check(q, k, v, spec, tag=tag, schedule=sched)
+        _same_as_paired(q, k, v, spec, tag, sched)
 
 
+@pytest.mark.parametrize("sched", SCHEDULES)
 @pytest.mark.parametrize("cap", [0, 2])
-def test_token_orders(cap, grid_cap):
+def test_token_orders(cap, sched, grid_cap):
     """Column-major heads (strided TMA views), the two 2x2-block orders (5D
     views), an explicit order and fp32 inputs (both through the reorder
     pre-pass, the kernel then launched as its programmatic dependent)."""
@@ -110,21 +126,22 @@ def test_token_orders(cap, grid_cap):
     spec = MaskSpec("sliding", [128, 128, 90, 300],
                     perm=[None, cm, block2x2_order(rows, cols), block2x2_order(rows, cols, by_columns=True)],
                     perm_grid=[None, (rows, cols), (rows, cols, "block2x2_row"), (rows, cols, "block2x2_col")])
-    check(q, k, v, spec, tag="grid orders", schedule="persistent")
-    _same_as_paired(q, k, v, spec, "grid orders")
+    check(q, k, v, spec, tag="grid orders", schedule=sched)
+    _same_as_paired(q, k, v, spec, "grid orders", sched)
     rng = np.random.default_rng(9)
     spec2 = MaskSpec("chunk", [256, 100, 256, 64], perm=[random_order(n, 3), None, cm, None],
                      sink=rng.standard_normal(4))
-    check(q, k, v, spec2, tag="explicit order", schedule="persistent")
-    _same_as_paired(q, k, v, spec2, "explicit order")
+    check(q, k, v, spec2, tag="explicit order", schedule=sched)
+    _same_as_paired(q, k, v, spec2, "explicit order", sched)
     qf, kf, vf = make_qkv(1, 2, 1000, 64, "f32", 1.0, seed=6, device="cuda")
     spec3 = MaskSpec("sliding", [32, 100])
-    check(qf, kf, vf, spec3, tag="fp32", schedule="persistent")
-    _same_as_paired(qf, kf, vf, spec3, "fp32")
+    check(qf, kf, vf, spec3, tag="fp32", schedule=sched)
+    _same_as_paired(qf, kf, vf, spec3, "fp32", sched)
 
 
+@pytest.mark.parametrize("sched", SCHEDULES)
 @pytest.mark.parametrize("cap", [0, 5])
-def test_grouped_query_heads(cap, grid_cap):
+def test_grouped_query_heads(cap, sched, grid_cap):
     """Grouped-query attention: 8 query heads sharing 2 K/V heads."""
     grid_cap(cap)
     from oracle import dense
@@ -135,11 +152,10 @@ def test_grouped_query_heads(cap, grid_cap):
     k = torch.randn((B, Hkv, n, d), generator=g, device="cuda").to(torch.bfloat16)
     v = torch.randn((B, Hkv, n, d), generator=g, device="cuda").to(torch.bfloat16)
     spec = MaskSpec("causal_window", [576] * H, sink=np.linspace(-1, 1, H))
-    o, lse = mattn.attention(q, k, v, mattn.prepare(spec, H, n, schedule="persistent"))
-    o_r, l_r = mattn.attention(q, k, v, mattn.prepare(spec, H, n, schedule="paired"))
+    o, lse = mattn.attention(q, k, v, mattn.prepare(spec, H, n, schedule=sched))
     torch.cuda.synchronize()
     assert mattn.device_status()[0] == 0
-    assert torch.equal(o, o_r) and torch.equal(lse, l_r)
+    _same_as_paired(q, k, v, spec, f"gqa {sched}", sched)
     rows = np.unique(np.r_[0, 127, 128, 575, 576, n - 1, np.random.default_rng(0).choice(n, 40, replace=False)])
     f = lambda t: t.float().cpu().numpy()  # noqa: E731
     ref_o, ref_l = dense.attention(f(q), f(k), f(v), spec, rows=rows)
@@ -149,8 +165,9 @@ def test_grouped_query_heads(cap, grid_cap):
     assert np.abs(f(lse)[0][:, rows] - ref_l).max() <= 1e-3
 
 
+@pytest.mark.parametrize("sched", SCHEDULES)
 @pytest.mark.parametrize("mask", ["sliding256_rowcol", "chunk512", "sliding256_blocks"])
-def test_vit16384_full_size(mask):
+def test_vit16384_full_size(mask, sched):
     """The 16,384-token ViT layer (B1 H16 d80) at full size, in the launch
     configuration the benchmark times: sampled heads (raster, column-major
     and 2x2-block heads) against the oracle on sampled rows, all heads equal
@@ -160,25 +177,27 @@ def test_vit16384_full_size(mask):
     spec = make_mask(wl, mask, seed=0)
     rng = np.random.default_rng(1)
     rows = np.unique(np.r_[0, 255, 256, 8191, wl.N - 1, rng.choice(wl.N, 48, replace=False)])
-    check(q, k, v, spec, rows=rows, heads=[(0, 0), (0, 5), (0, 8), (0, 15)], tag=mask, schedule="persistent")
-    _same_as_paired(q, k, v, spec, mask)
+    check(q, k, v, spec, rows=rows, heads=[(0, 0), (0, 5), (0, 8), (0, 15)], tag=mask, schedule=sched)
+    _same_as_paired(q, k, v, spec, mask, sched)
 
 
-def test_causal_windows_with_sink_full_size():
+@pytest.mark.parametrize("sched", SCHEDULES)
+def test_causal_windows_with_sink_full_size(sched):
     """The head-wise causal-window LM layer (B1 H16 L4096 d128, windows
     512..4096, sink logits) at full size."""
     wl = WORKLOADS["causal4096"]
     q, k, v = make_workload_inputs(wl, seed=0, device="cuda")
     spec = make_mask(wl, "causal_window_sink", seed=0)
     rows = np.unique(np.r_[0, 511, 512, 2047, 2048, 4095, np.random.default_rng(2).choice(4096, 64, replace=False)])
-    check(q, k, v, spec, rows=rows, tag="causal4096", schedule="persistent")
-    _same_as_paired(q, k, v, spec, "causal4096")
+    check(q, k, v, spec, rows=rows, tag="causal4096", schedule=sched)
+    _same_as_paired(q, k, v, spec, "causal4096", sched)
 
 
-def test_rejects_block_sparse():
+@pytest.mark.parametrize("sched", SCHEDULES)
+def test_rejects_block_sparse(sched):
     from workloads import bernoulli_causal_blocks
 
     spec = MaskSpec("block", [128, 128], block=bernoulli_causal_blocks(2, 4, 0))
     q, k, v = make_qkv(1, 2, 512, 64, "bf16", 1.0, seed=0, device="cuda")
     with pytest.raises(RuntimeError, match="persistent"):
-        mattn.attention(q, k, v, mattn.prepare(spec, 2, 512, schedule="persistent"))
+        mattn.attention(q, k, v, mattn.prepare(spec, 2, 512, schedule=sched))
