@@ -80,6 +80,79 @@ def profile_traffic(workload: str):
         return None
 
 
+# ------------------------------------------------------------------ masks and counts
+def spec_head(spec, h: int):
+    """The mask of head h alone (a one-head MaskSpec for the oracle)."""
+    from workloads import MaskSpec
+
+    pick = lambda xs: None if xs is None else [xs[h]]  # noqa: E731
+    blk = None
+    if spec.block is not None:
+        b = np.asarray(spec.block)
+        blk = b[h:h + 1] if b.ndim == 3 else b
+    sink = None if spec.sink is None else np.asarray(spec.sink)[h:h + 1]
+    return MaskSpec(spec.kind, [spec.head_param[h]], perm=pick(spec.perm), perm_grid=pick(spec.perm_grid),
+                    block=blk, sink=sink, sink_tokens=getattr(spec, "sink_tokens", 0))
+
+
+def block_mask_pairs(spec, N: int, B: int = 1) -> int:
+    """Visible (query, key) pairs of a block-selection mask with N a multiple
+    of the block size: a kept block below the diagonal has Bs^2 pairs, a kept
+    diagonal block Bs (Bs + 1) / 2 (causality inside it); blocks above the
+    diagonal count nothing.  The unit count of the FLOP metric for the
+    reference arm, which does not load the library."""
+    blk = np.asarray(spec.block, dtype=bool)
+    if blk.ndim == 2:
+        blk = blk[None]
+    total = 0
+    for h in range(len(spec.head_param)):
+        bh = blk[h] if blk.shape[0] > 1 else blk[0]
+        bs = int(spec.head_param[h])
+        if N % bs:
+            raise ValueError("N must be a multiple of the block size")
+        total += int(np.tril(bh, -1).sum()) * bs * bs + int(np.diag(bh).sum()) * bs * (bs + 1) // 2
+    return B * total
+
+
+def cpu_info() -> dict:
+    """The host cores this process may use and the BLAS thread pool size."""
+    info = {"affinity": len(os.sched_getaffinity(0)), "nproc": os.cpu_count()}
+    try:
+        import threadpoolctl
+
+        pools = threadpoolctl.threadpool_info()
+        info["blas_threads"] = max((i.get("num_threads", 0) for i in pools), default=0)
+    except Exception:
+        info["blas_threads"] = None
+    return info
+
+
+def numa_info(gpu_index: int) -> dict:
+    """NUMA node of the GPU (sysfs) and the nodes of the host."""
+    out = {}
+    try:
+        bus = subprocess.run(["nvidia-smi", "-i", str(gpu_index), "--query-gpu=pci.bus_id", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=20).stdout.strip().lower()
+        dom, rest = bus.split(":", 1)
+        path = f"/sys/bus/pci/devices/{dom[-4:]}:{rest}/numa_node"
+        with open(path) as f:
+            out["gpu_node"] = int(f.read().strip())
+    except Exception:
+        out["gpu_node"] = None
+    try:
+        out["host_nodes"] = len([n for n in os.listdir("/sys/devices/system/node") if n.startswith("node")])
+    except Exception:
+        out["host_nodes"] = None
+    return out
+
+
+def headline_config(wl, mask_name: str, pairs: int, world: int) -> dict:
+    """The `config` of the benchmark line, the same in both arms."""
+    return {"workload": wl.name, "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d, "mask": mask_name,
+            "mask_detail": wl.description, "pairs": int(pairs), "l2": "inputs larger than L2 (3 GiB)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
 # ------------------------------------------------------------------ distributed
 def dist_env():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
@@ -217,6 +290,8 @@ def run_gpu(args):
     spec = make_mask(wl, mask_name, seed=0)
     mask = mattn.prepare(spec, wl.H, wl.N, device=dev)
     pairs = mattn.count_pairs(spec, wl.B, wl.H, wl.N)
+    if spec.kind == "block" and pairs != block_mask_pairs(spec, wl.N, wl.B):
+        raise RuntimeError("the library's pair count differs from the bitmap's")
     flops = effective_flops(pairs, wl.d)
     o = torch.empty_like(q)
     lse = torch.empty((wl.B, wl.H, wl.N), dtype=torch.float32, device=dev)
@@ -255,6 +330,27 @@ def run_gpu(args):
     achieved = flops / (per_launch_ms * 1e-3) / 1e12
     traffic = profile_traffic(wl_name)
 
+    # ---------------- the oracle on the GPU arm's own inputs (sampled rows)
+    parity = {}
+    cpu = None
+    if rank == 0 and world == 1 and not args.quick:
+        rows = sampled_rows(wl.N, 128, seed=1, extra=55)
+        heads = [0, wl.H - 1]
+        chk, secs, pr = oracle_check(q, k, v, o, lse, spec, heads, rows)
+        parity[f"{wl_name}/{mask_name}"] = chk
+        st_rows = rows[:16]
+        st_secs = oracle_single_thread(q, k, v, spec, 0, st_rows)
+        st_pairs = rows_pairs(spec, 0, wl.N, st_rows)
+        ci = cpu_info()
+        cpu = {"value": round(effective_flops(pr, wl.d) / secs / 1e12, 6), "unit": "TFLOP/s",
+               "cores": ci["affinity"], "cores_detail": ci, "kind": "oracle",
+               "sample": f"{wl_name}/{mask_name}: heads {heads}, {len(rows)} query rows each (first, last, block "
+                         f"edges, middle, random), every key scored in fp64 (numpy), {secs:.2f} s on all "
+                         f"{ci['affinity']} cores",
+               "single_thread": None if st_secs is None else {
+                   "value": round(effective_flops(st_pairs, wl.d) / st_secs / 1e12, 6), "unit": "TFLOP/s",
+                   "sample": f"head 0, {len(st_rows)} rows, one BLAS thread, {st_secs:.2f} s"}}
+
     # ---------------- end to end through the host-buffer entry point
     e2e = None
     if not args.quick:
@@ -274,10 +370,27 @@ def run_gpu(args):
         barrier(dist)
         tensor_bytes = q.numel() * q.element_size()
         bits_bytes = int(hmask.block_words_host.nbytes) if spec.kind == "block" else 0
+        # the host link alone: one pinned copy of q in and of o out, timed on the device
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record()
+        q.copy_(qh, non_blocking=True)
+        s1.record()
+        s1.synchronize()
+        h2d_gbs = tensor_bytes / (s0.elapsed_time(s1) * 1e-3) / 1e9
+        s0.record()
+        oh.copy_(o, non_blocking=True)
+        s1.record()
+        s1.synchronize()
+        d2h_gbs = tensor_bytes / (s0.elapsed_time(s1) * 1e-3) / 1e9
+        e2e_ms = 1e3 * e2e_s / e2e_steps
+        in_bytes, out_bytes = 3 * tensor_bytes + bits_bytes, tensor_bytes + lse.numel() * 4
         e2e = {"value": round(world * flops * e2e_steps / e2e_s / 1e12, 2), "unit": "TFLOP/s",
-               "h2d_bytes_per_step": 3 * tensor_bytes + bits_bytes,
-               "d2h_bytes_per_step": tensor_bytes + lse.numel() * 4,
-               "ms_per_step": round(1e3 * e2e_s / e2e_steps, 3), "entry_point": "mattn_fwd_host"}
+               "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
+               "ms_per_step": round(e2e_ms, 3), "entry_point": "mattn_fwd_host",
+               "h2d_gbs": round(h2d_gbs, 1), "d2h_gbs": round(d2h_gbs, 1),
+               "copy_ms_at_those_rates": round(1e3 * (in_bytes / (h2d_gbs * 1e9) + out_bytes / (d2h_gbs * 1e9)), 2),
+               "device_ms_per_step": round(ms_per_step, 3), "kernel_share": round(ms_per_step / e2e_ms, 3),
+               "numa": numa_info(local), "host_cpus": cpu_info()}
         del qh, kh, vh, oh, lh
 
     del q, k, v, o, lse
@@ -309,10 +422,21 @@ def run_gpu(args):
                                      flush=None if in_bytes > 2 * 129e6 else flush)
                 out_bytes = ox.numel() * ox.element_size() + lx.numel() * 4
                 tf = fl / (med * 1e-3) / 1e12
+                t_flop = fl / (peaks["bf16_tflops"] * 1e12)
+                t_byte = (in_bytes + out_bytes) / (peaks["hbm_gbs"] * 1e9)
                 workloads[f"{name}/{m}"] = {
                     "ms": round(med, 4), "tflops": round(tf, 1), "pct_peak": round(100 * tf / peaks["bf16_tflops"], 1),
+                    "pct_own_roofline": round(100 * max(t_flop, t_byte) / (med * 1e-3), 1),
+                    "roofline_bound": "tensor" if t_flop >= t_byte else "hbm",
+                    "schedule": mattn.plan_schedule(mk, wlx.B, wlx.N, wlx.d,
+                                                    mattn.F32 if wlx.dtype == "f32" else mattn.BF16),
                     "pairs": pr, "hbm_gbs_min_traffic": round((in_bytes + out_bytes) / (med * 1e-3) / 1e9, 1),
                     "l2": "inputs > L2" if in_bytes > 2 * 129e6 else "flushed (512 MiB write) before each run"}
+                if rank == 0 and name == "vit16384" and m == "sliding256_rowcol":
+                    # raster heads 0 and 7, column-major heads 8 and 15
+                    rows = sampled_rows(wlx.N, 256, seed=2, extra=40)
+                    chk, _, _ = oracle_check(qx, kx, vx, ox, lx, sp, [0, 7, 8, 15], rows)
+                    parity[f"{name}/{m}"] = chk
             if name == "bsparse128k":
                 # RRAttention's block selection on the same inputs (stride 8,
                 # block 128, tau 0.95): algorithmic work = Eq. 8's product,
@@ -352,9 +476,6 @@ def run_gpu(args):
         if rc != 0:
             raise RuntimeError(f"device error word {word:#x} after the workload sweep")
 
-    cpu = None
-    if rank == 0 and world == 1 and not args.quick:
-        cpu = cpu_baseline(seconds=args.cpu_seconds)
 
     if rank == 0:
         clocks = clk.summary()
@@ -362,15 +483,14 @@ def run_gpu(args):
             "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": wl_name, "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d, "mask": mask_name,
-                       "mask_detail": wl.description, "pairs": pairs, "l2": "inputs larger than L2 (3 GiB)",
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "config": headline_config(wl, mask_name, pairs, world),
             "pct_of_peak": round(100 * value / world / peaks["bf16_tflops"], 1),
             "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
                          "traffic": traffic, "peak_source": peaks["source"] + " burst bf16 (cuBLAS)",
                          "kernel": "attention_fwd_kernel<128,false>"},
             "cpu_baseline": cpu,
+            "parity": parity,
             "e2e": e2e,
             "gpu_launches": args.steps,
             "clocks": clocks,
@@ -380,6 +500,98 @@ def run_gpu(args):
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ oracle comparison and CPU baseline
+def sampled_rows(N: int, edge: int, seed: int, extra: int) -> np.ndarray:
+    """Query rows the oracle checks: the first and last rows, rows on both
+    sides of a block / window edge and of the middle, and `extra` random
+    ones (seeded)."""
+    rng = np.random.default_rng(seed)
+    edges = [0, 1, edge - 1, edge, N // 2 - 1, N // 2, N - edge - 1, N - edge, N - 1]
+    rows = {int(r) for r in edges if 0 <= r < N}
+    rows |= {int(r) for r in rng.choice(N, extra, replace=False)}
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def oracle_check(q, k, v, o, lse, spec, heads, rows):
+    """The fp64 oracle on the GPU arm's own inputs, for the given heads and
+    query rows, against the GPU's outputs.  Returns the errors (max abs and
+    relative L2 over O, max abs over the LSE), the oracle's seconds and the
+    visible pairs of the rows (the FLOP metric's units)."""
+    from oracle import dense
+
+    num = den = 0.0
+    max_abs = lse_err = 0.0
+    secs = 0.0
+    pairs = 0
+    group = q.shape[1] // k.shape[1]
+    for h in heads:
+        qh = q[0, h].float().cpu().numpy()[None, None]
+        kh = k[0, h // group].float().cpu().numpy()[None, None]
+        vh = v[0, h // group].float().cpu().numpy()[None, None]
+        sub = spec_head(spec, h)
+        t0 = time.perf_counter()
+        ro, rl = dense.attention(qh, kh, vh, sub, rows=rows)
+        secs += time.perf_counter() - t0
+        go = o[0, h].float().cpu().numpy()[rows].astype(np.float64)
+        gl = lse[0, h].cpu().numpy()[rows].astype(np.float64)
+        diff = go - ro[0]
+        max_abs = max(max_abs, float(np.abs(diff).max()))
+        num += float((diff ** 2).sum())
+        den += float((ro[0] ** 2).sum())
+        fin = np.isfinite(rl[0])
+        if fin.any():
+            lse_err = max(lse_err, float(np.abs(gl[fin] - rl[0][fin]).max()))
+        pairs += rows_pairs(spec, h, q.shape[2], rows)
+    return {"max_abs": max_abs, "rel_l2": (num / den) ** 0.5 if den > 0 else 0.0, "lse_max_abs": lse_err,
+            "rows": int(len(rows)), "heads": [int(h) for h in heads]}, secs, pairs
+
+
+def rows_pairs(spec, h: int, N: int, rows) -> int:
+    """Visible pairs of the given caller-order query rows of head h."""
+    from oracle import dense
+
+    sub = spec_head(spec, h)
+    pos = dense.inverse_permutation(dense._head_perm(sub, 0), N)
+    return sum(int(dense.dense_mask_strip(sub, 0, N, int(pos[r]), int(pos[r]) + 1).sum()) for r in rows)
+
+
+SINGLE_THREAD_CHILD = r"""
+import sys, time, numpy as np
+sys.path.insert(0, sys.argv[1])
+from oracle import dense
+import pickle
+d = np.load(sys.argv[2], allow_pickle=False)
+with open(sys.argv[3], "rb") as f:
+    spec = pickle.load(f)
+t0 = time.perf_counter()
+dense.attention(d["q"], d["k"], d["v"], spec, rows=d["rows"])
+print(time.perf_counter() - t0)
+"""
+
+
+def oracle_single_thread(q, k, v, spec, h, rows):
+    """Seconds of the oracle on one head's rows in a child process whose BLAS
+    runs one thread (the thread count of a numpy BLAS is fixed at import)."""
+    import pickle
+    import tempfile
+
+    with tempfile.TemporaryDirectory() as tmp:
+        group = q.shape[1] // k.shape[1]
+        data = os.path.join(tmp, "d.npz")
+        np.savez(data, q=q[0, h].float().cpu().numpy()[None, None], k=k[0, h // group].float().cpu().numpy()[None, None],
+                 v=v[0, h // group].float().cpu().numpy()[None, None], rows=rows)
+        sp = os.path.join(tmp, "s.pkl")
+        with open(sp, "wb") as f:
+            pickle.dump(spec_head(spec, h), f)
+        env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+                   BLIS_NUM_THREADS="1")
+        res = subprocess.run([sys.executable, "-c", SINGLE_THREAD_CHILD, ROOT, data, sp], capture_output=True,
+                             text=True, env=env, timeout=600)
+        if res.returncode != 0:
+            return None
+        return float(res.stdout.strip().splitlines()[-1])
 
 
 # ------------------------------------------------------------------ other stages (profiling aid)
@@ -519,24 +731,6 @@ def oracle_sample(seconds_target: float = 15.0):
     return tf, t_total, done_rows, desc
 
 
-def cpu_cores() -> int:
-    try:
-        import threadpoolctl
-
-        info = threadpoolctl.threadpool_info()
-        n = max((i.get("num_threads", 0) for i in info), default=0)
-        if n:
-            return int(n)
-    except Exception:
-        pass
-    return len(os.sched_getaffinity(0))
-
-
-def cpu_baseline(seconds: float = 15.0):
-    tf, secs, rows, desc = oracle_sample(seconds)
-    return {"value": round(tf, 6), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle", "sample": desc}
-
-
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -552,15 +746,18 @@ def run_reference(args):
         secs += s
         rows_total += rows
     value = statistics.mean(vals)
-    from workloads import WORKLOADS
+    from workloads import WORKLOADS, make_mask
 
     wl = WORKLOADS[HEADLINE[0]]
+    spec = make_mask(wl, HEADLINE[1], seed=0)
+    ci = cpu_info()
     line = {
         "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 1), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-        "config": {"workload": HEADLINE[0], "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d, "mask": HEADLINE[1]},
-        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+        "config": headline_config(wl, HEADLINE[1], block_mask_pairs(spec, wl.N, wl.B), world),
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": ci["affinity"], "cores_detail": ci,
+                         "kind": "oracle",
                          "sample": f"{rows_total} sampled query rows of head 0 over {args.steps} steps"},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }

@@ -81,7 +81,7 @@ class MaskDesc(ctypes.Structure):
 EXPORTS = (
     "mattn_fwd", "mattn_fwd_gqa", "mattn_fwd_host", "mattn_fwd_noalloc", "mattn_decode", "mattn_rr_select",
     "mattn_received",
-    "mattn_count_pairs", "mattn_plan_tiles", "mattn_plan_tiles_device",
+    "mattn_count_pairs", "mattn_plan_schedule", "mattn_plan_tiles", "mattn_plan_tiles_device",
     "mattn_device_status", "mattn_set_wait_timeout_ns", "mattn_status_string", "mattn_last_error",
     "mattn_version",
 )
@@ -110,6 +110,7 @@ def lib() -> ctypes.CDLL:
                                   vp, vp, vp]
     L.mattn_received.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, dp, vp]
     L.mattn_count_pairs.argtypes = [dp, i32, i32, i32, u64p]
+    L.mattn_plan_schedule.argtypes = [dp, i32, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_uint32)]
     L.mattn_plan_tiles.argtypes = [dp, i32, i32, vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]
     L.mattn_plan_tiles_device.argtypes = [dp, i32, i32, vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t), vp]
     L.mattn_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
@@ -120,7 +121,7 @@ def lib() -> ctypes.CDLL:
     L.mattn_last_error.argtypes = []
     L.mattn_version.argtypes = []
     for name in ("mattn_fwd", "mattn_fwd_gqa", "mattn_fwd_host", "mattn_fwd_noalloc", "mattn_decode", "mattn_rr_select", "mattn_received",
-                 "mattn_count_pairs", "mattn_plan_tiles",
+                 "mattn_count_pairs", "mattn_plan_schedule", "mattn_plan_tiles",
                  "mattn_plan_tiles_device", "mattn_device_status", "mattn_set_wait_timeout_ns",
                  "mattn_version"):
         getattr(L, name).restype = ctypes.c_int
@@ -225,10 +226,24 @@ class PreparedMask:
         return d
 
 
+_SCHEDULE_NAMES = {FLAG_SCHEDULE_PAIRED: "paired", FLAG_SCHEDULE_SPLIT: "split", FLAG_SCHEDULE_SINGLE: "single",
+                   FLAG_SCHEDULE_PERSISTENT: "persistent"}
+
+
+def plan_schedule(mask: "PreparedMask", B: int, N: int, d: int, dtype: int = None) -> str:
+    """The schedule the library runs for this mask and shape ("paired",
+    "split", "single" or "persistent"); host only."""
+    out = ctypes.c_uint32(0)
+    _check(lib().mattn_plan_schedule(ctypes.byref(mask.desc), B, mask.H, N, d, BF16 if dtype is None else dtype,
+                                     ctypes.byref(out)))
+    return _SCHEDULE_NAMES[out.value]
+
+
 def prepare(spec, H: int, N: int, device="cuda", scale: Optional[float] = None,
             schedule: Optional[str] = None) -> PreparedMask:
-    """schedule: None / "auto" (library's choice), "paired" or "split" (the
-    MATTN_FLAG_SCHEDULE_* flags); the result is the same up to rounding."""
+    """schedule: None / "auto" (library's choice), "paired", "split", "single"
+    or "persistent" (the MATTN_FLAG_SCHEDULE_* flags); the result is the same
+    up to rounding."""
     return PreparedMask(spec, H, N, device=device, scale=scale, schedule=schedule)
 
 

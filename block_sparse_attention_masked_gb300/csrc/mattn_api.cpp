@@ -1237,6 +1237,19 @@ int mattn_rr_select(const void* q, const void* k, int B, int H, int N, int d, in
   return MATTN_OK;
 }
 
+int mattn_plan_schedule(const mattn_mask_desc* desc, int B, int H, int N, int d, int dtype,
+                        uint32_t* schedule_out) {
+  if (!schedule_out) return fail(MATTN_ERR_INVALID_ARG, "schedule_out is NULL");
+  Normalized n;
+  int rc = normalize(desc, B, H, N, d, dtype, true, &n);
+  if (rc) return rc;
+  *schedule_out = n.single       ? MATTN_FLAG_SCHEDULE_SINGLE
+                  : n.persistent ? MATTN_FLAG_SCHEDULE_PERSISTENT
+                  : n.split      ? MATTN_FLAG_SCHEDULE_SPLIT
+                                 : MATTN_FLAG_SCHEDULE_PAIRED;
+  return MATTN_OK;
+}
+
 int mattn_count_pairs(const mattn_mask_desc* desc, int B, int H, int N, uint64_t* pairs_out) {
   if (!pairs_out) return fail(MATTN_ERR_INVALID_ARG, "pairs_out is NULL");
   Normalized n;

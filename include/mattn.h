@@ -353,6 +353,18 @@ int mattn_rr_select(const void* q, const void* k, int B, int H, int N, int d, in
                     uint64_t* block_bits, float* block_scores, void* stream);
 
 /*
+ * mattn_plan_schedule -- the schedule mattn_fwd would run for these
+ * arguments: one of the MATTN_FLAG_SCHEDULE_* flags (PAIRED, SPLIT, SINGLE,
+ * PERSISTENT), the descriptor's own flag if it sets one, else the
+ * library's choice (see the schedule flags above).  Host only: validates
+ * the arguments as mattn_fwd does (block_bits may be any non-NULL pointer,
+ * it is not read) and launches nothing.  The choice follows the rules the
+ * library states, not the pages: the pages have no counterpart.
+ */
+int mattn_plan_schedule(const mattn_mask_desc* desc, int B, int H, int N, int d, int dtype,
+                        uint32_t* schedule_out);
+
+/*
  * mattn_count_pairs -- exact number of visible (query, key) pairs summed over
  * B and H (the unit of the effective-FLOP count, 4*d FLOPs per pair).  Host
  * only; block_bits are read as HOST memory.

@@ -233,3 +233,47 @@ def test_column_major_grid_description_matches_explicit_order(L):
     b = mattn.PreparedMask(explicit, 1, n, host_side=True).host_desc()
     assert a.head_order[0] == mattn.ORDER_COLUMN_MAJOR and (a.grid_rows, a.grid_cols) == (16, 16)
     assert b.head_order[0] == 0 and b.n_perm == 1
+
+
+def test_plan_schedule_follows_the_stated_rules(L):
+    """The schedule mattn_fwd runs, on the host: a flag wins; otherwise SPLIT
+    for 128-blocks, SINGLE at head dim 256, PERSISTENT for interval masks
+    whose query tiles see about 12 key tiles or fewer, PAIRED for the rest."""
+    from workloads import WORKLOADS, make_mask
+
+    def sched(wl_name, mask, d=None, flags=None):
+        wl = WORKLOADS[wl_name]
+        spec = make_mask(wl, mask, seed=0)
+        pm = mattn.prepare(spec, wl.H, wl.N, device="cpu")
+        if flags is not None:
+            pm.desc.flags = flags
+        return mattn.plan_schedule(pm, wl.B, wl.N, d or wl.d, mattn.F32 if wl.dtype == "f32" else mattn.BF16)
+
+    assert sched("vit16384", "sliding256_rowcol") == "persistent"
+    assert sched("vit16384", "chunk512") == "persistent"
+    assert sched("vit16384", "full") == "paired"
+    assert sched("vit4096", "sliding128") == "persistent"
+    assert sched("causal4096", "causal_window_sink") == "paired"  # windows up to 4096: ~16 tiles on average
+    assert sched("gqa32k", "swa572_sinktok4") == "persistent"
+    assert sched("bsparse128k", "block128") == "split"
+    assert sched("prefill_d256", "swa576_sink") == "single"
+    assert sched("vit16384", "sliding256_rowcol", flags=mattn.FLAG_SCHEDULE_PAIRED) == "paired"
+    assert sched("vit16384", "full", flags=mattn.FLAG_SCHEDULE_PERSISTENT) == "persistent"
+    out = ctypes.c_uint32(0)
+    assert L.mattn_plan_schedule(None, 1, 1, 128, 64, mattn.BF16, ctypes.byref(out)) == mattn.ERR_INVALID_ARG
+
+
+def test_bench_pair_count_matches_the_oracle():
+    """The reference arm's closed-form pair count of a block mask (kept
+    blocks below the diagonal Bs^2 each, kept diagonal blocks Bs(Bs+1)/2)
+    equals the oracle's count from the dense mask."""
+    import bench
+    from oracle import dense
+    from workloads import MaskSpec, bernoulli_causal_blocks
+
+    n, H = 1024, 3
+    spec = MaskSpec("block", [128] * H, block=bernoulli_causal_blocks(H, n // 128, 5))
+    assert bench.block_mask_pairs(spec, n) == dense.pair_count(spec, n, n_heads=H)
+    assert bench.block_mask_pairs(spec, n, B=2) == 2 * dense.pair_count(spec, n, n_heads=H)
+    one = bench.spec_head(spec, 2)
+    assert one.head_param == [128] and np.array_equal(np.asarray(one.block)[0], np.asarray(spec.block)[2])
