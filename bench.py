@@ -37,6 +37,7 @@ import numpy as np  # noqa: E402
 METRIC = "effective attention TFLOP/s (unmasked FLOPs) and % of GB300 BF16 peak"
 HEADLINE = ("bsparse128k", "block128")
 KERNEL_SOURCES = ["block_sparse_attention_masked_gb300/csrc/attention_fwd.cu",
+                  "block_sparse_attention_masked_gb300/csrc/attention_tiles.cuh",
                   "block_sparse_attention_masked_gb300/csrc/ptx.cuh",
                   "block_sparse_attention_masked_gb300/csrc/plan_rules.h",
                   "block_sparse_attention_masked_gb300/csrc/tile_mma.cuh"]

@@ -560,6 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
         const int c_begin = (p.split && s == 1) ? kOHalf<D>() : 0;
         const int c_end = (p.split && s == 0) ? kOHalf<D>() : D;
         const uint32_t oo_tmem = tmem + lane_off + 256 + (s ^ 1) * 128;
+        const uint64_t o_policy = ptx::l2_policy_evict_first();
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 16) {
           if (c0 < c_begin || c0 >= c_end) continue;  // warp-uniform
@@ -581,17 +582,24 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
             for (int i = 0; i < 16; ++i) ov[i] = fmaf(ow[i], oo_scale, ov[i]);
           }
           if (valid) {
+            // O is written once and never re-read here: evict it from L2
+            // first, so that it does not push out the K / V tiles other
+            // query tiles of the head still read
             if (OUT_F32) {
-              float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.o) + orow + c0);
+              uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<float*>(p.o) + orow + c0);
 #pragma unroll
-              for (int i = 0; i < 4; ++i) dst[i] = make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
+              for (int i = 0; i < 4; ++i)
+                ptx::st_global_v4_hint(dst + i,
+                                       make_uint4(__float_as_uint(ov[4 * i]), __float_as_uint(ov[4 * i + 1]),
+                                                  __float_as_uint(ov[4 * i + 2]), __float_as_uint(ov[4 * i + 3])),
+                                       o_policy);
             } else {
               uint32_t pk[8];
 #pragma unroll
               for (int i = 0; i < 8; ++i) pk[i] = ptx::pack_bf16x2(ov[2 * i], ov[2 * i + 1]);
               uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + orow + c0);
-              dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-              dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+              ptx::st_global_v4_hint(dst, make_uint4(pk[0], pk[1], pk[2], pk[3]), o_policy);
+              ptx::st_global_v4_hint(dst + 1, make_uint4(pk[4], pk[5], pk[6], pk[7]), o_policy);
             }
           }
         }

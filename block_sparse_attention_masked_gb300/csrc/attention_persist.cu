@@ -579,7 +579,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
             break;
           }
           if (leader) {
-            store_tile<D>(p, pi.load, stage, sp.qt * kTile, pi.ip.bh);
+            store_tile<D>(p, pi.load, stage, sp.qt * kTile, pi.ip.bh, ptx::l2_policy_evict_first());
             ptx::bulk_commit_group();
           }
         }
@@ -602,12 +602,14 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
 #pragma unroll
               for (int i = 0; i < 4; ++i) dst[i] = make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
             } else {
+              // written once, not re-read: evicted from L2 first
+              const uint64_t o_policy = ptx::l2_policy_evict_first();
               uint32_t pk[8];
 #pragma unroll
               for (int i = 0; i < 8; ++i) pk[i] = ptx::pack_bf16x2(ov[2 * i], ov[2 * i + 1]);
               uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + orow + c0);
-              dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-              dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+              ptx::st_global_v4_hint(dst, make_uint4(pk[0], pk[1], pk[2], pk[3]), o_policy);
+              ptx::st_global_v4_hint(dst + 1, make_uint4(pk[4], pk[5], pk[6], pk[7]), o_policy);
             }
           }
         }

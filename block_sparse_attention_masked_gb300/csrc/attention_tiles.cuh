@@ -276,28 +276,34 @@ __device__ __forceinline__ void load_v_tile(const FwdParams& p, int mode, uint8_
 // TMA store of one 128-row O tile from shared memory (laid out as
 // load_tile writes a Q tile) to the output rows at sequence positions
 // [p0, p0 + 128) of row block bh, through the O view of the head's order
-// (`mode`, a LoadMode; requires p.o_tma).  Rows past N are clipped.
+// (`mode`, a LoadMode; requires p.o_tma).  Rows past N are clipped.  O is
+// written once and not re-read: its lines go first out of L2 (`policy`,
+// evict-first), ahead of the K / V tiles other query tiles still read.
 template <int D>
-__device__ __forceinline__ void store_tile(const FwdParams& p, int mode, const uint8_t* src, int p0, int bh) {
+__device__ __forceinline__ void store_tile(const FwdParams& p, int mode, const uint8_t* src, int p0, int bh,
+                                           uint64_t policy) {
   using G = Geo<D>;
   if (mode == kLoadRaster) {
 #pragma unroll
-    for (int c = 0; c < G::kChunks; ++c) ptx::tma_store_3d(&p.o_raster[0], src + c * G::kChunkBytes, c * 64, p0, bh);
-    if (G::kRem) ptx::tma_store_3d(&p.o_raster[1], src + G::kChunks * G::kChunkBytes, 0, p0, bh);
+    for (int c = 0; c < G::kChunks; ++c)
+      ptx::tma_store_3d_hint(&p.o_raster[0], src + c * G::kChunkBytes, c * 64, p0, bh, policy);
+    if (G::kRem) ptx::tma_store_3d_hint(&p.o_raster[1], src + G::kChunks * G::kChunkBytes, 0, p0, bh, policy);
   } else if (mode == kLoadBlock2x2Row || mode == kLoadBlock2x2Col) {
     const CUtensorMap* blocks = mode == kLoadBlock2x2Row ? p.o_blk : p.o_blkc;
     int c3, c4;
     block2x2_coords(p, mode, p0, bh, &c3, &c4);
 #pragma unroll
-    for (int c = 0; c < G::kChunks; ++c) ptx::tma_store_5d(&blocks[0], src + c * G::kChunkBytes, c * 64, 0, 0, c3, c4);
-    if (G::kRem) ptx::tma_store_5d(&blocks[1], src + G::kChunks * G::kChunkBytes, 0, 0, 0, c3, c4);
+    for (int c = 0; c < G::kChunks; ++c)
+      ptx::tma_store_5d_hint(&blocks[0], src + c * G::kChunkBytes, c * 64, 0, 0, c3, c4, policy);
+    if (G::kRem) ptx::tma_store_5d_hint(&blocks[1], src + G::kChunks * G::kChunkBytes, 0, 0, 0, c3, c4, policy);
   } else {
     const int col = p0 / p.grid_rows;
     const int r0 = p0 - col * p.grid_rows;
 #pragma unroll
     for (int c = 0; c < G::kChunks; ++c)
-      ptx::tma_store_4d(&p.o_colmaj[0], src + c * G::kChunkBytes, c * 64, col, r0, bh);
-    if (G::kRem) ptx::tma_store_4d(&p.o_colmaj[1], src + G::kChunks * G::kChunkBytes, 0, col, r0, bh);
+      ptx::tma_store_4d_hint(&p.o_colmaj[0], src + c * G::kChunkBytes, c * 64, col, r0, bh, policy);
+    if (G::kRem)
+      ptx::tma_store_4d_hint(&p.o_colmaj[1], src + G::kChunks * G::kChunkBytes, 0, col, r0, bh, policy);
   }
 }
 

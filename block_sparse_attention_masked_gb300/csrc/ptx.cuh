@@ -210,26 +210,32 @@ __device__ __forceinline__ void tma_load_5d_hint(void* dst, const CUtensorMap* t
       : "memory");
 }
 
-// TMA stores of a shared-memory tile to a tensor (bulk-group completion):
-// the tile's layout is the one a load through the same map would write.
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* tm, const void* src, int c0, int c1, int c2) {
-  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-                   reinterpret_cast<uint64_t>(tm)),
-               "r"(smem_addr(src)), "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
+// TMA stores of a shared-memory tile to a tensor (bulk-group completion),
+// with an L2 eviction-priority hint (policy operand): the tile's layout is
+// the one a load through the same map would write.
+__device__ __forceinline__ void tma_store_3d_hint(const CUtensorMap* tm, const void* src, int c0, int c1, int c2,
+                                                  uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3, %4}], [%1], %5;" ::"l"(
+          reinterpret_cast<uint64_t>(tm)),
+      "r"(smem_addr(src)), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+      : "memory");
 }
-__device__ __forceinline__ void tma_store_4d(const CUtensorMap* tm, const void* src, int c0, int c1, int c2, int c3) {
-  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
-                   reinterpret_cast<uint64_t>(tm)),
-               "r"(smem_addr(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-               : "memory");
+__device__ __forceinline__ void tma_store_4d_hint(const CUtensorMap* tm, const void* src, int c0, int c1, int c2,
+                                                  int c3, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3, %4, %5}], [%1], %6;" ::"l"(
+          reinterpret_cast<uint64_t>(tm)),
+      "r"(smem_addr(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(policy)
+      : "memory");
 }
-__device__ __forceinline__ void tma_store_5d(const CUtensorMap* tm, const void* src, int c0, int c1, int c2, int c3,
-                                             int c4) {
-  asm volatile("cp.async.bulk.tensor.5d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5, %6}], [%1];" ::"l"(
-                   reinterpret_cast<uint64_t>(tm)),
-               "r"(smem_addr(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
-               : "memory");
+__device__ __forceinline__ void tma_store_5d_hint(const CUtensorMap* tm, const void* src, int c0, int c1, int c2,
+                                                  int c3, int c4, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3, %4, %5, %6}], [%1], %7;" ::"l"(
+          reinterpret_cast<uint64_t>(tm)),
+      "r"(smem_addr(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "l"(policy)
+      : "memory");
 }
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // The shared-memory sources of this thread's committed bulk stores have been read.
@@ -237,6 +243,14 @@ __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bu
 // This thread's committed bulk stores have completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+
+// 16-byte global store with an L2 eviction-priority hint (a policy made by
+// l2_policy_evict_first / _last), not allocated in L1.
+__device__ __forceinline__ void st_global_v4_hint(void* ptr, uint4 v, uint64_t policy) {
+  asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w), "l"(policy)
+               : "memory");
+}
 
 // L2 policies: keep (K, V tiles that many query tiles re-read) or drop
 // first (Q tiles, read once).
