@@ -392,3 +392,21 @@ def test_block2x2_orders_other_paths():
     ref = dense.received_attention(_host(qb), _host(kb), spec)
     got = _host(r)[0].astype(np.float64)
     assert (np.abs(got - ref) <= 2e-3 * ref + 1e-5).all()
+
+
+@pytest.mark.parametrize("d", [64, 80])
+def test_chunk2d_order(d):
+    """SWA-1D over the chunk-window order (SHS slides, Factor 2 background,
+    order (b)): the grid walked window by window, passed as an explicit
+    per-head order (the reorder copy), next to a raster head; a 64 x 64
+    grid in 8 x 8 windows and a 32 x 96 grid in 16 x 16 windows, which
+    puts window boundaries inside query tiles."""
+    from workloads import chunk2d_order
+
+    for rows, cols, win in ((64, 64, 8), (32, 96, 16)):
+        n = rows * cols
+        q, k, v = _qkv(1, 3, n, d, seed=rows + cols + d)
+        perm = [chunk2d_order(rows, cols, win), None, chunk2d_order(rows, cols, 2)]
+        for spec in (MaskSpec("sliding", [64, 64, 200], perm=perm),
+                     MaskSpec("chunk", [win * win, 128, 256], perm=perm, sink=np.array([0.3, -1.0, 0.0]))):
+            check(q, k, v, spec, tag=f"chunk2d {spec.kind} {rows}x{cols}/{win} d{d}")

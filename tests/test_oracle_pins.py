@@ -560,3 +560,41 @@ def test_block2x2_orders_hand_written():
     o, _ = dense.attention(q, q, v, spec)
     # token 5 sits at position 3, its window holds positions 2..4 = tokens 4, 5, 2
     np.testing.assert_allclose(o[0, 5], v[0, 0, [4, 5, 2]].mean(axis=0))
+
+
+def test_chunk2d_order_states_what_the_page_states():
+    """Order (b), Qwen2.5-VL's chunk windows walked window by window, on the
+    page's 4 x 8 grid: the window split, the anchor-15 window (positions
+    7..23) and where positions 16-23 land, all as the slide states them; the
+    walk inside a window is our reading, pinned only by the hand-written row
+    of the golden file."""
+    from workloads import chunk2d_order
+
+    lines = {}
+    for row in read_golden("chunk2d_order_4x8.txt"):
+        lines.setdefault(row[0], []).append(row[1:])
+    perm = chunk2d_order(4, 8, 4)
+    rows, cols = perm // 8, perm % 8
+    for w in lines["window"]:
+        p0, p1, c0, c1 = int(w[2]), int(w[3]), int(w[5]), int(w[6])
+        assert set(cols[p0:p1 + 1]) == set(range(c0, c1 + 1)) and set(rows[p0:p1 + 1]) == {0, 1, 2, 3}
+    a, lo, hi = (int(x) for x in (lines["anchor"][0][0], lines["anchor"][0][2], lines["anchor"][0][3]))
+    s0, s1 = (int(x) for x in lines["same_window"][0])
+    assert (cols[s0:s1 + 1] < 4).all() and cols[a] < 4
+    u = lines["upper_half"][0]
+    p0, p1, r0, r1, c0, c1 = int(u[0]), int(u[1]), int(u[3]), int(u[4]), int(u[6]), int(u[7])
+    assert set(rows[p0:p1 + 1]) == set(range(r0, r1 + 1)) and set(cols[p0:p1 + 1]) == set(range(c0, c1 + 1))
+    assert list(perm) == [int(x) for x in lines["reading"][0]]
+    # the oracle's sliding window over this order: the anchor's keys are the
+    # tokens at positions 7..23 (q = 0: O is their plain mean)
+    spec = _one_head("sliding", 8, perm=perm)
+    q = np.zeros((1, 1, 32, 2))
+    v = np.arange(64, dtype=np.float64).reshape(1, 1, 32, 2)
+    o, lse = dense.attention(q, q, v, spec)
+    anchor_token = int(perm[a])
+    np.testing.assert_allclose(o[0, anchor_token], v[0, 0, perm[lo:hi + 1]].mean(axis=0))
+    np.testing.assert_allclose(lse[0, anchor_token], np.log(hi - lo + 1))
+    # and on a real grid the generator is a permutation in windows of win x win
+    big = chunk2d_order(64, 64, 8)
+    assert np.array_equal(np.sort(big), np.arange(64 * 64))
+    assert set(big[:64] // 64) == set(range(8)) and set(big[:64] % 64) == set(range(8))

@@ -83,6 +83,31 @@ def block2x2_order(rows: int, cols: int, by_columns: bool = False) -> np.ndarray
     return ((2 * R + dr) * cols + 2 * C + dc).astype(np.int64)
 
 
+def chunk2d_order(rows: int, cols: int, win: int) -> np.ndarray:
+    """perm[p] for the chunk-window walk of a rows x cols raster-numbered
+    grid (SHS slides, Factor 2 background, order (b): Qwen2.5-VL's chunk
+    windows, every block of window 0 walked before window 1).  The grid is
+    cut into win x win-patch windows, taken left to right then top to
+    bottom; inside a window its 2x2 patch blocks go left to right then top to
+    bottom, and inside a block the four patches in raster order (the figure
+    is not in the text: the walk inside a window is our reading, the window
+    by window part is the slide's).  win must be even and divide rows and
+    cols."""
+    if win % 2 or rows % win or cols % win:
+        raise ValueError("win must be even and divide the grid")
+    out = []
+    for wr in range(rows // win):
+        for wc in range(cols // win):
+            for br in range(win // 2):
+                for bc in range(win // 2):
+                    for dr in range(2):
+                        for dc in range(2):
+                            r = wr * win + 2 * br + dr
+                            c = wc * win + 2 * bc + dc
+                            out.append(r * cols + c)
+    return np.array(out, dtype=np.int64)
+
+
 def random_order(n: int, seed: int) -> np.ndarray:
     return np.random.default_rng(seed).permutation(n).astype(np.int64)
 
