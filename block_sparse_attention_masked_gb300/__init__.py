@@ -28,6 +28,10 @@ import numpy as np
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmattn.so")
+# The same library with device bounds checks compiled in (MATTN_DEBUG=1):
+# loaded instead of LIB_PATH when the environment sets MATTN_DEBUG=1, or
+# after use_debug_library(True).
+DEBUG_LIB_PATH = os.path.join(_PKG, "libmattn_debug.so")
 
 OK = 0
 ERR_INVALID_ARG = -1
@@ -36,6 +40,11 @@ ERR_CUDA = -3
 ERR_TIMEOUT = -4
 ERR_NO_DEVICE = -5
 ERR_CAPACITY = -6
+ERR_BOUNDS = -7
+# device error-word bits of a failed debug check (mattn.h, "Debug library")
+ERRW_BOUNDS = 1 << 5
+ERRW_SITE = {"item": 1 << 8, "key_tile": 1 << 9, "load": 1 << 10, "store": 1 << 11, "order": 1 << 12,
+             "ring": 1 << 13}
 
 KIND = {"full": 0, "chunk": 1, "sliding": 2, "causal_window": 3, "block": 4}
 BF16, F32 = 0, 1
@@ -82,22 +91,38 @@ EXPORTS = (
     "mattn_fwd", "mattn_fwd_gqa", "mattn_fwd_host", "mattn_fwd_noalloc", "mattn_decode", "mattn_rr_select",
     "mattn_received",
     "mattn_count_pairs", "mattn_plan_schedule", "mattn_plan_tiles", "mattn_plan_tiles_device",
-    "mattn_device_status", "mattn_set_wait_timeout_ns", "mattn_status_string", "mattn_last_error",
-    "mattn_version",
+    "mattn_device_status", "mattn_debug_checks", "mattn_set_wait_timeout_ns", "mattn_status_string",
+    "mattn_last_error", "mattn_version",
 )
 
 _lib = None
+_libs = {}
+_use_debug = os.environ.get("MATTN_DEBUG", "0") not in ("", "0")
+
+
+def use_debug_library(on: bool = True) -> None:
+    """Route every later call to libmattn_debug.so (on) or libmattn.so.
+    Each library keeps its own device state (plans, workspaces, error
+    word); both may be loaded in one process."""
+    global _lib, _use_debug
+    _use_debug = bool(on)
+    _lib = None
 
 
 def lib() -> ctypes.CDLL:
-    """Load libmattn.so (built by ``build.py`` / ``__graft_entry__.build()``)."""
+    """Load libmattn.so, or libmattn_debug.so (built by ``build.py`` /
+    ``__graft_entry__.build()``)."""
     global _lib
     if _lib is not None:
         return _lib
-    if not os.path.exists(LIB_PATH):
-        raise RuntimeError(f"libmattn.so is not built ({LIB_PATH}); run "
+    path = DEBUG_LIB_PATH if _use_debug else LIB_PATH
+    if path in _libs:
+        _lib = _libs[path]
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{os.path.basename(path)} is not built ({path}); run "
                            "python -m block_sparse_attention_masked_gb300.build")
-    L = ctypes.CDLL(LIB_PATH)
+    L = ctypes.CDLL(path)
     vp, i32, u64p = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_uint64)
     dp = ctypes.POINTER(MaskDesc)
     L.mattn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, dp, vp]
@@ -114,6 +139,7 @@ def lib() -> ctypes.CDLL:
     L.mattn_plan_tiles.argtypes = [dp, i32, i32, vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]
     L.mattn_plan_tiles_device.argtypes = [dp, i32, i32, vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t), vp]
     L.mattn_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    L.mattn_debug_checks.argtypes = []
     L.mattn_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
     L.mattn_status_string.restype = ctypes.c_char_p
     L.mattn_status_string.argtypes = [i32]
@@ -122,9 +148,10 @@ def lib() -> ctypes.CDLL:
     L.mattn_version.argtypes = []
     for name in ("mattn_fwd", "mattn_fwd_gqa", "mattn_fwd_host", "mattn_fwd_noalloc", "mattn_decode", "mattn_rr_select", "mattn_received",
                  "mattn_count_pairs", "mattn_plan_schedule", "mattn_plan_tiles",
-                 "mattn_plan_tiles_device", "mattn_device_status", "mattn_set_wait_timeout_ns",
-                 "mattn_version"):
+                 "mattn_plan_tiles_device", "mattn_device_status", "mattn_debug_checks",
+                 "mattn_set_wait_timeout_ns", "mattn_version"):
         getattr(L, name).restype = ctypes.c_int
+    _libs[path] = L
     _lib = L
     return L
 

@@ -125,7 +125,9 @@ __device__ __forceinline__ void build_block_list(const FwdParams& p, int2 item, 
           if (kt > km) break;
           const uint32_t use0 = (((u0 >> bpos) & 1ull) && kt <= km0) ? 1u : 0u;
           const uint32_t use1 = (((u1 >> bpos) & 1ull) && kt <= km1) ? 1u : 0u;
-          list[pos++] = (uint32_t)kt | (use0 << 30) | (use1 << 31);
+          // (debug builds: never past the list's capacity; the kernel checks the count)
+          if (!kDebugChecks || pos < kMaxList) list[pos] = (uint32_t)kt | (use0 << 30) | (use1 << 31);
+          ++pos;
           used0 += (int)use0;
           used1 += (int)use1;
         }
@@ -168,8 +170,9 @@ __device__ __forceinline__ void issue_q_loads(const FwdParams& p, const ItemPlan
     const SubPlan& sp = s ? ip.sp1 : ip.sp0;
     if (!list_has(L, s, p.split) || (p.split && s == 1)) continue;  // split: one Q tile for both pipelines
     ptx::mbar_arrive_expect_tx(&bar->q_full[s], G::kTileBytes);
-    load_tile<D>(p, false, load_mode, sq + s * G::kTileBytes, &bar->q_full[s], sp.qt * kTile, ip.bh,
-                 ptx::l2_policy_evict_first());
+    if (!load_tile<D>(p, false, load_mode, sq + s * G::kTileBytes, &bar->q_full[s], sp.qt * kTile, ip.bh,
+                      ptx::l2_policy_evict_first()))
+      abort_cta(bar);
   }
 }
 
@@ -190,6 +193,12 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int2 item = p.items[blockIdx.x];
+  // debug builds: a work item outside the launch's heads and query tiles
+  // ends the CTA here, before any barrier or allocation
+  if (!item_in_range(p, blockIdx.x, item)) {
+    if (threadIdx.x == 0) debug_check(p.err, false, kSiteItem);
+    if (kDebugChecks) return;
+  }
   // the head's row of the per-head table (param, load, store, perm_row) in
   // one load
   const int4 head_row = __ldg(reinterpret_cast<const int4*>(p.head_info) + item.x % p.H);
@@ -238,9 +247,13 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
       k_early = L0.n < KS ? L0.n : KS;
       const uint64_t keep = ptx::l2_policy_evict_last();
       for (int j = 0; j < k_early; ++j) {  // fresh ring slots: nothing to wait for
+        const int kt = list_kt(L0, j);
+        if (!check_or_abort(p, bar, key_tile_ok(p, kt), kSiteKeyTile)) break;
         ptx::mbar_arrive_expect_tx(&bar->k_full[j], G::kTileBytes);
-        load_tile<D>(p, true, load_mode, sk + j * G::kTileBytes, &bar->k_full[j], list_kt(L0, j) * kTile,
-                     ip.bh_kv, keep);
+        if (!load_tile<D>(p, true, load_mode, sk + j * G::kTileBytes, &bar->k_full[j], kt * kTile, ip.bh_kv, keep)) {
+          abort_cta(bar);
+          break;
+        }
       }
     }
   }
@@ -253,7 +266,15 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
   ptx::tc_fence_after();
   const uint32_t tmem = bar->tmem_base;
 
-  if (threadIdx.x == 0) bar->tl = make_list(p, ip, list_e, bar->list_n);
+  if (threadIdx.x == 0) {
+    bar->tl = make_list(p, ip, list_e, bar->list_n);
+    // debug builds: a block list past its capacity is dropped (nothing read
+    // beyond the entries written)
+    if (p.kind == kBlockSparse && !check_or_abort(p, bar, bar->list_n[0] <= kMaxList, kSiteKeyTile)) {
+      bar->tl.n = 0;
+      bar->tl.use_n0 = bar->tl.use_n1 = 0;
+    }
+  }
   __syncthreads();
   const TileList& L = bar->tl;
 
@@ -282,16 +303,20 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
       for (int j = is_k ? k_early : 0; j < L.n; ++j) {
         const int kt = list_kt(L, j);
         const int slot = j % S;
+        if (debug_aborted(abort_flag) || !check_or_abort(p, bar, key_tile_ok(p, kt), kSiteKeyTile)) break;
         if (!ptx::mbar_wait(&empty[slot], ((j / S) & 1) ^ 1, p.timeout_ns, abort_flag)) {
           raise_error(p, bar, kErrProducer);
           break;
         }
         ptx::mbar_arrive_expect_tx(&full[slot], G::kTileBytes);
-        if (is_k)
-          load_tile<D>(p, true, load_mode, ring + slot * G::kTileBytes, &full[slot], kt * kTile, ip.bh_kv,
-                       keep);
-        else
-          load_v_tile<D>(p, load_mode, ring + slot * G::kTileBytes, &full[slot], kt * kTile, ip.bh_kv, keep);
+        const bool issued =
+            is_k ? load_tile<D>(p, true, load_mode, ring + slot * G::kTileBytes, &full[slot], kt * kTile, ip.bh_kv,
+                                keep)
+                 : load_v_tile<D>(p, load_mode, ring + slot * G::kTileBytes, &full[slot], kt * kTile, ip.bh_kv, keep);
+        if (!issued) {
+          abort_cta(bar);
+          break;
+        }
       }
       if (*abort_flag) {
         // let copies already in flight land before the CTA's shared memory goes away
@@ -551,10 +576,11 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
         // the common maximum; the LSE from the same normaliser
         float o_scale, oo_scale, lse_v;
         finalize_row(m, l, m_o, l_o, bar->sink_log2, &o_scale, &oo_scale, &lse_v);
-        const bool valid = pos < p.N;
+        bool valid = pos < p.N;
         const int store_mode = bar->head_store;
         const int perm_row = bar->head_perm_row;
-        const int64_t tok = valid ? token_of(p, store_mode, perm_row, pos) : 0;
+        const int64_t tok = valid ? out_token(p, store_mode, perm_row, pos) : 0;
+        if (kDebugChecks && tok < 0) valid = false;
         const int64_t orow = ((int64_t)ip.bh * p.N + tok) * D;
         // columns written: all (paired); this sub-tile's half (split)
         const int c_begin = (p.split && s == 1) ? kOHalf<D>() : 0;
@@ -670,11 +696,12 @@ __global__ void gather_kernel(const GatherParams p) {
   const int64_t bh = row / p.N;
   const int h = (int)(bh % p.H);
   const int store_mode = p.head_info[h * 4 + kHeadStore];
+  const int perm_row = p.head_info[h * 4 + kHeadPermRow];
+  // debug builds: the head's explicit-order row and the token it holds
+  if (!debug_check(p.err, store_mode != kStoreExplicit || (perm_row >= 0 && perm_row < p.n_perm), kSiteItem)) return;
   const int64_t tok = token_at(store_mode, p.grid_rows, p.grid_cols,
-                               store_mode == kStoreExplicit
-                                   ? p.perm + (int64_t)p.head_info[h * 4 + kHeadPermRow] * p.N
-                                   : nullptr,
-                               pos);
+                               store_mode == kStoreExplicit ? p.perm + (int64_t)perm_row * p.N : nullptr, pos);
+  if (!debug_check(p.err, tok >= 0 && tok < p.N, kSiteOrder)) return;
   const int64_t src_bh = t == 0 ? bh : (bh / p.H) * (p.H / p.kv_group) + h / p.kv_group;
   const int64_t src_off = (src_bh * p.N + tok) * p.d + c8;
   uint4 out;

@@ -145,6 +145,22 @@ __device__ __forceinline__ PItem load_pitem(const FwdParams& p, int it) {
   return r;
 }
 
+// A descriptor whose fields index inside the launch (debug checks): the
+// head row and its batch entry and head, the first query tile, the list
+// counts and the entries each sub-tile uses, the load and store modes.  The
+// key tiles its list names are checked where they are loaded.
+__device__ __forceinline__ bool pitem_ok(const FwdParams& p, const PItem& r) {
+  const int nt = (p.N + kTile - 1) / kTile;
+  const int n = r.L.n;
+  auto uses_ok = [n](int first, int last) {
+    return (first == -1 && last == -1) || (first >= 0 && first <= last && last < n);
+  };
+  return r.ip.h >= 0 && r.ip.h < p.H && r.ip.b >= 0 && r.ip.b < p.B && r.ip.bh == r.ip.b * p.H + r.ip.h &&
+         r.ip.sp0.qt >= 0 && r.ip.sp0.qt < nt && n >= 0 && n <= nt && r.L.na >= 0 && r.L.na <= n &&
+         uses_ok(r.first0, r.last0) && uses_ok(r.first1, r.last1) && r.load >= kLoadRaster &&
+         r.load <= kLoadBlock2x2Col && r.store >= kStoreIdentity && r.store <= kStoreBlock2x2Col;
+}
+
 // Visible key interval [lo, hi] of query position pos in 32-bit arithmetic
 // (N <= 2^30): the rule of plan_rules.h's row_interval with the parameter
 // clamped to N, which leaves the interval clipped to [0, N - 1] unchanged.
@@ -254,9 +270,16 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
         if (kit < p.n_items) {
           const int slot = e % KS;
           if (ptx::mbar_test_wait(&bar->k_empty[slot], ((e / KS) & 1) ^ 1)) {
+            const int kt = list_kt(ki.L, kj);
+            if (!check_or_abort(p, bar, pitem_ok(p, ki), kSiteItem) ||
+                !check_or_abort(p, bar, key_tile_ok(p, kt), kSiteKeyTile))
+              break;
             ptx::mbar_arrive_expect_tx(&bar->k_full[slot], G::kTileBytes);
-            load_tile<D>(p, true, ki.load, sk + slot * G::kTileBytes, &bar->k_full[slot], list_kt(ki.L, kj) * kTile,
-                         ki.ip.bh_kv, keep);
+            if (!load_tile<D>(p, true, ki.load, sk + slot * G::kTileBytes, &bar->k_full[slot], kt * kTile,
+                              ki.ip.bh_kv, keep)) {
+              abort_cta(bar);
+              break;
+            }
             ++e;
             if (++kj == ki.L.n) {
               kj = 0;
@@ -271,11 +294,15 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
         if (qit < p.n_items) {
           const int slot = t % NQ;
           if (ptx::mbar_test_wait(&bar->q_empty[slot], ((t / NQ) & 1) ^ 1)) {
+            if (!check_or_abort(p, bar, pitem_ok(p, qi), kSiteItem)) break;
             if (qi.first(qs) >= 0) {
               const SubPlan& sp = qs ? qi.ip.sp1 : qi.ip.sp0;
               ptx::mbar_arrive_expect_tx(&bar->q_full[slot], G::kTileBytes);
-              load_tile<D>(p, false, qi.load, sq + slot * G::kTileBytes, &bar->q_full[slot], sp.qt * kTile,
-                           qi.ip.bh, once);
+              if (!load_tile<D>(p, false, qi.load, sq + slot * G::kTileBytes, &bar->q_full[slot], sp.qt * kTile,
+                                qi.ip.bh, once)) {
+                abort_cta(bar);
+                break;
+              }
             } else {
               ptx::mbar_arrive(&bar->q_full[slot]);  // no rows: an empty fill keeps the slot's phases in step
             }
@@ -319,16 +346,26 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
       for (int it = blockIdx.x; ok && it < p.n_items; it += gridDim.x) {
         const PItem pi = load_pitem(p, it);
         prefetch_pitem(p, it + gridDim.x);
+        if (!check_or_abort(p, bar, pitem_ok(p, pi), kSiteItem)) break;
         for (int j = 0; j < pi.L.n; ++j, ++e) {
           const int slot = e % VS;
+          const int kt = list_kt(pi.L, j);
+          if (debug_aborted(abort_flag) || !check_or_abort(p, bar, key_tile_ok(p, kt), kSiteKeyTile)) {
+            ok = false;
+            break;
+          }
           if (!ptx::mbar_wait(&bar->v_empty[slot], ((e / VS) & 1) ^ 1, p.timeout_ns, abort_flag)) {
             raise_error(p, bar, kErrProducer);
             ok = false;
             break;
           }
           ptx::mbar_arrive_expect_tx(&bar->v_full[slot], G::kTileBytes);
-          load_v_tile<D>(p, pi.load, sv + slot * G::kTileBytes, &bar->v_full[slot], list_kt(pi.L, j) * kTile,
-                         pi.ip.bh_kv, keep);
+          if (!load_v_tile<D>(p, pi.load, sv + slot * G::kTileBytes, &bar->v_full[slot], kt * kTile, pi.ip.bh_kv,
+                              keep)) {
+            abort_cta(bar);
+            ok = false;
+            break;
+          }
         }
       }
       if (*abort_flag) {
@@ -372,6 +409,10 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
     for (int it = blockIdx.x; ok && it < p.n_items; it += gridDim.x, ++i) {
       const PItem pi = load_pitem(p, it);
       prefetch_pitem(p, it + gridDim.x);
+      if (!check_or_abort(p, bar, pitem_ok(p, pi), kSiteItem)) {
+        ok = false;
+        break;
+      }
       const TileList& L = pi.L;
       const int first_use = pi.first(s), last_use = pi.last(s);
       const int t = 2 * i + s;
@@ -461,6 +502,10 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
     for (int it = blockIdx.x; ok && it < p.n_items; it += gridDim.x) {
       const PItem pi = load_pitem(p, it);
       prefetch_pitem(p, it + gridDim.x);
+      if (!check_or_abort(p, bar, pitem_ok(p, pi), kSiteItem)) {
+        ok = false;
+        break;
+      }
       const TileList& L = pi.L;
       const SubPlan& sp = s ? pi.ip.sp1 : pi.ip.sp0;
       const int pos = sp.qt * kTile + row;
@@ -546,8 +591,9 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
       const float b2 = p.sink ? __ldg(p.sink + pi.ip.h) * kLog2e : -INFINITY;
       float o_scale, unused, lse_v;
       finalize_row(m, l, -INFINITY, 0.f, b2, &o_scale, &unused, &lse_v);
-      const bool valid = pos < p.N;
-      const int64_t tok = valid ? token_of(p, pi.store, pi.perm_row, pos) : 0;
+      bool valid = pos < p.N;
+      const int64_t tok = valid ? out_token(p, pi.store, pi.perm_row, pos) : 0;
+      if (kDebugChecks && tok < 0) valid = false;
       const int64_t orow = ((int64_t)pi.ip.bh * p.N + tok) * D;
       if (PG::kStage && p.o_tma) {
         // Through shared memory: each thread writes its row into this
@@ -579,7 +625,8 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
             break;
           }
           if (leader) {
-            store_tile<D>(p, pi.load, stage, sp.qt * kTile, pi.ip.bh, ptx::l2_policy_evict_first());
+            if (!store_tile<D>(p, pi.load, stage, sp.qt * kTile, pi.ip.bh, ptx::l2_policy_evict_first()))
+              abort_cta(bar);
             ptx::bulk_commit_group();
           }
         }

@@ -121,7 +121,9 @@ __device__ __forceinline__ void build_list_sp(const FwdParams& p, int h, int qt,
       for (int i = 0; i < c; ++i) {
         const int kt = n * c + i;
         if (kt > qt) break;
-        list[pos++] = (uint32_t)kt;
+        // (debug builds: never past the list's capacity; the kernel checks the count)
+        if (!kDebugChecks || pos < kBlockListMax) list[pos] = (uint32_t)kt;
+        ++pos;
       }
     }
     base += __shfl_sync(0xffffffffu, incl, 31);
@@ -132,6 +134,14 @@ __device__ __forceinline__ void build_list_sp(const FwdParams& p, int h, int qt,
 __device__ __forceinline__ void fail_d256(const FwdParams& p, BarD256* bar, uint32_t bit) {
   *reinterpret_cast<volatile int*>(&bar->abort_flag) = 1;
   atomicOr(p.err, bit);
+}
+
+// Debug checks (debug_check in kernel_params.h): a failed one also raises
+// the CTA's abort flag; always true in the product build.
+__device__ __forceinline__ bool check_d256(const FwdParams& p, BarD256* bar, bool ok, uint32_t site) {
+  if (debug_check(p.err, ok, site)) return true;
+  *reinterpret_cast<volatile int*>(&bar->abort_flag) = 1;
+  return false;
 }
 
 template <int D, int KT>
@@ -153,6 +163,13 @@ __global__ void __launch_bounds__(kThreadsD256, 1) attention_sp_kernel(const __g
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int2 item = p.items[blockIdx.x];  // (b * H + h, query tile)
+  // debug builds: a work item outside the launch's heads and query tiles
+  // ends the CTA here, before any barrier or allocation
+  if (!((int)blockIdx.x < p.n_items && item.x >= 0 && item.x < p.B * p.H && item.y >= 0 &&
+        (int64_t)item.y * kTile < p.N)) {
+    if (threadIdx.x == 0) debug_check(p.err, false, kSiteItem);
+    if (kDebugChecks) return;
+  }
   const int bh = item.x, qt = item.y;
   const int h = bh % p.H, b = bh / p.H;
   const int bh_kv = b * p.H_kv + h / p.kv_group;
@@ -209,6 +226,10 @@ __global__ void __launch_bounds__(kThreadsD256, 1) attention_sp_kernel(const __g
   if (block) {
     L.e = list_e;
     L.n = bar->list_n;
+    if (kDebugChecks && L.n > kBlockListMax) {  // debug builds: a list past its capacity is dropped
+      if (threadIdx.x == 0) check_d256(p, bar, false, kSiteKeyTile);
+      L.n = 0;
+    }
   }
   // key tiles of KT keys: plan tile j gives pieces kSub j .. kSub j + kSub - 1
   // (the last ones only when they hold keys < N)
@@ -225,15 +246,24 @@ __global__ void __launch_bounds__(kThreadsD256, 1) attention_sp_kernel(const __g
       const uint64_t keep = ptx::l2_policy_evict_last();
       const uint64_t once = ptx::l2_policy_evict_first();
       ptx::mbar_arrive_expect_tx(&bar->q_full, kQBytes);
+      // (debug builds: tile coordinates inside the [B*H][N][d] and [B*H_kv][N][d] views)
+      if (check_d256(p, bar, (int64_t)qt * kTile < p.N && bh >= 0 && bh < p.B * p.H, kSiteLoad)) {
 #pragma unroll
-      for (int c = 0; c < kD / 64; ++c)
-        ptx::tma_load_3d_hint(sq + c * kQChunk, &p.tq[0], &bar->q_full, c * 64, qt * kTile, bh, once);
+        for (int c = 0; c < kD / 64; ++c)
+          ptx::tma_load_3d_hint(sq + c * kQChunk, &p.tq[0], &bar->q_full, c * 64, qt * kTile, bh, once);
+      }
       // K and V halves in list order, interleaved so that neither ring
       // waits behind the other
       for (int t = 0; t < n_half; ++t) {
         const int slot = t % kStagesD256;
         const uint32_t par = ((t / kStagesD256) & 1) ^ 1;
         const int k0 = half_key0(t);
+        if (kDebugChecks) {
+          const int kt = list_kt_d256(L, t / kSub);
+          if (*abort_flag || !check_d256(p, bar, kt >= 0 && (int64_t)kt * kTile < p.N, kSiteKeyTile) ||
+              !check_d256(p, bar, k0 >= 0 && k0 < p.N && bh_kv >= 0 && bh_kv < p.B * p.H_kv, kSiteLoad))
+            break;
+        }
         if (!ptx::mbar_wait(&bar->k_empty[slot], par, p.timeout_ns, abort_flag)) {
           fail_d256(p, bar, kErrProducer);
           break;
@@ -484,12 +514,16 @@ __global__ void __launch_bounds__(kThreadsD256, 1) attention_sp_kernel(const __g
       // caller token of this position (the inputs were reordered to
       // positions; the output goes back to token order)
       const int store_mode = p.head_info[h * 4 + kHeadStore];
-      const int64_t tok = !valid ? pos
+      const int perm_row = p.head_info[h * 4 + kHeadPermRow];
+      // debug builds: the head's explicit-order row and the token it holds
+      // are checked; a row that fails is not stored
+      bool store = valid &&
+                   debug_check(p.err, store_mode != kStoreExplicit || (perm_row >= 0 && perm_row < p.n_perm), kSiteItem);
+      const int64_t tok = !store ? pos
                                  : token_at(store_mode, p.grid_rows, p.grid_cols,
-                                            store_mode == kStoreExplicit
-                                                ? p.perm + (int64_t)p.head_info[h * 4 + kHeadPermRow] * p.N
-                                                : nullptr,
+                                            store_mode == kStoreExplicit ? p.perm + (int64_t)perm_row * p.N : nullptr,
                                             pos);
+      store = store && debug_check(p.err, tok >= 0 && tok < p.N, kSiteOrder);
       const int64_t orow = ((int64_t)bh * p.N + tok) * kD;
 #pragma unroll 1
       for (int c0 = 0; c0 < kD; c0 += 32) {
@@ -501,7 +535,7 @@ __global__ void __launch_bounds__(kThreadsD256, 1) attention_sp_kernel(const __g
 #pragma unroll
           for (int i = 0; i < 32; ++i) ov[i] = 0.f;
         }
-        if (valid) {
+        if (store) {
           if (p.out_f32) {
             float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.o) + orow + c0);
 #pragma unroll
@@ -518,7 +552,7 @@ __global__ void __launch_bounds__(kThreadsD256, 1) attention_sp_kernel(const __g
           }
         }
       }
-      if (valid && p.lse) p.lse[(int64_t)bh * p.N + tok] = lse_v;
+      if (store && p.lse) p.lse[(int64_t)bh * p.N + tok] = lse_v;
     }
   }
 

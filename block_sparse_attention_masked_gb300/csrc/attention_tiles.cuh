@@ -187,6 +187,40 @@ __device__ __forceinline__ void raise_error(const FwdParams& p, Bar* bar, uint32
   atomicOr(p.err, bit);
 }
 
+// Debug checks (debug_check in kernel_params.h).  A failed check also
+// raises the CTA's abort flag, so that every role leaves as after a
+// timed-out wait; always true in the product build.
+template <typename Bar>
+__device__ __forceinline__ bool check_or_abort(const FwdParams& p, Bar* bar, bool ok, uint32_t site) {
+  if (debug_check(p.err, ok, site)) return true;
+  *reinterpret_cast<volatile int*>(&bar->abort_flag) = 1;
+  return false;
+}
+
+// The abort flag after a failed check that recorded itself (load_tile,
+// store_tile).
+template <typename Bar>
+__device__ __forceinline__ void abort_cta(Bar* bar) {
+  *reinterpret_cast<volatile int*>(&bar->abort_flag) = 1;
+}
+
+// Debug builds: whether the CTA has been aborted, so that the copy threads
+// stop issuing; always false in the product build.
+__device__ __forceinline__ bool debug_aborted(volatile int* abort_flag) { return kDebugChecks && *abort_flag; }
+
+// A key tile of the sequence (debug checks of key-tile list entries).
+__device__ __forceinline__ bool key_tile_ok(const FwdParams& p, int kt) {
+  return kt >= 0 && (int64_t)kt * kTile < p.N;
+}
+
+// A work item of this launch: its index, its head row and its query tile
+// (pair) inside the sequence (debug checks).
+__device__ __forceinline__ bool item_in_range(const FwdParams& p, int index, int2 it) {
+  const int nt = (p.N + kTile - 1) / kTile;
+  const int ny = p.split ? nt : (nt + 1) / 2;
+  return index >= 0 && index < p.n_items && it.x >= 0 && it.x < p.B * p.H && it.y >= 0 && it.y < ny;
+}
+
 // 2x2-block orders: the 5D view's coordinates (c3, c4) of the tile at
 // position p0 (32 consecutive blocks).  Row-major view (d, dc, dr, C,
 // R + bh * rows/2): 32 blocks of one block row (cols % 64 == 0).
@@ -207,14 +241,37 @@ __device__ __forceinline__ void block2x2_coords(const FwdParams& p, int mode, in
   }
 }
 
+// Whether the 128-position tile at position p0 of view row bh (nbh rows)
+// lies inside the view that `mode` selects, on the coordinates load_tile
+// computes (debug checks).
+__device__ __forceinline__ bool tile_in_view(const FwdParams& p, int mode, int p0, int bh, int nbh) {
+  if (p0 < 0 || p0 >= p.N || (p0 & (kTile - 1)) || bh < 0 || bh >= nbh) return false;
+  if (mode == kLoadRaster) return true;
+  if (mode == kLoadColumnMajor) {
+    if (p.grid_rows <= 0 || p.grid_cols <= 0) return false;
+    const int col = p0 / p.grid_rows, r0 = p0 - col * p.grid_rows;
+    return col < p.grid_cols && r0 + kTile <= p.grid_rows;
+  }
+  if (mode != kLoadBlock2x2Row && mode != kLoadBlock2x2Col) return false;
+  const int half_rows = p.grid_rows >> 1, half_cols = p.grid_cols >> 1;
+  if (half_rows <= 0 || half_cols <= 0) return false;
+  int c3, c4;
+  block2x2_coords(p, mode, p0, bh, &c3, &c4);
+  const int64_t block_rows = (int64_t)nbh * half_rows;  // the view's block-row extent
+  if (mode == kLoadBlock2x2Row) return c3 >= 0 && c3 + 32 <= half_cols && c4 >= 0 && c4 < block_rows;
+  return c3 >= 0 && c3 + 32 <= block_rows && c4 >= 0 && c4 < half_cols;
+}
+
 // TMA load of one 128-row Q (is_k false) or K tile (all d columns) starting
 // at sequence position p0, through the raster view, the column-major view or
 // a 2x2-block view (`mode`, a LoadMode).  `policy` is the L2 eviction
-// priority of the tile's lines.
+// priority of the tile's lines.  Debug builds: false, and nothing loaded,
+// when the tile is outside the view.
 template <int D>
-__device__ __forceinline__ void load_tile(const FwdParams& p, bool is_k, int mode, uint8_t* dst, uint64_t* bar, int p0,
+__device__ __forceinline__ bool load_tile(const FwdParams& p, bool is_k, int mode, uint8_t* dst, uint64_t* bar, int p0,
                                           int bh, uint64_t policy) {
   using G = Geo<D>;
+  if (!debug_check(p.err, tile_in_view(p, mode, p0, bh, p.B * (is_k ? p.H_kv : p.H)), kSiteLoad)) return false;
   if (mode == kLoadRaster) {
     const CUtensorMap* raster = is_k ? p.tk : p.tq;
 #pragma unroll
@@ -245,14 +302,16 @@ __device__ __forceinline__ void load_tile(const FwdParams& p, bool is_k, int mod
     if (G::kRem)
       ptx::tma_load_4d_hint(dst + G::kChunks * G::kChunkBytes, &colmaj[1], bar, 0, col, r0, bh, policy);
   }
+  return true;
 }
 
 // TMA load of one 128-row V tile in its uniform-swizzle layout (map [0] of
-// the V views has a kVW-column box).
+// the V views has a kVW-column box); false as load_tile.
 template <int D>
-__device__ __forceinline__ void load_v_tile(const FwdParams& p, int mode, uint8_t* dst, uint64_t* bar, int p0,
+__device__ __forceinline__ bool load_v_tile(const FwdParams& p, int mode, uint8_t* dst, uint64_t* bar, int p0,
                                             int bh, uint64_t policy) {
   using G = Geo<D>;
+  if (!debug_check(p.err, tile_in_view(p, mode, p0, bh, p.B * p.H_kv), kSiteLoad)) return false;
   if (mode == kLoadRaster) {
 #pragma unroll
     for (int c = 0; c < G::kVChunks; ++c)
@@ -271,6 +330,7 @@ __device__ __forceinline__ void load_v_tile(const FwdParams& p, int mode, uint8_
     for (int c = 0; c < G::kVChunks; ++c)
       ptx::tma_load_4d_hint(dst + c * G::kVChunkBytes, &p.cv[0], bar, c * G::kVW, col, r0, bh, policy);
   }
+  return true;
 }
 
 // TMA store of one 128-row O tile from shared memory (laid out as
@@ -279,10 +339,12 @@ __device__ __forceinline__ void load_v_tile(const FwdParams& p, int mode, uint8_
 // (`mode`, a LoadMode; requires p.o_tma).  Rows past N are clipped.  O is
 // written once and not re-read: its lines go first out of L2 (`policy`,
 // evict-first), ahead of the K / V tiles other query tiles still read.
+// Debug builds: false, and nothing stored, when the tile is outside the view.
 template <int D>
-__device__ __forceinline__ void store_tile(const FwdParams& p, int mode, const uint8_t* src, int p0, int bh,
+__device__ __forceinline__ bool store_tile(const FwdParams& p, int mode, const uint8_t* src, int p0, int bh,
                                            uint64_t policy) {
   using G = Geo<D>;
+  if (!debug_check(p.err, tile_in_view(p, mode, p0, bh, p.B * p.H), kSiteStore)) return false;
   if (mode == kLoadRaster) {
 #pragma unroll
     for (int c = 0; c < G::kChunks; ++c)
@@ -305,6 +367,7 @@ __device__ __forceinline__ void store_tile(const FwdParams& p, int mode, const u
     if (G::kRem)
       ptx::tma_store_4d_hint(&p.o_colmaj[1], src + G::kChunks * G::kChunkBytes, 0, col, r0, bh, policy);
   }
+  return true;
 }
 
 // Writes 8 bf16 values (one 16-byte unit u of the d columns) of row `row`
@@ -446,6 +509,19 @@ __device__ __forceinline__ void rescale_o(uint32_t o_tmem, float alpha, int c_be
 __device__ __forceinline__ int64_t token_of(const FwdParams& p, int store_mode, int perm_row, int64_t pos) {
   return token_at(store_mode, p.grid_rows, p.grid_cols,
                   store_mode == kStoreExplicit ? p.perm + (int64_t)perm_row * p.N : nullptr, pos);
+}
+
+// token_of for an output row at position pos < N.  Debug builds check the
+// head's explicit-order row against the orders passed (kSiteItem) and the
+// token against [0, N) (kSiteOrder: the device does not otherwise check
+// that an explicit order is a permutation), and return -1 after a failed
+// check: the row is then not stored.
+__device__ __forceinline__ int64_t out_token(const FwdParams& p, int store_mode, int perm_row, int64_t pos) {
+  if (!debug_check(p.err, store_mode != kStoreExplicit || (perm_row >= 0 && perm_row < p.n_perm), kSiteItem))
+    return -1;
+  const int64_t tok = token_of(p, store_mode, perm_row, pos);
+  if (!debug_check(p.err, tok >= 0 && tok < p.N, kSiteOrder)) return -1;
+  return tok;
 }
 
 // Final normalisation of one query row: O = (O_a e_a + O_b e_b) /

@@ -192,18 +192,35 @@ __global__ void __launch_bounds__(DecGeo<D, GP>::kThreads, 1) decode_split_kerne
         }
         const int j0 = i_begin + s * U;
         const int j1 = (j0 + U < i_end) ? j0 + U : i_end;
+        // debug builds: the ring slot and the keys it takes (at most U, inside
+        // this CTA's share); else nothing is copied and the CTA aborts
+        if (!debug_check(p.err, slot >= 0 && slot < NS && j0 >= i_begin && j0 < j1 && j1 - j0 <= U && j1 <= i_end,
+                         kSiteRing)) {
+          *abort_flag = 1;
+          break;
+        }
         ptx::mbar_arrive_expect_tx(&bar->full[slot], (uint32_t)((j1 - j0) * Geo::kRow * 2));
         uint8_t* sk = ring + slot * Geo::kSlot;
         uint8_t* sv = sk + U * Geo::kRow;
         // the slot's keys: at most two contiguous runs (a range boundary)
         int j = j0;
+        bool copied = true;
         while (j < j1) {
           const int run_end = (j < na && j1 > na) ? na : j1;
           const int k0 = key_at(j);
+          // debug builds: the run's cache rows inside the sequence's cached keys
+          if (!debug_check(p.err, k0 >= 0 && run_end > j && k0 + (run_end - j) <= len && len <= p.L, kSiteLoad)) {
+            copied = false;
+            break;
+          }
           const uint32_t bytes = (uint32_t)((run_end - j) * Geo::kRow);
           ptx::bulk_load_g2s(sk + (j - j0) * Geo::kRow, kb + (int64_t)k0 * Geo::kRow, bytes, &bar->full[slot]);
           ptx::bulk_load_g2s(sv + (j - j0) * Geo::kRow, vb + (int64_t)k0 * Geo::kRow, bytes, &bar->full[slot]);
           j = run_end;
+        }
+        if (kDebugChecks && !copied) {
+          *abort_flag = 1;
+          break;
         }
       }
       if (*abort_flag) {
@@ -245,6 +262,13 @@ __global__ void __launch_bounds__(DecGeo<D, GP>::kThreads, 1) decode_split_kerne
       const int s = gid / Geo::GPS, gi = gid % Geo::GPS;
       const int slot = s % NS;
       if ((slot * Geo::GPS + gi) % Geo::kCons != warp) continue;  // warp-uniform
+      // debug builds: the (ring slot, group) pair read inside the ring
+      if (kDebugChecks && !__all_sync(0xffffffffu, debug_check(lane == 0 ? p.err : nullptr,
+                                                               slot >= 0 && slot < NS && gi >= 0 && gi < Geo::GPS,
+                                                               kSiteRing))) {
+        if (lane == 0) *abort_flag = 1;
+        break;
+      }
       const bool got = ptx::mbar_wait(&bar->full[slot], (s / NS) & 1, p.timeout_ns, abort_flag);
       if (!__all_sync(0xffffffffu, got)) {
         if (lane == 0) {

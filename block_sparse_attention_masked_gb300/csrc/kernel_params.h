@@ -53,14 +53,44 @@ __host__ __device__ __forceinline__ int64_t token_at(int mode, int64_t rows, int
   return pos;
 }
 
-// Device error-word bits (which wait gave up).
+// Device error-word bits: which wait gave up, or which debug check failed.
 enum ErrBits : uint32_t {
   kErrProducer = 1u << 0,
   kErrMma = 1u << 1,
   kErrSoftmax = 1u << 2,
   kErrEpilogue = 1u << 3,
   kErrSelfTest = 1u << 4,
+  kErrBounds = 1u << 5,    // a debug bounds check failed; the site bits say where
+  kSiteItem = 1u << 8,     // a work item: its index or a field of its descriptor
+  kSiteKeyTile = 1u << 9,  // a key-tile list entry, or the list's capacity
+  kSiteLoad = 1u << 10,    // the coordinates of a TMA or bulk load
+  kSiteStore = 1u << 11,   // the row of an O / LSE / output store, or TMA store coordinates
+  kSiteOrder = 1u << 12,   // an explicit-order value outside [0, N)
+  kSiteRing = 1u << 13,    // a decode ring slot or the key range copied into it
 };
+
+// Debug configuration (libmattn_debug.so, compiled with -DMATTN_DEBUG=1):
+// before each use, the kernels check every coordinate handed to a TMA or
+// bulk copy, every work item and key-tile list entry, every explicit-order
+// value and every decode ring slot against the extent it indexes.  A failed
+// check ORs kErrBounds and the site's bit into the device error word, raises
+// the CTA's abort flag where the CTA has one, and skips the access; the CTA
+// then leaves the way it leaves after a timed-out wait.  Nothing traps.  The
+// product build compiles every check out.
+#ifndef MATTN_DEBUG
+#define MATTN_DEBUG 0
+#endif
+constexpr bool kDebugChecks = MATTN_DEBUG != 0;
+
+#ifdef __CUDACC__
+// True when `ok` holds or the checks are compiled out; otherwise records
+// the failure (kErrBounds | site) in the error word and returns false.
+__device__ __forceinline__ bool debug_check(uint32_t* err, bool ok, uint32_t site) {
+  if (!kDebugChecks || ok) return true;
+  if (err) atomicOr(err, kErrBounds | site);
+  return false;
+}
+#endif
 
 // A work item of the persistent kernel with its key-tile plan worked out on
 // the host (plan_rules.h), six int4 per item:
@@ -87,6 +117,7 @@ struct FwdParams {
   const int4* pitems;               // persistent kernel: kPersistItemInt4 int4 per work item
   const int32_t* head_info;         // [H][4], HeadField
   const int32_t* perm;              // explicit orders [n_perm][N]
+  int n_perm;
   const uint64_t* block_bits;       // [block_heads][Nb][wpr]
   const float* sink;                // [H] or null
   uint32_t* err;                    // device error word
@@ -130,6 +161,8 @@ struct GatherParams {
   int kv_group;
   int src_f32;
   int grid_rows, grid_cols;
+  int n_perm;
+  uint32_t* err;                    // device error word (debug checks)
 };
 
 // RRAttention block selection (rr_select.cu).
@@ -170,6 +203,7 @@ struct RecvParams {
   float* r;                   // out: [B][H][N] received attention, caller token order
   const int32_t* head_info;   // [H][4], HeadField
   const int32_t* perm;        // explicit orders [n_perm][N]
+  int n_perm;
   const uint64_t* block_bits; // [block_heads][Nb][wpr]
   uint32_t* err;
   unsigned long long timeout_ns;

@@ -50,6 +50,15 @@ std::atomic<unsigned long long> g_timeout_ns{0};
 // Test hook: an upper bound on the persistent kernel's grid (0 = one CTA per
 // SM), so that small problems still give each CTA many work items.
 std::atomic<int> g_persist_grid_cap{0};
+// Debug library test hook: a defect planted in the next forward launch's
+// plan (kCorrupt*), consumed by that launch.
+enum DebugCorruption : int {
+  kCorruptNone = 0,
+  kCorruptItemHead = 1,     // the first work item names head row B*H (one past the last)
+  kCorruptKeyTiles = 2,     // persistent: the first item's key-tile window starts past the last key tile
+  kCorruptGridRows = 3,     // the kernel is told half the grid rows (column-major heads read through TMA)
+};
+std::atomic<int> g_debug_corrupt{kCorruptNone};
 
 unsigned long long wait_timeout_ns() {
   unsigned long long t = g_timeout_ns.load();
@@ -642,6 +651,42 @@ int check_device_ptrs(const void* q, const void* k, const void* v, const void* o
   return MATTN_OK;
 }
 
+// Debug library test hook: writes the launch's work list with defect `what`
+// planted into `buf` and points the launch at it.  The checks of the debug
+// kernels must catch each defect before it is used to address memory.
+int plant_defect(int what, const Normalized& n, const Plan& plan, cudaStream_t stream, DeviceBuf* buf,
+                 FwdParams* p) {
+  const int nt = (n.N + kTile - 1) / kTile;
+  if (what == kCorruptGridRows) {
+    p->grid_rows /= 2;
+    return MATTN_OK;
+  }
+  if (n.persistent) {
+    std::vector<int4> d = plan.pitems_host;
+    if (d.empty()) return fail(MATTN_ERR_INVALID_ARG, "no work items to corrupt");
+    if (what == kCorruptItemHead) d[0].x = n.B * n.H;
+    else if (what == kCorruptKeyTiles) d[1].y = nt + 3;
+    else return fail(MATTN_ERR_INVALID_ARG, "unknown defect %d", what);
+    int rc = buf->reserve(d.size() * sizeof(int4), "cudaMalloc(corrupted items)");
+    if (rc) return rc;
+    MATTN_CUDA(cudaMemcpyAsync(buf->ptr, d.data(), d.size() * sizeof(int4), cudaMemcpyHostToDevice, stream),
+               "upload corrupted items");
+    p->pitems = static_cast<const int4*>(buf->ptr);
+    return MATTN_OK;
+  }
+  if (what != kCorruptItemHead)
+    return fail(MATTN_ERR_INVALID_ARG, "defect %d needs the persistent schedule", what);
+  std::vector<int2> items = plan.items_host;
+  if (items.empty()) return fail(MATTN_ERR_INVALID_ARG, "no work items to corrupt");
+  items[0].x = n.B * n.H;
+  int rc = buf->reserve(items.size() * sizeof(int2), "cudaMalloc(corrupted items)");
+  if (rc) return rc;
+  MATTN_CUDA(cudaMemcpyAsync(buf->ptr, items.data(), items.size() * sizeof(int2), cudaMemcpyHostToDevice, stream),
+             "upload corrupted items");
+  p->items = static_cast<const int2*>(buf->ptr);
+  return MATTN_OK;
+}
+
 int fwd_locked(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N, int d,
                int dtype, const mattn_mask_desc* desc, cudaStream_t stream, int self_test) {
   if (H_kv < 1 || H % H_kv != 0)
@@ -680,6 +725,8 @@ int fwd_locked(const void* q, const void* k, const void* v, void* o, float* lse,
     gp.src_f32 = dtype == MATTN_F32;
     gp.grid_rows = desc->grid_rows;
     gp.grid_cols = desc->grid_cols;
+    gp.n_perm = desc->perm ? desc->n_perm : 0;
+    gp.err = st->err;
     MATTN_CUDA(launch_gather(gp, stream), "gather launch");
   }
   // the copies hold one K / V head per query head
@@ -726,6 +773,7 @@ int fwd_locked(const void* q, const void* k, const void* v, void* o, float* lse,
   p.n_items = (int)plan->items_host.size();
   p.head_info = plan->head_info;
   p.perm = desc->perm;
+  p.n_perm = desc->perm ? desc->n_perm : 0;
   p.block_bits = n.kind == kBlockSparse ? desc->block_bits : nullptr;
   p.sink = desc->sink;
   p.err = st->err;
@@ -743,6 +791,17 @@ int fwd_locked(const void* q, const void* k, const void* v, void* o, float* lse,
   p.self_test_timeout = self_test;
   p.split = n.split ? 1 : 0;
   p.out_f32 = dtype == MATTN_F32 ? 1 : 0;
+  // the launch's corrupted work list (debug library test hook), freed on return
+  struct Planted {
+    DeviceBuf b;
+    ~Planted() {
+      if (b.ptr) cudaFree(b.ptr);
+    }
+  } planted;
+  if (kDebugChecks) {
+    const int what = g_debug_corrupt.exchange(kCorruptNone);
+    if (what != kCorruptNone && (rc = plant_defect(what, n, *plan, stream, &planted.b, &p))) return rc;
+  }
   if (n.single)
     MATTN_CUDA(launch_attention_sp(p, d, stream), "attention launch (single pipeline)");
   else if (n.persistent) {
@@ -751,6 +810,7 @@ int fwd_locked(const void* q, const void* k, const void* v, void* o, float* lse,
     MATTN_CUDA(launch_attention_persist(p, d, dtype == MATTN_F32, grid, stream), "attention launch (persistent)");
   } else
     MATTN_CUDA(launch_attention(p, d, dtype == MATTN_F32, stream), "attention launch");
+  if (planted.b.ptr) MATTN_CUDA(cudaStreamSynchronize(stream), "corrupted launch");  // before the list is freed
   return MATTN_OK;
 }
 
@@ -861,6 +921,18 @@ int mattn_internal_fwd_wait_selftest(const void* q, const void* k, const void* v
                                      int N, int d, int dtype, const mattn_mask_desc* desc, void* stream) {
   std::lock_guard<std::mutex> lk(g_mutex);
   return fwd_locked(q, k, v, o, lse, B, H, H, N, d, dtype, desc, static_cast<cudaStream_t>(stream), 1);
+}
+
+// Test hook (not in the public header), debug library only: plants defect
+// `what` (1: a work item's head row past the last; 2: a persistent item's
+// key tiles past the last; 3: half the grid rows for column-major heads)
+// into the next forward launch, whose device checks must report it as
+// MATTN_ERR_BOUNDS.  The product library refuses (MATTN_ERR_UNSUPPORTED).
+int mattn_internal_debug_corrupt(int what) {
+  if (!kDebugChecks) return fail(MATTN_ERR_UNSUPPORTED, "defects are planted only in the debug library");
+  if (what < kCorruptNone || what > kCorruptGridRows) return fail(MATTN_ERR_INVALID_ARG, "unknown defect %d", what);
+  g_debug_corrupt.store(what);
+  return MATTN_OK;
 }
 
 // Test hook (not in the public header): caps the persistent kernel's grid
@@ -1133,6 +1205,8 @@ int mattn_received(const void* q, const void* k, const float* lse, float* r, int
     gp.src_f32 = dtype == MATTN_F32;
     gp.grid_rows = desc->grid_rows;
     gp.grid_cols = desc->grid_cols;
+    gp.n_perm = desc->perm ? desc->n_perm : 0;
+    gp.err = st->err;
     MATTN_CUDA(launch_gather(gp, stream), "gather launch");
   }
   RecvParams p;
@@ -1147,6 +1221,7 @@ int mattn_received(const void* q, const void* k, const float* lse, float* r, int
   p.r = r;
   p.head_info = plan->head_info;
   p.perm = desc->perm;
+  p.n_perm = desc->perm ? desc->n_perm : 0;
   p.block_bits = n.kind == kBlockSparse ? desc->block_bits : nullptr;
   p.err = st->err;
   p.timeout_ns = wait_timeout_ns();
@@ -1368,9 +1443,12 @@ int mattn_device_status(void* stream, uint32_t* detail_out) {
   MATTN_CUDA(cudaMemcpy(&word, st->err, sizeof(word), cudaMemcpyDeviceToHost), "read error word");
   MATTN_CUDA(cudaMemset(st->err, 0, sizeof(word)), "clear error word");
   if (detail_out) *detail_out = word;
+  if (word & kErrBounds) return fail(MATTN_ERR_BOUNDS, "a device bounds check failed (error word 0x%x)", word);
   if (word) return fail(MATTN_ERR_TIMEOUT, "a device wait gave up (error word 0x%x)", word);
   return MATTN_OK;
 }
+
+int mattn_debug_checks(void) { return kDebugChecks ? 1 : 0; }
 
 int mattn_set_wait_timeout_ns(uint64_t ns) {
   g_timeout_ns.store(ns);
@@ -1387,6 +1465,7 @@ const char* mattn_status_string(int status) {
     case MATTN_ERR_TIMEOUT: return "MATTN_ERR_TIMEOUT";
     case MATTN_ERR_NO_DEVICE: return "MATTN_ERR_NO_DEVICE";
     case MATTN_ERR_CAPACITY: return "MATTN_ERR_CAPACITY";
+    case MATTN_ERR_BOUNDS: return "MATTN_ERR_BOUNDS";
     default: return "MATTN_ERR_UNKNOWN";
   }
 }

@@ -98,6 +98,8 @@ int fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse
     MATTN_NOALLOC_CUDA(cudaStreamSynchronize(stream), "stream sync");
     MATTN_NOALLOC_CUDA(cudaMemcpy(&word, err, sizeof(word), cudaMemcpyDeviceToHost), "read error word");
     *wait_error_out = word;
+    if (word & kErrBounds)
+      return report_error(MATTN_ERR_BOUNDS, "a device bounds check failed (error word 0x%x)", word);
     if (word) return report_error(MATTN_ERR_TIMEOUT, "a device wait gave up (error word 0x%x)", word);
   }
   return MATTN_OK;

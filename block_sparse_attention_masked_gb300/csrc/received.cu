@@ -113,16 +113,33 @@ __device__ __forceinline__ void build_q_list(const RecvParams& p, const uint64_t
     const uint32_t any = __ballot_sync(0xffffffffu, u0 || u1);
     if (u0 || u1) {
       const int pos = base + __popc(any & ((1u << lane) - 1u));
-      list[pos] = (uint32_t)qt | ((u0 ? 1u : 0u) << 30) | ((u1 ? 1u : 0u) << 31);
+      if (!kDebugChecks || pos < kBlockListMax) list[pos] = (uint32_t)qt | ((u0 ? 1u : 0u) << 30) | ((u1 ? 1u : 0u) << 31);
     }
     base += __popc(any);
   }
   if (lane == 0) *n_out = base;
 }
 
+// Caller token at position pos.  Debug builds check the head's
+// explicit-order row and the token (debug_check) and return -1 after a
+// failed check: the value is then neither read nor stored.
 __device__ __forceinline__ int64_t rc_token_of(const RecvParams& p, int store_mode, int perm_row, int64_t pos) {
-  return token_at(store_mode, p.grid_rows, p.grid_cols,
-                  store_mode == kStoreExplicit ? p.perm + (int64_t)perm_row * p.N : nullptr, pos);
+  if (!debug_check(p.err, store_mode != kStoreExplicit || (perm_row >= 0 && perm_row < p.n_perm), kSiteItem))
+    return -1;
+  const int64_t tok = token_at(store_mode, p.grid_rows, p.grid_cols,
+                               store_mode == kStoreExplicit ? p.perm + (int64_t)perm_row * p.N : nullptr, pos);
+  if (!debug_check(p.err, tok >= 0 && tok < p.N, kSiteOrder)) return -1;
+  return tok;
+}
+
+// A 128-position tile of view row bh inside the raster or column-major
+// view, on the coordinates rc_load computes (debug checks).
+__device__ __forceinline__ bool rc_tile_ok(const RecvParams& p, bool column_major, int p0, int bh) {
+  if (p0 < 0 || p0 >= p.N || (p0 & (kTile - 1)) || bh < 0 || bh >= p.B * p.H) return false;
+  if (!column_major) return true;
+  if (p.grid_rows <= 0) return false;
+  const int col = p0 / p.grid_rows, r0 = p0 - col * p.grid_rows;
+  return col < p.grid_cols && r0 + kTile <= p.grid_rows;
 }
 
 // TMA load of one 128-row tile at sequence position p0 (raster view, or the
@@ -203,6 +220,10 @@ __global__ void __launch_bounds__(kRcThreads, 1) received_kernel(const __grid_co
     if (Q.block) {
       Q.n = bar->list_n;
       Q.lo = 0;
+      if (kDebugChecks && !debug_check(p.err, Q.n <= kBlockListMax, kSiteKeyTile)) {
+        *abort_flag = 1;  // debug builds: a list past its capacity is dropped
+        Q.n = 0;
+      }
     } else {
       const bool e0 = Q.lo0 <= Q.hi0, e1 = Q.lo1 <= Q.hi1;
       Q.lo = e0 ? (e1 ? min(Q.lo0, Q.lo1) : Q.lo0) : Q.lo1;
@@ -218,11 +239,21 @@ __global__ void __launch_bounds__(kRcThreads, 1) received_kernel(const __grid_co
     // ------------------------------------------------------------ loads
     if (lane == 0) {
       ptx::mbar_arrive_expect_tx(&bar->k_full, nk * T::kTileBytes);
-      for (int s = 0; s < nk; ++s)
+      for (int s = 0; s < nk; ++s) {
+        // (debug builds: tile coordinates inside the view, else no load and the CTA aborts)
+        if (!debug_check(p.err, rc_tile_ok(p, colmaj, (kt0 + s) * kTile, bh), kSiteLoad)) {
+          *abort_flag = 1;
+          break;
+        }
         rc_load<D>(p.tk, p.ck, colmaj, p.grid_rows, sk + s * T::kTileBytes, &bar->k_full, (kt0 + s) * kTile, bh);
+      }
       for (int j = 0; j < QL.n; ++j) {
         const int qt = ql_qt(QL, j);
         const int slot = j % kRcStages;
+        if (kDebugChecks && (*abort_flag || !debug_check(p.err, rc_tile_ok(p, colmaj, qt * kTile, bh), kSiteLoad))) {
+          *abort_flag = 1;
+          break;
+        }
         if (!ptx::mbar_wait(&bar->q_empty[slot], ((j / kRcStages) & 1) ^ 1, p.timeout_ns, abort_flag)) {
           rc_raise(p, bar, kErrProducer);
           break;
@@ -338,7 +369,8 @@ __global__ void __launch_bounds__(kRcThreads, 1) received_kernel(const __grid_co
     if (t < p.N) {
       const int store_mode = p.head_info[h * 4 + kHeadStore];
       const int perm_row = p.head_info[h * 4 + kHeadPermRow];
-      p.r[(int64_t)bh * p.N + rc_token_of(p, store_mode, perm_row, t)] = racc;
+      const int64_t tok = rc_token_of(p, store_mode, perm_row, t);
+      if (!kDebugChecks || tok >= 0) p.r[(int64_t)bh * p.N + tok] = racc;
     }
   }
 
@@ -360,6 +392,7 @@ __global__ void lse_positions_kernel(const RecvParams p, const float* lse) {
   const int64_t pos = i - bh * p.N;
   const int h = (int)(bh % p.H);
   const int64_t tok = rc_token_of(p, p.head_info[h * 4 + kHeadStore], p.head_info[h * 4 + kHeadPermRow], pos);
+  if (kDebugChecks && tok < 0) return;
   p.lse2p[bh * p.lse_pitch + pos] = lse[bh * p.N + tok] * 1.4426950408889634f;
 }
 

@@ -161,11 +161,17 @@ __global__ void __launch_bounds__(kRrScoreThreads, 1) rr_scores_kernel(const __g
       // view [B*H][L/S][S][d] turns that into one 128-row box per tile.
       const int off = p.S - 1 - (h % p.S);
       ptx::mbar_arrive_expect_tx(&bar->q_full, nq * T::kTileBytes);
-      for (int s = 0; s < nq; ++s)
+      for (int s = 0; s < nq; ++s) {
+        // (debug builds: coordinates inside the [B*H][L/S][S][d] view, else no load and the CTA aborts)
+        if (!debug_check(p.err, off >= 0 && off < p.S && q0 + s * kTile < p.n_s && bh < p.BH, kSiteLoad)) {
+          *abort_flag = 1;
+          break;
+        }
 #pragma unroll
         for (int c = 0; c < T::kChunks; ++c)
           ptx::tma_load_4d(sq + s * T::kTileBytes + c * T::kChunkBytes, &p.tq[0], &bar->q_full, c * 64, off,
                            q0 + s * kTile, bh);
+      }
       const uint64_t keep = ptx::l2_policy_evict_last();  // every query tile of the head re-reads Ksum
       for (int t = 0; t < steps; ++t) {
         const int slot = t % kRrStages;
@@ -174,6 +180,10 @@ __global__ void __launch_bounds__(kRrScoreThreads, 1) rr_scores_kernel(const __g
           break;
         }
         const int kt = t % n_kt;
+        if (kDebugChecks && (*abort_flag || !debug_check(p.err, kt * kTile < p.n_s && bh < p.BH, kSiteLoad))) {
+          *abort_flag = 1;
+          break;
+        }
         ptx::mbar_arrive_expect_tx(&bar->k_full[slot], T::kTileBytes);
 #pragma unroll
         for (int c = 0; c < T::kChunks; ++c)

@@ -45,6 +45,18 @@
  * happen) makes the kernel record MATTN_ERR_TIMEOUT in the device error word
  * and return early instead of hanging; mattn_device_status() reports it.
  * No entry point aborts or throws.
+ *
+ * Debug library: libmattn_debug.so is the same library built with
+ * MATTN_DEBUG=1.  Its kernels check, before each use, every coordinate
+ * handed to a TMA or bulk copy, every work item and key-tile list entry,
+ * every explicit-order value (which the product library does not check:
+ * an order that is no permutation of 0..N-1 is undefined behaviour there)
+ * and every decode ring slot.  A failed check records MATTN_ERR_BOUNDS in
+ * the device error word, skips the access, and the CTA returns; nothing
+ * traps.  mattn_device_status() then returns MATTN_ERR_BOUNDS with the
+ * failed sites in its detail word (bit 5 set; bits 8..13: work item,
+ * key-tile entry, load coordinates, store row, explicit-order value, ring
+ * slot).  Results are those of the product library otherwise.
  */
 #ifndef MATTN_H_
 #define MATTN_H_
@@ -63,7 +75,8 @@ typedef enum {
   MATTN_ERR_CUDA = -3,         /* a CUDA runtime / driver call failed         */
   MATTN_ERR_TIMEOUT = -4,      /* a device wait ran past its limit            */
   MATTN_ERR_NO_DEVICE = -5,    /* no sm_103 device is current                 */
-  MATTN_ERR_CAPACITY = -6      /* more than a fixed-size buffer can hold      */
+  MATTN_ERR_CAPACITY = -6,     /* more than a fixed-size buffer can hold      */
+  MATTN_ERR_BOUNDS = -7        /* debug library: a device bounds check failed */
 } mattn_status;
 
 /* Mask kinds; all heads of one call share the kind (per-head parameters). */
@@ -254,7 +267,8 @@ int mattn_fwd_host(const void* q, const void* k, const void* v, void* o, float* 
  *                   like mattn_fwd (a device wait that gives up is then not
  *                   reported).  Non-NULL: the call synchronises `stream`,
  *                   stores the kernel's error word there (0 = none) and
- *                   returns MATTN_ERR_TIMEOUT if it is non-zero.
+ *                   returns MATTN_ERR_TIMEOUT if it is non-zero
+ *                   (MATTN_ERR_BOUNDS if a debug check failed).
  *
  * Limits (the static array is sized for them, MATTN_NOALLOC_SCRATCH_BYTES
  * in all, held on every device that loads the library until the process
@@ -394,11 +408,15 @@ int mattn_plan_tiles_device(const mattn_mask_desc* desc, int H, int N, int32_t* 
 
 /*
  * mattn_device_status -- synchronises `stream`, then reads and clears the
- * current device's error word: MATTN_OK, or MATTN_ERR_TIMEOUT when a kernel
- * gave up on a wait since the last call.  *detail_out (may be NULL) receives
- * the raw word (which wait gave up).
+ * current device's error word: MATTN_OK; MATTN_ERR_BOUNDS when a debug
+ * check failed since the last call (debug library only); else
+ * MATTN_ERR_TIMEOUT when a kernel gave up on a wait.  *detail_out (may be
+ * NULL) receives the raw word (which wait gave up, which checks failed).
  */
 int mattn_device_status(void* stream, uint32_t* detail_out);
+
+/* 1 in the debug library (device bounds checks compiled in), else 0. */
+int mattn_debug_checks(void);
 
 /*
  * mattn_set_wait_timeout_ns -- limit for every device-side wait (default
