@@ -488,6 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
       ptx::tmem_ld32(s_tmem + 64, *reinterpret_cast<float(*)[32]>(&x[64]));
       ptx::tmem_ld32(s_tmem + 96, *reinterpret_cast<float(*)[32]>(&x[96]));
       ptx::tmem_wait_ld();
+      uint32_t none = 0u;  // 32-column groups this lane sees nothing of
       const bool partial = sub_partial(p, sp, kt);
       if (partial) {
         // visible key columns of this row inside the tile: [c_lo, c_hi]
@@ -496,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
         const int c_hi = (int)(hi - k0 < -1 ? -1 : (hi - k0 > 128 ? 128 : hi - k0));
         // and the sink keys of the tile: columns [0, c_s]
         const int c_s = (int)(sink_hi - k0 < -1 ? -1 : (sink_hi - k0 > 128 ? 128 : sink_hi - k0));
-        mask_row(x, c_lo, c_hi, c_s);
+        none = mask_row(x, c_lo, c_hi, c_s);
       }
       // P = exp2(s * scale * log2e - m) into tensor memory.  tcgen05.ld / st
       // are warp-collective, so every branch below is taken by whole warps
@@ -508,13 +509,13 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
         // guards against overflow (the final normalisation uses the same m
         // for numerator and denominator), so it is kept while every P stays
         // below 2^40; a tile that breaks this (rare) is redone below.
-        ts = exp_to_tmem(x, sl2, m, s_tmem);
+        ts = exp_to_tmem(x, sl2, m, s_tmem, none);
         slow = __any_sync(0xffffffffu, !(ts <= kMaxTileSum));
         if (slow) ptx::tmem_wait_st();  // let these stores land before they are overwritten
       }
       if (slow) {
         // tile maximum first (also the first tile of a row)
-        const float m_new = fmaxf(m, row_max(x) * sl2);
+        const float m_new = fmaxf(m, row_max(x, none) * sl2);
         const bool need_rescale = (m != -INFINITY) && (m_new > m);
         if (m == -INFINITY) m = m_new;  // nothing accumulated yet (all earlier P were zero)
         if (__any_sync(0xffffffffu, need_rescale)) {
@@ -525,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
             m = m_new;
           }
         }
-        ts = exp_to_tmem(x, sl2, (m == -INFINITY) ? 0.f : m, s_tmem);
+        ts = exp_to_tmem(x, sl2, (m == -INFINITY) ? 0.f : m, s_tmem, none);
       }
       l += ts;
       ptx::tmem_wait_st();

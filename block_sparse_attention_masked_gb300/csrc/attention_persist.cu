@@ -532,6 +532,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
         ptx::tmem_ld32(s_tmem + 64, *reinterpret_cast<float(*)[32]>(&x[64]));
         ptx::tmem_ld32(s_tmem + 96, *reinterpret_cast<float(*)[32]>(&x[96]));
         ptx::tmem_wait_ld();
+        uint32_t none = 0u;  // 32-column groups this lane sees nothing of
         if (sub_partial(p, sp, kt)) {
           // visible key columns of this row inside the tile: [c_lo, c_hi],
           // and the sink keys of the tile: columns [0, c_s]
@@ -539,19 +540,19 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
           const int c_lo = min(max(lo - k0, -1), 128);
           const int c_hi = min(max(hi - k0, -1), 128);
           const int c_s = min(max(sink_hi - k0, -1), 128);
-          mask_row(x, c_lo, c_hi, c_s);
+          none = mask_row(x, c_lo, c_hi, c_s);
         }
         // P = exp2(s * scale * log2e - m) into tensor memory (the stale-max
         // rule of attention_fwd.cu: m only guards against overflow)
         float ts;
         bool slow = __any_sync(0xffffffffu, m == -INFINITY);
         if (!slow) {
-          ts = exp_to_tmem(x, sl2, m, s_tmem);
+          ts = exp_to_tmem(x, sl2, m, s_tmem, none);
           slow = __any_sync(0xffffffffu, !(ts <= kMaxTileSum));
           if (slow) ptx::tmem_wait_st();
         }
         if (slow) {
-          const float m_new = fmaxf(m, row_max(x) * sl2);
+          const float m_new = fmaxf(m, row_max(x, none) * sl2);
           const bool need_rescale = (m != -INFINITY) && (m_new > m);
           if (m == -INFINITY) m = m_new;
           if (__any_sync(0xffffffffu, need_rescale)) {
@@ -564,7 +565,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
               m = m_new;
             }
           }
-          ts = exp_to_tmem(x, sl2, (m == -INFINITY) ? 0.f : m, s_tmem);
+          ts = exp_to_tmem(x, sl2, (m == -INFINITY) ? 0.f : m, s_tmem, none);
         }
         l += ts;
         ptx::tmem_wait_st();

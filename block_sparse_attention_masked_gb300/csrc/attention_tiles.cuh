@@ -416,18 +416,24 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
 // moving a share of them to an FMA-pipe polynomial measured slower at every
 // share tried, as did a truncating pack with a second sum over the
 // truncated values (one more add and two integer ops per pair).
+// `none` (from mask_row) has bit g set for the 32-column groups this lane
+// sees nothing of: their scores may be left unmasked, and their P is made
+// zero by exponentiating against -inf (one select per group keeps the pass
+// straight-line code; branching around groups measured slower).
 // (NC = 128 for a whole row; a thread holding half a row passes its 64
 // scores and the tensor-memory address of its half of P.)
 template <int NC>
-__device__ __forceinline__ float exp_to_tmem(const float (&x)[NC], float sl2, float mref, uint32_t p_tmem) {
+__device__ __forceinline__ float exp_to_tmem(const float (&x)[NC], float sl2, float mref, uint32_t p_tmem,
+                                             uint32_t none = 0u) {
   static_assert(NC % 32 == 0, "whole 32-column groups");
   const float2 sl2v = make_float2(sl2, sl2);
-  const float2 negm = make_float2(-mref, -mref);
   float2 acc[2];
 #pragma unroll
   for (int i = 0; i < 2; ++i) acc[i] = make_float2(0.f, 0.f);
 #pragma unroll
   for (int c0 = 0; c0 < NC; c0 += 32) {
+    const float nm = ((none >> (c0 / 32)) & 1u) ? -INFINITY : -mref;
+    const float2 negm = make_float2(nm, nm);
     uint32_t pk[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -451,42 +457,53 @@ __device__ __forceinline__ uint32_t range_bits(int g, int lo, int hi) {
   return (0xffffffffu >> (31 - b0)) & (0xffffffffu << a0);
 }
 
-// Boundary mask of one row of a PARTIAL tile: x[c] = -inf for the key
-// columns c of the 128-key tile outside this row's visible interval
-// [c_lo, c_hi] and outside its sink columns [0, c_s] (c_s < 0: none).
-// Each 32-column group gets a visibility bit mask; a column's bit, sign-
-// extended to a full word, selects between x and -inf bitwise, so no
-// column needs a predicate or a branch (per-column branches, or skipping
-// whole groups with warp votes, cost far more here: registers spill).
+// Boundary mask of one row of a PARTIAL tile: the key columns c of the
+// 128-key tile outside this row's visible interval [c_lo, c_hi] and
+// outside its sink columns [0, c_s] (c_s < 0: none) are made invisible.
+// Each 32-column group gets a visibility bit mask per lane.  A group this
+// lane sees nothing of is only reported (bit g of the result), and the
+// exponential pass and the row maximum take it as -inf as a whole; a group
+// that some lane of the warp sees in part has its columns set one by one,
+// x[c] = -inf where the column's bit is clear.  A window's boundary tile,
+// whose rows are 32 consecutive positions per warp, thus pays per-column
+// selects on one group per warp instead of all four.
 // (x may hold NC < 128 columns of the row, starting at tile column col0, a
 // multiple of 32.)
 template <int NC>
-__device__ __forceinline__ void mask_row(float (&x)[NC], int c_lo, int c_hi, int c_s, int col0 = 0) {
+__device__ __forceinline__ uint32_t mask_row(float (&x)[NC], int c_lo, int c_hi, int c_s, int col0 = 0) {
+  uint32_t none = 0u;
 #pragma unroll
   for (int g = 0; g < NC / 32; ++g) {
     const int gt = g + col0 / 32;  // 32-column group of the tile
     const uint32_t vis = range_bits(gt, c_lo, c_hi) | range_bits(gt, 0, c_s);
+    if (vis == 0u) none |= 1u << g;
+    if (__any_sync(0xffffffffu, vis != 0u && vis != 0xffffffffu)) {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const uint32_t keep = (uint32_t)((int32_t)(vis << (31 - j)) >> 31);  // all ones when column visible
-      const uint32_t xb = __float_as_uint(x[32 * g + j]);
-      x[32 * g + j] = __uint_as_float((xb & keep) | (0xff800000u & ~keep));
+      for (int j = 0; j < 32; ++j) x[32 * g + j] = ((vis >> j) & 1u) ? x[32 * g + j] : -INFINITY;
     }
   }
+  return none;
 }
 
 // Maximum of the 128 raw scores of this thread's row (8 independent chains;
-// measured faster here than three-input maxima).
+// measured faster here than three-input maxima), over the 32-column groups
+// not flagged in `none` (mask_row's bits).
 template <int NC>
-__device__ __forceinline__ float row_max(const float (&x)[NC]) {
-  float a[8];
+__device__ __forceinline__ float row_max(const float (&x)[NC], uint32_t none = 0u) {
+  float r = -INFINITY;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) a[i] = x[i];
+  for (int c = 0; c < NC; c += 32) {
+    float a[8];
 #pragma unroll
-  for (int c = 8; c < NC; c += 8)
+    for (int i = 0; i < 8; ++i) a[i] = x[c + i];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) a[i] = fmaxf(a[i], x[c + i]);
-  return fmaxf(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])), fmaxf(fmaxf(a[4], a[5]), fmaxf(a[6], a[7])));
+    for (int u = 8; u < 32; u += 8)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) a[i] = fmaxf(a[i], x[c + u + i]);
+    const float g = fmaxf(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])), fmaxf(fmaxf(a[4], a[5]), fmaxf(a[6], a[7])));
+    r = ((none >> (c / 32)) & 1u) ? r : fmaxf(r, g);
+  }
+  return r;
 }
 
 // O row *= alpha in tensor memory (warp-collective; alpha is per lane), for
