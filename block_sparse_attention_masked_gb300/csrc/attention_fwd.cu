@@ -176,7 +176,7 @@ __device__ __forceinline__ void issue_q_loads(const FwdParams& p, const ItemPlan
   }
 }
 
-template <int D, bool OUT_F32>
+template <int D, bool OUT_F32, bool MASK>
 __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid_constant__ FwdParams p) {
   using G = Geo<D>;
   constexpr int KS = G::kStages;
@@ -489,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
       ptx::tmem_ld32(s_tmem + 96, *reinterpret_cast<float(*)[32]>(&x[96]));
       ptx::tmem_wait_ld();
       uint32_t none = 0u;  // 32-column groups this lane sees nothing of
-      const bool partial = sub_partial(p, sp, kt);
+      const bool partial = MASK && sub_partial(p, sp, kt);
       if (partial) {
         // visible key columns of this row inside the tile: [c_lo, c_hi]
         const int64_t k0 = (int64_t)kt * kTile;
@@ -719,10 +719,10 @@ __global__ void gather_kernel(const GatherParams p) {
   *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dst[t]) + row * p.d + c8) = out;
 }
 
-template <int D, bool F32>
+template <int D, bool F32, bool MASK>
 cudaError_t launch_one(const FwdParams& p, cudaStream_t stream) {
   const size_t smem = attention_smem_bytes(D);
-  auto kern = attention_fwd_kernel<D, F32>;
+  auto kern = attention_fwd_kernel<D, F32, MASK>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   if (!p.after_prepass) {
@@ -769,9 +769,12 @@ size_t attention_smem_bytes(int d) {
 
 cudaError_t launch_attention(const FwdParams& p, int d, bool out_f32, cudaStream_t stream) {
   if (p.n_items <= 0) return cudaSuccess;
-#define MATTN_CASE(DD)                                                              \
-  case DD:                                                                          \
-    return out_f32 ? launch_one<DD, true>(p, stream) : launch_one<DD, false>(p, stream);
+  // bf16 launches without PARTIAL tiles run the build without the boundary
+  // mask: its code, even when never taken, slows the exponential pass
+#define MATTN_CASE(DD)                                                                                 \
+  case DD:                                                                                             \
+    return out_f32 ? launch_one<DD, true, true>(p, stream)                                             \
+                   : (p.no_partial ? launch_one<DD, false, false>(p, stream) : launch_one<DD, false, true>(p, stream));
   switch (d) {
     MATTN_CASE(32)
     MATTN_CASE(64)

@@ -141,6 +141,10 @@ struct FwdParams {
                                     // stored in its load order: raster, column-major or 2x2 blocks)
   int after_prepass;                // 1: launched as a programmatic dependent of the reorder
                                     // pre-pass, whose copies its loads read
+  int no_partial;                   // 1: no key tile of the launch is PARTIAL for any query
+                                    // tile (full or chunk masks on 128-aligned sizes), so the
+                                    // kernels run their build without the boundary mask
+                                    // (0, the zeroed default: the build with it)
 };
 
 struct PlanDumpParams {

@@ -266,6 +266,19 @@ int normalize(const mattn_mask_desc* desc, int B, int H, int N, int d, int dtype
   return MATTN_OK;
 }
 
+// Whether no key tile of the launch is PARTIAL for any query tile: full
+// masks, and chunks that are multiples of the tile (or cover the sequence),
+// on a sequence length that is a multiple of the tile.  Every other kind has
+// PARTIAL tiles (windows' edges, causal diagonals, sink columns).
+bool launch_has_no_partial(const Normalized& n) {
+  if (n.N % kTile != 0) return false;
+  if (n.kind == kFull) return true;
+  if (n.kind != kChunk) return false;
+  for (const auto& hp : n.heads)
+    if (hp.param % kTile != 0 && hp.param < n.N) return false;
+  return true;
+}
+
 // ------------------------------------------------------------ planning (host)
 template <typename Fn>
 void walk_tiles_host(const Normalized& n, const uint64_t* host_bits, int h, int qt, Fn&& fn) {
@@ -770,6 +783,7 @@ int fwd_locked(const void* q, const void* k, const void* v, void* o, float* lse,
   p.items = plan->items;
   p.pitems = plan->pitems;
   p.after_prepass = (n.need_copy && !n.single) ? 1 : 0;
+  p.no_partial = launch_has_no_partial(n) ? 1 : 0;
   p.n_items = (int)plan->items_host.size();
   p.head_info = plan->head_info;
   p.perm = desc->perm;
@@ -885,6 +899,7 @@ int prepare_in_place_launch(const void* q, const void* k, const void* v, void* o
   p.scale_log2 = n.scale * 1.4426950408889634f;
   p.self_test_timeout = 0;
   p.split = n.split ? 1 : 0;
+  p.no_partial = launch_has_no_partial(n) ? 1 : 0;
   out->items = std::move(items);
   out->head_info.assign((size_t)H * 4, 0);
   for (int h = 0; h < H; ++h) {
