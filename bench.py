@@ -331,28 +331,8 @@ def run_gpu(args):
     achieved = flops / (per_launch_ms * 1e-3) / 1e12
     traffic = profile_traffic(wl_name)
 
-    # ---------------- the oracle on the GPU arm's own inputs (sampled rows)
-    parity = {}
-    cpu = None
-    if rank == 0 and world == 1 and not args.quick:
-        rows = sampled_rows(wl.N, 128, seed=1, extra=55)
-        heads = [0, wl.H - 1]
-        chk, secs, pr = oracle_check(q, k, v, o, lse, spec, heads, rows)
-        parity[f"{wl_name}/{mask_name}"] = chk
-        st_rows = rows[:16]
-        st_secs = oracle_single_thread(q, k, v, spec, 0, st_rows)
-        st_pairs = rows_pairs(spec, 0, wl.N, st_rows)
-        ci = cpu_info()
-        cpu = {"value": round(effective_flops(pr, wl.d) / secs / 1e12, 6), "unit": "TFLOP/s",
-               "cores": ci["affinity"], "cores_detail": ci, "kind": "oracle",
-               "sample": f"{wl_name}/{mask_name}: heads {heads}, {len(rows)} query rows each (first, last, block "
-                         f"edges, middle, random), every key scored in fp64 (numpy), {secs:.2f} s on all "
-                         f"{ci['affinity']} cores",
-               "single_thread": None if st_secs is None else {
-                   "value": round(effective_flops(st_pairs, wl.d) / st_secs / 1e12, 6), "unit": "TFLOP/s",
-                   "sample": f"head 0, {len(st_rows)} rows, one BLAS thread, {st_secs:.2f} s"}}
-
-    # ---------------- end to end through the host-buffer entry point
+    # ---------------- end to end through the host-buffer entry point (before the
+    # oracle's host work below, which would share the host with its copies)
     e2e = None
     if not args.quick:
         qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
@@ -393,6 +373,27 @@ def run_gpu(args):
                "device_ms_per_step": round(ms_per_step, 3), "kernel_share": round(ms_per_step / e2e_ms, 3),
                "numa": numa_info(local), "host_cpus": cpu_info()}
         del qh, kh, vh, oh, lh
+
+    # ---------------- the oracle on the GPU arm's own inputs (sampled rows)
+    parity = {}
+    cpu = None
+    if rank == 0 and world == 1 and not args.quick:
+        rows = sampled_rows(wl.N, 128, seed=1, extra=55)
+        heads = [0, wl.H - 1]
+        chk, secs, pr = oracle_check(q, k, v, o, lse, spec, heads, rows)
+        parity[f"{wl_name}/{mask_name}"] = chk
+        st_rows = rows[:16]
+        st_secs = oracle_single_thread(q, k, v, spec, 0, st_rows)
+        st_pairs = rows_pairs(spec, 0, wl.N, st_rows)
+        ci = cpu_info()
+        cpu = {"value": round(effective_flops(pr, wl.d) / secs / 1e12, 6), "unit": "TFLOP/s",
+               "cores": ci["affinity"], "cores_detail": ci, "kind": "oracle",
+               "sample": f"{wl_name}/{mask_name}: heads {heads}, {len(rows)} query rows each (first, last, block "
+                         f"edges, middle, random), every key scored in fp64 (numpy), {secs:.2f} s on all "
+                         f"{ci['affinity']} cores",
+               "single_thread": None if st_secs is None else {
+                   "value": round(effective_flops(st_pairs, wl.d) / st_secs / 1e12, 6), "unit": "TFLOP/s",
+                   "sample": f"head 0, {len(st_rows)} rows, one BLAS thread, {st_secs:.2f} s"}}
 
     del q, k, v, o, lse
     torch.cuda.empty_cache()
