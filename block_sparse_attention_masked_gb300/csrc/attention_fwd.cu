@@ -503,15 +503,21 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
       // are warp-collective, so every branch below is taken by whole warps
       // (each lane applying its own factors).
       float ts;
-      bool slow = __any_sync(0xffffffffu, m == -INFINITY);
-      if (!slow) {
-        // Running maximum known: exponentiate against it directly.  It only
-        // guards against overflow (the final normalisation uses the same m
-        // for numerator and denominator), so it is kept while every P stays
-        // below 2^40; a tile that breaks this (rare) is redone below.
-        ts = exp_to_tmem(x, sl2, m, s_tmem, none);
-        slow = __any_sync(0xffffffffu, !(ts <= kMaxTileSum));
-        if (slow) ptx::tmem_wait_st();  // let these stores land before they are overwritten
+      // Exponentiate against the running maximum, or against 0 for a row's
+      // first visible scores (kMinTileSum).  It only guards against overflow
+      // (the final normalisation uses the same m for numerator and
+      // denominator), so it is kept while every P stays below 2^40; a tile that
+      // breaks this, or a first tile whose visible scores all came out below
+      // 2^-64, is redone below against the tile's own maximum (rare).
+      const bool first = m == -INFINITY;
+      ts = exp_to_tmem(x, sl2, first ? 0.f : m, s_tmem, none);
+      // none == 0xf: this lane sees nothing of the tile (partial tiles only)
+      const bool sees = (none & 0xfu) != 0xfu;
+      bool slow = __any_sync(0xffffffffu, !(ts <= kMaxTileSum) || (first && sees && !(ts >= kMinTileSum)));
+      if (slow) {
+        ptx::tmem_wait_st();  // let these stores land before they are overwritten
+      } else if (first && sees) {
+        m = 0.f;  // the row's reference from here on
       }
       if (slow) {
         // tile maximum first (also the first tile of a row)

@@ -321,11 +321,21 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
         // P = exp2(s * scale * log2e - m) into tensor memory (the stale-max
         // rule of attention_fwd.cu: m only guards against overflow)
         float ts;
-        bool slow = __any_sync(0xffffffffu, m == -INFINITY);
-        if (!slow) {
-          ts = exp_to_tmem(x, sl2, m, s_tmem, none);
-          slow = __any_sync(0xffffffffu, !(ts <= kMaxTileSum));
-          if (slow) ptx::tmem_wait_st();
+        // Exponentiate against the running maximum, or against 0 for a row's
+        // first visible scores (kMinTileSum).  It only guards against overflow
+        // (the final normalisation uses the same m for numerator and
+        // denominator), so it is kept while every P stays below 2^40; a tile that
+        // breaks this, or a first tile whose visible scores all came out below
+        // 2^-64, is redone below against the tile's own maximum (rare).
+        const bool first = m == -INFINITY;
+        ts = exp_to_tmem(x, sl2, first ? 0.f : m, s_tmem, none);
+        // none == 0xf: this lane sees nothing of the tile (partial tiles only)
+        const bool sees = (none & 0xfu) != 0xfu;
+        bool slow = __any_sync(0xffffffffu, !(ts <= kMaxTileSum) || (first && sees && !(ts >= kMinTileSum)));
+        if (slow) {
+          ptx::tmem_wait_st();  // let these stores land before they are overwritten
+        } else if (first && sees) {
+          m = 0.f;  // the row's reference from here on
         }
         if (slow) {
           const float m_new = fmaxf(m, row_max(x, none) * sl2);

@@ -31,6 +31,14 @@ constexpr float kLn2 = 0.6931471805599453f;
 // 2^40 (no overflow in fp32 or bf16, nor in O's fp32 accumulation); a tile
 // above it is redone against the tile's true maximum.
 constexpr float kMaxTileSum = 1099511627776.0f;  // 2^40
+// Before a row has a running maximum, its first tile is exponentiated
+// against 0 and kept when the row sum lands in [2^-64, 2^40]: every P is
+// then finite and the row's largest is at least 2^-71, so whatever flushes
+// to zero is below 2^-55 of it (the standard algorithm, exponentiating
+// against the true maximum, drops the same terms below 2^-126 of it).  A
+// row that sees scores in the tile but sums below 2^-64 (all scores far
+// below 0), or above 2^40, is redone against the tile's own maximum.
+constexpr float kMinTileSum = 5.421010862427522e-20f;  // 2^-64
 
 // The CTA's key-tile list: entry j (0 <= j < n) is key tile kt(j).  Paired,
 // sub-tile s multiplies entry j when uses(j, s); split, entry j belongs to
