@@ -149,8 +149,11 @@ def numa_info(gpu_index: int) -> dict:
 
 def headline_config(wl, mask_name: str, pairs: int, world: int) -> dict:
     """The `config` of the benchmark line, the same in both arms."""
+    in_bytes = wl.B * (wl.H + 2 * (wl.kv_heads or wl.H)) * wl.N * wl.d * (4 if wl.dtype == "f32" else 2)
+    l2 = (f"inputs larger than L2 ({in_bytes / 2**30:.2f} GiB)" if in_bytes > 2 * 129e6
+          else "flushed (512 MiB write) before each run")
     return {"workload": wl.name, "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d, "mask": mask_name,
-            "mask_detail": wl.description, "pairs": int(pairs), "l2": "inputs larger than L2 (3 GiB)",
+            "mask_detail": wl.description, "pairs": int(pairs), "l2": l2,
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
@@ -479,6 +482,10 @@ def run_gpu(args):
             raise RuntimeError(f"device error word {word:#x} after the workload sweep")
 
 
+    sched = mattn.plan_schedule(mask, wl.B, wl.N, wl.d, mattn.F32 if wl.dtype == "f32" else mattn.BF16)
+    family = {"paired": "attention_fwd_kernel", "split": "attention_fwd_kernel",
+              "persistent": "attention_persist_kernel", "single": "attention_sp_kernel"}.get(sched, sched)
+    headline_kernel = f"{family}<{wl.d}> ({sched} schedule)"
     if rank == 0:
         clocks = clk.summary()
         line = {
@@ -490,7 +497,7 @@ def run_gpu(args):
             "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
                          "traffic": traffic, "peak_source": peaks["source"] + " burst bf16 (cuBLAS)",
-                         "kernel": "attention_fwd_kernel<128,false>"},
+                         "kernel": headline_kernel},
             "cpu_baseline": cpu,
             "parity": parity,
             "e2e": e2e,

@@ -410,3 +410,37 @@ def test_chunk2d_order(d):
         for spec in (MaskSpec("sliding", [64, 64, 200], perm=perm),
                      MaskSpec("chunk", [win * win, 128, 256], perm=perm, sink=np.array([0.3, -1.0, 0.0]))):
             check(q, k, v, spec, tag=f"chunk2d {spec.kind} {rows}x{cols}/{win} d{d}")
+
+
+def _extreme_qkv(H, N, d, seed):
+    """Scores s_ij = A_i b_j along one direction u (plus small noise): row
+    scales A_i cycle through -150, -80, -30, 1, 30, 80, 150 and key scales
+    b_j ramp from 0.8 to 1.0.  Rows at -150 see only scores whose
+    exponentials against 0 flush to zero (below 2^-126: kept, they would
+    give O = 0 and LSE = -inf), rows at -80 first-tile sums below 2^-64,
+    rows at 80 and 150 first tiles above 2^40 (150: exponentials that
+    overflow to inf) and later tiles another 2^40 and more above the first
+    tile's maximum (the running maximum is raised and O rescaled)."""
+    g = torch.Generator().manual_seed(seed)
+    u = torch.randn(H, 1, d, generator=g)
+    u = u / u.norm(dim=-1, keepdim=True)
+    a = torch.tensor([-150.0, -80.0, -30.0, 1.0, 30.0, 80.0, 150.0]).repeat(N // 7 + 1)[:N] * (d ** 0.5)
+    b = torch.linspace(0.8, 1.0, N)
+    q = a[None, :, None] * u + 0.05 * torch.randn(H, N, d, generator=g)
+    k = b[None, :, None] * u + 0.05 * torch.randn(H, N, d, generator=g)
+    v = torch.randn(H, N, d, generator=g)
+    return tuple(t[None].to(torch.bfloat16).cuda() for t in (q, k, v))
+
+
+@pytest.mark.parametrize("schedule", ["paired", "split", "persistent"])
+@pytest.mark.parametrize("d", [80, 128])
+def test_extreme_score_ranges(d, schedule):
+    """Rows whose scores lie far below 0 and rows whose scores grow by more
+    than 2^40 across key tiles: the exponentials' reference (0 for a row's
+    first visible tile, then the running maximum) is redone against the
+    tile's own maximum where it would underflow or overflow."""
+    N = 1000
+    q, k, v = _extreme_qkv(2, N, d, seed=d)
+    for spec in (MaskSpec("full", [0, 0]), MaskSpec("sliding", [200, 130]), MaskSpec("chunk", [256, 500]),
+                 MaskSpec("causal_window", [300, 1000], sink=np.array([0.5, -2.0]))):
+        check(q, k, v, spec, tag=f"{spec.kind} d{d} {schedule}", schedule=schedule)
