@@ -11,8 +11,8 @@
 // and O_s / (l_s + exp(sink)) with the log-sum-exp at the end (SHS slides
 // Eq. 1 for the sink; the FlashAttention idea of the Vision transformers
 // lesson).  What differs is the schedule: the grid has one CTA per SM and
-// CTA c takes work items c, c + G, c + 2G, ... (G = grid size; the host's
-// list is heaviest first).  Its key-tile lists are walked as one stream, so
+// each CTA takes the work items the host assigned it (longest first, each
+// to the least-loaded CTA).  Its key-tile lists are walked as one stream, so
 // the K/V rings, the MMA issue order and the softmax never drain between
 // items: the next item's Q tiles are loaded while the current one runs (Q
 // slots rotate) and its first Q K^T goes to the tensor core in the same
@@ -182,9 +182,10 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
     uint32_t pcount = 0;  // P tiles consumed
     int e = 0;
     int i = 0;  // the CTA's item count so far
-    for (int it = blockIdx.x; ok && it < p.n_items; it += gridDim.x, ++i) {
+    const CtaItems items = cta_items(p);
+    for (int it = items.first; ok && it < items.end; ++it, ++i) {
       const PItem pi = load_pitem(p, it);
-      prefetch_pitem(p, it + gridDim.x);
+      prefetch_pitem(p, it + 1);
       if (!check_or_abort(p, bar, pitem_ok(p, pi), kSiteItem)) {
         ok = false;
         break;
@@ -275,9 +276,10 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
     int o_items = 0;     // items whose O_s has been read
     uint32_t sync_seq = 0;  // uses of stage_sync[s]
     bool ok = true;
-    for (int it = blockIdx.x; ok && it < p.n_items; it += gridDim.x) {
+    const CtaItems items = cta_items(p);
+    for (int it = items.first; ok && it < items.end; ++it) {
       const PItem pi = load_pitem(p, it);
-      prefetch_pitem(p, it + gridDim.x);
+      prefetch_pitem(p, it + 1);
       if (!check_or_abort(p, bar, pitem_ok(p, pi), kSiteItem)) {
         ok = false;
         break;

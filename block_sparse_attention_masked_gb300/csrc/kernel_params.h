@@ -115,6 +115,7 @@ struct FwdParams {
   float* lse;                       // [B][H][N] or null
   const int2* items;                // (b*H + h, query-tile pair), or (b*H + h, query tile) when split
   const int4* pitems;               // persistent kernel: kPersistItemInt4 int4 per work item
+  const int* cta_off;               // persistent kernel: CTA c takes pitems [cta_off[c], cta_off[c+1])
   const int32_t* head_info;         // [H][4], HeadField
   const int32_t* perm;              // explicit orders [n_perm][N]
   int n_perm;

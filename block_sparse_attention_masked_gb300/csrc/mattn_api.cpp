@@ -15,6 +15,7 @@
 #include <map>
 #include <memory>
 #include <mutex>
+#include <queue>
 #include <string>
 #include <vector>
 
@@ -97,9 +98,11 @@ struct Normalized {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Average key tiles per query tile up to which an interval mask runs on the
-// persistent kernel by default (measured on GB300: windows of 3-7 tiles ran
-// 1.2-1.6x faster persistent, lists of 16 and more 3-20% slower).
-constexpr double kPersistMaxTiles = 12.0;
+// persistent kernel by default.  Measured on GB300 with the items assigned
+// longest first: windows of 3-7 tiles 1.2-1.6x faster persistent, head-wise
+// windows of 5-33 tiles (17 on average) and 32-tile full masks 0-4% faster,
+// 128-tile full masks 1.5% slower.
+constexpr double kPersistMaxTiles = 40.0;
 
 // allow_block_tma: the caller's kernel reads the 2x2-block row-major order
 // through its 5D TMA views (the attention forward); otherwise such heads go
@@ -386,10 +389,13 @@ std::vector<int4> build_persist_items(const Normalized& n, const std::vector<int
 struct Plan {
   std::vector<int2> items_host;
   std::vector<int32_t> head_info_host;
-  std::vector<int4> pitems_host;  // persistent kernel: the items' descriptors
+  std::vector<int4> pitems_host;  // persistent kernel: the items' descriptors, CTA by CTA
+  std::vector<int> cta_off_host;  // persistent kernel: CTA c takes descriptors [off[c], off[c+1])
+  int persist_grid = 0;           // persistent kernel: CTAs of the launch
   int2* items = nullptr;
   int32_t* head_info = nullptr;
   int4* pitems = nullptr;
+  int* cta_off = nullptr;
 };
 
 struct DeviceBuf {
@@ -449,11 +455,51 @@ int device_state(DeviceState** out) {
   return MATTN_OK;
 }
 
-std::string plan_key(const Normalized& n) {
+// The persistent kernel's work items assigned to `grid` CTAs: longest first,
+// each to the CTA with the least load so far (the longest-processing-time
+// rule), then laid out CTA by CTA so that CTA c takes descriptors
+// [off[c], off[c + 1]).  An item's load is the tile products its sub-tiles
+// multiply plus a fixed share for its set-up and output (kItemOverheadTiles).
+// Items of one mask kind with equal windows get equal loads and fall to the
+// CTAs in turn; head-wise windows (a few key tiles next to tens) no longer
+// leave the CTAs holding two long items to run while others idle.
+constexpr int kItemOverheadTiles = 4;
+
+void assign_persist_items(std::vector<int4>* d, int grid, std::vector<int>* off) {
+  const size_t n = d->size() / kPersistItemInt4;
+  std::vector<std::pair<int, int>> order(n);  // (load, item)
+  for (size_t i = 0; i < n; ++i) {
+    const int4 u = (*d)[i * kPersistItemInt4 + 5];  // first / last entries of each sub-tile
+    const int tiles = (u.x >= 0 ? u.y - u.x + 1 : 0) + (u.z >= 0 ? u.w - u.z + 1 : 0);
+    order[i] = {tiles + kItemOverheadTiles, (int)i};
+  }
+  std::stable_sort(order.begin(), order.end(), [](const auto& a, const auto& b) { return a.first > b.first; });
+  std::vector<std::vector<int>> per(grid);
+  std::priority_queue<std::pair<long, int>, std::vector<std::pair<long, int>>, std::greater<>> heap;
+  for (int c = 0; c < grid; ++c) heap.push({0, c});
+  for (const auto& [load, i] : order) {
+    auto [l, c] = heap.top();
+    heap.pop();
+    per[c].push_back(i);
+    heap.push({l + load, c});
+  }
+  std::vector<int4> out;
+  out.reserve(d->size());
+  off->assign(grid + 1, 0);
+  for (int c = 0; c < grid; ++c) {
+    (*off)[c] = (int)(out.size() / kPersistItemInt4);
+    for (int i : per[c])
+      for (int w = 0; w < kPersistItemInt4; ++w) out.push_back((*d)[(size_t)i * kPersistItemInt4 + w]);
+  }
+  (*off)[grid] = (int)(out.size() / kPersistItemInt4);
+  d->swap(out);
+}
+
+std::string plan_key(const Normalized& n, int persist_grid) {
   std::string k;
   char buf[96];
   snprintf(buf, sizeof(buf), "%d|%d|%d|%d|%d|%d|%d|%d|%d|", n.kind, n.B, n.H, n.N, n.need_copy ? 1 : 0,
-           n.split ? 1 : 0, n.sink_tokens, n.single ? 1 : 0, n.persistent ? 1 : 0);
+           n.split ? 1 : 0, n.sink_tokens, n.single ? 1 : 0, n.persistent ? persist_grid : 0);
   k += buf;
   for (const auto& hp : n.heads) {
     snprintf(buf, sizeof(buf), "%d,%d,%d,%d;", hp.param, hp.load, hp.store, hp.perm_row);
@@ -462,8 +508,10 @@ std::string plan_key(const Normalized& n) {
   return k;
 }
 
-int get_plan(DeviceState* st, const Normalized& n, cudaStream_t stream, Plan** out) {
-  std::string key = plan_key(n);
+// persist_grid: the persistent kernel's CTAs before clamping to the item
+// count (one per SM, or the test hook's cap); ignored for other schedules.
+int get_plan(DeviceState* st, const Normalized& n, cudaStream_t stream, Plan** out, int persist_grid = 0) {
+  std::string key = plan_key(n, persist_grid);
   auto it = st->plans.find(key);
   if (it != st->plans.end()) {
     *out = it->second.get();
@@ -480,11 +528,17 @@ int get_plan(DeviceState* st, const Normalized& n, cudaStream_t stream, Plan** o
   }
   if (n.persistent) {
     pl->pitems_host = build_persist_items(n, pl->items_host);
+    pl->persist_grid = std::max(1, std::min<int>(persist_grid, (int)pl->items_host.size()));
+    assign_persist_items(&pl->pitems_host, pl->persist_grid, &pl->cta_off_host);
     MATTN_CUDA(cudaMalloc(&pl->pitems, std::max<size_t>(1, pl->pitems_host.size()) * sizeof(int4)),
                "cudaMalloc(item descriptors)");
     MATTN_CUDA(cudaMemcpyAsync(pl->pitems, pl->pitems_host.data(), pl->pitems_host.size() * sizeof(int4),
                                cudaMemcpyHostToDevice, stream),
                "upload item descriptors");
+    MATTN_CUDA(cudaMalloc(&pl->cta_off, pl->cta_off_host.size() * sizeof(int)), "cudaMalloc(CTA item ranges)");
+    MATTN_CUDA(cudaMemcpyAsync(pl->cta_off, pl->cta_off_host.data(), pl->cta_off_host.size() * sizeof(int),
+                               cudaMemcpyHostToDevice, stream),
+               "upload CTA item ranges");
   }
   MATTN_CUDA(cudaMalloc(&pl->items, std::max<size_t>(1, pl->items_host.size()) * sizeof(int2)), "cudaMalloc(items)");
   MATTN_CUDA(cudaMalloc(&pl->head_info, pl->head_info_host.size() * sizeof(int32_t)), "cudaMalloc(head table)");
@@ -715,7 +769,8 @@ int fwd_locked(const void* q, const void* k, const void* v, void* o, float* lse,
   rc = get_encoder();
   if (rc) return rc;
   Plan* plan = nullptr;
-  rc = get_plan(st, n, stream, &plan);
+  const int cap = g_persist_grid_cap.load();
+  rc = get_plan(st, n, stream, &plan, (cap > 0 && cap < st->sm_count) ? cap : st->sm_count);
   if (rc) return rc;
 
   const size_t elems = (size_t)B * H * N * d;
@@ -782,6 +837,7 @@ int fwd_locked(const void* q, const void* k, const void* v, void* o, float* lse,
   p.lse = lse;
   p.items = plan->items;
   p.pitems = plan->pitems;
+  p.cta_off = plan->cta_off;
   p.after_prepass = (n.need_copy && !n.single) ? 1 : 0;
   p.no_partial = launch_has_no_partial(n) ? 1 : 0;
   p.n_items = (int)plan->items_host.size();
@@ -819,9 +875,8 @@ int fwd_locked(const void* q, const void* k, const void* v, void* o, float* lse,
   if (n.single)
     MATTN_CUDA(launch_attention_sp(p, d, stream), "attention launch (single pipeline)");
   else if (n.persistent) {
-    const int cap = g_persist_grid_cap.load();
-    const int grid = (cap > 0 && cap < st->sm_count) ? cap : st->sm_count;
-    MATTN_CUDA(launch_attention_persist(p, d, dtype == MATTN_F32, grid, stream), "attention launch (persistent)");
+    MATTN_CUDA(launch_attention_persist(p, d, dtype == MATTN_F32, plan->persist_grid, stream),
+               "attention launch (persistent)");
   } else
     MATTN_CUDA(launch_attention(p, d, dtype == MATTN_F32, stream), "attention launch");
   if (planted.b.ptr) MATTN_CUDA(cudaStreamSynchronize(stream), "corrupted launch");  // before the list is freed

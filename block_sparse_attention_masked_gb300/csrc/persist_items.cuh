@@ -1,9 +1,8 @@
-// Work items of the persistent attention kernels (attention_persist.cu,
-// attention_stream.cu) and the two TMA producer loops they share.  A work
-// item is a query-tile pair of one (batch, head) whose key-tile plan the
-// host worked out (plan_rules.h; layout kPersistItemInt4 in kernel_params.h);
-// CTA c takes items c, c + G, c + 2G, ... (G = grid size) and walks their
-// key-tile lists as one stream.
+// Work items of the persistent attention kernel (attention_persist.cu) and
+// its two TMA producer loops.  A work item is a query-tile pair of one
+// (batch, head) whose key-tile plan the host worked out (plan_rules.h;
+// layout kPersistItemInt4 in kernel_params.h); each CTA takes the items the
+// host assigned it (cta_items) and walks their key-tile lists as one stream.
 #pragma once
 
 #include <cuda.h>
@@ -115,6 +114,20 @@ __device__ __forceinline__ void row_interval32(int kind, int param, int n, int p
   }
 }
 
+// The CTA's work items: descriptors [first, end) of p.pitems (the host
+// assigns items to CTAs and lays them out CTA by CTA).  Debug builds: an
+// empty range, after recording the failure, when the range is not inside
+// the launch's items.
+struct CtaItems {
+  int first, end;
+};
+
+__device__ __forceinline__ CtaItems cta_items(const FwdParams& p) {
+  CtaItems r{__ldg(p.cta_off + blockIdx.x), __ldg(p.cta_off + blockIdx.x + 1)};
+  if (!debug_check(p.err, r.first >= 0 && r.first <= r.end && r.end <= p.n_items, kSiteItem)) r.end = r.first;
+  return r;
+}
+
 // Q and K producer (one thread): Q tile t = 2 i + s (i = the CTA's i-th
 // item, s its sub-tile) goes to slot t % NQ, K tiles of the concatenated
 // key-tile lists to ring slot e % KS.  `Bar` has q_full / q_empty [NQ],
@@ -132,25 +145,27 @@ __device__ __forceinline__ void produce_q_k(const FwdParams& p, Bar* bar, uint8_
   // that stays busy while the other stream's slot frees up).
   const uint64_t keep = ptx::l2_policy_evict_last();
   const uint64_t once = ptx::l2_policy_evict_first();
-  int qit = blockIdx.x, kit = blockIdx.x;  // items of the Q and K streams
+  const CtaItems items = cta_items(p);
+  const int iend = items.end;
+  int qit = items.first, kit = items.first;  // items of the Q and K streams
   PItem qi, ki;
-  if (qit < p.n_items) qi = load_pitem(p, qit);
-  if (kit < p.n_items) ki = load_pitem(p, kit);
-  prefetch_pitem(p, qit + gridDim.x);
+  if (qit < iend) qi = load_pitem(p, qit);
+  if (kit < iend) ki = load_pitem(p, kit);
+  prefetch_pitem(p, qit + 1);
   int qs = 0;      // sub-tile of the next Q tile
   int t = 0;       // next Q tile
   int kj = 0;      // next entry of the current K item
   int e = 0;       // next entry of the K stream
-  while (kit < p.n_items && ki.L.n == 0) {  // (no item has an empty list; kept for safety)
-    kit += gridDim.x;
-    if (kit < p.n_items) ki = load_pitem(p, kit);
+  while (kit < iend && ki.L.n == 0) {  // (no item has an empty list; kept for safety)
+    ++kit;
+    if (kit < iend) ki = load_pitem(p, kit);
   }
   uint64_t t_idle = 0;  // start of the current stretch without progress
   uint32_t idle = 0;
   bool failed = false;
-  while (qit < p.n_items || kit < p.n_items) {
+  while (qit < iend || kit < iend) {
     bool moved = false;
-    if (kit < p.n_items) {
+    if (kit < iend) {
       const int slot = e % KS;
       if (ptx::mbar_test_wait(&bar->k_empty[slot], ((e / KS) & 1) ^ 1)) {
         const int kt = list_kt(ki.L, kj);
@@ -167,14 +182,14 @@ __device__ __forceinline__ void produce_q_k(const FwdParams& p, Bar* bar, uint8_
         if (++kj == ki.L.n) {
           kj = 0;
           do {
-            kit += gridDim.x;
-            if (kit < p.n_items) ki = load_pitem(p, kit);
-          } while (kit < p.n_items && ki.L.n == 0);
+            ++kit;
+            if (kit < iend) ki = load_pitem(p, kit);
+          } while (kit < iend && ki.L.n == 0);
         }
         moved = true;
       }
     }
-    if (qit < p.n_items) {
+    if (qit < iend) {
       const int slot = t % NQ;
       if (ptx::mbar_test_wait(&bar->q_empty[slot], ((t / NQ) & 1) ^ 1)) {
         if (!check_or_abort(p, bar, pitem_ok(p, qi), kSiteItem)) break;
@@ -192,9 +207,9 @@ __device__ __forceinline__ void produce_q_k(const FwdParams& p, Bar* bar, uint8_
         ++t;
         if (++qs == 2) {
           qs = 0;
-          qit += gridDim.x;
-          if (qit < p.n_items) qi = load_pitem(p, qit);
-          prefetch_pitem(p, qit + gridDim.x);
+          ++qit;
+          if (qit < iend) qi = load_pitem(p, qit);
+          prefetch_pitem(p, qit + 1);
         }
         moved = true;
       }
@@ -228,9 +243,10 @@ __device__ __forceinline__ void produce_v(const FwdParams& p, Bar* bar, uint8_t*
   const uint64_t keep = ptx::l2_policy_evict_last();
   int e = 0;
   bool ok = true;
-  for (int it = blockIdx.x; ok && it < p.n_items; it += gridDim.x) {
+  const CtaItems items = cta_items(p);
+  for (int it = items.first; ok && it < items.end; ++it) {
     const PItem pi = load_pitem(p, it);
-    prefetch_pitem(p, it + gridDim.x);
+    prefetch_pitem(p, it + 1);
     if (!check_or_abort(p, bar, pitem_ok(p, pi), kSiteItem)) break;
     for (int j = 0; j < pi.L.n; ++j, ++e) {
       const int slot = e % VS;
