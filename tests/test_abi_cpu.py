@@ -238,7 +238,7 @@ def test_column_major_grid_description_matches_explicit_order(L):
 def test_plan_schedule_follows_the_stated_rules(L):
     """The schedule mattn_fwd runs, on the host: a flag wins; otherwise SPLIT
     for 128-blocks, SINGLE at head dim 256, PERSISTENT for interval masks
-    whose query tiles see about 12 key tiles or fewer, PAIRED for the rest."""
+    whose query tiles see about 40 key tiles or fewer, PAIRED for the rest."""
     from workloads import WORKLOADS, make_mask
 
     def sched(wl_name, mask, d=None, flags=None):
@@ -253,7 +253,8 @@ def test_plan_schedule_follows_the_stated_rules(L):
     assert sched("vit16384", "chunk512") == "persistent"
     assert sched("vit16384", "full") == "paired"
     assert sched("vit4096", "sliding128") == "persistent"
-    assert sched("causal4096", "causal_window_sink") == "paired"  # windows up to 4096: ~16 tiles on average
+    assert sched("causal4096", "causal_window_sink") == "persistent"  # windows up to 4096: ~16 tiles on average
+    assert sched("vit4096", "full") == "persistent"  # 32 tiles
     assert sched("gqa32k", "swa572_sinktok4") == "persistent"
     assert sched("bsparse128k", "block128") == "split"
     assert sched("prefill_d256", "swa576_sink") == "single"
