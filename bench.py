@@ -347,13 +347,14 @@ def run_gpu(args):
         e2e_steps = max(1, min(args.steps, 5))
         barrier(dist)
         torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        call_ms = []
-        for _ in range(e2e_steps):
-            tc = time.perf_counter()
-            mattn.attention_host(qh, kh, vh, hmask, out=oh, lse=lh)
-            call_ms.append(round(1e3 * (time.perf_counter() - tc), 3))
-        e2e_s = max_over_ranks(dist, time.perf_counter() - t0, device=dev)
+        with ClockSampler(local) as e2e_clk:
+            t0 = time.perf_counter()
+            call_ms = []
+            for _ in range(e2e_steps):
+                tc = time.perf_counter()
+                mattn.attention_host(qh, kh, vh, hmask, out=oh, lse=lh)
+                call_ms.append(round(1e3 * (time.perf_counter() - tc), 3))
+            e2e_s = max_over_ranks(dist, time.perf_counter() - t0, device=dev)
         barrier(dist)
         tensor_bytes = q.numel() * q.element_size()
         bits_bytes = int(hmask.block_words_host.nbytes) if spec.kind == "block" else 0
@@ -373,7 +374,8 @@ def run_gpu(args):
         in_bytes, out_bytes = 3 * tensor_bytes + bits_bytes, tensor_bytes + lse.numel() * 4
         e2e = {"value": round(world * flops * e2e_steps / e2e_s / 1e12, 2), "unit": "TFLOP/s",
                "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
-               "ms_per_step": round(e2e_ms, 3), "calls_ms": call_ms, "entry_point": "mattn_fwd_host",
+               "ms_per_step": round(e2e_ms, 3), "calls_ms": call_ms, "clocks": e2e_clk.summary(),
+               "entry_point": "mattn_fwd_host",
                "h2d_gbs": round(h2d_gbs, 1), "d2h_gbs": round(d2h_gbs, 1),
                "copy_ms_at_those_rates": round(1e3 * (in_bytes / (h2d_gbs * 1e9) + out_bytes / (d2h_gbs * 1e9)), 2),
                "device_ms_per_step": round(ms_per_step, 3), "kernel_share": round(ms_per_step / e2e_ms, 3),
