@@ -367,6 +367,28 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
       // first S: wait for the P V, read O_s, write O / (l + exp(sink)) and
       // the LSE in caller token order.
       const bool has_o = list_has(L, s, false);
+      // What does not need O comes first, while the last P V runs: the
+      // row's scale, its LSE (stored) and output row, and (staged output)
+      // the staging tile, free once its previous store has read it.
+      const float b2 = p.sink ? __ldg(p.sink + pi.ip.h) * kLog2e : -INFINITY;
+      float o_scale, unused, lse_v;
+      finalize_row(m, l, -INFINITY, 0.f, b2, &o_scale, &unused, &lse_v);
+      bool valid = pos < p.N;
+      const int64_t tok = valid ? out_token(p, pi.store, pi.perm_row, pos) : 0;
+      if (kDebugChecks && tok < 0) valid = false;
+      const int64_t orow = ((int64_t)pi.ip.bh * p.N + tok) * D;
+      if (valid && p.lse) p.lse[(int64_t)pi.ip.bh * p.N + tok] = lse_v;
+      const bool staged = PG::kStage && p.o_tma;
+      uint8_t* stage = sstage + s * G::kTileBytes;
+      const bool leader = quarter == 0 && lane == 0;
+      if (staged && has_o) {
+        if (leader) ptx::bulk_wait_read_all();  // the previous store has read the tile
+        if (!__all_sync(0xffffffffu, ptx::mbar_sync(&bar->stage_sync[s], sync_seq, p.timeout_ns, abort_flag))) {
+          if (lane == 0) raise_error(p, bar, kErrEpilogue);
+          ok = false;
+          break;
+        }
+      }
       if (has_o) {
         bool got = ptx::mbar_wait(&bar->o_full[s], o_items & 1, p.timeout_ns, abort_flag);
         if (!__all_sync(0xffffffffu, got)) {
@@ -377,25 +399,10 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
         ++o_items;
         ptx::tc_fence_after();
       }
-      const float b2 = p.sink ? __ldg(p.sink + pi.ip.h) * kLog2e : -INFINITY;
-      float o_scale, unused, lse_v;
-      finalize_row(m, l, -INFINITY, 0.f, b2, &o_scale, &unused, &lse_v);
-      bool valid = pos < p.N;
-      const int64_t tok = valid ? out_token(p, pi.store, pi.perm_row, pos) : 0;
-      if (kDebugChecks && tok < 0) valid = false;
-      const int64_t orow = ((int64_t)pi.ip.bh * p.N + tok) * D;
-      if (PG::kStage && p.o_tma) {
+      if (staged) {
         // Through shared memory: each thread writes its row into this
         // sub-tile's staging tile, one thread stores the tile with TMA.
-        uint8_t* stage = sstage + s * G::kTileBytes;
-        const bool leader = quarter == 0 && lane == 0;
         if (has_o) {
-          if (leader) ptx::bulk_wait_read_all();  // the previous store has read the tile
-          if (!__all_sync(0xffffffffu, ptx::mbar_sync(&bar->stage_sync[s], sync_seq, p.timeout_ns, abort_flag))) {
-            if (lane == 0) raise_error(p, bar, kErrEpilogue);
-            ok = false;
-            break;
-          }
 #pragma unroll
           for (int c0 = 0; c0 < D; c0 += 16) {
             float ov[16];
@@ -450,7 +457,6 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
           }
         }
       }
-      if (valid && p.lse) p.lse[(int64_t)pi.ip.bh * p.N + tok] = lse_v;
     }
   }
 
