@@ -55,6 +55,7 @@ struct SpGeo {
 constexpr float kLog2eX = 1.4426950408889634f;
 constexpr float kLn2X = 0.6931471805599453f;
 constexpr float kMaxTileSumX = 1099511627776.0f;  // 2^40, as in the d <= 128 kernel
+constexpr float kMinTileSumX = 5.421010862427522e-20f;  // 2^-64: a row's first tile against 0, as there
 
 struct BarD256 {
   uint64_t q_full;
@@ -406,10 +407,12 @@ __global__ void __launch_bounds__(kThreadsD256, 1) attention_sp_kernel(const __g
       const bool partial = block ? block_tile_class(qt, kt, p.N) == kTilePartial
                            : p.sink_tokens > 0 ? sink_window_tile_class(param, p.sink_tokens, p.N, qt, kt) == kTilePartial
                                                : interval_tile_class(L.r, kt) == kTilePartial;
+      bool sees = true;  // this row sees a key of the tile
       if (partial || k0 + kKT > p.N) {
         const int c_lo = (int)(lo - k0 < -1 ? -1 : (lo - k0 > kKT ? kKT : lo - k0));
         const int c_hi = (int)(hi - k0 < -1 ? -1 : (hi - k0 > kKT ? kKT : hi - k0));
         const int c_s = (int)(sink_hi - k0 < -1 ? -1 : (sink_hi - k0 > kKT ? kKT : sink_hi - k0));
+        sees = c_s >= 0 || (max(c_lo, 0) <= min(c_hi, kKT - 1));
         if (c_s < 0) {
 #pragma unroll
           for (int c = 0; c < kKT; ++c)
@@ -420,9 +423,11 @@ __global__ void __launch_bounds__(kThreadsD256, 1) attention_sp_kernel(const __g
             if ((c < c_lo || c > c_hi) && c > c_s) x[c] = -INFINITY;
         }
       }
-      // exponentiate against the running (stale) maximum; a tile whose row
-      // sum would pass 2^40 is redone against its own maximum, rescaling O
-      // once the previous P V (which adds into O) is done
+      // exponentiate against the running (stale) maximum, or against 0 for a
+      // row's first visible scores; a tile whose row sum passes 2^40, or a
+      // first tile whose visible scores sum below 2^-64, is redone against
+      // its own maximum, rescaling O once the previous P V (which adds into
+      // O) is done
       auto exp_pass = [&](float mref, float& sum) {
         const float2 sl2v = make_float2(sl2, sl2);
         const float2 negm = make_float2(-mref, -mref);
@@ -443,11 +448,13 @@ __global__ void __launch_bounds__(kThreadsD256, 1) attention_sp_kernel(const __g
         sum = a.x + a.y;
       };
       float ts = 0.f;
-      bool slow = __any_sync(0xffffffffu, m == -INFINITY);
-      if (!slow) {
-        exp_pass(m, ts);
-        slow = __any_sync(0xffffffffu, !(ts <= kMaxTileSumX));
-        if (slow) ptx::tmem_wait_st();
+      const bool first = m == -INFINITY;
+      exp_pass(first ? 0.f : m, ts);
+      bool slow = __any_sync(0xffffffffu, !(ts <= kMaxTileSumX) || (first && sees && !(ts >= kMinTileSumX)));
+      if (slow) {
+        ptx::tmem_wait_st();
+      } else if (first && sees) {
+        m = 0.f;  // the row's reference from here on
       }
       if (slow) {
         float mx = x[0];

@@ -58,7 +58,7 @@ def _subset(spec, hs):
                     sink_tokens=getattr(spec, "sink_tokens", 0))
 
 
-def check(q, k, v, spec, rows=None, heads=None, tag="", schedule=None):
+def check(q, k, v, spec, rows=None, heads=None, tag="", schedule=None, max_abs=MAX_ABS):
     B, H, N, d = q.shape
     mask = mattn.prepare(spec, H, N, schedule=schedule)
     o, lse = mattn.attention(q, k, v, mask)
@@ -91,7 +91,7 @@ def check(q, k, v, spec, rows=None, heads=None, tag="", schedule=None):
     diff = np.where(fin, got_lse, 0.0) - np.where(fin, ref_lse, 0.0)
     lse_bad = fin & (np.abs(diff) > lse_tol)
     lse_err = np.abs(got_lse[fin] - ref_lse[fin]).max() if fin.any() else 0.0
-    assert err.max() <= MAX_ABS, f"{tag}: max abs {err.max():.3e}"
+    assert err.max() <= max_abs, f"{tag}: max abs {err.max():.3e}"
     assert rel <= REL_L2, f"{tag}: rel L2 {rel:.3e}"
     assert not lse_bad.any(), f"{tag}: lse err {lse_err:.3e} above tolerance"
     return o, lse
@@ -432,15 +432,21 @@ def _extreme_qkv(H, N, d, seed):
     return tuple(t[None].to(torch.bfloat16).cuda() for t in (q, k, v))
 
 
-@pytest.mark.parametrize("schedule", ["paired", "split", "persistent"])
-@pytest.mark.parametrize("d", [80, 128])
+@pytest.mark.parametrize("d,schedule", [(80, "paired"), (80, "split"), (80, "persistent"), (128, "paired"),
+                                        (128, "split"), (128, "persistent"), (128, "single"), (256, "single")])
 def test_extreme_score_ranges(d, schedule):
     """Rows whose scores lie far below 0 and rows whose scores grow by more
     than 2^40 across key tiles: the exponentials' reference (0 for a row's
     first visible tile, then the running maximum) is redone against the
-    tile's own maximum where it would underflow or overflow."""
+    tile's own maximum where it would underflow or overflow.
+
+    These rows' softmax weights sit on a few keys, so the bf16 rounding of P
+    (2^-9 relative per weight; O moves by up to 2^-9 sum_j w_j |V_j|) is
+    hardly averaged: the per-element bound is 4e-2 here instead of 2e-2
+    (measured up to 2.2e-2 at d = 256, the same before and after the
+    reference-0 rule); rel L2 and LSE keep their usual bounds."""
     N = 1000
     q, k, v = _extreme_qkv(2, N, d, seed=d)
     for spec in (MaskSpec("full", [0, 0]), MaskSpec("sliding", [200, 130]), MaskSpec("chunk", [256, 500]),
                  MaskSpec("causal_window", [300, 1000], sink=np.array([0.5, -2.0]))):
-        check(q, k, v, spec, tag=f"{spec.kind} d{d} {schedule}", schedule=schedule)
+        check(q, k, v, spec, tag=f"{spec.kind} d{d} {schedule}", schedule=schedule, max_abs=4e-2)
