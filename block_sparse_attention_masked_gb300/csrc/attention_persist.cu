@@ -86,6 +86,7 @@ struct PBarriers {
   uint32_t tmem_base;
   int abort_flag;
   uint32_t mma_turn;       // ticket of the MMA group that may be issued next
+  int item_first, item_end;  // the CTA's work items (read_cta_items)
 };
 
 template <int D, bool OUT_F32, bool MASK>
@@ -112,6 +113,12 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
     // after the reorder pre-pass: no wait of this CTA may start while its
     // copies are still being written
     if (p.after_prepass) asm volatile("griddepcontrol.wait;" ::: "memory");
+    // the CTA's item range, the raster maps' descriptors and (below) its
+    // first item's descriptor are fetched while the barriers are set up
+    const CtaItems items = read_cta_items(p);
+    ptx::prefetch_tmap(&p.tq[0]);
+    ptx::prefetch_tmap(&p.tk[0]);
+    ptx::prefetch_tmap(&p.tv[0]);
     for (int i = 0; i < NQ; ++i) {
       ptx::mbar_init(&bar->q_full[i], 1);
       ptx::mbar_init(&bar->q_empty[i], 1);
@@ -132,6 +139,9 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
     ptx::mbar_init(&bar->never, 1);
     bar->abort_flag = 0;
     bar->mma_turn = 0;
+    bar->item_first = items.first;
+    bar->item_end = items.end;
+    prefetch_pitem(p, items.first);
     ptx::fence_barrier_init();
   }
   if (warp == 1) {
@@ -182,7 +192,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
     uint32_t pcount = 0;  // P tiles consumed
     int e = 0;
     int i = 0;  // the CTA's item count so far
-    const CtaItems items = cta_items(p);
+    const CtaItems items = cta_items(bar);
     for (int it = items.first; ok && it < items.end; ++it, ++i) {
       const PItem pi = load_pitem(p, it);
       prefetch_pitem(p, it + 1);
@@ -276,7 +286,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
     int o_items = 0;     // items whose O_s has been read
     uint32_t sync_seq = 0;  // uses of stage_sync[s]
     bool ok = true;
-    const CtaItems items = cta_items(p);
+    const CtaItems items = cta_items(bar);
     for (int it = items.first; ok && it < items.end; ++it) {
       const PItem pi = load_pitem(p, it);
       prefetch_pitem(p, it + 1);

@@ -115,17 +115,23 @@ __device__ __forceinline__ void row_interval32(int kind, int param, int n, int p
 }
 
 // The CTA's work items: descriptors [first, end) of p.pitems (the host
-// assigns items to CTAs and lays them out CTA by CTA).  Debug builds: an
-// empty range, after recording the failure, when the range is not inside
-// the launch's items.
+// assigns items to CTAs and lays them out CTA by CTA).  Thread 0 reads the
+// range at the start of the kernel (read_cta_items) and leaves it in
+// shared memory for every role.  Debug builds: an empty range, after
+// recording the failure, when the range is not inside the launch's items.
 struct CtaItems {
   int first, end;
 };
 
-__device__ __forceinline__ CtaItems cta_items(const FwdParams& p) {
+__device__ __forceinline__ CtaItems read_cta_items(const FwdParams& p) {
   CtaItems r{__ldg(p.cta_off + blockIdx.x), __ldg(p.cta_off + blockIdx.x + 1)};
   if (!debug_check(p.err, r.first >= 0 && r.first <= r.end && r.end <= p.n_items, kSiteItem)) r.end = r.first;
   return r;
+}
+
+template <typename Bar>
+__device__ __forceinline__ CtaItems cta_items(const Bar* bar) {
+  return CtaItems{bar->item_first, bar->item_end};
 }
 
 // Q and K producer (one thread): Q tile t = 2 i + s (i = the CTA's i-th
@@ -145,7 +151,7 @@ __device__ __forceinline__ void produce_q_k(const FwdParams& p, Bar* bar, uint8_
   // that stays busy while the other stream's slot frees up).
   const uint64_t keep = ptx::l2_policy_evict_last();
   const uint64_t once = ptx::l2_policy_evict_first();
-  const CtaItems items = cta_items(p);
+  const CtaItems items = cta_items(bar);
   const int iend = items.end;
   int qit = items.first, kit = items.first;  // items of the Q and K streams
   PItem qi, ki;
@@ -243,7 +249,7 @@ __device__ __forceinline__ void produce_v(const FwdParams& p, Bar* bar, uint8_t*
   const uint64_t keep = ptx::l2_policy_evict_last();
   int e = 0;
   bool ok = true;
-  const CtaItems items = cta_items(p);
+  const CtaItems items = cta_items(bar);
   for (int it = items.first; ok && it < items.end; ++it) {
     const PItem pi = load_pitem(p, it);
     prefetch_pitem(p, it + 1);
