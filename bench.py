@@ -192,10 +192,13 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
+    _n = 0
+
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join("/tmp", f"mattn_clocks_{os.getpid()}.csv")
+        ClockSampler._n += 1  # one file per sampler: several may be open in one process
+        self.path = os.path.join("/tmp", f"mattn_clocks_{os.getpid()}_{ClockSampler._n}.csv")
 
     def __enter__(self):
         try:
@@ -322,6 +325,7 @@ def run_gpu(args):
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
         barrier(dist)
+    clocks = clk.summary()  # the timed region's samples, read before any other sampler runs
     step_ms = [s.elapsed_time(e) for s, e in ev]
     total_ms = sum(step_ms)
     total_ms = max_over_ranks(dist, total_ms, device=dev)
@@ -492,7 +496,6 @@ def run_gpu(args):
               "persistent": "attention_persist_kernel", "single": "attention_sp_kernel"}.get(sched, sched)
     headline_kernel = f"{family}<{wl.d}> ({sched} schedule)"
     if rank == 0:
-        clocks = clk.summary()
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
@@ -501,7 +504,11 @@ def run_gpu(args):
             "pct_of_peak": round(100 * value / world / peaks["bf16_tflops"], 1),
             "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
-                         "traffic": traffic, "peak_source": peaks["source"] + " burst bf16 (cuBLAS)",
+                         "traffic": traffic,
+                         "traffic_source": (None if traffic is None else
+                                            f"carried from the committed ncu capture profiles/attention_fwd_{wl_name}.md "
+                                            f"(kernel source hash {kernel_source_hash()}); not measured in this run"),
+                         "peak_source": peaks["source"] + " burst bf16 (cuBLAS)",
                          "kernel": headline_kernel},
             "cpu_baseline": cpu,
             "parity": parity,
