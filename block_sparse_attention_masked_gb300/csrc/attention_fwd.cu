@@ -488,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
       ptx::tmem_ld32(s_tmem + 64, *reinterpret_cast<float(*)[32]>(&x[64]));
       ptx::tmem_ld32(s_tmem + 96, *reinterpret_cast<float(*)[32]>(&x[96]));
       ptx::tmem_wait_ld();
-      uint32_t none = 0u;  // 32-column groups this lane sees nothing of
+      bool sees = true;  // this row sees a key of the tile
       const bool partial = MASK && sub_partial(p, sp, kt);
       if (partial) {
         // visible key columns of this row inside the tile: [c_lo, c_hi]
@@ -497,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
         const int c_hi = (int)(hi - k0 < -1 ? -1 : (hi - k0 > 128 ? 128 : hi - k0));
         // and the sink keys of the tile: columns [0, c_s]
         const int c_s = (int)(sink_hi - k0 < -1 ? -1 : (sink_hi - k0 > 128 ? 128 : sink_hi - k0));
-        none = mask_row(x, c_lo, c_hi, c_s);
+        sees = mask_row(x, c_lo, c_hi, c_s);
       }
       // P = exp2(s * scale * log2e - m) into tensor memory.  tcgen05.ld / st
       // are warp-collective, so every branch below is taken by whole warps
@@ -510,9 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
       // breaks this, or a first tile whose visible scores all came out below
       // 2^-64, is redone below against the tile's own maximum (rare).
       const bool first = m == -INFINITY;
-      ts = exp_to_tmem(x, sl2, first ? 0.f : m, s_tmem, none);
-      // none == 0xf: this lane sees nothing of the tile (partial tiles only)
-      const bool sees = (none & 0xfu) != 0xfu;
+      ts = exp_to_tmem(x, sl2, first ? 0.f : m, s_tmem);
       bool slow = __any_sync(0xffffffffu, !(ts <= kMaxTileSum) || (first && sees && !(ts >= kMinTileSum)));
       if (slow) {
         ptx::tmem_wait_st();  // let these stores land before they are overwritten
@@ -521,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
       }
       if (slow) {
         // tile maximum first (also the first tile of a row)
-        const float m_new = fmaxf(m, row_max(x, none) * sl2);
+        const float m_new = fmaxf(m, row_max(x) * sl2);
         const bool need_rescale = (m != -INFINITY) && (m_new > m);
         if (m == -INFINITY) m = m_new;  // nothing accumulated yet (all earlier P were zero)
         if (__any_sync(0xffffffffu, need_rescale)) {
@@ -532,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_fwd_kernel(const __grid
             m = m_new;
           }
         }
-        ts = exp_to_tmem(x, sl2, (m == -INFINITY) ? 0.f : m, s_tmem, none);
+        ts = exp_to_tmem(x, sl2, (m == -INFINITY) ? 0.f : m, s_tmem);
       }
       l += ts;
       ptx::tmem_wait_st();

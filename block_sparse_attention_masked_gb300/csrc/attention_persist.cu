@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
         ptx::tmem_ld32(s_tmem + 64, *reinterpret_cast<float(*)[32]>(&x[64]));
         ptx::tmem_ld32(s_tmem + 96, *reinterpret_cast<float(*)[32]>(&x[96]));
         ptx::tmem_wait_ld();
-        uint32_t none = 0u;  // 32-column groups this lane sees nothing of
+        bool sees = true;  // this row sees a key of the tile
         if (MASK && sub_partial(p, sp, kt)) {
           // visible key columns of this row inside the tile: [c_lo, c_hi],
           // and the sink keys of the tile: columns [0, c_s]
@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
           const int c_lo = min(max(lo - k0, -1), 128);
           const int c_hi = min(max(hi - k0, -1), 128);
           const int c_s = min(max(sink_hi - k0, -1), 128);
-          none = mask_row(x, c_lo, c_hi, c_s);
+          sees = mask_row(x, c_lo, c_hi, c_s);
         }
         // P = exp2(s * scale * log2e - m) into tensor memory (the stale-max
         // rule of attention_fwd.cu: m only guards against overflow)
@@ -340,9 +340,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
         // breaks this, or a first tile whose visible scores all came out below
         // 2^-64, is redone below against the tile's own maximum (rare).
         const bool first = m == -INFINITY;
-        ts = exp_to_tmem(x, sl2, first ? 0.f : m, s_tmem, none);
-        // none == 0xf: this lane sees nothing of the tile (partial tiles only)
-        const bool sees = (none & 0xfu) != 0xfu;
+        ts = exp_to_tmem(x, sl2, first ? 0.f : m, s_tmem);
         bool slow = __any_sync(0xffffffffu, !(ts <= kMaxTileSum) || (first && sees && !(ts >= kMinTileSum)));
         if (slow) {
           ptx::tmem_wait_st();  // let these stores land before they are overwritten
@@ -350,7 +348,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
           m = 0.f;  // the row's reference from here on
         }
         if (slow) {
-          const float m_new = fmaxf(m, row_max(x, none) * sl2);
+          const float m_new = fmaxf(m, row_max(x) * sl2);
           const bool need_rescale = (m != -INFINITY) && (m_new > m);
           if (m == -INFINITY) m = m_new;
           if (__any_sync(0xffffffffu, need_rescale)) {
@@ -363,7 +361,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
               m = m_new;
             }
           }
-          ts = exp_to_tmem(x, sl2, (m == -INFINITY) ? 0.f : m, s_tmem, none);
+          ts = exp_to_tmem(x, sl2, (m == -INFINITY) ? 0.f : m, s_tmem);
         }
         l += ts;
         ptx::tmem_wait_st();

@@ -423,11 +423,12 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
 // returns the row sum of the fp32 values.  All exponentials use MUFU ex2:
 // moving a share of them to an FMA-pipe polynomial measured slower at every
 // share tried, as did a truncating pack with a second sum over the
-// truncated values (one more add and two integer ops per pair).
-// `none` (from mask_row) has bit g set for the 32-column groups this lane
-// sees nothing of: their scores may be left unmasked, and their P is made
-// zero by exponentiating against -inf (one select per group keeps the pass
-// straight-line code; branching around groups measured slower).
+// truncated values (one more add and two integer ops per pair).  Masked
+// scores are -inf (mask_row) and give exactly 0.  `none` may flag 32-column
+// groups (bit g) to be exponentiated against -inf as a whole; every caller
+// passes 0, and the per-group reference is kept in this form because the
+// unmasked pass measured slower with the reference hoisted out of the group
+// loop (16384-token ViT full 1.09 -> 1.12 ms).
 // (NC = 128 for a whole row; a thread holding half a row passes its 64
 // scores and the tensor-memory address of its half of P.)
 template <int NC>
@@ -465,39 +466,33 @@ __device__ __forceinline__ uint32_t range_bits(int g, int lo, int hi) {
   return (0xffffffffu >> (31 - b0)) & (0xffffffffu << a0);
 }
 
-// Boundary mask of one row of a PARTIAL tile: the key columns c of the
-// 128-key tile outside this row's visible interval [c_lo, c_hi] and
-// outside its sink columns [0, c_s] (c_s < 0: none) are made invisible.
-// Each 32-column group gets a visibility bit mask per lane.  A group this
-// lane sees nothing of is only reported (bit g of the result), and the
-// exponential pass and the row maximum take it as -inf as a whole; a group
-// that some lane of the warp sees in part has its columns set one by one,
-// x[c] = -inf where the column's bit is clear.  A window's boundary tile,
-// whose rows are 32 consecutive positions per warp, thus pays per-column
-// selects on one group per warp instead of all four.
+// Boundary mask of one row of a PARTIAL tile: x[c] = -inf for the key
+// columns c of the 128-key tile outside this row's visible interval
+// [c_lo, c_hi] and outside its sink columns [0, c_s] (c_s < 0: none), one
+// select per column from its 32-column group's bit mask, with no branch
+// per group (measured faster than selecting only in the groups some lane
+// of the warp sees in part and flagging the empty ones: 16384-token ViT
+// sliding window 92.9 -> 89.2 us, head-wise causal windows 64.2 -> 60.1
+// us).  Returns whether the row sees any column of the tile.
 // (x may hold NC < 128 columns of the row, starting at tile column col0, a
 // multiple of 32.)
 template <int NC>
-__device__ __forceinline__ uint32_t mask_row(float (&x)[NC], int c_lo, int c_hi, int c_s, int col0 = 0) {
-  uint32_t none = 0u;
+__device__ __forceinline__ bool mask_row(float (&x)[NC], int c_lo, int c_hi, int c_s, int col0 = 0) {
 #pragma unroll
   for (int g = 0; g < NC / 32; ++g) {
     const int gt = g + col0 / 32;  // 32-column group of the tile
     const uint32_t vis = range_bits(gt, c_lo, c_hi) | range_bits(gt, 0, c_s);
-    if (vis == 0u) none |= 1u << g;
-    if (__any_sync(0xffffffffu, vis != 0u && vis != 0xffffffffu)) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) x[32 * g + j] = ((vis >> j) & 1u) ? x[32 * g + j] : -INFINITY;
-    }
+    for (int j = 0; j < 32; ++j) x[32 * g + j] = ((vis >> j) & 1u) ? x[32 * g + j] : -INFINITY;
   }
-  return none;
+  const int a = max(c_lo, col0), b = min(c_hi, col0 + NC - 1);
+  return a <= b || c_s >= col0;
 }
 
 // Maximum of the 128 raw scores of this thread's row (8 independent chains;
-// measured faster here than three-input maxima), over the 32-column groups
-// not flagged in `none` (mask_row's bits).
+// measured faster here than three-input maxima).
 template <int NC>
-__device__ __forceinline__ float row_max(const float (&x)[NC], uint32_t none = 0u) {
+__device__ __forceinline__ float row_max(const float (&x)[NC]) {
   float r = -INFINITY;
 #pragma unroll
   for (int c = 0; c < NC; c += 32) {
@@ -509,7 +504,7 @@ __device__ __forceinline__ float row_max(const float (&x)[NC], uint32_t none = 0
 #pragma unroll
       for (int i = 0; i < 8; ++i) a[i] = fmaxf(a[i], x[c + u + i]);
     const float g = fmaxf(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])), fmaxf(fmaxf(a[4], a[5]), fmaxf(a[6], a[7])));
-    r = ((none >> (c / 32)) & 1u) ? r : fmaxf(r, g);
+    r = fmaxf(r, g);
   }
   return r;
 }
