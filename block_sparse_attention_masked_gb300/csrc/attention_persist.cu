@@ -23,6 +23,11 @@
 // few key tiles) spend most of a one-item-per-CTA launch in set-up and
 // epilogue; here those overlap the neighbouring items' work.
 //
+// A split item (built when a plan holds one: SPLIT) is one query tile whose
+// key tiles alternate between the two sub-tiles; each keeps its own (m, l,
+// O) and at the item's end the two are merged (the split schedule of
+// attention_fwd.cu, per item): long query tiles then take half the steps.
+//
 // Roles (384 threads):
 //   warp 0        TMA producer: Q tiles into their slots and K tiles into their ring
 //   warp 1        tensor-memory allocator; MMA issuer of sub-tile 0
@@ -82,14 +87,16 @@ struct PBarriers {
   uint64_t o_full[2];      // the item's last P V of sub-tile s is done
   uint64_t drain[2];       // MMA drain on abort, one per issuer
   uint64_t stage_sync[2];  // per sub-tile: barrier of its 128 softmax threads (output staging)
+  uint64_t split_sync;     // the 256 softmax threads (merge of a split item)
   uint64_t never;          // self-test: nothing ever arrives here
   uint32_t tmem_base;
   int abort_flag;
   uint32_t mma_turn;       // ticket of the MMA group that may be issued next
   int item_first, item_end;  // the CTA's work items (read_cta_items)
+  float2 xch[kTile];         // split items: sub-tile 1's (m, l) per row, then the two scales
 };
 
-template <int D, bool OUT_F32, bool MASK>
+template <int D, bool OUT_F32, bool MASK, bool SPLIT>
 __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const __grid_constant__ FwdParams p) {
   using G = Geo<D>;
   constexpr int KS = G::kStages;
@@ -136,6 +143,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
       ptx::mbar_init(&bar->drain[s], 1);
       ptx::mbar_init(&bar->stage_sync[s], kTile);
     }
+    ptx::mbar_init(&bar->split_sync, 2 * kTile);
     ptx::mbar_init(&bar->never, 1);
     bar->abort_flag = 0;
     bar->mma_turn = 0;
@@ -214,7 +222,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
         if (lane == 0) ptx::mbar_arrive(&bar->q_empty[qslot]);
       }
       for (int j = 0; j < L.n; ++j, ++e) {
-        const bool use = list_uses(L, j, s);
+        const bool use = pi.uses<SPLIT>(j, s);
         const int ks = e % KS;
         const bool rel_v = e >= 1;
         const int ve = e - 1;
@@ -285,6 +293,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
     uint32_t count = 0;  // S tiles of this sub-tile so far (all items)
     int o_items = 0;     // items whose O_s has been read
     uint32_t sync_seq = 0;  // uses of stage_sync[s]
+    uint32_t split_seq = 0;  // uses of split_sync
     bool ok = true;
     const CtaItems items = cta_items(bar);
     for (int it = items.first; ok && it < items.end; ++it) {
@@ -304,7 +313,7 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
       float m = -INFINITY;  // running (stale) max of scaled scores, log2 domain
       float l = 0.f;        // running sum of exp2(x - m)
       for (int jj = 0; jj < L.n; ++jj) {
-        if (!list_uses(L, jj, s)) continue;
+        if (!pi.uses<SPLIT>(jj, s)) continue;
         const int kt = list_kt(L, jj);
         bool got = ptx::mbar_wait(&bar->s_full[s], count & 1, p.timeout_ns, abort_flag);
         if (!__all_sync(0xffffffffu, got)) {
@@ -374,11 +383,106 @@ __global__ void __launch_bounds__(kPThreads, 1) attention_persist_kernel(const _
       // While the tensor core runs this item's last P V and the next item's
       // first S: wait for the P V, read O_s, write O / (l + exp(sink)) and
       // the LSE in caller token order.
-      const bool has_o = list_has(L, s, false);
+      const bool has_o = pi.first(s) >= 0;
+      const bool has_oo = pi.first(s ^ 1) >= 0;  // the other sub-tile's O of this item
+      const float b2 = p.sink ? __ldg(p.sink + pi.ip.h) * kLog2e : -INFINITY;
+      if (SPLIT && pi.split) {
+        // Both sub-tiles hold partial (m, l, O) of the same rows: merged as
+        // O = (O_0 e_0 + O_1 e_1) / (l_0 e_0 + l_1 e_1 + exp(sink)), e_s =
+        // exp2(m_s - M) against the common maximum M; sub-tile 1 hands its
+        // (m, l) to sub-tile 0, which forms both scales (and the LSE), and
+        // each writes half of the O columns.
+        bool valid = pos < p.N;
+        const int64_t tok = valid ? out_token(p, pi.store, pi.perm_row, pos) : 0;
+        if (kDebugChecks && tok < 0) valid = false;
+        const int64_t orow = ((int64_t)pi.ip.bh * p.N + tok) * D;
+        auto sync_all = [&]() {
+          if (__all_sync(0xffffffffu, ptx::mbar_sync(&bar->split_sync, split_seq, p.timeout_ns, abort_flag)))
+            return true;
+          if (lane == 0) raise_error(p, bar, kErrEpilogue);
+          return false;
+        };
+        // this sub-tile's O is complete; after the first barrier so is the
+        // other's (its threads waited for it before arriving)
+        if (has_o) {
+          const bool got = ptx::mbar_wait(&bar->o_full[s], o_items & 1, p.timeout_ns, abort_flag);
+          if (!__all_sync(0xffffffffu, got)) {
+            if (lane == 0) raise_error(p, bar, kErrEpilogue);
+            ok = false;
+            break;
+          }
+          ++o_items;
+        }
+        if (s == 1) bar->xch[row] = make_float2(m, l);
+        if (!sync_all()) {
+          ok = false;
+          break;
+        }
+        float2 sc;
+        if (s == 0) {
+          const float2 o1 = bar->xch[row];
+          float lse_v;
+          finalize_row(m, l, o1.x, o1.y, b2, &sc.x, &sc.y, &lse_v);
+          if (valid && p.lse) p.lse[(int64_t)pi.ip.bh * p.N + tok] = lse_v;
+          bar->xch[row] = sc;
+        }
+        if (!sync_all()) {
+          ok = false;
+          break;
+        }
+        if (s == 1) sc = bar->xch[row];
+        ptx::tc_fence_after();
+        const float sc_self = s ? sc.y : sc.x, sc_other = s ? sc.x : sc.y;
+        const uint32_t oo_tmem = tmem + lane_off + 256 + (s ^ 1) * 128;
+        constexpr int kHalf = 16 * ((D + 31) / 32);  // columns [0, kHalf) by sub-tile 0, the rest by 1
+        const uint64_t o_policy = ptx::l2_policy_evict_first();
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 16) {
+          if (s ? c0 < kHalf : c0 >= kHalf) continue;  // warp-uniform
+          float ov[16];
+          if (has_o) {
+            ptx::tmem_ld16(o_tmem + c0, ov);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ov[i] *= sc_self;
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ov[i] = 0.f;
+          }
+          if (has_oo) {
+            float ow[16];
+            ptx::tmem_ld16(oo_tmem + c0, ow);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ov[i] = fmaf(ow[i], sc_other, ov[i]);
+          }
+          if (valid) {
+            if (OUT_F32) {
+              float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.o) + orow + c0);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) dst[i] = make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
+            } else {
+              uint32_t pk[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) pk[i] = ptx::pack_bf16x2(ov[2 * i], ov[2 * i + 1]);
+              uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + orow + c0);
+              ptx::st_global_v4_hint(dst, make_uint4(pk[0], pk[1], pk[2], pk[3]), o_policy);
+              ptx::st_global_v4_hint(dst + 1, make_uint4(pk[4], pk[5], pk[6], pk[7]), o_policy);
+            }
+          }
+        }
+        // neither sub-tile writes its next item's first P (which lets the
+        // next P V overwrite its O) before both have read both O's
+        ptx::tc_fence_before();
+        if (!sync_all()) {
+          ok = false;
+          break;
+        }
+        continue;
+      }
       // What does not need O comes first, while the last P V runs: the
       // row's scale, its LSE (stored) and output row, and (staged output)
       // the staging tile, free once its previous store has read it.
-      const float b2 = p.sink ? __ldg(p.sink + pi.ip.h) * kLog2e : -INFINITY;
       float o_scale, unused, lse_v;
       finalize_row(m, l, -INFINITY, 0.f, b2, &o_scale, &unused, &lse_v);
       bool valid = pos < p.N;
@@ -486,10 +590,10 @@ size_t persist_smem_for() {
   return (size_t)(PG::kQSlots + 2 * G::kStages + PG::kStageTiles) * G::kTileBytes + sizeof(PBarriers) + 1024;
 }
 
-template <int D, bool F32, bool MASK>
+template <int D, bool F32, bool MASK, bool SPLIT = false>
 cudaError_t launch_persist_one(const FwdParams& p, int grid, cudaStream_t stream) {
   const size_t smem = persist_smem_for<D, F32>();
-  auto kern = attention_persist_kernel<D, F32, MASK>;
+  auto kern = attention_persist_kernel<D, F32, MASK, SPLIT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -521,11 +625,15 @@ size_t attention_persist_smem_bytes(int d) {
 cudaError_t launch_attention_persist(const FwdParams& p, int d, bool out_f32, int grid, cudaStream_t stream) {
   if (p.n_items <= 0) return cudaSuccess;
   if (grid > p.n_items) grid = p.n_items;
-  // bf16 launches without PARTIAL tiles run the build without the boundary mask
-#define MATTN_CASE(DD)                                                                        \
-  case DD:                                                                                    \
-    return out_f32 ? launch_persist_one<DD, true, true>(p, grid, stream)                      \
-                   : (p.no_partial ? launch_persist_one<DD, false, false>(p, grid, stream)    \
+  // bf16 launches without PARTIAL tiles run the build without the boundary
+  // mask; launches with split items the build with their merge (masked)
+#define MATTN_CASE(DD)                                                                           \
+  case DD:                                                                                       \
+    if (p.has_split)                                                                             \
+      return out_f32 ? launch_persist_one<DD, true, true, true>(p, grid, stream)                 \
+                     : launch_persist_one<DD, false, true, true>(p, grid, stream);               \
+    return out_f32 ? launch_persist_one<DD, true, true>(p, grid, stream)                         \
+                   : (p.no_partial ? launch_persist_one<DD, false, false>(p, grid, stream)       \
                                    : launch_persist_one<DD, false, true>(p, grid, stream));
   switch (d) {
     MATTN_CASE(32)

@@ -98,8 +98,13 @@ __device__ __forceinline__ bool debug_check(uint32_t* err, bool ok, uint32_t sit
 //   [1] list entries n, window start lo, sink entries na, the head's mask parameter
 //   [2] window key tiles lo0, hi0, lo1, hi1 of the two sub-tiles (empty: lo > hi)
 //   [3] FULL key tiles flo0, fhi0, flo1, fhi1 inside them
-//   [4] sink tiles ns0, ns1, load mode | store mode << 8, explicit-order row
+//   [4] sink tiles ns0, ns1, load mode | store mode << 8 | split << 16, explicit-order row
 //   [5] first and last entries used by sub-tile 0 and by sub-tile 1 (-1: none)
+// A split item (bit 16 of [4].z) is one query tile qt0 whose list entries
+// alternate between the sub-tiles (entry j to sub-tile j % 2), both with the
+// query tile's own plan in [2]-[4]; the sub-tiles' partial results are
+// merged at its end.  The host makes long items split so that no CTA waits
+// on one item longer than its share of the launch.
 constexpr int kPersistItemInt4 = 6;
 
 struct FwdParams {
@@ -116,6 +121,7 @@ struct FwdParams {
   const int2* items;                // (b*H + h, query-tile pair), or (b*H + h, query tile) when split
   const int4* pitems;               // persistent kernel: kPersistItemInt4 int4 per work item
   const int* cta_off;               // persistent kernel: CTA c takes pitems [cta_off[c], cta_off[c+1])
+  int has_split;                    // persistent kernel: some item is a split item
   const int32_t* head_info;         // [H][4], HeadField
   const int32_t* perm;              // explicit orders [n_perm][N]
   int n_perm;

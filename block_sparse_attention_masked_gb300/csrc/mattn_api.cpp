@@ -51,6 +51,10 @@ std::atomic<unsigned long long> g_timeout_ns{0};
 // Test hook: an upper bound on the persistent kernel's grid (0 = one CTA per
 // SM), so that small problems still give each CTA many work items.
 std::atomic<int> g_persist_grid_cap{0};
+// Test hook: which persistent items are split (0: the load rule of
+// split_persist_items; 1: every item whose query tiles have two or more key
+// tiles; -1: none).
+std::atomic<int> g_persist_split{0};
 // Debug library test hook: a defect planted in the next forward launch's
 // plan (kCorrupt*), consumed by that launch.
 enum DebugCorruption : int {
@@ -385,6 +389,76 @@ std::vector<int4> build_persist_items(const Normalized& n, const std::vector<int
   return out;
 }
 
+// The split item of query tile qt of row block bh (layout kPersistItemInt4):
+// the query tile's own key tiles, entry j multiplied by sub-tile j % 2.
+void make_split_item(const Normalized& n, int bh, int qt, int4* d) {
+  const int h = bh % n.H, b = bh / n.H;
+  const HeadPlan& hp = n.heads[h];
+  const KRange r = interval_krange(n.kind, hp.param, n.N, qt);
+  const int ns = sink_tiles(n.sink_tokens, n.N, qt);
+  int lo, cnt, na;
+  pair_list_span(r.lo, r.hi, r.lo, r.hi, ns, ns, &lo, &cnt, &na);
+  d[0] = make_int4(bh, h, b, qt);
+  d[1] = make_int4(cnt, lo, na, hp.param);
+  d[2] = make_int4(r.lo, r.hi, r.lo, r.hi);
+  d[3] = make_int4(r.flo, r.fhi, r.flo, r.fhi);
+  d[4] = make_int4(ns, ns, hp.load | (hp.store << 8) | (1 << 16), hp.perm_row);
+  const int last0 = cnt >= 1 ? ((cnt - 1) & ~1) : -1;
+  const int last1 = cnt >= 2 ? ((cnt - 1) % 2 == 1 ? cnt - 1 : cnt - 2) : -1;
+  d[5] = make_int4(cnt >= 1 ? 0 : -1, last0, cnt >= 2 ? 1 : -1, last1);
+}
+
+// Fixed share of an item's load for its set-up and output, in tile products.
+constexpr int kItemOverheadTiles = 4;
+
+// An item's load for the work assignment: the tile products its sub-tiles
+// multiply plus kItemOverheadTiles.  Both sub-tiles run side by side, so a
+// paired item takes about max(t0, t1) steps and a split item of t tiles
+// about t / 2: both are about half the load.
+int persist_item_load(const int4* d) {
+  if ((d[4].z >> 16) & 1) return d[1].x + kItemOverheadTiles;
+  const int4 u = d[5];  // first / last entries of each sub-tile
+  return (u.x >= 0 ? u.y - u.x + 1 : 0) + (u.z >= 0 ? u.w - u.z + 1 : 0) + kItemOverheadTiles;
+}
+
+// Long paired items become split items.  The CTA that holds the longest
+// item cannot finish before it, and a paired item's two query tiles run side
+// by side, each over its whole key-tile list: head-wise causal windows of
+// up to 32 key tiles made single items of ~60 tile products against ~35 per
+// CTA on average.  An item whose load is above a CTA's fair share (the total
+// over the grid) is replaced by one split item per query tile, whose key
+// tiles the two sub-tiles take in turn (half the steps; no K / V shared
+// between the two query tiles, which matters little for so few items).
+void split_persist_items(const Normalized& n, int grid, std::vector<int4>* d) {
+  const int mode = g_persist_split.load();
+  if (mode < 0) return;
+  const size_t cnt = d->size() / kPersistItemInt4;
+  long total = 0;
+  for (size_t i = 0; i < cnt; ++i) total += persist_item_load(&(*d)[i * kPersistItemInt4]);
+  const long fair = total / std::max(1, grid);
+  const int nt = (n.N + kTile - 1) / kTile;
+  std::vector<int4> out;
+  out.reserve(d->size());
+  for (size_t i = 0; i < cnt; ++i) {
+    const int4* it = &(*d)[i * kPersistItemInt4];
+    const int4 u = it[5];
+    const int t0 = u.x >= 0 ? u.y - u.x + 1 : 0, t1 = u.z >= 0 ? u.w - u.z + 1 : 0;
+    const bool split = mode > 0 ? (t0 >= 2 || t1 >= 2) : persist_item_load(it) > fair;
+    if (!split) {
+      out.insert(out.end(), it, it + kPersistItemInt4);
+      continue;
+    }
+    for (int s = 0; s < 2; ++s) {
+      const int qt = it[0].w + s;
+      if ((s ? t1 : t0) == 0 || qt >= nt) continue;
+      int4 sd[kPersistItemInt4];
+      make_split_item(n, it[0].x, qt, sd);
+      out.insert(out.end(), sd, sd + kPersistItemInt4);
+    }
+  }
+  d->swap(out);
+}
+
 // ------------------------------------------------------------ per-device state
 struct Plan {
   std::vector<int2> items_host;
@@ -392,6 +466,7 @@ struct Plan {
   std::vector<int4> pitems_host;  // persistent kernel: the items' descriptors, CTA by CTA
   std::vector<int> cta_off_host;  // persistent kernel: CTA c takes descriptors [off[c], off[c+1])
   int persist_grid = 0;           // persistent kernel: CTAs of the launch
+  bool has_split = false;         // persistent kernel: some item is a split item
   int2* items = nullptr;
   int32_t* head_info = nullptr;
   int4* pitems = nullptr;
@@ -458,21 +533,14 @@ int device_state(DeviceState** out) {
 // The persistent kernel's work items assigned to `grid` CTAs: longest first,
 // each to the CTA with the least load so far (the longest-processing-time
 // rule), then laid out CTA by CTA so that CTA c takes descriptors
-// [off[c], off[c + 1]).  An item's load is the tile products its sub-tiles
-// multiply plus a fixed share for its set-up and output (kItemOverheadTiles).
-// Items of one mask kind with equal windows get equal loads and fall to the
-// CTAs in turn; head-wise windows (a few key tiles next to tens) no longer
-// leave the CTAs holding two long items to run while others idle.
-constexpr int kItemOverheadTiles = 4;
-
+// [off[c], off[c + 1]).  An item's load is persist_item_load.  Items of one
+// mask kind with equal windows get equal loads and fall to the CTAs in turn;
+// head-wise windows (a few key tiles next to tens) no longer leave the CTAs
+// holding two long items to run while others idle.
 void assign_persist_items(std::vector<int4>* d, int grid, std::vector<int>* off) {
   const size_t n = d->size() / kPersistItemInt4;
   std::vector<std::pair<int, int>> order(n);  // (load, item)
-  for (size_t i = 0; i < n; ++i) {
-    const int4 u = (*d)[i * kPersistItemInt4 + 5];  // first / last entries of each sub-tile
-    const int tiles = (u.x >= 0 ? u.y - u.x + 1 : 0) + (u.z >= 0 ? u.w - u.z + 1 : 0);
-    order[i] = {tiles + kItemOverheadTiles, (int)i};
-  }
+  for (size_t i = 0; i < n; ++i) order[i] = {persist_item_load(&(*d)[i * kPersistItemInt4]), (int)i};
   std::stable_sort(order.begin(), order.end(), [](const auto& a, const auto& b) { return a.first > b.first; });
   std::vector<std::vector<int>> per(grid);
   std::priority_queue<std::pair<long, int>, std::vector<std::pair<long, int>>, std::greater<>> heap;
@@ -498,8 +566,9 @@ void assign_persist_items(std::vector<int4>* d, int grid, std::vector<int>* off)
 std::string plan_key(const Normalized& n, int persist_grid) {
   std::string k;
   char buf[96];
-  snprintf(buf, sizeof(buf), "%d|%d|%d|%d|%d|%d|%d|%d|%d|", n.kind, n.B, n.H, n.N, n.need_copy ? 1 : 0,
-           n.split ? 1 : 0, n.sink_tokens, n.single ? 1 : 0, n.persistent ? persist_grid : 0);
+  snprintf(buf, sizeof(buf), "%d|%d|%d|%d|%d|%d|%d|%d|%d|%d|", n.kind, n.B, n.H, n.N, n.need_copy ? 1 : 0,
+           n.split ? 1 : 0, n.sink_tokens, n.single ? 1 : 0, n.persistent ? persist_grid : 0,
+           n.persistent ? g_persist_split.load() : 0);
   k += buf;
   for (const auto& hp : n.heads) {
     snprintf(buf, sizeof(buf), "%d,%d,%d,%d;", hp.param, hp.load, hp.store, hp.perm_row);
@@ -529,7 +598,11 @@ int get_plan(DeviceState* st, const Normalized& n, cudaStream_t stream, Plan** o
   if (n.persistent) {
     pl->pitems_host = build_persist_items(n, pl->items_host);
     pl->persist_grid = std::max(1, std::min<int>(persist_grid, (int)pl->items_host.size()));
+    split_persist_items(n, pl->persist_grid, &pl->pitems_host);
+    pl->persist_grid = std::max(1, std::min<int>(persist_grid, (int)(pl->pitems_host.size() / kPersistItemInt4)));
     assign_persist_items(&pl->pitems_host, pl->persist_grid, &pl->cta_off_host);
+    for (size_t i = 0; i < pl->pitems_host.size(); i += kPersistItemInt4)
+      pl->has_split = pl->has_split || ((pl->pitems_host[i + 4].z >> 16) & 1);
     MATTN_CUDA(cudaMalloc(&pl->pitems, std::max<size_t>(1, pl->pitems_host.size()) * sizeof(int4)),
                "cudaMalloc(item descriptors)");
     MATTN_CUDA(cudaMemcpyAsync(pl->pitems, pl->pitems_host.data(), pl->pitems_host.size() * sizeof(int4),
@@ -840,7 +913,10 @@ int fwd_locked(const void* q, const void* k, const void* v, void* o, float* lse,
   p.cta_off = plan->cta_off;
   p.after_prepass = (n.need_copy && !n.single) ? 1 : 0;
   p.no_partial = launch_has_no_partial(n) ? 1 : 0;
-  p.n_items = (int)plan->items_host.size();
+  // work items of the launch: the persistent kernel's descriptors (long
+  // paired items may have become two split items), else the work list
+  p.n_items = n.persistent ? (int)(plan->pitems_host.size() / kPersistItemInt4) : (int)plan->items_host.size();
+  p.has_split = n.persistent && plan->has_split ? 1 : 0;
   p.head_info = plan->head_info;
   p.perm = desc->perm;
   p.n_perm = desc->perm ? desc->n_perm : 0;
@@ -1010,6 +1086,15 @@ int mattn_internal_debug_corrupt(int what) {
 int mattn_internal_set_persist_grid(int ctas) {
   if (ctas < 0) return fail(MATTN_ERR_INVALID_ARG, "ctas must be >= 0");
   g_persist_grid_cap.store(ctas);
+  return MATTN_OK;
+}
+
+// Test hook (not in the public header): which persistent items are split
+// (0: the load rule; 1: every item whose query tiles see two or more key
+// tiles; -1: none).
+int mattn_internal_set_persist_split(int mode) {
+  if (mode < -1 || mode > 1) return fail(MATTN_ERR_INVALID_ARG, "mode must be -1, 0 or 1");
+  g_persist_split.store(mode);
   return MATTN_OK;
 }
 

@@ -26,8 +26,14 @@ struct PItem {
   TileList L;
   int load, store, perm_row;
   int first0, last0, first1, last1;  // first and last entries each sub-tile uses (-1: none)
+  bool split;                        // one query tile, entries dealt to the sub-tiles in turn
   __device__ __forceinline__ int first(int s) const { return s ? first1 : first0; }
   __device__ __forceinline__ int last(int s) const { return s ? last1 : last0; }
+  // whether sub-tile s multiplies list entry j (SPLIT: builds that take split items)
+  template <bool SPLIT>
+  __device__ __forceinline__ bool uses(int j, int s) const {
+    return (SPLIT && split) ? (j & 1) == s : list_uses(L, j, s);
+  }
 };
 
 __device__ __forceinline__ const int4* pitem_ptr(const FwdParams& p, int it) {
@@ -70,7 +76,12 @@ __device__ __forceinline__ PItem load_pitem(const FwdParams& p, int it) {
   r.L.e = nullptr;
   r.L.block = false;
   r.load = g.z & 0xff;
-  r.store = g.z >> 8;
+  r.store = (g.z >> 8) & 0xff;
+  r.split = ((g.z >> 16) & 1) != 0;
+  if (r.split) {  // both sub-tiles take the one query tile
+    r.ip.sp1.qt = a.w;
+    r.ip.sp1.rows = r.ip.sp0.rows;
+  }
   r.perm_row = g.w;
   r.first0 = u.x; r.last0 = u.y;
   r.first1 = u.z; r.last1 = u.w;

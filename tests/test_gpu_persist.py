@@ -61,18 +61,34 @@ def grid_cap():
 SCHEDULES = ["persistent"]
 
 
-def _same_as_paired(q, k, v, spec, tag, schedule="persistent"):
-    """The persistent kernel does a paired item's arithmetic exactly: equal
-    bits.  The streamed kernel splits each row's softmax between two thread
-    groups, so its row sums are added in another order: O within one bf16
-    (or 2^-20 fp32) rounding step of the paired result, LSE within 1e-5."""
+@pytest.fixture
+def split_mode():
+    """Sets which persistent items are split (test hook: -1 none, 0 the load
+    rule, 1 every item whose query tiles see two or more key tiles) for one
+    test and restores the rule."""
+    L = mattn.lib()
+    L.mattn_internal_set_persist_split.argtypes = [ctypes.c_int]
+
+    def set_mode(m):
+        assert L.mattn_internal_set_persist_split(m) == 0
+
+    yield set_mode
+    L.mattn_internal_set_persist_split(0)
+
+
+def _same_as_paired(q, k, v, spec, tag, schedule="persistent", exact=True):
+    """Without split items the persistent kernel does a paired item's
+    arithmetic exactly: equal bits.  A split item deals a query tile's key
+    tiles to the two sub-tiles and merges their partial sums at the end, so
+    its sums are added in another order: O within one bf16 (or 2^-20 fp32)
+    rounding step of the paired result, LSE within 1e-5."""
     B, H, N, d = q.shape
     o_p, l_p = mattn.attention(q, k, v, mattn.prepare(spec, H, N, schedule=schedule))
     o_r, l_r = mattn.attention(q, k, v, mattn.prepare(spec, H, N, schedule="paired"))
     torch.cuda.synchronize()
     rc, word = mattn.device_status()
     assert rc == 0, f"{tag}: device error word {word:#x}"
-    if schedule == "persistent":
+    if exact:
         assert torch.equal(o_p, o_r), f"{tag}: O differs from the paired kernel"
         assert torch.equal(l_p, l_r), f"{tag}: LSE differs from the paired kernel"
         return
@@ -96,29 +112,36 @@ def _specs(H, n):
 
 
 @pytest.mark.parametrize("sched", SCHEDULES)
+@pytest.mark.parametrize("split", [-1, 1])
 @pytest.mark.parametrize("cap", [0, 3])
 @pytest.mark.parametrize("d", [32, 64, 80, 96, 128])
 @pytest.mark.parametrize("n", [256, 1000, 2200])
-def test_interval_kinds(d, n, cap, sched, grid_cap):
+def test_interval_kinds(d, n, cap, split, sched, grid_cap, split_mode):
     """Every interval kind with per-head parameters, ragged N (a partial last
     query tile, and at 1000 / 2200 an odd tile count whose last pair has one
-    empty sub-tile), with and without a capped grid."""
+    empty sub-tile), with and without a capped grid, with no item split and
+    with every item split (each query tile's key tiles dealt to the two
+    sub-tiles, merged at its end)."""
     grid_cap(cap)
+    split_mode(split)
     H = 3
     q, k, v = make_qkv(2, H, n, d, "bf16", 1.0, seed=d * 7 + n, device="cuda")
     for spec in _specs(H, n):
-        tag = f"{spec.kind} d{d} n{n} cap{cap} {sched}"
+        tag = f"{spec.kind} d{d} n{n} cap{cap} split{split} {sched}"
         check(q, k, v, spec, tag=tag, schedule=sched)
-        _same_as_paired(q, k, v, spec, tag, sched)
+        _same_as_paired(q, k, v, spec, tag, sched, exact=split < 0)
 
 
 @pytest.mark.parametrize("sched", SCHEDULES)
+@pytest.mark.parametrize("split", [-1, 1])
 @pytest.mark.parametrize("cap", [0, 2])
-def test_token_orders(cap, sched, grid_cap):
+def test_token_orders(cap, split, sched, grid_cap, split_mode):
     """Column-major heads (strided TMA views), the two 2x2-block orders (5D
     views), an explicit order and fp32 inputs (both through the reorder
     pre-pass, the kernel then launched as its programmatic dependent)."""
     grid_cap(cap)
+    split_mode(split)
+    ex = split < 0
     rows, cols = 64, 64
     n, d = rows * cols, 80
     q, k, v = make_qkv(1, 4, n, d, "bf16", 0.5, seed=5, device="cuda")
@@ -127,23 +150,25 @@ def test_token_orders(cap, sched, grid_cap):
                     perm=[None, cm, block2x2_order(rows, cols), block2x2_order(rows, cols, by_columns=True)],
                     perm_grid=[None, (rows, cols), (rows, cols, "block2x2_row"), (rows, cols, "block2x2_col")])
     check(q, k, v, spec, tag="grid orders", schedule=sched)
-    _same_as_paired(q, k, v, spec, "grid orders", sched)
+    _same_as_paired(q, k, v, spec, "grid orders", sched, exact=ex)
     rng = np.random.default_rng(9)
     spec2 = MaskSpec("chunk", [256, 100, 256, 64], perm=[random_order(n, 3), None, cm, None],
                      sink=rng.standard_normal(4))
     check(q, k, v, spec2, tag="explicit order", schedule=sched)
-    _same_as_paired(q, k, v, spec2, "explicit order", sched)
+    _same_as_paired(q, k, v, spec2, "explicit order", sched, exact=ex)
     qf, kf, vf = make_qkv(1, 2, 1000, 64, "f32", 1.0, seed=6, device="cuda")
     spec3 = MaskSpec("sliding", [32, 100])
     check(qf, kf, vf, spec3, tag="fp32", schedule=sched)
-    _same_as_paired(qf, kf, vf, spec3, "fp32", sched)
+    _same_as_paired(qf, kf, vf, spec3, "fp32", sched, exact=ex)
 
 
 @pytest.mark.parametrize("sched", SCHEDULES)
+@pytest.mark.parametrize("split", [-1, 1])
 @pytest.mark.parametrize("cap", [0, 5])
-def test_grouped_query_heads(cap, sched, grid_cap):
+def test_grouped_query_heads(cap, split, sched, grid_cap, split_mode):
     """Grouped-query attention: 8 query heads sharing 2 K/V heads."""
     grid_cap(cap)
+    split_mode(split)
     from oracle import dense
 
     B, H, Hkv, n, d = 1, 8, 2, 3000, 128
@@ -155,7 +180,7 @@ def test_grouped_query_heads(cap, sched, grid_cap):
     o, lse = mattn.attention(q, k, v, mattn.prepare(spec, H, n, schedule=sched))
     torch.cuda.synchronize()
     assert mattn.device_status()[0] == 0
-    _same_as_paired(q, k, v, spec, f"gqa {sched}", sched)
+    _same_as_paired(q, k, v, spec, f"gqa {sched}", sched, exact=split < 0)
     rows = np.unique(np.r_[0, 127, 128, 575, 576, n - 1, np.random.default_rng(0).choice(n, 40, replace=False)])
     f = lambda t: t.float().cpu().numpy()  # noqa: E731
     ref_o, ref_l = dense.attention(f(q), f(k), f(v), spec, rows=rows)
@@ -178,7 +203,7 @@ def test_vit16384_full_size(mask, sched):
     rng = np.random.default_rng(1)
     rows = np.unique(np.r_[0, 255, 256, 8191, wl.N - 1, rng.choice(wl.N, 48, replace=False)])
     check(q, k, v, spec, rows=rows, heads=[(0, 0), (0, 5), (0, 8), (0, 15)], tag=mask, schedule=sched)
-    _same_as_paired(q, k, v, spec, mask, sched)
+    _same_as_paired(q, k, v, spec, mask, sched, exact=False)
 
 
 @pytest.mark.parametrize("sched", SCHEDULES)
@@ -190,7 +215,7 @@ def test_causal_windows_with_sink_full_size(sched):
     spec = make_mask(wl, "causal_window_sink", seed=0)
     rows = np.unique(np.r_[0, 511, 512, 2047, 2048, 4095, np.random.default_rng(2).choice(4096, 64, replace=False)])
     check(q, k, v, spec, rows=rows, tag="causal4096", schedule=sched)
-    _same_as_paired(q, k, v, spec, "causal4096", sched)
+    _same_as_paired(q, k, v, spec, "causal4096", sched, exact=False)
 
 
 @pytest.mark.parametrize("sched", SCHEDULES)
