@@ -30,6 +30,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "attention_tiles.cuh"
 #include "kernel_params.h"
 #include "plan_rules.h"
 #include "ptx.cuh"
@@ -412,16 +413,7 @@ __global__ void __launch_bounds__(kThreadsD256, 1) attention_sp_kernel(const __g
         const int c_lo = (int)(lo - k0 < -1 ? -1 : (lo - k0 > kKT ? kKT : lo - k0));
         const int c_hi = (int)(hi - k0 < -1 ? -1 : (hi - k0 > kKT ? kKT : hi - k0));
         const int c_s = (int)(sink_hi - k0 < -1 ? -1 : (sink_hi - k0 > kKT ? kKT : sink_hi - k0));
-        sees = c_s >= 0 || (max(c_lo, 0) <= min(c_hi, kKT - 1));
-        if (c_s < 0) {
-#pragma unroll
-          for (int c = 0; c < kKT; ++c)
-            if (c < c_lo || c > c_hi) x[c] = -INFINITY;
-        } else {
-#pragma unroll
-          for (int c = 0; c < kKT; ++c)
-            if ((c < c_lo || c > c_hi) && c > c_s) x[c] = -INFINITY;
-        }
+        sees = mask_row(x, c_lo, c_hi, c_s);
       }
       // exponentiate against the running (stale) maximum, or against 0 for a
       // row's first visible scores; a tile whose row sum passes 2^40, or a

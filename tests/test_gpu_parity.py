@@ -285,7 +285,11 @@ def test_host_pipeline_over_head_chunks():
     """mattn_fwd_host cuts the call into chunks of heads on two streams: per
     head parameters, per head block bitmaps, sinks and explicit orders must
     follow their heads into the chunks (B = 2, H = 7: chunks of uneven
-    size), and the result equals the device entry point's."""
+    size), and the result equals the device entry point's: bit for bit,
+    except where the persistent kernel's work split differs between the
+    chunks and the whole call (an item above a CTA's fair share is split,
+    and a split item adds its sums in another order): there within one bf16
+    rounding step on O and 1e-5 on the LSE."""
     B, H, N, d = 2, 7, 640, 64
     q, k, v = make_qkv(B, H, N, d, "bf16", 1.0, 21, device="cpu")
     nb = -(-N // 128)
@@ -300,15 +304,32 @@ def test_host_pipeline_over_head_chunks():
         o, lse = mattn.attention_host(q.pin_memory(), k.pin_memory(), v.pin_memory(), spec)
         od, lsed = mattn.attention(qd, kd, vd, mattn.prepare(spec, H, N))
         torch.cuda.synchronize()
-        assert torch.equal(o, od.cpu()), spec.kind
-        assert torch.equal(lse, lsed.cpu()), spec.kind
+        _same_host_device(o, lse, od, lsed, mattn.plan_schedule(mattn.prepare(spec, H, N), B, N, d) != "persistent",
+                          spec.kind)
+
+
+def _same_host_device(o, lse, od, lsed, exact, tag):
+    """Host-pipeline result against the device entry point's: equal bits, or
+    (persistent schedule, whose split items depend on the launch) O within one
+    bf16 rounding step and the LSE within 1e-5."""
+    od, lsed = od.cpu(), lsed.cpu()
+    if exact:
+        assert torch.equal(o, od), tag
+        assert torch.equal(lse, lsed), tag
+        return
+    a, r = o.float(), od.float()
+    assert ((a - r).abs() <= 2.0 ** -7 * r.abs() + 1e-6).all(), tag
+    fin = torch.isfinite(lsed)
+    assert torch.equal(fin, torch.isfinite(lse)), tag
+    assert (lse[fin] - lsed[fin]).abs().max().item() <= 1e-5, tag
 
 
 def test_host_pipeline_with_grid_orders():
     """mattn_fwd_host over head chunks with per-head grid orders (raster,
     both 2x2-block orders, the column-major grid transpose): chunks whose
     heads all read through tensor maps run in place, the others through the
-    reorder copy; every chunk's result equals the device entry point's."""
+    reorder copy; every chunk's result equals the device entry point's (to
+    one rounding step where the persistent kernel splits items)."""
     from workloads import block2x2_order
 
     B, H, side, d = 1, 7, 64, 64
@@ -323,8 +344,8 @@ def test_host_pipeline_with_grid_orders():
     o, lse = mattn.attention_host(q.pin_memory(), k.pin_memory(), v.pin_memory(), spec)
     od, lsed = mattn.attention(q.cuda(), k.cuda(), v.cuda(), mattn.prepare(spec, H, N))
     torch.cuda.synchronize()
-    assert torch.equal(o, od.cpu())
-    assert torch.equal(lse, lsed.cpu())
+    _same_host_device(o, lse, od, lsed, mattn.plan_schedule(mattn.prepare(spec, H, N), B, N, d) != "persistent",
+                      "grid orders")
 
 
 @pytest.mark.parametrize("d", [64, 80, 128])
