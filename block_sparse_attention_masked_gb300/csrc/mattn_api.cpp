@@ -1089,6 +1089,45 @@ int mattn_internal_set_persist_grid(int ctas) {
   return MATTN_OK;
 }
 
+// Test hook (not in the public header), host only: the persistent kernel's
+// work items for these arguments on a grid of `grid` CTAs, as the launch
+// would build them (paired items, the long ones split, assigned longest
+// first): kPersistItemInt4 x 4 int32 per item into items_out (capacity
+// cap_items items), the CTA ranges (grid' + 1 ints, grid' = the CTAs the
+// launch would use) into off_out (capacity cap_off), their counts into
+// *n_items_out and *grid_out.  MATTN_ERR_UNSUPPORTED when the arguments do
+// not run the persistent schedule.
+int mattn_internal_persist_plan(const mattn_mask_desc* desc, int B, int H, int N, int d, int grid, int32_t* items_out,
+                                size_t cap_items, int32_t* off_out, size_t cap_off, size_t* n_items_out,
+                                int* grid_out) {
+  if (!n_items_out || !grid_out) return fail(MATTN_ERR_INVALID_ARG, "n_items_out / grid_out is NULL");
+  if (grid < 1) return fail(MATTN_ERR_INVALID_ARG, "grid must be >= 1");
+  Normalized n;
+  int rc = normalize(desc, B, H, N, d, MATTN_BF16, true, &n);
+  if (rc) return rc;
+  if (!n.persistent) return fail(MATTN_ERR_UNSUPPORTED, "these arguments do not run the persistent schedule");
+  const std::vector<int2> items = build_items(n);
+  std::vector<int4> d4 = build_persist_items(n, items);
+  int g = std::max(1, std::min<int>(grid, (int)items.size()));
+  split_persist_items(n, g, &d4);
+  g = std::max(1, std::min<int>(grid, (int)(d4.size() / kPersistItemInt4)));
+  std::vector<int> off;
+  assign_persist_items(&d4, g, &off);
+  const size_t cnt = d4.size() / kPersistItemInt4;
+  *n_items_out = cnt;
+  *grid_out = g;
+  if (cnt > cap_items || (size_t)g + 1 > cap_off || (cnt && !items_out) || !off_out)
+    return fail(MATTN_ERR_CAPACITY, "plan has %zu items and %d CTAs", cnt, g);
+  for (size_t i = 0; i < d4.size(); ++i) {
+    items_out[4 * i + 0] = d4[i].x;
+    items_out[4 * i + 1] = d4[i].y;
+    items_out[4 * i + 2] = d4[i].z;
+    items_out[4 * i + 3] = d4[i].w;
+  }
+  for (int c = 0; c <= g; ++c) off_out[c] = off[c];
+  return MATTN_OK;
+}
+
 // Test hook (not in the public header): which persistent items are split
 // (0: the load rule; 1: every item whose query tiles see two or more key
 // tiles; -1: none).
