@@ -348,7 +348,7 @@ def run_gpu(args):
         hmask = mattn.PreparedMask(spec, wl.H, wl.N, host_side=True)
         for _ in range(max(1, min(args.warmup, 2))):
             mattn.attention_host(qh, kh, vh, hmask, out=oh, lse=lh)
-        e2e_steps = max(1, min(args.steps, 5))
+        e2e_steps = max(1, min(args.steps, 10))
         barrier(dist)
         torch.cuda.synchronize()
         with ClockSampler(local) as e2e_clk:
