@@ -383,7 +383,8 @@ def run_gpu(args):
                "h2d_gbs": round(h2d_gbs, 1), "d2h_gbs": round(d2h_gbs, 1),
                "copy_ms_at_those_rates": round(1e3 * (in_bytes / (h2d_gbs * 1e9) + out_bytes / (d2h_gbs * 1e9)), 2),
                "device_ms_per_step": round(ms_per_step, 3), "kernel_share": round(ms_per_step / e2e_ms, 3),
-               "numa": numa_info(local), "host_cpus": cpu_info()}
+               "numa": numa_info(local), "host_cpus": cpu_info(),
+               "host_buffers_pinned": all(t.is_pinned() for t in (qh, kh, vh, oh, lh))}
         del qh, kh, vh, oh, lh
 
     # ---------------- the oracle on the GPU arm's own inputs (sampled rows)
