@@ -130,7 +130,10 @@ typedef enum { MATTN_BF16 = 0, MATTN_F32 = 1 } mattn_dtype;
  * items run on a persistent grid of one CTA per SM, each CTA walking its
  * items back to back: the next item's Q tiles load and its first Q K^T runs
  * while the current item's output is written, instead of every CTA paying
- * its own set-up and epilogue. */
+ * its own set-up and epilogue.  A paired item longer than a CTA's share of
+ * the launch becomes one item per query tile whose key tiles the two
+ * pipelines take in turn, merged at its end (the SPLIT schedule's
+ * arithmetic for that query tile: the same result up to rounding order). */
 #define MATTN_FLAG_SCHEDULE_PERSISTENT 8u
 
 typedef struct {
